@@ -1,0 +1,428 @@
+"""Plain fp64 CPU oracle of one DFlash/DSpine block-drafter proposal round.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this module.
+The CUDA library never calls it and shares no code with it.
+
+Everything is NumPy float64, written step by step in the order the pages state the
+method, with no blocking, fusion or reordering.  Inputs are bf16- or fp32-valued
+arrays (any NumPy float dtype); they are widened to float64 on use and never rounded.
+
+Sources (cited by page title and section throughout):
+  [DFlash-notes]  NInfer maintainer page "dflash.md" (DFlash / DFlash2 backends):
+                  the conditioning equations, the context K/V projection, the draft
+                  input table, the local-window attention rule, the per-layer equations,
+                  the proposal head and the ring storage paragraph.
+  [Bridge]        "DSpine for Qwen3.8-27B: Causal Features Through Depth", section
+                  "The bridge: read 1,024 features, write through rank 512".
+  [Cache]         same page, section "An attention window is not a cache-size guarantee".
+  [Transfer]      "DSpine 完全拆解", section "统一转移空间" (unified transfer space).
+  [Gate]          "DSpine 完全拆解", section "相邻因果注入" / "门控与写回" (gate and write).
+  [BlockCausal]   "DSpine 完全拆解", section "块因果注意力" (block-causal attention).
+  [Backbone]      "DSpark, every bolt and rivet", section 5.1 "The parallel backbone".
+
+Readings taken where the pages are schematic or garbled (each also listed in the design doc):
+  R-gate   g = sigmoid(G c_t + G_p c_{t-1} + b), m = g * (A c_{t-1}); b absent means 0.
+  R-eps    the bridge floor epsilon is the config's RMSNorm eps; r itself has no eps.
+  R-scale  the code scale is sqrt(Rc); anchor code = sqrt(Rc) * codebook[anchor].
+  R-read   one read matrix R_l per layer, applied to every row of the block.
+  R-anchor row 0 of each request's block takes the anchor code in every layer and
+           receives no write; all writes use the pre-injection codes of that layer.
+  R-rms    the write scale r is the RMS of the pre-injection receiver state, no eps.
+  R-last   every layer, including the last, is followed by its injection.
+  R-rope   split-half rotation: (x_j, x_{j+D/2}) -> (x_j cos - x_{j+D/2} sin,
+           x_{j+D/2} cos + x_j sin), angle = pos * theta^(-2j/D).
+  R-gqa    query head h reads KV head h // (Hq / Hkv).
+  R-mask   a key at position p is visible from a query at position P iff |P - p| < S
+           for a local layer (every populated position for a full layer); the
+           block-causal flag additionally hides block keys j > i.
+  R-tie    argmax ties go to the lowest token id; only the K mask rows are scored.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=F64)
+
+
+# --------------------------------------------------------------------------- norms
+def plain_rmsnorm(x, w, eps: float) -> np.ndarray:
+    """w * x / sqrt(mean(x^2) + eps) over the last axis.  [DFlash-notes], conditioning."""
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return _f64(w) * x / np.sqrt(ms + eps)
+
+
+def plain_head_rmsnorm(x, w, eps: float, head_dim: int) -> np.ndarray:
+    """plain_rmsnorm applied to each head_dim-wide head of the last axis.
+    [DFlash-notes], per-layer equations (query/key normalisation)."""
+    x = _f64(x)
+    shp = x.shape
+    xh = x.reshape(shp[:-1] + (shp[-1] // head_dim, head_dim))
+    return plain_rmsnorm(xh, w, eps).reshape(shp)
+
+
+# --------------------------------------------------------------------------- rope
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """theta^(-2j/D) for j < D/2 (R-rope)."""
+    j = np.arange(head_dim // 2, dtype=F64)
+    return theta ** (-2.0 * j / head_dim)
+
+
+def rope_1d(x, positions, head_dim: int, theta: float) -> np.ndarray:
+    """Full-head split-half rotary embedding at absolute scalar positions.
+
+    x: [T, n_heads * head_dim]; positions: [T].  [DFlash-notes] (scalar RoPE,
+    full-head split-half) with the reading R-rope."""
+    x = _f64(x)
+    T = x.shape[0]
+    half = head_dim // 2
+    ang = _f64(positions)[:, None] * rope_inv_freq(head_dim, theta)[None, :]   # [T, half]
+    cos = np.cos(ang)[:, None, :]
+    sin = np.sin(ang)[:, None, :]
+    xh = x.reshape(T, -1, head_dim)
+    x1, x2 = xh[..., :half], xh[..., half:]
+    out = np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+    return out.reshape(x.shape)
+
+
+# --------------------------------------------------------------------------- context
+def context_fusion(s, w_feature, context_norm, eps: float) -> np.ndarray:
+    """c_t = plain_rmsnorm(W_feature s_t, context_norm); W_feature is bias-free.
+    s: [T, n_tgt * H] (the captured residuals concatenated in recorded order).
+    [DFlash-notes], conditioning; [Backbone] context feature extraction."""
+    return plain_rmsnorm(_f64(s) @ _f64(w_feature).T, context_norm, eps)
+
+
+def context_kv(c, positions, wk, wv, k_norm, eps: float, head_dim: int, theta: float):
+    """One draft layer's context K/V from the common c_t:
+    k = rope_1d(plain_head_rmsnorm(W_k c, key_norm), t);  v = W_v c.
+    Raw k is normalised without any intermediate rounding.  [DFlash-notes], context K/V."""
+    c = _f64(c)
+    k = rope_1d(plain_head_rmsnorm(c @ _f64(wk).T, k_norm, eps, head_dim), positions,
+                head_dim, theta)
+    v = c @ _f64(wv).T
+    return k, v
+
+
+def ring_slot(position: int, capacity: int) -> int:
+    """Absolute position p lives in slot p mod S of a ring of capacity S.
+    [DFlash-notes], ring storage."""
+    return position % capacity
+
+
+def ring_live_interval(frontier: int, capacity: int):
+    """[max(0, F - S), F): the positions a ring of capacity S holds at frontier F.
+    [DFlash-notes], ring storage."""
+    return max(0, frontier - capacity), frontier
+
+
+def materialize(geo, weights, feats, positions, frontier_after: int, rings=None,
+                request: int = 0) -> Dict[str, list]:
+    """Store one request's context K/V for the given positions into per-layer rings.
+
+    feats: [n, n_tgt*H] captured residual rows for ``positions`` (ascending).  Only
+    positions in each ring's final live interval [F - S, F) (F = ``frontier_after``)
+    are stored; the frontier still covers the whole chunk.  [DFlash-notes], context
+    prefill and ring storage.
+
+    rings: {"k": [L arrays [B, Hkv, cap, D]], "v": [...]} (created if None, B = 1).
+    """
+    L, Hkv, D = geo.n_layers, geo.n_kv_heads, geo.head_dim
+    if rings is None:
+        rings = {"k": [np.zeros((1, Hkv, geo.capacity(l), D)) for l in range(L)],
+                 "v": [np.zeros((1, Hkv, geo.capacity(l), D)) for l in range(L)]}
+    positions = np.asarray(positions, dtype=np.int64)
+    c = context_fusion(feats, weights["w_feature"], weights["context_norm"], geo.eps)
+    for l in range(L):
+        lw = weights["layers"][l]
+        k, v = context_kv(c, positions, lw["wk"], lw["wv"], lw["k_norm"], geo.eps, D,
+                          geo.rope_theta)
+        cap = geo.capacity(l)
+        lo, hi = ring_live_interval(frontier_after, cap)
+        for t, p in enumerate(positions):
+            if lo <= p < hi:
+                s = ring_slot(int(p), cap)
+                rings["k"][l][request, :, s, :] = k[t].reshape(Hkv, D)
+                rings["v"][l][request, :, s, :] = v[t].reshape(Hkv, D)
+    return rings
+
+
+# --------------------------------------------------------------------------- attention
+def key_visible(p_query: int, p_key: int, window: int) -> bool:
+    """|p_key - p_query| < S for a local layer (S = window > 0); always for a full
+    layer (window == 0).  [DFlash-notes], local-window attention rule."""
+    return window <= 0 or abs(p_key - p_query) < window
+
+
+def block_attention(q, k_blk, v_blk, k_ctx, v_ctx, ctx_positions, frontier: int,
+                    window: int, block_causal: bool, n_q_heads: int, n_kv_heads: int,
+                    head_dim: int) -> np.ndarray:
+    """softmax(q K^T / sqrt(D) + mask) V over concat(context, block) for one request.
+
+    q: [W, Hq*D] (block rows at positions F..F+W-1); k_blk, v_blk: [W, Hkv*D];
+    k_ctx, v_ctx: [n_ctx, Hkv, D] at ``ctx_positions`` (all < F).  Returns [W, Hq*D].
+    [DFlash-notes] per-layer equations and window rule; [BlockCausal] for the flag.
+    Explicit max-subtracted softmax."""
+    W = q.shape[0]
+    D = head_dim
+    G = n_q_heads // n_kv_heads
+    qh = _f64(q).reshape(W, n_q_heads, D)
+    kb = _f64(k_blk).reshape(W, n_kv_heads, D)
+    vb = _f64(v_blk).reshape(W, n_kv_heads, D)
+    kc = _f64(k_ctx)
+    vc = _f64(v_ctx)
+    ctx_positions = np.asarray(ctx_positions, dtype=np.int64)
+    n_ctx = kc.shape[0]
+    out = np.zeros((W, n_q_heads, D))
+    scale = 1.0 / math.sqrt(D)
+    for i in range(W):
+        pq = frontier + i
+        vis_ctx = np.array([key_visible(pq, int(p), window) for p in ctx_positions], bool)
+        vis_blk = np.array([key_visible(pq, frontier + j, window) and
+                            (not block_causal or j <= i) for j in range(W)], bool)
+        for h in range(n_q_heads):
+            g = h // G
+            keys = np.concatenate([kc[:, g, :], kb[:, g, :]], axis=0)      # [n_ctx+W, D]
+            vals = np.concatenate([vc[:, g, :], vb[:, g, :]], axis=0)
+            vis = np.concatenate([vis_ctx, vis_blk])
+            s = keys @ qh[i, h] * scale
+            s = np.where(vis, s, -np.inf)
+            s = s - np.max(s)
+            p = np.exp(s)
+            p = p / np.sum(p)
+            out[i, h] = p @ vals
+    return out.reshape(W, n_q_heads * D)
+
+
+def block_attention_bruteforce(q, k_blk, v_blk, k_ctx, v_ctx, ctx_positions, frontier,
+                               window, block_causal, n_q_heads, n_kv_heads, head_dim):
+    """The same attention as a per-(query, key) double loop with scalar arithmetic.
+    Used only to check ``block_attention`` on tiny inputs."""
+    W = q.shape[0]
+    D = head_dim
+    G = n_q_heads // n_kv_heads
+    q = _f64(q).reshape(W, n_q_heads, D)
+    kb = _f64(k_blk).reshape(W, n_kv_heads, D)
+    vb = _f64(v_blk).reshape(W, n_kv_heads, D)
+    kc, vc = _f64(k_ctx), _f64(v_ctx)
+    keys_pos = [int(p) for p in ctx_positions] + [frontier + j for j in range(W)]
+    out = np.zeros((W, n_q_heads, D))
+    for i in range(W):
+        for h in range(n_q_heads):
+            g = h // G
+            scores, vals = [], []
+            for kk, pk in enumerate(keys_pos):
+                is_blk = kk >= len(ctx_positions)
+                j = kk - len(ctx_positions)
+                if window > 0 and abs(pk - (frontier + i)) >= window:
+                    continue
+                if is_blk and block_causal and j > i:
+                    continue
+                kvec = kb[j, g] if is_blk else kc[kk, g]
+                vvec = vb[j, g] if is_blk else vc[kk, g]
+                dot = 0.0
+                for d in range(D):
+                    dot += q[i, h, d] * kvec[d]
+                scores.append(dot / math.sqrt(D))
+                vals.append(vvec)
+            mx = max(scores)
+            ws = [math.exp(s - mx) for s in scores]
+            tot = sum(ws)
+            acc = np.zeros(D)
+            for wgt, vv in zip(ws, vals):
+                acc += (wgt / tot) * vv
+            out[i, h] = acc
+    return out.reshape(W, n_q_heads * D)
+
+
+# --------------------------------------------------------------------------- layer
+def silu(x):
+    x = _f64(x)
+    return x / (1.0 + np.exp(-x))
+
+
+def sigmoid(x):
+    x = _f64(x)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def dflash_layer(x, lw, geo, positions, k_ctx, v_ctx, ctx_positions, frontier: int,
+                 layer: int):
+    """One draft layer for one request's block (no injection).  [DFlash-notes]:
+        n = plain_rmsnorm(x, input_norm)
+        q = rope(head_rmsnorm(W_q n)), k = rope(head_rmsnorm(W_k n)), v = W_v n
+        a = attention(q, [K_ctx; k], [V_ctx; v]) ; y = x + W_o a
+        m = plain_rmsnorm(y, post_attention_norm)
+        x_next = y + W_down(SiLU(W_gate m) * (W_up m))
+    Returns (x_next, block k, block v)."""
+    D, eps, th = geo.head_dim, geo.eps, geo.rope_theta
+    x = _f64(x)
+    n = plain_rmsnorm(x, lw["in_norm"], eps)
+    q = rope_1d(plain_head_rmsnorm(n @ _f64(lw["wq"]).T, lw["q_norm"], eps, D), positions, D, th)
+    k = rope_1d(plain_head_rmsnorm(n @ _f64(lw["wk"]).T, lw["k_norm"], eps, D), positions, D, th)
+    v = n @ _f64(lw["wv"]).T
+    a = block_attention(q, k, v, k_ctx, v_ctx, ctx_positions, frontier, geo.windows[layer],
+                        geo.block_causal, geo.n_q_heads, geo.n_kv_heads, D)
+    y = x + a @ _f64(lw["wo"]).T
+    m = plain_rmsnorm(y, lw["post_norm"], eps)
+    x_next = y + (silu(m @ _f64(lw["w_gate"]).T) * (m @ _f64(lw["w_up"]).T)) @ _f64(lw["w_down"]).T
+    return x_next, k, v
+
+
+# --------------------------------------------------------------------------- bridge
+def bridge_read(x, r_read, code_width: int, eps: float):
+    """DSpine code read for every row:  r = sqrt(mean x^2),  z = R_l x / (r + eps),
+    c = sqrt(Rc) z / (||z|| + eps).  Returns (c [W, Rc], r [W]).
+    [Bridge] read equations; [Transfer] (one learned projection per layer)."""
+    x = _f64(x)
+    r = np.sqrt(np.mean(x * x, axis=-1))
+    z = (x / (r + eps)[:, None]) @ _f64(r_read).T
+    c = math.sqrt(code_width) * z / (np.linalg.norm(z, axis=-1) + eps)[:, None]
+    return c, r
+
+
+def anchor_code(codebook_row, code_width: int) -> np.ndarray:
+    """Anchor rows use sqrt(Rc) times the anchor token's stored code.  [Bridge];
+    [Transfer] (a known token enters the space as r C_x)."""
+    return math.sqrt(code_width) * _f64(codebook_row)
+
+
+def inject(x, c, r, g_recv, g_pred, a_val, w_write, gate_bias=None) -> np.ndarray:
+    """Adjacent gated causal injection for one request's block (R-gate, R-anchor, R-rms):
+        for i >= 1: g = sigmoid(G c_i + G_p c_{i-1} + b),  m = g * (A c_{i-1}),
+                    x'_i = x_i + r_i W_l m
+        x'_0 = x_0 (the anchor receives no write)
+    All codes are the pre-injection codes of this layer.  [Bridge]; [Gate]."""
+    x = _f64(x)
+    c = _f64(c)
+    b = np.zeros(_f64(g_recv).shape[0]) if gate_bias is None else _f64(gate_bias)
+    G, Gp, A, Wl = _f64(g_recv), _f64(g_pred), _f64(a_val), _f64(w_write)
+    out = x.copy()
+    for i in range(1, x.shape[0]):
+        g = sigmoid(G @ c[i] + Gp @ c[i - 1] + b)
+        m = g * (A @ c[i - 1])
+        out[i] = x[i] + r[i] * (Wl @ m)
+    return out
+
+
+# --------------------------------------------------------------------------- head
+def lm_head_logits(h, embed_head, chunk: int = 16384) -> np.ndarray:
+    """logits = E h with the tied [V, H] head, computed in vocabulary chunks to bound
+    memory (a plain matrix product; chunking does not change any value)."""
+    h = _f64(h)
+    E = embed_head
+    V = E.shape[0]
+    out = np.empty((h.shape[0], V))
+    for v0 in range(0, V, chunk):
+        out[:, v0:v0 + chunk] = h @ _f64(E[v0:v0 + chunk]).T
+    return out
+
+
+def argmax_lowest(logits) -> np.ndarray:
+    """Per-row argmax; ties resolve to the lowest token id (R-tie)."""
+    return np.argmax(_f64(logits), axis=-1)
+
+
+def top2_gap(logits) -> np.ndarray:
+    s = np.sort(_f64(logits), axis=-1)
+    return s[:, -1] - s[:, -2]
+
+
+# --------------------------------------------------------------------------- round
+def ring_context(rings, layer: int, request: int, frontier: int, capacity: int):
+    """The context K/V a request's ring holds for one layer: positions of the live
+    interval in ascending order, read from slot p mod S."""
+    lo, hi = ring_live_interval(frontier, capacity)
+    pos = np.arange(lo, hi, dtype=np.int64)
+    slots = pos % capacity
+    k = _f64(rings["k"][layer][request])[:, slots, :].transpose(1, 0, 2)   # [n, Hkv, D]
+    v = _f64(rings["v"][layer][request])[:, slots, :].transpose(1, 0, 2)
+    return k, v, pos
+
+
+def draft_request(geo, weights, rings, request: int, anchor: int, frontier: int,
+                  mask_id: int, n_masks: int) -> Dict[str, np.ndarray]:
+    """One request's block through every draft layer (plus injection when the
+    geometry has a code width), then the final norm.  [DFlash-notes] draft input
+    table and per-layer equations; [Bridge] and [Gate] for the injection."""
+    W = n_masks + 1
+    E = weights["embed_head"]
+    ids = [anchor] + [mask_id] * n_masks
+    x = _f64(np.stack([np.asarray(E[i]) for i in ids]))                 # [W, H]
+    positions = frontier + np.arange(W, dtype=np.int64)
+    inj = geo.code_width > 0
+    layers_x = []
+    for l in range(geo.n_layers):
+        lw = weights["layers"][l]
+        k_ctx, v_ctx, cpos = ring_context(rings, l, request, frontier, geo.capacity(l))
+        x, _, _ = dflash_layer(x, lw, geo, positions, k_ctx, v_ctx, cpos, frontier, l)
+        if inj:
+            c, r = bridge_read(x, lw["r_read"], geo.code_width, geo.eps)
+            c[0] = anchor_code(weights["codebook"][anchor], geo.code_width)
+            x = inject(x, c, r, weights["g_recv"], weights["g_pred"], weights["a_val"],
+                       lw["w_write"], weights.get("gate_bias"))
+        layers_x.append(x.copy())
+    h = plain_rmsnorm(x, weights["final_norm"], geo.eps)
+    return {"x_layers": np.stack(layers_x), "h": h}
+
+
+def draft_round(geo, weights, rings, anchors: Sequence[int], frontiers: Sequence[int],
+                mask_id: int, n_masks: int, with_head: bool = True) -> Dict[str, np.ndarray]:
+    """The whole proposal round for B independent requests.
+    Returns x_layers [L, B, W, H], h [B, W, H] and, with the head, the mask rows'
+    logits [B, K, V], argmax tokens [B, K] and top-2 gaps [B, K].
+    [DFlash-notes] proposal head: only the K mask columns are scored."""
+    outs = [draft_request(geo, weights, rings, b, int(anchors[b]), int(frontiers[b]),
+                          mask_id, n_masks) for b in range(len(anchors))]
+    res = {"x_layers": np.stack([o["x_layers"] for o in outs], axis=1),
+           "h": np.stack([o["h"] for o in outs])}
+    if with_head:
+        B = len(anchors)
+        hm = res["h"][:, 1:, :].reshape(B * n_masks, -1)
+        logits = lm_head_logits(hm, weights["embed_head"])
+        res["logits"] = logits.reshape(B, n_masks, -1)
+        res["tokens"] = argmax_lowest(logits).reshape(B, n_masks)
+        res["gap"] = top2_gap(logits).reshape(B, n_masks)
+    return res
+
+
+# --------------------------------------------------------------------------- sizes
+def kv_bytes_per_position(n_layers: int, n_kv_heads: int, head_dim: int,
+                          k_bytes: int, v_bytes: int) -> int:
+    """Draft K/V bytes one retained position occupies over all layers.  [Cache]."""
+    return n_layers * n_kv_heads * head_dim * (k_bytes + v_bytes)
+
+
+def ring_image_bytes(n_layers: int, n_kv_heads: int, head_dim: int, capacity: int,
+                     k_bytes: int = 2, v_bytes: int = 2) -> int:
+    """Bytes of all local rings of one request.  [DFlash-notes], ring storage."""
+    return kv_bytes_per_position(n_layers, n_kv_heads, head_dim, k_bytes, v_bytes) * capacity
+
+
+def injection_param_count(hidden: int, n_layers: int, code_width: int, msg_width: int) -> int:
+    """Per layer one read R_l [Rc, H] and one write W_l [H, Mc]; the receiver gate,
+    predecessor gate and value maps [Mc, Rc] are shared by all layers (R-read).
+    [Bridge]; [Gate]; [Transfer] (about 33M extra parameters at Qwen3-8B geometry)."""
+    return n_layers * (code_width * hidden + hidden * msg_width) + 3 * msg_width * code_width
+
+
+def round_weight_bytes(geo, elem_bytes: int = 2) -> int:
+    """Weight bytes one round streams: every draft layer's projections (and the
+    bridge's, when present), the shared gate maps and the tied head."""
+    H, D, L = geo.hidden, geo.head_dim, geo.n_layers
+    per_layer = (H * geo.n_q_heads * D + 2 * H * geo.n_kv_heads * D + geo.n_q_heads * D * H
+                 + 3 * H * geo.ffn + 4 * H + 2 * D)
+    if geo.code_width > 0:
+        per_layer += geo.code_width * H + H * geo.msg_width
+    total = L * per_layer + geo.vocab * H + H
+    if geo.code_width > 0:
+        total += 3 * geo.msg_width * geo.code_width
+    return total * elem_bytes

@@ -1,0 +1,554 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Every check here compares the oracle with something other than itself: a value the
+pages print (tests/golden/page_numbers.json), a closed form worked by hand, a
+textbook identity, an invariant, or a brute-force loop on tiny inputs.  Each is
+chosen so that a plausible slip in the oracle (a dropped term, a wrong sign or
+index, a transposed operand, a mis-scaled softmax) fails at least one of them.
+"""
+import cmath
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import dspine_oracle as O
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")))
+rng = np.random.default_rng(1234)
+
+
+class Geo:
+    """A small geometry object with the fields the oracle reads."""
+
+    def __init__(self, **kw):
+        d = dict(hidden=16, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=8, ffn=24,
+                 vocab=40, n_target_layers=2, windows=(0, 0), code_width=8, msg_width=4,
+                 eps=1e-6, rope_theta=1e4, block_causal=False, full_capacity=64)
+        d.update(kw)
+        self.__dict__.update(d)
+
+    def capacity(self, l):
+        s = self.windows[l]
+        return s if s > 0 else self.full_capacity
+
+
+def rand_weights(g, seed=0, zero_write=False, gate_bias=False):
+    r = np.random.default_rng(seed)
+    H, D = g.hidden, g.head_dim
+
+    def m(*s):
+        return r.normal(0, 0.3, s)
+
+    def gain(n):
+        return 1.0 + r.normal(0, 0.1, n)
+
+    w = {"w_feature": m(H, g.n_target_layers * H), "context_norm": gain(H),
+         "final_norm": gain(H), "embed_head": m(g.vocab, H), "layers": []}
+    if g.code_width:
+        cb = r.normal(0, 1, (g.vocab, g.code_width))
+        w["codebook"] = cb / np.linalg.norm(cb, axis=1, keepdims=True)
+        w["g_recv"], w["g_pred"], w["a_val"] = (m(g.msg_width, g.code_width) for _ in range(3))
+        w["gate_bias"] = r.normal(0, 0.3, g.msg_width) if gate_bias else None
+    for _ in range(g.n_layers):
+        lw = {"in_norm": gain(H), "wq": m(g.n_q_heads * D, H), "wk": m(g.n_kv_heads * D, H),
+              "wv": m(g.n_kv_heads * D, H), "q_norm": gain(D), "k_norm": gain(D),
+              "wo": m(H, g.n_q_heads * D), "post_norm": gain(H), "w_gate": m(g.ffn, H),
+              "w_up": m(g.ffn, H), "w_down": m(H, g.ffn)}
+        if g.code_width:
+            lw["r_read"] = m(g.code_width, H)
+            lw["w_write"] = np.zeros((H, g.msg_width)) if zero_write else m(H, g.msg_width)
+        w["layers"].append(lw)
+    return w
+
+
+def rand_rings(g, B, frontiers, seed=5):
+    r = np.random.default_rng(seed)
+    rings = {"k": [], "v": []}
+    for l in range(g.n_layers):
+        cap = g.capacity(l)
+        rings["k"].append(r.normal(0, 1, (B, g.n_kv_heads, cap, g.head_dim)))
+        rings["v"].append(r.normal(0, 1, (B, g.n_kv_heads, cap, g.head_dim)))
+    return rings
+
+
+# ----------------------------------------------------------------- plain_rmsnorm
+def test_rmsnorm_constant_vector_closed_form():
+    # x = c * 1: mean(x^2) = c^2, so out = w * c / sqrt(c^2 + eps)  (eps INSIDE the root)
+    for c, eps in [(3.0, 1e-6), (0.5, 1.0), (-2.0, 0.25)]:
+        x = np.full(6, c)
+        w = np.array([1.0, 2.0, 0.5, -1.0, 3.0, 0.0])
+        np.testing.assert_allclose(O.plain_rmsnorm(x, w, eps), w * c / math.sqrt(c * c + eps),
+                                   rtol=1e-15)
+
+
+def test_rmsnorm_hand_value():
+    # x = [3, 4], eps = 0: mean square 12.5, so x / 3.5355339... = [0.84852814, 1.13137085]
+    out = O.plain_rmsnorm(np.array([3.0, 4.0]), np.array([1.0, 0.5]), 0.0)
+    np.testing.assert_allclose(out, [0.848528137423857, 0.565685424949238], rtol=1e-14)
+
+
+def test_rmsnorm_unit_gain_has_rms_one():
+    x = rng.normal(0, 5, (7, 33))
+    y = O.plain_rmsnorm(x, np.ones(33), 1e-6)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, atol=1e-6)
+    assert np.linalg.norm(y[0]) == pytest.approx(math.sqrt(33), rel=1e-6)
+
+
+def test_head_rmsnorm_normalises_each_head_separately():
+    x = np.concatenate([rng.normal(0, 1, 8), 100 * rng.normal(0, 1, 8)])[None, :]
+    y = O.plain_head_rmsnorm(x, np.ones(8), 0.0, 8).reshape(2, 8)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), [1.0, 1.0], rtol=1e-13)
+
+
+# ----------------------------------------------------------------- RoPE
+def test_rope_hand_value_split_half():
+    # D = 4, theta = 100: inv_freq = [1, 0.1]. pos 1 rotates pair (x0, x2) by 1 rad.
+    x = np.array([[1.0, 0.0, 0.0, 0.0]])
+    out = O.rope_1d(x, [1], 4, 100.0)
+    np.testing.assert_allclose(out, [[0.5403023058681398, 0.0, 0.8414709848078965, 0.0]],
+                               atol=1e-15)
+    x = np.array([[0.0, 1.0, 0.0, 0.0]])     # pair (x1, x3) rotates by 0.1 rad
+    out = O.rope_1d(x, [1], 4, 100.0)
+    np.testing.assert_allclose(out, [[0.0, 0.9950041652780258, 0.0, 0.09983341664682815]],
+                               atol=1e-15)
+
+
+def test_rope_equals_complex_rotation():
+    # (x_j + i x_{j+D/2}) * exp(i * pos * theta^(-2j/D)) for every head and j.
+    D, theta = 16, 1e7
+    x = rng.normal(0, 1, (3, 2 * D))
+    pos = [0, 7, 4093]
+    out = O.rope_1d(x, pos, D, theta)
+    for t in range(3):
+        for h in range(2):
+            for j in range(D // 2):
+                z = complex(x[t, h * D + j], x[t, h * D + j + D // 2])
+                z *= cmath.exp(1j * pos[t] * theta ** (-2.0 * j / D))
+                assert out[t, h * D + j] == pytest.approx(z.real, abs=1e-12)
+                assert out[t, h * D + j + D // 2] == pytest.approx(z.imag, abs=1e-12)
+
+
+def test_rope_position_zero_identity_and_norm():
+    D = 128
+    x = rng.normal(0, 1, (4, 3 * D))
+    np.testing.assert_array_equal(O.rope_1d(x, [0, 0, 0, 0], D, 1e7), x)
+    y = O.rope_1d(x, [1, 100, 5000, 123456], D, 1e7)
+    np.testing.assert_allclose(np.linalg.norm(y.reshape(4, 3, D), axis=-1),
+                               np.linalg.norm(x.reshape(4, 3, D), axis=-1), rtol=1e-12)
+
+
+def test_rope_relative_position():
+    D = 64
+    q, k = rng.normal(0, 1, (1, D)), rng.normal(0, 1, (1, D))
+    dots = [float((O.rope_1d(q, [m], D, 1e7) @ O.rope_1d(k, [n], D, 1e7).T)[0, 0])
+            for m, n in [(10, 3), (1010, 1003), (40000, 39993)]]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-9)
+
+
+# ----------------------------------------------------------------- context
+def test_context_fusion_hand_case():
+    # W_feature = [I I] sums the two captured layers; then plain_rmsnorm.
+    H = 2
+    W = np.concatenate([np.eye(H), np.eye(H)], axis=1)
+    s = np.array([[1.0, 2.0, 2.0, 2.0]])          # layer0 = [1,2], layer1 = [2,2] -> [3,4]
+    c = O.context_fusion(s, W, np.ones(H), 0.0)
+    np.testing.assert_allclose(c, [[0.848528137423857, 1.131370849898476]], rtol=1e-14)
+
+
+def test_context_kv_position_independence_and_chunking():
+    g = Geo(windows=(5, 0), full_capacity=32)
+    w = rand_weights(g)
+    n = 12
+    feats = rng.normal(0, 1, (n, g.n_target_layers * g.hidden))
+    pos = np.arange(3, 3 + n)
+    full = O.materialize(g, w, feats, pos, 3 + n)
+    # one position at a time, ascending, with the same final frontier
+    one = None
+    for t in range(n):
+        one = O.materialize(g, w, feats[t:t + 1], pos[t:t + 1], 3 + n, rings=one)
+    # two uneven chunks
+    ch = O.materialize(g, w, feats[:7], pos[:7], 3 + n)
+    ch = O.materialize(g, w, feats[7:], pos[7:], 3 + n, rings=ch)
+    # (BLAS may sum a batched product in another order than a single row: 1e-12)
+    for l in range(g.n_layers):
+        for key in ("k", "v"):
+            np.testing.assert_allclose(full[key][l], one[key][l], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(full[key][l], ch[key][l], rtol=1e-12, atol=1e-13)
+
+
+def test_materialize_stores_only_final_window():
+    g = Geo(windows=(4, 0), full_capacity=32)
+    w = rand_weights(g)
+    n = 11
+    feats = rng.normal(0, 1, (n, g.n_target_layers * g.hidden))
+    pos = np.arange(n)
+    rings = O.materialize(g, w, feats, pos, n)
+    # Local ring (S=4) holds exactly positions 7..10 at slots p mod 4.
+    c = O.context_fusion(feats, w["w_feature"], w["context_norm"], g.eps)
+    k, v = O.context_kv(c, pos, w["layers"][0]["wk"], w["layers"][0]["wv"],
+                        w["layers"][0]["k_norm"], g.eps, g.head_dim, g.rope_theta)
+    for p in range(7, 11):
+        np.testing.assert_array_equal(rings["k"][0][0, :, p % 4, :],
+                                      k[p].reshape(g.n_kv_heads, g.head_dim))
+    # the full-context ring holds every position
+    k1, _ = O.context_kv(c, pos, w["layers"][1]["wk"], w["layers"][1]["wv"],
+                         w["layers"][1]["k_norm"], g.eps, g.head_dim, g.rope_theta)
+    for p in range(11):
+        np.testing.assert_array_equal(rings["k"][1][0, :, p, :],
+                                      k1[p].reshape(g.n_kv_heads, g.head_dim))
+    # storing only the tail chunk gives the same local ring
+    tail = O.materialize(g, w, feats[7:], pos[7:], n)
+    np.testing.assert_allclose(tail["k"][0], rings["k"][0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(tail["v"][0], rings["v"][0], rtol=1e-12, atol=1e-13)
+    assert O.ring_live_interval(11, 4) == (7, 11)
+    assert O.ring_live_interval(3, 4) == (0, 3)
+    assert O.ring_slot(4097, 2048) == 1
+
+
+# ----------------------------------------------------------------- attention
+def _att_inputs(W, n_ctx, Hq, Hkv, D, seed):
+    r = np.random.default_rng(seed)
+    return (r.normal(0, 1, (W, Hq * D)), r.normal(0, 1, (W, Hkv * D)),
+            r.normal(0, 1, (W, Hkv * D)), r.normal(0, 1, (n_ctx, Hkv, D)),
+            r.normal(0, 1, (n_ctx, Hkv, D)))
+
+
+@pytest.mark.parametrize("window,causal", [(0, False), (0, True), (3, False), (5, True),
+                                           (5, False), (2, True)])
+def test_attention_matches_bruteforce(window, causal):
+    W, F, Hq, Hkv, D = 4, 9, 4, 2, 4
+    q, kb, vb, kc, vc = _att_inputs(W, F, Hq, Hkv, D, window * 10 + causal)
+    pos = np.arange(F)
+    a = O.block_attention(q, kb, vb, kc, vc, pos, F, window, causal, Hq, Hkv, D)
+    b = O.block_attention_bruteforce(q, kb, vb, kc, vc, pos, F, window, causal, Hq, Hkv, D)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_softmax_scale_hand_value():
+    # D=4, one context key and one block key; scores 2*1/sqrt(4) = 1 and 0.
+    D = 4
+    q = np.array([[2.0, 0, 0, 0]])
+    kc = np.array([[[1.0, 0, 0, 0]]])             # [n_ctx=1, Hkv=1, D]
+    vc = np.array([[[1.0, 0, 0, 0]]])
+    kb = np.zeros((1, D))
+    vb = np.array([[0.0, 1.0, 0, 0]])
+    out = O.block_attention(q, kb, vb, kc, vc, [0], 1, 0, False, 1, 1, D)
+    e = math.e
+    np.testing.assert_allclose(out, [[e / (1 + e), 1 / (1 + e), 0, 0]], rtol=1e-14)
+
+
+def _visible_sets(W, F, S, causal):
+    """With q = 0 every visible key gets the same weight; one-hot values make the
+    output row the indicator of the visible keys divided by their count."""
+    n_ctx = F
+    D = n_ctx + W
+    q = np.zeros((W, D))
+    kb = np.zeros((W, D))
+    kc = np.zeros((n_ctx, 1, D))
+    vc = np.eye(D)[:n_ctx][:, None, :]
+    vb = np.eye(D)[n_ctx:]
+    out = O.block_attention(q, kb, vb, kc, vc, np.arange(n_ctx), F, S, causal, 1, 1, D)
+    return out > 1e-12
+
+
+def test_window_endpoints_and_visible_counts():
+    for case in GOLD["visible_context_full_left"]["cases"]:
+        S, F, W = case["S"], case["F"], case["W"]
+        vis = _visible_sets(W, F, S, False)
+        for i in range(W):
+            ctx = np.nonzero(vis[i, :F])[0]
+            assert len(ctx) == max(0, S - 1 - i)         # page-printed count
+            if S - 1 - i > 0:
+                assert ctx.min() == F + i - (S - 1)      # distance S-1 visible
+            if F + i - S >= 0:
+                assert not vis[i, F + i - S]             # distance S hidden
+            np.testing.assert_array_equal(vis[i, F:], [abs(j - i) < S for j in range(W)])
+
+
+def test_block_causal_mask():
+    W, F = 5, 6
+    vis = _visible_sets(W, F, 0, True)
+    for i in range(W):
+        assert vis[i, :F].all()
+        np.testing.assert_array_equal(vis[i, F:], [j <= i for j in range(W)])
+
+
+def test_local_equals_full_when_window_covers_everything():
+    W, F, Hq, Hkv, D = 4, 10, 4, 2, 8
+    q, kb, vb, kc, vc = _att_inputs(W, F, Hq, Hkv, D, 7)
+    a = O.block_attention(q, kb, vb, kc, vc, np.arange(F), F, F + W, False, Hq, Hkv, D)
+    b = O.block_attention(q, kb, vb, kc, vc, np.arange(F), F, 0, False, Hq, Hkv, D)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_gqa_equals_mha_with_duplicated_kv_heads():
+    W, F, Hq, Hkv, D = 3, 7, 4, 2, 8
+    q, kb, vb, kc, vc = _att_inputs(W, F, Hq, Hkv, D, 9)
+    a = O.block_attention(q, kb, vb, kc, vc, np.arange(F), F, 4, False, Hq, Hkv, D)
+    rep = lambda t: np.repeat(t.reshape(t.shape[0], Hkv, D), Hq // Hkv, axis=1)
+    b = O.block_attention(q, rep(kb).reshape(W, -1), rep(vb).reshape(W, -1), rep(kc), rep(vc),
+                          np.arange(F), F, 4, False, Hq, Hq, D)
+    np.testing.assert_allclose(a, b, rtol=1e-14)
+
+
+# ----------------------------------------------------------------- layer
+def test_silu_and_sigmoid_values():
+    np.testing.assert_allclose(O.sigmoid(np.array([0.0, 1.0])), [0.5, 0.7310585786300049])
+    np.testing.assert_allclose(O.silu(np.array([0.0, 1.0, -1.0])),
+                               [0.0, 0.7310585786300049, -0.2689414213699951])
+
+
+def _identity_layer_geo():
+    return Geo(hidden=2, n_q_heads=1, n_kv_heads=1, head_dim=2, ffn=2, eps=0.0,
+               code_width=0, msg_width=0, windows=(0, 0), n_layers=1)
+
+
+def test_layer_swiglu_hand_value():
+    # Attention output removed (W_o = 0); W_gate = I, W_up = 2I, W_down = I, unit gains.
+    # y = x = [1, 1]: m = [1, 1]; x_next = y + SiLU(m) * 2m = 1 + 2 * 0.7310585786
+    g = _identity_layer_geo()
+    lw = {"in_norm": np.ones(2), "wq": np.eye(2), "wk": np.eye(2), "wv": np.eye(2),
+          "q_norm": np.ones(2), "k_norm": np.ones(2), "wo": np.zeros((2, 2)),
+          "post_norm": np.ones(2), "w_gate": np.eye(2), "w_up": 2 * np.eye(2),
+          "w_down": np.eye(2)}
+    x = np.array([[1.0, 1.0]])
+    out, _, _ = O.dflash_layer(x, lw, g, np.array([5]), np.zeros((0, 1, 2)),
+                               np.zeros((0, 1, 2)), np.zeros(0, np.int64), 5, 0)
+    np.testing.assert_allclose(out, [[2.4621171572600098, 2.4621171572600098]], rtol=1e-14)
+
+
+def test_layer_attention_residual_hand_value():
+    # W_q = W_k = 0 -> q = k = 0 -> uniform weights over the visible keys.
+    # Context values [2, 0] and [0, 4]; the block's own value W_v n with W_v = 0.
+    # a = mean([2,0],[0,4],[0,0]) = [2/3, 4/3]; W_o = I; MLP removed (W_down = 0).
+    # (eps > 0 so that the head norm of the all-zero q and k is 0, not 0/0.)
+    g = _identity_layer_geo()
+    g.eps = 1e-6
+    lw = {"in_norm": np.ones(2), "wq": np.zeros((2, 2)), "wk": np.zeros((2, 2)),
+          "wv": np.zeros((2, 2)), "q_norm": np.ones(2), "k_norm": np.ones(2),
+          "wo": np.eye(2), "post_norm": np.ones(2), "w_gate": np.eye(2), "w_up": np.eye(2),
+          "w_down": np.zeros((2, 2))}
+    x = np.array([[1.0, -1.0]])
+    kc = np.zeros((2, 1, 2))
+    vc = np.array([[[2.0, 0.0]], [[0.0, 4.0]]])
+    out, _, _ = O.dflash_layer(x, lw, g, np.array([2]), kc, vc, np.arange(2), 2, 0)
+    np.testing.assert_allclose(out, [[1 + 2 / 3, -1 + 4 / 3]], rtol=1e-14)
+
+
+# ----------------------------------------------------------------- bridge
+def test_bridge_read_hand_value_and_norm():
+    # x = [3, 4], R = I (Rc = 2), eps = 0: c = sqrt(2) * [0.6, 0.8]; r = sqrt(12.5)
+    c, r = O.bridge_read(np.array([[3.0, 4.0]]), np.eye(2), 2, 0.0)
+    np.testing.assert_allclose(c, [[math.sqrt(2) * 0.6, math.sqrt(2) * 0.8]], rtol=1e-14)
+    np.testing.assert_allclose(r, [math.sqrt(12.5)], rtol=1e-15)
+    x = rng.normal(0, 3, (5, 40))
+    R = rng.normal(0, 1, (16, 40))
+    c, _ = O.bridge_read(x, R, 16, 1e-6)
+    np.testing.assert_allclose(np.linalg.norm(c, axis=-1), 4.0, rtol=1e-6)
+    c2, _ = O.bridge_read(7.5 * x, R, 16, 1e-6)
+    np.testing.assert_allclose(c2, c, rtol=1e-6)
+
+
+def test_anchor_code_exact():
+    row = rng.normal(0, 1, 64)
+    row /= np.linalg.norm(row)
+    np.testing.assert_array_equal(O.anchor_code(row, 64), 8.0 * row)
+    assert np.linalg.norm(O.anchor_code(row, 1024)) == pytest.approx(32.0, rel=1e-12)
+
+
+def _scalar_inject(G, Gp, A, Wl, x, c, b=None):
+    one = lambda v: np.array([[v]])
+    return O.inject(np.array(x, float)[:, None], np.array(c, float)[:, None],
+                    np.abs(np.array(x, float)), one(G), one(Gp), one(A), one(Wl),
+                    None if b is None else np.array([b]))[:, 0]
+
+
+def test_inject_hand_values():
+    # H = Rc = Mc = 1.  x = [2, 3] so r_1 = 3; predecessor code c_0 = 2, receiver c_1 = 1.
+    # Gate 0 everywhere: g = 1/2, m = A c_0 / 2 = 1, write = r_1 * W m = 3.
+    np.testing.assert_allclose(_scalar_inject(0, 0, 1, 1, [2, 3], [2, 1]), [2, 6])
+    # Predecessor gate drives g -> 1: write = 3 * 2 = 6.
+    np.testing.assert_allclose(_scalar_inject(0, 50, 1, 1, [2, 3], [2, 1]), [2, 9])
+    # Receiver gate drives g -> 0: no write.
+    np.testing.assert_allclose(_scalar_inject(-50, 0, 1, 1, [2, 3], [2, 1]), [2, 3])
+    # The value comes from the predecessor's code (c_0), not the receiver's.
+    np.testing.assert_allclose(_scalar_inject(0, 0, 1, 1, [2, 3], [0, 1]), [2, 3])
+    # Bias enters the gate: b = +50 -> g = 1.
+    np.testing.assert_allclose(_scalar_inject(0, 0, 1, 1, [2, 3], [2, 1], b=50), [2, 9])
+    # Sign of the write follows W and A: W = -1 gives 3 - 3 = 0.
+    np.testing.assert_allclose(_scalar_inject(0, 0, 1, -1, [2, 3], [2, 1]), [2, 0])
+    # A negative receiver state scales by its RMS |x| (positive).
+    np.testing.assert_allclose(_scalar_inject(0, 0, 1, 1, [2, -3], [2, 1]), [2, 0])
+
+
+def test_inject_anchor_untouched_zero_write_identity_and_locality():
+    W, H, Rc, Mc = 6, 10, 8, 4
+    x = rng.normal(0, 1, (W, H))
+    c = rng.normal(0, 1, (W, Rc))
+    r = np.sqrt(np.mean(x * x, axis=-1))
+    G, Gp, A = (rng.normal(0, 1, (Mc, Rc)) for _ in range(3))
+    Wl = rng.normal(0, 1, (H, Mc))
+    out = O.inject(x, c, r, G, Gp, A, Wl)
+    np.testing.assert_array_equal(out[0], x[0])
+    np.testing.assert_array_equal(O.inject(x, c, r, G, Gp, A, np.zeros((H, Mc))), x)
+    for j in range(W):
+        c2 = c.copy()
+        c2[j] += 1.0
+        diff = np.any(O.inject(x, c2, r, G, Gp, A, Wl) != out, axis=1)
+        expect = np.zeros(W, bool)
+        if j >= 1:
+            expect[j] = True           # receiver gate term G c_j
+        if j + 1 < W:
+            expect[j + 1] = True       # predecessor terms G_p c_j and A c_j
+        np.testing.assert_array_equal(diff, expect)
+
+
+def test_inject_positive_homogeneity():
+    W, H, Rc, Mc = 5, 12, 8, 4
+    x = rng.normal(0, 1, (W, H))
+    R = rng.normal(0, 1, (Rc, H))
+    G, Gp, A = (rng.normal(0, 1, (Mc, Rc)) for _ in range(3))
+    Wl = rng.normal(0, 1, (H, Mc))
+
+    def step(xx):
+        c, r = O.bridge_read(xx, R, Rc, 0.0)
+        return O.inject(xx, c, r, G, Gp, A, Wl)
+
+    np.testing.assert_allclose(step(3.0 * x), 3.0 * step(x), rtol=1e-12)
+
+
+# ----------------------------------------------------------------- head
+def test_argmax_bruteforce_and_ties():
+    logits = rng.normal(0, 1, (6, 50))
+    logits[2, 7] = logits[2, 31] = logits[2].max() + 1.0      # tie -> 7
+    got = O.argmax_lowest(logits)
+    for i in range(6):
+        best, bi = -np.inf, -1
+        for v in range(50):
+            if logits[i, v] > best:
+                best, bi = logits[i, v], v
+        assert got[i] == bi
+    assert got[2] == 7
+    gap = O.top2_gap(logits)
+    assert gap[2] == 0.0
+
+
+def test_lm_head_chunking_matches_product():
+    h = rng.normal(0, 1, (3, 16))
+    E = rng.normal(0, 1, (100, 16))
+    np.testing.assert_allclose(O.lm_head_logits(h, E, chunk=7), h @ E.T, rtol=1e-13)
+
+
+# ----------------------------------------------------------------- full round
+def _round(g, w, B=2, F=(9, 13), seed=3, mask_id=0, anchors=None, **kw):
+    rings = rand_rings(g, B, F, seed)
+    anchors = anchors or [5, 17][:B]
+    return O.draft_round(g, w, rings, anchors, list(F)[:B], mask_id, 5, **kw), rings
+
+
+def test_round_zero_write_equals_plain_dflash():
+    g = Geo(windows=(6, 0))
+    w = rand_weights(g, zero_write=True)
+    a, _ = _round(g, w)
+    g0 = Geo(windows=(6, 0), code_width=0, msg_width=0)
+    b, _ = _round(g0, w)
+    for key in ("x_layers", "h", "logits"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_round_requests_are_isolated_and_permutable():
+    g = Geo(windows=(5, 0))
+    w = rand_weights(g, gate_bias=True)
+    rings = rand_rings(g, 2, (9, 13))
+    ab = O.draft_round(g, w, rings, [5, 17], [9, 13], 0, 5)
+    sw = {"k": [k[::-1].copy() for k in rings["k"]], "v": [v[::-1].copy() for v in rings["v"]]}
+    ba = O.draft_round(g, w, sw, [17, 5], [13, 9], 0, 5)
+    np.testing.assert_array_equal(ab["x_layers"][:, 0], ba["x_layers"][:, 1])
+    np.testing.assert_array_equal(ab["tokens"][1], ba["tokens"][0])
+    # changing request 1's ring leaves request 0 unchanged
+    rings2 = {"k": [k.copy() for k in rings["k"]], "v": [v.copy() for v in rings["v"]]}
+    rings2["k"][0][1] += 1.0
+    c = O.draft_round(g, w, rings2, [5, 17], [9, 13], 0, 5)
+    np.testing.assert_array_equal(c["h"][0], ab["h"][0])
+    assert np.any(c["h"][1] != ab["h"][1])
+
+
+def test_round_with_no_layer_updates_is_embedding_nearest_row():
+    # W_o = 0, W_down = 0, W_write = 0: every layer is the identity, so the final state is
+    # the embedding rows and each mask row's proposal is argmax_v E_v . rmsnorm(E_MASK).
+    g = Geo(windows=(0, 0))
+    w = rand_weights(g)
+    for lw in w["layers"]:
+        lw["wo"][:] = 0
+        lw["w_down"][:] = 0
+        lw["w_write"][:] = 0
+    res, _ = _round(g, w, mask_id=11)
+    E = w["embed_head"]
+    n2 = sum(E[11][d] ** 2 for d in range(g.hidden)) / g.hidden
+    hm = [w["final_norm"][d] * E[11][d] / math.sqrt(n2 + g.eps) for d in range(g.hidden)]
+    best = max(range(g.vocab), key=lambda v: (sum(E[v][d] * hm[d] for d in range(g.hidden)), -v))
+    assert (res["tokens"] == best).all()
+    np.testing.assert_allclose(res["x_layers"][-1][0, 0], E[5], rtol=0, atol=0)
+
+
+def test_round_injection_changes_only_successors_of_the_anchor_row():
+    g = Geo(windows=(0, 0), n_layers=1)
+    w = rand_weights(g)
+    res, _ = _round(g, w, B=1, F=(9,))
+    w0 = rand_weights(g, zero_write=True)
+    ref, _ = _round(g, w0, B=1, F=(9,))
+    # anchor row: identical with or without the write (its incoming write is zero)
+    np.testing.assert_array_equal(res["x_layers"][0][0, 0], ref["x_layers"][0][0, 0])
+    assert np.all(np.any(res["x_layers"][0][0, 1:] != ref["x_layers"][0][0, 1:], axis=-1))
+
+
+# ----------------------------------------------------------------- page-printed numbers
+def test_kv_bytes_per_position_and_windows():
+    gd = GOLD["kv_bytes_per_position"]
+    geo = gd["geometry"]
+    per = O.kv_bytes_per_position(geo["n_layers"], geo["n_kv_heads"], geo["head_dim"],
+                                  geo["k_bytes"], geo["v_bytes"])
+    assert per == gd["value"]
+    assert per * GOLD["kv_bytes_window_8192_mib"]["capacity"] == \
+        GOLD["kv_bytes_window_8192_mib"]["value"] * 2 ** 20
+    assert per * GOLD["kv_bytes_131072_gib"]["capacity"] == \
+        GOLD["kv_bytes_131072_gib"]["value"] * 2 ** 30
+
+
+def test_ring_image_40mib():
+    gd = GOLD["ring_image_27b_dflash2_mib"]
+    g = gd["geometry"]
+    assert O.ring_image_bytes(g["n_layers"], g["n_kv_heads"], g["head_dim"], g["capacity"],
+                              g["k_bytes"], g["v_bytes"]) == gd["value"] * 2 ** 20
+
+
+def test_injection_parameter_count_pins_shared_and_per_layer_maps():
+    gd = GOLD["injection_params_qwen3_8b_millions"]
+    g = gd["geometry"]
+    n = O.injection_param_count(g["hidden"], g["n_layers"], g["code_width"], g["msg_width"])
+    assert round(n / 1e6) == gd["value"]
+    assert n == 33_030_144
+    # Per-layer gate maps (instead of shared) would give about 41M; a second per-layer
+    # read matrix about 54M: both miss the page's ~33M.
+    assert round((n + 4 * 3 * g["msg_width"] * g["code_width"]) / 1e6) != gd["value"]
+    assert round((n + g["n_layers"] * g["code_width"] * g["hidden"]) / 1e6) != gd["value"]
+
+
+def test_codebook_and_table_sizes():
+    gd = GOLD["codebook_mib"]
+    assert gd["shape"][0] * gd["shape"][1] * gd["elem_bytes"] / 2 ** 20 == pytest.approx(gd["value"], abs=0.5)
+    gd = GOLD["greedy_tail_tables_mib"]
+    tot = sum(a * b for a, b in gd["shapes"]) * gd["elem_bytes"] / 2 ** 20
+    assert tot == pytest.approx(gd["value"], abs=0.05)
+
+
+def test_27b_block_geometry():
+    gd = GOLD["block_27b"]
+    import bdsynth
+    w = bdsynth.DSPINE27B_B1
+    assert w.W == gd["W"] and w.n_masks == gd["masks"]
+    assert w.n_q_heads * w.head_dim == gd["q_proj_width"] and w.hidden == gd["hidden"]
+    assert w.mask_token_id == GOLD["qwen3_mask_token_id"]["value"]

@@ -1,0 +1,195 @@
+"""Thin ctypes binding of ``libblockdrafter.so`` (argument marshalling only).
+
+The functions carry the C ABI's names without the ``bd_`` prefix and take torch tensors
+(device memory) or plain ints; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing the import of this
+module's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from .builder import LIBPATH
+
+MAX_LAYERS = 16
+BF16, F32 = 0, 1
+BIDIRECTIONAL, CAUSAL = 0, 1
+
+STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "BD_ERR_CUDA",
+          -4: "BD_ERR_DEVICE_TIMEOUT", -5: "BD_ERR_WORKSPACE"}
+
+EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
+           "bd_lm_head_argmax", "bd_last_error", "bd_sync_status")
+
+
+class BdError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Config(C.Structure):
+    _fields_ = [("hidden", C.c_int), ("n_layers", C.c_int), ("n_q_heads", C.c_int),
+                ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
+                ("vocab", C.c_int), ("n_target_layers", C.c_int),
+                ("window", C.c_int * MAX_LAYERS), ("ring_capacity", C.c_int * MAX_LAYERS),
+                ("eps", C.c_float), ("rope_theta", C.c_float), ("mask_token_id", C.c_int),
+                ("code_width", C.c_int), ("msg_width", C.c_int), ("block_mask", C.c_int),
+                ("dtype", C.c_int)]
+
+
+LAYER_FIELDS = ("in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "post_norm", "w_gate",
+                "w_up", "w_down", "r_read", "w_write")
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in LAYER_FIELDS]
+
+
+class Weights(C.Structure):
+    _fields_ = [("w_feature", C.c_void_p), ("context_norm", C.c_void_p),
+                ("final_norm", C.c_void_p), ("embed_head", C.c_void_p), ("codebook", C.c_void_p),
+                ("g_recv", C.c_void_p), ("g_pred", C.c_void_p), ("a_val", C.c_void_p),
+                ("gate_bias", C.c_void_p), ("layer", LayerWeights * MAX_LAYERS)]
+
+
+class KvCache(C.Structure):
+    _fields_ = [("k", C.c_void_p * MAX_LAYERS), ("v", C.c_void_p * MAX_LAYERS),
+                ("b_max", C.c_int)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load the library (built by ``block_drafter_gb300.builder.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBPATH):
+            raise RuntimeError(f"libblockdrafter.so is not built ({LIBPATH}); run "
+                               "block_drafter_gb300.builder.build() first")
+        L = C.CDLL(LIBPATH)
+        vp, i, sz = C.c_void_p, C.c_int, C.c_size_t
+        L.bd_abi_version.restype = i
+        L.bd_workspace_bytes.restype = sz
+        L.bd_workspace_bytes.argtypes = [C.POINTER(Config), i, i, i]
+        L.bd_ctx_kv_materialize.restype = i
+        L.bd_ctx_kv_materialize.argtypes = [C.POINTER(Config), C.POINTER(Weights),
+                                            C.POINTER(KvCache), vp, vp, vp, vp, i, vp, sz, vp]
+        L.bd_draft_round.restype = i
+        L.bd_draft_round.argtypes = [C.POINTER(Config), C.POINTER(Weights), C.POINTER(KvCache),
+                                     vp, vp, i, i, vp, vp, vp, vp, sz, vp]
+        L.bd_lm_head_argmax.restype = i
+        L.bd_lm_head_argmax.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, vp, vp,
+                                        vp, sz, vp]
+        L.bd_last_error.restype = C.c_char_p
+        L.bd_sync_status.restype = i
+        L.bd_sync_status.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise BdError(status, lib().bd_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+# ------------------------------------------------------------------ marshalling
+def make_config(*, hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab,
+                n_target_layers, windows: Sequence[int], ring_capacity: Sequence[int], eps,
+                rope_theta, mask_token_id, code_width=0, msg_width=0, block_causal=False,
+                dtype=BF16) -> Config:
+    c = Config()
+    c.hidden, c.n_layers, c.n_q_heads, c.n_kv_heads = hidden, n_layers, n_q_heads, n_kv_heads
+    c.head_dim, c.ffn, c.vocab, c.n_target_layers = head_dim, ffn, vocab, n_target_layers
+    for l in range(n_layers):
+        c.window[l] = int(windows[l])
+        c.ring_capacity[l] = int(ring_capacity[l])
+    c.eps, c.rope_theta, c.mask_token_id = eps, rope_theta, mask_token_id
+    c.code_width, c.msg_width = code_width, msg_width
+    c.block_mask = CAUSAL if block_causal else BIDIRECTIONAL
+    c.dtype = dtype
+    return c
+
+
+def make_weights(cfg: Config, w: dict) -> Weights:
+    """``w``: dict of device tensors with the keys of ``bd_weights`` (and a ``layers``
+    list of per-layer dicts with the keys of ``bd_layer_weights``)."""
+    s = Weights()
+    for k in ("w_feature", "context_norm", "final_norm", "embed_head", "codebook", "g_recv",
+              "g_pred", "a_val", "gate_bias"):
+        t = w.get(k)
+        setattr(s, k, _ptr(t) if t is not None else None)
+    for l, lw in enumerate(w["layers"][:cfg.n_layers]):
+        for k in LAYER_FIELDS:
+            t = lw.get(k) if lw is not None else None
+            setattr(s.layer[l], k, _ptr(t) if t is not None else None)
+    return s
+
+
+def make_kv(k: Sequence[torch.Tensor], v: Sequence[torch.Tensor], b_max: int) -> KvCache:
+    s = KvCache()
+    for l, (kk, vv) in enumerate(zip(k, v)):
+        s.k[l] = kk.data_ptr()
+        s.v[l] = vv.data_ptr()
+    s.b_max = b_max
+    return s
+
+
+# ------------------------------------------------------------------ entry points
+def abi_version() -> int:
+    return lib().bd_abi_version()
+
+
+def workspace_bytes(cfg: Config, b_max: int, max_masks: int, max_ctx_rows: int) -> int:
+    n = lib().bd_workspace_bytes(C.byref(cfg), b_max, max_masks, max_ctx_rows)
+    if n == 0:
+        raise BdError(-1, "invalid config or sizes for bd_workspace_bytes")
+    return n
+
+
+def ctx_kv_materialize(cfg: Config, weights: Weights, kv: KvCache, target_feats: torch.Tensor,
+                       row_request: torch.Tensor, row_pos: torch.Tensor,
+                       ctx_frontier: torch.Tensor, workspace: torch.Tensor, stream=None):
+    _check(lib().bd_ctx_kv_materialize(
+        C.byref(cfg), C.byref(weights), C.byref(kv), _ptr(target_feats), _ptr(row_request),
+        _ptr(row_pos), _ptr(ctx_frontier), int(target_feats.shape[0]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def draft_round(cfg: Config, weights: Weights, kv: KvCache, anchor_ids: torch.Tensor,
+                frontier: torch.Tensor, n_masks: int, head_in: torch.Tensor,
+                workspace: torch.Tensor, hidden_out: Optional[torch.Tensor] = None,
+                layers_out: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().bd_draft_round(
+        C.byref(cfg), C.byref(weights), C.byref(kv), _ptr(anchor_ids), _ptr(frontier),
+        int(anchor_ids.shape[0]), int(n_masks), _ptr(head_in), _ptr(hidden_out),
+        _ptr(layers_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def lm_head_argmax(cfg: Config, weights: Weights, hidden: torch.Tensor, token_out: torch.Tensor,
+                   workspace: torch.Tensor, max_logit_out: Optional[torch.Tensor] = None,
+                   stream=None):
+    _check(lib().bd_lm_head_argmax(
+        C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
+        _ptr(max_logit_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def sync_status(stream=None):
+    _check(lib().bd_sync_status(_stream(stream)))

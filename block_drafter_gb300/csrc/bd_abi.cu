@@ -1,0 +1,589 @@
+// C ABI of the drafter library: argument validation, workspace planning and the launch
+// sequences of the three entry points.  Every step of the round runs in this library's
+// kernels; nothing here computes on the host beyond launch geometry and the RoPE
+// inverse frequencies.
+#include "../../include/blockdrafter.h"
+#include "bd_internal.h"
+#include "bd_kernels.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+namespace {
+
+using namespace bd;
+
+thread_local std::string t_last_error;
+
+bd_status fail(bd_status s, const std::string &msg) {
+  t_last_error = msg;
+  return s;
+}
+
+#define BD_TRY(expr)                                       \
+  do {                                                     \
+    std::string _e = (expr);                               \
+    if (!_e.empty()) return fail(BD_ERR_CUDA, _e);         \
+  } while (0)
+
+constexpr int kMaxB = 8;
+constexpr int kMaxMasks = 15;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int elem_bytes(const bd_config *c) { return c->dtype == BD_BF16 ? 2 : 4; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sms_for_sizing() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();
+  return 256;  // conservative when no device is visible
+}
+
+// ------------------------------------------------------------------ validation
+std::string check_config(const bd_config *c) {
+  char b[256];
+  if (!c) return "config is NULL";
+  if (c->dtype != BD_BF16 && c->dtype != BD_F32) return "dtype must be BD_BF16 or BD_F32";
+  const int e = elem_bytes(c);
+  auto k_ok = [&](long long k) { return k > 0 && (k * e) % 16 == 0; };
+  if (c->hidden <= 0 || !k_ok(c->hidden)) return "hidden must be > 0 and hidden*elem a multiple of 16 bytes";
+  if (c->n_layers < 1 || c->n_layers > BD_MAX_LAYERS) return "n_layers out of range 1..16";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  if (c->n_kv_heads <= 0 || c->n_q_heads <= 0 || c->n_q_heads % c->n_kv_heads != 0)
+    return "n_q_heads must be a positive multiple of n_kv_heads";
+  if (c->ffn <= 0 || !k_ok(c->ffn)) return "ffn must be > 0 and ffn*elem a multiple of 16 bytes";
+  if (c->vocab <= 0) return "vocab must be > 0";
+  if (c->n_target_layers <= 0) return "n_target_layers must be > 0";
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return "mask_token_id outside [0, vocab)";
+  if (c->block_mask != BD_BLOCK_BIDIRECTIONAL && c->block_mask != BD_BLOCK_CAUSAL)
+    return "block_mask must be 0 or 1";
+  if (!(c->eps > 0.f) || !(c->rope_theta > 1.f)) return "eps must be > 0 and rope_theta > 1";
+  if (c->code_width < 0 || c->msg_width < 0) return "code/message widths must be >= 0";
+  if ((c->code_width > 0) != (c->msg_width > 0)) return "code_width and msg_width must both be 0 or both > 0";
+  if (c->code_width > 0 && (!k_ok(c->code_width) || !k_ok(c->msg_width)))
+    return "code_width*elem and msg_width*elem must be multiples of 16 bytes";
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->window[l] < 0) return "window must be >= 0";
+    if (c->ring_capacity[l] <= 0) return "ring_capacity must be > 0";
+    if (c->window[l] > 0 && c->ring_capacity[l] < c->window[l] - 1) {
+      snprintf(b, sizeof b, "layer %d: ring_capacity %d cannot hold the %d-position window", l,
+               c->ring_capacity[l], c->window[l] - 1);
+      return b;
+    }
+  }
+  return {};
+}
+
+std::string check_weights(const bd_config *c, const bd_weights *w) {
+  if (!w) return "weights are NULL";
+  auto chk = [](const void *p) { return p != nullptr && aligned16(p); };
+  if (!chk(w->w_feature) || !chk(w->context_norm) || !chk(w->final_norm) || !chk(w->embed_head))
+    return "a shared weight pointer is NULL or not 16-byte aligned";
+  if (c->code_width > 0) {
+    if (!chk(w->codebook) || !chk(w->g_recv) || !chk(w->g_pred) || !chk(w->a_val))
+      return "bridge weights (codebook, g_recv, g_pred, a_val) are NULL or misaligned";
+    if (w->gate_bias && !aligned16(w->gate_bias)) return "gate_bias is not 16-byte aligned";
+  }
+  for (int l = 0; l < c->n_layers; ++l) {
+    const bd_layer_weights &L = w->layer[l];
+    if (!chk(L.in_norm) || !chk(L.wq) || !chk(L.wk) || !chk(L.wv) || !chk(L.q_norm) ||
+        !chk(L.k_norm) || !chk(L.wo) || !chk(L.post_norm) || !chk(L.w_gate) || !chk(L.w_up) ||
+        !chk(L.w_down))
+      return "layer " + std::to_string(l) + ": a weight pointer is NULL or not 16-byte aligned";
+    if (c->code_width > 0 && (!chk(L.r_read) || !chk(L.w_write)))
+      return "layer " + std::to_string(l) + ": r_read / w_write NULL or misaligned";
+  }
+  return {};
+}
+
+std::string check_kv(const bd_config *c, const bd_kv_cache *kv, int B) {
+  if (!kv) return "kv cache is NULL";
+  if (kv->b_max < B || kv->b_max < 1) return "kv->b_max smaller than the number of requests";
+  for (int l = 0; l < c->n_layers; ++l)
+    if (!kv->k[l] || !kv->v[l] || !aligned16(kv->k[l]) || !aligned16(kv->v[l]))
+      return "kv ring pointer NULL or misaligned";
+  return {};
+}
+
+RopeFreq rope_freq(const bd_config *c) {
+  RopeFreq f;
+  memset(&f, 0, sizeof f);
+  const int half = c->head_dim / 2;
+  for (int j = 0; j < half; ++j)
+    f.inv[j] = std::pow(static_cast<double>(c->rope_theta), -2.0 * j / c->head_dim);
+  return f;
+}
+
+// ------------------------------------------------------------------ workspace planning
+struct Carve {
+  size_t off = 0;
+  char *base = nullptr;
+  template <typename T> T *take(size_t count) {
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off = align_up(off + count * sizeof(T));
+    return p;
+  }
+};
+
+int att_splits(const bd_config *c, int l, int B, int W, int sms) {
+  const int cap = c->ring_capacity[l];
+  const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
+  const int max_keys = ctx + W;
+  const int max_splits = (max_keys + 63) / 64;
+  int s = (2 * sms + B * c->n_kv_heads - 1) / (B * c->n_kv_heads);
+  if (s < 1) s = 1;
+  return s < max_splits ? s : max_splits;
+}
+int att_max_keys(const bd_config *c, int l, int W) {
+  const int cap = c->ring_capacity[l];
+  const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
+  return ctx + W;
+}
+
+// Shared scratch of every GEMM launch of one entry-point call.
+struct GemmWs {
+  float *partials;
+  size_t partial_floats;
+  unsigned *counters;
+  size_t n_counters;
+};
+void carve_gemm(Carve &cv, GemmWs &g, int max_block_n, size_t max_tiles, int sms) {
+  g.partial_floats = gemm_partial_floats(sms, max_block_n);
+  g.partials = cv.take<float>(g.partial_floats);
+  g.n_counters = max_tiles;
+  g.counters = cv.take<unsigned>(max_tiles);
+}
+
+size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + tile_rows - 1) / tile_rows); }
+
+struct RoundWs {
+  GemmWs g;
+  float *x, *z, *pre, *r, *part_o;
+  float2 *rope, *part_ml;
+  void *xn, *q, *kblk, *vblk, *att, *hmid, *c, *m;
+};
+size_t round_max_tiles(const bd_config *c, int T) {
+  const int ntn = (T + gemm_block_n(T) - 1) / gemm_block_n(T);
+  size_t t = tiles_of(c->n_q_heads * c->head_dim, 128) + 2 * tiles_of(c->n_kv_heads * c->head_dim, 128);
+  t = std::max(t, tiles_of(c->hidden, 128));
+  t = std::max(t, tiles_of(c->ffn, 64));
+  if (c->code_width > 0) {
+    t = std::max(t, tiles_of(c->code_width, 128));
+    t = std::max(t, 3 * tiles_of(c->msg_width, 128));
+  }
+  return t * ntn;
+}
+void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sms) {
+  const int T = B * W;
+  const int e = elem_bytes(c);
+  const int H = c->hidden, QD = c->n_q_heads * c->head_dim, KD = c->n_kv_heads * c->head_dim;
+  carve_gemm(cv, w.g, gemm_block_n(T), round_max_tiles(c, T), sms);
+  w.x = cv.take<float>(static_cast<size_t>(T) * H);
+  w.xn = cv.take<char>(static_cast<size_t>(T) * H * e);
+  w.q = cv.take<char>(static_cast<size_t>(T) * QD * e);
+  w.kblk = cv.take<char>(static_cast<size_t>(T) * KD * e);
+  w.vblk = cv.take<char>(static_cast<size_t>(T) * KD * e);
+  w.att = cv.take<char>(static_cast<size_t>(T) * QD * e);
+  w.hmid = cv.take<char>(static_cast<size_t>(T) * c->ffn * e);
+  w.rope = cv.take<float2>(static_cast<size_t>(T) * (c->head_dim / 2));
+  size_t po = 0, pm = 0;
+  for (int l = 0; l < c->n_layers; ++l) {
+    const int s = att_splits(c, l, B, W, sms);
+    po = std::max(po, attention_partial_floats(B, c->n_kv_heads, s, c->head_dim));
+    pm = std::max(pm, attention_ml_count(B, c->n_kv_heads, s));
+  }
+  w.part_o = cv.take<float>(po);
+  w.part_ml = cv.take<float2>(pm);
+  if (c->code_width > 0) {
+    w.r = cv.take<float>(T);
+    w.z = cv.take<float>(static_cast<size_t>(T) * c->code_width);
+    w.c = cv.take<char>(static_cast<size_t>(T) * c->code_width * e);
+    w.pre = cv.take<float>(static_cast<size_t>(T) * 3 * c->msg_width);
+    w.m = cv.take<char>(static_cast<size_t>(T) * c->msg_width * e);
+  } else {
+    w.r = w.z = w.pre = nullptr;
+    w.c = w.m = nullptr;
+  }
+}
+
+struct MatWs {
+  GemmWs g;
+  float *feat;
+  void *cmat;
+  float2 *rope;
+};
+size_t mat_max_tiles(const bd_config *c, int n) {
+  const int bn = gemm_block_n(n);
+  const size_t ntn = static_cast<size_t>((n + bn - 1) / bn);
+  const size_t kv_tiles = static_cast<size_t>(std::min(c->n_layers, kMaxSegs / 2)) * 2 *
+                          tiles_of(c->n_kv_heads * c->head_dim, 128);
+  return std::max(tiles_of(c->hidden, 128), kv_tiles) * ntn;
+}
+void carve_mat(Carve &cv, MatWs &w, const bd_config *c, int n, int sms) {
+  carve_gemm(cv, w.g, gemm_block_n(n), mat_max_tiles(c, n), sms);
+  w.feat = cv.take<float>(static_cast<size_t>(n) * c->hidden);
+  w.cmat = cv.take<char>(static_cast<size_t>(n) * c->hidden * elem_bytes(c));
+  w.rope = cv.take<float2>(static_cast<size_t>(n) * (c->head_dim / 2));
+}
+
+struct HeadWs {
+  GemmWs g;
+  float *amax_val;
+  int32_t *amax_idx;
+};
+void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
+  const size_t m_tiles = tiles_of(c->vocab, 128);
+  const int bn = gemm_block_n(rows);
+  carve_gemm(cv, w.g, bn, m_tiles * ((rows + bn - 1) / bn), sms);
+  w.amax_val = cv.take<float>(m_tiles * rows);
+  w.amax_idx = cv.take<int32_t>(m_tiles * rows);
+}
+
+GemmScratch scratch_of(const GemmWs &g) {
+  return GemmScratch{g.partials, g.partial_floats, g.counters, g.n_counters};
+}
+
+std::string memset_counters(const GemmWs &g, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(g.counters, 0, g.n_counters * sizeof(unsigned), s);
+  return e == cudaSuccess ? std::string() : std::string("memset: ") + cudaGetErrorString(e);
+}
+
+GemmPlan make_plan(const bd_config *c, const void *x, int n_tok, int K) {
+  GemmPlan p;
+  memset(&p, 0, sizeof p);
+  p.dtype = c->dtype == BD_BF16 ? 0 : 1;
+  p.x = x;
+  p.n_tokens = n_tok;
+  p.K = K;
+  p.args.eps = c->eps;
+  p.args.head_dim = c->head_dim;
+  p.args.n_kv_heads = c->n_kv_heads;
+  p.args.vocab = c->vocab;
+  return p;
+}
+void add_w(GemmPlan &p, const void *ptr, int rows) {
+  p.w[p.n_w].ptr = ptr;
+  p.w[p.n_w].rows = rows;
+  ++p.n_w;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int bd_abi_version(void) { return BD_ABI_VERSION; }
+
+const char *bd_last_error(void) { return t_last_error.c_str(); }
+
+size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int max_ctx_rows) {
+  if (!check_config(cfg).empty()) return 0;
+  if (b_max < 1 || b_max > kMaxB || max_masks < 1 || max_masks > kMaxMasks || max_ctx_rows < 1)
+    return 0;
+  const int sms = sms_for_sizing();
+  size_t need = 0;
+  for (int B = 1; B <= b_max; ++B) {
+    Carve cv;
+    RoundWs w;
+    carve_round(cv, w, cfg, B, max_masks + 1, sms);
+    need = std::max(need, cv.off);
+    Carve ch;
+    HeadWs hw;
+    carve_head(ch, hw, cfg, B * max_masks, sms);
+    need = std::max(need, ch.off);
+  }
+  Carve cm;
+  MatWs mw;
+  carve_mat(cm, mw, cfg, max_ctx_rows, sms);
+  need = std::max(need, cm.off);
+  return need;
+}
+
+bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
+                                const void *target_feats, const int32_t *row_request,
+                                const int64_t *row_pos, const int64_t *ctx_frontier, int n_rows,
+                                void *workspace, size_t workspace_bytes, void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if ((e = check_weights(cfg, w)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if ((e = check_kv(cfg, kv, 1)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if (n_rows < 1) return fail(BD_ERR_INVALID_ARG, "n_rows must be >= 1");
+  if (!target_feats || !aligned16(target_feats)) return fail(BD_ERR_INVALID_ARG, "target_feats NULL or misaligned");
+  if (!row_request || !row_pos || !ctx_frontier) return fail(BD_ERR_INVALID_ARG, "row_request/row_pos/ctx_frontier NULL");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const int sms = num_sms();
+  Carve cv;
+  cv.base = static_cast<char *>(workspace);
+  MatWs mw;
+  carve_mat(cv, mw, cfg, n_rows, sms);
+  if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for materialisation");
+  const int H = cfg->hidden, D = cfg->head_dim, KD = cfg->n_kv_heads * D;
+  const RopeFreq freq = rope_freq(cfg);
+  const GemmScratch sc = scratch_of(mw.g);
+
+  BD_TRY(memset_counters(mw.g, s));
+  BD_TRY(launch_rope_table(row_pos, n_rows, mw.rope, D / 2, freq, s));
+  {  // S1: W_feature s_t (fp32 out), then plain_rmsnorm with context_norm
+    GemmPlan p = make_plan(cfg, target_feats, n_rows, cfg->n_target_layers * H);
+    add_w(p, w->w_feature, H);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = mw.feat;
+    p.args.ld_out = H;
+    BD_TRY(launch_gemm(p, sc, s));
+    BD_TRY(launch_rownorm(cfg->dtype, mw.feat, n_rows, H, w->context_norm, cfg->eps, NORM_PLAIN,
+                          mw.cmat, nullptr, nullptr, nullptr, 1, s));
+  }
+  // S2: every layer's context K (head norm + RoPE) and V, scattered into the rings
+  for (int l0 = 0; l0 < cfg->n_layers; l0 += kMaxSegs / 2) {
+    const int l1 = std::min(cfg->n_layers, l0 + kMaxSegs / 2);
+    GemmPlan p = make_plan(cfg, mw.cmat, n_rows, H);
+    p.args.epi = EPI_HEADS;
+    p.args.rope = mw.rope;
+    p.args.row_req = row_request;
+    p.args.row_pos = row_pos;
+    p.args.frontier = ctx_frontier;
+    p.args.n_req = kv->b_max;
+    for (int l = l0; l < l1; ++l) {
+      const int sk = p.n_w;
+      add_w(p, w->layer[l].wk, KD);
+      add_w(p, w->layer[l].wv, KD);
+      p.args.seg[sk] = GemmSeg{};
+      p.args.seg[sk].kind = HK_K;
+      p.args.seg[sk].norm = w->layer[l].k_norm;
+      p.args.seg[sk].dst = kv->k[l];
+      p.args.seg[sk].dst_mode = HD_RING;
+      p.args.seg[sk].cap = cfg->ring_capacity[l];
+      p.args.seg[sk + 1] = p.args.seg[sk];
+      p.args.seg[sk + 1].kind = HK_V;
+      p.args.seg[sk + 1].norm = nullptr;
+      p.args.seg[sk + 1].dst = kv->v[l];
+    }
+    BD_TRY(launch_gemm(p, sc, s));
+  }
+  return BD_OK;
+}
+
+bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
+                         const int32_t *anchor_ids, const int64_t *frontier, int B, int n_masks,
+                         void *head_in, float *hidden_out, float *layers_out, void *workspace,
+                         size_t workspace_bytes, void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if (B < 1 || B > kMaxB) return fail(BD_ERR_INVALID_ARG, "B must be in 1..8");
+  if (n_masks < 1 || n_masks > kMaxMasks) return fail(BD_ERR_INVALID_ARG, "n_masks must be in 1..15");
+  if ((e = check_weights(cfg, w)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if ((e = check_kv(cfg, kv, B)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if (!anchor_ids || !frontier) return fail(BD_ERR_INVALID_ARG, "anchor_ids/frontier NULL");
+  if (!head_in || !aligned16(head_in)) return fail(BD_ERR_INVALID_ARG, "head_in NULL or misaligned");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  const int W = n_masks + 1, T = B * W;
+  const int G = cfg->n_q_heads / cfg->n_kv_heads;
+  if (cfg->dtype == BD_BF16 && G * W > attention_rows_max())
+    return fail(BD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*(n_masks+1) must be <= 64");
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (cfg->dtype == BD_F32 && att_max_keys(cfg, l, W) > 48 * 1024)
+      return fail(BD_ERR_UNSUPPORTED, "fp32 attention supports at most 49152 keys per layer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const int sms = num_sms();
+  Carve cv;
+  cv.base = static_cast<char *>(workspace);
+  RoundWs rw;
+  carve_round(cv, rw, cfg, B, W, sms);
+  if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for this round");
+
+  const int H = cfg->hidden, D = cfg->head_dim;
+  const int QD = cfg->n_q_heads * D, KD = cfg->n_kv_heads * D;
+  const RopeFreq freq = rope_freq(cfg);
+  const GemmScratch sc = scratch_of(rw.g);
+  const int dt = cfg->dtype;
+
+  BD_TRY(memset_counters(rw.g, s));
+  // S3: block input rows and the RoPE table of positions F_b + i
+  BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
+                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, s));
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const bd_layer_weights &L = w->layer[l];
+    // S4: n = rmsnorm(x); q, k, v with head norm + RoPE
+    BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
+                          nullptr, nullptr, W, s));
+    {
+      GemmPlan p = make_plan(cfg, rw.xn, T, H);
+      add_w(p, L.wq, QD);
+      add_w(p, L.wk, KD);
+      add_w(p, L.wv, KD);
+      p.args.epi = EPI_HEADS;
+      p.args.rope = rw.rope;
+      p.args.block_w = W;
+      p.args.seg[0].kind = HK_Q;
+      p.args.seg[0].norm = L.q_norm;
+      p.args.seg[0].dst = rw.q;
+      p.args.seg[0].dst_mode = HD_TOKEN_MAJOR;
+      p.args.seg[0].ld = QD;
+      p.args.seg[1].kind = HK_K;
+      p.args.seg[1].norm = L.k_norm;
+      p.args.seg[1].dst = rw.kblk;
+      p.args.seg[1].dst_mode = HD_BLOCK;
+      p.args.seg[2].kind = HK_V;
+      p.args.seg[2].dst = rw.vblk;
+      p.args.seg[2].dst_mode = HD_BLOCK;
+      BD_TRY(launch_gemm(p, sc, s));
+    }
+    // S5: block attention over the ring context and the block
+    {
+      AttArgs a;
+      memset(&a, 0, sizeof a);
+      a.q = rw.q;
+      a.ring_k = kv->k[l];
+      a.ring_v = kv->v[l];
+      a.blk_k = rw.kblk;
+      a.blk_v = rw.vblk;
+      a.out = rw.att;
+      a.frontier = frontier;
+      a.part_o = rw.part_o;
+      a.part_ml = rw.part_ml;
+      a.B = B;
+      a.W = W;
+      a.n_q_heads = cfg->n_q_heads;
+      a.n_kv_heads = cfg->n_kv_heads;
+      a.head_dim = D;
+      a.window = cfg->window[l];
+      a.cap = cfg->ring_capacity[l];
+      a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
+      a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
+      a.max_keys = att_max_keys(cfg, l, W);
+      BD_TRY(launch_attention(a, dt, s));
+    }
+    // S6: y = x + W_o a (in place)
+    {
+      GemmPlan p = make_plan(cfg, rw.att, T, QD);
+      add_w(p, L.wo, H);
+      p.args.epi = EPI_RESID_F32;
+      p.args.out_f32 = rw.x;
+      p.args.ld_out = H;
+      p.args.resid = rw.x;
+      p.args.ld_resid = H;
+      BD_TRY(launch_gemm(p, sc, s));
+    }
+    // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m)
+    BD_TRY(launch_rownorm(dt, rw.x, T, H, L.post_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
+                          nullptr, nullptr, W, s));
+    {
+      GemmPlan p = make_plan(cfg, rw.xn, T, H);
+      add_w(p, L.w_gate, cfg->ffn);
+      add_w(p, L.w_up, cfg->ffn);
+      p.pair_mode = true;
+      p.args.epi = EPI_SWIGLU;
+      p.args.out_act = rw.hmid;
+      p.args.ld_act = cfg->ffn;
+      BD_TRY(launch_gemm(p, sc, s));
+    }
+    {
+      GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
+      add_w(p, L.w_down, H);
+      p.args.epi = EPI_RESID_F32;
+      p.args.out_f32 = rw.x;
+      p.args.ld_out = H;
+      p.args.resid = rw.x;
+      p.args.ld_resid = H;
+      BD_TRY(launch_gemm(p, sc, s));
+    }
+    if (cfg->code_width > 0) {
+      const int Rc = cfg->code_width, Mc = cfg->msg_width;
+      // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
+      BD_TRY(launch_rownorm(dt, rw.x, T, H, nullptr, cfg->eps, NORM_BRIDGE, rw.xn, rw.r, nullptr,
+                            nullptr, W, s));
+      {
+        GemmPlan p = make_plan(cfg, rw.xn, T, H);
+        add_w(p, L.r_read, Rc);
+        p.args.epi = EPI_STORE_F32;
+        p.args.out_f32 = rw.z;
+        p.args.ld_out = Rc;
+        BD_TRY(launch_gemm(p, sc, s));
+      }
+      BD_TRY(launch_code(dt, rw.z, T, Rc, w->codebook, anchor_ids, cfg->vocab, W, cfg->eps, rw.c, s));
+      // S9: [G c; G_p c; A c] in one launch, gate/message, then the RMS-scaled write
+      {
+        GemmPlan p = make_plan(cfg, rw.c, T, Rc);
+        add_w(p, w->g_recv, Mc);
+        add_w(p, w->g_pred, Mc);
+        add_w(p, w->a_val, Mc);
+        p.args.epi = EPI_STORE_F32;
+        p.args.out_f32 = rw.pre;
+        p.args.ld_out = 3 * Mc;
+        p.args.seg[0].out_col = 0;
+        p.args.seg[1].out_col = Mc;
+        p.args.seg[2].out_col = 2 * Mc;
+        BD_TRY(launch_gemm(p, sc, s));
+      }
+      BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, s));
+      {
+        GemmPlan p = make_plan(cfg, rw.m, T, Mc);
+        add_w(p, L.w_write, H);
+        p.args.epi = EPI_INJECT;
+        p.args.out_f32 = rw.x;
+        p.args.ld_out = H;
+        p.args.row_scale = rw.r;
+        p.args.block_w = W;
+        BD_TRY(launch_gemm(p, sc, s));
+      }
+    }
+    if (layers_out)
+      BD_TRY(launch_copy_f32(rw.x, layers_out + static_cast<size_t>(l) * T * H,
+                             static_cast<size_t>(T) * H, s));
+  }
+  BD_TRY(launch_rownorm(dt, rw.x, T, H, w->final_norm, cfg->eps, NORM_FINAL, nullptr, nullptr,
+                        hidden_out, head_in, W, s));
+  return BD_OK;
+}
+
+bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const void *hidden, int rows,
+                            int32_t *token_out, float *max_logit_out, void *workspace,
+                            size_t workspace_bytes, void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if (!w || !w->embed_head || !aligned16(w->embed_head))
+    return fail(BD_ERR_INVALID_ARG, "embed_head NULL or misaligned");
+  if (rows < 1 || rows > kMaxB * kMaxMasks) return fail(BD_ERR_INVALID_ARG, "rows must be in 1..120");
+  if (!hidden || !aligned16(hidden)) return fail(BD_ERR_INVALID_ARG, "hidden NULL or misaligned");
+  if (!token_out) return fail(BD_ERR_INVALID_ARG, "token_out NULL");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  Carve cv;
+  cv.base = static_cast<char *>(workspace);
+  HeadWs hw;
+  carve_head(cv, hw, cfg, rows, num_sms());
+  if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
+  BD_TRY(memset_counters(hw.g, s));
+  GemmPlan p = make_plan(cfg, hidden, rows, cfg->hidden);
+  add_w(p, w->embed_head, cfg->vocab);
+  p.args.epi = EPI_ARGMAX;
+  p.args.amax_val = hw.amax_val;
+  p.args.amax_idx = hw.amax_idx;
+  BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
+  BD_TRY(launch_argmax_reduce(hw.amax_val, hw.amax_idx, static_cast<int>(tiles_of(cfg->vocab, 128)),
+                              rows, token_out, max_logit_out, s));
+  return BD_OK;
+}
+
+bd_status bd_sync_status(void *stream_) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
+  if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
+  const unsigned word = take_error_word_gemm() | take_error_word_att() | take_error_word_small();
+  if (word & DEVERR_TIMEOUT) return fail(BD_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
+  if (word & DEVERR_BAD_INDEX)
+    return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");
+  return BD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,696 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   D[tok, row] = sum_k X[tok, k] * W[row, k]
+//
+// Swap-AB: a 128-row weight tile is the MMA's A operand (M = 128), the token rows of the
+// drafter block are the B operand (N = block_n <= 256, a multiple of 16).  Both operands
+// are K-major tiles that TMA writes into shared memory with 128-byte swizzling; the fp32
+// accumulator lives in tensor memory and is read back by four epilogue warps.
+//
+// Work split (stream-K): the (tile, k-block) units of all segments are cut into n_ctas
+// contiguous ranges of equal length, so every SM streams the same number of weight bytes
+// whatever the matrix shapes.  A tile split between CTAs is finished by the CTA that
+// arrives last on the tile's counter; it adds the other CTAs' partial tiles in CTA
+// order, so results do not depend on arrival order.  No CTA ever waits on another.
+//
+// Warp roles: warp 0 = TMA producer (one lane), warp 1 = TMEM owner and MMA issuer (one
+// lane), warps 2-5 = epilogue (128 threads, one accumulator row each).
+#include "bd_device.cuh"
+#include "bd_internal.h"
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+namespace bd {
+
+BD_DEFINE_ERROR_TAKER(take_error_word_gemm)
+
+template <typename T> struct MmaTraits;
+template <> struct MmaTraits<__nv_bfloat16> {
+  static constexpr int BK = 64;   // k elements per 128-byte smem row
+  static constexpr int UK = 16;   // k per tcgen05.mma (kind::f16)
+  static constexpr uint32_t fmt = 1;
+};
+template <> struct MmaTraits<float> {
+  static constexpr int BK = 32;
+  static constexpr int UK = 8;    // kind::tf32
+  static constexpr uint32_t fmt = 2;
+};
+
+constexpr int kATileBytes = kBM * 128;  // 16 KB: 128 rows x 128 bytes
+constexpr int kXStride = 17;            // epilogue exchange row stride (floats)
+constexpr int kMaxStages = 12;
+constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
+
+struct SmemLayout {
+  size_t off_b, off_x, off_red, off_bar, total;
+};
+__host__ __device__ inline SmemLayout smem_layout(int stages, int block_n) {
+  SmemLayout L;
+  L.off_b = static_cast<size_t>(stages) * kATileBytes;
+  L.off_x = L.off_b + static_cast<size_t>(stages) * block_n * 128;
+  L.off_red = L.off_x + kBM * kXStride * 4;
+  L.off_bar = L.off_red + 2 * 64 * 4;
+  L.total = L.off_bar + (2 * stages + 4) * 8 + 16 + 1024;  // + alignment slack
+  return L;
+}
+
+// Walks the (tile, k-block range) segments of one CTA's stream-K unit range.
+struct SegWalk {
+  long long u, u1;
+  int kb;
+  __device__ bool next(int &tile, int &kb0, int &kb1) {
+    if (u >= u1) return false;
+    tile = static_cast<int>(u / kb);
+    kb0 = static_cast<int>(u % kb);
+    const long long rem = u1 - u;
+    kb1 = static_cast<int>(rem < (kb - kb0) ? kb0 + rem : kb);
+    u += kb1 - kb0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ long long unit_begin(long long U, int P, int c) {
+  return static_cast<long long>(c) * U / P;
+}
+// CTA whose unit range contains unit u.
+__device__ __forceinline__ int cta_of_unit(long long U, int P, long long u) {
+  return static_cast<int>(((u + 1) * P - 1) / U);
+}
+
+__device__ __forceinline__ int seg_of_tile(const GemmArgs &p, int m_tile) {
+  int s = 0;
+#pragma unroll 1
+  for (int i = 1; i < p.n_segs; ++i)
+    if (m_tile >= p.seg[i].tile_begin) s = i;
+  return s;
+}
+
+// ------------------------------------------------------------------ producer
+template <typename T>
+__device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *sA,
+                              uint8_t *sB, uint64_t *full, uint64_t *empty, long long u0,
+                              long long u1, volatile int *sabort) {
+  constexpr int BK = MmaTraits<T>::BK;
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_x = policy_evict_last();
+  const int S = p.stages;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.block_n) * 128u;
+  const uint32_t stage_bytes = kATileBytes + b_bytes;
+
+  auto load_a = [&](int m_tile, int kbi, uint8_t *dst, uint64_t *bar) {
+    if (p.pair_mode) {
+      tma_load_2d(dst, &maps.a[0], bar, kbi * BK, m_tile * 64, pol_w);
+      tma_load_2d(dst + 64 * 128, &maps.a[1], bar, kbi * BK, m_tile * 64, pol_w);
+    } else {
+      const int s = seg_of_tile(p, m_tile);
+      tma_load_2d(dst, &maps.a[s], bar, kbi * BK, (m_tile - p.seg[s].tile_begin) * kBM, pol_w);
+    }
+  };
+
+  // The weight tiles do not depend on the previous kernel: start streaming them before
+  // waiting for it (programmatic dependent launch).
+  const long long total = u1 - u0;
+  const int pre = static_cast<int>(total < S ? total : S);
+  {
+    SegWalk w{u0, u1, p.kb};
+    int tile, kb0, kb1, q = 0;
+    while (q < pre && w.next(tile, kb0, kb1)) {
+      const int m_tile = tile / p.n_tiles_n;
+      for (int kbi = kb0; kbi < kb1 && q < pre; ++kbi, ++q) {
+        mbar_arrive_expect_tx(&full[q], stage_bytes);
+        load_a(m_tile, kbi, sA + static_cast<size_t>(q) * kATileBytes, &full[q]);
+      }
+    }
+  }
+  pdl_wait();
+  SegWalk w{u0, u1, p.kb};
+  int tile, kb0, kb1;
+  long long q = 0;
+  while (w.next(tile, kb0, kb1)) {
+    const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
+    for (int kbi = kb0; kbi < kb1; ++kbi, ++q) {
+      const int s = static_cast<int>(q % S);
+      const uint32_t round = static_cast<uint32_t>(q / S);
+      if (q >= pre) {
+        if (*sabort || !mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
+          *sabort = 1;
+          return;
+        }
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        load_a(m_tile, kbi, sA + static_cast<size_t>(s) * kATileBytes, &full[s]);
+      }
+      tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &maps.b, &full[s], kbi * BK,
+                  n_tile * p.block_n, pol_x);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <typename T>
+__device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
+                         uint64_t *empty, uint64_t *accf, uint64_t *acce, uint32_t tmem_base,
+                         long long u0, long long u1, volatile int *sabort) {
+  constexpr int BK = MmaTraits<T>::BK, UK = MmaTraits<T>::UK;
+  const uint32_t idesc = umma_idesc(MmaTraits<T>::fmt, kBM, p.block_n);
+  const int S = p.stages;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.block_n) * 128u;
+  SegWalk w{u0, u1, p.kb};
+  int tile, kb0, kb1, e = 0;
+  long long q = 0;
+  while (w.next(tile, kb0, kb1)) {
+    const int a = e & 1;
+    const uint32_t ra = static_cast<uint32_t>(e >> 1);
+    if (*sabort || !mbar_wait(&acce[a], (ra & 1u) ^ 1u)) {
+      *sabort = 1;
+      return;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem_base + static_cast<uint32_t>(a * p.block_n);
+    for (int kbi = kb0; kbi < kb1; ++kbi, ++q) {
+      const int s = static_cast<int>(q % S);
+      if (*sabort || !mbar_wait(&full[s], static_cast<uint32_t>(q / S) & 1u)) {
+        *sabort = 1;
+        return;
+      }
+      tc_fence_after();
+      const uint32_t abase = smem_u32(sA + static_cast<size_t>(s) * kATileBytes);
+      const uint32_t bbase = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+#pragma unroll
+      for (int k = 0; k < BK / UK; ++k) {
+        const uint64_t ad = umma_desc_sw128(abase + k * 32);
+        const uint64_t bd = umma_desc_sw128(bbase + k * 32);
+        const uint32_t acc = (kbi > kb0 || k > 0) ? 1u : 0u;
+        if constexpr (MmaTraits<T>::fmt == 1)
+          umma_bf16(d, ad, bd, idesc, acc);
+        else
+          umma_tf32(d, ad, bd, idesc, acc);
+      }
+      umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+    }
+    umma_commit(&accf[a]);     // accumulator ready for the epilogue
+    ++e;
+  }
+}
+
+// ------------------------------------------------------------------ epilogue ops
+// Each op gets the fp32 values v[0..15] of tile row r (0..127) for token columns
+// tok0 .. tok0+15 and must call the same named barriers on all 128 threads.
+template <typename T>
+__device__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0, float (&v)[16],
+                          float *xbuf, float *red, int32_t *redi) {
+  const int q = r >> 5;
+  const int lane = r & 31;
+  switch (p.epi) {
+    case EPI_STORE_F32:
+    case EPI_RESID_F32:
+    case EPI_INJECT: {
+      const int s = seg_of_tile(p, m_tile);
+      const int row = (m_tile - p.seg[s].tile_begin) * kBM + r;
+      if (row >= p.seg[s].rows) break;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int tok = tok0 + jj;
+        if (tok >= p.n_tokens) break;
+        const size_t o = static_cast<size_t>(tok) * p.ld_out + row;
+        if (p.epi == EPI_STORE_F32) {
+          p.out_f32[o + p.seg[s].out_col] = v[jj];
+        } else if (p.epi == EPI_RESID_F32) {
+          p.out_f32[o] = p.resid[static_cast<size_t>(tok) * p.ld_resid + row] + v[jj];
+        } else if (tok % p.block_w != 0) {
+          p.out_f32[o] += p.row_scale[tok] * v[jj];
+        }
+      }
+      break;
+    }
+    case EPI_SWIGLU: {
+      // rows 0..63: gate features f, rows 64..127: up features f (same f)
+      if (r >= 64) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) xbuf[(r - 64) * kXStride + jj] = v[jj];
+      }
+      named_bar(2, 128);
+      if (r < 64) {
+        const int f = m_tile * 64 + r;
+        if (f < p.seg[0].rows) {
+          T *out = static_cast<T *>(p.out_act);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int tok = tok0 + jj;
+            if (tok >= p.n_tokens) break;
+            const float g = v[jj];
+            const float u = xbuf[r * kXStride + jj];
+            const float h = g / (1.0f + __expf(-g)) * u;
+            out[static_cast<size_t>(tok) * p.ld_act + f] = from_f<T>(h);
+          }
+        }
+      }
+      named_bar(2, 128);
+      break;
+    }
+    case EPI_HEADS: {
+      const int s = seg_of_tile(p, m_tile);
+      const GemmSeg &sg = p.seg[s];
+      const int D = p.head_dim;
+      const int row = (m_tile - sg.tile_begin) * kBM + r;
+      const int d = r % D;
+      const int head = row / D;
+      const bool normed = sg.kind != HK_V;
+      if (normed) {
+        // per-head RMSNorm over the D rows of the head, for each token column
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float ss = warp_sum(v[jj] * v[jj]);
+          if (lane == 0) red[q * 16 + jj] = ss;
+        }
+        named_bar(2, 128);
+        const float gain = to_f<T>(static_cast<const T *>(sg.norm)[d]);
+        const int q0 = (D == 128) ? 0 : (q & 2);
+        const int nq = D / 32;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          float ss = 0.f;
+          for (int k = 0; k < nq; ++k) ss += red[(q0 + k) * 16 + jj];
+          v[jj] = v[jj] * rsqrtf(ss / D + p.eps) * gain;
+          xbuf[r * kXStride + jj] = v[jj];
+        }
+        named_bar(2, 128);
+        // split-half rotation with the partner row of the same head
+        const int half = D / 2;
+        const int pr = d < half ? r + half : r - half;
+        const int j = d % half;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int tok = tok0 + jj;
+          if (tok >= p.n_tokens) break;
+          const float2 cs = p.rope[static_cast<size_t>(tok) * half + j];
+          const float pv = xbuf[pr * kXStride + jj];
+          v[jj] = d < half ? v[jj] * cs.x - pv * cs.y : v[jj] * cs.x + pv * cs.y;
+        }
+        named_bar(2, 128);
+      }
+      if (row >= sg.rows) break;
+      T *dst = static_cast<T *>(sg.dst);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int tok = tok0 + jj;
+        if (tok >= p.n_tokens) break;
+        size_t o;
+        if (sg.dst_mode == HD_TOKEN_MAJOR) {
+          o = static_cast<size_t>(tok) * sg.ld + row;
+        } else if (sg.dst_mode == HD_BLOCK) {
+          const int b = tok / p.block_w, i = tok % p.block_w;
+          o = ((static_cast<size_t>(b) * p.n_kv_heads + head) * p.block_w + i) * D + d;
+        } else {
+          const int req = p.row_req[tok];
+          const long long pos = p.row_pos[tok];
+          if (req < 0 || req >= p.n_req || pos < 0) {
+            atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+            continue;
+          }
+          const long long F = p.frontier[req];
+          if (pos < F - sg.cap || pos >= F) continue;  // outside the final live window
+          o = ((static_cast<size_t>(req) * p.n_kv_heads + head) * sg.cap + pos % sg.cap) * D + d;
+        }
+        dst[o] = from_f<T>(v[jj]);
+      }
+      break;
+    }
+    case EPI_ARGMAX: {
+      const int vid = m_tile * kBM + r;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        float best = vid < p.vocab ? v[jj] : -INFINITY;
+        int bi = vid < p.vocab ? vid : 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > best || (ov == best && oi < bi)) {
+            best = ov;
+            bi = oi;
+          }
+        }
+        if (lane == 0) {
+          red[q * 16 + jj] = best;
+          redi[q * 16 + jj] = bi;
+        }
+      }
+      named_bar(2, 128);
+      if (r < 16) {
+        const int tok = tok0 + r;
+        if (tok < p.n_tokens) {
+          float best = red[r];
+          int bi = redi[r];
+          for (int k = 1; k < 4; ++k) {
+            const float ov = red[k * 16 + r];
+            const int oi = redi[k * 16 + r];
+            if (ov > best || (ov == best && oi < bi)) {
+              best = ov;
+              bi = oi;
+            }
+          }
+          p.amax_val[static_cast<size_t>(m_tile) * p.n_tokens + tok] = best;
+          p.amax_idx[static_cast<size_t>(m_tile) * p.n_tokens + tok] = bi;
+        }
+      }
+      named_bar(2, 128);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// ------------------------------------------------------------------ epilogue
+template <typename T>
+__device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
+                              uint32_t tmem_base, long long u0, long long u1, float *xbuf,
+                              float *red, int32_t *redi, volatile int *sflag,
+                              volatile int *sabort) {
+  const int warp = threadIdx.x >> 5;
+  const int q = warp & 3;             // TMEM lane quarter this warp may access
+  const int r = q * 32 + (threadIdx.x & 31);
+  const int et = threadIdx.x - 64;    // 0..127 among epilogue threads
+  const int cta = blockIdx.x;
+  const long long U = p.units;
+  const int P = p.n_ctas;
+  const int first_tile = static_cast<int>(u0 / p.kb);
+  pdl_wait();
+  SegWalk w{u0, u1, p.kb};
+  int tile, kb0, kb1, e = 0;
+  while (w.next(tile, kb0, kb1)) {
+    const int a = e & 1;
+    const uint32_t ra = static_cast<uint32_t>(e >> 1);
+    ++e;
+    if (*sabort || !mbar_wait(&accf[a], ra & 1u)) {
+      *sabort = 1;
+      return;
+    }
+    tc_fence_after();
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(a * p.block_n);
+    const bool whole = (kb0 == 0 && kb1 == p.kb);
+    const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
+    int c_first = cta, c_last = cta;
+    if (!whole) {
+      const int slot = (tile == first_tile) ? 0 : 1;
+      float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * p.block_n * kBM;
+      for (int j0 = 0; j0 < p.block_n; j0 += 16) {
+        float v[16];
+        tmem_ld16(tbase + j0, v);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) mine[(j0 + jj) * kBM + r] = v[jj];
+      }
+      __threadfence();
+      named_bar(1, 128);
+      c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb);
+      c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1);
+      if (et == 0) {
+        const unsigned n = static_cast<unsigned>(c_last - c_first + 1);
+        const unsigned old = atomicAdd(&p.counters[tile], 1u);
+        const int last = (old == n - 1) ? 1 : 0;
+        if (last) p.counters[tile] = 0;  // ready for the next launch
+        *sflag = last;
+      }
+      named_bar(1, 128);
+      const int last = *sflag;
+      named_bar(1, 128);
+      if (!last) {
+        tc_fence_before();
+        mbar_arrive(&acce[a]);
+        continue;
+      }
+      __threadfence();
+    }
+    for (int j0 = 0; j0 < p.block_n; j0 += 16) {
+      float v[16];
+      tmem_ld16(tbase + j0, v);
+      if (!whole) {
+        float acc[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+        for (int c = c_first; c <= c_last; ++c) {
+          if (c == cta) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) acc[jj] += v[jj];
+          } else {
+            const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
+            const float *o =
+                p.partials + (static_cast<size_t>(c) * 2 + cslot) * p.block_n * kBM;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) acc[jj] += __ldcg(o + (j0 + jj) * kBM + r);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) v[jj] = acc[jj];
+      }
+      epi_chunk<T>(p, m_tile, r, n_tile * p.block_n + j0, v, xbuf, red, redi);
+    }
+    tc_fence_before();
+    mbar_arrive(&acce[a]);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <typename T>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const SmemLayout L = smem_layout(p.stages, p.block_n);
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + L.off_b;
+  float *xbuf = reinterpret_cast<float *>(smem + L.off_x);
+  float *red = reinterpret_cast<float *>(smem + L.off_red);
+  int32_t *redi = reinterpret_cast<int32_t *>(red + 64);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
+  uint64_t *empty = full + p.stages;
+  uint64_t *accf = empty + p.stages;
+  uint64_t *acce = accf + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
+  volatile int *sflag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *sabort = sflag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u0 = unit_begin(p.units, p.n_ctas, blockIdx.x);
+  const long long u1 = unit_begin(p.units, p.n_ctas, blockIdx.x + 1);
+  uint32_t ncols = 32;
+  while (ncols < static_cast<uint32_t>(2 * p.block_n)) ncols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&accf[0], 1);
+    mbar_init(&accf[1], 1);
+    mbar_init(&acce[0], 128);
+    mbar_init(&acce[1], 128);
+    *sabort = 0;
+    *sflag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.b);
+    for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) gemm_producer<T>(maps, p, sA, sB, full, empty, u0, u1, sabort);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) gemm_mma<T>(p, sA, sB, full, empty, accf, acce, tmem_base, u0, u1, sabort);
+    __syncwarp();
+  } else {
+    gemm_epilogue<T>(p, accf, acce, tmem_base, u0, u1, xbuf, red, redi, sflag, sabort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, ncols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void *ptr;
+  int dtype, inner, outer, box_inner, box_outer;
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
+           box_inner == o.box_inner && box_outer == o.box_outer;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey &k) const {
+    size_t h = std::hash<const void *>()(k.ptr);
+    h ^= (static_cast<size_t>(k.inner) * 0x9E3779B97F4A7C15ull) + (h << 6) + (h >> 2);
+    h ^= (static_cast<size_t>(k.outer) * 0xC2B2AE3D27D4EB4Full) + (h << 6) + (h >> 2);
+    h ^= static_cast<size_t>(k.box_outer * 131 + k.box_inner * 7 + k.dtype);
+    return h;
+  }
+};
+
+// Row-major [outer, inner] matrix -> 2-D tiled map, 128-byte swizzle, zero fill OOB.
+static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int inner, int outer,
+                            int box_inner, int box_outer) {
+  static std::mutex mu;
+  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+  const MapKey key{ptr, dtype, inner, outer, box_inner, box_outer};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return {};
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return "cuTensorMapEncodeTiled is unavailable";
+  const int elem = dtype == 0 ? 2 : 4;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = fn(&m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%d x %d] box [%d x %d]",
+             static_cast<int>(r), outer, inner, box_outer, box_inner);
+    return buf;
+  }
+  {
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = m;
+  }
+  *out = m;
+  return {};
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+  }
+  return n;
+}
+
+int gemm_block_n(int n_tokens) {
+  if (n_tokens <= 128) return ((n_tokens + 15) / 16) * 16;
+  return 256;
+}
+
+size_t gemm_partial_floats(int n_ctas, int block_n) {
+  return static_cast<size_t>(n_ctas) * 2 * block_n * kBM;
+}
+
+static int pick_stages(int block_n) {
+  for (int s = kMaxStages; s >= 2; --s)
+    if (smem_layout(s, block_n).total <= kSmemLimit) return s;
+  return 2;
+}
+
+template <typename T>
+static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemLimit));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const size_t smem = smem_layout(a.stages, a.block_n).total;
+  return launch_pdl(gemm_kernel<T>, dim3(a.n_ctas), dim3(kGemmThreads), smem, stream, maps, a);
+}
+
+std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stream) {
+  GemmArgs &a = plan.args;
+  const int BK = plan.dtype == 0 ? 64 : 32;
+  if (plan.n_tokens <= 0 || plan.K <= 0 || plan.n_w <= 0) return "empty GEMM";
+  if (plan.n_w > kMaxSegs) return "too many GEMM segments";
+  a.K = plan.K;
+  a.n_tokens = plan.n_tokens;
+  a.block_n = gemm_block_n(plan.n_tokens);
+  a.n_tiles_n = (plan.n_tokens + a.block_n - 1) / a.block_n;
+  a.pair_mode = plan.pair_mode ? 1 : 0;
+  a.kb = (plan.K + BK - 1) / BK;
+  int m_tiles = 0;
+  if (plan.pair_mode) {
+    if (plan.n_w != 2 || plan.w[0].rows != plan.w[1].rows) return "pair GEMM needs two equal matrices";
+    a.n_segs = 1;
+    a.seg[0].rows = plan.w[0].rows;
+    a.seg[0].tile_begin = 0;
+    m_tiles = (plan.w[0].rows + 63) / 64;
+  } else {
+    a.n_segs = plan.n_w;
+    for (int s = 0; s < plan.n_w; ++s) {
+      a.seg[s].rows = plan.w[s].rows;
+      a.seg[s].tile_begin = m_tiles;
+      m_tiles += (plan.w[s].rows + kBM - 1) / kBM;
+    }
+  }
+  a.m_tiles = m_tiles;
+  const long long tiles = static_cast<long long>(m_tiles) * a.n_tiles_n;
+  a.units = tiles * a.kb;
+  a.n_ctas = static_cast<int>(a.units < num_sms() ? a.units : num_sms());
+  a.stages = pick_stages(a.block_n);
+  a.partials = sc.partials;
+  a.counters = sc.counters;
+  if (gemm_partial_floats(a.n_ctas, a.block_n) > sc.partial_floats) return "GEMM partial scratch too small";
+  if (static_cast<size_t>(tiles) > sc.n_counters) return "GEMM counter scratch too small";
+
+  GemmMaps maps;
+  memset(&maps, 0, sizeof maps);
+  for (int s = 0; s < plan.n_w; ++s) {
+    std::string err = make_map(&maps.a[s], plan.w[s].ptr, plan.dtype, plan.K, plan.w[s].rows, BK,
+                               plan.pair_mode ? 64 : kBM);
+    if (!err.empty()) return err;
+  }
+  std::string err = make_map(&maps.b, plan.x, plan.dtype, plan.K, plan.n_tokens, BK, a.block_n);
+  if (!err.empty()) return err;
+  cudaError_t e = plan.dtype == 0 ? launch_typed<__nv_bfloat16>(maps, a, stream)
+                                  : launch_typed<float>(maps, a, stream);
+  if (e != cudaSuccess) return std::string("GEMM launch: ") + cudaGetErrorString(e);
+  return {};
+}
+
+}  // namespace bd

@@ -1,0 +1,128 @@
+// Internal host/device declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+#include <utility>
+
+namespace bd {
+
+// Device error word flags (set by kernels, read and cleared by bd_sync_status()).
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u };
+
+// ------------------------------------------------------------------ GEMM
+// D[tok, out] = X[tok, :] . W[out, :]  computed swap-AB on tcgen05: weight rows fill the
+// 128-wide MMA M dimension, tokens the N dimension.  One launch streams one or more
+// weight matrices ("segments") that share the activation operand X.
+constexpr int kMaxSegs = 12;
+constexpr int kBM = 128;
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+enum EpiMode : int {
+  EPI_STORE_F32 = 0,  // out[tok*ld + out_col + row] = acc
+  EPI_RESID_F32 = 1,  // out[tok*ld + row] = resid[tok*ld_resid + row] + acc
+  EPI_INJECT = 2,     // x[tok*ld + row] += scale[tok] * acc for non-anchor rows
+  EPI_SWIGLU = 3,     // pair tiles: out[tok*ld_act + f] = SiLU(gate_f) * up_f
+  EPI_HEADS = 4,      // per-head RMSNorm + split-half RoPE (Q/K), plain (V); scatter
+  EPI_ARGMAX = 5      // per-tile (max, lowest argmax) over 128 vocabulary rows
+};
+enum HeadKind : int { HK_Q = 0, HK_K = 1, HK_V = 2 };
+enum HeadDst : int { HD_TOKEN_MAJOR = 0, HD_BLOCK = 1, HD_RING = 2 };
+
+struct GemmSeg {
+  int rows;          // output rows of this weight matrix
+  int tile_begin;    // first m-tile of the segment
+  int out_col;       // EPI_STORE_F32: column offset of this segment in the output row
+  int kind;          // EPI_HEADS: HeadKind
+  int dst_mode;      // EPI_HEADS: HeadDst
+  int ld;            // EPI_HEADS token-major: row stride of dst
+  int cap;           // EPI_HEADS ring: ring capacity
+  int pad_;
+  const void *norm;  // EPI_HEADS: per-head gain [D] (Q/K)
+  void *dst;         // EPI_HEADS: destination base (config dtype)
+};
+
+struct GemmArgs {
+  int K, n_tokens, block_n, n_tiles_n, m_tiles, kb, n_ctas, n_segs, stages, pair_mode;
+  long long units;
+  int epi;
+  int ld_out, ld_resid, ld_act, block_w, head_dim, n_kv_heads, vocab, n_req;
+  float eps;
+  float *out_f32;
+  const float *resid;
+  const float *row_scale;
+  void *out_act;
+  const float2 *rope;             // [n_tokens][D/2] (cos, sin)
+  const int32_t *row_req;         // ring mode: request of each token row
+  const int64_t *row_pos;         // ring mode: absolute position of each token row
+  const int64_t *frontier;        // ring mode: context frontier after the call, per request
+  float *amax_val;                // [m_tiles][n_tokens]
+  int32_t *amax_idx;
+  float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
+  unsigned *counters;             // [m_tiles * n_tiles_n] arrival counters (start at 0)
+  GemmSeg seg[kMaxSegs];
+};
+
+struct GemmMaps {
+  CUtensorMap a[kMaxSegs];  // weight maps (pair mode: a[0] gate, a[1] up, 64-row boxes)
+  CUtensorMap b;            // activation map [n_tokens, K]
+};
+
+// Host description of one GEMM launch.
+struct GemmWeight {
+  const void *ptr;
+  int rows;
+};
+struct GemmPlan {
+  int dtype;                 // 0 bf16, 1 fp32
+  int K;
+  int n_tokens;
+  const void *x;             // activations [n_tokens, K] (config dtype), dev
+  int n_w;
+  GemmWeight w[kMaxSegs];
+  bool pair_mode;            // SwiGLU: w[0] = gate, w[1] = up (same rows)
+  GemmArgs args;             // epilogue fields filled by the caller; layout by the launcher
+};
+
+// Stream-K scratch a GEMM launch may use.
+struct GemmScratch {
+  float *partials;
+  size_t partial_floats;
+  unsigned *counters;
+  size_t n_counters;
+};
+
+unsigned take_error_word_gemm();
+unsigned take_error_word_att();
+unsigned take_error_word_small();
+
+size_t gemm_partial_floats(int n_ctas, int block_n);
+int num_sms();
+int gemm_block_n(int n_tokens);
+
+// Launch; returns an error message or empty string.
+std::string launch_gemm(GemmPlan &plan, const GemmScratch &scratch, cudaStream_t stream);
+
+// ------------------------------------------------------------------ launch helper
+// Launch with programmatic stream serialisation (PDL) so the next kernel's prologue can
+// overlap this kernel's tail; every kernel calls pdl_wait() before dependent accesses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace bd

@@ -1,0 +1,65 @@
+// Launchers of the non-GEMM kernels (attention, norms, embedding, bridge helpers).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace bd {
+
+struct AttArgs {
+  const void *q;        // [B*W, Hq*D] post-RoPE queries
+  const void *ring_k;   // [b_max, Hkv, cap, D] this layer's context ring
+  const void *ring_v;
+  const void *blk_k;    // [B, Hkv, W, D] block keys (post-RoPE)
+  const void *blk_v;
+  void *out;            // [B*W, Hq*D] attention output (config dtype)
+  const int64_t *frontier;  // [B]
+  float *part_o;        // [B, Hkv, n_splits, 64, D] fp32 unnormalised partial outputs
+  float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
+  int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
+};
+
+size_t attention_smem_bytes(int head_dim);
+size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim);
+size_t attention_ml_count(int B, int n_kv_heads, int n_splits);
+int attention_rows_max();
+std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream);
+
+// theta^(-2j/D) for j < D/2, computed on the host in double precision.
+struct RopeFreq {
+  double inv[64];
+};
+
+// Round prologue: x[b*W+i] = embed[id] (fp32), id = anchor_b for i = 0 else MASK, and the
+// (cos, sin) table of positions F_b + i.
+std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
+                              const int64_t *frontier, int B, int W, int mask_id, float *x,
+                              float2 *rope, int half, const RopeFreq &freq, cudaStream_t s);
+// (cos, sin) table of arbitrary absolute positions.
+std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
+                              const RopeFreq &freq, cudaStream_t s);
+
+enum NormMode : int {
+  NORM_PLAIN = 0,   // out = gain * x / sqrt(mean(x^2) + eps)
+  NORM_BRIDGE = 1,  // r = sqrt(mean(x^2)); out = x / (r + eps); r_out = r
+  NORM_FINAL = 2    // plain, plus fp32 copy and the mask-row copy for the LM head
+};
+std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain,
+                           float eps, int mode, void *out, float *r_out, float *f32_out,
+                           void *head_out, int W, cudaStream_t s);
+
+// c = sqrt(Rc) z / (||z|| + eps) for non-anchor rows; sqrt(Rc) * codebook[anchor] for anchors.
+std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
+                        const int32_t *anchors, int V, int W, float eps, void *c_out,
+                        cudaStream_t s);
+// m_i = sigmoid(G c_i + G_p c_{i-1} + b) * (A c_{i-1}) for i >= 1, m_0 = 0.
+std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias,
+                           int W, void *m_out, cudaStream_t s);
+// Per-row argmax over per-tile (max, lowest argmax) pairs; lowest id on ties.
+std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_tiles, int rows,
+                                 int32_t *tok_out, float *max_out, cudaStream_t s);
+// Copy rows [n, H] fp32 (used for the optional per-layer residual output).
+std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
+
+}  // namespace bd

@@ -1,0 +1,281 @@
+// Small bandwidth-trivial kernels around the GEMMs: embedding gather and RoPE tables,
+// row norms, the DSpine code finalisation and gated message, the split-vocab argmax
+// reduction.  Each launches with programmatic dependent launch and waits for the
+// previous kernel before touching data it produced or consumes.
+#include "bd_device.cuh"
+#include "bd_internal.h"
+#include "bd_kernels.h"
+
+namespace bd {
+
+BD_DEFINE_ERROR_TAKER(take_error_word_small)
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int i = 0; i < nw; ++i) s += red[i];
+  return s;
+}
+
+// (cos, sin) of pos * inv_freq[j]: the product and its reduction modulo 2 pi are done in
+// double precision so that large positions keep full single-precision angles.
+__device__ __forceinline__ float2 rope_cs(long long pos, double inv) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double ang = static_cast<double>(pos) * inv;
+  ang -= floor(ang / two_pi) * two_pi;
+  float s, c;
+  sincosf(static_cast<float>(ang), &s, &c);
+  return make_float2(c, s);
+}
+
+template <typename T>
+__global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *anchors,
+                                  const int64_t *frontier, int W, int mask_id, float *x,
+                                  float2 *rope, int half, RopeFreq freq) {
+  const int tok = blockIdx.x, b = tok / W, i = tok % W;
+  pdl_wait();
+  pdl_trigger();
+  int id = i == 0 ? anchors[b] : mask_id;
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+    id = 0;
+  }
+  const T *e = embed + static_cast<size_t>(id) * H;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) x[static_cast<size_t>(tok) * H + h] = to_f<T>(e[h]);
+  const long long pos = frontier[b] + i;
+  for (int j = threadIdx.x; j < half; j += blockDim.x)
+    rope[static_cast<size_t>(tok) * half + j] = rope_cs(pos, freq.inv[j]);
+}
+
+__global__ void rope_table_kernel(const int64_t *pos, int n, float2 *rope, int half,
+                                  RopeFreq freq) {
+  pdl_wait();
+  pdl_trigger();
+  const int total = n * half;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+    const int r = t / half, j = t % half;
+    rope[t] = rope_cs(pos[r], freq.inv[j]);
+  }
+}
+
+template <typename T>
+__global__ void rownorm_kernel(const float *x, int H, const T *gain, float eps, int mode, T *out,
+                               float *r_out, float *f32_out, T *head_out, int W) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const float *xr = x + static_cast<size_t>(row) * H;
+  float ss = 0.f;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) ss += xr[h] * xr[h];
+  ss = block_sum(ss, red);
+  if (mode == NORM_BRIDGE) {
+    const float r = sqrtf(ss / H);
+    const float s = 1.f / (r + eps);
+    for (int h = threadIdx.x; h < H; h += blockDim.x)
+      out[static_cast<size_t>(row) * H + h] = from_f<T>(xr[h] * s);
+    if (threadIdx.x == 0) r_out[row] = r;
+    return;
+  }
+  const float inv = rsqrtf(ss / H + eps);
+  const int i = row % W;
+  T *hrow = nullptr;
+  if (mode == NORM_FINAL && head_out != nullptr && i > 0)
+    hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    const float y = to_f<T>(gain[h]) * xr[h] * inv;
+    if (mode == NORM_PLAIN) {
+      out[static_cast<size_t>(row) * H + h] = from_f<T>(y);
+    } else {
+      if (f32_out) f32_out[static_cast<size_t>(row) * H + h] = y;
+      if (hrow) hrow[h] = from_f<T>(y);
+    }
+  }
+}
+
+template <typename T>
+__global__ void code_kernel(const float *z, int Rc, const T *codebook, const int32_t *anchors,
+                            int V, int W, float eps, T *c_out) {
+  __shared__ float red[32];
+  const int row = blockIdx.x, b = row / W, i = row % W;
+  pdl_wait();
+  pdl_trigger();
+  const float scale = sqrtf(static_cast<float>(Rc));
+  T *c = c_out + static_cast<size_t>(row) * Rc;
+  if (i == 0) {
+    int a = anchors[b];
+    if (a < 0 || a >= V) {
+      if (threadIdx.x == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      a = 0;
+    }
+    const T *cb = codebook + static_cast<size_t>(a) * Rc;
+    for (int k = threadIdx.x; k < Rc; k += blockDim.x) c[k] = from_f<T>(scale * to_f<T>(cb[k]));
+    return;
+  }
+  const float *zr = z + static_cast<size_t>(row) * Rc;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < Rc; k += blockDim.x) ss += zr[k] * zr[k];
+  ss = block_sum(ss, red);
+  const float s = scale / (sqrtf(ss) + eps);
+  for (int k = threadIdx.x; k < Rc; k += blockDim.x) c[k] = from_f<T>(zr[k] * s);
+}
+
+template <typename T>
+__global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, T *m_out) {
+  const int row = blockIdx.x, i = row % W;
+  pdl_wait();
+  pdl_trigger();
+  T *m = m_out + static_cast<size_t>(row) * Mc;
+  if (i == 0) {
+    for (int k = threadIdx.x; k < Mc; k += blockDim.x) m[k] = from_f<T>(0.f);
+    return;
+  }
+  const float *recv = pre + static_cast<size_t>(row) * 3 * Mc;         // G c_i
+  const float *pred = pre + static_cast<size_t>(row - 1) * 3 * Mc;     // [., G_p c_{i-1}, A c_{i-1}]
+  for (int k = threadIdx.x; k < Mc; k += blockDim.x) {
+    const float z = recv[k] + pred[Mc + k] + (bias ? to_f<T>(bias[k]) : 0.f);
+    const float g = 1.f / (1.f + expf(-z));
+    m[k] = from_f<T>(g * pred[2 * Mc + k]);
+  }
+}
+
+__global__ void argmax_reduce_kernel(const float *val, const int32_t *idx, int m_tiles, int rows,
+                                     int32_t *tok_out, float *max_out) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int row = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int t = threadIdx.x; t < m_tiles; t += blockDim.x) {
+    const float v = val[static_cast<size_t>(t) * rows + row];
+    const int i = idx[static_cast<size_t>(t) * rows + row];
+    if (v > best || (v == best && i < bi)) {
+      best = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sv[threadIdx.x >> 5] = best;
+    si[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    best = sv[0];
+    bi = si[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
+      if (sv[w] > best || (sv[w] == best && si[w] < bi)) {
+        best = sv[w];
+        bi = si[w];
+      }
+    tok_out[row] = bi;
+    if (max_out) max_out[row] = best;
+  }
+}
+
+__global__ void copy_f32_kernel(const float *src, float *dst, size_t n) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[t] = src[t];
+}
+
+// ------------------------------------------------------------------ launchers
+static std::string err(const char *what, cudaError_t e) {
+  return e == cudaSuccess ? std::string() : std::string(what) + ": " + cudaGetErrorString(e);
+}
+
+std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
+                              const int64_t *frontier, int B, int W, int mask_id, float *x,
+                              float2 *rope, int half, const RopeFreq &freq, cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(round_prep_kernel<__nv_bfloat16>, dim3(B * W), dim3(256), 0, s,
+                   static_cast<const __nv_bfloat16 *>(embed), H, V, anchors, frontier, W, mask_id, x,
+                   rope, half, freq);
+  else
+    e = launch_pdl(round_prep_kernel<float>, dim3(B * W), dim3(256), 0, s,
+                   static_cast<const float *>(embed), H, V, anchors, frontier, W, mask_id, x, rope,
+                   half, freq);
+  return err("round prep", e);
+}
+
+std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
+                              const RopeFreq &freq, cudaStream_t s) {
+  const int total = n * half;
+  const int blocks = (total + 255) / 256;
+  return err("rope table", launch_pdl(rope_table_kernel, dim3(blocks < 1024 ? blocks : 1024),
+                                      dim3(256), 0, s, pos, n, rope, half, freq));
+}
+
+std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain, float eps,
+                           int mode, void *out, float *r_out, float *f32_out, void *head_out, int W,
+                           cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(rownorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, x, H,
+                   static_cast<const __nv_bfloat16 *>(gain), eps, mode,
+                   static_cast<__nv_bfloat16 *>(out), r_out, f32_out,
+                   static_cast<__nv_bfloat16 *>(head_out), W);
+  else
+    e = launch_pdl(rownorm_kernel<float>, dim3(rows), dim3(256), 0, s, x, H,
+                   static_cast<const float *>(gain), eps, mode, static_cast<float *>(out), r_out,
+                   f32_out, static_cast<float *>(head_out), W);
+  return err("rownorm", e);
+}
+
+std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
+                        const int32_t *anchors, int V, int W, float eps, void *c_out,
+                        cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(code_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, z, Rc,
+                   static_cast<const __nv_bfloat16 *>(codebook), anchors, V, W, eps,
+                   static_cast<__nv_bfloat16 *>(c_out));
+  else
+    e = launch_pdl(code_kernel<float>, dim3(rows), dim3(256), 0, s, z, Rc,
+                   static_cast<const float *>(codebook), anchors, V, W, eps,
+                   static_cast<float *>(c_out));
+  return err("code", e);
+}
+
+std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias, int W,
+                           void *m_out, cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(message_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, pre, Mc,
+                   static_cast<const __nv_bfloat16 *>(bias), W, static_cast<__nv_bfloat16 *>(m_out));
+  else
+    e = launch_pdl(message_kernel<float>, dim3(rows), dim3(256), 0, s, pre, Mc,
+                   static_cast<const float *>(bias), W, static_cast<float *>(m_out));
+  return err("message", e);
+}
+
+std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_tiles, int rows,
+                                 int32_t *tok_out, float *max_out, cudaStream_t s) {
+  return err("argmax reduce", launch_pdl(argmax_reduce_kernel, dim3(rows), dim3(256), 0, s, val,
+                                         idx, m_tiles, rows, tok_out, max_out));
+}
+
+std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s) {
+  const size_t blocks = (n + 255) / 256;
+  return err("copy", launch_pdl(copy_f32_kernel, dim3(blocks < 1024 ? blocks : 1024), dim3(256), 0,
+                                s, src, dst, n));
+}
+
+}  // namespace bd

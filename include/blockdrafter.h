@@ -1,0 +1,204 @@
+/*
+ * blockdrafter.h -- C ABI of a GB300 (sm_103a) library that runs one proposal round of
+ * a DFlash-style parallel block drafter with DSpine's adjacent gated causal injection.
+ *
+ * Sources the operations follow (page title and section):
+ *   [DFlash-notes] NInfer maintainer page "dflash.md": conditioning equations, context
+ *                  K/V projection, draft input table, local-window attention rule,
+ *                  per-layer equations, proposal head, ring storage.
+ *   [Bridge]       "DSpine for Qwen3.8-27B: Causal Features Through Depth", section
+ *                  "The bridge: read 1,024 features, write through rank 512".
+ *   [Gate]         "DSpine 完全拆解", sections "相邻因果注入" and "门控与写回".
+ *   [BlockCausal]  "DSpine 完全拆解", section "块因果注意力".
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer marked "dev" is a device pointer the CALLER allocated and owns; the
+ *     library never allocates, frees or synchronises.  It enqueues kernels on `stream`
+ *     (a cudaStream_t passed as void*; NULL = legacy default stream) and returns.
+ *   - Matrices are row-major [out, in] (PyTorch nn.Linear layout), contiguous, in the
+ *     config's element type (bf16 or fp32), 16-byte aligned base addresses.
+ *   - Every call returns a bd_status and never aborts; bd_last_error() gives a
+ *     thread-local message for the last non-OK status.  Invalid arguments are
+ *     rejected on the host before anything is enqueued.
+ *   - `workspace` is caller-owned device scratch of at least bd_workspace_bytes(...)
+ *     bytes, 256-byte aligned; its contents need not be initialised and are
+ *     clobbered.  Calls that share a workspace must be ordered on one stream.
+ *   - Device-side waits are bounded; a wait that gives up sets a device error word
+ *     that bd_sync_status() reports as BD_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef BLOCKDRAFTER_H
+#define BLOCKDRAFTER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BD_ABI_VERSION 1
+#define BD_MAX_LAYERS 16
+
+typedef enum {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = -1,     /* null pointer, bad size, out-of-range id, misalignment  */
+  BD_ERR_UNSUPPORTED = -2,     /* geometry the kernels do not implement (never a fallback) */
+  BD_ERR_CUDA = -3,            /* a CUDA runtime/driver call failed                        */
+  BD_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait gave up                       */
+  BD_ERR_WORKSPACE = -5        /* workspace too small or misaligned                        */
+} bd_status;
+
+typedef enum { BD_BF16 = 0, BD_F32 = 1 } bd_dtype;
+
+/* Block attention among the W block rows.  [DFlash-notes] is bidirectional;
+ * [BlockCausal] lets row i see block rows 0..i only.  Context keys are unaffected. */
+typedef enum { BD_BLOCK_BIDIRECTIONAL = 0, BD_BLOCK_CAUSAL = 1 } bd_block_mask;
+
+/* Draft geometry; the fields mirror a DFlash draft config ([DFlash-notes], config
+ * fields: layer count, dimensions, eps, RoPE theta, layer attention types, sliding
+ * window, target block ids, mask token id) plus the DSpine bridge widths ([Bridge]). */
+typedef struct {
+  int hidden;                        /* H                                                  */
+  int n_layers;                      /* L <= BD_MAX_LAYERS                                 */
+  int n_q_heads, n_kv_heads;         /* Hq, Hkv (Hq % Hkv == 0)                            */
+  int head_dim;                      /* D: 64 or 128                                       */
+  int ffn;                           /* SwiGLU intermediate width I                        */
+  int vocab;                         /* V rows of the tied embedding / LM head             */
+  int n_target_layers;               /* captured target layers; W_feature is [H, n*H]      */
+  int window[BD_MAX_LAYERS];         /* sliding window S of layer l; 0 = full context      */
+  int ring_capacity[BD_MAX_LAYERS];  /* ring slots of layer l (>= window; full: max ctx)   */
+  float eps;                         /* RMSNorm eps, also the bridge's numerical floor     */
+  float rope_theta;                  /* split-half RoPE base                               */
+  int mask_token_id;                 /* MASK id fed to the K proposal rows                 */
+  int code_width;                    /* Rc; 0 disables the bridge (plain DFlash)           */
+  int msg_width;                     /* Mc                                                 */
+  int block_mask;                    /* bd_block_mask                                      */
+  int dtype;                         /* bd_dtype of weights, rings and activations         */
+} bd_config;
+
+/* Per-layer weights (dev, caller-owned, row-major [out, in], config dtype). */
+typedef struct {
+  const void *in_norm;   /* [H]                                                          */
+  const void *wq;        /* [Hq*D, H]                                                    */
+  const void *wk;        /* [Hkv*D, H]  used for block AND context keys                  */
+  const void *wv;        /* [Hkv*D, H]  used for block AND context values                */
+  const void *q_norm;    /* [D] per-head query RMSNorm gain                              */
+  const void *k_norm;    /* [D] per-head key RMSNorm gain                                */
+  const void *wo;        /* [H, Hq*D]                                                    */
+  const void *post_norm; /* [H]                                                          */
+  const void *w_gate;    /* [I, H]                                                       */
+  const void *w_up;      /* [I, H]                                                       */
+  const void *w_down;    /* [H, I]                                                       */
+  const void *r_read;    /* [Rc, H]  DSpine per-layer code read R_l (bridge only)        */
+  const void *w_write;   /* [H, Mc]  DSpine per-layer write W_l (bridge only)            */
+} bd_layer_weights;
+
+typedef struct {
+  const void *w_feature;    /* [H, n_target_layers*H], bias-free                          */
+  const void *context_norm; /* [H]                                                        */
+  const void *final_norm;   /* [H]                                                        */
+  const void *embed_head;   /* [V, H] tied target embedding and LM head                   */
+  const void *codebook;     /* [V, Rc] token-code table (bridge only)                     */
+  const void *g_recv;       /* [Mc, Rc] receiver gate G, shared by all layers             */
+  const void *g_pred;       /* [Mc, Rc] predecessor gate G_p, shared                      */
+  const void *a_val;        /* [Mc, Rc] predecessor value map A, shared                   */
+  const void *gate_bias;    /* [Mc] gate bias b, or NULL for b = 0                        */
+  bd_layer_weights layer[BD_MAX_LAYERS];
+} bd_weights;
+
+/* Context K/V rings ([DFlash-notes], ring storage): layer l holds
+ * k[l], v[l] = dev [b_max][Hkv][ring_capacity[l]][D] in the config dtype.  Absolute
+ * position p of request b lives in slot p mod ring_capacity[l]; a ring whose request
+ * has context frontier F holds the live interval [max(0, F - cap), F).  Request b of
+ * a round or a materialisation uses ring row b. */
+typedef struct {
+  void *k[BD_MAX_LAYERS];
+  void *v[BD_MAX_LAYERS];
+  int b_max;
+} bd_kv_cache;
+
+/* Library ABI version (BD_ABI_VERSION). */
+int bd_abi_version(void);
+
+/* Bytes of workspace any entry point below needs for rounds of up to `b_max`
+ * requests with up to `max_masks` masks (K) and materialisations of up to
+ * `max_ctx_rows` rows per call.  Returns 0 for an invalid or unsupported config. */
+size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int max_ctx_rows);
+
+/*
+ * Context K/V materialisation (S1 + S2).  [DFlash-notes], conditioning and context K/V:
+ *   c_t = plain_rmsnorm(W_feature s_t, context_norm)
+ *   for each layer l:  k = rope_1d(plain_head_rmsnorm(W_k^l c_t, k_norm^l), t)
+ *                      v = W_v^l c_t
+ * stored (bf16 round-to-nearest in a bf16 config) into ring row `row_request[r]` at
+ * slot row_pos[r] mod ring_capacity[l].
+ *
+ *   target_feats  dev [n_rows, n_target_layers*H]  captured residual rows s_t (the
+ *                 target layers' residual outputs concatenated in recorded order)
+ *   row_request   dev int32 [n_rows]  ring row (request) of each feature row, < b_max
+ *   row_pos       dev int64 [n_rows]  absolute context position t of each row (>= 0)
+ *   ctx_frontier  dev int64 [b_max]   each request's context frontier F AFTER this call.
+ *                 A row is stored in layer l only if row_pos >= F - ring_capacity[l]
+ *                 (the final live window); older rows of a long chunk are computed
+ *                 but not stored, while the frontier still covers the whole chunk.
+ *   n_rows        1 .. max_ctx_rows given to bd_workspace_bytes
+ * Rows of one request must have distinct positions.  Rows are independent: any split
+ * of a chunk into calls stores the same ring contents.
+ */
+bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
+                                const bd_kv_cache *kv, const void *target_feats,
+                                const int32_t *row_request, const int64_t *row_pos,
+                                const int64_t *ctx_frontier, int n_rows, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * One masked-block draft forward (S3 .. S9 and the final norm) for B requests.
+ * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for
+ * the injection after every layer when code_width > 0:
+ *   row (b, 0) = embed(anchor_ids[b]) at position F_b; rows (b, i>=1) = embed(MASK) at
+ *   F_b + i.  Each layer: rmsnorm -> Q/K/V (+ head norm, RoPE) -> attention over the
+ *   request's ring context and its own block -> W_o + residual -> rmsnorm -> SwiGLU +
+ *   residual -> [bridge read, anchor code, gated predecessor message, RMS-scaled write;
+ *   the anchor row receives no write].  Then final plain_rmsnorm.
+ *
+ *   anchor_ids  dev int32 [B]  anchor token a_b (< vocab)
+ *   frontier    dev int64 [B]  committed context length F_b >= 1 of request b; ring row b
+ *               must hold the live interval of every layer at that frontier
+ *   B           1 .. 8 requests;  n_masks  K in 1 .. 15 (block width W = K + 1)
+ *   head_in     dev [B*K, H] config dtype, OUT: final-normed mask rows, row b*K + (i-1)
+ *               for block row i >= 1 -- the input of bd_lm_head_argmax
+ *   hidden_out  dev fp32 [B*W, H] OUT final-normed rows of every block row, or NULL
+ *   layers_out  dev fp32 [L, B*W, H] OUT post-injection residual after each layer, or
+ *               NULL (a debugging/parity output; it adds device-to-device copies)
+ */
+bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
+                         const int32_t *anchor_ids, const int64_t *frontier, int B,
+                         int n_masks, void *head_in, float *hidden_out, float *layers_out,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Tied LM head with per-row argmax (S10).  [DFlash-notes], proposal head:
+ *   logits = embed_head . hidden_r ;  token_out[r] = argmax_v logits[v]
+ * Ties resolve to the lowest token id.  fp32 accumulation of config-dtype products.
+ *
+ *   hidden         dev [rows, H] config dtype (e.g. bd_draft_round's head_in)
+ *   rows           1 .. 8*15
+ *   token_out      dev int32 [rows]  OUT
+ *   max_logit_out  dev fp32 [rows]   OUT the winning logit, or NULL
+ */
+bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const void *hidden,
+                            int rows, int32_t *token_out, float *max_logit_out,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Thread-local description of the last non-OK status returned on this thread. */
+const char *bd_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word.  Returns
+ * BD_ERR_DEVICE_TIMEOUT if a bounded device wait gave up since the last check,
+ * BD_ERR_CUDA if the stream reports an error, BD_OK otherwise. */
+bd_status bd_sync_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLOCKDRAFTER_H */

@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports
+every symbol include/blockdrafter.h declares, sizes workspaces, and rejects invalid
+arguments before enqueuing anything."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import bdsynth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from block_drafter_gb300 import builder as bld
+    bld.build()
+    from block_drafter_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "blockdrafter.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bd_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_entry_points():
+    syms = header_symbols()
+    for s in ("bd_ctx_kv_materialize", "bd_draft_round", "bd_lm_head_argmax"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(B):
+    L = B.lib()
+    for s in header_symbols():
+        assert hasattr(L, s), s
+    assert set(B.EXPORTS) <= set(header_symbols())
+    assert B.abi_version() == 1
+
+
+def cfg_of(w, **kw):
+    from block_drafter_gb300.session import config_of
+    c = config_of(w, bdsynth.mask_token_id(w, 0))
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("name", list(bdsynth.WORKLOADS))
+def test_workspace_bytes_positive_for_every_workload(B, name):
+    w = bdsynth.WORKLOADS[name]
+    c = cfg_of(w)
+    n = B.lib().bd_workspace_bytes(C.byref(c), w.batch, w.n_masks, 2048)
+    assert n > 0
+    assert n < 8 << 30
+
+
+def test_workspace_bytes_rejects_bad_sizes(B):
+    c = cfg_of(bdsynth.TINY)
+    L = B.lib()
+    assert L.bd_workspace_bytes(C.byref(c), 0, 7, 16) == 0
+    assert L.bd_workspace_bytes(C.byref(c), 9, 7, 16) == 0
+    assert L.bd_workspace_bytes(C.byref(c), 1, 16, 16) == 0
+    bad = cfg_of(bdsynth.TINY, head_dim=96)
+    assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0
+    bad = cfg_of(bdsynth.TINY, n_q_heads=3)
+    assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0
+    bad = cfg_of(bdsynth.TINY, mask_token_id=1024)
+    assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0
+
+
+def _fake_weights(B, c, n_layers):
+    w = B.Weights()
+    p = 0x10000
+    for k in ("w_feature", "context_norm", "final_norm", "embed_head", "codebook", "g_recv",
+              "g_pred", "a_val"):
+        setattr(w, k, p)
+    for l in range(n_layers):
+        for k in B.LAYER_FIELDS:
+            setattr(w.layer[l], k, p)
+    return w
+
+
+def test_entry_points_reject_invalid_arguments_on_host(B):
+    L = B.lib()
+    c = cfg_of(bdsynth.TINY)
+    w = _fake_weights(B, c, c.n_layers)
+    kv = B.KvCache()
+    for l in range(c.n_layers):
+        kv.k[l] = 0x10000
+        kv.v[l] = 0x10000
+    kv.b_max = 1
+    ws = 0x100000
+    # B out of range
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 9, 7, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1 and b"B must be" in L.bd_last_error()
+    # K out of range
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 16, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1
+    # misaligned weight
+    w.layer[1].wq = 0x10008
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1 and b"layer 1" in L.bd_last_error()
+    w.layer[1].wq = 0x10000
+    # more requests than ring rows
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 2, 7, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1 and b"b_max" in L.bd_last_error()
+    # misaligned workspace
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
+                          None, None, ws + 16, 1 << 30, None)
+    assert st == -5
+    # head: rows out of range
+    st = L.bd_lm_head_argmax(C.byref(c), C.byref(w), 0x10000, 121, 0x10000, None, ws, 1 << 30, None)
+    assert st == -1
+    # materialise: no rows
+    st = L.bd_ctx_kv_materialize(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 0x10000,
+                                 0x10000, 0, ws, 1 << 30, None)
+    assert st == -1
+    # bridge on, bridge weights missing
+    w.g_pred = None
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1 and b"bridge" in L.bd_last_error()
+
+
+def test_unsupported_geometry_is_an_error_not_a_fallback(B):
+    L = B.lib()
+    # bf16 with 8 query heads per KV head and W = 16 -> 128 query rows per KV head
+    c = cfg_of(bdsynth.DSPINE27B_B1, n_kv_heads=4)
+    w = _fake_weights(B, c, c.n_layers)
+    kv = B.KvCache()
+    for l in range(c.n_layers):
+        kv.k[l] = kv.v[l] = 0x10000
+    kv.b_max = 1
+    st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 15, 0x10000,
+                          None, None, 0x100000, 1 << 34, None)
+    assert st == -2
+
+
+def test_ring_capacity_must_hold_the_window(B):
+    c = cfg_of(bdsynth.DSPINE27B_B1)
+    c.ring_capacity[2] = 100
+    assert B.lib().bd_workspace_bytes(C.byref(c), 1, 15, 16) == 0

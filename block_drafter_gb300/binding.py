@@ -23,7 +23,7 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
           -4: "BD_ERR_DEVICE_TIMEOUT", -5: "BD_ERR_WORKSPACE"}
 
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
-           "bd_lm_head_argmax", "bd_last_error", "bd_sync_status")
+           "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches")
 
 
 class BdError(RuntimeError):
@@ -89,6 +89,7 @@ def lib() -> C.CDLL:
         L.bd_last_error.restype = C.c_char_p
         L.bd_sync_status.restype = i
         L.bd_sync_status.argtypes = [vp]
+        L.bd_kernel_launches.restype = C.c_uint64
         _lib = L
     return _lib
 
@@ -189,6 +190,10 @@ def lm_head_argmax(cfg: Config, weights: Weights, hidden: torch.Tensor, token_ou
         C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
         _ptr(max_logit_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def kernel_launches() -> int:
+    return int(lib().bd_kernel_launches())
 
 
 def sync_status(stream=None):

@@ -2,15 +2,21 @@
 // sequences of the three entry points.  Every step of the round runs in this library's
 // kernels; nothing here computes on the host beyond launch geometry and the RoPE
 // inverse frequencies.
-#include "../../include/blockdrafter.h"
+#include "blockdrafter.h"
 #include "bd_internal.h"
 #include "bd_kernels.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <string>
+
+namespace bd {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace bd
 
 namespace {
 
@@ -136,8 +142,8 @@ int att_splits(const bd_config *c, int l, int B, int W, int sms) {
   const int cap = c->ring_capacity[l];
   const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
   const int max_keys = ctx + W;
-  const int max_splits = (max_keys + 63) / 64;
-  int s = (2 * sms + B * c->n_kv_heads - 1) / (B * c->n_kv_heads);
+  const int max_splits = (max_keys + 127) / 128;  // at least two 64-key blocks per split
+  int s = (sms + B * c->n_kv_heads - 1) / (B * c->n_kv_heads);
   if (s < 1) s = 1;
   return s < max_splits ? s : max_splits;
 }
@@ -165,7 +171,7 @@ size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + ti
 
 struct RoundWs {
   GemmWs g;
-  float *x, *z, *pre, *r, *part_o;
+  float *x, *z, *pre, *r, *part_o, *qkv_raw;
   float2 *rope, *part_ml;
   void *xn, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
@@ -186,6 +192,7 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sm
   const int H = c->hidden, QD = c->n_q_heads * c->head_dim, KD = c->n_kv_heads * c->head_dim;
   carve_gemm(cv, w.g, gemm_block_n(T), round_max_tiles(c, T), sms);
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
+  w.qkv_raw = cv.take<float>(static_cast<size_t>(T) * (QD + 2 * KD));
   w.xn = cv.take<char>(static_cast<size_t>(T) * H * e);
   w.q = cv.take<char>(static_cast<size_t>(T) * QD * e);
   w.kblk = cv.take<char>(static_cast<size_t>(T) * KD * e);
@@ -215,7 +222,7 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sm
 
 struct MatWs {
   GemmWs g;
-  float *feat;
+  float *feat, *kv_raw;
   void *cmat;
   float2 *rope;
 };
@@ -229,6 +236,7 @@ size_t mat_max_tiles(const bd_config *c, int n) {
 void carve_mat(Carve &cv, MatWs &w, const bd_config *c, int n, int sms) {
   carve_gemm(cv, w.g, gemm_block_n(n), mat_max_tiles(c, n), sms);
   w.feat = cv.take<float>(static_cast<size_t>(n) * c->hidden);
+  w.kv_raw = cv.take<float>(static_cast<size_t>(n) * c->n_layers * 2 * c->n_kv_heads * c->head_dim);
   w.cmat = cv.take<char>(static_cast<size_t>(n) * c->hidden * elem_bytes(c));
   w.rope = cv.take<float2>(static_cast<size_t>(n) * (c->head_dim / 2));
 }
@@ -262,9 +270,6 @@ GemmPlan make_plan(const bd_config *c, const void *x, int n_tok, int K) {
   p.x = x;
   p.n_tokens = n_tok;
   p.K = K;
-  p.args.eps = c->eps;
-  p.args.head_dim = c->head_dim;
-  p.args.n_kv_heads = c->n_kv_heads;
   p.args.vocab = c->vocab;
   return p;
 }
@@ -282,6 +287,8 @@ extern "C" {
 int bd_abi_version(void) { return BD_ABI_VERSION; }
 
 const char *bd_last_error(void) { return t_last_error.c_str(); }
+
+uint64_t bd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int max_ctx_rows) {
   if (!check_config(cfg).empty()) return 0;
@@ -342,32 +349,56 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
     BD_TRY(launch_rownorm(cfg->dtype, mw.feat, n_rows, H, w->context_norm, cfg->eps, NORM_PLAIN,
                           mw.cmat, nullptr, nullptr, nullptr, 1, s));
   }
-  // S2: every layer's context K (head norm + RoPE) and V, scattered into the rings
+  // S2: every layer's raw context K and V (fp32), then head norm + RoPE + ring scatter
+  const int ldkv = cfg->n_layers * 2 * KD;
   for (int l0 = 0; l0 < cfg->n_layers; l0 += kMaxSegs / 2) {
     const int l1 = std::min(cfg->n_layers, l0 + kMaxSegs / 2);
     GemmPlan p = make_plan(cfg, mw.cmat, n_rows, H);
-    p.args.epi = EPI_HEADS;
-    p.args.rope = mw.rope;
-    p.args.row_req = row_request;
-    p.args.row_pos = row_pos;
-    p.args.frontier = ctx_frontier;
-    p.args.n_req = kv->b_max;
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = mw.kv_raw;
+    p.args.ld_out = ldkv;
     for (int l = l0; l < l1; ++l) {
       const int sk = p.n_w;
       add_w(p, w->layer[l].wk, KD);
       add_w(p, w->layer[l].wv, KD);
-      p.args.seg[sk] = GemmSeg{};
-      p.args.seg[sk].kind = HK_K;
-      p.args.seg[sk].norm = w->layer[l].k_norm;
-      p.args.seg[sk].dst = kv->k[l];
-      p.args.seg[sk].dst_mode = HD_RING;
-      p.args.seg[sk].cap = cfg->ring_capacity[l];
-      p.args.seg[sk + 1] = p.args.seg[sk];
-      p.args.seg[sk + 1].kind = HK_V;
-      p.args.seg[sk + 1].norm = nullptr;
-      p.args.seg[sk + 1].dst = kv->v[l];
+      p.args.seg[sk].out_col = l * 2 * KD;
+      p.args.seg[sk + 1].out_col = l * 2 * KD + KD;
     }
     BD_TRY(launch_gemm(p, sc, s));
+  }
+  {
+    HeadPostArgs h;
+    memset(&h, 0, sizeof h);
+    h.raw = mw.kv_raw;
+    h.ld_raw = ldkv;
+    h.rows = n_rows;
+    h.D = D;
+    h.n_kv_heads = cfg->n_kv_heads;
+    h.W = 1;
+    h.n_req = kv->b_max;
+    h.eps = cfg->eps;
+    h.rope = mw.rope;
+    h.row_req = row_request;
+    h.row_pos = row_pos;
+    h.frontier = ctx_frontier;
+    for (int l = 0; l < cfg->n_layers; ++l) {
+      HeadSeg &k = h.seg[h.n_segs++];
+      k.kind = HK_K;
+      k.dst_mode = HD_RING;
+      k.col0 = l * 2 * KD;
+      k.n_heads = cfg->n_kv_heads;
+      k.cap = cfg->ring_capacity[l];
+      k.norm = w->layer[l].k_norm;
+      k.dst = kv->k[l];
+      HeadSeg &v = h.seg[h.n_segs++];
+      v = k;
+      v.kind = HK_V;
+      v.col0 = l * 2 * KD + KD;
+      v.norm = nullptr;
+      v.dst = kv->v[l];
+    }
+    h.total_heads = 2 * cfg->n_layers * cfg->n_kv_heads;
+    BD_TRY(launch_head_post(cfg->dtype, h, s));
   }
   return BD_OK;
 }
@@ -421,22 +452,29 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       add_w(p, L.wq, QD);
       add_w(p, L.wk, KD);
       add_w(p, L.wv, KD);
-      p.args.epi = EPI_HEADS;
-      p.args.rope = rw.rope;
-      p.args.block_w = W;
-      p.args.seg[0].kind = HK_Q;
-      p.args.seg[0].norm = L.q_norm;
-      p.args.seg[0].dst = rw.q;
-      p.args.seg[0].dst_mode = HD_TOKEN_MAJOR;
-      p.args.seg[0].ld = QD;
-      p.args.seg[1].kind = HK_K;
-      p.args.seg[1].norm = L.k_norm;
-      p.args.seg[1].dst = rw.kblk;
-      p.args.seg[1].dst_mode = HD_BLOCK;
-      p.args.seg[2].kind = HK_V;
-      p.args.seg[2].dst = rw.vblk;
-      p.args.seg[2].dst_mode = HD_BLOCK;
+      p.args.epi = EPI_STORE_F32;
+      p.args.out_f32 = rw.qkv_raw;
+      p.args.ld_out = QD + 2 * KD;
+      p.args.seg[0].out_col = 0;
+      p.args.seg[1].out_col = QD;
+      p.args.seg[2].out_col = QD + KD;
       BD_TRY(launch_gemm(p, sc, s));
+      HeadPostArgs h;
+      memset(&h, 0, sizeof h);
+      h.raw = rw.qkv_raw;
+      h.ld_raw = QD + 2 * KD;
+      h.rows = T;
+      h.D = D;
+      h.n_kv_heads = cfg->n_kv_heads;
+      h.W = W;
+      h.eps = cfg->eps;
+      h.rope = rw.rope;
+      h.n_segs = 3;
+      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q};
+      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk};
+      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk};
+      h.total_heads = cfg->n_q_heads + 2 * cfg->n_kv_heads;
+      BD_TRY(launch_head_post(dt, h, s));
     }
     // S5: block attention over the ring context and the block
     {

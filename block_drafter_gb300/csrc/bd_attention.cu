@@ -283,7 +283,9 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
   }
 }
 
-// Merge the splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// Merge the splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  One warp per
+// query row; lanes own D/32 consecutive output dims and the split weights are computed
+// by lanes and broadcast, so the per-split loads are independent of each other.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) attention_combine_kernel(AttArgs a) {
   const int bh = blockIdx.x;
@@ -295,33 +297,54 @@ __global__ void __launch_bounds__(256) attention_combine_kernel(AttArgs a) {
   pdl_wait();
   pdl_trigger();
   if (rr >= R) return;
+  constexpr int PER = D / 32;
   const float *po = a.part_o + static_cast<size_t>(bh) * a.n_splits * kAttRows * D;
   const float2 *pml = a.part_ml + static_cast<size_t>(bh) * a.n_splits * kAttRows;
   float M = -INFINITY;
-  for (int s = 0; s < a.n_splits; ++s) {
+  for (int s = lane; s < a.n_splits; s += 32) {
     const float2 ml = pml[s * kAttRows + rr];
     if (ml.y > 0.f) M = fmaxf(M, ml.x);
   }
-  constexpr int PER = D / 32;
+  M = warp_max(M);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
-  for (int s = 0; s < a.n_splits; ++s) {
-    const float2 ml = pml[s * kAttRows + rr];
-    if (!(ml.y > 0.f)) continue;
-    const float wgt = exp2f(ml.x - M);
-    L += wgt * ml.y;
-    const float *os = po + (static_cast<size_t>(s) * kAttRows + rr) * D;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += wgt * os[lane + 32 * e];
+  for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
+    const int s = s0 + lane;
+    float wgt = 0.f;
+    if (s < a.n_splits) {
+      const float2 ml = pml[s * kAttRows + rr];
+      if (ml.y > 0.f) {
+        wgt = exp2f(ml.x - M);
+        L += wgt * ml.y;
+      }
+    }
+    const int cnt = min(32, a.n_splits - s0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wgt, j);
+      const float *os = po + (static_cast<size_t>(s0 + j) * kAttRows + rr) * D + lane * PER;
+      if (PER == 4) {
+        const float4 o = *reinterpret_cast<const float4 *>(os);
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+        acc[2] += wj * o.z;
+        acc[3] += wj * o.w;
+      } else {
+        const float2 o = *reinterpret_cast<const float2 *>(os);
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+      }
+    }
   }
+  L = warp_sum(L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int gh = rr / a.W, i = rr % a.W;
   T *out = static_cast<T *>(a.out) +
-           (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D;
+           (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) out[lane + 32 * e] = from_f<T>(acc[e] * inv);
+  for (int e = 0; e < PER; ++e) out[e] = from_f<T>(acc[e] * inv);
 }
 
 // fp32 path (small geometries): one CTA per (query head, request), exact fp32 softmax.

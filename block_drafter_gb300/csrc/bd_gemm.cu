@@ -19,6 +19,7 @@
 #include "bd_internal.h"
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -42,15 +43,19 @@ template <> struct MmaTraits<float> {
 constexpr int kATileBytes = kBM * 128;  // 16 KB: 128 rows x 128 bytes
 constexpr int kXStride = 17;            // epilogue exchange row stride (floats)
 constexpr int kMaxStages = 12;
-constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
+constexpr long long kMinUnits = 8;
+constexpr size_t kSmemLimit = 232448 - 1024;  // 227 KB opt-in per block, less static smem
 
+// A pipeline stage holds kbox K-boxes of the weight tile (each 128 rows x 128 bytes, so
+// every weight row is read in kbox*128-byte contiguous pieces) and the matching kbox
+// boxes of the activation tile.
 struct SmemLayout {
   size_t off_b, off_x, off_red, off_bar, total;
 };
-__host__ __device__ inline SmemLayout smem_layout(int stages, int block_n) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int block_n, int kbox) {
   SmemLayout L;
-  L.off_b = static_cast<size_t>(stages) * kATileBytes;
-  L.off_x = L.off_b + static_cast<size_t>(stages) * block_n * 128;
+  L.off_b = static_cast<size_t>(stages) * kbox * kATileBytes;
+  L.off_x = L.off_b + static_cast<size_t>(stages) * kbox * block_n * 128;
   L.off_red = L.off_x + kBM * kXStride * 4;
   L.off_bar = L.off_red + 2 * 64 * 4;
   L.total = L.off_bar + (2 * stages + 4) * 8 + 16 + 1024;  // + alignment slack
@@ -97,17 +102,36 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_x = policy_evict_last();
   const int S = p.stages;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.block_n) * 128u;
-  const uint32_t stage_bytes = kATileBytes + b_bytes;
+  const int KB = p.kbox;
+  const uint32_t box_b = static_cast<uint32_t>(p.block_n) * 128u;
+  const uint32_t a_bytes = static_cast<uint32_t>(KB) * kATileBytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(KB) * box_b;
+  const int n_boxes = (p.K + BK - 1) / BK;  // boxes that hold any of the K columns
+  // Boxes of unit kbi that start inside K; a box past the end is neither loaded nor used.
+  auto boxes = [&](int kbi) { return min(KB, n_boxes - kbi * KB); };
+  auto unit_bytes = [&](int kbi) {
+    return static_cast<uint32_t>(boxes(kbi)) * (kATileBytes + box_b);
+  };
 
   auto load_a = [&](int m_tile, int kbi, uint8_t *dst, uint64_t *bar) {
-    if (p.pair_mode) {
-      tma_load_2d(dst, &maps.a[0], bar, kbi * BK, m_tile * 64, pol_w);
-      tma_load_2d(dst + 64 * 128, &maps.a[1], bar, kbi * BK, m_tile * 64, pol_w);
-    } else {
-      const int s = seg_of_tile(p, m_tile);
-      tma_load_2d(dst, &maps.a[s], bar, kbi * BK, (m_tile - p.seg[s].tile_begin) * kBM, pol_w);
+    const int s = p.pair_mode ? 0 : seg_of_tile(p, m_tile);
+    const int nb = boxes(kbi);
+    for (int j = 0; j < nb; ++j) {
+      const int x = (kbi * KB + j) * BK;
+      uint8_t *d = dst + static_cast<size_t>(j) * kATileBytes;
+      if (p.pair_mode) {
+        tma_load_2d(d, &maps.a[0], bar, x, m_tile * 64, pol_w);
+        tma_load_2d(d + 64 * 128, &maps.a[1], bar, x, m_tile * 64, pol_w);
+      } else {
+        tma_load_2d(d, &maps.a[s], bar, x, (m_tile - p.seg[s].tile_begin) * kBM, pol_w);
+      }
     }
+  };
+  auto load_b = [&](int n_tile, int kbi, uint8_t *dst, uint64_t *bar) {
+    const int nb = boxes(kbi);
+    for (int j = 0; j < nb; ++j)
+      tma_load_2d(dst + static_cast<size_t>(j) * box_b, &maps.b, bar, (kbi * KB + j) * BK,
+                  n_tile * p.block_n, pol_x);
   };
 
   // The weight tiles do not depend on the previous kernel: start streaming them before
@@ -120,8 +144,8 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
     while (q < pre && w.next(tile, kb0, kb1)) {
       const int m_tile = tile / p.n_tiles_n;
       for (int kbi = kb0; kbi < kb1 && q < pre; ++kbi, ++q) {
-        mbar_arrive_expect_tx(&full[q], stage_bytes);
-        load_a(m_tile, kbi, sA + static_cast<size_t>(q) * kATileBytes, &full[q]);
+        mbar_arrive_expect_tx(&full[q], unit_bytes(kbi));
+        load_a(m_tile, kbi, sA + static_cast<size_t>(q) * a_bytes, &full[q]);
       }
     }
   }
@@ -139,11 +163,10 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
           *sabort = 1;
           return;
         }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        load_a(m_tile, kbi, sA + static_cast<size_t>(s) * kATileBytes, &full[s]);
+        mbar_arrive_expect_tx(&full[s], unit_bytes(kbi));
+        load_a(m_tile, kbi, sA + static_cast<size_t>(s) * a_bytes, &full[s]);
       }
-      tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &maps.b, &full[s], kbi * BK,
-                  n_tile * p.block_n, pol_x);
+      load_b(n_tile, kbi, sB + static_cast<size_t>(s) * b_bytes, &full[s]);
     }
   }
 }
@@ -156,7 +179,11 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
   constexpr int BK = MmaTraits<T>::BK, UK = MmaTraits<T>::UK;
   const uint32_t idesc = umma_idesc(MmaTraits<T>::fmt, kBM, p.block_n);
   const int S = p.stages;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.block_n) * 128u;
+  const int KB = p.kbox;
+  const uint32_t box_b = static_cast<uint32_t>(p.block_n) * 128u;
+  const uint32_t a_bytes = static_cast<uint32_t>(KB) * kATileBytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(KB) * box_b;
+  const int n_boxes = (p.K + BK - 1) / BK;
   SegWalk w{u0, u1, p.kb};
   int tile, kb0, kb1, e = 0;
   long long q = 0;
@@ -176,17 +203,20 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
         return;
       }
       tc_fence_after();
-      const uint32_t abase = smem_u32(sA + static_cast<size_t>(s) * kATileBytes);
+      const uint32_t abase = smem_u32(sA + static_cast<size_t>(s) * a_bytes);
       const uint32_t bbase = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+      const int nb = min(KB, n_boxes - kbi * KB);
+      for (int j = 0; j < nb; ++j) {
 #pragma unroll
-      for (int k = 0; k < BK / UK; ++k) {
-        const uint64_t ad = umma_desc_sw128(abase + k * 32);
-        const uint64_t bd = umma_desc_sw128(bbase + k * 32);
-        const uint32_t acc = (kbi > kb0 || k > 0) ? 1u : 0u;
-        if constexpr (MmaTraits<T>::fmt == 1)
-          umma_bf16(d, ad, bd, idesc, acc);
-        else
-          umma_tf32(d, ad, bd, idesc, acc);
+        for (int k = 0; k < BK / UK; ++k) {
+          const uint64_t ad = umma_desc_sw128(abase + j * kATileBytes + k * 32);
+          const uint64_t bd = umma_desc_sw128(bbase + j * box_b + k * 32);
+          const uint32_t acc = (kbi > kb0 || j > 0 || k > 0) ? 1u : 0u;
+          if constexpr (MmaTraits<T>::fmt == 1)
+            umma_bf16(d, ad, bd, idesc, acc);
+          else
+            umma_tf32(d, ad, bd, idesc, acc);
+        }
       }
       umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
     }
@@ -196,14 +226,50 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
 }
 
 // ------------------------------------------------------------------ epilogue ops
+// Global operands an epilogue chunk reads (residual row values, the injection scale).  They are loaded before the chunk's accumulator is
+// ready -- for the first chunk while the MMAs still run -- so their latency is hidden.
+struct EpiOperands {
+  float a[16];  // RESID: resid values; INJECT: current x values
+  float b[16];  // INJECT: row scale r[tok]
+};
+
+template <typename T, int EPI>
+__device__ __forceinline__ void epi_load(const GemmArgs &p, int m_tile, int r, int tok0,
+                                         EpiOperands &op) {
+  switch (EPI) {
+    case EPI_RESID_F32:
+    case EPI_INJECT: {
+      const int s = seg_of_tile(p, m_tile);
+      const int row = (m_tile - p.seg[s].tile_begin) * kBM + r;
+      if (row >= p.seg[s].rows) break;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int tok = tok0 + jj;
+        if (tok < p.n_tokens) {
+          if (EPI == EPI_RESID_F32) {
+            op.a[jj] = p.resid[static_cast<size_t>(tok) * p.ld_resid + row];
+          } else {
+            op.a[jj] = p.out_f32[static_cast<size_t>(tok) * p.ld_out + row];
+            op.b[jj] = p.row_scale[tok];
+          }
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
 // Each op gets the fp32 values v[0..15] of tile row r (0..127) for token columns
 // tok0 .. tok0+15 and must call the same named barriers on all 128 threads.
-template <typename T>
-__device__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0, float (&v)[16],
-                          float *xbuf, float *red, int32_t *redi) {
+template <typename T, int EPI>
+__device__ __forceinline__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0,
+                                          float (&v)[16], const EpiOperands &op, float *xbuf,
+                                          float *red, int32_t *redi) {
   const int q = r >> 5;
   const int lane = r & 31;
-  switch (p.epi) {
+  switch (EPI) {
     case EPI_STORE_F32:
     case EPI_RESID_F32:
     case EPI_INJECT: {
@@ -215,12 +281,12 @@ __device__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0, float 
         const int tok = tok0 + jj;
         if (tok >= p.n_tokens) break;
         const size_t o = static_cast<size_t>(tok) * p.ld_out + row;
-        if (p.epi == EPI_STORE_F32) {
+        if (EPI == EPI_STORE_F32) {
           p.out_f32[o + p.seg[s].out_col] = v[jj];
-        } else if (p.epi == EPI_RESID_F32) {
-          p.out_f32[o] = p.resid[static_cast<size_t>(tok) * p.ld_resid + row] + v[jj];
+        } else if (EPI == EPI_RESID_F32) {
+          p.out_f32[o] = op.a[jj] + v[jj];
         } else if (tok % p.block_w != 0) {
-          p.out_f32[o] += p.row_scale[tok] * v[jj];
+          p.out_f32[o] = op.a[jj] + op.b[jj] * v[jj];
         }
       }
       break;
@@ -248,74 +314,6 @@ __device__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0, float 
         }
       }
       named_bar(2, 128);
-      break;
-    }
-    case EPI_HEADS: {
-      const int s = seg_of_tile(p, m_tile);
-      const GemmSeg &sg = p.seg[s];
-      const int D = p.head_dim;
-      const int row = (m_tile - sg.tile_begin) * kBM + r;
-      const int d = r % D;
-      const int head = row / D;
-      const bool normed = sg.kind != HK_V;
-      if (normed) {
-        // per-head RMSNorm over the D rows of the head, for each token column
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float ss = warp_sum(v[jj] * v[jj]);
-          if (lane == 0) red[q * 16 + jj] = ss;
-        }
-        named_bar(2, 128);
-        const float gain = to_f<T>(static_cast<const T *>(sg.norm)[d]);
-        const int q0 = (D == 128) ? 0 : (q & 2);
-        const int nq = D / 32;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          float ss = 0.f;
-          for (int k = 0; k < nq; ++k) ss += red[(q0 + k) * 16 + jj];
-          v[jj] = v[jj] * rsqrtf(ss / D + p.eps) * gain;
-          xbuf[r * kXStride + jj] = v[jj];
-        }
-        named_bar(2, 128);
-        // split-half rotation with the partner row of the same head
-        const int half = D / 2;
-        const int pr = d < half ? r + half : r - half;
-        const int j = d % half;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int tok = tok0 + jj;
-          if (tok >= p.n_tokens) break;
-          const float2 cs = p.rope[static_cast<size_t>(tok) * half + j];
-          const float pv = xbuf[pr * kXStride + jj];
-          v[jj] = d < half ? v[jj] * cs.x - pv * cs.y : v[jj] * cs.x + pv * cs.y;
-        }
-        named_bar(2, 128);
-      }
-      if (row >= sg.rows) break;
-      T *dst = static_cast<T *>(sg.dst);
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int tok = tok0 + jj;
-        if (tok >= p.n_tokens) break;
-        size_t o;
-        if (sg.dst_mode == HD_TOKEN_MAJOR) {
-          o = static_cast<size_t>(tok) * sg.ld + row;
-        } else if (sg.dst_mode == HD_BLOCK) {
-          const int b = tok / p.block_w, i = tok % p.block_w;
-          o = ((static_cast<size_t>(b) * p.n_kv_heads + head) * p.block_w + i) * D + d;
-        } else {
-          const int req = p.row_req[tok];
-          const long long pos = p.row_pos[tok];
-          if (req < 0 || req >= p.n_req || pos < 0) {
-            atomicOr(&g_error_word, DEVERR_BAD_INDEX);
-            continue;
-          }
-          const long long F = p.frontier[req];
-          if (pos < F - sg.cap || pos >= F) continue;  // outside the final live window
-          o = ((static_cast<size_t>(req) * p.n_kv_heads + head) * sg.cap + pos % sg.cap) * D + d;
-        }
-        dst[o] = from_f<T>(v[jj]);
-      }
       break;
     }
     case EPI_ARGMAX: {
@@ -365,7 +363,7 @@ __device__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0, float 
 }
 
 // ------------------------------------------------------------------ epilogue
-template <typename T>
+template <typename T, int EPI>
 __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
                               uint32_t tmem_base, long long u0, long long u1, float *xbuf,
                               float *red, int32_t *redi, volatile int *sflag,
@@ -385,6 +383,9 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
     const int a = e & 1;
     const uint32_t ra = static_cast<uint32_t>(e >> 1);
     ++e;
+    const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
+    EpiOperands op;
+    epi_load<T, EPI>(p, m_tile, r, n_tile * p.block_n, op);
     if (*sabort || !mbar_wait(&accf[a], ra & 1u)) {
       *sabort = 1;
       return;
@@ -393,7 +394,6 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                            static_cast<uint32_t>(a * p.block_n);
     const bool whole = (kb0 == 0 && kb1 == p.kb);
-    const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
     int c_first = cta, c_last = cta;
     if (!whole) {
       const int slot = (tile == first_tile) ? 0 : 1;
@@ -429,25 +429,37 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
       float v[16];
       tmem_ld16(tbase + j0, v);
       if (!whole) {
+        // Sum the contributors' partial tiles in CTA order (deterministic).  Loads of two
+        // contributors are issued before they are added so their L2 latencies overlap.
         float acc[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
-        for (int c = c_first; c <= c_last; ++c) {
-          if (c == cta) {
+        for (int c0 = c_first; c0 <= c_last; c0 += 2) {
+          float part[2][16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] += v[jj];
-          } else {
+          for (int u = 0; u < 2; ++u) {
+            const int c = c0 + u;
+            if (c > c_last || c == cta) continue;
             const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
-            const float *o =
-                p.partials + (static_cast<size_t>(c) * 2 + cslot) * p.block_n * kBM;
+            const float *o = p.partials + (static_cast<size_t>(c) * 2 + cslot) * p.block_n * kBM +
+                             static_cast<size_t>(j0) * kBM + r;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] += __ldcg(o + (j0 + jj) * kBM + r);
+            for (int jj = 0; jj < 16; ++jj) part[u][jj] = __ldcg(o + jj * kBM);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = c0 + u;
+            if (c > c_last) break;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) acc[jj] += (c == cta) ? v[jj] : part[u][jj];
           }
         }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) v[jj] = acc[jj];
       }
-      epi_chunk<T>(p, m_tile, r, n_tile * p.block_n + j0, v, xbuf, red, redi);
+      EpiOperands cur = op;
+      if (j0 + 16 < p.block_n) epi_load<T, EPI>(p, m_tile, r, n_tile * p.block_n + j0 + 16, op);
+      epi_chunk<T, EPI>(p, m_tile, r, n_tile * p.block_n + j0, v, cur, xbuf, red, redi);
     }
     tc_fence_before();
     mbar_arrive(&acce[a]);
@@ -455,13 +467,16 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
 }
 
 // ------------------------------------------------------------------ kernel
-template <typename T>
+// One instantiation per (element type, epilogue): each kernel carries only the code of
+// its own epilogue, which keeps the once-per-tile epilogue path small in the instruction
+// cache.
+template <typename T, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout(p.stages, p.block_n);
+  const SmemLayout L = smem_layout(p.stages, p.block_n, p.kbox);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
   float *xbuf = reinterpret_cast<float *>(smem + L.off_x);
@@ -515,7 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) gemm_mma<T>(p, sA, sB, full, empty, accf, acce, tmem_base, u0, u1, sabort);
     __syncwarp();
   } else {
-    gemm_epilogue<T>(p, accf, acce, tmem_base, u0, u1, xbuf, red, redi, sflag, sabort);
+    gemm_epilogue<T, EPI>(p, accf, acce, tmem_base, u0, u1, xbuf, red, redi, sflag, sabort);
   }
   tc_fence_before();
   __syncthreads();
@@ -623,23 +638,48 @@ size_t gemm_partial_floats(int n_ctas, int block_n) {
   return static_cast<size_t>(n_ctas) * 2 * block_n * kBM;
 }
 
-static int pick_stages(int block_n) {
+static int pick_stages(int block_n, int kbox) {
   for (int s = kMaxStages; s >= 2; --s)
-    if (smem_layout(s, block_n).total <= kSmemLimit) return s;
+    if (smem_layout(s, block_n, kbox).total <= kSmemLimit) return s;
   return 2;
 }
 
-template <typename T>
-static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStream_t stream) {
+// K boxes per stage: 4 (512-byte row pieces) unless that leaves fewer than 3 stages.
+static int pick_kbox(int block_n, int K, int BK) {
+  int kb = 4;
+  if (const char *e = getenv("BD_GEMM_KBOX")) {
+    const int v = atoi(e);
+    if (v == 1 || v == 2 || v == 4) kb = v;
+  }
+  while (kb > 1 && (pick_stages(block_n, kb) < 3 || K < kb * BK * 2)) kb >>= 1;
+  return kb;
+}
+
+template <typename T, int EPI>
+static cudaError_t launch_epi(const GemmMaps &maps, const GemmArgs &a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<T, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const size_t smem = smem_layout(a.stages, a.block_n).total;
-  return launch_pdl(gemm_kernel<T>, dim3(a.n_ctas), dim3(kGemmThreads), smem, stream, maps, a);
+  const size_t smem = smem_layout(a.stages, a.block_n, a.kbox).total;
+  return launch_pdl(gemm_kernel<T, EPI>, dim3(a.n_ctas), dim3(kGemmThreads), smem, stream, maps,
+                    a);
+}
+
+template <typename T>
+static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStream_t stream) {
+  switch (a.epi) {
+    case EPI_STORE_F32: return launch_epi<T, EPI_STORE_F32>(maps, a, stream);
+    case EPI_RESID_F32: return launch_epi<T, EPI_RESID_F32>(maps, a, stream);
+    case EPI_INJECT: return launch_epi<T, EPI_INJECT>(maps, a, stream);
+    case EPI_SWIGLU: return launch_epi<T, EPI_SWIGLU>(maps, a, stream);
+    case EPI_ARGMAX: return launch_epi<T, EPI_ARGMAX>(maps, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stream) {
@@ -652,7 +692,8 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   a.block_n = gemm_block_n(plan.n_tokens);
   a.n_tiles_n = (plan.n_tokens + a.block_n - 1) / a.block_n;
   a.pair_mode = plan.pair_mode ? 1 : 0;
-  a.kb = (plan.K + BK - 1) / BK;
+  a.kbox = pick_kbox(a.block_n, plan.K, BK);
+  a.kb = (plan.K + BK * a.kbox - 1) / (BK * a.kbox);
   int m_tiles = 0;
   if (plan.pair_mode) {
     if (plan.n_w != 2 || plan.w[0].rows != plan.w[1].rows) return "pair GEMM needs two equal matrices";
@@ -671,8 +712,12 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   a.m_tiles = m_tiles;
   const long long tiles = static_cast<long long>(m_tiles) * a.n_tiles_n;
   a.units = tiles * a.kb;
-  a.n_ctas = static_cast<int>(a.units < num_sms() ? a.units : num_sms());
-  a.stages = pick_stages(a.block_n);
+  // Every CTA streams at least kMinUnits k-blocks (128 KB of weights): small matrices
+  // use fewer CTAs instead of many tiny partial tiles.
+  const long long min_units = (kMinUnits + a.kbox - 1) / a.kbox;
+  const long long by_units = (a.units + min_units - 1) / min_units;
+  a.n_ctas = static_cast<int>(by_units < num_sms() ? by_units : num_sms());
+  a.stages = pick_stages(a.block_n, a.kbox);
   a.partials = sc.partials;
   a.counters = sc.counters;
   if (gemm_partial_floats(a.n_ctas, a.block_n) > sc.partial_floats) return "GEMM partial scratch too small";

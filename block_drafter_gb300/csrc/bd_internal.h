@@ -26,39 +26,28 @@ enum EpiMode : int {
   EPI_RESID_F32 = 1,  // out[tok*ld + row] = resid[tok*ld_resid + row] + acc
   EPI_INJECT = 2,     // x[tok*ld + row] += scale[tok] * acc for non-anchor rows
   EPI_SWIGLU = 3,     // pair tiles: out[tok*ld_act + f] = SiLU(gate_f) * up_f
-  EPI_HEADS = 4,      // per-head RMSNorm + split-half RoPE (Q/K), plain (V); scatter
-  EPI_ARGMAX = 5      // per-tile (max, lowest argmax) over 128 vocabulary rows
+  EPI_ARGMAX = 4      // per-tile (max, lowest argmax) over 128 vocabulary rows
 };
-enum HeadKind : int { HK_Q = 0, HK_K = 1, HK_V = 2 };
-enum HeadDst : int { HD_TOKEN_MAJOR = 0, HD_BLOCK = 1, HD_RING = 2 };
 
+// Epilogue code runs once per tile, so it is kept short: the instruction fetches of
+// long straight-line epilogues dominated the tail of small launches.
 struct GemmSeg {
   int rows;          // output rows of this weight matrix
   int tile_begin;    // first m-tile of the segment
   int out_col;       // EPI_STORE_F32: column offset of this segment in the output row
-  int kind;          // EPI_HEADS: HeadKind
-  int dst_mode;      // EPI_HEADS: HeadDst
-  int ld;            // EPI_HEADS token-major: row stride of dst
-  int cap;           // EPI_HEADS ring: ring capacity
   int pad_;
-  const void *norm;  // EPI_HEADS: per-head gain [D] (Q/K)
-  void *dst;         // EPI_HEADS: destination base (config dtype)
 };
 
-struct GemmArgs {
+struct __align__(16) GemmArgs {
   int K, n_tokens, block_n, n_tiles_n, m_tiles, kb, n_ctas, n_segs, stages, pair_mode;
+  int kbox;                       // 128-byte-wide K boxes per pipeline stage (1, 2 or 4)
   long long units;
   int epi;
-  int ld_out, ld_resid, ld_act, block_w, head_dim, n_kv_heads, vocab, n_req;
-  float eps;
+  int ld_out, ld_resid, ld_act, block_w, vocab;
   float *out_f32;
   const float *resid;
   const float *row_scale;
   void *out_act;
-  const float2 *rope;             // [n_tokens][D/2] (cos, sin)
-  const int32_t *row_req;         // ring mode: request of each token row
-  const int64_t *row_pos;         // ring mode: absolute position of each token row
-  const int64_t *frontier;        // ring mode: context frontier after the call, per request
   float *amax_val;                // [m_tiles][n_tokens]
   int32_t *amax_idx;
   float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
@@ -109,6 +98,8 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &scratch, cudaStream_t
 // ------------------------------------------------------------------ launch helper
 // Launch with programmatic stream serialisation (PDL) so the next kernel's prologue can
 // overlap this kernel's tail; every kernel calls pdl_wait() before dependent accesses.
+void count_launch();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args &&...args) {
@@ -122,6 +113,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

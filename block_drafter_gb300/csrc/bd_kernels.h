@@ -5,6 +5,8 @@
 
 #include <string>
 
+#include "bd_internal.h"
+
 namespace bd {
 
 struct AttArgs {
@@ -56,6 +58,33 @@ std::string launch_code(int dtype, const float *z, int rows, int Rc, const void 
 // m_i = sigmoid(G c_i + G_p c_{i-1} + b) * (A c_{i-1}) for i >= 1, m_0 = 0.
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias,
                            int W, void *m_out, cudaStream_t s);
+// Head post-processing of raw fp32 projections [rows, ld_raw]: for each head of each
+// segment, plain_head_rmsnorm + split-half RoPE (query/key segments) or a copy (value
+// segments), rounded to the config dtype and scattered to its destination.
+enum HeadKind : int { HK_Q = 0, HK_K = 1, HK_V = 2 };
+enum HeadDst : int {
+  HD_TOKEN_MAJOR = 0,  // dst[row * ld + head * D + d]
+  HD_BLOCK = 1,        // dst[((b * Hkv + head) * W + i) * D + d], row = b * W + i
+  HD_RING = 2          // dst[((req * Hkv + head) * cap + pos % cap) * D + d] if pos is live
+};
+constexpr int kMaxHeadSegs = 32;
+struct HeadSeg {
+  int kind, dst_mode, col0, n_heads, ld, cap;
+  const void *norm;  // [D] gain (query/key segments)
+  void *dst;
+};
+struct HeadPostArgs {
+  const float *raw;
+  int ld_raw, rows, D, n_kv_heads, W, n_req, n_segs, total_heads;
+  float eps;
+  const float2 *rope;        // [rows][D/2]
+  const int32_t *row_req;    // ring mode
+  const int64_t *row_pos;
+  const int64_t *frontier;
+  HeadSeg seg[kMaxHeadSegs];
+};
+std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);
+
 // Per-row argmax over per-tile (max, lowest argmax) pairs; lowest id on ties.
 std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_tiles, int rows,
                                  int32_t *tok_out, float *max_out, cudaStream_t s);

@@ -62,39 +62,155 @@ __global__ void rope_table_kernel(const int64_t *pos, int n, float2 *rope, int h
   }
 }
 
+template <typename T> __device__ __forceinline__ float4 load4(const T *p, int i4);
+template <> __device__ __forceinline__ float4 load4<float>(const float *p, int i4) {
+  return reinterpret_cast<const float4 *>(p)[i4];
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p, int i4) {
+  const uint2 u = reinterpret_cast<const uint2 *>(p)[i4];
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+template <typename T> __device__ __forceinline__ void store4(T *p, int i4, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float *p, int i4, float4 v) {
+  reinterpret_cast<float4 *>(p)[i4] = v;
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, int i4, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&b);
+  reinterpret_cast<uint2 *>(p)[i4] = u;
+}
+
+// One CTA per row.  Rows up to kNormVec * 4 * blockDim elements stay in registers between
+// the sum-of-squares and the output pass (float4 loads, all issued before the reduction).
+constexpr int kNormVec = 8;
+
 template <typename T>
-__global__ void rownorm_kernel(const float *x, int H, const T *gain, float eps, int mode, T *out,
-                               float *r_out, float *f32_out, T *head_out, int W) {
+__global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, const T *gain,
+                                                      float eps, int mode, T *out, float *r_out,
+                                                      float *f32_out, T *head_out, int W) {
   __shared__ float red[32];
   const int row = blockIdx.x;
   pdl_wait();
   pdl_trigger();
   const float *xr = x + static_cast<size_t>(row) * H;
+  const int H4 = H / 4;
+  float4 xv[kNormVec];
   float ss = 0.f;
-  for (int h = threadIdx.x; h < H; h += blockDim.x) ss += xr[h] * xr[h];
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i4 = threadIdx.x + k * blockDim.x;
+    xv[k] = i4 < H4 ? reinterpret_cast<const float4 *>(xr)[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k)
+    ss += xv[k].x * xv[k].x + xv[k].y * xv[k].y + xv[k].z * xv[k].z + xv[k].w * xv[k].w;
+  for (int i4 = threadIdx.x + kNormVec * blockDim.x; i4 < H4; i4 += blockDim.x) {
+    const float4 t = reinterpret_cast<const float4 *>(xr)[i4];
+    ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+  }
   ss = block_sum(ss, red);
+  float scale;
   if (mode == NORM_BRIDGE) {
     const float r = sqrtf(ss / H);
-    const float s = 1.f / (r + eps);
-    for (int h = threadIdx.x; h < H; h += blockDim.x)
-      out[static_cast<size_t>(row) * H + h] = from_f<T>(xr[h] * s);
+    scale = 1.f / (r + eps);
     if (threadIdx.x == 0) r_out[row] = r;
-    return;
+  } else {
+    scale = rsqrtf(ss / H + eps);
   }
-  const float inv = rsqrtf(ss / H + eps);
   const int i = row % W;
+  T *orow = (mode == NORM_FINAL) ? nullptr : out + static_cast<size_t>(row) * H;
   T *hrow = nullptr;
   if (mode == NORM_FINAL && head_out != nullptr && i > 0)
     hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    const float y = to_f<T>(gain[h]) * xr[h] * inv;
-    if (mode == NORM_PLAIN) {
-      out[static_cast<size_t>(row) * H + h] = from_f<T>(y);
-    } else {
-      if (f32_out) f32_out[static_cast<size_t>(row) * H + h] = y;
-      if (hrow) hrow[h] = from_f<T>(y);
+  float *frow = (mode == NORM_FINAL && f32_out) ? f32_out + static_cast<size_t>(row) * H : nullptr;
+  auto emit = [&](int i4, float4 t) {
+    float4 y = make_float4(t.x * scale, t.y * scale, t.z * scale, t.w * scale);
+    if (mode != NORM_BRIDGE) {
+      const float4 g = load4<T>(gain, i4);
+      y.x *= g.x;
+      y.y *= g.y;
+      y.z *= g.z;
+      y.w *= g.w;
+    }
+    if (orow) store4<T>(orow, i4, y);
+    if (hrow) store4<T>(hrow, i4, y);
+    if (frow) reinterpret_cast<float4 *>(frow)[i4] = y;
+  };
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i4 = threadIdx.x + k * blockDim.x;
+    if (i4 < H4) emit(i4, xv[k]);
+  }
+  for (int i4 = threadIdx.x + kNormVec * blockDim.x; i4 < H4; i4 += blockDim.x)
+    emit(i4, reinterpret_cast<const float4 *>(xr)[i4]);
+}
+
+// One warp per (row, head).  Lane l holds elements [l*E, l*E + E) of the head (E = D/32);
+// the split-half RoPE partner of element d is d +- D/2, which lives in lane l ^ 16.
+template <typename T, int E>
+__global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ HeadPostArgs a) {
+  const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  const int row = warp / a.total_heads;
+  int hg = warp % a.total_heads;
+  if (row >= a.rows) return;
+  int si = 0;
+  while (si + 1 < a.n_segs && hg >= a.seg[si].n_heads) {
+    hg -= a.seg[si].n_heads;
+    ++si;
+  }
+  const HeadSeg sg = a.seg[si];
+  const int D = E * 32, half = D / 2;
+  const int d0 = lane * E;
+  const float *src = a.raw + static_cast<size_t>(row) * a.ld_raw + sg.col0 + hg * D + d0;
+  float v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = src[e];
+  if (sg.kind != HK_V) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss += v[e] * v[e];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
+    const T *gain = static_cast<const T *>(sg.norm);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] *= inv * to_f<T>(gain[d0 + e]);
+    const float2 *cs = a.rope + static_cast<size_t>(row) * half;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float pv = __shfl_xor_sync(0xffffffffu, v[e], 16);
+      const int d = d0 + e;
+      const float2 c = cs[d % half];
+      v[e] = d < half ? v[e] * c.x - pv * c.y : v[e] * c.x + pv * c.y;
     }
   }
+  size_t o;
+  if (sg.dst_mode == HD_TOKEN_MAJOR) {
+    o = static_cast<size_t>(row) * sg.ld + hg * D;
+  } else if (sg.dst_mode == HD_BLOCK) {
+    const int b = row / a.W, i = row % a.W;
+    o = ((static_cast<size_t>(b) * a.n_kv_heads + hg) * a.W + i) * D;
+  } else {
+    const int req = a.row_req[row];
+    const long long pos = a.row_pos[row];
+    if (req < 0 || req >= a.n_req || pos < 0) {
+      if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      return;
+    }
+    const long long F = a.frontier[req];
+    if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
+    o = ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D;
+  }
+  T *dst = static_cast<T *>(sg.dst) + o + d0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = from_f<T>(v[e]);
 }
 
 template <typename T>
@@ -237,6 +353,19 @@ std::string launch_rownorm(int dtype, const float *x, int rows, int H, const voi
                    static_cast<const float *>(gain), eps, mode, static_cast<float *>(out), r_out,
                    f32_out, static_cast<float *>(head_out), W);
   return err("rownorm", e);
+}
+
+std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
+  const long long warps = static_cast<long long>(a.rows) * a.total_heads;
+  const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
+  cudaError_t e;
+  if (a.D == 128)
+    e = dtype == 0 ? launch_pdl(head_post_kernel<__nv_bfloat16, 4>, grid, dim3(256), 0, s, a)
+                   : launch_pdl(head_post_kernel<float, 4>, grid, dim3(256), 0, s, a);
+  else
+    e = dtype == 0 ? launch_pdl(head_post_kernel<__nv_bfloat16, 2>, grid, dim3(256), 0, s, a)
+                   : launch_pdl(head_post_kernel<float, 2>, grid, dim3(256), 0, s, a);
+  return err("head post", e);
 }
 
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,

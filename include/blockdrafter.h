@@ -190,6 +190,10 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const voi
                             int rows, int32_t *token_out, float *max_logit_out,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/* Number of kernels this library has enqueued (all threads) since it was loaded.
+ * Graph replays do not pass through the library and are not counted. */
+uint64_t bd_kernel_launches(void);
+
 /* Thread-local description of the last non-OK status returned on this thread. */
 const char *bd_last_error(void);
 

@@ -176,7 +176,7 @@ struct RoundWs {
   void *xn, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
 size_t round_max_tiles(const bd_config *c, int T) {
-  const int ntn = (T + gemm_block_n(T) - 1) / gemm_block_n(T);
+  const int ntn = (T + gemm_block_n(T) - 1) / gemm_block_n(T);  // 1 for T <= 128
   size_t t = tiles_of(c->n_q_heads * c->head_dim, 128) + 2 * tiles_of(c->n_kv_heads * c->head_dim, 128);
   t = std::max(t, tiles_of(c->hidden, 128));
   t = std::max(t, tiles_of(c->ffn, 64));
@@ -186,19 +186,23 @@ size_t round_max_tiles(const bd_config *c, int T) {
   }
   return t * ntn;
 }
+int pad16(int n) { return (n + 15) / 16 * 16; }
+
+// Activation buffers of the bf16 path hold a hi/lo pair: [2][pad16(T)][K] (hi block, then
+// the lo block); q and the block K/V hold [2][T][...].
 void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sms) {
-  const int T = B * W;
+  const int T = B * W, TP = pad16(T);
   const int e = elem_bytes(c);
   const int H = c->hidden, QD = c->n_q_heads * c->head_dim, KD = c->n_kv_heads * c->head_dim;
-  carve_gemm(cv, w.g, gemm_block_n(T), round_max_tiles(c, T), sms);
+  carve_gemm(cv, w.g, 2 * TP, round_max_tiles(c, T), sms);
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
   w.qkv_raw = cv.take<float>(static_cast<size_t>(T) * (QD + 2 * KD));
-  w.xn = cv.take<char>(static_cast<size_t>(T) * H * e);
-  w.q = cv.take<char>(static_cast<size_t>(T) * QD * e);
-  w.kblk = cv.take<char>(static_cast<size_t>(T) * KD * e);
-  w.vblk = cv.take<char>(static_cast<size_t>(T) * KD * e);
-  w.att = cv.take<char>(static_cast<size_t>(T) * QD * e);
-  w.hmid = cv.take<char>(static_cast<size_t>(T) * c->ffn * e);
+  w.xn = cv.take<char>(static_cast<size_t>(2 * TP) * H * e);
+  w.q = cv.take<char>(static_cast<size_t>(2 * T) * QD * e);
+  w.kblk = cv.take<char>(static_cast<size_t>(2 * T) * KD * e);
+  w.vblk = cv.take<char>(static_cast<size_t>(2 * T) * KD * e);
+  w.att = cv.take<char>(static_cast<size_t>(2 * TP) * QD * e);
+  w.hmid = cv.take<char>(static_cast<size_t>(2 * TP) * c->ffn * e);
   w.rope = cv.take<float2>(static_cast<size_t>(T) * (c->head_dim / 2));
   size_t po = 0, pm = 0;
   for (int l = 0; l < c->n_layers; ++l) {
@@ -211,9 +215,9 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sm
   if (c->code_width > 0) {
     w.r = cv.take<float>(T);
     w.z = cv.take<float>(static_cast<size_t>(T) * c->code_width);
-    w.c = cv.take<char>(static_cast<size_t>(T) * c->code_width * e);
+    w.c = cv.take<char>(static_cast<size_t>(2 * TP) * c->code_width * e);
     w.pre = cv.take<float>(static_cast<size_t>(T) * 3 * c->msg_width);
-    w.m = cv.take<char>(static_cast<size_t>(T) * c->msg_width * e);
+    w.m = cv.take<char>(static_cast<size_t>(2 * TP) * c->msg_width * e);
   } else {
     w.r = w.z = w.pre = nullptr;
     w.c = w.m = nullptr;
@@ -245,11 +249,13 @@ struct HeadWs {
   GemmWs g;
   float *amax_val;
   int32_t *amax_idx;
+  void *hl;  // bf16 hi/lo pair of the hidden rows [2][pad16(rows)][H]
 };
 void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   const size_t m_tiles = tiles_of(c->vocab, 128);
-  const int bn = gemm_block_n(rows);
-  carve_gemm(cv, w.g, bn, m_tiles * ((rows + bn - 1) / bn), sms);
+  const int bn = 2 * pad16(rows);
+  carve_gemm(cv, w.g, bn, m_tiles, sms);
+  w.hl = cv.take<char>(static_cast<size_t>(2 * pad16(rows)) * c->hidden * 2);
   w.amax_val = cv.take<float>(m_tiles * rows);
   w.amax_idx = cv.take<int32_t>(m_tiles * rows);
 }
@@ -347,7 +353,7 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
     p.args.ld_out = H;
     BD_TRY(launch_gemm(p, sc, s));
     BD_TRY(launch_rownorm(cfg->dtype, mw.feat, n_rows, H, w->context_norm, cfg->eps, NORM_PLAIN,
-                          mw.cmat, nullptr, nullptr, nullptr, 1, s));
+                          mw.cmat, nullptr, nullptr, nullptr, 1, 0, s));
   }
   // S2: every layer's raw context K and V (fp32), then head norm + RoPE + ring scatter
   const int ldkv = cfg->n_layers * 2 * KD;
@@ -405,7 +411,7 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
 
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B, int n_masks,
-                         void *head_in, float *hidden_out, float *layers_out, void *workspace,
+                         float *head_in, float *hidden_out, float *layers_out, void *workspace,
                          size_t workspace_bytes, void *stream_) {
   std::string e = check_config(cfg);
   if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
@@ -417,7 +423,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   if (!head_in || !aligned16(head_in)) return fail(BD_ERR_INVALID_ARG, "head_in NULL or misaligned");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
-  const int W = n_masks + 1, T = B * W;
+  const int W = n_masks + 1, T = B * W, TP = pad16(T);
   const int G = cfg->n_q_heads / cfg->n_kv_heads;
   if (cfg->dtype == BD_BF16 && G * W > attention_rows_max())
     return fail(BD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*(n_masks+1) must be <= 64");
@@ -437,6 +443,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const RopeFreq freq = rope_freq(cfg);
   const GemmScratch sc = scratch_of(rw.g);
   const int dt = cfg->dtype;
+  const bool split = dt == BD_BF16;  // bf16 activations enter the GEMMs as hi+lo pairs
+  auto lo = [&](int K) -> size_t { return split ? static_cast<size_t>(TP) * K : 0; };
 
   BD_TRY(memset_counters(rw.g, s));
   // S3: block input rows and the RoPE table of positions F_b + i
@@ -446,9 +454,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     const bd_layer_weights &L = w->layer[l];
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
-                          nullptr, nullptr, W, s));
+                          nullptr, nullptr, W, lo(H), s));
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
+      p.split = split;
       add_w(p, L.wq, QD);
       add_w(p, L.wk, KD);
       add_w(p, L.wv, KD);
@@ -470,9 +479,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       h.eps = cfg->eps;
       h.rope = rw.rope;
       h.n_segs = 3;
-      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q};
-      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk};
-      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk};
+      const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
+      const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
+      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo};
+      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo};
+      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo};
       h.total_heads = cfg->n_q_heads + 2 * cfg->n_kv_heads;
       BD_TRY(launch_head_post(dt, h, s));
     }
@@ -499,11 +510,15 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
       a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
       a.max_keys = att_max_keys(cfg, l, W);
+      a.q_lo = split ? static_cast<size_t>(T) * QD : 0;
+      a.blk_lo = split ? static_cast<size_t>(T) * KD : 0;
+      a.out_lo = lo(QD);
       BD_TRY(launch_attention(a, dt, s));
     }
     // S6: y = x + W_o a (in place)
     {
       GemmPlan p = make_plan(cfg, rw.att, T, QD);
+      p.split = split;
       add_w(p, L.wo, H);
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
@@ -514,19 +529,22 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     }
     // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m)
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.post_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
-                          nullptr, nullptr, W, s));
+                          nullptr, nullptr, W, lo(H), s));
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
+      p.split = split;
       add_w(p, L.w_gate, cfg->ffn);
       add_w(p, L.w_up, cfg->ffn);
       p.pair_mode = true;
       p.args.epi = EPI_SWIGLU;
       p.args.out_act = rw.hmid;
       p.args.ld_act = cfg->ffn;
+      p.args.act_lo = static_cast<long long>(lo(cfg->ffn));
       BD_TRY(launch_gemm(p, sc, s));
     }
     {
       GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
+      p.split = split;
       add_w(p, L.w_down, H);
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
@@ -539,19 +557,22 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       const int Rc = cfg->code_width, Mc = cfg->msg_width;
       // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
       BD_TRY(launch_rownorm(dt, rw.x, T, H, nullptr, cfg->eps, NORM_BRIDGE, rw.xn, rw.r, nullptr,
-                            nullptr, W, s));
+                            nullptr, W, lo(H), s));
       {
         GemmPlan p = make_plan(cfg, rw.xn, T, H);
+        p.split = split;
         add_w(p, L.r_read, Rc);
         p.args.epi = EPI_STORE_F32;
         p.args.out_f32 = rw.z;
         p.args.ld_out = Rc;
         BD_TRY(launch_gemm(p, sc, s));
       }
-      BD_TRY(launch_code(dt, rw.z, T, Rc, w->codebook, anchor_ids, cfg->vocab, W, cfg->eps, rw.c, s));
+      BD_TRY(launch_code(dt, rw.z, T, Rc, w->codebook, anchor_ids, cfg->vocab, W, cfg->eps, rw.c,
+                         lo(Rc), s));
       // S9: [G c; G_p c; A c] in one launch, gate/message, then the RMS-scaled write
       {
         GemmPlan p = make_plan(cfg, rw.c, T, Rc);
+        p.split = split;
         add_w(p, w->g_recv, Mc);
         add_w(p, w->g_pred, Mc);
         add_w(p, w->a_val, Mc);
@@ -563,9 +584,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         p.args.seg[2].out_col = 2 * Mc;
         BD_TRY(launch_gemm(p, sc, s));
       }
-      BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, s));
+      BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, lo(Mc), s));
       {
         GemmPlan p = make_plan(cfg, rw.m, T, Mc);
+        p.split = split;
         add_w(p, L.w_write, H);
         p.args.epi = EPI_INJECT;
         p.args.out_f32 = rw.x;
@@ -580,11 +602,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
                              static_cast<size_t>(T) * H, s));
   }
   BD_TRY(launch_rownorm(dt, rw.x, T, H, w->final_norm, cfg->eps, NORM_FINAL, nullptr, nullptr,
-                        hidden_out, head_in, W, s));
+                        hidden_out, head_in, W, 0, s));
   return BD_OK;
 }
 
-bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const void *hidden, int rows,
+bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
                             int32_t *token_out, float *max_logit_out, void *workspace,
                             size_t workspace_bytes, void *stream_) {
   std::string e = check_config(cfg);
@@ -603,7 +625,12 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const voi
   carve_head(cv, hw, cfg, rows, num_sms());
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
   BD_TRY(memset_counters(hw.g, s));
-  GemmPlan p = make_plan(cfg, hidden, rows, cfg->hidden);
+  const bool split = cfg->dtype == BD_BF16;
+  if (split)  // bf16 hi/lo pair of the fp32 hidden rows: the head sees ~16 mantissa bits
+    BD_TRY(launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hw.hl,
+                             static_cast<size_t>(pad16(rows)) * cfg->hidden, s));
+  GemmPlan p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
+  p.split = split;
   add_w(p, w->embed_head, cfg->vocab);
   p.args.epi = EPI_ARGMAX;
   p.args.amax_val = hw.amax_val;

@@ -63,9 +63,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 struct AttGeom {
   long long F;
-  int p_lo, n_ctx, n_keys, k_begin, k_end;
+  int p_lo, n_ctx, k_begin, k_end;
 };
 
+// Context keys [p_lo, F) of request b (the window's oldest visible position, clipped to
+// the ring's live interval) are split into n_splits chunks of whole 64-key blocks.
 __device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b, int split) {
   AttGeom g;
   g.F = a.frontier[b];
@@ -73,34 +75,84 @@ __device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b, int split) 
   if (g.F - a.cap > lo) lo = g.F - a.cap;  // the ring holds [F - cap, F)
   if (lo < 0) lo = 0;
   g.p_lo = static_cast<int>(lo);
-  g.n_ctx = static_cast<int>(g.F - lo);
-  g.n_keys = g.n_ctx + a.W;
-  int chunk = (g.n_keys + a.n_splits - 1) / a.n_splits;
+  g.n_ctx = g.F > lo ? static_cast<int>(g.F - lo) : 0;
+  int chunk = (g.n_ctx + a.n_splits - 1) / a.n_splits;
   chunk = (chunk + kAttKeys - 1) / kAttKeys * kAttKeys;
-  g.k_begin = split * chunk;
-  g.k_end = min(g.n_keys, g.k_begin + chunk);
+  g.k_begin = min(g.n_ctx, split * chunk);
+  g.k_end = min(g.n_ctx, g.k_begin + chunk);
   return g;
 }
 
-// Is key k (0-based over [context; block]) visible from block row i?
-__device__ __forceinline__ bool att_visible(const AttArgs &a, const AttGeom &g, int i, int k) {
+// Is context key k (0-based from p_lo) visible from block row i?
+__device__ __forceinline__ bool ctx_visible(const AttArgs &a, const AttGeom &g, int i, int k) {
   if (k >= g.k_end) return false;
-  if (k < g.n_ctx) {
-    const long long p = g.p_lo + k;
-    return a.window <= 0 || (g.F + i) - p < a.window;
-  }
-  const int j = k - g.n_ctx;
+  const long long p = g.p_lo + k;
+  return a.window <= 0 || (g.F + i) - p < a.window;
+}
+// Is block key j visible from block row i?
+__device__ __forceinline__ bool blk_visible(const AttArgs &a, int i, int j) {
+  if (j >= a.W) return false;
   if (a.window > 0 && abs(j - i) >= a.window) return false;
   return !a.causal || j <= i;
 }
 
+// hi/lo split of a probability pair for the bf16 A operand of P.V
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// Online-softmax update of one warp's 16 rows for a tile of NT*8 keys (scores already
+// scaled to log2 units and masked with -inf); returns the probabilities in s.
+template <int NT>
+__device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)[2],
+                                               float (&l_run)[2], float (&alpha)[2]) {
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+    const float m_new = fmaxf(m_run[hr], mx[hr]);
+    alpha[hr] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[hr] - m_new);
+    m_run[hr] = m_new;
+  }
+  float ls[2] = {0.f, 0.f};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int hr = e >> 1;
+      const float pv = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m_run[hr]);
+      s[nt][e] = pv;
+      ls[hr] += pv;
+    }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 1);
+    ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 2);
+    l_run[hr] = l_run[hr] * alpha[hr] + ls[hr];
+  }
+}
+
+// bf16 tensor-core path.  Q and the softmax probabilities P enter the MMAs as hi+lo bf16
+// pairs (fp32 accumulate), so their rounding does not reach the output; the ring's K/V
+// are exact bf16 data.  The block's own keys/values (produced this round, hi+lo) are
+// processed by the last split in a separate 16-key pass.
 template <int D>
-__global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
+__global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_constant__ AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int RS = D + kAttPad;  // smem row stride (elements)
-  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
-  __nv_bfloat16 *sK = sQ + kAttRows * RS;               // [2][kAttKeys][RS]
-  __nv_bfloat16 *sV = sK + 2 * kAttKeys * RS;           // [2][kAttKeys][RS]
+  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [2][64][RS] hi, lo
+  __nv_bfloat16 *sK = sQ + 2 * kAttRows * RS;                          // [2][64][RS]
+  __nv_bfloat16 *sV = sK + 2 * kAttKeys * RS;                          // [2][64][RS]
+  __nv_bfloat16 *sB = sV + 2 * kAttKeys * RS;                          // [4][16][RS] Kh Kl Vh Vl
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -109,6 +161,7 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
   pdl_wait();
   pdl_trigger();
   const AttGeom g = att_geom(a, b, split);
+  const bool do_block = split == a.n_splits - 1;
 
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
   const __nv_bfloat16 *ring_k = static_cast<const __nv_bfloat16 *>(a.ring_k);
@@ -116,37 +169,43 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
   const __nv_bfloat16 *blk_k = static_cast<const __nv_bfloat16 *>(a.blk_k);
   const __nv_bfloat16 *blk_v = static_cast<const __nv_bfloat16 *>(a.blk_v);
 
-  // ---- Q tile: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
+  // ---- Q tiles: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
   constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int c = tid; c < kAttRows * CPR; c += 128) {
-    const int rr = c / CPR, ch = c % CPR;
+  for (int c = tid; c < 2 * kAttRows * CPR; c += 128) {
+    const int part = c / (kAttRows * CPR), cc = c % (kAttRows * CPR);
+    const int rr = cc / CPR, ch = cc % CPR;
     const bool valid = rr < R;
     const int gh = valid ? rr / a.W : 0, i = valid ? rr % a.W : 0;
-    const __nv_bfloat16 *src =
-        q + (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + ch * 8;
-    cp_async16(smem_u32(sQ + rr * RS + ch * 8), src, valid);
+    const __nv_bfloat16 *src = q + (part ? a.q_lo : 0) +
+                               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
+                               (h * G + gh) * D + ch * 8;
+    cp_async16(smem_u32(sQ + (part * kAttRows + rr) * RS + ch * 8), src, valid);
   }
   auto load_kv = [&](int buf, int k0) {
     for (int c = tid; c < kAttKeys * CPR; c += 128) {
       const int kr = c / CPR, ch = c % CPR;
       const int k = k0 + kr;
       const bool valid = k < g.k_end;
-      const __nv_bfloat16 *sk = ring_k, *sv = ring_v;
       size_t off = 0;
       if (valid) {
-        if (k < g.n_ctx) {
-          const long long p = g.p_lo + k;
-          off = ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.cap + p % a.cap) * D;
-        } else {
-          sk = blk_k;
-          sv = blk_v;
-          off = ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.W + (k - g.n_ctx)) * D;
-        }
+        const long long p = g.p_lo + k;
+        off = ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.cap + p % a.cap) * D;
       }
-      cp_async16(smem_u32(sK + (buf * kAttKeys + kr) * RS + ch * 8), sk + off + ch * 8, valid);
-      cp_async16(smem_u32(sV + (buf * kAttKeys + kr) * RS + ch * 8), sv + off + ch * 8, valid);
+      cp_async16(smem_u32(sK + (buf * kAttKeys + kr) * RS + ch * 8), ring_k + off + ch * 8, valid);
+      cp_async16(smem_u32(sV + (buf * kAttKeys + kr) * RS + ch * 8), ring_v + off + ch * 8, valid);
     }
   };
+  if (do_block) {  // block keys/values: [Kh; Kl; Vh; Vl], 16 rows each (rows >= W zero)
+    for (int c = tid; c < 4 * 16 * CPR; c += 128) {
+      const int part = c / (16 * CPR), cc = c % (16 * CPR);
+      const int j = cc / CPR, ch = cc % CPR;
+      const bool valid = j < a.W;
+      const __nv_bfloat16 *base = (part < 2 ? blk_k : blk_v) + ((part & 1) ? a.blk_lo : 0);
+      const __nv_bfloat16 *src =
+          base + ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.W + (valid ? j : 0)) * D + ch * 8;
+      cp_async16(smem_u32(sB + (part * 16 + j) * RS + ch * 8), src, valid);
+    }
+  }
 
   float o[D / 8][4];
 #pragma unroll
@@ -159,21 +218,19 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
   const int iA = rowA % a.W, iB = rowB % a.W;
   const bool rvA = rowA < R, rvB = rowB < R;
 
-  int n_blocks = g.k_end > g.k_begin ? (g.k_end - g.k_begin + kAttKeys - 1) / kAttKeys : 0;
+  const int n_blocks = g.k_end > g.k_begin ? (g.k_end - g.k_begin + kAttKeys - 1) / kAttKeys : 0;
   if (n_blocks > 0) load_kv(0, g.k_begin);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
 
-  // Q fragments (A operand), kept in registers for the whole key range
-  uint32_t qf[D / 16][4];
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
+  // A fragments of Q (hi or lo) for k-step ks
+  auto q_frag = [&](int part, int ks, uint32_t (&f)[4]) {
     const int mi = lane >> 3;
     const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
     const int col = ks * 16 + (mi >> 1) * 8;
-    ldsm_x4(smem_u32(sQ + row * RS + col), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-  }
+    ldsm_x4(smem_u32(sQ + (part * kAttRows + row) * RS + col), f[0], f[1], f[2], f[3]);
+  };
 
   for (int blk = 0; blk < n_blocks; ++blk) {
     const int buf = blk & 1;
@@ -181,12 +238,15 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
     if (blk + 1 < n_blocks) load_kv(buf ^ 1, k0 + kAttKeys);
     cp_async_commit();
 
-    // S = Q K^T for 16 rows x 64 keys
+    // S = (Qh + Ql) K^T for 16 rows x 64 keys
     float s[kAttKeys / 8][4];
 #pragma unroll
     for (int nt = 0; nt < kAttKeys / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t qh[4], ql[4];
+      q_frag(0, ks, qh);
+      q_frag(1, ks, ql);
 #pragma unroll
       for (int nt = 0; nt < kAttKeys / 8; nt += 2) {
         const int mi = lane >> 3;
@@ -194,49 +254,23 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
         const int col = ks * 16 + (mi & 1) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(smem_u32(sK + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        mma16816(s[nt], qf[ks], b0, b1);
-        mma16816(s[nt + 1], qf[ks], b2, b3);
+        mma16816(s[nt], qh, b0, b1);
+        mma16816(s[nt + 1], qh, b2, b3);
+        mma16816(s[nt], ql, b0, b1);
+        mma16816(s[nt + 1], ql, b2, b3);
       }
     }
-    // mask + online softmax (base 2)
-    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < kAttKeys / 8; ++nt) {
+    for (int nt = 0; nt < kAttKeys / 8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int k = k0 + nt * 8 + 2 * t4 + (e & 1);
         const bool top = e < 2;
-        const bool vis = (top ? rvA : rvB) && att_visible(a, g, top ? iA : iB, k);
+        const bool vis = (top ? rvA : rvB) && ctx_visible(a, g, top ? iA : iB, k);
         s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
-        mx[top ? 0 : 1] = fmaxf(mx[top ? 0 : 1], s[nt][e]);
       }
-    }
     float alpha[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float m_new = fmaxf(m_run[hr], mx[hr]);
-      alpha[hr] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[hr] - m_new);
-      m_run[hr] = m_new;
-    }
-    float ls[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nt = 0; nt < kAttKeys / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int hr = e < 2 ? 0 : 1;
-        const float pv = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m_run[hr]);
-        s[nt][e] = pv;
-        ls[hr] += pv;
-      }
-    }
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 1);
-      ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 2);
-      l_run[hr] = l_run[hr] * alpha[hr] + ls[hr];
-    }
+    softmax_update<kAttKeys / 8>(s, m_run, l_run, alpha);
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
       o[n][0] *= alpha[0];
@@ -244,14 +278,14 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
       o[n][2] *= alpha[1];
       o[n][3] *= alpha[1];
     }
-    // O += P V
+    // O += (Ph + Pl) V
 #pragma unroll
     for (int kk = 0; kk < kAttKeys / 16; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      uint32_t ph[4], pl[4];
+      split_pack(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+      split_pack(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+      split_pack(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+      split_pack(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
 #pragma unroll
       for (int nd = 0; nd < D / 8; nd += 2) {
         const int mi = lane >> 3;
@@ -259,12 +293,77 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
         const int col = (nd + (mi >> 1)) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(smem_u32(sV + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        mma16816(o[nd], pa, b0, b1);
-        mma16816(o[nd + 1], pa, b2, b3);
+        mma16816(o[nd], ph, b0, b1);
+        mma16816(o[nd + 1], ph, b2, b3);
+        mma16816(o[nd], pl, b0, b1);
+        mma16816(o[nd + 1], pl, b2, b3);
       }
     }
     cp_async_wait<0>();
     __syncthreads();
+  }
+
+  if (do_block) {
+    // S = Qh Kh + Ql Kh + Qh Kl over the (up to) 16 block keys
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t qh[4], ql[4];
+      q_frag(0, ks, qh);
+      q_frag(1, ks, ql);
+      const int mi = lane >> 3;
+      const int key = (mi >> 1) * 8 + (lane & 7);
+      const int col = ks * 16 + (mi & 1) * 8;
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      ldsm_x4(smem_u32(sB + (0 * 16 + key) * RS + col), h0, h1, h2, h3);
+      ldsm_x4(smem_u32(sB + (1 * 16 + key) * RS + col), l0, l1, l2, l3);
+      mma16816(s[0], qh, h0, h1);
+      mma16816(s[1], qh, h2, h3);
+      mma16816(s[0], ql, h0, h1);
+      mma16816(s[1], ql, h2, h3);
+      mma16816(s[0], qh, l0, l1);
+      mma16816(s[1], qh, l2, l3);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = nt * 8 + 2 * t4 + (e & 1);
+        const bool top = e < 2;
+        const bool vis = (top ? rvA : rvB) && blk_visible(a, top ? iA : iB, j);
+        s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
+      }
+    float alpha[2];
+    softmax_update<2>(s, m_run, l_run, alpha);
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= alpha[0];
+      o[n][1] *= alpha[0];
+      o[n][2] *= alpha[1];
+      o[n][3] *= alpha[1];
+    }
+    uint32_t ph[4], pl[4];
+    split_pack(s[0][0], s[0][1], ph[0], pl[0]);
+    split_pack(s[0][2], s[0][3], ph[1], pl[1]);
+    split_pack(s[1][0], s[1][1], ph[2], pl[2]);
+    split_pack(s[1][2], s[1][3], ph[3], pl[3]);
+#pragma unroll
+    for (int nd = 0; nd < D / 8; nd += 2) {
+      const int mi = lane >> 3;
+      const int key = (mi & 1) * 8 + (lane & 7);
+      const int col = (nd + (mi >> 1)) * 8;
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      ldsm_x4_t(smem_u32(sB + (2 * 16 + key) * RS + col), h0, h1, h2, h3);
+      ldsm_x4_t(smem_u32(sB + (3 * 16 + key) * RS + col), l0, l1, l2, l3);
+      mma16816(o[nd], ph, h0, h1);
+      mma16816(o[nd + 1], ph, h2, h3);
+      mma16816(o[nd], pl, h0, h1);
+      mma16816(o[nd + 1], pl, h2, h3);
+      mma16816(o[nd], ph, l0, l1);
+      mma16816(o[nd + 1], ph, l2, l3);
+    }
   }
 
   // ---- partial outputs
@@ -287,7 +386,7 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(AttArgs a) {
 // query row; lanes own D/32 consecutive output dims and the split weights are computed
 // by lanes and broadcast, so the per-split loads are independent of each other.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) attention_combine_kernel(AttArgs a) {
+__global__ void __launch_bounds__(256) attention_combine_kernel(const __grid_constant__ AttArgs a) {
   const int bh = blockIdx.x;
   const int b = bh / a.n_kv_heads, h = bh % a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
@@ -344,11 +443,16 @@ __global__ void __launch_bounds__(256) attention_combine_kernel(AttArgs a) {
   T *out = static_cast<T *>(a.out) +
            (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) out[e] = from_f<T>(acc[e] * inv);
+  for (int e = 0; e < PER; ++e) {
+    const float y = acc[e] * inv;
+    const T hi = from_f<T>(y);
+    out[e] = hi;
+    if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
+  }
 }
 
 // fp32 path (small geometries): one CTA per (query head, request), exact fp32 softmax.
-__global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
+__global__ void __launch_bounds__(128) attention_f32_kernel(const __grid_constant__ AttArgs a) {
   extern __shared__ float sc[];  // [n_keys_max]
   const int qh = blockIdx.x, b = blockIdx.y;
   const int G = a.n_q_heads / a.n_kv_heads;
@@ -358,7 +462,8 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
   pdl_trigger();
   AttGeom g = att_geom(a, b, 0);
   g.k_begin = 0;
-  g.k_end = g.n_keys;
+  g.k_end = g.n_ctx;
+  const int n_keys = g.n_ctx + a.W;
   const float *q = static_cast<const float *>(a.q);
   const float *rk = static_cast<const float *>(a.ring_k);
   const float *rv = static_cast<const float *>(a.ring_v);
@@ -376,9 +481,9 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
   for (int i = 0; i < a.W; ++i) {
     const float *qi = q + (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + qh * D;
     float lmax = -INFINITY;
-    for (int k = threadIdx.x; k < g.n_keys; k += blockDim.x) {
+    for (int k = threadIdx.x; k < n_keys; k += blockDim.x) {
       float sdot = -INFINITY;
-      if (att_visible(a, g, i, k)) {
+      if (k < g.n_ctx ? ctx_visible(a, g, i, k) : blk_visible(a, i, k - g.n_ctx)) {
         const float *kp = key_ptr(k, false);
         float acc = 0.f;
         for (int d = 0; d < D; ++d) acc += qi[d] * kp[d];
@@ -394,7 +499,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) M = fmaxf(M, red[w]);
     __syncthreads();
     float lsum = 0.f;
-    for (int k = threadIdx.x; k < g.n_keys; k += blockDim.x) {
+    for (int k = threadIdx.x; k < n_keys; k += blockDim.x) {
       const float e = sc[k] == -INFINITY ? 0.f : expf(sc[k] - M);
       sc[k] = e;
       lsum += e;
@@ -406,7 +511,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) L += red[w];
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
       float acc = 0.f;
-      for (int k = 0; k < g.n_keys; ++k)
+      for (int k = 0; k < n_keys; ++k)
         if (sc[k] != 0.f) acc += sc[k] * key_ptr(k, true)[d];
       float *out = static_cast<float *>(a.out) +
                    (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + qh * D;
@@ -417,7 +522,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttArgs a) {
 }
 
 size_t attention_smem_bytes(int head_dim) {
-  return static_cast<size_t>(kAttRows + 4 * kAttKeys) * (head_dim + kAttPad) * 2;
+  return static_cast<size_t>(2 * kAttRows + 4 * kAttKeys + 4 * 16) * (head_dim + kAttPad) * 2;
 }
 size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim) {
   return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows * head_dim;

@@ -19,7 +19,6 @@
 #include "bd_internal.h"
 
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -129,9 +128,17 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
   };
   auto load_b = [&](int n_tile, int kbi, uint8_t *dst, uint64_t *bar) {
     const int nb = boxes(kbi);
-    for (int j = 0; j < nb; ++j)
-      tma_load_2d(dst + static_cast<size_t>(j) * box_b, &maps.b, bar, (kbi * KB + j) * BK,
-                  n_tile * p.block_n, pol_x);
+    for (int j = 0; j < nb; ++j) {
+      uint8_t *d = dst + static_cast<size_t>(j) * box_b;
+      const int x = (kbi * KB + j) * BK;
+      if (p.split) {  // [hi rows of the tile; lo rows of the tile]
+        tma_load_2d(d, &maps.b, bar, x, n_tile * p.ln, pol_x);
+        tma_load_2d(d + static_cast<size_t>(p.ln) * 128, &maps.b, bar, x, p.lo_row + n_tile * p.ln,
+                    pol_x);
+      } else {
+        tma_load_2d(d, &maps.b, bar, x, n_tile * p.block_n, pol_x);
+      }
+    }
   };
 
   // The weight tiles do not depend on the previous kernel: start streaming them before
@@ -309,7 +316,9 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs &p, int m_tile, int r, 
             const float g = v[jj];
             const float u = xbuf[r * kXStride + jj];
             const float h = g / (1.0f + __expf(-g)) * u;
-            out[static_cast<size_t>(tok) * p.ld_act + f] = from_f<T>(h);
+            const T hi = from_f<T>(h);
+            out[static_cast<size_t>(tok) * p.ld_act + f] = hi;
+            if (p.act_lo) out[p.act_lo + static_cast<size_t>(tok) * p.ld_act + f] = from_f<T>(h - to_f<T>(hi));
           }
         }
       }
@@ -363,6 +372,19 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs &p, int m_tile, int r, 
 }
 
 // ------------------------------------------------------------------ epilogue
+// Logical columns j0..j0+15 of the accumulator: the hi half, plus the lo half that sits
+// LW columns further when the activation operand is split.
+__device__ __forceinline__ void tmem_ld_logical(uint32_t tbase, int j0, int LW, int split,
+                                                float (&v)[16]) {
+  tmem_ld16(tbase + j0, v);
+  if (split) {
+    float w[16];
+    tmem_ld16(tbase + LW + j0, w);
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+  }
+}
+
 template <typename T, int EPI>
 __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
                               uint32_t tmem_base, long long u0, long long u1, float *xbuf,
@@ -384,8 +406,9 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
     const uint32_t ra = static_cast<uint32_t>(e >> 1);
     ++e;
     const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
+    const int LW = p.ln;  // logical token columns of the tile
     EpiOperands op;
-    epi_load<T, EPI>(p, m_tile, r, n_tile * p.block_n, op);
+    epi_load<T, EPI>(p, m_tile, r, n_tile * LW, op);
     if (*sabort || !mbar_wait(&accf[a], ra & 1u)) {
       *sabort = 1;
       return;
@@ -397,10 +420,10 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
     int c_first = cta, c_last = cta;
     if (!whole) {
       const int slot = (tile == first_tile) ? 0 : 1;
-      float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * p.block_n * kBM;
-      for (int j0 = 0; j0 < p.block_n; j0 += 16) {
+      float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM;
+      for (int j0 = 0; j0 < LW; j0 += 16) {
         float v[16];
-        tmem_ld16(tbase + j0, v);
+        tmem_ld_logical(tbase, j0, LW, p.split, v);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) mine[(j0 + jj) * kBM + r] = v[jj];
       }
@@ -425,9 +448,9 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
       }
       __threadfence();
     }
-    for (int j0 = 0; j0 < p.block_n; j0 += 16) {
+    for (int j0 = 0; j0 < LW; j0 += 16) {
       float v[16];
-      tmem_ld16(tbase + j0, v);
+      tmem_ld_logical(tbase, j0, LW, p.split, v);
       if (!whole) {
         // Sum the contributors' partial tiles in CTA order (deterministic).  Loads of two
         // contributors are issued before they are added so their L2 latencies overlap.
@@ -441,7 +464,7 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
             const int c = c0 + u;
             if (c > c_last || c == cta) continue;
             const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
-            const float *o = p.partials + (static_cast<size_t>(c) * 2 + cslot) * p.block_n * kBM +
+            const float *o = p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
                              static_cast<size_t>(j0) * kBM + r;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) part[u][jj] = __ldcg(o + jj * kBM);
@@ -458,8 +481,8 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
         for (int jj = 0; jj < 16; ++jj) v[jj] = acc[jj];
       }
       EpiOperands cur = op;
-      if (j0 + 16 < p.block_n) epi_load<T, EPI>(p, m_tile, r, n_tile * p.block_n + j0 + 16, op);
-      epi_chunk<T, EPI>(p, m_tile, r, n_tile * p.block_n + j0, v, cur, xbuf, red, redi);
+      if (j0 + 16 < LW) epi_load<T, EPI>(p, m_tile, r, n_tile * LW + j0 + 16, op);
+      epi_chunk<T, EPI>(p, m_tile, r, n_tile * LW + j0, v, cur, xbuf, red, redi);
     }
     tc_fence_before();
     mbar_arrive(&acce[a]);
@@ -638,20 +661,19 @@ size_t gemm_partial_floats(int n_ctas, int block_n) {
   return static_cast<size_t>(n_ctas) * 2 * block_n * kBM;
 }
 
+// Deepest pipeline that fits in shared memory (0 if not even two stages fit).
 static int pick_stages(int block_n, int kbox) {
   for (int s = kMaxStages; s >= 2; --s)
     if (smem_layout(s, block_n, kbox).total <= kSmemLimit) return s;
-  return 2;
+  return 0;
 }
 
-// K boxes per stage: 4 (512-byte row pieces) unless that leaves fewer than 3 stages.
+// K boxes per stage: as many as still leave a double-buffered pipeline (measured: two
+// stages of 4 boxes, i.e. 512-byte row pieces, stream faster than deeper pipelines of
+// narrower stages), and no more than half of K.
 static int pick_kbox(int block_n, int K, int BK) {
   int kb = 4;
-  if (const char *e = getenv("BD_GEMM_KBOX")) {
-    const int v = atoi(e);
-    if (v == 1 || v == 2 || v == 4) kb = v;
-  }
-  while (kb > 1 && (pick_stages(block_n, kb) < 3 || K < kb * BK * 2)) kb >>= 1;
+  while (kb > 1 && (pick_stages(block_n, kb) < 2 || K < kb * BK * 2)) kb >>= 1;
   return kb;
 }
 
@@ -689,8 +711,21 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   if (plan.n_w > kMaxSegs) return "too many GEMM segments";
   a.K = plan.K;
   a.n_tokens = plan.n_tokens;
-  a.block_n = gemm_block_n(plan.n_tokens);
-  a.n_tiles_n = (plan.n_tokens + a.block_n - 1) / a.block_n;
+  const int n_pad = (plan.n_tokens + 15) / 16 * 16;
+  if (plan.split) {
+    if (plan.dtype != 0 || n_pad > 128) return "split activations need bf16 and <= 128 tokens";
+    a.split = 1;
+    a.ln = n_pad;
+    a.lo_row = n_pad;
+    a.block_n = 2 * n_pad;
+    a.n_tiles_n = 1;
+  } else {
+    a.split = 0;
+    a.block_n = gemm_block_n(plan.n_tokens);
+    a.ln = a.block_n;
+    a.lo_row = 0;
+    a.n_tiles_n = (plan.n_tokens + a.block_n - 1) / a.block_n;
+  }
   a.pair_mode = plan.pair_mode ? 1 : 0;
   a.kbox = pick_kbox(a.block_n, plan.K, BK);
   a.kb = (plan.K + BK * a.kbox - 1) / (BK * a.kbox);
@@ -718,6 +753,7 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   const long long by_units = (a.units + min_units - 1) / min_units;
   a.n_ctas = static_cast<int>(by_units < num_sms() ? by_units : num_sms());
   a.stages = pick_stages(a.block_n, a.kbox);
+  if (a.stages < 2) return "GEMM tile does not fit in shared memory";
   a.partials = sc.partials;
   a.counters = sc.counters;
   if (gemm_partial_floats(a.n_ctas, a.block_n) > sc.partial_floats) return "GEMM partial scratch too small";
@@ -730,7 +766,9 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
                                plan.pair_mode ? 64 : kBM);
     if (!err.empty()) return err;
   }
-  std::string err = make_map(&maps.b, plan.x, plan.dtype, plan.K, plan.n_tokens, BK, a.block_n);
+  std::string err = plan.split
+      ? make_map(&maps.b, plan.x, plan.dtype, plan.K, 2 * a.lo_row, BK, a.ln)
+      : make_map(&maps.b, plan.x, plan.dtype, plan.K, plan.n_tokens, BK, a.block_n);
   if (!err.empty()) return err;
   cudaError_t e = plan.dtype == 0 ? launch_typed<__nv_bfloat16>(maps, a, stream)
                                   : launch_typed<float>(maps, a, stream);

@@ -41,9 +41,16 @@ struct GemmSeg {
 struct __align__(16) GemmArgs {
   int K, n_tokens, block_n, n_tiles_n, m_tiles, kb, n_ctas, n_segs, stages, pair_mode;
   int kbox;                       // 128-byte-wide K boxes per pipeline stage (1, 2 or 4)
+  // Split activations: the activation operand is a bf16 pair x = hi + lo stored as two
+  // row blocks [hi rows; lo rows] (lo block starting at row lo_row).  The MMA runs on
+  // block_n = 2 * ln columns (ln = logical tokens of a tile) and the epilogue adds the
+  // two halves, so activations enter at ~16-bit instead of 8-bit mantissa precision
+  // while the weight tile is still read once.
+  int split, ln, lo_row;
   long long units;
   int epi;
   int ld_out, ld_resid, ld_act, block_w, vocab;
+  long long act_lo;               // SWIGLU: element offset of the lo block of out_act (0: none)
   float *out_f32;
   const float *resid;
   const float *row_scale;
@@ -73,6 +80,7 @@ struct GemmPlan {
   int n_w;
   GemmWeight w[kMaxSegs];
   bool pair_mode;            // SwiGLU: w[0] = gate, w[1] = up (same rows)
+  bool split;                // x is a hi/lo pair [2][round_up(n_tokens,16)][K] (bf16 only)
   GemmArgs args;             // epilogue fields filled by the caller; layout by the launcher
 };
 

@@ -20,6 +20,7 @@ struct AttArgs {
   float *part_o;        // [B, Hkv, n_splits, 64, D] fp32 unnormalised partial outputs
   float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
   int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
+  size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
 };
 
 size_t attention_smem_bytes(int head_dim);
@@ -47,17 +48,20 @@ enum NormMode : int {
   NORM_BRIDGE = 1,  // r = sqrt(mean(x^2)); out = x / (r + eps); r_out = r
   NORM_FINAL = 2    // plain, plus fp32 copy and the mask-row copy for the LM head
 };
+// lo_off != 0: also write the rounding residual y - hi at out + lo_off (split activation).
 std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain,
                            float eps, int mode, void *out, float *r_out, float *f32_out,
-                           void *head_out, int W, cudaStream_t s);
+                           float *head_out, int W, size_t lo_off, cudaStream_t s);
+// fp32 -> bf16 hi (dst) and lo (dst + lo_off) of n elements.
+std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, cudaStream_t s);
 
 // c = sqrt(Rc) z / (||z|| + eps) for non-anchor rows; sqrt(Rc) * codebook[anchor] for anchors.
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
                         const int32_t *anchors, int V, int W, float eps, void *c_out,
-                        cudaStream_t s);
+                        size_t lo_off, cudaStream_t s);
 // m_i = sigmoid(G c_i + G_p c_{i-1} + b) * (A c_{i-1}) for i >= 1, m_0 = 0.
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias,
-                           int W, void *m_out, cudaStream_t s);
+                           int W, void *m_out, size_t lo_off, cudaStream_t s);
 // Head post-processing of raw fp32 projections [rows, ld_raw]: for each head of each
 // segment, plain_head_rmsnorm + split-half RoPE (query/key segments) or a copy (value
 // segments), rounded to the config dtype and scattered to its destination.
@@ -72,6 +76,7 @@ struct HeadSeg {
   int kind, dst_mode, col0, n_heads, ld, cap;
   const void *norm;  // [D] gain (query/key segments)
   void *dst;
+  size_t lo_off;     // != 0: also store the rounding residual at dst + lo_off
 };
 struct HeadPostArgs {
   const float *raw;

@@ -92,7 +92,8 @@ constexpr int kNormVec = 8;
 template <typename T>
 __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, const T *gain,
                                                       float eps, int mode, T *out, float *r_out,
-                                                      float *f32_out, T *head_out, int W) {
+                                                      float *f32_out, float *head_out, int W,
+                                                      size_t lo_off) {
   __shared__ float red[32];
   const int row = blockIdx.x;
   pdl_wait();
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, con
   }
   const int i = row % W;
   T *orow = (mode == NORM_FINAL) ? nullptr : out + static_cast<size_t>(row) * H;
-  T *hrow = nullptr;
+  float *hrow = nullptr;
   if (mode == NORM_FINAL && head_out != nullptr && i > 0)
     hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
   float *frow = (mode == NORM_FINAL && f32_out) ? f32_out + static_cast<size_t>(row) * H : nullptr;
@@ -137,8 +138,15 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, con
       y.z *= g.z;
       y.w *= g.w;
     }
-    if (orow) store4<T>(orow, i4, y);
-    if (hrow) store4<T>(hrow, i4, y);
+    if (orow) {
+      store4<T>(orow, i4, y);
+      if (lo_off) {  // residual of the rounding, so that hi + lo carries ~16 mantissa bits
+        const float4 h = make_float4(to_f<T>(from_f<T>(y.x)), to_f<T>(from_f<T>(y.y)),
+                                     to_f<T>(from_f<T>(y.z)), to_f<T>(from_f<T>(y.w)));
+        store4<T>(orow + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+      }
+    }
+    if (hrow) reinterpret_cast<float4 *>(hrow)[i4] = y;
     if (frow) reinterpret_cast<float4 *>(frow)[i4] = y;
   };
 #pragma unroll
@@ -148,6 +156,13 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, con
   }
   for (int i4 = threadIdx.x + kNormVec * blockDim.x; i4 < H4; i4 += blockDim.x)
     emit(i4, reinterpret_cast<const float4 *>(xr)[i4]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_split(T *p, size_t i, size_t lo_off, float v) {
+  const T h = from_f<T>(v);
+  p[i] = h;
+  if (lo_off) p[lo_off + i] = from_f<T>(v - to_f<T>(h));
 }
 
 // One warp per (row, head).  Lane l holds elements [l*E, l*E + E) of the head (E = D/32);
@@ -210,12 +225,12 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   }
   T *dst = static_cast<T *>(sg.dst) + o + d0;
 #pragma unroll
-  for (int e = 0; e < E; ++e) dst[e] = from_f<T>(v[e]);
+  for (int e = 0; e < E; ++e) store_split(dst, e, sg.lo_off, v[e]);
 }
 
 template <typename T>
 __global__ void code_kernel(const float *z, int Rc, const T *codebook, const int32_t *anchors,
-                            int V, int W, float eps, T *c_out) {
+                            int V, int W, float eps, T *c_out, size_t lo_off) {
   __shared__ float red[32];
   const int row = blockIdx.x, b = row / W, i = row % W;
   pdl_wait();
@@ -229,7 +244,7 @@ __global__ void code_kernel(const float *z, int Rc, const T *codebook, const int
       a = 0;
     }
     const T *cb = codebook + static_cast<size_t>(a) * Rc;
-    for (int k = threadIdx.x; k < Rc; k += blockDim.x) c[k] = from_f<T>(scale * to_f<T>(cb[k]));
+    for (int k = threadIdx.x; k < Rc; k += blockDim.x) store_split(c, k, lo_off, scale * to_f<T>(cb[k]));
     return;
   }
   const float *zr = z + static_cast<size_t>(row) * Rc;
@@ -237,17 +252,18 @@ __global__ void code_kernel(const float *z, int Rc, const T *codebook, const int
   for (int k = threadIdx.x; k < Rc; k += blockDim.x) ss += zr[k] * zr[k];
   ss = block_sum(ss, red);
   const float s = scale / (sqrtf(ss) + eps);
-  for (int k = threadIdx.x; k < Rc; k += blockDim.x) c[k] = from_f<T>(zr[k] * s);
+  for (int k = threadIdx.x; k < Rc; k += blockDim.x) store_split(c, k, lo_off, zr[k] * s);
 }
 
 template <typename T>
-__global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, T *m_out) {
+__global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, T *m_out,
+                               size_t lo_off) {
   const int row = blockIdx.x, i = row % W;
   pdl_wait();
   pdl_trigger();
   T *m = m_out + static_cast<size_t>(row) * Mc;
   if (i == 0) {
-    for (int k = threadIdx.x; k < Mc; k += blockDim.x) m[k] = from_f<T>(0.f);
+    for (int k = threadIdx.x; k < Mc; k += blockDim.x) store_split(m, k, lo_off, 0.f);
     return;
   }
   const float *recv = pre + static_cast<size_t>(row) * 3 * Mc;         // G c_i
@@ -255,7 +271,7 @@ __global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, T
   for (int k = threadIdx.x; k < Mc; k += blockDim.x) {
     const float z = recv[k] + pred[Mc + k] + (bias ? to_f<T>(bias[k]) : 0.f);
     const float g = 1.f / (1.f + expf(-z));
-    m[k] = from_f<T>(g * pred[2 * Mc + k]);
+    store_split(m, k, lo_off, g * pred[2 * Mc + k]);
   }
 }
 
@@ -303,6 +319,15 @@ __global__ void argmax_reduce_kernel(const float *val, const int32_t *idx, int m
   }
 }
 
+// fp32 rows -> bf16 hi rows [0, rows) and lo rows [lo_row, lo_row + rows).
+__global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+    store_split(dst, t, lo_off, src[t]);
+}
+
 __global__ void copy_f32_kernel(const float *src, float *dst, size_t n) {
   pdl_wait();
   pdl_trigger();
@@ -340,19 +365,25 @@ std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
 }
 
 std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain, float eps,
-                           int mode, void *out, float *r_out, float *f32_out, void *head_out, int W,
-                           cudaStream_t s) {
+                           int mode, void *out, float *r_out, float *f32_out, float *head_out, int W,
+                           size_t lo_off, cudaStream_t s) {
   cudaError_t e;
   if (dtype == 0)
     e = launch_pdl(rownorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, x, H,
                    static_cast<const __nv_bfloat16 *>(gain), eps, mode,
-                   static_cast<__nv_bfloat16 *>(out), r_out, f32_out,
-                   static_cast<__nv_bfloat16 *>(head_out), W);
+                   static_cast<__nv_bfloat16 *>(out), r_out, f32_out, head_out, W, lo_off);
   else
     e = launch_pdl(rownorm_kernel<float>, dim3(rows), dim3(256), 0, s, x, H,
                    static_cast<const float *>(gain), eps, mode, static_cast<float *>(out), r_out,
-                   f32_out, static_cast<float *>(head_out), W);
+                   f32_out, head_out, W, lo_off);
   return err("rownorm", e);
+}
+
+std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, cudaStream_t s) {
+  const size_t blocks = (n + 255) / 256;
+  return err("split rows", launch_pdl(split_rows_kernel, dim3(blocks < 2048 ? blocks : 2048),
+                                      dim3(256), 0, s, src, n, static_cast<__nv_bfloat16 *>(dst),
+                                      lo_off));
 }
 
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
@@ -370,28 +401,29 @@ std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
 
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
                         const int32_t *anchors, int V, int W, float eps, void *c_out,
-                        cudaStream_t s) {
+                        size_t lo_off, cudaStream_t s) {
   cudaError_t e;
   if (dtype == 0)
     e = launch_pdl(code_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, z, Rc,
                    static_cast<const __nv_bfloat16 *>(codebook), anchors, V, W, eps,
-                   static_cast<__nv_bfloat16 *>(c_out));
+                   static_cast<__nv_bfloat16 *>(c_out), lo_off);
   else
     e = launch_pdl(code_kernel<float>, dim3(rows), dim3(256), 0, s, z, Rc,
                    static_cast<const float *>(codebook), anchors, V, W, eps,
-                   static_cast<float *>(c_out));
+                   static_cast<float *>(c_out), lo_off);
   return err("code", e);
 }
 
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias, int W,
-                           void *m_out, cudaStream_t s) {
+                           void *m_out, size_t lo_off, cudaStream_t s) {
   cudaError_t e;
   if (dtype == 0)
     e = launch_pdl(message_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, pre, Mc,
-                   static_cast<const __nv_bfloat16 *>(bias), W, static_cast<__nv_bfloat16 *>(m_out));
+                   static_cast<const __nv_bfloat16 *>(bias), W, static_cast<__nv_bfloat16 *>(m_out),
+                   lo_off);
   else
     e = launch_pdl(message_kernel<float>, dim3(rows), dim3(256), 0, s, pre, Mc,
-                   static_cast<const float *>(bias), W, static_cast<float *>(m_out));
+                   static_cast<const float *>(bias), W, static_cast<float *>(m_out), lo_off);
   return err("message", e);
 }
 

@@ -65,7 +65,7 @@ class DraftSession:
     def alloc_outputs(self, Bn: int, n_masks: int):
         W = n_masks + 1
         H = self.geo.hidden
-        head_in = torch.empty(Bn * n_masks, H, dtype=self.dtype, device=self.device)
+        head_in = torch.empty(Bn * n_masks, H, dtype=torch.float32, device=self.device)
         tokens = torch.empty(Bn * n_masks, dtype=torch.int32, device=self.device)
         maxl = torch.empty(Bn * n_masks, dtype=torch.float32, device=self.device)
         hidden = torch.empty(Bn * W, H, dtype=torch.float32, device=self.device)

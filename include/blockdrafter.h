@@ -153,6 +153,10 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
 
 /*
  * One masked-block draft forward (S3 .. S9 and the final norm) for B requests.
+ * Numerics (bf16 config): weights and context K/V are used as stored; the residual
+ * stream is fp32; every activation that feeds a tensor-core product (normed rows,
+ * attention output, SwiGLU product, codes, messages, queries, softmax weights and the
+ * block's own keys/values) enters as a bf16 hi+lo pair with fp32 accumulation.
  * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for
  * the injection after every layer when code_width > 0:
  *   row (b, 0) = embed(anchor_ids[b]) at position F_b; rows (b, i>=1) = embed(MASK) at
@@ -165,28 +169,30 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
  *   frontier    dev int64 [B]  committed context length F_b >= 1 of request b; ring row b
  *               must hold the live interval of every layer at that frontier
  *   B           1 .. 8 requests;  n_masks  K in 1 .. 15 (block width W = K + 1)
- *   head_in     dev [B*K, H] config dtype, OUT: final-normed mask rows, row b*K + (i-1)
- *               for block row i >= 1 -- the input of bd_lm_head_argmax
+ *   head_in     dev fp32 [B*K, H] OUT: final-normed mask rows, row b*K + (i-1) for block
+ *               row i >= 1 -- the input of bd_lm_head_argmax
  *   hidden_out  dev fp32 [B*W, H] OUT final-normed rows of every block row, or NULL
  *   layers_out  dev fp32 [L, B*W, H] OUT post-injection residual after each layer, or
  *               NULL (a debugging/parity output; it adds device-to-device copies)
  */
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B,
-                         int n_masks, void *head_in, float *hidden_out, float *layers_out,
+                         int n_masks, float *head_in, float *hidden_out, float *layers_out,
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Tied LM head with per-row argmax (S10).  [DFlash-notes], proposal head:
  *   logits = embed_head . hidden_r ;  token_out[r] = argmax_v logits[v]
- * Ties resolve to the lowest token id.  fp32 accumulation of config-dtype products.
+ * Ties resolve to the lowest token id.  fp32 accumulation; in a bf16 config each hidden
+ * row enters the tensor cores as a bf16 hi+lo pair (about 16 mantissa bits), the head
+ * weights as stored.
  *
- *   hidden         dev [rows, H] config dtype (e.g. bd_draft_round's head_in)
+ *   hidden         dev fp32 [rows, H] (e.g. bd_draft_round's head_in)
  *   rows           1 .. 8*15
  *   token_out      dev int32 [rows]  OUT
  *   max_logit_out  dev fp32 [rows]   OUT the winning logit, or NULL
  */
-bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const void *hidden,
+bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const float *hidden,
                             int rows, int32_t *token_out, float *max_logit_out,
                             void *workspace, size_t workspace_bytes, void *stream);
 

@@ -1,10 +1,10 @@
 """GPU-vs-oracle parity through the C ABI on small seeded cases.
 
-Tolerances (hidden states): max|gpu - ref| / max|ref| <= 2e-2 for bf16 storage with
-fp32 accumulation; 1e-3... for the fp32 configuration the products run on tf32 tensor
-cores, whose 10-bit mantissa bounds each product's relative error by about 2^-11, so the
-same 2e-2 bound applies and the measured value is reported.  Argmax tokens are
-compared bit-exactly wherever the oracle's top-2 logit gap exceeds 1e-2.
+Tolerances (hidden states): max|gpu - ref| / max|ref| <= 2e-2 (bf16 storage, fp32
+accumulation).  The fp32 configuration runs its products on tf32 tensor cores (10-bit
+mantissa, relative product error below 2^-11), so the same bound applies; the measured
+values are printed.  Argmax tokens are compared bit-exactly wherever the oracle's top-2
+logit gap exceeds 1e-2.
 """
 import numpy as np
 import pytest
@@ -45,7 +45,7 @@ def test_lm_head_argmax_matches_oracle(dtype, H, V, rows):
     dt = bdsynth.torch_dtype(dtype)
     g = torch.Generator().manual_seed(H + V + rows)
     E = (torch.randn(V, H, generator=g) * 0.02).to(dt)
-    h = torch.randn(rows, H, generator=g).to(dt)
+    h = torch.randn(rows, H, generator=g)  # fp32 hidden rows (the head's input type)
     from block_drafter_gb300.session import config_of
     cfg = config_of(geo, 0)
     wd = {"w_feature": E, "context_norm": E, "final_norm": E, "embed_head": E, "layers": []}

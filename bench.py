@@ -315,6 +315,23 @@ def time_e2e(st: State, steps: int, warmup: int):
     return e0.elapsed_time(e1) / steps, bi, bo
 
 
+def recorded_traffic():
+    """DRAM bytes per launch of the roofline kernel from the committed ncu record, if the
+    kernel's sources are unchanged since the counters were taken (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    h = hashlib.sha256()
+    for f in rec["source_files"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -361,28 +378,28 @@ def cpu_threads():
 
 # ----------------------------------------------------------------------------- main
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 CPU oracle as it stands, on the host cores, each step
-    a bounded sample of the B=1 workload (request 0's catch-up, the first draft layer of
-    the round and the full head), scaled to rounds/s by the layer count."""
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores.  Each step
+    is one full oracle step of request 0 of the B=1 workload (catch-up materialisation of
+    its 16 pending rows, the 5-layer round over the 2047-position window, the LM head),
+    i.e. exactly the per-request work of one GPU step at B=1."""
     if rank != 0:
         return
+    import numpy as np
     geo = bdsynth.DSPINE27B_B1
-    w = bdsynth.make_weights(geo, args.seed, device="cpu", layers=[0])
-    w["layers"] = [w["layers"][0]]
-    wh = {k: (v if k == "layers" else (None if v is None else v.float().numpy())) for k, v in w.items()}
-    wh["layers"] = [{kk: vv.float().numpy() for kk, vv in w["layers"][0].items()}]
+    w = bdsynth.make_weights(geo, args.seed, device="cpu")
+    wh = {k: (None if v is None else v.float().numpy()) for k, v in w.items() if k != "layers"}
+    wh["layers"] = [{kk: vv.float().numpy() for kk, vv in lw.items()} for lw in w["layers"]]
+    del w
     F = bdsynth.frontiers(geo, args.seed)
     anchors = bdsynth.anchor_ids(geo, args.seed)
     mask = bdsynth.mask_token_id(geo, args.seed)
-    import numpy as np
     feats = bdsynth.target_features(geo, geo.W, args.seed).float().numpy()
     pos = np.arange(F[0] - geo.W, F[0])
     ts = []
     for k in range(args.warmup + args.steps):
-        t = oracle_step_sample(geo, wh, F, anchors, mask, feats, pos, n_layers=1)
+        t = oracle_step_sample(geo, wh, F, anchors, mask, feats, pos)
         if k >= args.warmup:
             ts.append(t)
-    # a full step runs L layers; scale the one-layer sample's layer share accordingly
     t_step = statistics.mean(ts)
     val = 1.0 / t_step
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
@@ -392,8 +409,8 @@ def run_reference(args, rank, world):
             "config": {"workload": geo.name, "B": 1, "W": geo.W, "context": F[0],
                        "window": geo.windows[0]},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                             "sample": "request 0: catch-up of 16 rows, draft layer 0 only "
-                                       "(of 5), full LM head; value = 1 / sample time"},
+                             "sample": "one full oracle step of request 0 per step: catch-up of "
+                                       "16 rows, 5-layer round, full LM head"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -436,7 +453,7 @@ def main():
     ms = max_over_ranks(ms, world)
     hbm, tf, peak_kind = peaks()
     by = st.bytes_per_step()
-    head_bytes = by["head"] + st.head_in.numel() * st.head_in.element_size()
+    head_bytes = by["head"] + st.head_in.numel() * st.head_in.element_size()  # weights + fp32 rows
     head_gbs = head_bytes / (per["head"] * 1e-3) / 1e9
     step_gbs = by["total"] / (ms * 1e-3) / 1e9
     e2e_ms, bi, bo = time_e2e(st, max(10, args.steps // 2), 3)
@@ -460,7 +477,8 @@ def main():
         "algorithmic_bytes_per_step": by,
         "roofline": {"bound": "hbm", "kernel": "LM head call (tcgen05 GEMM + split-vocab argmax reduce)",
                      "achieved": head_gbs, "peak": hbm, "unit": "GB/s", "frac": head_gbs / hbm,
-                     "traffic": None, "peak_kind": peak_kind},
+                     "traffic": recorded_traffic(), "algorithmic_bytes": head_bytes,
+                     "peak_kind": peak_kind},
         "clocks": ck,
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},

@@ -90,6 +90,9 @@ def lib() -> C.CDLL:
         L.bd_sync_status.restype = i
         L.bd_sync_status.argtypes = [vp]
         L.bd_kernel_launches.restype = C.c_uint64
+        L.bd_lm_head_argmax_noalloc.restype = i
+        L.bd_lm_head_argmax_noalloc.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, vp,
+                                                vp, vp]
         _lib = L
     return _lib
 
@@ -190,6 +193,15 @@ def lm_head_argmax(cfg: Config, weights: Weights, hidden: torch.Tensor, token_ou
         C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
         _ptr(max_logit_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def lm_head_argmax_noalloc(cfg: Config, weights: Weights, hidden: torch.Tensor,
+                           token_out: torch.Tensor, max_logit_out: Optional[torch.Tensor] = None,
+                           stream=None):
+    """bd_lm_head_argmax without a workspace (scratch in the library's static device array)."""
+    _check(lib().bd_lm_head_argmax_noalloc(
+        C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
+        _ptr(max_logit_out), _stream(stream)))
 
 
 def kernel_launches() -> int:

@@ -13,16 +13,19 @@
 #include <cstring>
 #include <string>
 
+namespace {
+thread_local std::string t_last_error;
+}  // namespace
+
 namespace bd {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void set_last_error(const std::string &msg) { t_last_error = msg; }
 }  // namespace bd
 
 namespace {
 
 using namespace bd;
-
-thread_local std::string t_last_error;
 
 bd_status fail(bd_status s, const std::string &msg) {
   t_last_error = msg;

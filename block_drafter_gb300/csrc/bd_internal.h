@@ -107,6 +107,7 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &scratch, cudaStream_t
 // Launch with programmatic stream serialisation (PDL) so the next kernel's prologue can
 // overlap this kernel's tail; every kernel calls pdl_wait() before dependent accesses.
 void count_launch();
+void set_last_error(const std::string &msg);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

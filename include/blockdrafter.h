@@ -196,6 +196,30 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
                             int rows, int32_t *token_out, float *max_logit_out,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * bd_lm_head_argmax without a workspace, for callers that cannot allocate device
+ * memory (no counterpart in the papers; it computes exactly what bd_lm_head_argmax
+ * computes, with the same kernels).  Callers such as a serving engine whose pool owns
+ * all device memory after start-up, or a plugin host that gives the library no
+ * allocation hook, cannot hand over a workspace; this entry point allocates nothing.
+ *
+ * Its scratch is one file-scope device array of BD_NOALLOC_SCRATCH_BYTES that every GPU
+ * loading the library holds until the process exits.  Limits: rows <= 32, hidden <=
+ * 8192, vocab <= 262144; larger sizes return BD_ERR_INVALID_ARG with a message.
+ * All calls share the array and it keeps the previous call's contents (the counters
+ * that must start at zero are cleared by every call), so calls that overlap on the GPU
+ * -- on two streams or from two threads -- race and must be ordered by the caller.
+ * The first call on a device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.
+ */
+#define BD_NOALLOC_MAX_ROWS 32
+#define BD_NOALLOC_MAX_HIDDEN 8192
+#define BD_NOALLOC_MAX_VOCAB 262144
+#define BD_NOALLOC_SCRATCH_BYTES (12u << 20)
+bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_weights *w,
+                                    const float *hidden, int rows, int32_t *token_out,
+                                    float *max_logit_out, void *stream);
+
 /* Number of kernels this library has enqueued (all threads) since it was loaded.
  * Graph replays do not pass through the library and are not counted. */
 uint64_t bd_kernel_launches(void);

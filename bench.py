@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-b8", action="store_true")
+    ap.add_argument("--workload", default="b1", choices=["b1", "b8"],
+                    help="the main line's workload (b1: the metric's configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--profile-case", action="store_true",
@@ -438,7 +440,7 @@ def main():
         print(json.dumps({"profile_case": geo.name, "layers": 1, "ok": True}))
         return
 
-    geo = bdsynth.DSPINE27B_B1
+    geo = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8
     st = State(geo, args.seed)
     n0 = binding.kernel_launches()
     st.step()
@@ -485,7 +487,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_per_step": launches_per_step,
     }
-    if not args.no_b8:
+    if not args.no_b8 and args.workload == "b1":
         geo8 = bdsynth.DSPINE27B_B8
         st8 = State(geo8, args.seed, weights=st.w)
         ms8, per8 = time_graphs(st8, args.steps, args.warmup, world)

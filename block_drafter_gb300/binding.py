@@ -23,7 +23,8 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
           -4: "BD_ERR_DEVICE_TIMEOUT", -5: "BD_ERR_WORKSPACE"}
 
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
-           "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches")
+           "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
+           "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc")
 
 
 class BdError(RuntimeError):
@@ -54,7 +55,8 @@ class Weights(C.Structure):
     _fields_ = [("w_feature", C.c_void_p), ("context_norm", C.c_void_p),
                 ("final_norm", C.c_void_p), ("embed_head", C.c_void_p), ("codebook", C.c_void_p),
                 ("g_recv", C.c_void_p), ("g_pred", C.c_void_p), ("a_val", C.c_void_p),
-                ("gate_bias", C.c_void_p), ("layer", LayerWeights * MAX_LAYERS)]
+                ("gate_bias", C.c_void_p), ("layer", LayerWeights * MAX_LAYERS),
+                ("packed", C.c_void_p)]
 
 
 class KvCache(C.Structure):
@@ -90,6 +92,10 @@ def lib() -> C.CDLL:
         L.bd_sync_status.restype = i
         L.bd_sync_status.argtypes = [vp]
         L.bd_kernel_launches.restype = C.c_uint64
+        L.bd_packed_bytes.restype = sz
+        L.bd_packed_bytes.argtypes = [C.POINTER(Config)]
+        L.bd_pack_weights.restype = i
+        L.bd_pack_weights.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, sz, vp]
         L.bd_lm_head_argmax_noalloc.restype = i
         L.bd_lm_head_argmax_noalloc.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, vp,
                                                 vp, vp]
@@ -157,6 +163,23 @@ def make_kv(k: Sequence[torch.Tensor], v: Sequence[torch.Tensor], b_max: int) ->
 # ------------------------------------------------------------------ entry points
 def abi_version() -> int:
     return lib().bd_abi_version()
+
+
+def packed_bytes(cfg: Config) -> int:
+    n = lib().bd_packed_bytes(C.byref(cfg))
+    if n == 0:
+        raise BdError(-1, "invalid config for bd_packed_bytes")
+    return n
+
+
+def pack_weights(cfg: Config, weights: Weights, packed: torch.Tensor, stream=None) -> int:
+    """Writes the packed image into ``packed`` (uint8 device tensor) at its first
+    1024-byte aligned address and returns that address (to store in weights.packed)."""
+    base = packed.data_ptr()
+    aligned = (base + 1023) // 1024 * 1024
+    nbytes = packed.numel() - (aligned - base)
+    _check(lib().bd_pack_weights(C.byref(cfg), C.byref(weights), aligned, nbytes, _stream(stream)))
+    return aligned
 
 
 def workspace_bytes(cfg: Config, b_max: int, max_masks: int, max_ctx_rows: int) -> int:

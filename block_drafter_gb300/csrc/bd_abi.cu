@@ -93,6 +93,8 @@ std::string check_config(const bd_config *c) {
 std::string check_weights(const bd_config *c, const bd_weights *w) {
   if (!w) return "weights are NULL";
   auto chk = [](const void *p) { return p != nullptr && aligned16(p); };
+  if (w->packed && (reinterpret_cast<uintptr_t>(w->packed) & 1023))
+    return "packed image not 1024-byte aligned";
   if (!chk(w->w_feature) || !chk(w->context_norm) || !chk(w->final_norm) || !chk(w->embed_head))
     return "a shared weight pointer is NULL or not 16-byte aligned";
   if (c->code_width > 0) {
@@ -146,7 +148,8 @@ int att_splits(const bd_config *c, int l, int B, int W, int sms) {
   const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
   const int max_keys = ctx + W;
   const int max_splits = (max_keys + 127) / 128;  // at least two 64-key blocks per split
-  int s = (sms + B * c->n_kv_heads - 1) / (B * c->n_kv_heads);
+  // two attention CTAs fit per SM: fill 2 * SMs slots in a single wave
+  int s = (2 * sms) / (B * c->n_kv_heads);
   if (s < 1) s = 1;
   return s < max_splits ? s : max_splits;
 }
@@ -282,9 +285,11 @@ GemmPlan make_plan(const bd_config *c, const void *x, int n_tok, int K) {
   p.args.vocab = c->vocab;
   return p;
 }
-void add_w(GemmPlan &p, const void *ptr, int rows) {
+void add_w(GemmPlan &p, const void *ptr, int rows, const uint8_t *packed_base = nullptr,
+           size_t packed_off = 0) {
   p.w[p.n_w].ptr = ptr;
   p.w[p.n_w].rows = rows;
+  p.w[p.n_w].packed = packed_base ? packed_base + packed_off : nullptr;
   ++p.n_w;
 }
 
@@ -322,6 +327,24 @@ size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int ma
   return need;
 }
 
+size_t bd_packed_bytes(const bd_config *cfg) {
+  if (!check_config(cfg).empty()) return 0;
+  return packed_layout(cfg).total;
+}
+
+bd_status bd_pack_weights(const bd_config *cfg, const bd_weights *w, void *packed,
+                          size_t packed_bytes, void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if ((e = check_weights(cfg, w)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if (!packed || (reinterpret_cast<uintptr_t>(packed) & 1023))
+    return fail(BD_ERR_INVALID_ARG, "packed image NULL or not 1024-byte aligned");
+  if (packed_bytes < packed_layout(cfg).total)
+    return fail(BD_ERR_INVALID_ARG, "packed image smaller than bd_packed_bytes()");
+  BD_TRY(pack_all(cfg, w, static_cast<uint8_t *>(packed), static_cast<cudaStream_t>(stream_)));
+  return BD_OK;
+}
+
 bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                                 const void *target_feats, const int32_t *row_request,
                                 const int64_t *row_pos, const int64_t *ctx_frontier, int n_rows,
@@ -345,12 +368,14 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
   const int H = cfg->hidden, D = cfg->head_dim, KD = cfg->n_kv_heads * D;
   const RopeFreq freq = rope_freq(cfg);
   const GemmScratch sc = scratch_of(mw.g);
+  const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
+  const PackedLayout PL = packed_layout(cfg);
 
   BD_TRY(memset_counters(mw.g, s));
   BD_TRY(launch_rope_table(row_pos, n_rows, mw.rope, D / 2, freq, s));
   {  // S1: W_feature s_t (fp32 out), then plain_rmsnorm with context_norm
     GemmPlan p = make_plan(cfg, target_feats, n_rows, cfg->n_target_layers * H);
-    add_w(p, w->w_feature, H);
+    add_w(p, w->w_feature, H, pk, PL.w_feature);
     p.args.epi = EPI_STORE_F32;
     p.args.out_f32 = mw.feat;
     p.args.ld_out = H;
@@ -368,8 +393,8 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
     p.args.ld_out = ldkv;
     for (int l = l0; l < l1; ++l) {
       const int sk = p.n_w;
-      add_w(p, w->layer[l].wk, KD);
-      add_w(p, w->layer[l].wv, KD);
+      add_w(p, w->layer[l].wk, KD, pk, PL.wk[l]);
+      add_w(p, w->layer[l].wv, KD, pk, PL.wv[l]);
       p.args.seg[sk].out_col = l * 2 * KD;
       p.args.seg[sk + 1].out_col = l * 2 * KD + KD;
     }
@@ -446,7 +471,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const RopeFreq freq = rope_freq(cfg);
   const GemmScratch sc = scratch_of(rw.g);
   const int dt = cfg->dtype;
-  const bool split = dt == BD_BF16;  // bf16 activations enter the GEMMs as hi+lo pairs
+  const bool split = dt == BD_BF16;
+  const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
+  const PackedLayout PL = packed_layout(cfg);  // bf16 activations enter the GEMMs as hi+lo pairs
   auto lo = [&](int K) -> size_t { return split ? static_cast<size_t>(TP) * K : 0; };
 
   BD_TRY(memset_counters(rw.g, s));
@@ -461,9 +488,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
       p.split = split;
-      add_w(p, L.wq, QD);
-      add_w(p, L.wk, KD);
-      add_w(p, L.wv, KD);
+      add_w(p, L.wq, QD, pk, PL.wq[l]);
+      add_w(p, L.wk, KD, pk, PL.wk[l]);
+      add_w(p, L.wv, KD, pk, PL.wv[l]);
       p.args.epi = EPI_STORE_F32;
       p.args.out_f32 = rw.qkv_raw;
       p.args.ld_out = QD + 2 * KD;
@@ -522,7 +549,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     {
       GemmPlan p = make_plan(cfg, rw.att, T, QD);
       p.split = split;
-      add_w(p, L.wo, H);
+      add_w(p, L.wo, H, pk, PL.wo[l]);
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
       p.args.ld_out = H;
@@ -536,8 +563,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
       p.split = split;
-      add_w(p, L.w_gate, cfg->ffn);
-      add_w(p, L.w_up, cfg->ffn);
+      add_w(p, L.w_gate, cfg->ffn, pk, PL.gate_up[l]);
+      add_w(p, L.w_up, cfg->ffn, pk, PL.gate_up[l]);
       p.pair_mode = true;
       p.args.epi = EPI_SWIGLU;
       p.args.out_act = rw.hmid;
@@ -548,7 +575,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     {
       GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
       p.split = split;
-      add_w(p, L.w_down, H);
+      add_w(p, L.w_down, H, pk, PL.w_down[l]);
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
       p.args.ld_out = H;
@@ -564,7 +591,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       {
         GemmPlan p = make_plan(cfg, rw.xn, T, H);
         p.split = split;
-        add_w(p, L.r_read, Rc);
+        add_w(p, L.r_read, Rc, pk, PL.r_read[l]);
         p.args.epi = EPI_STORE_F32;
         p.args.out_f32 = rw.z;
         p.args.ld_out = Rc;
@@ -576,9 +603,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       {
         GemmPlan p = make_plan(cfg, rw.c, T, Rc);
         p.split = split;
-        add_w(p, w->g_recv, Mc);
-        add_w(p, w->g_pred, Mc);
-        add_w(p, w->a_val, Mc);
+        add_w(p, w->g_recv, Mc, pk, PL.g_recv);
+        add_w(p, w->g_pred, Mc, pk, PL.g_pred);
+        add_w(p, w->a_val, Mc, pk, PL.a_val);
         p.args.epi = EPI_STORE_F32;
         p.args.out_f32 = rw.pre;
         p.args.ld_out = 3 * Mc;
@@ -591,7 +618,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       {
         GemmPlan p = make_plan(cfg, rw.m, T, Mc);
         p.split = split;
-        add_w(p, L.w_write, H);
+        add_w(p, L.w_write, H, pk, PL.w_write[l]);
         p.args.epi = EPI_INJECT;
         p.args.out_f32 = rw.x;
         p.args.ld_out = H;
@@ -634,7 +661,8 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
                              static_cast<size_t>(pad16(rows)) * cfg->hidden, s));
   GemmPlan p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
   p.split = split;
-  add_w(p, w->embed_head, cfg->vocab);
+  add_w(p, w->embed_head, cfg->vocab, static_cast<const uint8_t *>(w->packed),
+        w->packed ? packed_layout(cfg).head : 0);
   p.args.epi = EPI_ARGMAX;
   p.args.amax_val = hw.amax_val;
   p.args.amax_idx = hw.amax_idx;
@@ -647,7 +675,8 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
 bd_status bd_sync_status(void *stream_) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
-  const unsigned word = take_error_word_gemm() | take_error_word_att() | take_error_word_small();
+  const unsigned word = take_error_word_gemm() | take_error_word_att() | take_error_word_small() |
+                        take_error_word_pack();
   if (word & DEVERR_TIMEOUT) return fail(BD_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
   if (word & DEVERR_BAD_INDEX)
     return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");

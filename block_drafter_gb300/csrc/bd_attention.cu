@@ -17,6 +17,8 @@
 #include "bd_internal.h"
 #include "bd_kernels.h"
 
+#include <climits>
+
 namespace bd {
 
 BD_DEFINE_ERROR_TAKER(take_error_word_att)
@@ -146,13 +148,12 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
 // are exact bf16 data.  The block's own keys/values (produced this round, hi+lo) are
 // processed by the last split in a separate 16-key pass.
 template <int D>
-__global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_constant__ AttArgs a) {
+__global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_constant__ AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int RS = D + kAttPad;  // smem row stride (elements)
   __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [2][64][RS] hi, lo
   __nv_bfloat16 *sK = sQ + 2 * kAttRows * RS;                          // [2][64][RS]
   __nv_bfloat16 *sV = sK + 2 * kAttKeys * RS;                          // [2][64][RS]
-  __nv_bfloat16 *sB = sV + 2 * kAttKeys * RS;                          // [4][16][RS] Kh Kl Vh Vl
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -195,7 +196,11 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
       cp_async16(smem_u32(sV + (buf * kAttKeys + kr) * RS + ch * 8), ring_v + off + ch * 8, valid);
     }
   };
-  if (do_block) {  // block keys/values: [Kh; Kl; Vh; Vl], 16 rows each (rows >= W zero)
+  // Block keys/values [Kh; Kl; Vh; Vl] (16 rows each, rows >= W zero) go into the K
+  // buffer the context loop leaves free after its last block (buffer n_blocks & 1); they
+  // are loaded while that last block is processed.
+  auto load_block = [&](int buf) {
+    __nv_bfloat16 *dstb = sK + buf * kAttKeys * RS;
     for (int c = tid; c < 4 * 16 * CPR; c += 128) {
       const int part = c / (16 * CPR), cc = c % (16 * CPR);
       const int j = cc / CPR, ch = cc % CPR;
@@ -203,9 +208,9 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
       const __nv_bfloat16 *base = (part < 2 ? blk_k : blk_v) + ((part & 1) ? a.blk_lo : 0);
       const __nv_bfloat16 *src =
           base + ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.W + (valid ? j : 0)) * D + ch * 8;
-      cp_async16(smem_u32(sB + (part * 16 + j) * RS + ch * 8), src, valid);
+      cp_async16(smem_u32(dstb + (part * 16 + j) * RS + ch * 8), src, valid);
     }
-  }
+  };
 
   float o[D / 8][4];
 #pragma unroll
@@ -220,7 +225,10 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
 
   const int n_blocks = g.k_end > g.k_begin ? (g.k_end - g.k_begin + kAttKeys - 1) / kAttKeys : 0;
   if (n_blocks > 0) load_kv(0, g.k_begin);
+  else if (do_block) load_block(0);
   cp_async_commit();
+  // the first context position every block row can see: keys from here on need no mask
+  const long long p_all = a.window > 0 ? g.F + a.W - a.window : LLONG_MIN;
   cp_async_wait<0>();
   __syncthreads();
 
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
     const int buf = blk & 1;
     const int k0 = g.k_begin + blk * kAttKeys;
     if (blk + 1 < n_blocks) load_kv(buf ^ 1, k0 + kAttKeys);
+    else if (do_block) load_block(buf ^ 1);
     cp_async_commit();
 
     // S = (Qh + Ql) K^T for 16 rows x 64 keys
@@ -260,15 +269,22 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
         mma16816(s[nt + 1], ql, b2, b3);
       }
     }
+    if (k0 + kAttKeys <= g.k_end && g.p_lo + k0 >= p_all) {  // every key visible to every row
 #pragma unroll
-    for (int nt = 0; nt < kAttKeys / 8; ++nt)
+      for (int nt = 0; nt < kAttKeys / 8; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = k0 + nt * 8 + 2 * t4 + (e & 1);
-        const bool top = e < 2;
-        const bool vis = (top ? rvA : rvB) && ctx_visible(a, g, top ? iA : iB, k);
-        s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
-      }
+        for (int e = 0; e < 4; ++e) s[nt][e] *= sl2;
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < kAttKeys / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = k0 + nt * 8 + 2 * t4 + (e & 1);
+          const bool top = e < 2;
+          const bool vis = (top ? rvA : rvB) && ctx_visible(a, g, top ? iA : iB, k);
+          s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
+        }
+    }
     float alpha[2];
     softmax_update<kAttKeys / 8>(s, m_run, l_run, alpha);
 #pragma unroll
@@ -304,6 +320,11 @@ __global__ void __launch_bounds__(128) attention_bf16_kernel(const __grid_consta
   }
 
   if (do_block) {
+    if (n_blocks == 0) {  // the block tile was loaded with Q; nothing else is in flight
+      cp_async_wait<0>();
+      __syncthreads();
+    }
+    const __nv_bfloat16 *sB = sK + (n_blocks & 1) * kAttKeys * RS;  // [Kh; Kl; Vh; Vl]
     // S = Qh Kh + Ql Kh + Qh Kl over the (up to) 16 block keys
     float s[2][4];
 #pragma unroll
@@ -522,7 +543,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(const __grid_constan
 }
 
 size_t attention_smem_bytes(int head_dim) {
-  return static_cast<size_t>(2 * kAttRows + 4 * kAttKeys + 4 * 16) * (head_dim + kAttPad) * 2;
+  return static_cast<size_t>(2 * kAttRows + 4 * kAttKeys) * (head_dim + kAttPad) * 2;
 }
 size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim) {
   return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows * head_dim;

@@ -115,6 +115,14 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
   auto load_a = [&](int m_tile, int kbi, uint8_t *dst, uint64_t *bar) {
     const int s = p.pair_mode ? 0 : seg_of_tile(p, m_tile);
     const int nb = boxes(kbi);
+    if (p.packed) {  // the unit's boxes are one contiguous piece of the packed image
+      const GemmSeg &sg = p.seg[s];
+      const size_t box0 = static_cast<size_t>(m_tile - sg.tile_begin) * sg.n_kb_pack +
+                          static_cast<size_t>(kbi) * KB;
+      bulk_load(dst, sg.packed + box0 * kATileBytes, static_cast<uint32_t>(nb) * kATileBytes, bar,
+                pol_w);
+      return;
+    }
     for (int j = 0; j < nb; ++j) {
       const int x = (kbi * KB + j) * BK;
       uint8_t *d = dst + static_cast<size_t>(j) * kATileBytes;
@@ -534,7 +542,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.b);
-    for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
+    if (!p.packed)
+      for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, ncols);
@@ -761,10 +770,20 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
 
   GemmMaps maps;
   memset(&maps, 0, sizeof maps);
-  for (int s = 0; s < plan.n_w; ++s) {
-    std::string err = make_map(&maps.a[s], plan.w[s].ptr, plan.dtype, plan.K, plan.w[s].rows, BK,
-                               plan.pair_mode ? 64 : kBM);
-    if (!err.empty()) return err;
+  a.packed = plan.w[0].packed != nullptr ? 1 : 0;
+  if (a.packed) {
+    const int elem = plan.dtype == 0 ? 2 : 4;
+    for (int s = 0; s < a.n_segs; ++s) {
+      if (!plan.w[s].packed) return "packed GEMM with an unpacked segment";
+      a.seg[s].packed = static_cast<const uint8_t *>(plan.w[s].packed);
+      a.seg[s].n_kb_pack = static_cast<int>(packed_kb(plan.K, elem));
+    }
+  } else {
+    for (int s = 0; s < plan.n_w; ++s) {
+      std::string err = make_map(&maps.a[s], plan.w[s].ptr, plan.dtype, plan.K, plan.w[s].rows, BK,
+                                 plan.pair_mode ? 64 : kBM);
+      if (!err.empty()) return err;
+    }
   }
   std::string err = plan.split
       ? make_map(&maps.b, plan.x, plan.dtype, plan.K, 2 * a.lo_row, BK, a.ln)

@@ -8,6 +8,8 @@
 #include <string>
 #include <utility>
 
+#include "blockdrafter.h"
+
 namespace bd {
 
 // Device error word flags (set by kernels, read and cleared by bd_sync_status()).
@@ -32,10 +34,11 @@ enum EpiMode : int {
 // Epilogue code runs once per tile, so it is kept short: the instruction fetches of
 // long straight-line epilogues dominated the tail of small launches.
 struct GemmSeg {
-  int rows;          // output rows of this weight matrix
-  int tile_begin;    // first m-tile of the segment
-  int out_col;       // EPI_STORE_F32: column offset of this segment in the output row
-  int pad_;
+  int rows;               // output rows of this weight matrix
+  int tile_begin;         // first m-tile of the segment
+  int out_col;            // EPI_STORE_F32: column offset of this segment in the output row
+  int n_kb_pack;          // packed: 128-byte K boxes per 128-row tile
+  const uint8_t *packed;  // packed image of this matrix (see PackedLayout), or null
 };
 
 struct __align__(16) GemmArgs {
@@ -47,6 +50,7 @@ struct __align__(16) GemmArgs {
   // two halves, so activations enter at ~16-bit instead of 8-bit mantissa precision
   // while the weight tile is still read once.
   int split, ln, lo_row;
+  int packed;                     // weights come from packed images (contiguous bulk copies)
   long long units;
   int epi;
   int ld_out, ld_resid, ld_act, block_w, vocab;
@@ -71,6 +75,7 @@ struct GemmMaps {
 struct GemmWeight {
   const void *ptr;
   int rows;
+  const void *packed;  // packed image of the matrix (pair mode: the interleaved pair), or null
 };
 struct GemmPlan {
   int dtype;                 // 0 bf16, 1 fp32
@@ -95,6 +100,28 @@ struct GemmScratch {
 unsigned take_error_word_gemm();
 unsigned take_error_word_att();
 unsigned take_error_word_small();
+
+// ------------------------------------------------------------------ packed weights
+// Packed image of one [rows, K] matrix: 128-row tiles, each split into 128-byte K boxes;
+// box (tile t, box k) is 16 KB at ((t * n_kb) + k) * 16384, in the 128-byte-swizzled
+// shared-memory order (16-byte chunk c of row r stored at chunk c ^ (r % 8)).  A pair
+// image (SwiGLU gate/up) has tiles of 64 gate rows followed by the same 64 up rows.
+constexpr size_t kPackBox = 16384;
+inline size_t packed_kb(int K, int elem) { return (static_cast<size_t>(K) * elem + 127) / 128; }
+inline size_t packed_matrix_bytes(int rows, int K, int elem, bool pair) {
+  const size_t rt = pair ? (static_cast<size_t>(rows) + 63) / 64 : (static_cast<size_t>(rows) + 127) / 128;
+  return rt * packed_kb(K, elem) * kPackBox;
+}
+struct PackedLayout {
+  size_t w_feature, head, g_recv, g_pred, a_val;
+  size_t wq[BD_MAX_LAYERS], wk[BD_MAX_LAYERS], wv[BD_MAX_LAYERS], wo[BD_MAX_LAYERS];
+  size_t gate_up[BD_MAX_LAYERS], w_down[BD_MAX_LAYERS], r_read[BD_MAX_LAYERS],
+      w_write[BD_MAX_LAYERS];
+  size_t total;
+};
+PackedLayout packed_layout(const bd_config *c);
+std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cudaStream_t s);
+unsigned take_error_word_pack();
 
 size_t gemm_partial_floats(int n_ctas, int block_n);
 int num_sms();

@@ -137,6 +137,8 @@ extern "C" bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_we
   p.split = split;
   p.w[0].ptr = w->embed_head;
   p.w[0].rows = cfg->vocab;
+  p.w[0].packed = w->packed ? static_cast<const uint8_t *>(w->packed) + packed_layout(cfg).head
+                            : nullptr;
   p.n_w = 1;
   p.args.vocab = cfg->vocab;
   p.args.epi = EPI_ARGMAX;

@@ -28,13 +28,18 @@ def config_of(geo, mask_id: int) -> B.Config:
 
 class DraftSession:
     def __init__(self, geo, weights: dict, mask_id: int, b_max: int, max_masks: int = 15,
-                 max_ctx_rows: int = 2048, device="cuda"):
+                 max_ctx_rows: int = 2048, device="cuda", packed: bool = True):
         self.geo = geo
         self.device = torch.device(device)
         self.dtype = torch.bfloat16 if geo.dtype == "bf16" else torch.float32
         self.cfg = config_of(geo, mask_id)
         self.weights = weights
         self.wstruct = B.make_weights(self.cfg, weights)
+        self.packed = None
+        if packed:  # one-time packed image: GEMMs stream contiguous weight tiles from it
+            self.packed = torch.empty(B.packed_bytes(self.cfg) + 1024, dtype=torch.uint8,
+                                      device=self.device)
+            self.wstruct.packed = B.pack_weights(self.cfg, self.wstruct, self.packed)
         self.b_max = b_max
         self.k = [torch.zeros(b_max, geo.n_kv_heads, geo.capacity(l), geo.head_dim,
                               dtype=self.dtype, device=self.device) for l in range(geo.n_layers)]

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 1
+#define BD_ABI_VERSION 2
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -104,6 +104,11 @@ typedef struct {
   const void *a_val;        /* [Mc, Rc] predecessor value map A, shared                   */
   const void *gate_bias;    /* [Mc] gate bias b, or NULL for b = 0                        */
   bd_layer_weights layer[BD_MAX_LAYERS];
+  /* Optional packed image of every projection matrix written by bd_pack_weights (dev,
+   * caller-owned), or NULL.  When set, the tensor-core products stream weight tiles from
+   * it (one contiguous copy per pipeline stage); the row-major matrices above are still
+   * required (embedding rows, norm gains, codebook and the raw layout are read from them). */
+  const void *packed;
 } bd_weights;
 
 /* Context K/V rings ([DFlash-notes], ring storage): layer l holds
@@ -124,6 +129,21 @@ int bd_abi_version(void);
  * requests with up to `max_masks` masks (K) and materialisations of up to
  * `max_ctx_rows` rows per call.  Returns 0 for an invalid or unsupported config. */
 size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int max_ctx_rows);
+
+/* Bytes of the packed weight image for `cfg` (0 for an invalid config). */
+size_t bd_packed_bytes(const bd_config *cfg);
+
+/*
+ * Writes the packed image of every projection matrix of `w` into `packed` (dev,
+ * caller-owned, >= bd_packed_bytes(cfg) bytes, 1024-byte aligned).  The image holds each
+ * matrix as 128-row x 128-byte tiles, each tile contiguous and already in the 128-byte
+ * swizzled order the tensor cores read from shared memory (the SwiGLU gate and up
+ * matrices interleaved 64 rows each per tile); out-of-range rows/columns are zero.  It is
+ * a pure permutation of the weights: results are identical with or without it.  Run it
+ * once after loading the weights, then set w->packed = packed.
+ */
+bd_status bd_pack_weights(const bd_config *cfg, const bd_weights *w, void *packed,
+                          size_t packed_bytes, void *stream);
 
 /*
  * Context K/V materialisation (S1 + S2).  [DFlash-notes], conditioning and context K/V:

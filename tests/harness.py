@@ -58,7 +58,7 @@ class Case:
 
     def __init__(self, geo: bdsynth.Workload, seed: int = 0, *, zero_write=False, gate_bias=False,
                  frontiers: Optional[List[int]] = None, anchors: Optional[List[int]] = None,
-                 gen_device="cpu", max_ctx_rows: int = 2048, weights=None):
+                 gen_device="cpu", max_ctx_rows: int = 2048, weights=None, packed: bool = True):
         from block_drafter_gb300.session import DraftSession
         self.geo, self.seed = geo, seed
         self.mask_id = bdsynth.mask_token_id(geo, seed)
@@ -70,7 +70,7 @@ class Case:
         self.w_host = w
         self.gen_device = gen_device
         self.sess = DraftSession(geo, self.w_dev, self.mask_id, b_max=geo.batch,
-                                 max_masks=geo.n_masks, max_ctx_rows=max_ctx_rows)
+                                 max_masks=geo.n_masks, max_ctx_rows=max_ctx_rows, packed=packed)
         self.max_ctx_rows = max_ctx_rows
 
     # ---- context

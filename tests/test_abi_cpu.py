@@ -38,7 +38,8 @@ def test_library_exports_every_declared_symbol(B):
     for s in header_symbols():
         assert hasattr(L, s), s
     assert set(B.EXPORTS) <= set(header_symbols())
-    assert B.abi_version() == 1
+    hdr = open(os.path.join(ROOT, "include", "blockdrafter.h")).read()
+    assert B.abi_version() == int(re.search(r"#define BD_ABI_VERSION (\d+)", hdr).group(1))
 
 
 def cfg_of(w, **kw):
@@ -148,3 +149,18 @@ def test_ring_capacity_must_hold_the_window(B):
     c = cfg_of(bdsynth.DSPINE27B_B1)
     c.ring_capacity[2] = 100
     assert B.lib().bd_workspace_bytes(C.byref(c), 1, 15, 16) == 0
+
+
+def test_packed_bytes_cover_every_matrix(B):
+    """The packed image holds each projection matrix once (plus tile padding)."""
+    for name in ("dspine_b16_27b_b1", "dflash_35b_a3b_b8", "tiny_fp32"):
+        w = bdsynth.WORKLOADS[name]
+        c = cfg_of(w)
+        n = B.lib().bd_packed_bytes(C.byref(c))
+        el = 2 if w.dtype == "bf16" else 4
+        H, QD, KD = w.hidden, w.n_q_heads * w.head_dim, w.n_kv_heads * w.head_dim
+        mats = H * w.n_target_layers * H + w.vocab * H + w.n_layers * (QD * H + 2 * KD * H + H * QD + 3 * H * w.ffn)
+        if w.code_width:
+            mats += 3 * w.msg_width * w.code_width + w.n_layers * (w.code_width * H + H * w.msg_width)
+        assert n >= mats * el
+        assert n < mats * el * 1.05 + (16 << 20)

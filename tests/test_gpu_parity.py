@@ -151,3 +151,18 @@ def test_round_is_deterministic_and_requests_independent():
     W = geo.W
     assert torch.equal(g3["hidden"][:2 * W], g1["hidden"][:2 * W])
     assert not torch.equal(g3["hidden"][2 * W:], g1["hidden"][2 * W:])
+
+
+@pytest.mark.parametrize("geo", [SMALL_BF16, bdsynth.TINY])
+def test_packed_and_raw_weights_give_identical_results(geo):
+    """The packed image is a permutation of the weights: materialisation, round and head
+    must be bit-identical with and without it."""
+    a = Hn.Case(geo, seed=8, max_ctx_rows=128, packed=True)
+    b = Hn.Case(geo, seed=8, max_ctx_rows=128, packed=False, weights=a.w_host)
+    a.fill_rings()
+    b.fill_rings()
+    for l in range(geo.n_layers):
+        assert torch.equal(a.sess.k[l], b.sess.k[l]) and torch.equal(a.sess.v[l], b.sess.v[l])
+    ga, gb = a.run_gpu(), b.run_gpu()
+    for key in ("layers", "hidden", "tokens", "max_logit"):
+        assert torch.equal(ga[key], gb[key]), key

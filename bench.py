@@ -51,8 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--profile-case", action="store_true",
-                    help="run one step of a one-layer 27B-geometry round (B=1) and exit: "
-                         "the small case the ncu captures use")
+                    help="run two steps of a one-layer 27B-geometry round (batch from "
+                         "--workload) and exit: the small case the ncu captures use")
     return ap.parse_args()
 
 
@@ -429,12 +429,18 @@ def main():
     builder.build()
     binding.lib()
     if args.profile_case:
-        # GEMM launch order of this case: [0] W_feature and [1] K/V of the ring fill, then
-        # the step: [2] W_feature, [3] K/V, [4] QKV, [5] W_o, [6] gate/up, [7] down,
-        # [8] code read, [9] gate/value maps, [10] write, [11] LM head.
-        geo = bdsynth.DSPINE27B_B1.with_(n_layers=1, windows=(2048,))
+        # One warm step, then the profiled step inside the NVTX range "profiled_step"
+        # (ncu --nvtx --nvtx-include "profiled_step/").  GEMM launch order of the step:
+        # [0] W_feature, [1] K/V, [2] QKV, [3] W_o, [4] gate/up, [5] down, [6] code read,
+        # [7] gate/value maps, [8] write, [9] LM head.
+        base = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8
+        geo = base.with_(n_layers=1, windows=(2048,))
         st = State(geo, args.seed)
         st.step()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("profiled_step")
+        st.step()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         binding.sync_status()
         print(json.dumps({"profile_case": geo.name, "layers": 1, "ok": True}))

@@ -170,7 +170,7 @@ void carve_gemm(Carve &cv, GemmWs &g, int max_block_n, size_t max_tiles, int sms
   g.partial_floats = gemm_partial_floats(sms, max_block_n);
   g.partials = cv.take<float>(g.partial_floats);
   g.n_counters = max_tiles;
-  g.counters = cv.take<unsigned>(max_tiles);
+  g.counters = cv.take<unsigned>(2 * max_tiles);  // arrival and done counters
 }
 
 size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + tile_rows - 1) / tile_rows); }
@@ -271,7 +271,7 @@ GemmScratch scratch_of(const GemmWs &g) {
 }
 
 std::string memset_counters(const GemmWs &g, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(g.counters, 0, g.n_counters * sizeof(unsigned), s);
+  cudaError_t e = cudaMemsetAsync(g.counters, 0, 2 * g.n_counters * sizeof(unsigned), s);
   return e == cudaSuccess ? std::string() : std::string("memset: ") + cudaGetErrorString(e);
 }
 
@@ -553,8 +553,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
       p.args.ld_out = H;
-      p.args.resid = rw.x;
-      p.args.ld_resid = H;
       BD_TRY(launch_gemm(p, sc, s));
     }
     // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m)
@@ -579,8 +577,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.epi = EPI_RESID_F32;
       p.args.out_f32 = rw.x;
       p.args.ld_out = H;
-      p.args.resid = rw.x;
-      p.args.ld_resid = H;
       BD_TRY(launch_gemm(p, sc, s));
     }
     if (cfg->code_width > 0) {

@@ -9,9 +9,10 @@
 //
 // Work split (stream-K): the (tile, k-block) units of all segments are cut into n_ctas
 // contiguous ranges of equal length, so every SM streams the same number of weight bytes
-// whatever the matrix shapes.  A tile split between CTAs is finished by the CTA that
-// arrives last on the tile's counter; it adds the other CTAs' partial tiles in CTA
-// order, so results do not depend on arrival order.  No CTA ever waits on another.
+// whatever the matrix shapes.  The CTAs that share a tile store fp32 partial tiles and,
+// after their own mainloops, each sums a share of the tile over all partials in CTA
+// order, so results do not depend on arrival order.  These are the only waits between
+// CTAs; a launch never has more CTAs than SMs.
 //
 // Warp roles: warp 0 = TMA producer (one lane), warp 1 = TMEM owner and MMA issuer (one
 // lane), warps 2-5 = epilogue (128 threads, one accumulator row each).
@@ -48,16 +49,22 @@ constexpr size_t kSmemLimit = 232448 - 1024;  // 227 KB opt-in per block, less s
 // A pipeline stage holds kbox K-boxes of the weight tile (each 128 rows x 128 bytes, so
 // every weight row is read in kbox*128-byte contiguous pieces) and the matching kbox
 // boxes of the activation tile.
+constexpr int kOutStage = 16 * kBM * 4;  // 8 KB: one 16-column chunk of fp32 results
+
+// Stage area (the pipeline), then the epilogue's buffers: exchange, two output staging
+// buffers, argmax scratch, INJECT row scales, barriers.
 struct SmemLayout {
-  size_t off_b, off_x, off_red, off_bar, total;
+  size_t off_b, off_x, off_out, off_red, off_rs, off_bar, total;
 };
 __host__ __device__ inline SmemLayout smem_layout(int stages, int block_n, int kbox) {
   SmemLayout L;
   L.off_b = static_cast<size_t>(stages) * kbox * kATileBytes;
   L.off_x = L.off_b + static_cast<size_t>(stages) * kbox * block_n * 128;
-  L.off_red = L.off_x + kBM * kXStride * 4;
-  L.off_bar = L.off_red + 2 * 64 * 4;
-  L.total = L.off_bar + (2 * stages + 4) * 8 + 16 + 1024;  // + alignment slack
+  L.off_out = (L.off_x + kBM * kXStride * 4 + 1023) / 1024 * 1024;
+  L.off_red = L.off_out + 2 * kOutStage;
+  L.off_rs = L.off_red + 2 * 64 * 4;
+  L.off_bar = L.off_rs + 256 * 4;
+  L.total = L.off_bar + (2 * stages + 5) * 8 + 16 + 1024;  // + alignment slack
   return L;
 }
 
@@ -240,145 +247,6 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
   }
 }
 
-// ------------------------------------------------------------------ epilogue ops
-// Global operands an epilogue chunk reads (residual row values, the injection scale).  They are loaded before the chunk's accumulator is
-// ready -- for the first chunk while the MMAs still run -- so their latency is hidden.
-struct EpiOperands {
-  float a[16];  // RESID: resid values; INJECT: current x values
-  float b[16];  // INJECT: row scale r[tok]
-};
-
-template <typename T, int EPI>
-__device__ __forceinline__ void epi_load(const GemmArgs &p, int m_tile, int r, int tok0,
-                                         EpiOperands &op) {
-  switch (EPI) {
-    case EPI_RESID_F32:
-    case EPI_INJECT: {
-      const int s = seg_of_tile(p, m_tile);
-      const int row = (m_tile - p.seg[s].tile_begin) * kBM + r;
-      if (row >= p.seg[s].rows) break;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int tok = tok0 + jj;
-        if (tok < p.n_tokens) {
-          if (EPI == EPI_RESID_F32) {
-            op.a[jj] = p.resid[static_cast<size_t>(tok) * p.ld_resid + row];
-          } else {
-            op.a[jj] = p.out_f32[static_cast<size_t>(tok) * p.ld_out + row];
-            op.b[jj] = p.row_scale[tok];
-          }
-        }
-      }
-      break;
-    }
-    default:
-      break;
-  }
-}
-
-// Each op gets the fp32 values v[0..15] of tile row r (0..127) for token columns
-// tok0 .. tok0+15 and must call the same named barriers on all 128 threads.
-template <typename T, int EPI>
-__device__ __forceinline__ void epi_chunk(const GemmArgs &p, int m_tile, int r, int tok0,
-                                          float (&v)[16], const EpiOperands &op, float *xbuf,
-                                          float *red, int32_t *redi) {
-  const int q = r >> 5;
-  const int lane = r & 31;
-  switch (EPI) {
-    case EPI_STORE_F32:
-    case EPI_RESID_F32:
-    case EPI_INJECT: {
-      const int s = seg_of_tile(p, m_tile);
-      const int row = (m_tile - p.seg[s].tile_begin) * kBM + r;
-      if (row >= p.seg[s].rows) break;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int tok = tok0 + jj;
-        if (tok >= p.n_tokens) break;
-        const size_t o = static_cast<size_t>(tok) * p.ld_out + row;
-        if (EPI == EPI_STORE_F32) {
-          p.out_f32[o + p.seg[s].out_col] = v[jj];
-        } else if (EPI == EPI_RESID_F32) {
-          p.out_f32[o] = op.a[jj] + v[jj];
-        } else if (tok % p.block_w != 0) {
-          p.out_f32[o] = op.a[jj] + op.b[jj] * v[jj];
-        }
-      }
-      break;
-    }
-    case EPI_SWIGLU: {
-      // rows 0..63: gate features f, rows 64..127: up features f (same f)
-      if (r >= 64) {
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) xbuf[(r - 64) * kXStride + jj] = v[jj];
-      }
-      named_bar(2, 128);
-      if (r < 64) {
-        const int f = m_tile * 64 + r;
-        if (f < p.seg[0].rows) {
-          T *out = static_cast<T *>(p.out_act);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int tok = tok0 + jj;
-            if (tok >= p.n_tokens) break;
-            const float g = v[jj];
-            const float u = xbuf[r * kXStride + jj];
-            const float h = g / (1.0f + __expf(-g)) * u;
-            const T hi = from_f<T>(h);
-            out[static_cast<size_t>(tok) * p.ld_act + f] = hi;
-            if (p.act_lo) out[p.act_lo + static_cast<size_t>(tok) * p.ld_act + f] = from_f<T>(h - to_f<T>(hi));
-          }
-        }
-      }
-      named_bar(2, 128);
-      break;
-    }
-    case EPI_ARGMAX: {
-      const int vid = m_tile * kBM + r;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        float best = vid < p.vocab ? v[jj] : -INFINITY;
-        int bi = vid < p.vocab ? vid : 0x7fffffff;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > best || (ov == best && oi < bi)) {
-            best = ov;
-            bi = oi;
-          }
-        }
-        if (lane == 0) {
-          red[q * 16 + jj] = best;
-          redi[q * 16 + jj] = bi;
-        }
-      }
-      named_bar(2, 128);
-      if (r < 16) {
-        const int tok = tok0 + r;
-        if (tok < p.n_tokens) {
-          float best = red[r];
-          int bi = redi[r];
-          for (int k = 1; k < 4; ++k) {
-            const float ov = red[k * 16 + r];
-            const int oi = redi[k * 16 + r];
-            if (ov > best || (ov == best && oi < bi)) {
-              best = ov;
-              bi = oi;
-            }
-          }
-          p.amax_val[static_cast<size_t>(m_tile) * p.n_tokens + tok] = best;
-          p.amax_idx[static_cast<size_t>(m_tile) * p.n_tokens + tok] = bi;
-        }
-      }
-      named_bar(2, 128);
-      break;
-    }
-    default:
-      break;
-  }
-}
-
 // ------------------------------------------------------------------ epilogue
 // Logical columns j0..j0+15 of the accumulator: the hi half, plus the lo half that sits
 // LW columns further when the activation operand is split.
@@ -393,30 +261,290 @@ __device__ __forceinline__ void tmem_ld_logical(uint32_t tbase, int j0, int LW, 
   }
 }
 
+// Results leave the SM through shared memory: the 128 epilogue threads write a chunk of
+// 16 token columns into one of two staging buffers and one thread hands it to TMA (a
+// tiled store, an in-L2 reduce-add, or a contiguous bulk store).  Stores from the
+// threads themselves stall on write acknowledgements when L2 is busy with the weight
+// stream; the TMA unit takes them off the threads' critical path.
+struct EpiSmem {
+  uint8_t *out;    // [2][kOutStage] staging buffers
+  int next;        // buffer the next chunk uses
+  float *xbuf;     // [128][kXStride] exchange / transpose buffer
+  float *red;      // [4][16] per-warp column maxima
+  int32_t *redi;   // [4][16] their indices
+  float *rs;       // [256] INJECT row scales of the current tile's tokens
+};
+
+// Claims the next staging buffer: the bulk group that last read it (two chunks ago) must
+// have finished reading.  Ends with a barrier of the 128 epilogue threads.
+__device__ __forceinline__ uint8_t *stage_claim(EpiSmem &es, int et) {
+  uint8_t *sb = es.out + es.next * kOutStage;
+  es.next ^= 1;
+  if (et == 0) bulk_wait_read<1>();
+  named_bar(1, 128);
+  return sb;
+}
+// Publishes the staged chunk to the async proxy; thread et == 0 then issues the copy.
+__device__ __forceinline__ void stage_publish() {
+  fence_proxy_async_shared();
+  named_bar(1, 128);
+}
+
+// Per-(vocab tile, token) maximum and its lowest index: the chunk is transposed through
+// shared memory so that each thread scans 16 rows of one column serially (rows in
+// ascending order, so a strict comparison keeps the lowest index), then the two row
+// groups of a warp and the four warps are merged.
+__device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int tok0, int r,
+                                             int et, const float (&v)[16], EpiSmem &es) {
+  const int row_id = m_tile * kBM + r;
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) es.xbuf[r * kXStride + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
+  named_bar(1, 128);
+  const int col = et & 15, grp = et >> 4;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int row = grp * 16 + i;
+    const float x = es.xbuf[row * kXStride + col];
+    if (x > best) {
+      best = x;
+      bi = m_tile * kBM + row;
+    }
+  }
+  const float ob = __shfl_xor_sync(0xffffffffu, best, 16);
+  const int oi = __shfl_xor_sync(0xffffffffu, bi, 16);
+  if (ob > best || (ob == best && oi < bi)) {
+    best = ob;
+    bi = oi;
+  }
+  if ((et & 31) < 16) {
+    es.red[(et >> 5) * 16 + col] = best;
+    es.redi[(et >> 5) * 16 + col] = bi;
+  }
+  named_bar(1, 128);
+  if (et < 16) {
+    float b = es.red[et];
+    int i = es.redi[et];
+    for (int w = 1; w < 4; ++w) {
+      const float x = es.red[w * 16 + et];
+      const int xi = es.redi[w * 16 + et];
+      if (x > b || (x == b && xi < i)) {
+        b = x;
+        i = xi;
+      }
+    }
+    const int tok = tok0 + et;
+    if (tok < p.n_tokens) {
+      p.amax_val[static_cast<size_t>(m_tile) * p.n_tokens + tok] = b;
+      p.amax_idx[static_cast<size_t>(m_tile) * p.n_tokens + tok] = i;
+    }
+  }
+}
+
+// Writes the finished values v (tile row r, token columns tok0..tok0+15; j0 = tok0 minus
+// the tile's first token) of m_tile to the epilogue's destination.
 template <typename T, int EPI>
-__device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
-                              uint32_t tmem_base, long long u0, long long u1, float *xbuf,
-                              float *red, int32_t *redi, volatile int *sflag,
-                              volatile int *sabort) {
+__device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs &p, int m_tile,
+                                           int tok0, int j0, int r, int et,
+                                           const float (&v)[16], EpiSmem &es) {
+  if (EPI == EPI_ARGMAX) {
+    argmax_chunk(p, m_tile, tok0, r, et, v, es);
+    return;
+  }
+  if (EPI == EPI_SWIGLU && r >= 64) {  // up features go to the gate rows' threads
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) es.xbuf[(r - 64) * kXStride + jj] = v[jj];
+  }
+  uint8_t *sb = stage_claim(es, et);
+  if (EPI == EPI_SWIGLU) {
+    // rows 0..63: gate features f, rows 64..127: up features f (same f)
+    if (r < 64) {
+      T *hi = reinterpret_cast<T *>(sb);
+      T *lo = hi + 16 * 64;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const float g = v[jj];
+        const float u = es.xbuf[r * kXStride + jj];
+        const float h = g / (1.0f + __expf(-g)) * u;
+        const T hv = from_f<T>(h);
+        hi[jj * 64 + r] = hv;
+        if (p.act_lo) lo[jj * 64 + r] = from_f<T>(h - to_f<T>(hv));
+      }
+    }
+  } else {
+    float *f = reinterpret_cast<float *>(sb);
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      float x = v[jj];
+      // anchor rows receive no write: adding -0 leaves every value bit-identical
+      if (EPI == EPI_INJECT) x = ((tok0 + jj) % p.block_w == 0) ? -0.0f : es.rs[j0 + jj] * x;
+      f[jj * kBM + r] = x;
+    }
+  }
+  stage_publish();
+  if (et == 0) {
+    if (EPI == EPI_STORE_F32) {
+      const int s = seg_of_tile(p, m_tile);
+      tma_store_2d(&maps.out[s], sb, (m_tile - p.seg[s].tile_begin) * kBM, tok0);
+    } else if (EPI == EPI_RESID_F32 || EPI == EPI_INJECT) {
+      tma_reduce_add_2d(&maps.out[0], sb, m_tile * kBM, tok0);
+    } else if (EPI == EPI_SWIGLU) {
+      tma_store_2d(&maps.out[0], sb, m_tile * 64, tok0);
+      if (p.act_lo) tma_store_2d(&maps.out[1], sb + 16 * 64 * sizeof(T), m_tile * 64, tok0);
+    }
+    bulk_commit();
+  }
+}
+
+// INJECT: row scales of the tile's tokens, read once per tile.  Safe to overwrite here:
+// every thread has passed the barrier that ends the previous chunk's staging.
+__device__ __forceinline__ void load_row_scales(const GemmArgs &p, int tile_tok0, int LW, int et,
+                                                EpiSmem &es) {
+  for (int t = et; t < LW; t += 128) {
+    const int tok = tile_tok0 + t;
+    es.rs[t] = tok < p.n_tokens ? p.row_scale[tok] : 0.f;
+  }
+}
+
+// Split tiles.  Every CTA that computed part of a tile stores its fp32 partial (layout
+// [LW columns][128 rows]) in its own slot and counts itself on the tile's counter.  After
+// its mainloop each contributor waits until all n have arrived and then sums its share
+// of the tile's 16-column chunks (chunk k belongs to the contributor k mod n) over all n
+// partials, in CTA order, so results do not depend on which CTA got there first.  Every
+// contributor of a tile waits only for partials that the others write before their own
+// waits, and all CTAs of a launch are resident at once (one per SM), so the waits end.
+struct FixupStage {
+  uint8_t *base;     // stage area (the pipeline's A and B buffers, idle after the mainloop)
+  int pieces;        // 8 KB pieces it holds
+  uint64_t *bar;     // completion barrier of the piece loads
+  uint32_t phase;
+};
+
+template <typename T, int EPI>
+__device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, int r, int et,
+                           FixupStage &fs, EpiSmem &es, volatile int *sabort) {
+  constexpr uint32_t kPiece = 16 * kBM * 4;
+  const long long U = p.units;
+  const int P = p.n_ctas;
+  const int LW = p.ln;
+  const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
+  const int c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb);
+  const int c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1);
+  const int n = c_last - c_first + 1;
+  const int me = static_cast<int>(blockIdx.x) - c_first;
+  unsigned *arrived = p.counters + tile;
+  unsigned *done = p.counters + p.n_counter_tiles + tile;
+  const int n_chunks = LW / 16;
+  const int my_chunks = me < n_chunks ? (n_chunks - me + n - 1) / n : 0;  // chunks me, me+n, ...
+  if (my_chunks > 0) {
+    if (et == 0) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire(arrived) < static_cast<unsigned>(n)) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          atomicOr(&g_error_word, DEVERR_TIMEOUT);
+          *sabort = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+      fence_proxy_async_global();
+    }
+    named_bar(1, 128);
+    if (*sabort) return false;
+    if (EPI == EPI_INJECT) load_row_scales(p, n_tile * LW, LW, et, es);
+    // Issue the loads of as many whole chunks (n partial pieces each) as the stage area
+    // holds, wait once, then sum and emit them; a tile with more partials than pieces
+    // takes several rounds per chunk.
+    auto load = [&](int k, int c0, int cn, int slot0) {
+      const uint64_t pol = policy_evict_first();
+      for (int i = 0; i < cn; ++i) {
+        const int c = c_first + c0 + i;
+        const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
+        const float *src = p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
+                           static_cast<size_t>(k) * 16 * kBM;
+        bulk_load(fs.base + static_cast<size_t>(slot0 + i) * kPiece, src, kPiece, fs.bar, pol);
+      }
+    };
+    auto add = [&](float (&acc)[16], int slot0, int cn) {
+      for (int i = 0; i < cn; ++i) {
+        const float *src = reinterpret_cast<const float *>(fs.base + static_cast<size_t>(slot0 + i) * kPiece);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) acc[jj] += src[jj * kBM + r];
+      }
+    };
+    if (n <= fs.pieces) {
+      const int per_batch = fs.pieces / n;
+      for (int b0 = 0; b0 < my_chunks; b0 += per_batch) {
+        const int bn = min(per_batch, my_chunks - b0);
+        if (et == 0) {
+          mbar_arrive_expect_tx(fs.bar, static_cast<uint32_t>(bn * n) * kPiece);
+          for (int j = 0; j < bn; ++j) load(me + (b0 + j) * n, 0, n, j * n);
+        }
+        if (!mbar_wait(fs.bar, fs.phase)) return false;
+        fs.phase ^= 1u;
+        for (int j = 0; j < bn; ++j) {
+          const int k = me + (b0 + j) * n;
+          float acc[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+          add(acc, j * n, n);
+          emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, r, et, acc, es);
+        }
+        named_bar(1, 128);  // every thread is done with the pieces before they are refilled
+      }
+    } else {
+      for (int j = 0; j < my_chunks; ++j) {
+        const int k = me + j * n;
+        float acc[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+        for (int c0 = 0; c0 < n; c0 += fs.pieces) {
+          const int cn = min(fs.pieces, n - c0);
+          if (et == 0) {
+            mbar_arrive_expect_tx(fs.bar, static_cast<uint32_t>(cn) * kPiece);
+            load(k, c0, cn, 0);
+          }
+          if (!mbar_wait(fs.bar, fs.phase)) return false;
+          fs.phase ^= 1u;
+          add(acc, 0, cn);
+          named_bar(1, 128);
+        }
+        emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, r, et, acc, es);
+      }
+    }
+  }
+  if (et == 0) {
+    if (atomicAdd(done, 1u) == static_cast<unsigned>(n - 1)) {  // every contributor is past its wait
+      *arrived = 0u;
+      *done = 0u;
+    }
+  }
+  return true;
+}
+
+template <typename T, int EPI>
+__device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t *accf,
+                              uint64_t *acce, uint32_t tmem_base, long long u0, long long u1,
+                              EpiSmem &es, FixupStage &fs, volatile int *sabort) {
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;             // TMEM lane quarter this warp may access
   const int r = q * 32 + (threadIdx.x & 31);
   const int et = threadIdx.x - 64;    // 0..127 among epilogue threads
   const int cta = blockIdx.x;
-  const long long U = p.units;
-  const int P = p.n_ctas;
   const int first_tile = static_cast<int>(u0 / p.kb);
   pdl_wait();
   SegWalk w{u0, u1, p.kb};
   int tile, kb0, kb1, e = 0;
+  int split0 = -1, split1 = -1;  // split tiles this CTA contributed to
   while (w.next(tile, kb0, kb1)) {
     const int a = e & 1;
     const uint32_t ra = static_cast<uint32_t>(e >> 1);
     ++e;
     const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
     const int LW = p.ln;  // logical token columns of the tile
-    EpiOperands op;
-    epi_load<T, EPI>(p, m_tile, r, n_tile * LW, op);
+    const bool whole = (kb0 == 0 && kb1 == p.kb);
+    if (EPI == EPI_INJECT && whole) load_row_scales(p, n_tile * LW, LW, et, es);
     if (*sabort || !mbar_wait(&accf[a], ra & 1u)) {
       *sabort = 1;
       return;
@@ -424,77 +552,49 @@ __device__ void gemm_epilogue(const GemmArgs &p, uint64_t *accf, uint64_t *acce,
     tc_fence_after();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                            static_cast<uint32_t>(a * p.block_n);
-    const bool whole = (kb0 == 0 && kb1 == p.kb);
-    int c_first = cta, c_last = cta;
     if (!whole) {
       const int slot = (tile == first_tile) ? 0 : 1;
       float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM;
       for (int j0 = 0; j0 < LW; j0 += 16) {
         float v[16];
         tmem_ld_logical(tbase, j0, LW, p.split, v);
+        uint8_t *sb = stage_claim(es, et);
+        float *f = reinterpret_cast<float *>(sb);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) mine[(j0 + jj) * kBM + r] = v[jj];
+        for (int jj = 0; jj < 16; ++jj) f[jj * kBM + r] = v[jj];
+        stage_publish();
+        if (et == 0) {
+          bulk_store(mine + static_cast<size_t>(j0) * kBM, sb, 16 * kBM * 4);
+          bulk_commit();
+        }
       }
-      __threadfence();
-      named_bar(1, 128);
-      c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb);
-      c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1);
+      tc_fence_before();
+      mbar_arrive(&acce[a]);  // the accumulator is free for the MMA warp
       if (et == 0) {
-        const unsigned n = static_cast<unsigned>(c_last - c_first + 1);
-        const unsigned old = atomicAdd(&p.counters[tile], 1u);
-        const int last = (old == n - 1) ? 1 : 0;
-        if (last) p.counters[tile] = 0;  // ready for the next launch
-        *sflag = last;
+        bulk_wait<0>();  // the partial has reached global memory
+        fence_proxy_async_global();
+        __threadfence();
+        atomicAdd(&p.counters[tile], 1u);
       }
-      named_bar(1, 128);
-      const int last = *sflag;
-      named_bar(1, 128);
-      if (!last) {
-        tc_fence_before();
-        mbar_arrive(&acce[a]);
-        continue;
-      }
-      __threadfence();
+      if (split0 < 0) split0 = tile; else split1 = tile;
+      continue;
     }
     for (int j0 = 0; j0 < LW; j0 += 16) {
       float v[16];
       tmem_ld_logical(tbase, j0, LW, p.split, v);
-      if (!whole) {
-        // Sum the contributors' partial tiles in CTA order (deterministic).  Loads of two
-        // contributors are issued before they are added so their L2 latencies overlap.
-        float acc[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
-        for (int c0 = c_first; c0 <= c_last; c0 += 2) {
-          float part[2][16];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = c0 + u;
-            if (c > c_last || c == cta) continue;
-            const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
-            const float *o = p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
-                             static_cast<size_t>(j0) * kBM + r;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) part[u][jj] = __ldcg(o + jj * kBM);
-          }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = c0 + u;
-            if (c > c_last) break;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] += (c == cta) ? v[jj] : part[u][jj];
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) v[jj] = acc[jj];
-      }
-      EpiOperands cur = op;
-      if (j0 + 16 < LW) epi_load<T, EPI>(p, m_tile, r, n_tile * LW + j0 + 16, op);
-      epi_chunk<T, EPI>(p, m_tile, r, n_tile * LW + j0, v, cur, xbuf, red, redi);
+      emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + j0, j0, r, et, v, es);
     }
     tc_fence_before();
     mbar_arrive(&acce[a]);
   }
+  // Every accumulator of this CTA has been waited for, so all of its MMAs (and the loads
+  // they consumed) are complete: the stage area is free for the fixups.
+  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, r, et, fs, es, sabort)) {
+    *sabort = 1;
+  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, r, et, fs, es, sabort)) {
+    *sabort = 1;
+  }
+  if (et == 0) bulk_wait<0>();  // every store of this CTA is complete before it exits
 }
 
 // ------------------------------------------------------------------ kernel
@@ -510,16 +610,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const SmemLayout L = smem_layout(p.stages, p.block_n, p.kbox);
   uint8_t *sA = smem;
   uint8_t *sB = smem + L.off_b;
-  float *xbuf = reinterpret_cast<float *>(smem + L.off_x);
-  float *red = reinterpret_cast<float *>(smem + L.off_red);
-  int32_t *redi = reinterpret_cast<int32_t *>(red + 64);
+  EpiSmem es;
+  es.out = smem + L.off_out;
+  es.next = 0;
+  es.xbuf = reinterpret_cast<float *>(smem + L.off_x);
+  es.red = reinterpret_cast<float *>(smem + L.off_red);
+  es.redi = reinterpret_cast<int32_t *>(es.red + 64);
+  es.rs = reinterpret_cast<float *>(smem + L.off_rs);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
   uint64_t *empty = full + p.stages;
   uint64_t *accf = empty + p.stages;
   uint64_t *acce = accf + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
-  volatile int *sflag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  volatile int *sabort = sflag + 1;
+  uint64_t *fixb = acce + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixb + 1);
+  volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long u0 = unit_begin(p.units, p.n_ctas, blockIdx.x);
@@ -536,8 +640,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(&accf[1], 1);
     mbar_init(&acce[0], 128);
     mbar_init(&acce[1], 128);
+    mbar_init(&fixb[0], 1);
     *sabort = 0;
-    *sflag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -562,7 +666,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) gemm_mma<T>(p, sA, sB, full, empty, accf, acce, tmem_base, u0, u1, sabort);
     __syncwarp();
   } else {
-    gemm_epilogue<T, EPI>(p, accf, acce, tmem_base, u0, u1, xbuf, red, redi, sflag, sabort);
+    FixupStage fs{smem, static_cast<int>(L.off_x / kOutStage), fixb, 0u};
+    gemm_epilogue<T, EPI>(maps, p, accf, acce, tmem_base, u0, u1, es, fs, sabort);
   }
   tc_fence_before();
   __syncthreads();
@@ -594,10 +699,12 @@ static EncodeTiledFn encode_fn() {
 
 struct MapKey {
   const void *ptr;
-  int dtype, inner, outer, box_inner, box_outer;
+  int dtype, inner, outer, box_inner, box_outer, swizzle;
+  long long stride;
   bool operator==(const MapKey &o) const {
     return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
-           box_inner == o.box_inner && box_outer == o.box_outer;
+           box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle &&
+           stride == o.stride;
   }
 };
 struct MapKeyHash {
@@ -605,17 +712,21 @@ struct MapKeyHash {
     size_t h = std::hash<const void *>()(k.ptr);
     h ^= (static_cast<size_t>(k.inner) * 0x9E3779B97F4A7C15ull) + (h << 6) + (h >> 2);
     h ^= (static_cast<size_t>(k.outer) * 0xC2B2AE3D27D4EB4Full) + (h << 6) + (h >> 2);
-    h ^= static_cast<size_t>(k.box_outer * 131 + k.box_inner * 7 + k.dtype);
+    h ^= static_cast<size_t>(k.box_outer * 131 + k.box_inner * 7 + k.dtype * 3 + k.swizzle);
+    h ^= (static_cast<size_t>(k.stride) * 0x165667B19E3779F9ull) + (h << 6) + (h >> 2);
     return h;
   }
 };
 
-// Row-major [outer, inner] matrix -> 2-D tiled map, 128-byte swizzle, zero fill OOB.
+// Row-major [outer, inner] matrix (rows `stride` elements apart) -> 2-D tiled map with
+// zero fill out of bounds; 128-byte swizzle for MMA operands, none for result tiles.
 static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int inner, int outer,
-                            int box_inner, int box_outer) {
+                            int box_inner, int box_outer, bool swizzle = true,
+                            long long stride = 0) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-  const MapKey key{ptr, dtype, inner, outer, box_inner, box_outer};
+  if (stride == 0) stride = inner;
+  const MapKey key{ptr, dtype, inner, outer, box_inner, box_outer, swizzle ? 1 : 0, stride};
   {
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
@@ -628,13 +739,14 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
   if (!fn) return "cuTensorMapEncodeTiled is unavailable";
   const int elem = dtype == 0 ? 2 : 4;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * elem};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride) * elem};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
   CUresult r = fn(&m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   2, const_cast<void *>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[160];
@@ -765,6 +877,7 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   if (a.stages < 2) return "GEMM tile does not fit in shared memory";
   a.partials = sc.partials;
   a.counters = sc.counters;
+  a.n_counter_tiles = static_cast<int>(sc.n_counters);
   if (gemm_partial_floats(a.n_ctas, a.block_n) > sc.partial_floats) return "GEMM partial scratch too small";
   if (static_cast<size_t>(tiles) > sc.n_counters) return "GEMM counter scratch too small";
 
@@ -788,6 +901,32 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   std::string err = plan.split
       ? make_map(&maps.b, plan.x, plan.dtype, plan.K, 2 * a.lo_row, BK, a.ln)
       : make_map(&maps.b, plan.x, plan.dtype, plan.K, plan.n_tokens, BK, a.block_n);
+  if (!err.empty()) return err;
+  // Result maps: [n_tokens rows, output columns], boxes of 16 tokens.
+  switch (a.epi) {
+    case EPI_STORE_F32:
+      for (int s = 0; s < a.n_segs && err.empty(); ++s)
+        err = make_map(&maps.out[s], a.out_f32 + a.seg[s].out_col, 1, a.seg[s].rows, plan.n_tokens,
+                       kBM, 16, false, a.ld_out);
+      break;
+    case EPI_RESID_F32:
+    case EPI_INJECT:
+      err = make_map(&maps.out[0], a.out_f32, 1, plan.w[0].rows, plan.n_tokens, kBM, 16, false,
+                     a.ld_out);
+      break;
+    case EPI_SWIGLU: {
+      err = make_map(&maps.out[0], a.out_act, plan.dtype, plan.w[0].rows, plan.n_tokens, 64, 16,
+                     false, a.ld_act);
+      if (err.empty() && a.act_lo) {
+        const size_t esz = plan.dtype == 0 ? 2 : 4;
+        err = make_map(&maps.out[1], static_cast<const char *>(a.out_act) + a.act_lo * esz,
+                       plan.dtype, plan.w[0].rows, plan.n_tokens, 64, 16, false, a.ld_act);
+      }
+      break;
+    }
+    default:
+      break;
+  }
   if (!err.empty()) return err;
   cudaError_t e = plan.dtype == 0 ? launch_typed<__nv_bfloat16>(maps, a, stream)
                                   : launch_typed<float>(maps, a, stream);

@@ -25,14 +25,12 @@ constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 enum EpiMode : int {
   EPI_STORE_F32 = 0,  // out[tok*ld + out_col + row] = acc
-  EPI_RESID_F32 = 1,  // out[tok*ld + row] = resid[tok*ld_resid + row] + acc
+  EPI_RESID_F32 = 1,  // out[tok*ld + row] += acc (one addition per element: deterministic)
   EPI_INJECT = 2,     // x[tok*ld + row] += scale[tok] * acc for non-anchor rows
   EPI_SWIGLU = 3,     // pair tiles: out[tok*ld_act + f] = SiLU(gate_f) * up_f
   EPI_ARGMAX = 4      // per-tile (max, lowest argmax) over 128 vocabulary rows
 };
 
-// Epilogue code runs once per tile, so it is kept short: the instruction fetches of
-// long straight-line epilogues dominated the tail of small launches.
 struct GemmSeg {
   int rows;               // output rows of this weight matrix
   int tile_begin;         // first m-tile of the segment
@@ -53,22 +51,24 @@ struct __align__(16) GemmArgs {
   int packed;                     // weights come from packed images (contiguous bulk copies)
   long long units;
   int epi;
-  int ld_out, ld_resid, ld_act, block_w, vocab;
+  int ld_out, ld_act, block_w, vocab;
   long long act_lo;               // SWIGLU: element offset of the lo block of out_act (0: none)
   float *out_f32;
-  const float *resid;
   const float *row_scale;
   void *out_act;
   float *amax_val;                // [m_tiles][n_tokens]
   int32_t *amax_idx;
   float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
-  unsigned *counters;             // [m_tiles * n_tiles_n] arrival counters (start at 0)
+  unsigned *counters;             // [2][n_counter_tiles] arrival / done counters (start at 0)
+  int n_counter_tiles;
   GemmSeg seg[kMaxSegs];
 };
 
 struct GemmMaps {
-  CUtensorMap a[kMaxSegs];  // weight maps (pair mode: a[0] gate, a[1] up, 64-row boxes)
-  CUtensorMap b;            // activation map [n_tokens, K]
+  CUtensorMap a[kMaxSegs];    // weight maps (pair mode: a[0] gate, a[1] up, 64-row boxes)
+  CUtensorMap b;              // activation map [n_tokens, K]
+  CUtensorMap out[kMaxSegs];  // result maps [n_tokens, rows], boxes of 16 tokens: STORE one
+                              // per segment, RESID/INJECT out[0] = x, SWIGLU hi and lo
 };
 
 // Host description of one GEMM launch.
@@ -93,8 +93,8 @@ struct GemmPlan {
 struct GemmScratch {
   float *partials;
   size_t partial_floats;
-  unsigned *counters;
-  size_t n_counters;
+  unsigned *counters;  // 2 * n_counters words, zero on entry; every launch leaves them zero
+  size_t n_counters;   // tiles a launch may have
 };
 
 unsigned take_error_word_gemm();

@@ -30,7 +30,7 @@ namespace {
 // Scratch layout (bytes, each region 256-aligned):
 //   split hidden rows  2 * 32 * 8192 * 2            =  1 MiB
 //   per-tile maxima    2048 * 32 * 4 (+ indices)    =  0.5 MiB
-//   tile counters      2048 * 4                     =  8 KiB
+//   tile counters      2 * 2048 * 4                 = 16 KiB
 //   stream-K partials  160 * 2 * 64 * 128 * 4       = 10 MiB
 constexpr size_t kMaxRows = BD_NOALLOC_MAX_ROWS;
 constexpr size_t kMaxHidden = BD_NOALLOC_MAX_HIDDEN;
@@ -38,7 +38,7 @@ constexpr size_t kMaxTiles = BD_NOALLOC_MAX_VOCAB / 128;
 constexpr size_t kMaxCtas = 160;
 constexpr size_t kSplitBytes = 2 * kMaxRows * kMaxHidden * 2;
 constexpr size_t kAmaxBytes = kMaxTiles * kMaxRows * 4;
-constexpr size_t kCounterBytes = kMaxTiles * 4;
+constexpr size_t kCounterBytes = 2 * kMaxTiles * 4;
 constexpr size_t kPartialFloats = kMaxCtas * 2 * (2 * kMaxRows) * kBM;
 constexpr size_t kScratchBytes = kSplitBytes + 2 * kAmaxBytes + kCounterBytes + kPartialFloats * 4;
 static_assert(kScratchBytes <= BD_NOALLOC_SCRATCH_BYTES, "scratch layout exceeds the stated size");
@@ -120,7 +120,7 @@ extern "C" bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_we
   float *partials = reinterpret_cast<float *>(base + off);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream_);
-  cudaError_t e = cudaMemsetAsync(counters, 0, m_tiles * sizeof(unsigned), s);
+  cudaError_t e = cudaMemsetAsync(counters, 0, 2 * m_tiles * sizeof(unsigned), s);
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("memset: ") + cudaGetErrorString(e));
   const bool split = cfg->dtype == BD_BF16;
   const size_t pad = (static_cast<size_t>(rows) + 15) / 16 * 16;

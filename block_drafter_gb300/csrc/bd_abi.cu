@@ -270,10 +270,8 @@ GemmScratch scratch_of(const GemmWs &g) {
   return GemmScratch{g.partials, g.partial_floats, g.counters, g.n_counters};
 }
 
-std::string memset_counters(const GemmWs &g, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(g.counters, 0, 2 * g.n_counters * sizeof(unsigned), s);
-  return e == cudaSuccess ? std::string() : std::string("memset: ") + cudaGetErrorString(e);
-}
+// The call's tile counters (arrival and done), zeroed by its first kernel.
+ZeroSpan counters_of(const GemmWs &g) { return ZeroSpan{g.counters, 2 * g.n_counters}; }
 
 GemmPlan make_plan(const bd_config *c, const void *x, int n_tok, int K) {
   GemmPlan p;
@@ -371,8 +369,7 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
   const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
   const PackedLayout PL = packed_layout(cfg);
 
-  BD_TRY(memset_counters(mw.g, s));
-  BD_TRY(launch_rope_table(row_pos, n_rows, mw.rope, D / 2, freq, s));
+  BD_TRY(launch_rope_table(row_pos, n_rows, mw.rope, D / 2, freq, counters_of(mw.g), s));
   {  // S1: W_feature s_t (fp32 out), then plain_rmsnorm with context_norm
     GemmPlan p = make_plan(cfg, target_feats, n_rows, cfg->n_target_layers * H);
     add_w(p, w->w_feature, H, pk, PL.w_feature);
@@ -476,10 +473,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const PackedLayout PL = packed_layout(cfg);  // bf16 activations enter the GEMMs as hi+lo pairs
   auto lo = [&](int K) -> size_t { return split ? static_cast<size_t>(TP) * K : 0; };
 
-  BD_TRY(memset_counters(rw.g, s));
   // S3: block input rows and the RoPE table of positions F_b + i
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
-                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, s));
+                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, counters_of(rw.g), s));
   for (int l = 0; l < cfg->n_layers; ++l) {
     const bd_layer_weights &L = w->layer[l];
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE
@@ -650,11 +646,12 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
   HeadWs hw;
   carve_head(cv, hw, cfg, rows, num_sms());
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
-  BD_TRY(memset_counters(hw.g, s));
   const bool split = cfg->dtype == BD_BF16;
   if (split)  // bf16 hi/lo pair of the fp32 hidden rows: the head sees ~16 mantissa bits
     BD_TRY(launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hw.hl,
-                             static_cast<size_t>(pad16(rows)) * cfg->hidden, s));
+                             static_cast<size_t>(pad16(rows)) * cfg->hidden, counters_of(hw.g), s));
+  else
+    BD_TRY(launch_zero(counters_of(hw.g), s));
   GemmPlan p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
   p.split = split;
   add_w(p, w->embed_head, cfg->vocab, static_cast<const uint8_t *>(w->packed),

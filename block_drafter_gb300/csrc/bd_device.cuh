@@ -140,6 +140,11 @@ __device__ __forceinline__ void tma_store_2d(const void *map, const void *src, i
                ::"l"(map), "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const void *map, const void *src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // Element-wise global += shared over the box (performed in L2).
 __device__ __forceinline__ void tma_reduce_add_2d(const void *map, const void *src, int x, int y) {
   asm volatile(

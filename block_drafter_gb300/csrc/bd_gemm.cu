@@ -390,8 +390,10 @@ __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs 
     } else if (EPI == EPI_RESID_F32 || EPI == EPI_INJECT) {
       tma_reduce_add_2d(&maps.out[0], sb, m_tile * kBM, tok0);
     } else if (EPI == EPI_SWIGLU) {
-      tma_store_2d(&maps.out[0], sb, m_tile * 64, tok0);
-      if (p.act_lo) tma_store_2d(&maps.out[1], sb + 16 * 64 * sizeof(T), m_tile * 64, tok0);
+      if (p.act_lo)
+        tma_store_3d(&maps.out[0], sb, m_tile * 64, tok0, 0);
+      else
+        tma_store_2d(&maps.out[0], sb, m_tile * 64, tok0);
     }
     bulk_commit();
   }
@@ -649,6 +651,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (!p.packed)
       for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
   }
+  if (threadIdx.x == 64) {  // result maps, used by the epilogue's stores
+    const int n_out = EPI == EPI_STORE_F32 ? p.n_segs : (EPI == EPI_ARGMAX ? 0 : 1);
+    for (int s = 0; s < n_out; ++s) tma_prefetch_desc(&maps.out[s]);
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, ncols);
     tmem_relinquish();
@@ -699,12 +705,12 @@ static EncodeTiledFn encode_fn() {
 
 struct MapKey {
   const void *ptr;
-  int dtype, inner, outer, box_inner, box_outer, swizzle;
-  long long stride;
+  int dtype, inner, outer, box_inner, box_outer, swizzle, planes;
+  long long stride, plane_stride;
   bool operator==(const MapKey &o) const {
     return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
            box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle &&
-           stride == o.stride;
+           stride == o.stride && planes == o.planes && plane_stride == o.plane_stride;
   }
 };
 struct MapKeyHash {
@@ -714,19 +720,24 @@ struct MapKeyHash {
     h ^= (static_cast<size_t>(k.outer) * 0xC2B2AE3D27D4EB4Full) + (h << 6) + (h >> 2);
     h ^= static_cast<size_t>(k.box_outer * 131 + k.box_inner * 7 + k.dtype * 3 + k.swizzle);
     h ^= (static_cast<size_t>(k.stride) * 0x165667B19E3779F9ull) + (h << 6) + (h >> 2);
+    h ^= (static_cast<size_t>(k.plane_stride * 8 + k.planes) * 0x27D4EB2F165667C5ull) + (h << 6) +
+         (h >> 2);
     return h;
   }
 };
 
 // Row-major [outer, inner] matrix (rows `stride` elements apart) -> 2-D tiled map with
 // zero fill out of bounds; 128-byte swizzle for MMA operands, none for result tiles.
+// planes > 1 adds a third dimension: `planes` such matrices plane_stride elements apart,
+// all of them in every box.
 static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int inner, int outer,
                             int box_inner, int box_outer, bool swizzle = true,
-                            long long stride = 0) {
+                            long long stride = 0, int planes = 1, long long plane_stride = 0) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
   if (stride == 0) stride = inner;
-  const MapKey key{ptr, dtype, inner, outer, box_inner, box_outer, swizzle ? 1 : 0, stride};
+  const MapKey key{ptr,   dtype,          inner,  outer, box_inner, box_outer, swizzle ? 1 : 0,
+                   planes, stride, plane_stride};
   {
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
@@ -738,13 +749,16 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
   EncodeTiledFn fn = encode_fn();
   if (!fn) return "cuTensorMapEncodeTiled is unavailable";
   const int elem = dtype == 0 ? 2 : 4;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride) * elem};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride) * elem,
+                           static_cast<cuuint64_t>(plane_stride) * elem};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer),
+                       static_cast<cuuint32_t>(planes)};
+  cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
   CUresult r = fn(&m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                  2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  planes > 1 ? 3 : 2, const_cast<void *>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -914,16 +928,10 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
       err = make_map(&maps.out[0], a.out_f32, 1, plan.w[0].rows, plan.n_tokens, kBM, 16, false,
                      a.ld_out);
       break;
-    case EPI_SWIGLU: {
+    case EPI_SWIGLU:  // hi and lo planes (act_lo elements apart) in one box
       err = make_map(&maps.out[0], a.out_act, plan.dtype, plan.w[0].rows, plan.n_tokens, 64, 16,
-                     false, a.ld_act);
-      if (err.empty() && a.act_lo) {
-        const size_t esz = plan.dtype == 0 ? 2 : 4;
-        err = make_map(&maps.out[1], static_cast<const char *>(a.out_act) + a.act_lo * esz,
-                       plan.dtype, plan.w[0].rows, plan.n_tokens, 64, 16, false, a.ld_act);
-      }
+                     false, a.ld_act, a.act_lo ? 2 : 1, a.act_lo);
       break;
-    }
     default:
       break;
   }

@@ -68,7 +68,8 @@ struct GemmMaps {
   CUtensorMap a[kMaxSegs];    // weight maps (pair mode: a[0] gate, a[1] up, 64-row boxes)
   CUtensorMap b;              // activation map [n_tokens, K]
   CUtensorMap out[kMaxSegs];  // result maps [n_tokens, rows], boxes of 16 tokens: STORE one
-                              // per segment, RESID/INJECT out[0] = x, SWIGLU hi and lo
+                              // per segment, RESID/INJECT out[0] = x, SWIGLU out[0] with the
+                              // hi and lo planes as a third dimension
 };
 
 // Host description of one GEMM launch.

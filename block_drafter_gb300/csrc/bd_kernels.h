@@ -36,12 +36,22 @@ struct RopeFreq {
 
 // Round prologue: x[b*W+i] = embed[id] (fp32), id = anchor_b for i = 0 else MASK, and the
 // (cos, sin) table of positions F_b + i.
+// Words a call's first kernel sets to zero (the GEMM tile counters of the call): doing it
+// there instead of with a memset keeps the call one chain of dependent launches.
+struct ZeroSpan {
+  unsigned *p;
+  size_t n;
+};
+
 std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
                               const int64_t *frontier, int B, int W, int mask_id, float *x,
-                              float2 *rope, int half, const RopeFreq &freq, cudaStream_t s);
+                              float2 *rope, int half, const RopeFreq &freq, ZeroSpan z,
+                              cudaStream_t s);
 // (cos, sin) table of arbitrary absolute positions.
 std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
-                              const RopeFreq &freq, cudaStream_t s);
+                              const RopeFreq &freq, ZeroSpan z, cudaStream_t s);
+// Only zeroes (for calls whose first kernel is a GEMM).
+std::string launch_zero(ZeroSpan z, cudaStream_t s);
 
 enum NormMode : int {
   NORM_PLAIN = 0,   // out = gain * x / sqrt(mean(x^2) + eps)
@@ -53,7 +63,8 @@ std::string launch_rownorm(int dtype, const float *x, int rows, int H, const voi
                            float eps, int mode, void *out, float *r_out, float *f32_out,
                            float *head_out, int W, size_t lo_off, cudaStream_t s);
 // fp32 -> bf16 hi (dst) and lo (dst + lo_off) of n elements.
-std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, cudaStream_t s);
+std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,
+                              cudaStream_t s);
 
 // c = sqrt(Rc) z / (||z|| + eps) for non-anchor rows; sqrt(Rc) * codebook[anchor] for anchors.
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,

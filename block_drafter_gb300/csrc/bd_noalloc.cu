@@ -120,14 +120,14 @@ extern "C" bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_we
   float *partials = reinterpret_cast<float *>(base + off);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream_);
-  cudaError_t e = cudaMemsetAsync(counters, 0, 2 * m_tiles * sizeof(unsigned), s);
-  if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("memset: ") + cudaGetErrorString(e));
+  // the first kernel clears the tile counters before the GEMM uses them
+  const ZeroSpan zero{counters, 2 * m_tiles};
   const bool split = cfg->dtype == BD_BF16;
   const size_t pad = (static_cast<size_t>(rows) + 15) / 16 * 16;
-  if (split) {
-    err = launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hl, pad * cfg->hidden, s);
-    if (!err.empty()) return fail(BD_ERR_CUDA, err);
-  }
+  err = split ? launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hl,
+                                  pad * cfg->hidden, zero, s)
+              : launch_zero(zero, s);
+  if (!err.empty()) return fail(BD_ERR_CUDA, err);
   GemmPlan p;
   memset(&p, 0, sizeof p);
   p.dtype = split ? 0 : 1;

@@ -32,13 +32,22 @@ __device__ __forceinline__ float2 rope_cs(long long pos, double inv) {
   return make_float2(c, s);
 }
 
+// Grid-stride zeroing of a ZeroSpan (after the kernel's pdl_wait: the previous kernel,
+// which may still use the words, has completed).
+__device__ __forceinline__ void zero_span(ZeroSpan z) {
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < z.n;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+    z.p[t] = 0u;
+}
+
 template <typename T>
 __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *anchors,
                                   const int64_t *frontier, int W, int mask_id, float *x,
-                                  float2 *rope, int half, RopeFreq freq) {
+                                  float2 *rope, int half, RopeFreq freq, ZeroSpan z) {
   const int tok = blockIdx.x, b = tok / W, i = tok % W;
   pdl_wait();
   pdl_trigger();
+  zero_span(z);
   int id = i == 0 ? anchors[b] : mask_id;
   if (id < 0 || id >= V) {
     if (threadIdx.x == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
@@ -52,9 +61,10 @@ __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *a
 }
 
 __global__ void rope_table_kernel(const int64_t *pos, int n, float2 *rope, int half,
-                                  RopeFreq freq) {
+                                  RopeFreq freq, ZeroSpan z) {
   pdl_wait();
   pdl_trigger();
+  zero_span(z);
   const int total = n * half;
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
     const int r = t / half, j = t % half;
@@ -320,12 +330,20 @@ __global__ void argmax_reduce_kernel(const float *val, const int32_t *idx, int m
 }
 
 // fp32 rows -> bf16 hi rows [0, rows) and lo rows [lo_row, lo_row + rows).
-__global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off) {
+__global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off,
+                                  ZeroSpan z) {
   pdl_wait();
   pdl_trigger();
+  zero_span(z);
   for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < n;
        t += static_cast<size_t>(gridDim.x) * blockDim.x)
     store_split(dst, t, lo_off, src[t]);
+}
+
+__global__ void zero_kernel(ZeroSpan z) {
+  pdl_wait();
+  pdl_trigger();
+  zero_span(z);
 }
 
 __global__ void copy_f32_kernel(const float *src, float *dst, size_t n) {
@@ -343,25 +361,32 @@ static std::string err(const char *what, cudaError_t e) {
 
 std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
                               const int64_t *frontier, int B, int W, int mask_id, float *x,
-                              float2 *rope, int half, const RopeFreq &freq, cudaStream_t s) {
+                              float2 *rope, int half, const RopeFreq &freq, ZeroSpan z,
+                              cudaStream_t s) {
   cudaError_t e;
   if (dtype == 0)
     e = launch_pdl(round_prep_kernel<__nv_bfloat16>, dim3(B * W), dim3(256), 0, s,
                    static_cast<const __nv_bfloat16 *>(embed), H, V, anchors, frontier, W, mask_id, x,
-                   rope, half, freq);
+                   rope, half, freq, z);
   else
     e = launch_pdl(round_prep_kernel<float>, dim3(B * W), dim3(256), 0, s,
                    static_cast<const float *>(embed), H, V, anchors, frontier, W, mask_id, x, rope,
-                   half, freq);
+                   half, freq, z);
   return err("round prep", e);
 }
 
 std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
-                              const RopeFreq &freq, cudaStream_t s) {
+                              const RopeFreq &freq, ZeroSpan z, cudaStream_t s) {
   const int total = n * half;
   const int blocks = (total + 255) / 256;
   return err("rope table", launch_pdl(rope_table_kernel, dim3(blocks < 1024 ? blocks : 1024),
-                                      dim3(256), 0, s, pos, n, rope, half, freq));
+                                      dim3(256), 0, s, pos, n, rope, half, freq, z));
+}
+
+std::string launch_zero(ZeroSpan z, cudaStream_t s) {
+  const size_t blocks = (z.n + 255) / 256;
+  return err("zero", launch_pdl(zero_kernel, dim3(blocks < 64 ? (blocks > 0 ? blocks : 1) : 64),
+                                dim3(256), 0, s, z));
 }
 
 std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain, float eps,
@@ -379,11 +404,12 @@ std::string launch_rownorm(int dtype, const float *x, int rows, int H, const voi
   return err("rownorm", e);
 }
 
-std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, cudaStream_t s) {
+std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,
+                              cudaStream_t s) {
   const size_t blocks = (n + 255) / 256;
   return err("split rows", launch_pdl(split_rows_kernel, dim3(blocks < 2048 ? blocks : 2048),
                                       dim3(256), 0, s, src, n, static_cast<__nv_bfloat16 *>(dst),
-                                      lo_off));
+                                      lo_off, z));
 }
 
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {

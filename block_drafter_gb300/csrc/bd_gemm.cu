@@ -62,7 +62,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int block_n, int k
   L.off_x = L.off_b + static_cast<size_t>(stages) * kbox * block_n * 128;
   L.off_out = (L.off_x + kBM * kXStride * 4 + 1023) / 1024 * 1024;
   L.off_red = L.off_out + 2 * kOutStage;
-  L.off_rs = L.off_red + 2 * 64 * 4;
+  L.off_rs = L.off_red + 2 * (kEpiThreads / 2) * 4;  // maxima and indices, 16 per warp
   L.off_bar = L.off_rs + 256 * 4;
   L.total = L.off_bar + (2 * stages + 5) * 8 + 16 + 1024;  // + alignment slack
   return L;
@@ -248,64 +248,77 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
 }
 
 // ------------------------------------------------------------------ epilogue
-// Logical columns j0..j0+15 of the accumulator: the hi half, plus the lo half that sits
-// LW columns further when the activation operand is split.
-__device__ __forceinline__ void tmem_ld_logical(uint32_t tbase, int j0, int LW, int split,
-                                                float (&v)[16]) {
-  tmem_ld16(tbase + j0, v);
+// Each epilogue thread owns accumulator row r (its warp's TMEM lane quarter) and kCW of
+// the 16 token columns of a chunk, starting at column c0 of the chunk.
+constexpr int kCW = 16 / kEpiSlices;
+struct EpiPos {
+  int r;   // tile row 0..127
+  int et;  // 0..kEpiThreads-1 among the epilogue threads
+  int c0;  // first column of this thread's slice of a chunk
+};
+
+// Columns col..col+kCW-1 of the accumulator: the hi half, plus the lo half that sits LW
+// columns further when the activation operand is split.
+__device__ __forceinline__ void tmem_ld_logical(uint32_t tbase, int col, int LW, int split,
+                                                float (&v)[kCW]) {
+  static_assert(kCW == 8, "tmem_ld_logical loads 8 columns per thread");
+  tmem_ld8(tbase + col, v);
   if (split) {
-    float w[16];
-    tmem_ld16(tbase + LW + j0, w);
+    float w[kCW];
+    tmem_ld8(tbase + LW + col, w);
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+    for (int jj = 0; jj < kCW; ++jj) v[jj] += w[jj];
   }
 }
 
-// Results leave the SM through shared memory: the 128 epilogue threads write a chunk of
-// 16 token columns into one of two staging buffers and one thread hands it to TMA (a
-// tiled store, an in-L2 reduce-add, or a contiguous bulk store).  Stores from the
-// threads themselves stall on write acknowledgements when L2 is busy with the weight
-// stream; the TMA unit takes them off the threads' critical path.
+// Results leave the SM through shared memory: the epilogue threads write a chunk of 16
+// token columns into one of two staging buffers and one thread hands it to TMA (a tiled
+// store, an in-L2 reduce-add, or a contiguous bulk store), so no thread waits for write
+// acknowledgements.
 struct EpiSmem {
   uint8_t *out;    // [2][kOutStage] staging buffers
   int next;        // buffer the next chunk uses
   float *xbuf;     // [128][kXStride] exchange / transpose buffer
-  float *red;      // [4][16] per-warp column maxima
-  int32_t *redi;   // [4][16] their indices
+  float *red;      // [kEpiThreads / 32][16] per-warp column maxima
+  int32_t *redi;   // [kEpiThreads / 32][16] their indices
   float *rs;       // [256] INJECT row scales of the current tile's tokens
 };
 
 // Claims the next staging buffer: the bulk group that last read it (two chunks ago) must
-// have finished reading.  Ends with a barrier of the 128 epilogue threads.
+// have finished reading.  Ends with a barrier of the epilogue threads.
 __device__ __forceinline__ uint8_t *stage_claim(EpiSmem &es, int et) {
   uint8_t *sb = es.out + es.next * kOutStage;
   es.next ^= 1;
   if (et == 0) bulk_wait_read<1>();
-  named_bar(1, 128);
+  named_bar(1, kEpiThreads);
   return sb;
 }
 // Publishes the staged chunk to the async proxy; thread et == 0 then issues the copy.
 __device__ __forceinline__ void stage_publish() {
   fence_proxy_async_shared();
-  named_bar(1, 128);
+  named_bar(1, kEpiThreads);
 }
 
 // Per-(vocab tile, token) maximum and its lowest index: the chunk is transposed through
-// shared memory so that each thread scans 16 rows of one column serially (rows in
-// ascending order, so a strict comparison keeps the lowest index), then the two row
-// groups of a warp and the four warps are merged.
-__device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int tok0, int r,
-                                             int et, const float (&v)[16], EpiSmem &es) {
-  const int row_id = m_tile * kBM + r;
+// shared memory so that each thread scans a group of rows of one column serially (rows
+// in ascending order, so a strict comparison keeps the lowest index), then the row
+// groups are merged within warps and across warps.
+__device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int tok0,
+                                             const EpiPos &ps, const float (&v)[kCW],
+                                             EpiSmem &es) {
+  constexpr int kWarps = kEpiThreads / 32;
+  constexpr int kRowsPerGroup = kBM * 16 / kEpiThreads;  // 8 rows per thread
+  const int row_id = m_tile * kBM + ps.r;
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) es.xbuf[r * kXStride + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
-  named_bar(1, 128);
-  const int col = et & 15, grp = et >> 4;
+  for (int jj = 0; jj < kCW; ++jj)
+    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
+  named_bar(1, kEpiThreads);
+  const int col = ps.et & 15, grp = ps.et >> 4;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int row = grp * 16 + i;
+#pragma unroll
+  for (int i = 0; i < kRowsPerGroup; ++i) {
+    const int row = grp * kRowsPerGroup + i;
     const float x = es.xbuf[row * kXStride + col];
     if (x > best) {
       best = x;
@@ -318,23 +331,23 @@ __device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int 
     best = ob;
     bi = oi;
   }
-  if ((et & 31) < 16) {
-    es.red[(et >> 5) * 16 + col] = best;
-    es.redi[(et >> 5) * 16 + col] = bi;
+  if ((ps.et & 31) < 16) {
+    es.red[(ps.et >> 5) * 16 + col] = best;
+    es.redi[(ps.et >> 5) * 16 + col] = bi;
   }
-  named_bar(1, 128);
-  if (et < 16) {
-    float b = es.red[et];
-    int i = es.redi[et];
-    for (int w = 1; w < 4; ++w) {
-      const float x = es.red[w * 16 + et];
-      const int xi = es.redi[w * 16 + et];
+  named_bar(1, kEpiThreads);
+  if (ps.et < 16) {
+    float b = es.red[ps.et];
+    int i = es.redi[ps.et];
+    for (int w = 1; w < kWarps; ++w) {
+      const float x = es.red[w * 16 + ps.et];
+      const int xi = es.redi[w * 16 + ps.et];
       if (x > b || (x == b && xi < i)) {
         b = x;
         i = xi;
       }
     }
-    const int tok = tok0 + et;
+    const int tok = tok0 + ps.et;
     if (tok < p.n_tokens) {
       p.amax_val[static_cast<size_t>(m_tile) * p.n_tokens + tok] = b;
       p.amax_idx[static_cast<size_t>(m_tile) * p.n_tokens + tok] = i;
@@ -342,48 +355,51 @@ __device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int 
   }
 }
 
-// Writes the finished values v (tile row r, token columns tok0..tok0+15; j0 = tok0 minus
-// the tile's first token) of m_tile to the epilogue's destination.
+// Writes the finished values v (tile row ps.r, token columns tok0+ps.c0 .. +kCW-1; j0 =
+// tok0 minus the tile's first token) of m_tile to the epilogue's destination.
 template <typename T, int EPI>
 __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs &p, int m_tile,
-                                           int tok0, int j0, int r, int et,
-                                           const float (&v)[16], EpiSmem &es) {
+                                           int tok0, int j0, const EpiPos &ps,
+                                           const float (&v)[kCW], EpiSmem &es) {
   if (EPI == EPI_ARGMAX) {
-    argmax_chunk(p, m_tile, tok0, r, et, v, es);
+    argmax_chunk(p, m_tile, tok0, ps, v, es);
     return;
   }
+  const int r = ps.r, c0 = ps.c0;
   if (EPI == EPI_SWIGLU && r >= 64) {  // up features go to the gate rows' threads
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) es.xbuf[(r - 64) * kXStride + jj] = v[jj];
+    for (int jj = 0; jj < kCW; ++jj) es.xbuf[(r - 64) * kXStride + c0 + jj] = v[jj];
   }
-  uint8_t *sb = stage_claim(es, et);
+  uint8_t *sb = stage_claim(es, ps.et);
   if (EPI == EPI_SWIGLU) {
     // rows 0..63: gate features f, rows 64..127: up features f (same f)
     if (r < 64) {
       T *hi = reinterpret_cast<T *>(sb);
       T *lo = hi + 16 * 64;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
+      for (int jj = 0; jj < kCW; ++jj) {
+        const int c = c0 + jj;
         const float g = v[jj];
-        const float u = es.xbuf[r * kXStride + jj];
+        const float u = es.xbuf[r * kXStride + c];
         const float h = g / (1.0f + __expf(-g)) * u;
         const T hv = from_f<T>(h);
-        hi[jj * 64 + r] = hv;
-        if (p.act_lo) lo[jj * 64 + r] = from_f<T>(h - to_f<T>(hv));
+        hi[c * 64 + r] = hv;
+        if (p.act_lo) lo[c * 64 + r] = from_f<T>(h - to_f<T>(hv));
       }
     }
   } else {
     float *f = reinterpret_cast<float *>(sb);
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
+    for (int jj = 0; jj < kCW; ++jj) {
+      const int c = c0 + jj;
       float x = v[jj];
       // anchor rows receive no write: adding -0 leaves every value bit-identical
-      if (EPI == EPI_INJECT) x = ((tok0 + jj) % p.block_w == 0) ? -0.0f : es.rs[j0 + jj] * x;
-      f[jj * kBM + r] = x;
+      if (EPI == EPI_INJECT) x = ((tok0 + c) % p.block_w == 0) ? -0.0f : es.rs[j0 + c] * x;
+      f[c * kBM + r] = x;
     }
   }
   stage_publish();
-  if (et == 0) {
+  if (ps.et == 0) {
     if (EPI == EPI_STORE_F32) {
       const int s = seg_of_tile(p, m_tile);
       tma_store_2d(&maps.out[s], sb, (m_tile - p.seg[s].tile_begin) * kBM, tok0);
@@ -403,7 +419,7 @@ __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs 
 // every thread has passed the barrier that ends the previous chunk's staging.
 __device__ __forceinline__ void load_row_scales(const GemmArgs &p, int tile_tok0, int LW, int et,
                                                 EpiSmem &es) {
-  for (int t = et; t < LW; t += 128) {
+  for (int t = et; t < LW; t += kEpiThreads) {
     const int tok = tile_tok0 + t;
     es.rs[t] = tok < p.n_tokens ? p.row_scale[tok] : 0.f;
   }
@@ -424,7 +440,7 @@ struct FixupStage {
 };
 
 template <typename T, int EPI>
-__device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, int r, int et,
+__device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, const EpiPos &ps,
                            FixupStage &fs, EpiSmem &es, volatile int *sabort) {
   constexpr uint32_t kPiece = 16 * kBM * 4;
   const long long U = p.units;
@@ -439,6 +455,7 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, in
   unsigned *done = p.counters + p.n_counter_tiles + tile;
   const int n_chunks = LW / 16;
   const int my_chunks = me < n_chunks ? (n_chunks - me + n - 1) / n : 0;  // chunks me, me+n, ...
+  const int et = ps.et;
   if (my_chunks > 0) {
     if (et == 0) {
       const unsigned long long t0 = globaltimer();
@@ -452,7 +469,7 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, in
       }
       fence_proxy_async_global();
     }
-    named_bar(1, 128);
+    named_bar(1, kEpiThreads);
     if (*sabort) return false;
     if (EPI == EPI_INJECT) load_row_scales(p, n_tile * LW, LW, et, es);
     // Issue the loads of as many whole chunks (n partial pieces each) as the stage area
@@ -468,11 +485,12 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, in
         bulk_load(fs.base + static_cast<size_t>(slot0 + i) * kPiece, src, kPiece, fs.bar, pol);
       }
     };
-    auto add = [&](float (&acc)[16], int slot0, int cn) {
+    auto add = [&](float (&acc)[kCW], int slot0, int cn) {
       for (int i = 0; i < cn; ++i) {
-        const float *src = reinterpret_cast<const float *>(fs.base + static_cast<size_t>(slot0 + i) * kPiece);
+        const float *src =
+            reinterpret_cast<const float *>(fs.base + static_cast<size_t>(slot0 + i) * kPiece);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) acc[jj] += src[jj * kBM + r];
+        for (int jj = 0; jj < kCW; ++jj) acc[jj] += src[(ps.c0 + jj) * kBM + ps.r];
       }
     };
     if (n <= fs.pieces) {
@@ -487,20 +505,20 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, in
         fs.phase ^= 1u;
         for (int j = 0; j < bn; ++j) {
           const int k = me + (b0 + j) * n;
-          float acc[16];
+          float acc[kCW];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+          for (int jj = 0; jj < kCW; ++jj) acc[jj] = 0.f;
           add(acc, j * n, n);
-          emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, r, et, acc, es);
+          emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, ps, acc, es);
         }
-        named_bar(1, 128);  // every thread is done with the pieces before they are refilled
+        named_bar(1, kEpiThreads);  // every thread is done with the pieces before they are refilled
       }
     } else {
       for (int j = 0; j < my_chunks; ++j) {
         const int k = me + j * n;
-        float acc[16];
+        float acc[kCW];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+        for (int jj = 0; jj < kCW; ++jj) acc[jj] = 0.f;
         for (int c0 = 0; c0 < n; c0 += fs.pieces) {
           const int cn = min(fs.pieces, n - c0);
           if (et == 0) {
@@ -510,9 +528,9 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, in
           if (!mbar_wait(fs.bar, fs.phase)) return false;
           fs.phase ^= 1u;
           add(acc, 0, cn);
-          named_bar(1, 128);
+          named_bar(1, kEpiThreads);
         }
-        emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, r, et, acc, es);
+        emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, ps, acc, es);
       }
     }
   }
@@ -530,9 +548,12 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
                               uint64_t *acce, uint32_t tmem_base, long long u0, long long u1,
                               EpiSmem &es, FixupStage &fs, volatile int *sabort) {
   const int warp = threadIdx.x >> 5;
-  const int q = warp & 3;             // TMEM lane quarter this warp may access
-  const int r = q * 32 + (threadIdx.x & 31);
-  const int et = threadIdx.x - 64;    // 0..127 among epilogue threads
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  EpiPos ps;
+  ps.r = q * 32 + (threadIdx.x & 31);
+  ps.et = threadIdx.x - 64;
+  ps.c0 = ((warp - 2) >> 2) * kCW;  // warps 2-5 take the first columns, 6-9 the next
+  const int r = ps.r, et = ps.et;
   const int cta = blockIdx.x;
   const int first_tile = static_cast<int>(u0 / p.kb);
   pdl_wait();
@@ -558,12 +579,12 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
       const int slot = (tile == first_tile) ? 0 : 1;
       float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM;
       for (int j0 = 0; j0 < LW; j0 += 16) {
-        float v[16];
-        tmem_ld_logical(tbase, j0, LW, p.split, v);
+        float v[kCW];
+        tmem_ld_logical(tbase, j0 + ps.c0, LW, p.split, v);
         uint8_t *sb = stage_claim(es, et);
         float *f = reinterpret_cast<float *>(sb);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) f[jj * kBM + r] = v[jj];
+        for (int jj = 0; jj < kCW; ++jj) f[(ps.c0 + jj) * kBM + r] = v[jj];
         stage_publish();
         if (et == 0) {
           bulk_store(mine + static_cast<size_t>(j0) * kBM, sb, 16 * kBM * 4);
@@ -582,18 +603,18 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
       continue;
     }
     for (int j0 = 0; j0 < LW; j0 += 16) {
-      float v[16];
-      tmem_ld_logical(tbase, j0, LW, p.split, v);
-      emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + j0, j0, r, et, v, es);
+      float v[kCW];
+      tmem_ld_logical(tbase, j0 + ps.c0, LW, p.split, v);
+      emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + j0, j0, ps, v, es);
     }
     tc_fence_before();
     mbar_arrive(&acce[a]);
   }
   // Every accumulator of this CTA has been waited for, so all of its MMAs (and the loads
   // they consumed) are complete: the stage area is free for the fixups.
-  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, r, et, fs, es, sabort)) {
+  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, ps, fs, es, sabort)) {
     *sabort = 1;
-  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, r, et, fs, es, sabort)) {
+  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, ps, fs, es, sabort)) {
     *sabort = 1;
   }
   if (et == 0) bulk_wait<0>();  // every store of this CTA is complete before it exits
@@ -617,7 +638,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   es.next = 0;
   es.xbuf = reinterpret_cast<float *>(smem + L.off_x);
   es.red = reinterpret_cast<float *>(smem + L.off_red);
-  es.redi = reinterpret_cast<int32_t *>(es.red + 64);
+  es.redi = reinterpret_cast<int32_t *>(es.red + kEpiThreads / 2);
   es.rs = reinterpret_cast<float *>(smem + L.off_rs);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_bar);
   uint64_t *empty = full + p.stages;
@@ -640,8 +661,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&accf[0], 1);
     mbar_init(&accf[1], 1);
-    mbar_init(&acce[0], 128);
-    mbar_init(&acce[1], 128);
+    mbar_init(&acce[0], kEpiThreads);
+    mbar_init(&acce[1], kEpiThreads);
     mbar_init(&fixb[0], 1);
     *sabort = 0;
     fence_barrier_init();

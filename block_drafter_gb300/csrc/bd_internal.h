@@ -21,7 +21,12 @@ enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u };
 // weight matrices ("segments") that share the activation operand X.
 constexpr int kMaxSegs = 12;
 constexpr int kBM = 128;
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// Epilogue: kEpiSlices warps per TMEM lane quarter, each taking 16 / kEpiSlices of a
+// 16-column chunk, so every SM sub-partition has kEpiSlices epilogue warps whose
+// instruction latencies overlap.
+constexpr int kEpiSlices = 2;
+constexpr int kEpiThreads = 128 * kEpiSlices;
+constexpr int kGemmThreads = 64 + kEpiThreads;  // warp 0 TMA, warp 1 MMA, then the epilogue
 
 enum EpiMode : int {
   EPI_STORE_F32 = 0,  // out[tok*ld + out_col + row] = acc

@@ -50,6 +50,8 @@ def parse():
                     help="the main line's workload (b1: the metric's configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--profile-full", action="store_true",
+                    help="with --profile-case: all draft layers instead of one")
     ap.add_argument("--profile-case", action="store_true",
                     help="run two steps of a one-layer 27B-geometry round (batch from "
                          "--workload) and exit: the small case the ncu captures use")
@@ -434,7 +436,7 @@ def main():
         # [0] W_feature, [1] K/V, [2] QKV, [3] W_o, [4] gate/up, [5] down, [6] code read,
         # [7] gate/value maps, [8] write, [9] LM head.
         base = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8
-        geo = base.with_(n_layers=1, windows=(2048,))
+        geo = base if args.profile_full else base.with_(n_layers=1, windows=(2048,))
         st = State(geo, args.seed)
         st.step()
         torch.cuda.synchronize()
@@ -443,7 +445,7 @@ def main():
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         binding.sync_status()
-        print(json.dumps({"profile_case": geo.name, "layers": 1, "ok": True}))
+        print(json.dumps({"profile_case": geo.name, "layers": geo.n_layers, "ok": True}))
         return
 
     geo = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8

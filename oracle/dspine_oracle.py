@@ -20,6 +20,9 @@ Sources (cited by page title and section throughout):
   [Gate]          "DSpine 完全拆解", section "相邻因果注入" / "门控与写回" (gate and write).
   [BlockCausal]   "DSpine 完全拆解", section "块因果注意力" (block-causal attention).
   [Backbone]      "DSpark, every bolt and rivet", section 5.1 "The parallel backbone".
+  [Refine]        "DSpine for Qwen3.8-27B: Causal Features Through Depth", section "The
+                  last write is refined using discrete candidates" (16 candidates per
+                  proposal row; the fallback path scores with the BF16 vocabulary head).
 
 Readings taken where the pages are schematic or garbled (each also listed in the design doc):
   R-gate   g = sigmoid(G c_t + G_p c_{t-1} + b), m = g * (A c_{t-1}); b absent means 0.
@@ -37,6 +40,8 @@ Readings taken where the pages are schematic or garbled (each also listed in DES
            for a local layer (every populated position for a full layer); the
            block-causal flag additionally hides block keys j > i.
   R-tie    argmax ties go to the lowest token id; only the K mask rows are scored.
+  R-topk   a row's k candidates are its k largest exact logits over the whole
+           vocabulary, by descending score; equal scores keep the lower token id first.
 """
 from __future__ import annotations
 
@@ -329,6 +334,15 @@ def lm_head_logits(h, embed_head, chunk: int = 16384) -> np.ndarray:
 def argmax_lowest(logits) -> np.ndarray:
     """Per-row argmax; ties resolve to the lowest token id (R-tie)."""
     return np.argmax(_f64(logits), axis=-1)
+
+
+def lm_head_topk(logits, k: int):
+    """[Refine]: the k candidate tokens of each row and their scores -- the k largest
+    logits of the full vocabulary, by descending score, equal scores by ascending token
+    id (R-topk).  A stable sort of the negated logits gives exactly that order."""
+    logits = _f64(logits)
+    ids = np.argsort(-logits, axis=-1, kind="stable")[:, :k]
+    return ids, np.take_along_axis(logits, ids, axis=-1)
 
 
 def top2_gap(logits) -> np.ndarray:

@@ -436,6 +436,54 @@ def test_argmax_bruteforce_and_ties():
     assert gap[2] == 0.0
 
 
+def _topk_by_repeated_max(row, k):
+    """Selection written out: k times, take the largest remaining score, scanning ids in
+    ascending order so the lowest id wins a tie; remove it."""
+    left = list(range(len(row)))
+    ids = []
+    for _ in range(k):
+        best = None
+        for v in left:
+            if best is None or row[v] > row[best]:
+                best = v
+        ids.append(best)
+        left.remove(best)
+    return ids
+
+
+def test_topk_bruteforce_with_ties():
+    logits = rng.normal(0, 1, (5, 40))
+    logits[1, [3, 20, 33]] = logits[1].max() + 0.5          # three-way tie at the top
+    logits[3, [8, 9]] = np.sort(logits[3])[-5]               # a tie inside the top 16
+    logits[4] = np.round(logits[4], 1)                        # many ties
+    for k in (1, 5, 16, 40):
+        ids, sc = O.lm_head_topk(logits, k)
+        for i in range(5):
+            ref = _topk_by_repeated_max(list(logits[i]), k)
+            assert list(ids[i]) == ref, (k, i)
+            assert list(sc[i]) == [logits[i, v] for v in ref]
+    ids, _ = O.lm_head_topk(logits, 3)
+    assert list(ids[1]) == [3, 20, 33]
+
+
+def test_topk_first_is_argmax_and_scores_are_dot_products():
+    h = rng.normal(0, 1, (4, 24))
+    E = rng.normal(0, 1, (300, 24))
+    E[77] = E[5]                                             # duplicate row: equal scores
+    logits = O.lm_head_logits(h, E)
+    ids, sc = O.lm_head_topk(logits, 16)
+    assert (ids[:, 0] == O.argmax_lowest(logits)).all()
+    for i in range(4):
+        np.testing.assert_allclose(sc[i], [float(E[v] @ h[i]) for v in ids[i]], rtol=1e-12)
+        assert (np.diff(sc[i]) <= 0).all()
+        if 5 in ids[i] and 77 in ids[i]:
+            assert list(ids[i]).index(5) < list(ids[i]).index(77)
+    # every score outside the top 16 is <= the 16th
+    for i in range(4):
+        rest = np.delete(logits[i], ids[i])
+        assert rest.max() <= sc[i, -1]
+
+
 def test_lm_head_chunking_matches_product():
     h = rng.normal(0, 1, (3, 16))
     E = rng.normal(0, 1, (100, 16))

@@ -35,6 +35,7 @@ import torch  # noqa: E402
 
 import bdsynth  # noqa: E402
 
+TOPK = 16  # candidates per proposal row of the top-k head (timed beside the step)
 METRIC = "draft rounds/s (B=1, W=16, 27B DSpine-b16 geometry)"
 UNIT = "rounds/s"
 
@@ -183,6 +184,9 @@ class State:
         self.front = front
         self.anchors = torch.tensor(self.anchors_l, dtype=torch.int32, device=dev)
         self.head_in, self.tokens, self.maxl, _ = self.sess.alloc_outputs(B, geo.n_masks)
+        rows = self.head_in.shape[0]
+        self.cand = torch.empty(rows, TOPK, dtype=torch.int32, device=dev)
+        self.cand_score = torch.empty(rows, TOPK, dtype=torch.float32, device=dev)
         torch.cuda.synchronize()
 
     def materialize(self):
@@ -193,6 +197,9 @@ class State:
 
     def head(self):
         self.sess.head(self.head_in, self.tokens, self.maxl)
+
+    def head_topk(self):
+        self.sess.head_topk(self.head_in, TOPK, self.cand, self.cand_score)
 
     def step(self):
         self.materialize()
@@ -288,6 +295,21 @@ def time_graphs(st: State, steps: int, warmup: int, world: int):
            "round": sum(e[1].elapsed_time(e[2]) for e in ev) / steps,
            "head": sum(e[2].elapsed_time(e[3]) for e in ev) / steps}
     return tot / steps, per
+
+
+def time_call(fn, steps: int, warmup: int):
+    """Mean device time (ms) of one call replayed from a captured graph."""
+    g = capture(fn)
+    for _ in range(warmup):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
 
 
 def time_e2e(st: State, steps: int, warmup: int):
@@ -494,6 +516,7 @@ def main():
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_per_step": launches_per_step,
+        "head_topk16_us": 1000.0 * time_call(st.head_topk, args.steps, args.warmup),
     }
     if not args.no_b8 and args.workload == "b1":
         geo8 = bdsynth.DSPINE27B_B8
@@ -506,7 +529,8 @@ def main():
                       "rounds_per_s": world * 1000.0 / ms8,
                       "breakdown_us": {k: 1000.0 * v for k, v in per8.items()},
                       "achieved_step_gbs": gbs8, "frac_of_measured_hbm": gbs8 / hbm,
-                      "algorithmic_bytes_per_step": by8}
+                      "algorithmic_bytes_per_step": by8,
+                      "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup)}
         del st8
     if rank == 0 and not args.no_cpu_baseline:
         import numpy as np

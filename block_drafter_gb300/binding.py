@@ -24,7 +24,9 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
 
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
            "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
-           "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc")
+           "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk")
+
+TOPK_MAX = 16
 
 
 class BdError(RuntimeError):
@@ -99,6 +101,9 @@ def lib() -> C.CDLL:
         L.bd_lm_head_argmax_noalloc.restype = i
         L.bd_lm_head_argmax_noalloc.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, vp,
                                                 vp, vp]
+        L.bd_lm_head_topk.restype = i
+        L.bd_lm_head_topk.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, i, vp, vp, vp,
+                                      sz, vp]
         _lib = L
     return _lib
 
@@ -215,6 +220,16 @@ def lm_head_argmax(cfg: Config, weights: Weights, hidden: torch.Tensor, token_ou
     _check(lib().bd_lm_head_argmax(
         C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
         _ptr(max_logit_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def lm_head_topk(cfg: Config, weights: Weights, hidden: torch.Tensor, k: int,
+                 token_out: torch.Tensor, workspace: torch.Tensor,
+                 score_out: Optional[torch.Tensor] = None, stream=None):
+    """The k best candidates per hidden row: token_out / score_out [rows, k]."""
+    _check(lib().bd_lm_head_topk(
+        C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), int(k), _ptr(token_out),
+        _ptr(score_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
 

@@ -255,6 +255,10 @@ struct HeadWs {
   GemmWs g;
   float *amax_val;
   int32_t *amax_idx;
+  float *topk_val;    // [m_tiles][rows][kTopK] per-tile candidate lists
+  int32_t *topk_idx;
+  float *topk_part_val;  // [rows][slices][kTopK] per-slice lists
+  int32_t *topk_part_idx;
   void *hl;  // bf16 hi/lo pair of the hidden rows [2][pad16(rows)][H]
 };
 void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
@@ -264,6 +268,11 @@ void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   w.hl = cv.take<char>(static_cast<size_t>(2 * pad16(rows)) * c->hidden * 2);
   w.amax_val = cv.take<float>(m_tiles * rows);
   w.amax_idx = cv.take<int32_t>(m_tiles * rows);
+  w.topk_val = cv.take<float>(m_tiles * rows * kTopK);
+  w.topk_idx = cv.take<int32_t>(m_tiles * rows * kTopK);
+  const size_t slices = static_cast<size_t>(topk_slices(static_cast<int>(m_tiles)));
+  w.topk_part_val = cv.take<float>(rows * slices * kTopK);
+  w.topk_part_idx = cv.take<int32_t>(rows * slices * kTopK);
 }
 
 GemmScratch scratch_of(const GemmWs &g) {
@@ -628,9 +637,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   return BD_OK;
 }
 
-bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
-                            int32_t *token_out, float *max_logit_out, void *workspace,
-                            size_t workspace_bytes, void *stream_) {
+// Checks shared by the head entry points, carves the head workspace and enqueues the
+// hi/lo split of the hidden rows (or the counter clear); returns the GEMM plan.
+static bd_status head_prepare(const bd_config *cfg, const bd_weights *w, const float *hidden,
+                              int rows, const int32_t *token_out, void *workspace,
+                              size_t workspace_bytes, cudaStream_t s, HeadWs &hw, GemmPlan &p) {
   std::string e = check_config(cfg);
   if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
   if (!w || !w->embed_head || !aligned16(w->embed_head))
@@ -640,10 +651,8 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
   if (!token_out) return fail(BD_ERR_INVALID_ARG, "token_out NULL");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
-  cudaStream_t s = static_cast<cudaStream_t>(stream_);
   Carve cv;
   cv.base = static_cast<char *>(workspace);
-  HeadWs hw;
   carve_head(cv, hw, cfg, rows, num_sms());
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
   const bool split = cfg->dtype == BD_BF16;
@@ -652,16 +661,48 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
                              static_cast<size_t>(pad16(rows)) * cfg->hidden, counters_of(hw.g), s));
   else
     BD_TRY(launch_zero(counters_of(hw.g), s));
-  GemmPlan p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
+  p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
   p.split = split;
   add_w(p, w->embed_head, cfg->vocab, static_cast<const uint8_t *>(w->packed),
         w->packed ? packed_layout(cfg).head : 0);
+  return BD_OK;
+}
+
+bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
+                            int32_t *token_out, float *max_logit_out, void *workspace,
+                            size_t workspace_bytes, void *stream_) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  HeadWs hw;
+  GemmPlan p;
+  const bd_status st = head_prepare(cfg, w, hidden, rows, token_out, workspace, workspace_bytes, s,
+                                    hw, p);
+  if (st != BD_OK) return st;
   p.args.epi = EPI_ARGMAX;
   p.args.amax_val = hw.amax_val;
   p.args.amax_idx = hw.amax_idx;
   BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
   BD_TRY(launch_argmax_reduce(hw.amax_val, hw.amax_idx, static_cast<int>(tiles_of(cfg->vocab, 128)),
                               rows, token_out, max_logit_out, s));
+  return BD_OK;
+}
+
+bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
+                          int k, int32_t *token_out, float *score_out, void *workspace,
+                          size_t workspace_bytes, void *stream_) {
+  if (k < 1 || k > BD_TOPK_MAX) return fail(BD_ERR_INVALID_ARG, "k must be in 1..16");
+  if (cfg && cfg->vocab < k) return fail(BD_ERR_INVALID_ARG, "vocab smaller than k");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  HeadWs hw;
+  GemmPlan p;
+  const bd_status st = head_prepare(cfg, w, hidden, rows, token_out, workspace, workspace_bytes, s,
+                                    hw, p);
+  if (st != BD_OK) return st;
+  p.args.epi = EPI_TOPK;
+  p.args.topk_val = hw.topk_val;
+  p.args.topk_idx = hw.topk_idx;
+  BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
+  BD_TRY(launch_topk_reduce(hw.topk_val, hw.topk_idx, static_cast<int>(tiles_of(cfg->vocab, 128)),
+                            rows, k, hw.topk_part_val, hw.topk_part_idx, token_out, score_out, s));
   return BD_OK;
 }
 

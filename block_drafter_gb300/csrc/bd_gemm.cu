@@ -355,6 +355,84 @@ __device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int 
   }
 }
 
+// (score, id) order of the candidate lists: higher score first, equal scores lower id first.
+__device__ __forceinline__ bool cand_better(float a, int ai, float b, int bi) {
+  return a > b || (a == b && ai < bi);
+}
+
+// Per-(vocab tile, token) 16 best rows, in candidate order.  The chunk is transposed
+// through shared memory; the 16 threads of a half warp own one token column, 8 rows each,
+// sorted locally; 16 rounds of a half-warp argmax over the list heads then give the
+// column's candidates in order (the winning thread drops its head).  The lists are staged
+// in shared memory and leave as two contiguous bulk stores per chunk.
+__device__ __forceinline__ void topk_chunk(const GemmArgs &p, int m_tile, int tok0,
+                                           const EpiPos &ps, const float (&v)[kCW],
+                                           EpiSmem &es) {
+  static_assert(kEpiThreads == 256, "16 token columns x 16 threads per column");
+  const int row_id = m_tile * kBM + ps.r;
+#pragma unroll
+  for (int jj = 0; jj < kCW; ++jj)
+    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
+  uint8_t *sb = stage_claim(es, ps.et);  // also orders the transpose writes before the reads
+  float *sv = reinterpret_cast<float *>(sb);                 // [16 tokens][kTopK]
+  int32_t *si = reinterpret_cast<int32_t *>(sb + 16 * kTopK * 4);
+  const int col = ps.et >> 4, l16 = ps.et & 15;
+  float lv[8];
+  int li[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = l16 * 8 + i;
+    lv[i] = es.xbuf[row * kXStride + col];
+    li[i] = m_tile * kBM + row;
+  }
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+#pragma unroll
+    for (int j = i; j > 0; --j)
+      if (cand_better(lv[j], li[j], lv[j - 1], li[j - 1])) {
+        const float tv = lv[j];
+        lv[j] = lv[j - 1];
+        lv[j - 1] = tv;
+        const int ti = li[j];
+        li[j] = li[j - 1];
+        li[j - 1] = ti;
+      }
+  for (int rnd = 0; rnd < kTopK; ++rnd) {
+    float bv = lv[0];
+    int bi = li[0];
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (cand_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (li[0] == bi) {  // this thread's head was taken
+#pragma unroll
+      for (int i = 0; i < 7; ++i) {
+        lv[i] = lv[i + 1];
+        li[i] = li[i + 1];
+      }
+      lv[7] = -INFINITY;
+      li[7] = 0x7fffffff;
+    }
+    if (l16 == 0) {
+      sv[col * kTopK + rnd] = bv;
+      si[col * kTopK + rnd] = bi;
+    }
+  }
+  stage_publish();  // also frees the transpose buffer for the next chunk
+  const int n_tok = min(16, p.n_tokens - tok0);
+  if (ps.et == 0 && n_tok > 0) {
+    const size_t o = (static_cast<size_t>(m_tile) * p.n_tokens + tok0) * kTopK;
+    bulk_store(p.topk_val + o, sv, static_cast<uint32_t>(n_tok) * kTopK * 4);
+    bulk_store(p.topk_idx + o, si, static_cast<uint32_t>(n_tok) * kTopK * 4);
+    bulk_commit();
+  }
+}
+
 // Writes the finished values v (tile row ps.r, token columns tok0+ps.c0 .. +kCW-1; j0 =
 // tok0 minus the tile's first token) of m_tile to the epilogue's destination.
 template <typename T, int EPI>
@@ -363,6 +441,10 @@ __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs 
                                            const float (&v)[kCW], EpiSmem &es) {
   if (EPI == EPI_ARGMAX) {
     argmax_chunk(p, m_tile, tok0, ps, v, es);
+    return;
+  }
+  if (EPI == EPI_TOPK) {
+    topk_chunk(p, m_tile, tok0, ps, v, es);
     return;
   }
   const int r = ps.r, c0 = ps.c0;
@@ -673,7 +755,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
   }
   if (threadIdx.x == 64) {  // result maps, used by the epilogue's stores
-    const int n_out = EPI == EPI_STORE_F32 ? p.n_segs : (EPI == EPI_ARGMAX ? 0 : 1);
+    const int n_out = EPI == EPI_STORE_F32 ? p.n_segs : (EPI == EPI_ARGMAX || EPI == EPI_TOPK ? 0 : 1);
     for (int s = 0; s < n_out; ++s) tma_prefetch_desc(&maps.out[s]);
   }
   if (warp == 1) {
@@ -856,6 +938,7 @@ static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStr
     case EPI_INJECT: return launch_epi<T, EPI_INJECT>(maps, a, stream);
     case EPI_SWIGLU: return launch_epi<T, EPI_SWIGLU>(maps, a, stream);
     case EPI_ARGMAX: return launch_epi<T, EPI_ARGMAX>(maps, a, stream);
+    case EPI_TOPK: return launch_epi<T, EPI_TOPK>(maps, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -33,8 +33,10 @@ enum EpiMode : int {
   EPI_RESID_F32 = 1,  // out[tok*ld + row] += acc (one addition per element: deterministic)
   EPI_INJECT = 2,     // x[tok*ld + row] += scale[tok] * acc for non-anchor rows
   EPI_SWIGLU = 3,     // pair tiles: out[tok*ld_act + f] = SiLU(gate_f) * up_f
-  EPI_ARGMAX = 4      // per-tile (max, lowest argmax) over 128 vocabulary rows
+  EPI_ARGMAX = 4,     // per-tile (max, lowest argmax) over 128 vocabulary rows
+  EPI_TOPK = 5        // per-tile 16 best (score, id) over 128 vocabulary rows
 };
+constexpr int kTopK = 16;  // candidates per tile and per row of the top-k head
 
 struct GemmSeg {
   int rows;               // output rows of this weight matrix
@@ -63,6 +65,8 @@ struct __align__(16) GemmArgs {
   void *out_act;
   float *amax_val;                // [m_tiles][n_tokens]
   int32_t *amax_idx;
+  float *topk_val;                // [m_tiles][n_tokens][kTopK], descending
+  int32_t *topk_idx;
   float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
   unsigned *counters;             // [2][n_counter_tiles] arrival / done counters (start at 0)
   int n_counter_tiles;

@@ -104,6 +104,15 @@ std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);
 // Per-row argmax over per-tile (max, lowest argmax) pairs; lowest id on ties.
 std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_tiles, int rows,
                                  int32_t *tok_out, float *max_out, cudaStream_t s);
+// Per-row k best (k <= kTopK) over the per-tile candidate lists [m_tiles][rows][kTopK]:
+// descending score, equal scores to the lower id.  Two launches: slices of at most
+// kTopKTilesPerSlice tiles per row (scratch part_* [rows][topk_slices][kTopK]), then one
+// warp per row over the slices.
+constexpr int kTopKTilesPerSlice = 128;
+int topk_slices(int m_tiles);
+std::string launch_topk_reduce(const float *val, const int32_t *idx, int m_tiles, int rows, int k,
+                               float *part_val, int32_t *part_idx, int32_t *tok_out,
+                               float *score_out, cudaStream_t s);
 // Copy rows [n, H] fp32 (used for the optional per-layer residual output).
 std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
 

@@ -329,6 +329,160 @@ __global__ void argmax_reduce_kernel(const float *val, const int32_t *idx, int m
   }
 }
 
+// Candidate order: higher score first, equal scores to the lower id.
+__device__ __forceinline__ bool cand_better(float a, int ai, float b, int bi) {
+  return a > b || (a == b && ai < bi);
+}
+// Insert (x, xi) into the sorted list (L, I) of kTopK entries if it beats the last one.
+__device__ __forceinline__ bool cand_insert(float (&L)[kTopK], int (&I)[kTopK], float x, int xi) {
+  if (!cand_better(x, xi, L[kTopK - 1], I[kTopK - 1])) return false;
+  bool placed = false;
+#pragma unroll
+  for (int j = kTopK - 1; j > 0; --j) {
+    if (!placed) {
+      if (cand_better(x, xi, L[j - 1], I[j - 1])) {
+        L[j] = L[j - 1];
+        I[j] = I[j - 1];
+      } else {
+        L[j] = x;
+        I[j] = xi;
+        placed = true;
+      }
+    }
+  }
+  if (!placed) {
+    L[0] = x;
+    I[0] = xi;
+  }
+  return true;
+}
+
+// Top-k merge, stage 1: CTA (slice, row) merges the candidate lists of vocabulary tiles
+// [slice * per, slice * per + per) of one row into one list.  Each thread inserts the
+// lists of its tiles into a private sorted list (a tile's list is sorted, so its scan stops
+// at the first candidate that does not enter); the 32 lists of a warp are merged by 16
+// rounds of a warp argmax over the list heads (the winner drops its head), then the 8
+// warp lists the same way by the first warp.
+__global__ void __launch_bounds__(256) topk_slice_kernel(const float *val, const int32_t *idx,
+                                                         int m_tiles, int rows, int per,
+                                                         float *part_val, int32_t *part_idx) {
+  __shared__ float wv[8][kTopK];
+  __shared__ int wi[8][kTopK];
+  pdl_wait();
+  pdl_trigger();
+  const int slice = blockIdx.x, row = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float L[kTopK];
+  int I[kTopK];
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    L[j] = -INFINITY;
+    I[j] = 0x7fffffff;
+  }
+  const int m_end = min(m_tiles, (slice + 1) * per);
+  for (int m = slice * per + threadIdx.x; m < m_end; m += blockDim.x) {
+    const size_t o = (static_cast<size_t>(m) * rows + row) * kTopK;
+    const float4 *pv = reinterpret_cast<const float4 *>(val + o);
+    const int4 *pi = reinterpret_cast<const int4 *>(idx + o);
+    float4 cv[kTopK / 4];
+    int4 ci[kTopK / 4];
+#pragma unroll
+    for (int q = 0; q < kTopK / 4; ++q) {
+      cv[q] = pv[q];
+      ci[q] = pi[q];
+    }
+    const float *fv = reinterpret_cast<const float *>(cv);
+    const int *fi = reinterpret_cast<const int *>(ci);
+#pragma unroll
+    for (int j = 0; j < kTopK; ++j)
+      if (!cand_insert(L, I, fv[j], fi[j])) break;
+  }
+  for (int rnd = 0; rnd < kTopK; ++rnd) {
+    float bv = L[0];
+    int bi = I[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (cand_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (I[0] == bi && L[0] == bv) {
+#pragma unroll
+      for (int j = 0; j < kTopK - 1; ++j) {
+        L[j] = L[j + 1];
+        I[j] = I[j + 1];
+      }
+      L[kTopK - 1] = -INFINITY;
+      I[kTopK - 1] = 0x7fffffff;
+    }
+    if (lane == 0) {
+      wv[warp][rnd] = bv;
+      wi[warp][rnd] = bi;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  int ptr = 0;  // lane w < 8 walks warp w's list
+  const size_t o = (static_cast<size_t>(row) * gridDim.x + slice) * kTopK;
+  for (int rnd = 0; rnd < kTopK; ++rnd) {
+    float bv = (lane < 8 && ptr < kTopK) ? wv[lane][ptr] : -INFINITY;
+    int bi = (lane < 8 && ptr < kTopK) ? wi[lane][ptr] : 0x7fffffff;
+    const float mv = bv;
+    const int mi = bi;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (cand_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane < 8 && mi == bi && mv == bv) ++ptr;
+    if (lane == 0) {
+      part_val[o + rnd] = bv;
+      part_idx[o + rnd] = bi;
+    }
+  }
+}
+
+// Top-k merge, stage 2: one warp per row merges the row's slice lists (lane s walks list
+// s) and writes the k best.
+__global__ void __launch_bounds__(32) topk_final_kernel(const float *part_val,
+                                                        const int32_t *part_idx, int slices,
+                                                        int k, int32_t *tok_out,
+                                                        float *score_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, lane = threadIdx.x;
+  const size_t base = (static_cast<size_t>(row) * slices + lane) * kTopK;
+  int ptr = 0;
+  for (int rnd = 0; rnd < k; ++rnd) {
+    const bool has = lane < slices && ptr < kTopK;
+    float bv = has ? part_val[base + ptr] : -INFINITY;
+    int bi = has ? part_idx[base + ptr] : 0x7fffffff;
+    const float mv = bv;
+    const int mi = bi;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (cand_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (has && mi == bi && mv == bv) ++ptr;
+    if (lane == 0) {
+      tok_out[static_cast<size_t>(row) * k + rnd] = bi;
+      if (score_out) score_out[static_cast<size_t>(row) * k + rnd] = bv;
+    }
+  }
+}
+
 // fp32 rows -> bf16 hi rows [0, rows) and lo rows [lo_row, lo_row + rows).
 __global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off,
                                   ZeroSpan z) {
@@ -457,6 +611,21 @@ std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_til
                                  int32_t *tok_out, float *max_out, cudaStream_t s) {
   return err("argmax reduce", launch_pdl(argmax_reduce_kernel, dim3(rows), dim3(256), 0, s, val,
                                          idx, m_tiles, rows, tok_out, max_out));
+}
+
+int topk_slices(int m_tiles) { return (m_tiles + kTopKTilesPerSlice - 1) / kTopKTilesPerSlice; }
+
+std::string launch_topk_reduce(const float *val, const int32_t *idx, int m_tiles, int rows, int k,
+                               float *part_val, int32_t *part_idx, int32_t *tok_out,
+                               float *score_out, cudaStream_t s) {
+  const int slices = topk_slices(m_tiles);
+  if (slices > 32) return "top-k reduce: vocabulary too large";
+  cudaError_t e = launch_pdl(topk_slice_kernel, dim3(slices, rows), dim3(256), 0, s, val, idx,
+                             m_tiles, rows, kTopKTilesPerSlice, part_val, part_idx);
+  if (e == cudaSuccess)
+    e = launch_pdl(topk_final_kernel, dim3(rows), dim3(32), 0, s, part_val, part_idx, slices, k,
+                   tok_out, score_out);
+  return err("top-k reduce", e);
 }
 
 std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s) {

@@ -67,6 +67,11 @@ class DraftSession:
         B.lm_head_argmax(self.cfg, self.wstruct, hidden, token_out, self.workspace,
                          max_logit_out, stream)
 
+    def head_topk(self, hidden: torch.Tensor, k: int, token_out: torch.Tensor,
+                  score_out: Optional[torch.Tensor] = None, stream=None):
+        B.lm_head_topk(self.cfg, self.wstruct, hidden, k, token_out, self.workspace, score_out,
+                       stream)
+
     def alloc_outputs(self, Bn: int, n_masks: int):
         W = n_masks + 1
         H = self.geo.hidden

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 2
+#define BD_ABI_VERSION 3
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -215,6 +215,27 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
 bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const float *hidden,
                             int rows, int32_t *token_out, float *max_logit_out,
                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Tied LM head with the k best candidates per row (k <= 16; the candidate sets of the
+ * last-write refinement).  "DSpine for Qwen3.8-27B: Causal Features Through Depth",
+ * section "The last write is refined using discrete candidates": the released drafter
+ * keeps 16 candidates per proposal row, and its fallback path scores them with the BF16
+ * vocabulary head -- the exact version computed here (no FP8 pre-selection):
+ *   logits = embed_head . hidden_r ;  the k largest logits of row r, by descending
+ *   score, equal scores to the lower token id.
+ * Arithmetic as in bd_lm_head_argmax; candidate r*k + 0 is bd_lm_head_argmax's token.
+ *
+ *   hidden     dev fp32 [rows, H];  rows 1 .. 8*15;  k 1 .. BD_TOPK_MAX (and <= vocab)
+ *   token_out  dev int32 [rows, k]  OUT candidate ids, best first
+ *   score_out  dev fp32 [rows, k]   OUT their logits, or NULL
+ * Errors: BD_ERR_INVALID_ARG for k, rows or pointers out of range; the workspace is the
+ * one bd_workspace_bytes sizes (it covers both head entry points).
+ */
+#define BD_TOPK_MAX 16
+bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
+                          int k, int32_t *token_out, float *score_out, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * bd_lm_head_argmax without a workspace, for callers that cannot allocate device

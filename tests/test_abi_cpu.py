@@ -120,6 +120,15 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     # head: rows out of range
     st = L.bd_lm_head_argmax(C.byref(c), C.byref(w), 0x10000, 121, 0x10000, None, ws, 1 << 30, None)
     assert st == -1
+    # top-k head: k out of range, rows out of range, misaligned workspace
+    for k in (0, 17):
+        st = L.bd_lm_head_topk(C.byref(c), C.byref(w), 0x10000, 4, k, 0x10000, None, ws, 1 << 30, None)
+        assert st == -1 and b"k must be" in L.bd_last_error()
+    st = L.bd_lm_head_topk(C.byref(c), C.byref(w), 0x10000, 0, 16, 0x10000, None, ws, 1 << 30, None)
+    assert st == -1
+    st = L.bd_lm_head_topk(C.byref(c), C.byref(w), 0x10000, 4, 16, 0x10000, None, ws + 16, 1 << 30,
+                           None)
+    assert st == -5
     # materialise: no rows
     st = L.bd_ctx_kv_materialize(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 0x10000,
                                  0x10000, 0, ws, 1 << 30, None)

@@ -23,6 +23,8 @@ Sources (cited by page title and section throughout):
   [Refine]        "DSpine for Qwen3.8-27B: Causal Features Through Depth", section "The
                   last write is refined using discrete candidates" (16 candidates per
                   proposal row; the fallback path scores with the BF16 vocabulary head).
+  [Tail]          "DSpine 完全拆解", section "前驱条件解码与 transition cache"
+                  (last-write refinement, the K x K transition table, greedy walk).
 
 Readings taken where the pages are schematic or garbled (each also listed in the design doc):
   R-gate   g = sigmoid(G c_t + G_p c_{t-1} + b), m = g * (A c_{t-1}); b absent means 0.
@@ -42,6 +44,15 @@ Readings taken where the pages are schematic or garbled (each also listed in DES
   R-tie    argmax ties go to the lowest token id; only the K mask rows are scored.
   R-topk   a row's k candidates are its k largest exact logits over the whole
            vocabulary, by descending score; equal scores keep the lower token id first.
+  R-tail   last-write refinement of block row i with predecessor token s: the last
+           layer's injection into row i is redone from its pre-injection state u_i, its
+           receiver code c_i and RMS r_i, with the predecessor code replaced by
+           sqrt(Rc) * codebook[s]; the result goes through the final norm and the tied
+           head.  Row 1's predecessor is the anchor, whose code the round already used,
+           so row 1 keeps the round's scores; rows i >= 2 get the table
+           T_i[p, j] = score of candidate j of row i after refinement with candidate p of
+           row i - 1.  The greedy walk takes, row by row, the lowest-rank argmax of the
+           table row of the previous choice.
 """
 from __future__ import annotations
 
@@ -378,14 +389,19 @@ def draft_request(geo, weights, rings, request: int, anchor: int, frontier: int,
         lw = weights["layers"][l]
         k_ctx, v_ctx, cpos = ring_context(rings, l, request, frontier, geo.capacity(l))
         x, _, _ = dflash_layer(x, lw, geo, positions, k_ctx, v_ctx, cpos, frontier, l)
+        tail = None
         if inj:
             c, r = bridge_read(x, lw["r_read"], geo.code_width, geo.eps)
             c[0] = anchor_code(weights["codebook"][anchor], geo.code_width)
+            tail = {"u": x.copy(), "c": c, "r": r}
             x = inject(x, c, r, weights["g_recv"], weights["g_pred"], weights["a_val"],
                        lw["w_write"], weights.get("gate_bias"))
         layers_x.append(x.copy())
     h = plain_rmsnorm(x, weights["final_norm"], geo.eps)
-    return {"x_layers": np.stack(layers_x), "h": h}
+    out = {"x_layers": np.stack(layers_x), "h": h}
+    if inj:
+        out["tail"] = tail  # the last layer's pre-injection state, codes and RMS
+    return out
 
 
 def draft_round(geo, weights, rings, anchors: Sequence[int], frontiers: Sequence[int],
@@ -398,6 +414,8 @@ def draft_round(geo, weights, rings, anchors: Sequence[int], frontiers: Sequence
                           mask_id, n_masks) for b in range(len(anchors))]
     res = {"x_layers": np.stack([o["x_layers"] for o in outs], axis=1),
            "h": np.stack([o["h"] for o in outs])}
+    if geo.code_width > 0:
+        res["tail"] = [o["tail"] for o in outs]
     if with_head:
         B = len(anchors)
         hm = res["h"][:, 1:, :].reshape(B * n_masks, -1)
@@ -406,6 +424,46 @@ def draft_round(geo, weights, rings, anchors: Sequence[int], frontiers: Sequence
         res["tokens"] = argmax_lowest(logits).reshape(B, n_masks)
         res["gap"] = top2_gap(logits).reshape(B, n_masks)
     return res
+
+
+# --------------------------------------------------------------------------- tail
+def refine_state(geo, weights, tail, i: int, s: int) -> np.ndarray:
+    """Last-write refinement of block row i (>= 1) with predecessor token s (R-tail):
+        c_pred = sqrt(Rc) C_s,  g = sigmoid(G c_i + G_p c_pred + b),  m = g * (A c_pred),
+        x' = u_i + r_i W_L m,   h' = plain_rmsnorm(x', final_norm).
+    [Tail] last-write refinement; [Gate] for the injection it redoes."""
+    lw = weights["layers"][geo.n_layers - 1]
+    u, c, r = _f64(tail["u"][i]), _f64(tail["c"][i]), float(tail["r"][i])
+    b = np.zeros(_f64(weights["g_recv"]).shape[0]) if weights.get("gate_bias") is None \
+        else _f64(weights["gate_bias"])
+    c_pred = anchor_code(weights["codebook"][s], geo.code_width)
+    g = sigmoid(_f64(weights["g_recv"]) @ c + _f64(weights["g_pred"]) @ c_pred + b)
+    m = g * (_f64(weights["a_val"]) @ c_pred)
+    x = u + r * (_f64(lw["w_write"]) @ m)
+    return plain_rmsnorm(x[None, :], weights["final_norm"], geo.eps)[0]
+
+
+def refine_tail(geo, weights, tail, anchor: int, cand):
+    """Transition tables and greedy walk of one request's block (R-tail).
+    cand [K, k]: candidate token ids of block rows 1..K (row i at cand[i - 1]).
+    Returns (scores1 [k], tables [K-1, k, k], picks [K] candidate indices, tokens [K]);
+    tables[i - 2][p, j] = E[cand[i-1][j]] . refine_state(i, cand[i-2][p]).
+    [Tail]: the K x K pair scores, then the left-to-right lookup."""
+    E = weights["embed_head"]
+    K, k = cand.shape
+    h1 = refine_state(geo, weights, tail, 1, anchor)
+    scores1 = np.array([float(_f64(E[v]) @ h1) for v in cand[0]])
+    tables = np.zeros((K - 1, k, k))
+    for i in range(2, K + 1):
+        for p in range(k):
+            h = refine_state(geo, weights, tail, i, int(cand[i - 2][p]))
+            tables[i - 2, p] = [float(_f64(E[v]) @ h) for v in cand[i - 1]]
+    picks = np.zeros(K, dtype=np.int64)
+    picks[0] = int(np.argmax(scores1))             # lowest rank on ties
+    for i in range(2, K + 1):
+        picks[i - 1] = int(np.argmax(tables[i - 2, picks[i - 2]]))
+    tokens = np.array([cand[i][picks[i]] for i in range(K)])
+    return scores1, tables, picks, tokens
 
 
 # --------------------------------------------------------------------------- sizes

@@ -600,3 +600,71 @@ def test_27b_block_geometry():
     assert w.W == gd["W"] and w.n_masks == gd["masks"]
     assert w.n_q_heads * w.head_dim == gd["q_proj_width"] and w.hidden == gd["hidden"]
     assert w.mask_token_id == GOLD["qwen3_mask_token_id"]["value"]
+
+
+# ----------------------------------------------------------------- last-write refinement
+def _cands(res, b, k):
+    ids, _ = O.lm_head_topk(res["logits"][b], k)
+    return ids
+
+
+def test_refining_row_one_with_the_anchor_reproduces_the_round():
+    g = Geo(windows=(6, 0))
+    w = rand_weights(g, gate_bias=True)
+    res, _ = _round(g, w)
+    for b, a in enumerate([5, 17]):
+        h1 = O.refine_state(g, w, res["tail"][b], 1, a)
+        np.testing.assert_allclose(h1, res["h"][b, 1], rtol=1e-12, atol=1e-12)
+
+
+def test_refining_with_the_predicted_code_reproduces_every_row():
+    # Give token t the round's predicted (unit-scaled) code of row i - 1: refining row i
+    # with t must then redo exactly the round's last injection into row i.
+    g = Geo(windows=(6, 0))
+    w = rand_weights(g)
+    res, _ = _round(g, w, B=1, F=(9,))
+    tail = res["tail"][0]
+    for i in range(2, 6):
+        w2 = dict(w)
+        cb = np.array(w["codebook"], dtype=np.float64)
+        cb[3] = tail["c"][i - 1] / math.sqrt(g.code_width)
+        w2["codebook"] = cb
+        np.testing.assert_allclose(O.refine_state(g, w2, tail, i, 3), res["h"][0, i],
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_zero_write_tables_do_not_depend_on_the_predecessor():
+    g = Geo(windows=(6, 0))
+    w = rand_weights(g, zero_write=True)
+    res, _ = _round(g, w, B=1, F=(9,))
+    cand = _cands(res, 0, 4)
+    s1, tables, picks, tokens = O.refine_tail(g, w, res["tail"][0], 5, cand)
+    for t in tables:
+        assert np.allclose(t, t[0][None, :], rtol=1e-12, atol=1e-12)
+    # every row then picks its best candidate, which is the round's own argmax
+    assert (tokens == res["tokens"][0]).all() and (picks == 0).all()
+    np.testing.assert_allclose(s1, res["logits"][0, 0, cand[0]], rtol=1e-12)
+
+
+def test_walk_follows_the_previous_choice_and_tables_are_local():
+    g = Geo(windows=(6, 0))
+    w = rand_weights(g, seed=2)
+    res, _ = _round(g, w, B=1, F=(9,))
+    cand = _cands(res, 0, 4)
+    s1, tables, picks, tokens = O.refine_tail(g, w, res["tail"][0], 5, cand)
+    assert picks[0] == int(np.argmax(s1))
+    for i in range(2, 6):
+        row = tables[i - 2][picks[i - 2]]
+        assert picks[i - 1] == int(np.argmax(row))
+        assert tokens[i - 1] == cand[i - 1][picks[i - 1]]
+    # table entry (i, p, j) by its definition: refine row i with candidate p of row i-1,
+    # score candidate j of row i
+    for i, p, j in ((2, 0, 1), (4, 3, 2), (5, 1, 0)):
+        h = O.refine_state(g, w, res["tail"][0], i, int(cand[i - 2][p]))
+        assert abs(tables[i - 2][p, j] - float(np.asarray(w["embed_head"])[cand[i - 1][j]] @ h)) < 1e-12
+    # changing row 3's pre-injection state changes table 3 only
+    t2 = {k: np.array(v, copy=True) for k, v in res["tail"][0].items()}
+    t2["u"][3] *= 1.5
+    _, tables2, _, _ = O.refine_tail(g, w, t2, 5, cand)
+    changed = [not np.allclose(tables2[t], tables[t]) for t in range(4)]
+    assert changed == [False, True, False, False]

@@ -187,6 +187,8 @@ class State:
         rows = self.head_in.shape[0]
         self.cand = torch.empty(rows, TOPK, dtype=torch.int32, device=dev)
         self.cand_score = torch.empty(rows, TOPK, dtype=torch.float32, device=dev)
+        self.tail = self.sess.alloc_tail_state(B, geo.n_masks)
+        self.refined = torch.empty(rows, dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
     def materialize(self):
@@ -200,6 +202,14 @@ class State:
 
     def head_topk(self):
         self.sess.head_topk(self.head_in, TOPK, self.cand, self.cand_score)
+
+    def round_with_tail(self):
+        self.sess.round(self.anchors, self.front, self.geo.n_masks, self.head_in,
+                        tail_state=self.tail)
+
+    def refine(self):
+        self.sess.refine_tail(self.tail, self.cand, self.cand_score, self.geo.batch,
+                              self.geo.n_masks, self.refined)
 
     def step(self):
         self.materialize()
@@ -310,6 +320,15 @@ def time_call(fn, steps: int, warmup: int):
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps
+
+
+def refine_us(st: State, args) -> float:
+    """Device time of the last-write refinement (tables + walk) after a round that exported
+    its tail state and a top-16 head that produced the candidates."""
+    st.round_with_tail()
+    st.head_topk()
+    torch.cuda.synchronize()
+    return 1000.0 * time_call(st.refine, args.steps, args.warmup)
 
 
 def time_e2e(st: State, steps: int, warmup: int):
@@ -517,6 +536,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_per_step": launches_per_step,
         "head_topk16_us": 1000.0 * time_call(st.head_topk, args.steps, args.warmup),
+        "refine_tail_us": refine_us(st, args),
     }
     if not args.no_b8 and args.workload == "b1":
         geo8 = bdsynth.DSPINE27B_B8
@@ -530,7 +550,8 @@ def main():
                       "breakdown_us": {k: 1000.0 * v for k, v in per8.items()},
                       "achieved_step_gbs": gbs8, "frac_of_measured_hbm": gbs8 / hbm,
                       "algorithmic_bytes_per_step": by8,
-                      "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup)}
+                      "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup),
+                      "refine_tail_us": refine_us(st8, args)}
         del st8
     if rank == 0 and not args.no_cpu_baseline:
         import numpy as np

@@ -24,7 +24,8 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
 
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
            "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
-           "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk")
+           "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk",
+           "bd_refine_tail")
 
 TOPK_MAX = 16
 
@@ -86,7 +87,10 @@ def lib() -> C.CDLL:
                                             C.POINTER(KvCache), vp, vp, vp, vp, i, vp, sz, vp]
         L.bd_draft_round.restype = i
         L.bd_draft_round.argtypes = [C.POINTER(Config), C.POINTER(Weights), C.POINTER(KvCache),
-                                     vp, vp, i, i, vp, vp, vp, vp, sz, vp]
+                                     vp, vp, i, i, vp, vp, vp, vp, vp, sz, vp]
+        L.bd_refine_tail.restype = i
+        L.bd_refine_tail.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, vp, vp, i, i, i,
+                                     vp, vp, vp, vp, sz, vp]
         L.bd_lm_head_argmax.restype = i
         L.bd_lm_head_argmax.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, vp, vp,
                                         vp, sz, vp]
@@ -206,11 +210,30 @@ def ctx_kv_materialize(cfg: Config, weights: Weights, kv: KvCache, target_feats:
 def draft_round(cfg: Config, weights: Weights, kv: KvCache, anchor_ids: torch.Tensor,
                 frontier: torch.Tensor, n_masks: int, head_in: torch.Tensor,
                 workspace: torch.Tensor, hidden_out: Optional[torch.Tensor] = None,
-                layers_out: Optional[torch.Tensor] = None, stream=None):
+                layers_out: Optional[torch.Tensor] = None, stream=None,
+                tail_state: Optional[torch.Tensor] = None):
     _check(lib().bd_draft_round(
         C.byref(cfg), C.byref(weights), C.byref(kv), _ptr(anchor_ids), _ptr(frontier),
         int(anchor_ids.shape[0]), int(n_masks), _ptr(head_in), _ptr(hidden_out),
-        _ptr(layers_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(layers_out), _ptr(tail_state), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tail_state_floats(cfg: Config, B: int, n_masks: int) -> int:
+    """Size of bd_draft_round's tail_state: T*H + T + T*Mc floats, T = B*(n_masks+1)."""
+    T = B * (n_masks + 1)
+    return T * (cfg.hidden + 1 + cfg.msg_width)
+
+
+def refine_tail(cfg: Config, weights: Weights, tail_state: torch.Tensor, cand_ids: torch.Tensor,
+                cand_scores: torch.Tensor, B: int, n_masks: int, token_out: torch.Tensor,
+                workspace: torch.Tensor, pick_out: Optional[torch.Tensor] = None,
+                table_out: Optional[torch.Tensor] = None, stream=None):
+    """Last-write refinement + transition tables + greedy walk (bd_refine_tail)."""
+    _check(lib().bd_refine_tail(
+        C.byref(cfg), C.byref(weights), _ptr(tail_state), _ptr(cand_ids), _ptr(cand_scores),
+        int(B), int(n_masks), int(cand_ids.shape[1]), _ptr(token_out), _ptr(pick_out),
+        _ptr(table_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
 

@@ -275,6 +275,34 @@ void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   w.topk_part_idx = cv.take<int32_t>(rows * slices * kTopK);
 }
 
+// Last-write refinement of B requests, K mask rows, kc candidates per row:
+// n = B (K - 1) kc predecessor pairs.
+struct TailWs {
+  GemmWs g;
+  void *cg;       // [n][Rc] predecessor candidates' codebook rows
+  float *pre2;    // [n][2 Mc] (G_p C_s, A C_s)
+  void *m;        // [2][pad16(n)][Mc] refined message, hi+lo pair
+  float *delta;   // [n][H] W_L m
+  float *table;   // [B][K-1][kc][kc] when the caller wants no copy
+};
+int tail_pairs(int B, int K, int kc) { return B * (K - 1) * kc; }
+void carve_tail(Carve &cv, TailWs &w, const bd_config *c, int B, int K, int kc, int sms) {
+  const int n = tail_pairs(B, K, kc);
+  const int e = elem_bytes(c);
+  const int np = pad16(n > 0 ? n : 1);
+  // GEMM tiles: the gate/value maps (2 Mc rows) over n columns, the write (H rows) over
+  // n columns in 128-column tiles
+  const size_t ntn = static_cast<size_t>((np + 127) / 128);
+  const size_t tiles = std::max(2 * tiles_of(c->msg_width, 128) * ((n + 255) / 256 + 1),
+                                tiles_of(c->hidden, 128) * ntn);
+  carve_gemm(cv, w.g, 256, tiles, sms);
+  w.cg = cv.take<char>(static_cast<size_t>(np) * c->code_width * e);
+  w.pre2 = cv.take<float>(static_cast<size_t>(np) * 2 * c->msg_width);
+  w.m = cv.take<char>(static_cast<size_t>(2 * np) * c->msg_width * e);
+  w.delta = cv.take<float>(static_cast<size_t>(np) * c->hidden);
+  w.table = cv.take<float>(static_cast<size_t>(B) * (K - 1) * kc * kc);
+}
+
 GemmScratch scratch_of(const GemmWs &g) {
   return GemmScratch{g.partials, g.partial_floats, g.counters, g.n_counters};
 }
@@ -326,6 +354,12 @@ size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int ma
     HeadWs hw;
     carve_head(ch, hw, cfg, B * max_masks, sms);
     need = std::max(need, ch.off);
+    if (cfg->code_width > 0 && max_masks >= 2) {
+      Carve ct;
+      TailWs tw;
+      carve_tail(ct, tw, cfg, B, max_masks, BD_TOPK_MAX, sms);
+      need = std::max(need, ct.off);
+    }
   }
   Carve cm;
   MatWs mw;
@@ -445,8 +479,8 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
 
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B, int n_masks,
-                         float *head_in, float *hidden_out, float *layers_out, void *workspace,
-                         size_t workspace_bytes, void *stream_) {
+                         float *head_in, float *hidden_out, float *layers_out, float *tail_state,
+                         void *workspace, size_t workspace_bytes, void *stream_) {
   std::string e = check_config(cfg);
   if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
   if (B < 1 || B > kMaxB) return fail(BD_ERR_INVALID_ARG, "B must be in 1..8");
@@ -455,6 +489,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   if ((e = check_kv(cfg, kv, B)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
   if (!anchor_ids || !frontier) return fail(BD_ERR_INVALID_ARG, "anchor_ids/frontier NULL");
   if (!head_in || !aligned16(head_in)) return fail(BD_ERR_INVALID_ARG, "head_in NULL or misaligned");
+  if (tail_state && cfg->code_width == 0)
+    return fail(BD_ERR_INVALID_ARG, "tail_state needs the injection bridge (code_width > 0)");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   const int W = n_masks + 1, T = B * W, TP = pad16(T);
@@ -616,6 +652,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         BD_TRY(launch_gemm(p, sc, s));
       }
       BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, lo(Mc), s));
+      if (tail_state && l == cfg->n_layers - 1)  // the state the last-write refinement redoes
+        BD_TRY(launch_tail_export(rw.x, rw.r, rw.pre, T, H, Mc, tail_state, s));
       {
         GemmPlan p = make_plan(cfg, rw.m, T, Mc);
         p.split = split;
@@ -703,6 +741,69 @@ bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float
   BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
   BD_TRY(launch_topk_reduce(hw.topk_val, hw.topk_idx, static_cast<int>(tiles_of(cfg->vocab, 128)),
                             rows, k, hw.topk_part_val, hw.topk_part_idx, token_out, score_out, s));
+  return BD_OK;
+}
+
+bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float *tail_state,
+                         const int32_t *cand_ids, const float *cand_scores, int B, int n_masks, int kc,
+                         int32_t *token_out, int32_t *pick_out, float *table_out, void *workspace,
+                         size_t workspace_bytes, void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if (cfg->code_width == 0) return fail(BD_ERR_INVALID_ARG, "the refinement needs the injection bridge");
+  if (B < 1 || B > kMaxB) return fail(BD_ERR_INVALID_ARG, "B must be in 1..8");
+  if (n_masks < 2 || n_masks > kMaxMasks) return fail(BD_ERR_INVALID_ARG, "n_masks must be in 2..15");
+  if (kc < 1 || kc > BD_TOPK_MAX || kc > cfg->vocab) return fail(BD_ERR_INVALID_ARG, "kc must be in 1..16");
+  if ((e = check_weights(cfg, w)).empty() == false) return fail(BD_ERR_INVALID_ARG, e);
+  if (!tail_state || !cand_ids || !cand_scores || !token_out)
+    return fail(BD_ERR_INVALID_ARG, "tail_state, cand_ids, cand_scores and token_out are required");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  const int K = n_masks, W = K + 1, T = B * W, H = cfg->hidden;
+  const int Rc = cfg->code_width, Mc = cfg->msg_width, dt = cfg->dtype;
+  const int n = tail_pairs(B, K, kc);
+  Carve cv;
+  cv.base = static_cast<char *>(workspace);
+  TailWs tw;
+  carve_tail(cv, tw, cfg, B, K, kc, num_sms());
+  if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the refinement");
+  const float *u = tail_state;
+  const float *r = tail_state + static_cast<size_t>(T) * H;
+  const float *gc = r + T;
+  const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
+  const PackedLayout PL = packed_layout(cfg);
+  float *table = table_out ? table_out : tw.table;
+
+  BD_TRY(launch_zero(counters_of(tw.g), s));
+  BD_TRY(launch_tail_gather(dt, w->codebook, cfg->vocab, Rc, cand_ids, K, kc, n, tw.cg, s));
+  {  // G_p C_s and A C_s for every predecessor candidate (codebook rows are exact inputs)
+    GemmPlan p = make_plan(cfg, tw.cg, n, Rc);
+    add_w(p, w->g_pred, Mc, pk, PL.g_pred);
+    add_w(p, w->a_val, Mc, pk, PL.a_val);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = tw.pre2;
+    p.args.ld_out = 2 * Mc;
+    p.args.seg[0].out_col = 0;
+    p.args.seg[1].out_col = Mc;
+    BD_TRY(launch_gemm(p, scratch_of(tw.g), s));
+  }
+  const bool split = dt == BD_BF16;
+  const size_t lo_m = split ? static_cast<size_t>(pad16(n)) * Mc : 0;
+  BD_TRY(launch_tail_message(dt, tw.pre2, gc, w->gate_bias, K, W, kc, Mc,
+                             std::sqrt(static_cast<float>(Rc)), n, tw.m, lo_m, s));
+  {  // delta = W_L m, the refined write before its RMS scale
+    GemmPlan p = make_plan(cfg, tw.m, n, Mc);
+    p.split = split;
+    add_w(p, w->layer[cfg->n_layers - 1].w_write, H, pk, PL.w_write[cfg->n_layers - 1]);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = tw.delta;
+    p.args.ld_out = H;
+    BD_TRY(launch_gemm(p, scratch_of(tw.g), s));
+  }
+  BD_TRY(launch_tail_scores(dt, u, r, tw.delta, w->embed_head, w->final_norm, cand_ids, B, K, W, kc, H,
+                            cfg->vocab, cfg->eps, table, s));
+  BD_TRY(launch_tail_walk(table, cand_scores, cand_ids, B, K, kc, token_out, pick_out, s));
   return BD_OK;
 }
 

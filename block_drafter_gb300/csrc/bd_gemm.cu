@@ -951,13 +951,13 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   a.K = plan.K;
   a.n_tokens = plan.n_tokens;
   const int n_pad = (plan.n_tokens + 15) / 16 * 16;
-  if (plan.split) {
-    if (plan.dtype != 0 || n_pad > 128) return "split activations need bf16 and <= 128 tokens";
+  if (plan.split) {  // n-tiles of up to 128 tokens, each with its hi and lo rows
+    if (plan.dtype != 0) return "split activations need bf16";
     a.split = 1;
-    a.ln = n_pad;
+    a.ln = n_pad <= 128 ? n_pad : 128;
     a.lo_row = n_pad;
-    a.block_n = 2 * n_pad;
-    a.n_tiles_n = 1;
+    a.block_n = 2 * a.ln;
+    a.n_tiles_n = (n_pad + a.ln - 1) / a.ln;
   } else {
     a.split = 0;
     a.block_n = gemm_block_n(plan.n_tokens);

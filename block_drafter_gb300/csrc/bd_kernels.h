@@ -113,6 +113,21 @@ int topk_slices(int m_tiles);
 std::string launch_topk_reduce(const float *val, const int32_t *idx, int m_tiles, int rows, int k,
                                float *part_val, int32_t *part_idx, int32_t *tok_out,
                                float *score_out, cudaStream_t s);
+// Last-write refinement: state export [T][H] u | [T] r | [T][Mc] G c (from pre [T][3 Mc]),
+// the predecessor candidates' codebook rows, the refined message (hi+lo pair), the
+// refined scores [B][K-1][kc][kc] and the greedy walk.
+std::string launch_tail_export(const float *x, const float *r, const float *pre, int T, int H,
+                               int Mc, float *out, cudaStream_t s);
+std::string launch_tail_gather(int dtype, const void *codebook, int V, int Rc, const int32_t *cand,
+                               int K, int kc, int n_pairs, void *out, cudaStream_t s);
+std::string launch_tail_message(int dtype, const float *pre2, const float *gc, const void *bias, int K,
+                                int W, int kc, int Mc, float scale, int n_pairs, void *m_out,
+                                size_t lo_off, cudaStream_t s);
+std::string launch_tail_scores(int dtype, const float *u, const float *r, const float *delta,
+                               const void *embed, const void *gain, const int32_t *cand, int B, int K,
+                               int W, int kc, int H, int V, float eps, float *table, cudaStream_t s);
+std::string launch_tail_walk(const float *table, const float *cand_score, const int32_t *cand, int B,
+                             int K, int kc, int32_t *token_out, int32_t *pick_out, cudaStream_t s);
 // Copy rows [n, H] fp32 (used for the optional per-layer residual output).
 std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
 

@@ -508,6 +508,212 @@ __global__ void copy_f32_kernel(const float *src, float *dst, size_t n) {
     dst[t] = src[t];
 }
 
+// ------------------------------------------------------------------ last-write refinement
+// "DSpine 完全拆解", section on predecessor-conditioned decoding and the transition cache.
+
+// The last layer's state the refinement redoes its injection from: the pre-injection
+// residual u [T][H], the receiver RMS r [T] and the receiver gate term G c [T][Mc]
+// (columns 0..Mc of the gate-map GEMM output pre [T][3 Mc]).
+__global__ void tail_export_kernel(const float *x, const float *r, const float *pre, int T, int H,
+                                   int Mc, float *out) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t nx = static_cast<size_t>(T) * H, ng = static_cast<size_t>(T) * Mc;
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < nx + T + ng;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (t < nx) {
+      out[t] = x[t];
+    } else if (t < nx + T) {
+      out[t] = r[t - nx];
+    } else {
+      const size_t g = t - nx - T;
+      out[t] = pre[(g / Mc) * 3 * Mc + g % Mc];
+    }
+  }
+}
+
+// Pair n = ((b * (K - 1) + (i - 2)) * kc + p) takes predecessor candidate p of block row
+// i - 1: its codebook row, for the predecessor-gate and value maps.
+template <typename T>
+__global__ void tail_gather_kernel(const T *codebook, int V, int Rc, const int32_t *cand, int K,
+                                   int kc, int n_pairs, T *out) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.x;
+  if (n >= n_pairs) return;
+  const int p = n % kc, bi = n / kc, b = bi / (K - 1), i = bi % (K - 1) + 2;
+  int s = cand[(static_cast<size_t>(b) * K + (i - 2)) * kc + p];
+  if (s < 0 || s >= V) {
+    if (threadIdx.x == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+    s = 0;
+  }
+  const T *src = codebook + static_cast<size_t>(s) * Rc;
+  for (int k = threadIdx.x; k < Rc; k += blockDim.x) out[static_cast<size_t>(n) * Rc + k] = src[k];
+}
+
+// m = sigmoid(G c_i + sqrt(Rc) G_p C_s + b) * (sqrt(Rc) A C_s) for pair n (row i of request
+// b); pre2 [n][2 Mc] = [G_p C_s, A C_s]; written as the bf16 hi+lo pair of the write GEMM.
+template <typename T>
+__global__ void tail_message_kernel(const float *pre2, const float *gc, const T *bias, int K, int W,
+                                    int kc, int Mc, float scale, T *m_out, size_t lo_off) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.x;
+  const int bi = n / kc, b = bi / (K - 1), i = bi % (K - 1) + 2;
+  const float *g_recv = gc + (static_cast<size_t>(b) * W + i) * Mc;
+  const float *pp = pre2 + static_cast<size_t>(n) * 2 * Mc;
+  for (int f = threadIdx.x; f < Mc; f += blockDim.x) {
+    const float z = g_recv[f] + scale * pp[f] + (bias ? to_f<T>(bias[f]) : 0.f);
+    const float g = 1.f / (1.f + expf(-z));
+    store_split(m_out + static_cast<size_t>(n) * Mc, f, lo_off, g * scale * pp[Mc + f]);
+  }
+}
+
+// Eight consecutive elements as fp32 (one 16-byte load for bf16, two for fp32).
+template <typename T> __device__ __forceinline__ void load8(const T *p, float (&o)[8]);
+template <> __device__ __forceinline__ void load8<float>(const float *p, float (&o)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&o)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    o[2 * q] = f.x;
+    o[2 * q + 1] = f.y;
+  }
+}
+
+// One CTA per predecessor pair n (request b, block row i >= 2, candidate p of row i-1):
+// the refined state x' = u_i + r_i delta_n goes through the final norm and is scored
+// against the head rows of row i's kc candidates.  Two passes over H in 8-element vectors
+// (the mean square, then the dot products); the pairs of one row share the candidate head
+// rows through L2.  Requires H % 8 == 0.
+template <typename T>
+__global__ void __launch_bounds__(256) tail_scores_kernel(const float *u, const float *r,
+                                                          const float *delta, const T *embed,
+                                                          const T *gain, const int32_t *cand,
+                                                          int K, int W, int kc, int H, int V,
+                                                          float eps, float *table) {
+  __shared__ float part[8][kTopK + 1];
+  __shared__ int cid[kTopK];
+  __shared__ float s_inv;
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.x, bi = n / kc, b = bi / (K - 1), i = bi % (K - 1) + 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t t = static_cast<size_t>(b) * W + i;  // the block row
+  const float *ut = u + t * H;
+  const float *dn = delta + static_cast<size_t>(n) * H;
+  const float rt = r[t];
+  if (threadIdx.x < kc) {
+    int c = cand[(static_cast<size_t>(b) * K + (i - 1)) * kc + threadIdx.x];
+    if (c < 0 || c >= V) {
+      atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      c = 0;
+    }
+    cid[threadIdx.x] = c;
+  }
+  float ss = 0.f;
+  for (int d = threadIdx.x * 8; d < H; d += blockDim.x * 8) {
+    float uu[8], dd[8];
+    load8<float>(ut + d, uu);
+    load8<float>(dn + d, dd);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float x = uu[q] + rt * dd[q];
+      ss += x * x;
+    }
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) part[warp][0] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += part[w][0];
+    s_inv = rsqrtf(tot / static_cast<float>(H) + eps);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  float acc[kTopK];
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) acc[j] = 0.f;
+  for (int d = threadIdx.x * 8; d < H; d += blockDim.x * 8) {
+    float uu[8], dd[8], gg[8], h[8];
+    load8<float>(ut + d, uu);
+    load8<float>(dn + d, dd);
+    load8<T>(gain + d, gg);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = gg[q] * (uu[q] + rt * dd[q]) * inv;
+#pragma unroll
+    for (int j = 0; j < kTopK; ++j) {
+      if (j < kc) {
+        float e[8];
+        load8<T>(embed + static_cast<size_t>(cid[j]) * H + d, e);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[j] += h[q] * e[q];
+      }
+    }
+  }
+  __syncthreads();  // part[] is reused
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const float v = warp_sum(acc[j]);
+    if (lane == 0) part[warp][j] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < kc) {
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += part[w][threadIdx.x];
+    table[static_cast<size_t>(n) * kc + threadIdx.x] = tot;
+  }
+}
+
+// Greedy walk of request b (one warp, the request's tables staged in shared memory):
+// row 1 takes the lowest-rank best of its own scores, row i >= 2 the lowest-rank best of
+// the table row of row i - 1's choice.
+__global__ void __launch_bounds__(32) tail_walk_kernel(const float *table, const float *cand_score,
+                                                       const int32_t *cand, int K, int kc,
+                                                       int32_t *token_out, int32_t *pick_out) {
+  extern __shared__ float tb[];  // [(K - 1) * kc * kc]
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const size_t tsz = static_cast<size_t>(K - 1) * kc * kc;
+  for (size_t q = lane; q < tsz; q += 32) tb[q] = table[b * tsz + q];
+  __syncwarp();
+  auto best = [&](float v) {  // lowest lane among the maxima of lanes < kc
+    float bv = lane < kc ? v : -INFINITY;
+    int bl = lane < kc ? lane : 0x7fffffff;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int ol = __shfl_xor_sync(0xffffffffu, bl, off);
+      if (ov > bv || (ov == bv && ol < bl)) {
+        bv = ov;
+        bl = ol;
+      }
+    }
+    return bl;
+  };
+  int j = best(lane < kc ? cand_score[static_cast<size_t>(b) * K * kc + lane] : 0.f);
+  if (lane == 0) {
+    token_out[static_cast<size_t>(b) * K] = cand[static_cast<size_t>(b) * K * kc + j];
+    if (pick_out) pick_out[static_cast<size_t>(b) * K] = j;
+  }
+  for (int i = 2; i <= K; ++i) {
+    const float v = lane < kc ? tb[(static_cast<size_t>(i - 2) * kc + j) * kc + lane] : 0.f;
+    j = best(v);
+    if (lane == 0) {
+      const size_t row = static_cast<size_t>(b) * K + (i - 1);
+      token_out[row] = cand[row * kc + j];
+      if (pick_out) pick_out[row] = j;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 static std::string err(const char *what, cudaError_t e) {
   return e == cudaSuccess ? std::string() : std::string(what) + ": " + cudaGetErrorString(e);
@@ -632,6 +838,71 @@ std::string launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t
   const size_t blocks = (n + 255) / 256;
   return err("copy", launch_pdl(copy_f32_kernel, dim3(blocks < 1024 ? blocks : 1024), dim3(256), 0,
                                 s, src, dst, n));
+}
+
+}  // namespace bd
+
+namespace bd {
+
+std::string launch_tail_export(const float *x, const float *r, const float *pre, int T, int H,
+                               int Mc, float *out, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(T) * (H + 1 + Mc);
+  const size_t blocks = (n + 255) / 256;
+  return err("tail export", launch_pdl(tail_export_kernel, dim3(blocks < 1024 ? blocks : 1024),
+                                       dim3(256), 0, s, x, r, pre, T, H, Mc, out));
+}
+
+std::string launch_tail_gather(int dtype, const void *codebook, int V, int Rc, const int32_t *cand,
+                               int K, int kc, int n_pairs, void *out, cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(tail_gather_kernel<__nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s,
+                   static_cast<const __nv_bfloat16 *>(codebook), V, Rc, cand, K, kc, n_pairs,
+                   static_cast<__nv_bfloat16 *>(out));
+  else
+    e = launch_pdl(tail_gather_kernel<float>, dim3(n_pairs), dim3(128), 0, s,
+                   static_cast<const float *>(codebook), V, Rc, cand, K, kc, n_pairs,
+                   static_cast<float *>(out));
+  return err("tail gather", e);
+}
+
+std::string launch_tail_message(int dtype, const float *pre2, const float *gc, const void *bias, int K,
+                                int W, int kc, int Mc, float scale, int n_pairs, void *m_out,
+                                size_t lo_off, cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(tail_message_kernel<__nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s, pre2, gc,
+                   static_cast<const __nv_bfloat16 *>(bias), K, W, kc, Mc, scale,
+                   static_cast<__nv_bfloat16 *>(m_out), lo_off);
+  else
+    e = launch_pdl(tail_message_kernel<float>, dim3(n_pairs), dim3(128), 0, s, pre2, gc,
+                   static_cast<const float *>(bias), K, W, kc, Mc, scale,
+                   static_cast<float *>(m_out), lo_off);
+  return err("tail message", e);
+}
+
+std::string launch_tail_scores(int dtype, const float *u, const float *r, const float *delta,
+                               const void *embed, const void *gain, const int32_t *cand, int B, int K,
+                               int W, int kc, int H, int V, float eps, float *table, cudaStream_t s) {
+  cudaError_t e;
+  const dim3 grid(B * (K - 1) * kc);  // one CTA per predecessor pair
+  if (H % 8 != 0) return "tail scores: hidden size must be a multiple of 8";
+  if (dtype == 0)
+    e = launch_pdl(tail_scores_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, u, r, delta,
+                   static_cast<const __nv_bfloat16 *>(embed),
+                   static_cast<const __nv_bfloat16 *>(gain), cand, K, W, kc, H, V, eps, table);
+  else
+    e = launch_pdl(tail_scores_kernel<float>, grid, dim3(256), 0, s, u, r, delta,
+                   static_cast<const float *>(embed), static_cast<const float *>(gain), cand, K, W,
+                   kc, H, V, eps, table);
+  return err("tail scores", e);
+}
+
+std::string launch_tail_walk(const float *table, const float *cand_score, const int32_t *cand, int B,
+                             int K, int kc, int32_t *token_out, int32_t *pick_out, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(K - 1) * kc * kc * sizeof(float);
+  return err("tail walk", launch_pdl(tail_walk_kernel, dim3(B), dim3(32), smem, s, table, cand_score,
+                                     cand, K, kc, token_out, pick_out));
 }
 
 }  // namespace bd

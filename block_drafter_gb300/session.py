@@ -57,9 +57,21 @@ class DraftSession:
     # S3 .. S9 + final norm
     def round(self, anchor_ids: torch.Tensor, frontier: torch.Tensor, n_masks: int,
               head_in: torch.Tensor, hidden_out: Optional[torch.Tensor] = None,
-              layers_out: Optional[torch.Tensor] = None, stream=None):
+              layers_out: Optional[torch.Tensor] = None, stream=None,
+              tail_state: Optional[torch.Tensor] = None):
         B.draft_round(self.cfg, self.wstruct, self.kv, anchor_ids, frontier, n_masks, head_in,
-                      self.workspace, hidden_out, layers_out, stream)
+                      self.workspace, hidden_out, layers_out, stream, tail_state)
+
+    def alloc_tail_state(self, Bn: int, n_masks: int) -> torch.Tensor:
+        return torch.empty(B.tail_state_floats(self.cfg, Bn, n_masks), dtype=torch.float32,
+                           device=self.device)
+
+    def refine_tail(self, tail_state: torch.Tensor, cand_ids: torch.Tensor,
+                    cand_scores: torch.Tensor, Bn: int, n_masks: int, token_out: torch.Tensor,
+                    pick_out: Optional[torch.Tensor] = None,
+                    table_out: Optional[torch.Tensor] = None, stream=None):
+        B.refine_tail(self.cfg, self.wstruct, tail_state, cand_ids, cand_scores, Bn, n_masks,
+                      token_out, self.workspace, pick_out, table_out, stream)
 
     # S10
     def head(self, hidden: torch.Tensor, token_out: torch.Tensor,

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 3
+#define BD_ABI_VERSION 4
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -194,11 +194,16 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
  *   hidden_out  dev fp32 [B*W, H] OUT final-normed rows of every block row, or NULL
  *   layers_out  dev fp32 [L, B*W, H] OUT post-injection residual after each layer, or
  *               NULL (a debugging/parity output; it adds device-to-device copies)
+ *   tail_state  dev fp32 OUT, or NULL: the last layer's state the last-write refinement
+ *               redoes its injection from (input of bd_refine_tail), T = B*W rows:
+ *               [T*H] pre-injection residual u, then [T] its RMS r, then [T*Mc] the
+ *               receiver gate term G c.  Requires code_width > 0.
  */
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B,
                          int n_masks, float *head_in, float *hidden_out, float *layers_out,
-                         void *workspace, size_t workspace_bytes, void *stream);
+                         float *tail_state, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /*
  * Tied LM head with per-row argmax (S10).  [DFlash-notes], proposal head:
@@ -236,6 +241,34 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
 bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
                           int k, int32_t *token_out, float *score_out, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * Last-write refinement, transition tables and greedy walk (the DSpine tail).
+ * "DSpine for Qwen3.8-27B: Causal Features Through Depth", section "The last write is
+ * refined using discrete candidates", and "DSpine 完全拆解", section on predecessor-
+ * conditioned decoding and the transition cache.  For block row i >= 2 of request b and
+ * each candidate s of row i-1 the last layer's injection into row i is redone from
+ * tail_state with the predecessor code replaced by sqrt(Rc) * codebook[s]:
+ *   g = sigmoid(G c_i + G_p c_s + b),  m = g * (A c_s),  x' = u_i + r_i W_L m,
+ *   h' = plain_rmsnorm(x', final_norm),  table[b][i-2][p][j] = embed_head[cand_j] . h'
+ * over row i's candidates j.  Row 1 keeps its own scores (its predecessor is the anchor,
+ * which the round already used).  The greedy walk takes row 1's lowest-rank best
+ * candidate, then for i = 2..K the lowest-rank best of the table row of row i-1's choice.
+ *
+ *   tail_state   dev fp32, from bd_draft_round of the same B and n_masks
+ *   cand_ids     dev int32 [B*K, kc]  candidates of the mask rows (e.g. bd_lm_head_topk)
+ *   cand_scores  dev fp32 [B*K, kc]   their scores (row 1 of each request is read)
+ *   B 1..8;  n_masks K 2..15;  kc 1..BD_TOPK_MAX
+ *   token_out    dev int32 [B*K]  OUT the walk's tokens
+ *   pick_out     dev int32 [B*K]  OUT the chosen candidate indices, or NULL
+ *   table_out    dev fp32 [B, K-1, kc, kc]  OUT the transition tables, or NULL
+ * Errors: BD_ERR_INVALID_ARG (ranges, NULL inputs, no bridge); out-of-range candidate
+ * ids are reported by bd_sync_status.  Workspace as sized by bd_workspace_bytes.
+ */
+bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float *tail_state,
+                         const int32_t *cand_ids, const float *cand_scores, int B, int n_masks,
+                         int kc, int32_t *token_out, int32_t *pick_out, float *table_out,
+                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * bd_lm_head_argmax without a workspace, for callers that cannot allocate device

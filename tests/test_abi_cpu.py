@@ -97,25 +97,25 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     ws = 0x100000
     # B out of range
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 9, 7, 0x10000,
-                          None, None, ws, 1 << 30, None)
+                          None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"B must be" in L.bd_last_error()
     # K out of range
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 16, 0x10000,
-                          None, None, ws, 1 << 30, None)
+                          None, None, None, ws, 1 << 30, None)
     assert st == -1
     # misaligned weight
     w.layer[1].wq = 0x10008
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, ws, 1 << 30, None)
+                          None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"layer 1" in L.bd_last_error()
     w.layer[1].wq = 0x10000
     # more requests than ring rows
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 2, 7, 0x10000,
-                          None, None, ws, 1 << 30, None)
+                          None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"b_max" in L.bd_last_error()
     # misaligned workspace
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, ws + 16, 1 << 30, None)
+                          None, None, None, ws + 16, 1 << 30, None)
     assert st == -5
     # head: rows out of range
     st = L.bd_lm_head_argmax(C.byref(c), C.byref(w), 0x10000, 121, 0x10000, None, ws, 1 << 30, None)
@@ -129,6 +129,17 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     st = L.bd_lm_head_topk(C.byref(c), C.byref(w), 0x10000, 4, 16, 0x10000, None, ws + 16, 1 << 30,
                            None)
     assert st == -5
+    # refinement: K < 2, kc out of range, missing inputs
+    st = L.bd_refine_tail(C.byref(c), C.byref(w), 0x10000, 0x10000, 0x10000, 1, 1, 16, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1 and b"n_masks" in L.bd_last_error()
+    for kc in (0, 17):
+        st = L.bd_refine_tail(C.byref(c), C.byref(w), 0x10000, 0x10000, 0x10000, 1, 7, kc, 0x10000,
+                              None, None, ws, 1 << 30, None)
+        assert st == -1 and b"kc" in L.bd_last_error()
+    st = L.bd_refine_tail(C.byref(c), C.byref(w), None, 0x10000, 0x10000, 1, 7, 16, 0x10000,
+                          None, None, ws, 1 << 30, None)
+    assert st == -1
     # materialise: no rows
     st = L.bd_ctx_kv_materialize(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 0x10000,
                                  0x10000, 0, ws, 1 << 30, None)
@@ -136,7 +147,7 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     # bridge on, bridge weights missing
     w.g_pred = None
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, ws, 1 << 30, None)
+                          None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"bridge" in L.bd_last_error()
 
 
@@ -150,7 +161,7 @@ def test_unsupported_geometry_is_an_error_not_a_fallback(B):
         kv.k[l] = kv.v[l] = 0x10000
     kv.b_max = 1
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 15, 0x10000,
-                          None, None, 0x100000, 1 << 34, None)
+                          None, None, None, 0x100000, 1 << 34, None)
     assert st == -2
 
 

@@ -1,0 +1,114 @@
+"""GPU-vs-oracle parity of the last-write refinement (bd_refine_tail) through the C ABI.
+
+The round runs on the GPU with its tail state exported, the top-16 head gives the
+candidate sets, bd_refine_tail builds the transition tables and walks them.  The oracle
+refines with the same candidate sets (their own parity is tested in test_gpu_topk.py)
+from its own fp64 round.  Tables: max |gpu - ref| / max |ref| <= 2e-3 in bf16 (hi+lo
+activations) and 1e-2 in the fp32 configuration, whose products run on tf32 tensor
+cores (10-bit mantissa) in the round and in both refinement GEMMs.  The walk is
+compared step by step while the oracle's choice leads its runner-up by more than GAP;
+after a closer decision the two walks may legitimately part, so the comparison of that
+request stops there.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bdsynth
+import harness as Hn
+from oracle import dspine_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TABLE_TOL = {"bf16": 2e-3, "f32": 1e-2}
+GAP = 1e-2
+
+SMALL_BF16 = bdsynth.Workload(
+    name="small_bf16", hidden=512, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
+    ffn=1024, vocab=4000, n_target_layers=3, windows=(64, 0), code_width=128, msg_width=64,
+    batch=3, n_masks=15, dtype="bf16", ctx_min=40, ctx_max=300, full_capacity=320)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_drafter_gb300 import builder
+    builder.build()
+
+
+def _gpu_tail(case, kc=16):
+    g = case.geo
+    Bn, K = g.batch, g.n_masks
+    dev = "cuda"
+    anchors = torch.tensor(case.anchors, dtype=torch.int32, device=dev)
+    front = torch.tensor(case.frontiers, dtype=torch.int64, device=dev)
+    head_in, _, _, _ = case.sess.alloc_outputs(Bn, K)
+    tail = case.sess.alloc_tail_state(Bn, K)
+    case.sess.round(anchors, front, K, head_in, tail_state=tail)
+    cand = torch.empty(Bn * K, kc, dtype=torch.int32, device=dev)
+    cs = torch.empty(Bn * K, kc, dtype=torch.float32, device=dev)
+    case.sess.head_topk(head_in, kc, cand, cs)
+    tok = torch.empty(Bn * K, dtype=torch.int32, device=dev)
+    pick = torch.empty(Bn * K, dtype=torch.int32, device=dev)
+    table = torch.empty(Bn, K - 1, kc, kc, dtype=torch.float32, device=dev)
+    for _ in range(2):  # twice: the tile counters must reset themselves
+        case.sess.refine_tail(tail, cand, cs, Bn, K, tok, pick, table)
+    from block_drafter_gb300 import binding
+    binding.sync_status()
+    return {"cand": cand.cpu().numpy().reshape(Bn, K, kc), "tok": tok.cpu().numpy().reshape(Bn, K),
+            "pick": pick.cpu().numpy().reshape(Bn, K), "table": table.cpu().numpy()}
+
+
+def _compare(case, gpu):
+    g = case.geo
+    ref = case.run_oracle(with_head=False)
+    wnp = Hn.weights_to_np(case.w_host)
+    rep = {"table_err": 0.0, "steps_compared": 0}
+    for b in range(g.batch):
+        cand = gpu["cand"][b]
+        assert (gpu["tok"][b] == cand[np.arange(g.n_masks), gpu["pick"][b]]).all()
+        s1, tables, picks, tokens = O.refine_tail(g, wnp, ref["tail"][b], case.anchors[b], cand)
+        err = Hn.rel_err(gpu["table"][b], tables)
+        rep["table_err"] = max(rep["table_err"], err)
+        assert err <= TABLE_TOL[g.dtype], (b, err)
+        # the walk, step by step, while the oracle's decision is clear
+        rows = [s1] + [tables[i - 2][picks[i - 2]] for i in range(2, g.n_masks + 1)]
+        for i, row in enumerate(rows):
+            srt = np.sort(row)
+            if srt[-1] - srt[-2] <= GAP:
+                break
+            assert gpu["pick"][b, i] == picks[i], (b, i, gpu["pick"][b], picks)
+            rep["steps_compared"] += 1
+    return rep
+
+
+@pytest.mark.parametrize("geo,seed", [(SMALL_BF16, 0), (SMALL_BF16, 3), (bdsynth.TINY, 1)])
+def test_refine_tail_matches_oracle(geo, seed):
+    case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
+    case.fill_rings()
+    gpu = _gpu_tail(case)
+    rep = _compare(case, gpu)
+    print(geo.name, seed, rep)
+    assert rep["steps_compared"] >= geo.batch  # not vacuous
+
+
+def test_refine_tail_gate_bias_matches_oracle():
+    case = Hn.Case(SMALL_BF16, seed=4, gate_bias=True, max_ctx_rows=128)
+    case.fill_rings()
+    rep = _compare(case, _gpu_tail(case))
+    assert rep["steps_compared"] >= 1
+
+
+def test_refine_tail_fewer_candidates():
+    case = Hn.Case(SMALL_BF16, seed=5, max_ctx_rows=128)
+    case.fill_rings()
+    rep = _compare(case, _gpu_tail(case, kc=5))
+    assert rep["steps_compared"] >= 1
+
+
+def test_zero_write_tables_are_independent_of_the_predecessor():
+    w = bdsynth.make_weights(SMALL_BF16, 6, zero_write=True)
+    case = Hn.Case(SMALL_BF16, seed=6, weights=w, max_ctx_rows=128)
+    case.fill_rings()
+    gpu = _gpu_tail(case)
+    t = gpu["table"]
+    assert np.array_equal(t, np.broadcast_to(t[:, :, :1, :], t.shape))

@@ -147,7 +147,7 @@ int att_splits(const bd_config *c, int l, int B, int W, int sms) {
   const int cap = c->ring_capacity[l];
   const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
   const int max_keys = ctx + W;
-  const int max_splits = (max_keys + 127) / 128;  // at least two 64-key blocks per split
+  const int max_splits = (max_keys + 63) / 64;  // at least one 64-key block per split
   // two attention CTAs fit per SM: fill 2 * SMs slots in a single wave
   int s = (2 * sms) / (B * c->n_kv_heads);
   if (s < 1) s = 1;
@@ -177,6 +177,7 @@ size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + ti
 
 struct RoundWs {
   GemmWs g;
+  unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
   float *x, *z, *pre, *r, *part_o, *qkv_raw;
   float2 *rope, *part_ml;
   void *xn, *q, *kblk, *vblk, *att, *hmid, *c, *m;
@@ -201,6 +202,7 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sm
   const int e = elem_bytes(c);
   const int H = c->hidden, QD = c->n_q_heads * c->head_dim, KD = c->n_kv_heads * c->head_dim;
   carve_gemm(cv, w.g, 2 * TP, round_max_tiles(c, T), sms);
+  w.att_cnt = cv.take<unsigned>(2 * static_cast<size_t>(B) * c->n_kv_heads);
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
   w.qkv_raw = cv.take<float>(static_cast<size_t>(T) * (QD + 2 * KD));
   w.xn = cv.take<char>(static_cast<size_t>(2 * TP) * H * e);
@@ -519,8 +521,12 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   auto lo = [&](int K) -> size_t { return split ? static_cast<size_t>(TP) * K : 0; };
 
   // S3: block input rows and the RoPE table of positions F_b + i
+  // the first kernel clears the GEMM tile counters and the attention split counters
+  // (carved back to back)
+  const ZeroSpan zero{rw.g.counters, static_cast<size_t>(rw.att_cnt - rw.g.counters) +
+                                         2 * static_cast<size_t>(B) * cfg->n_kv_heads};
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
-                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, counters_of(rw.g), s));
+                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, zero, s));
   for (int l = 0; l < cfg->n_layers; ++l) {
     const bd_layer_weights &L = w->layer[l];
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE
@@ -571,6 +577,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.frontier = frontier;
       a.part_o = rw.part_o;
       a.part_ml = rw.part_ml;
+      a.counters = rw.att_cnt;
       a.B = B;
       a.W = W;
       a.n_q_heads = cfg->n_q_heads;

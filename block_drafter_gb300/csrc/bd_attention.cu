@@ -143,6 +143,70 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
   }
 }
 
+// Merge the splits of query row rr of (request b, KV head h):
+//   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// One warp; lanes own D/32 consecutive output dims and the split weights are computed by
+// lanes and broadcast, so the per-split loads are independent of each other.  The
+// partials were written by other CTAs of the launch: read through L2.
+template <typename T, int D>
+__device__ __forceinline__ void combine_row(const AttArgs &a, int b, int h, int rr, int lane) {
+  const int G = a.n_q_heads / a.n_kv_heads;
+  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
+  constexpr int PER = D / 32;
+  const float *po = a.part_o + bh * a.n_splits * kAttRows * D;
+  const float2 *pml = a.part_ml + bh * a.n_splits * kAttRows;
+  float M = -INFINITY;
+  for (int s = lane; s < a.n_splits; s += 32) {
+    const float2 ml = __ldcg(pml + s * kAttRows + rr);
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  M = warp_max(M);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
+    const int s = s0 + lane;
+    float wgt = 0.f;
+    if (s < a.n_splits) {
+      const float2 ml = __ldcg(pml + s * kAttRows + rr);
+      if (ml.y > 0.f) {
+        wgt = exp2f(ml.x - M);
+        L += wgt * ml.y;
+      }
+    }
+    const int cnt = min(32, a.n_splits - s0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wgt, j);
+      const float *os = po + (static_cast<size_t>(s0 + j) * kAttRows + rr) * D + lane * PER;
+      if (PER == 4) {
+        const float4 o = __ldcg(reinterpret_cast<const float4 *>(os));
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+        acc[2] += wj * o.z;
+        acc[3] += wj * o.w;
+      } else {
+        const float2 o = __ldcg(reinterpret_cast<const float2 *>(os));
+        acc[0] += wj * o.x;
+        acc[1] += wj * o.y;
+      }
+    }
+  }
+  L = warp_sum(L);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int gh = rr / a.W, i = rr % a.W;
+  T *out = static_cast<T *>(a.out) +
+           (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const float y = acc[e] * inv;
+    const T hi = from_f<T>(y);
+    out[e] = hi;
+    if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
+  }
+}
+
 // bf16 tensor-core path.  Q and the softmax probabilities P enter the MMAs as hi+lo bf16
 // pairs (fp32 accumulate), so their rounding does not reach the output; the ring's K/V
 // are exact bf16 data.  The block's own keys/values (produced this round, hi+lo) are
@@ -401,74 +465,38 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
     pml[rowA] = make_float2(m_run[0], l_run[0]);
     pml[rowB] = make_float2(m_run[1], l_run[1]);
   }
-}
 
-// Merge the splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  One warp per
-// query row; lanes own D/32 consecutive output dims and the split weights are computed
-// by lanes and broadcast, so the per-split loads are independent of each other.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) attention_combine_kernel(const __grid_constant__ AttArgs a) {
-  const int bh = blockIdx.x;
-  const int b = bh / a.n_kv_heads, h = bh % a.n_kv_heads;
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const int R = G * a.W;
-  const int rr = blockIdx.y * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
-  if (rr >= R) return;
-  constexpr int PER = D / 32;
-  const float *po = a.part_o + static_cast<size_t>(bh) * a.n_splits * kAttRows * D;
-  const float2 *pml = a.part_ml + static_cast<size_t>(bh) * a.n_splits * kAttRows;
-  float M = -INFINITY;
-  for (int s = lane; s < a.n_splits; s += 32) {
-    const float2 ml = pml[s * kAttRows + rr];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
-  M = warp_max(M);
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
-    const int s = s0 + lane;
-    float wgt = 0.f;
-    if (s < a.n_splits) {
-      const float2 ml = pml[s * kAttRows + rr];
-      if (ml.y > 0.f) {
-        wgt = exp2f(ml.x - M);
-        L += wgt * ml.y;
+  // ---- merge the splits in this launch: every split of (b, h) counts itself once its
+  // partial is stored, waits (bounded) for the others, then merges its share of the rows.
+  // A launch has at most two CTAs per SM and never more than two per SM of the GPU, so all
+  // splits are resident together; each stores its partial before it waits.
+  __shared__ int s_abort;
+  unsigned *arrived = a.counters + bh;
+  unsigned *done = a.counters + static_cast<size_t>(a.B) * a.n_kv_heads + bh;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    s_abort = 0;
+    atomicAdd(arrived, 1u);
+    const unsigned long long t0 = globaltimer();
+    while (ld_acquire(arrived) < static_cast<unsigned>(a.n_splits)) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        atomicOr(&g_error_word, DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
       }
-    }
-    const int cnt = min(32, a.n_splits - s0);
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wgt, j);
-      const float *os = po + (static_cast<size_t>(s0 + j) * kAttRows + rr) * D + lane * PER;
-      if (PER == 4) {
-        const float4 o = *reinterpret_cast<const float4 *>(os);
-        acc[0] += wj * o.x;
-        acc[1] += wj * o.y;
-        acc[2] += wj * o.z;
-        acc[3] += wj * o.w;
-      } else {
-        const float2 o = *reinterpret_cast<const float2 *>(os);
-        acc[0] += wj * o.x;
-        acc[1] += wj * o.y;
-      }
+      __nanosleep(32);
     }
   }
-  L = warp_sum(L);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int gh = rr / a.W, i = rr % a.W;
-  T *out = static_cast<T *>(a.out) +
-           (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const float y = acc[e] * inv;
-    const T hi = from_f<T>(y);
-    out[e] = hi;
-    if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
+  __syncthreads();
+  if (s_abort) return;
+  const int rp = (R + a.n_splits - 1) / a.n_splits;
+  const int r1 = min(R, (split + 1) * rp);
+  for (int rr = split * rp + warp; rr < r1; rr += 4) combine_row<__nv_bfloat16, D>(a, b, h, rr, lane);
+  __syncthreads();
+  if (tid == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
+    *arrived = 0u;  // every split is past its wait: ready for the next launch
+    *done = 0u;
   }
 }
 
@@ -568,7 +596,6 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
     return {};
   }
   const size_t smem = attention_smem_bytes(a.head_dim);
-  const int R = a.n_q_heads / a.n_kv_heads * a.W;
   if (a.head_dim == 128) {
     static bool set = false;
     if (!set) {
@@ -578,9 +605,6 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
     }
     e = launch_pdl(attention_bf16_kernel<128>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128),
                    smem, stream, a);
-    if (e == cudaSuccess)
-      e = launch_pdl(attention_combine_kernel<__nv_bfloat16, 128>, dim3(a.B * a.n_kv_heads, (R + 7) / 8),
-                     dim3(256), 0, stream, a);
   } else {
     static bool set = false;
     if (!set) {
@@ -590,9 +614,6 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
     }
     e = launch_pdl(attention_bf16_kernel<64>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128), smem,
                    stream, a);
-    if (e == cudaSuccess)
-      e = launch_pdl(attention_combine_kernel<__nv_bfloat16, 64>, dim3(a.B * a.n_kv_heads, (R + 7) / 8),
-                     dim3(256), 0, stream, a);
   }
   if (e != cudaSuccess) return std::string("attention launch: ") + cudaGetErrorString(e);
   return {};

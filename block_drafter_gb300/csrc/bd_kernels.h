@@ -19,6 +19,7 @@ struct AttArgs {
   const int64_t *frontier;  // [B]
   float *part_o;        // [B, Hkv, n_splits, 64, D] fp32 unnormalised partial outputs
   float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
+  unsigned *counters;   // [2][B * Hkv] split arrival / done counters (start at 0)
   int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
 };

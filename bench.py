@@ -3,9 +3,12 @@
 
 One step = one pass of the whole hot path for one batch of requests:
   S1+S2  catch-up materialisation of the W pending target-feature rows of every request
-         (the rows the previous round committed) into the context rings,
+         (the rows the previous round committed) into the context rings -- inside the
+         round call: the feature projection first, then each layer's context K/V in the
+         same product as the block's Q/K/V,
   S3..S9 one masked-block draft round (all layers, DSpine injection),
   S10    tied LM head + per-row argmax.
+The same step with the catch-up as a separate materialisation call is timed beside it.
 Default workload: the 27B-geometry DSpine-b16 round at B=1 (window 2048 over a
 4096-token context, W=16); the B=8 round (contexts uniform in [512, 16384]) is timed in
 the same run and reported under "b8".  Inputs are seeded synthetic tensors, resident in
@@ -195,6 +198,12 @@ class State:
         self.sess.materialize(self.feats, self.row_req, self.row_pos, self.front)
 
     def round(self):
+        """The round with this step's pending rows caught up inside the call."""
+        self.sess.round(self.anchors, self.front, self.geo.n_masks, self.head_in,
+                        pending=(self.feats, self.row_req, self.row_pos))
+
+    def round_plain(self):
+        """The round alone (its context already complete)."""
         self.sess.round(self.anchors, self.front, self.geo.n_masks, self.head_in)
 
     def head(self):
@@ -205,15 +214,20 @@ class State:
 
     def round_with_tail(self):
         self.sess.round(self.anchors, self.front, self.geo.n_masks, self.head_in,
-                        tail_state=self.tail)
+                        tail_state=self.tail, pending=(self.feats, self.row_req, self.row_pos))
 
     def refine(self):
         self.sess.refine_tail(self.tail, self.cand, self.cand_score, self.geo.batch,
                               self.geo.n_masks, self.refined)
 
     def step(self):
-        self.materialize()
         self.round()
+        self.head()
+
+    def step_separate(self):
+        """The same step with the catch-up as its own materialisation call."""
+        self.materialize()
+        self.round_plain()
         self.head()
 
     # algorithmic bytes of one step: every weight byte once, the windowed context K/V
@@ -279,31 +293,27 @@ def capture(fn):
 
 
 def time_graphs(st: State, steps: int, warmup: int, world: int):
-    """Replays [materialise | round | head] graphs back to back; events between them give
+    """Replays [round with catch-up | head] graphs back to back; events between them give
     the per-call times, the outer pair the step time."""
-    g_mat, g_round, g_head = capture(st.materialize), capture(st.round), capture(st.head)
+    g_round, g_head = capture(st.round), capture(st.head)
     for _ in range(warmup):
-        g_mat.replay()
         g_round.replay()
         g_head.replay()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     for k in range(steps):
         ev[k][0].record()
-        g_mat.replay()
-        ev[k][1].record()
         g_round.replay()
-        ev[k][2].record()
+        ev[k][1].record()
         g_head.replay()
-        ev[k][3].record()
+        ev[k][2].record()
     torch.cuda.synchronize()
     barrier(world)
-    tot = ev[0][0].elapsed_time(ev[-1][3])
-    per = {"materialize": sum(e[0].elapsed_time(e[1]) for e in ev) / steps,
-           "round": sum(e[1].elapsed_time(e[2]) for e in ev) / steps,
-           "head": sum(e[2].elapsed_time(e[3]) for e in ev) / steps}
+    tot = ev[0][0].elapsed_time(ev[-1][2])
+    per = {"round_with_catch_up": sum(e[0].elapsed_time(e[1]) for e in ev) / steps,
+           "head": sum(e[1].elapsed_time(e[2]) for e in ev) / steps}
     return tot / steps, per
 
 
@@ -320,6 +330,19 @@ def time_call(fn, steps: int, warmup: int):
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps
+
+
+def round_only(st: State, args) -> dict:
+    """The round without pending rows (its context already complete)."""
+    us = 1000.0 * time_call(st.round_plain, args.steps, args.warmup)
+    return {"us": us, "rounds_per_s": 1e6 / us}
+
+
+def separate_catch_up(st: State, args) -> dict:
+    """The catch-up as its own materialisation call, and the whole step done that way."""
+    mat = 1000.0 * time_call(st.materialize, args.steps, args.warmup)
+    step = 1000.0 * time_call(st.step_separate, args.steps, args.warmup)
+    return {"materialize_us": mat, "step_us": step}
 
 
 def refine_us(st: State, args) -> float:
@@ -474,8 +497,8 @@ def main():
     if args.profile_case:
         # One warm step, then the profiled step inside the NVTX range "profiled_step"
         # (ncu --nvtx --nvtx-include "profiled_step/").  GEMM launch order of the step:
-        # [0] W_feature, [1] K/V, [2] QKV, [3] W_o, [4] gate/up, [5] down, [6] code read,
-        # [7] gate/value maps, [8] write, [9] LM head.
+        # [0] W_feature (catch-up), [1] QKV (+ the pending rows' K/V), [2] W_o, [3] gate/up,
+        # [4] down, [5] code read, [6] gate/value maps, [7] write, [8] LM head.
         base = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8
         geo = base if args.profile_full else base.with_(n_layers=1, windows=(2048,))
         st = State(geo, args.seed)
@@ -517,12 +540,15 @@ def main():
         "data": "synthetic (seeded; random-init weights of the 27B DSpine-b16 drafter geometry)",
         "config": {"workload": geo.name, "B": geo.batch, "W": geo.W, "context": st.F[0],
                    "window": geo.windows[0], "hidden": geo.hidden, "layers": geo.n_layers,
-                   "vocab": geo.vocab, "step": "catch-up materialise 16 rows + draft round + LM head argmax",
+                   "vocab": geo.vocab,
+                   "step": "draft round with the catch-up of 16 pending rows per request fused in "
+                           "+ LM head argmax",
                    "l2": "inputs larger than L2 (weights streamed per step >> 129 MB)",
                    "parallelism": f"replicas x{world}"},
         "us_per_step": 1000.0 * ms,
         "breakdown_us": {k: 1000.0 * v for k, v in per.items()},
-        "round_only": {"us": 1000.0 * per["round"], "rounds_per_s": 1000.0 / per["round"]},
+        "round_only": round_only(st, args),
+        "separate_catch_up": separate_catch_up(st, args),
         "achieved_step_gbs": step_gbs,
         "step_roofline_frac": {"of_measured_hbm": step_gbs / hbm, "of_8tbs": step_gbs / 8000.0},
         "algorithmic_bytes_per_step": by,
@@ -548,6 +574,8 @@ def main():
         line["b8"] = {"workload": geo8.name, "contexts": st8.F, "us_per_step": 1000.0 * ms8,
                       "rounds_per_s": world * 1000.0 / ms8,
                       "breakdown_us": {k: 1000.0 * v for k, v in per8.items()},
+                      "round_only": round_only(st8, args),
+                      "separate_catch_up": separate_catch_up(st8, args),
                       "achieved_step_gbs": gbs8, "frac_of_measured_hbm": gbs8 / hbm,
                       "algorithmic_bytes_per_step": by8,
                       "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup),

@@ -67,6 +67,11 @@ class KvCache(C.Structure):
                 ("b_max", C.c_int)]
 
 
+class Pending(C.Structure):
+    _fields_ = [("feats", C.c_void_p), ("request", C.c_void_p), ("pos", C.c_void_p),
+                ("n_rows", C.c_int)]
+
+
 _lib = None
 
 
@@ -87,7 +92,7 @@ def lib() -> C.CDLL:
                                             C.POINTER(KvCache), vp, vp, vp, vp, i, vp, sz, vp]
         L.bd_draft_round.restype = i
         L.bd_draft_round.argtypes = [C.POINTER(Config), C.POINTER(Weights), C.POINTER(KvCache),
-                                     vp, vp, i, i, vp, vp, vp, vp, vp, sz, vp]
+                                     vp, vp, i, i, vp, vp, vp, vp, C.POINTER(Pending), vp, sz, vp]
         L.bd_refine_tail.restype = i
         L.bd_refine_tail.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, vp, vp, i, i, i,
                                      vp, vp, vp, vp, sz, vp]
@@ -211,11 +216,17 @@ def draft_round(cfg: Config, weights: Weights, kv: KvCache, anchor_ids: torch.Te
                 frontier: torch.Tensor, n_masks: int, head_in: torch.Tensor,
                 workspace: torch.Tensor, hidden_out: Optional[torch.Tensor] = None,
                 layers_out: Optional[torch.Tensor] = None, stream=None,
-                tail_state: Optional[torch.Tensor] = None):
+                tail_state: Optional[torch.Tensor] = None, pending: Optional[tuple] = None):
+    """pending = (feats [n, n_tgt*H], request int32 [n], pos int64 [n]) or None: context
+    rows the round materialises before it drafts (frontier is the frontier they complete)."""
+    pd = None
+    if pending is not None:
+        feats, req, pos = pending
+        pd = Pending(_ptr(feats), _ptr(req), _ptr(pos), int(feats.shape[0]))
     _check(lib().bd_draft_round(
         C.byref(cfg), C.byref(weights), C.byref(kv), _ptr(anchor_ids), _ptr(frontier),
         int(anchor_ids.shape[0]), int(n_masks), _ptr(head_in), _ptr(hidden_out),
-        _ptr(layers_out), _ptr(tail_state), _ptr(workspace),
+        _ptr(layers_out), _ptr(tail_state), None if pd is None else C.byref(pd), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -40,6 +40,7 @@ bd_status fail(bd_status s, const std::string &msg) {
 
 constexpr int kMaxB = 8;
 constexpr int kMaxMasks = 15;
+constexpr int kMaxPendPerReq = 16;  // pending context rows a round takes per request
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -178,40 +179,63 @@ size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + ti
 struct RoundWs {
   GemmWs g;
   unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
-  float *x, *z, *pre, *r, *part_o, *qkv_raw;
+  float *x, *z, *pre, *r, *part_o, *qkv_raw, *feat, *kv_raw;
   float2 *rope, *part_ml;
-  void *xn, *q, *kblk, *vblk, *att, *hmid, *c, *m;
+  void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
-size_t round_max_tiles(const bd_config *c, int T) {
-  const int ntn = (T + gemm_block_n(T) - 1) / gemm_block_n(T);  // 1 for T <= 128
-  size_t t = tiles_of(c->n_q_heads * c->head_dim, 128) + 2 * tiles_of(c->n_kv_heads * c->head_dim, 128);
-  t = std::max(t, tiles_of(c->hidden, 128));
-  t = std::max(t, tiles_of(c->ffn, 64));
-  if (c->code_width > 0) {
-    t = std::max(t, tiles_of(c->code_width, 128));
-    t = std::max(t, 3 * tiles_of(c->msg_width, 128));
-  }
-  return t * ntn;
-}
 int pad16(int n) { return (n + 15) / 16 * 16; }
+// Upper bound on the n-tiles of a GEMM over n tokens (split activations: 128 tokens per
+// tile; otherwise gemm_block_n's tile, never smaller).
+int n_tiles_of(int n) { return (pad16(n) + 127) / 128; }
+// Tiles of the round's largest GEMM: the Q/K/V product also carries the T_q - T pending
+// context rows, the others the T block rows; the catch-up's feature projection has H rows.
+size_t round_max_tiles(const bd_config *c, int T, int Tq) {
+  size_t t = (tiles_of(c->n_q_heads * c->head_dim, 128) + 2 * tiles_of(c->n_kv_heads * c->head_dim, 128)) *
+             n_tiles_of(Tq);
+  size_t o = std::max(tiles_of(c->hidden, 128), tiles_of(c->ffn, 64));
+  if (c->code_width > 0) {
+    o = std::max(o, tiles_of(c->code_width, 128));
+    o = std::max(o, 3 * tiles_of(c->msg_width, 128));
+  }
+  return std::max(t, o * n_tiles_of(T));
+}
+
+size_t mat_max_tiles(const bd_config *c, int n);
+
+// Pending context rows ride in the block's Q/K/V product while the product keeps a single
+// n-tile (T + n_pend <= 128 token columns); beyond that an extra n-tile would re-stream
+// the Q/K/V weights and double the tensor work, so the catch-up then runs as its own
+// K/V product over every layer (the materialisation's), still inside the round.
+bool fuse_ctx(int T, int n_pend) { return n_pend > 0 && pad16(T + n_pend) <= 128; }
 
 // Activation buffers of the bf16 path hold a hi/lo pair: [2][pad16(T)][K] (hi block, then
-// the lo block); q and the block K/V hold [2][T][...].
-void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int sms) {
-  const int T = B * W, TP = pad16(T);
+// the lo block); q and the block K/V hold [2][T][...].  The Q/K/V input xq holds
+// T + n_pend rows per block when the pending rows are fused (the block rows, then the
+// pending context rows c_t); otherwise c_t goes to cmat and its raw K/V to kv_raw.
+void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_pend, int sms) {
+  const bool fuse = fuse_ctx(B * W, n_pend);
+  const int T = B * W, TP = pad16(T), Tq = T + (fuse ? n_pend : 0), TQ = pad16(Tq);
   const int e = elem_bytes(c);
   const int H = c->hidden, QD = c->n_q_heads * c->head_dim, KD = c->n_kv_heads * c->head_dim;
-  carve_gemm(cv, w.g, 2 * TP, round_max_tiles(c, T), sms);
+  size_t tiles = round_max_tiles(c, T, Tq);
+  if (n_pend > 0 && !fuse) tiles = std::max(tiles, mat_max_tiles(c, n_pend));
+  carve_gemm(cv, w.g, 2 * std::max(std::min(TQ, 128), pad16(std::min(n_pend, 128))), tiles, sms);
   w.att_cnt = cv.take<unsigned>(2 * static_cast<size_t>(B) * c->n_kv_heads);
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
-  w.qkv_raw = cv.take<float>(static_cast<size_t>(T) * (QD + 2 * KD));
+  w.qkv_raw = cv.take<float>(static_cast<size_t>(Tq) * (QD + 2 * KD));
+  w.feat = n_pend > 0 ? cv.take<float>(static_cast<size_t>(n_pend) * H) : nullptr;
+  w.cmat = n_pend > 0 && !fuse ? cv.take<char>(static_cast<size_t>(n_pend) * H * e) : nullptr;
+  w.kv_raw = n_pend > 0 && !fuse
+                 ? cv.take<float>(static_cast<size_t>(n_pend) * c->n_layers * 2 * KD)
+                 : nullptr;
   w.xn = cv.take<char>(static_cast<size_t>(2 * TP) * H * e);
+  w.xq = cv.take<char>(static_cast<size_t>(2 * TQ) * H * e);
   w.q = cv.take<char>(static_cast<size_t>(2 * T) * QD * e);
   w.kblk = cv.take<char>(static_cast<size_t>(2 * T) * KD * e);
   w.vblk = cv.take<char>(static_cast<size_t>(2 * T) * KD * e);
   w.att = cv.take<char>(static_cast<size_t>(2 * TP) * QD * e);
   w.hmid = cv.take<char>(static_cast<size_t>(2 * TP) * c->ffn * e);
-  w.rope = cv.take<float2>(static_cast<size_t>(T) * (c->head_dim / 2));
+  w.rope = cv.take<float2>(static_cast<size_t>(T + n_pend) * (c->head_dim / 2));
   size_t po = 0, pm = 0;
   for (int l = 0; l < c->n_layers; ++l) {
     const int s = att_splits(c, l, B, W, sms);
@@ -332,6 +356,70 @@ void add_w(GemmPlan &p, const void *ptr, int rows, const uint8_t *packed_base = 
 
 }  // namespace
 
+// S2 for n context rows c (config dtype, [n][H]): every layer's raw K|V in one product
+// (up to kMaxSegs/2 layers per launch) into kv_raw [n][L*2*Hkv*D], then head norm + RoPE +
+// ring scatter of every layer in one launch (row r at position pos[r] of ring row
+// req[r] < n_req, stored only inside the final live window of frontier[req[r]]).
+static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
+                                const void *cmat, int n_rows, float *kv_raw, const float2 *rope,
+                                const int32_t *row_request, const int64_t *row_pos,
+                                const int64_t *ctx_frontier, int n_req, const GemmScratch &sc,
+                                cudaStream_t s) {
+  const int H = cfg->hidden, D = cfg->head_dim, KD = cfg->n_kv_heads * D;
+  const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
+  const PackedLayout PL = packed_layout(cfg);
+  const int ldkv = cfg->n_layers * 2 * KD;
+  for (int l0 = 0; l0 < cfg->n_layers; l0 += kMaxSegs / 2) {
+    const int l1 = std::min(cfg->n_layers, l0 + kMaxSegs / 2);
+    GemmPlan p = make_plan(cfg, cmat, n_rows, H);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = kv_raw;
+    p.args.ld_out = ldkv;
+    for (int l = l0; l < l1; ++l) {
+      const int sk = p.n_w;
+      add_w(p, w->layer[l].wk, KD, pk, PL.wk[l]);
+      add_w(p, w->layer[l].wv, KD, pk, PL.wv[l]);
+      p.args.seg[sk].out_col = l * 2 * KD;
+      p.args.seg[sk + 1].out_col = l * 2 * KD + KD;
+    }
+    BD_TRY(launch_gemm(p, sc, s));
+  }
+  HeadPostArgs h;
+  memset(&h, 0, sizeof h);
+  h.raw = kv_raw;
+  h.ld_raw = ldkv;
+  h.D = D;
+  h.n_kv_heads = cfg->n_kv_heads;
+  h.W = 1;
+  h.n_req = n_req;
+  h.eps = cfg->eps;
+  h.rope = rope;
+  h.row_req = row_request;
+  h.row_pos = row_pos;
+  h.frontier = ctx_frontier;
+  int n_segs = 0;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    HeadSeg &k = h.seg[n_segs++];
+    k.kind = HK_K;
+    k.dst_mode = HD_RING;
+    k.col0 = l * 2 * KD;
+    k.n_heads = cfg->n_kv_heads;
+    k.cap = cfg->ring_capacity[l];
+    k.norm = w->layer[l].k_norm;
+    k.dst = kv->k[l];
+    HeadSeg &v = h.seg[n_segs++];
+    v = k;
+    v.kind = HK_V;
+    v.col0 = l * 2 * KD + KD;
+    v.norm = nullptr;
+    v.dst = kv->v[l];
+  }
+  h.n_groups = 1;
+  h.grp[0] = HeadGroup{0, n_rows, 0, n_segs, 2 * cfg->n_layers * cfg->n_kv_heads};
+  BD_TRY(launch_head_post(cfg->dtype, h, s));
+  return BD_OK;
+}
+
 // ====================================================================== C ABI
 extern "C" {
 
@@ -350,7 +438,7 @@ size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int ma
   for (int B = 1; B <= b_max; ++B) {
     Carve cv;
     RoundWs w;
-    carve_round(cv, w, cfg, B, max_masks + 1, sms);
+    carve_round(cv, w, cfg, B, max_masks + 1, kMaxPendPerReq * B, sms);
     need = std::max(need, cv.off);
     Carve ch;
     HeadWs hw;
@@ -408,7 +496,7 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
   MatWs mw;
   carve_mat(cv, mw, cfg, n_rows, sms);
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for materialisation");
-  const int H = cfg->hidden, D = cfg->head_dim, KD = cfg->n_kv_heads * D;
+  const int H = cfg->hidden, D = cfg->head_dim;
   const RopeFreq freq = rope_freq(cfg);
   const GemmScratch sc = scratch_of(mw.g);
   const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
@@ -426,63 +514,15 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
                           mw.cmat, nullptr, nullptr, nullptr, 1, 0, s));
   }
   // S2: every layer's raw context K and V (fp32), then head norm + RoPE + ring scatter
-  const int ldkv = cfg->n_layers * 2 * KD;
-  for (int l0 = 0; l0 < cfg->n_layers; l0 += kMaxSegs / 2) {
-    const int l1 = std::min(cfg->n_layers, l0 + kMaxSegs / 2);
-    GemmPlan p = make_plan(cfg, mw.cmat, n_rows, H);
-    p.args.epi = EPI_STORE_F32;
-    p.args.out_f32 = mw.kv_raw;
-    p.args.ld_out = ldkv;
-    for (int l = l0; l < l1; ++l) {
-      const int sk = p.n_w;
-      add_w(p, w->layer[l].wk, KD, pk, PL.wk[l]);
-      add_w(p, w->layer[l].wv, KD, pk, PL.wv[l]);
-      p.args.seg[sk].out_col = l * 2 * KD;
-      p.args.seg[sk + 1].out_col = l * 2 * KD + KD;
-    }
-    BD_TRY(launch_gemm(p, sc, s));
-  }
-  {
-    HeadPostArgs h;
-    memset(&h, 0, sizeof h);
-    h.raw = mw.kv_raw;
-    h.ld_raw = ldkv;
-    h.rows = n_rows;
-    h.D = D;
-    h.n_kv_heads = cfg->n_kv_heads;
-    h.W = 1;
-    h.n_req = kv->b_max;
-    h.eps = cfg->eps;
-    h.rope = mw.rope;
-    h.row_req = row_request;
-    h.row_pos = row_pos;
-    h.frontier = ctx_frontier;
-    for (int l = 0; l < cfg->n_layers; ++l) {
-      HeadSeg &k = h.seg[h.n_segs++];
-      k.kind = HK_K;
-      k.dst_mode = HD_RING;
-      k.col0 = l * 2 * KD;
-      k.n_heads = cfg->n_kv_heads;
-      k.cap = cfg->ring_capacity[l];
-      k.norm = w->layer[l].k_norm;
-      k.dst = kv->k[l];
-      HeadSeg &v = h.seg[h.n_segs++];
-      v = k;
-      v.kind = HK_V;
-      v.col0 = l * 2 * KD + KD;
-      v.norm = nullptr;
-      v.dst = kv->v[l];
-    }
-    h.total_heads = 2 * cfg->n_layers * cfg->n_kv_heads;
-    BD_TRY(launch_head_post(cfg->dtype, h, s));
-  }
-  return BD_OK;
+  return enqueue_ctx_kv(cfg, w, kv, mw.cmat, n_rows, mw.kv_raw, mw.rope, row_request, row_pos,
+                        ctx_frontier, kv->b_max, sc, s);
 }
 
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B, int n_masks,
                          float *head_in, float *hidden_out, float *layers_out, float *tail_state,
-                         void *workspace, size_t workspace_bytes, void *stream_) {
+                         const bd_pending *pending, void *workspace, size_t workspace_bytes,
+                         void *stream_) {
   std::string e = check_config(cfg);
   if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
   if (B < 1 || B > kMaxB) return fail(BD_ERR_INVALID_ARG, "B must be in 1..8");
@@ -493,6 +533,13 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   if (!head_in || !aligned16(head_in)) return fail(BD_ERR_INVALID_ARG, "head_in NULL or misaligned");
   if (tail_state && cfg->code_width == 0)
     return fail(BD_ERR_INVALID_ARG, "tail_state needs the injection bridge (code_width > 0)");
+  const int n_pend = pending ? pending->n_rows : 0;
+  if (pending) {
+    if (n_pend < 0 || n_pend > kMaxPendPerReq * B)
+      return fail(BD_ERR_INVALID_ARG, "pending->n_rows must be in 0..16*B");
+    if (n_pend > 0 && (!pending->feats || !aligned16(pending->feats) || !pending->request || !pending->pos))
+      return fail(BD_ERR_INVALID_ARG, "pending feats/request/pos NULL or misaligned");
+  }
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   const int W = n_masks + 1, T = B * W, TP = pad16(T);
@@ -507,8 +554,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   Carve cv;
   cv.base = static_cast<char *>(workspace);
   RoundWs rw;
-  carve_round(cv, rw, cfg, B, W, sms);
+  carve_round(cv, rw, cfg, B, W, n_pend, sms);
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for this round");
+  const bool fuse = fuse_ctx(T, n_pend);
+  const int Tq = T + (fuse ? n_pend : 0), TQ = pad16(Tq);
 
   const int H = cfg->hidden, D = cfg->head_dim;
   const int QD = cfg->n_q_heads * D, KD = cfg->n_kv_heads * D;
@@ -526,14 +575,37 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const ZeroSpan zero{rw.g.counters, static_cast<size_t>(rw.att_cnt - rw.g.counters) +
                                          2 * static_cast<size_t>(B) * cfg->n_kv_heads};
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
-                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq, zero, s));
+                           cfg->mask_token_id, rw.x, rw.rope, D / 2, freq,
+                           n_pend > 0 ? pending->pos : nullptr, n_pend, zero, s));
+  const size_t lo_q = split ? static_cast<size_t>(TQ) * H : 0;  // lo block of xq
+  if (n_pend > 0) {  // S1 of the catch-up: c_t = plain_rmsnorm(W_feature s_t)
+    GemmPlan p = make_plan(cfg, pending->feats, n_pend, cfg->n_target_layers * H);
+    add_w(p, w->w_feature, H, pk, PL.w_feature);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = rw.feat;
+    p.args.ld_out = H;
+    BD_TRY(launch_gemm(p, sc, s));
+    if (fuse) {  // into rows T.. of xq, with a zero lo part
+      char *ctx_rows = static_cast<char *>(rw.xq) + static_cast<size_t>(T) * H * elem_bytes(cfg);
+      BD_TRY(launch_rownorm(dt, rw.feat, n_pend, H, w->context_norm, cfg->eps, NORM_CTX, ctx_rows,
+                            nullptr, nullptr, nullptr, 1, lo_q, s));
+    } else {  // S2 of the catch-up as its own product over every layer
+      BD_TRY(launch_rownorm(dt, rw.feat, n_pend, H, w->context_norm, cfg->eps, NORM_PLAIN, rw.cmat,
+                            nullptr, nullptr, nullptr, 1, 0, s));
+      const bd_status st = enqueue_ctx_kv(cfg, w, kv, rw.cmat, n_pend, rw.kv_raw,
+                                          rw.rope + static_cast<size_t>(T) * (D / 2),
+                                          pending->request, pending->pos, frontier, B, sc, s);
+      if (st != BD_OK) return st;
+    }
+  }
   for (int l = 0; l < cfg->n_layers; ++l) {
     const bd_layer_weights &L = w->layer[l];
-    // S4: n = rmsnorm(x); q, k, v with head norm + RoPE
-    BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
-                          nullptr, nullptr, W, lo(H), s));
+    // S4: n = rmsnorm(x); q, k, v with head norm + RoPE.  The pending context rows ride
+    // along in the same product: their K/V (S2) use the same W_k, W_v tiles.
+    BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xq, nullptr,
+                          nullptr, nullptr, W, lo_q, s));
     {
-      GemmPlan p = make_plan(cfg, rw.xn, T, H);
+      GemmPlan p = make_plan(cfg, rw.xq, Tq, H);
       p.split = split;
       add_w(p, L.wq, QD, pk, PL.wq[l]);
       add_w(p, L.wk, KD, pk, PL.wk[l]);
@@ -549,19 +621,29 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       memset(&h, 0, sizeof h);
       h.raw = rw.qkv_raw;
       h.ld_raw = QD + 2 * KD;
-      h.rows = T;
       h.D = D;
       h.n_kv_heads = cfg->n_kv_heads;
       h.W = W;
       h.eps = cfg->eps;
       h.rope = rw.rope;
-      h.n_segs = 3;
       const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
       const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
       h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo};
       h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo};
       h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo};
-      h.total_heads = cfg->n_q_heads + 2 * cfg->n_kv_heads;
+      h.n_groups = 1;
+      h.grp[0] = HeadGroup{0, T, 0, 3, cfg->n_q_heads + 2 * cfg->n_kv_heads};
+      if (fuse) {  // the pending rows' context K/V go to the rings (before attention)
+        const int cap = cfg->ring_capacity[l];
+        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0};
+        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0};
+        h.n_groups = 2;
+        h.grp[1] = HeadGroup{T, n_pend, 3, 2, 2 * cfg->n_kv_heads};
+        h.n_req = B;
+        h.row_req = pending->request;
+        h.row_pos = pending->pos;
+        h.frontier = frontier;
+      }
       BD_TRY(launch_head_post(dt, h, s));
     }
     // S5: block attention over the ring context and the block

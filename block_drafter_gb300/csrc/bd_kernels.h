@@ -35,8 +35,6 @@ struct RopeFreq {
   double inv[64];
 };
 
-// Round prologue: x[b*W+i] = embed[id] (fp32), id = anchor_b for i = 0 else MASK, and the
-// (cos, sin) table of positions F_b + i.
 // Words a call's first kernel sets to zero (the GEMM tile counters of the call): doing it
 // there instead of with a memset keeps the call one chain of dependent launches.
 struct ZeroSpan {
@@ -44,10 +42,13 @@ struct ZeroSpan {
   size_t n;
 };
 
+// Round prologue: x[b*W+i] = embed[id] (fp32), id = anchor_b for i = 0 else MASK, the
+// (cos, sin) rows of positions F_b + i (rows 0 .. B*W-1), then the rows of n_pend pending
+// context positions (rows B*W ..).
 std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
                               const int64_t *frontier, int B, int W, int mask_id, float *x,
-                              float2 *rope, int half, const RopeFreq &freq, ZeroSpan z,
-                              cudaStream_t s);
+                              float2 *rope, int half, const RopeFreq &freq, const int64_t *pend_pos,
+                              int n_pend, ZeroSpan z, cudaStream_t s);
 // (cos, sin) table of arbitrary absolute positions.
 std::string launch_rope_table(const int64_t *pos, int n, float2 *rope, int half,
                               const RopeFreq &freq, ZeroSpan z, cudaStream_t s);
@@ -57,7 +58,8 @@ std::string launch_zero(ZeroSpan z, cudaStream_t s);
 enum NormMode : int {
   NORM_PLAIN = 0,   // out = gain * x / sqrt(mean(x^2) + eps)
   NORM_BRIDGE = 1,  // r = sqrt(mean(x^2)); out = x / (r + eps); r_out = r
-  NORM_FINAL = 2    // plain, plus fp32 copy and the mask-row copy for the LM head
+  NORM_FINAL = 2,   // plain, plus fp32 copy and the mask-row copy for the LM head
+  NORM_CTX = 3      // plain; the lo part is written as zero (c_t enters products as bf16)
 };
 // lo_off != 0: also write the rounding residual y - hi at out + lo_off (split activation).
 std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain,
@@ -90,14 +92,19 @@ struct HeadSeg {
   void *dst;
   size_t lo_off;     // != 0: also store the rounding residual at dst + lo_off
 };
+// Rows row0 .. row0+rows-1 take segments seg0 .. seg0+n_segs-1 (total_heads heads in all).
+struct HeadGroup {
+  int row0, rows, seg0, n_segs, total_heads;
+};
 struct HeadPostArgs {
   const float *raw;
-  int ld_raw, rows, D, n_kv_heads, W, n_req, n_segs, total_heads;
+  int ld_raw, D, n_kv_heads, W, n_req, n_groups;
   float eps;
-  const float2 *rope;        // [rows][D/2]
-  const int32_t *row_req;    // ring mode
+  const float2 *rope;        // [rows][D/2], by absolute row
+  const int32_t *row_req;    // ring mode, by row - row0 of the group
   const int64_t *row_pos;
   const int64_t *frontier;
+  HeadGroup grp[2];
   HeadSeg seg[kMaxHeadSegs];
 };
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);

@@ -42,12 +42,19 @@ __device__ __forceinline__ void zero_span(ZeroSpan z) {
 
 template <typename T>
 __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *anchors,
-                                  const int64_t *frontier, int W, int mask_id, float *x,
-                                  float2 *rope, int half, RopeFreq freq, ZeroSpan z) {
+                                  const int64_t *frontier, int W, int n_tok, int mask_id, float *x,
+                                  float2 *rope, int half, RopeFreq freq, const int64_t *pend_pos,
+                                  ZeroSpan z) {
   const int tok = blockIdx.x, b = tok / W, i = tok % W;
   pdl_wait();
   pdl_trigger();
   zero_span(z);
+  if (tok >= n_tok) {  // a pending context row: its RoPE row only
+    const long long pos = pend_pos[tok - n_tok];
+    for (int j = threadIdx.x; j < half; j += blockDim.x)
+      rope[static_cast<size_t>(tok) * half + j] = rope_cs(pos, freq.inv[j]);
+    return;
+  }
   int id = i == 0 ? anchors[b] : mask_id;
   if (id < 0 || id >= V) {
     if (threadIdx.x == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
@@ -150,7 +157,9 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, con
     }
     if (orow) {
       store4<T>(orow, i4, y);
-      if (lo_off) {  // residual of the rounding, so that hi + lo carries ~16 mantissa bits
+      if (lo_off && mode == NORM_CTX) {
+        store4<T>(orow + lo_off, i4, make_float4(0.f, 0.f, 0.f, 0.f));
+      } else if (lo_off) {  // residual of the rounding: hi + lo carries ~16 mantissa bits
         const float4 h = make_float4(to_f<T>(from_f<T>(y.x)), to_f<T>(from_f<T>(y.y)),
                                      to_f<T>(from_f<T>(y.z)), to_f<T>(from_f<T>(y.w)));
         store4<T>(orow + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
@@ -183,11 +192,18 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   const int lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();
-  const int row = warp / a.total_heads;
-  int hg = warp % a.total_heads;
-  if (row >= a.rows) return;
-  int si = 0;
-  while (si + 1 < a.n_segs && hg >= a.seg[si].n_heads) {
+  int wg = warp, g = 0;
+  if (a.n_groups > 1 && wg >= a.grp[0].rows * a.grp[0].total_heads) {
+    wg -= a.grp[0].rows * a.grp[0].total_heads;
+    g = 1;
+  }
+  const HeadGroup gr = a.grp[g];
+  const int rr = wg / gr.total_heads;  // row within the group
+  int hg = wg % gr.total_heads;
+  if (rr >= gr.rows) return;
+  const int row = gr.row0 + rr;
+  int si = gr.seg0;
+  while (si + 1 < gr.seg0 + gr.n_segs && hg >= a.seg[si].n_heads) {
     hg -= a.seg[si].n_heads;
     ++si;
   }
@@ -223,8 +239,8 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
     const int b = row / a.W, i = row % a.W;
     o = ((static_cast<size_t>(b) * a.n_kv_heads + hg) * a.W + i) * D;
   } else {
-    const int req = a.row_req[row];
-    const long long pos = a.row_pos[row];
+    const int req = a.row_req[rr];
+    const long long pos = a.row_pos[rr];
     if (req < 0 || req >= a.n_req || pos < 0) {
       if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
       return;
@@ -721,17 +737,18 @@ static std::string err(const char *what, cudaError_t e) {
 
 std::string launch_round_prep(int dtype, const void *embed, int H, int V, const int32_t *anchors,
                               const int64_t *frontier, int B, int W, int mask_id, float *x,
-                              float2 *rope, int half, const RopeFreq &freq, ZeroSpan z,
-                              cudaStream_t s) {
+                              float2 *rope, int half, const RopeFreq &freq, const int64_t *pend_pos,
+                              int n_pend, ZeroSpan z, cudaStream_t s) {
   cudaError_t e;
+  const int T = B * W;
   if (dtype == 0)
-    e = launch_pdl(round_prep_kernel<__nv_bfloat16>, dim3(B * W), dim3(256), 0, s,
-                   static_cast<const __nv_bfloat16 *>(embed), H, V, anchors, frontier, W, mask_id, x,
-                   rope, half, freq, z);
+    e = launch_pdl(round_prep_kernel<__nv_bfloat16>, dim3(T + n_pend), dim3(256), 0, s,
+                   static_cast<const __nv_bfloat16 *>(embed), H, V, anchors, frontier, W, T, mask_id,
+                   x, rope, half, freq, pend_pos, z);
   else
-    e = launch_pdl(round_prep_kernel<float>, dim3(B * W), dim3(256), 0, s,
-                   static_cast<const float *>(embed), H, V, anchors, frontier, W, mask_id, x, rope,
-                   half, freq, z);
+    e = launch_pdl(round_prep_kernel<float>, dim3(T + n_pend), dim3(256), 0, s,
+                   static_cast<const float *>(embed), H, V, anchors, frontier, W, T, mask_id, x,
+                   rope, half, freq, pend_pos, z);
   return err("round prep", e);
 }
 
@@ -773,7 +790,8 @@ std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_o
 }
 
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
-  const long long warps = static_cast<long long>(a.rows) * a.total_heads;
+  long long warps = 0;
+  for (int g = 0; g < a.n_groups; ++g) warps += static_cast<long long>(a.grp[g].rows) * a.grp[g].total_heads;
   const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
   cudaError_t e;
   if (a.D == 128)

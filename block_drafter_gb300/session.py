@@ -58,9 +58,12 @@ class DraftSession:
     def round(self, anchor_ids: torch.Tensor, frontier: torch.Tensor, n_masks: int,
               head_in: torch.Tensor, hidden_out: Optional[torch.Tensor] = None,
               layers_out: Optional[torch.Tensor] = None, stream=None,
-              tail_state: Optional[torch.Tensor] = None):
+              tail_state: Optional[torch.Tensor] = None, pending: Optional[tuple] = None):
+        """pending = (feats, row_request, row_pos): context rows (at most 16 per request)
+        materialised inside the round before it drafts; frontier is the frontier they
+        complete."""
         B.draft_round(self.cfg, self.wstruct, self.kv, anchor_ids, frontier, n_masks, head_in,
-                      self.workspace, hidden_out, layers_out, stream, tail_state)
+                      self.workspace, hidden_out, layers_out, stream, tail_state, pending)
 
     def alloc_tail_state(self, Bn: int, n_masks: int) -> torch.Tensor:
         return torch.empty(B.tail_state_floats(self.cfg, Bn, n_masks), dtype=torch.float32,

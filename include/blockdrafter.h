@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 4
+#define BD_ABI_VERSION 5
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -127,7 +127,8 @@ int bd_abi_version(void);
 
 /* Bytes of workspace any entry point below needs for rounds of up to `b_max`
  * requests with up to `max_masks` masks (K) and materialisations of up to
- * `max_ctx_rows` rows per call.  Returns 0 for an invalid or unsupported config. */
+ * `max_ctx_rows` rows per call (a round's own pending rows, up to 16 per request, are
+ * always covered).  Returns 0 for an invalid or unsupported config. */
 size_t bd_workspace_bytes(const bd_config *cfg, int b_max, int max_masks, int max_ctx_rows);
 
 /* Bytes of the packed weight image for `cfg` (0 for an invalid config). */
@@ -172,6 +173,30 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
                                 size_t workspace_bytes, void *stream);
 
 /*
+ * Pending context rows a round materialises before it drafts (the decode-step catch-up,
+ * [DFlash-notes] paragraph on the processed-token frontier: feature rows the target has
+ * committed but the drafter has not yet turned into context K/V are converted first, so
+ * that the draft context extends to F when the block is proposed).
+ * The rows' context K/V are computed and stored exactly as bd_ctx_kv_materialize would
+ * (c_t enters the K/V products as bf16 in a bf16 config), but inside the round: the
+ * feature projection runs first and every layer's context K/V products share the weight
+ * tiles of that layer's block Q/K/V product (one read of W_k and W_v per layer).
+ *
+ *   feats    dev [n_rows, n_target_layers*H]  captured residual rows s_t
+ *   request  dev int32 [n_rows]  request (ring row) of each row, < B of the round
+ *   pos      dev int64 [n_rows]  absolute position t of each row, < frontier[request];
+ *            stored in layer l only if t >= frontier[request] - ring_capacity[l]
+ *   n_rows   0 .. 16*B (0 = nothing pending)
+ * Rows of one request must have distinct positions.
+ */
+typedef struct {
+  const void *feats;
+  const int32_t *request;
+  const int64_t *pos;
+  int n_rows;
+} bd_pending;
+
+/*
  * One masked-block draft forward (S3 .. S9 and the final norm) for B requests.
  * Numerics (bf16 config): weights and context K/V are used as stored; the residual
  * stream is fp32; every activation that feeds a tensor-core product (normed rows,
@@ -198,12 +223,14 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
  *               redoes its injection from (input of bd_refine_tail), T = B*W rows:
  *               [T*H] pre-injection residual u, then [T] its RMS r, then [T*Mc] the
  *               receiver gate term G c.  Requires code_width > 0.
+ *   pending     host pointer to a bd_pending (its arrays are dev), or NULL: context rows
+ *               to materialise first; frontier[] is then the frontier they complete
  */
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                          const int32_t *anchor_ids, const int64_t *frontier, int B,
                          int n_masks, float *head_in, float *hidden_out, float *layers_out,
-                         float *tail_state, void *workspace, size_t workspace_bytes,
-                         void *stream);
+                         float *tail_state, const bd_pending *pending, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /*
  * Tied LM head with per-row argmax (S10).  [DFlash-notes], proposal head:

@@ -25,6 +25,9 @@ Sources (cited by page title and section throughout):
                   proposal row; the fallback path scores with the BF16 vocabulary head).
   [Tail]          "DSpine 完全拆解", section "前驱条件解码与 transition cache"
                   (last-write refinement, the K x K transition table, greedy walk).
+  [Frontier]      "dflash.md", the paragraph on the processed-token frontier F: committed
+                  target feature rows that the drafter has not yet converted are
+                  materialised before the block is proposed, so the context reaches F.
 
 Readings taken where the pages are schematic or garbled (each also listed in the design doc):
   R-gate   g = sigmoid(G c_t + G_p c_{t-1} + b), m = g * (A c_{t-1}); b absent means 0.
@@ -42,6 +45,9 @@ Readings taken where the pages are schematic or garbled (each also listed in DES
            for a local layer (every populated position for a full layer); the
            block-causal flag additionally hides block keys j > i.
   R-tie    argmax ties go to the lowest token id; only the K mask rows are scored.
+  R-catch  a round given pending rows first materialises them exactly as a separate
+           materialisation would (each request's rows into its own rings, stored only
+           inside the final live window of the frontier they complete), then drafts.
   R-topk   a row's k candidates are its k largest exact logits over the whole
            vocabulary, by descending score; equal scores keep the lower token id first.
   R-tail   last-write refinement of block row i with predecessor token s: the last
@@ -404,12 +410,31 @@ def draft_request(geo, weights, rings, request: int, anchor: int, frontier: int,
     return out
 
 
+def catch_up(geo, weights, rings, frontiers: Sequence[int], feats, requests, positions):
+    """Materialise pending context rows before a round (R-catch, [Frontier]): row t
+    (features feats[t], request requests[t], position positions[t]) goes into its
+    request's rings; ``frontiers[b]`` is the frontier the rows complete.  The rings are
+    updated in place and returned."""
+    requests = np.asarray(requests, dtype=np.int64)
+    positions = np.asarray(positions, dtype=np.int64)
+    for b in sorted(set(requests.tolist())):
+        sel = np.nonzero(requests == b)[0]
+        materialize(geo, weights, _f64(feats)[sel], positions[sel], int(frontiers[b]),
+                    rings=rings, request=b)
+    return rings
+
+
 def draft_round(geo, weights, rings, anchors: Sequence[int], frontiers: Sequence[int],
-                mask_id: int, n_masks: int, with_head: bool = True) -> Dict[str, np.ndarray]:
+                mask_id: int, n_masks: int, with_head: bool = True,
+                pending=None) -> Dict[str, np.ndarray]:
     """The whole proposal round for B independent requests.
     Returns x_layers [L, B, W, H], h [B, W, H] and, with the head, the mask rows'
     logits [B, K, V], argmax tokens [B, K] and top-2 gaps [B, K].
-    [DFlash-notes] proposal head: only the K mask columns are scored."""
+    [DFlash-notes] proposal head: only the K mask columns are scored.
+    pending = (feats, requests, positions): rows caught up into ``rings`` first
+    (catch_up)."""
+    if pending is not None:
+        catch_up(geo, weights, rings, frontiers, *pending)
     outs = [draft_request(geo, weights, rings, b, int(anchors[b]), int(frontiers[b]),
                           mask_id, n_masks) for b in range(len(anchors))]
     res = {"x_layers": np.stack([o["x_layers"] for o in outs], axis=1),

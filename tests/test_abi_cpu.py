@@ -97,26 +97,33 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     ws = 0x100000
     # B out of range
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 9, 7, 0x10000,
-                          None, None, None, ws, 1 << 30, None)
+                          None, None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"B must be" in L.bd_last_error()
     # K out of range
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 16, 0x10000,
-                          None, None, None, ws, 1 << 30, None)
+                          None, None, None, None, ws, 1 << 30, None)
     assert st == -1
     # misaligned weight
     w.layer[1].wq = 0x10008
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, None, ws, 1 << 30, None)
+                          None, None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"layer 1" in L.bd_last_error()
     w.layer[1].wq = 0x10000
     # more requests than ring rows
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 2, 7, 0x10000,
-                          None, None, None, ws, 1 << 30, None)
+                          None, None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"b_max" in L.bd_last_error()
     # misaligned workspace
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, None, ws + 16, 1 << 30, None)
+                          None, None, None, None, ws + 16, 1 << 30, None)
     assert st == -5
+    # pending catch-up rows: more than 16 per request, missing arrays, misaligned features
+    for pd in (B.Pending(0x10000, 0x10000, 0x10000, 17), B.Pending(None, 0x10000, 0x10000, 1),
+               B.Pending(0x10000, None, 0x10000, 1), B.Pending(0x10008, 0x10000, 0x10000, 1),
+               B.Pending(0x10000, 0x10000, 0x10000, -1)):
+        st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
+                              None, None, None, C.byref(pd), ws, 1 << 30, None)
+        assert st == -1 and b"pending" in L.bd_last_error()
     # head: rows out of range
     st = L.bd_lm_head_argmax(C.byref(c), C.byref(w), 0x10000, 121, 0x10000, None, ws, 1 << 30, None)
     assert st == -1
@@ -147,7 +154,7 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     # bridge on, bridge weights missing
     w.g_pred = None
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 7, 0x10000,
-                          None, None, None, ws, 1 << 30, None)
+                          None, None, None, None, ws, 1 << 30, None)
     assert st == -1 and b"bridge" in L.bd_last_error()
 
 
@@ -161,7 +168,7 @@ def test_unsupported_geometry_is_an_error_not_a_fallback(B):
         kv.k[l] = kv.v[l] = 0x10000
     kv.b_max = 1
     st = L.bd_draft_round(C.byref(c), C.byref(w), C.byref(kv), 0x10000, 0x10000, 1, 15, 0x10000,
-                          None, None, None, 0x100000, 1 << 34, None)
+                          None, None, None, None, 0x100000, 1 << 34, None)
     assert st == -2
 
 

@@ -1,0 +1,219 @@
+"""A round that catches up its pending context rows inside the call (bd_draft_round's
+`pending` argument), through the C ABI.
+
+Three comparisons on the same seeded inputs:
+  * against the oracle: the rings read back before the round, the oracle's catch_up of
+    the pending rows (R-catch), then its round -- hidden states max|gpu-ref|/max|ref|
+    <= 2e-2, tokens exact where the oracle's top-2 gap exceeds 1e-2, and the rings'
+    pending slots against the oracle's K/V with the same bound;
+  * against a separate bd_ctx_kv_materialize of the same rows followed by a plain
+    round on the GPU: the two paths do the same arithmetic in a different summation
+    order, so the stored K/V agree to within one bf16 step (2^-7 of the ring's
+    largest magnitude bounds one unit in the last place of any element) and the
+    hidden states to 1e-3;
+  * ragged pending counts (including requests with none), both ways the round runs the
+    catch-up (inside the block's Q/K/V product while block and pending rows fit one
+    128-column tile; otherwise as its own K/V product over every layer), and at the 27B
+    size 16 pending rows per request at B=1 (fused) and B=8 (separate product).
+Before the round every pending slot of every ring is overwritten with a sentinel, so a
+row the round failed to store would show up in the attention.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bdsynth
+import harness as Hn
+from oracle import dspine_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+SENTINEL = 3.0
+
+SMALL_BF16 = bdsynth.Workload(
+    name="small_bf16", hidden=512, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
+    ffn=1024, vocab=4000, n_target_layers=3, windows=(64, 0), code_width=128, msg_width=64,
+    batch=3, n_masks=15, dtype="bf16", ctx_min=40, ctx_max=300, full_capacity=320)
+
+SMALL_D64 = bdsynth.Workload(
+    name="small_d64_bf16", hidden=256, n_layers=2, n_q_heads=4, n_kv_heads=1, head_dim=64,
+    ffn=768, vocab=1000, n_target_layers=2, windows=(24, 24), code_width=64, msg_width=32,
+    batch=2, n_masks=7, dtype="bf16", ctx_min=5, ctx_max=90, full_capacity=0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_drafter_gb300 import builder
+    builder.build()
+
+
+class CatchUp:
+    """A case whose rings hold every request's live window except its newest n_pend[b]
+    rows, which are the round's pending rows."""
+
+    def __init__(self, geo, seed, n_pend, gen_device="cpu"):
+        self.case = Hn.Case(geo, seed=seed, max_ctx_rows=2048, gen_device=gen_device)
+        c = self.case
+        dev = "cuda"
+        self.n_pend = list(n_pend)
+        early = [F - n for F, n in zip(c.frontiers, self.n_pend)]
+        pf, pr, pp = [], [], []
+        for b in range(geo.batch):
+            lo, hi = c.request_rows(b)
+            f = c.features(b, lo, hi - lo).to(dev)  # one draw per request: rows lo .. F-1
+            n_early = early[b] - lo
+            if n_early > 0:
+                for c0 in range(0, n_early, 2048):
+                    n = min(2048, n_early - c0)
+                    c.sess.materialize(
+                        f[c0:c0 + n], torch.full((n,), b, dtype=torch.int32, device=dev),
+                        torch.arange(lo + c0, lo + c0 + n, dtype=torch.int64, device=dev),
+                        torch.tensor(early, dtype=torch.int64, device=dev))
+            if self.n_pend[b]:
+                pf.append(f[n_early:])
+                pr += [b] * self.n_pend[b]
+                pp += list(range(early[b], hi))
+        # pending rows in interleaved request order (the call must not depend on it)
+        order = np.argsort(np.array(pp) % 7, kind="stable")
+        feats = torch.cat(pf)[torch.as_tensor(order, device=dev)].contiguous()
+        self.req = torch.tensor(np.array(pr)[order], dtype=torch.int32, device=dev)
+        self.pos = torch.tensor(np.array(pp)[order], dtype=torch.int64, device=dev)
+        self.feats = feats
+        for l in range(geo.n_layers):
+            cap = geo.capacity(l)
+            for b, p in zip(self.req.tolist(), self.pos.tolist()):
+                c.sess.k[l][b, :, p % cap] = SENTINEL
+                c.sess.v[l][b, :, p % cap] = SENTINEL
+        torch.cuda.synchronize()
+        self.rings0 = [(k.clone(), v.clone()) for k, v in zip(c.sess.k, c.sess.v)]
+
+    def restore(self):
+        for (k0, v0), k, v in zip(self.rings0, self.case.sess.k, self.case.sess.v):
+            k.copy_(k0)
+            v.copy_(v0)
+        torch.cuda.synchronize()
+
+    def run_fused(self):
+        self.restore()
+        return self._round(pending=(self.feats, self.req, self.pos))
+
+    def run_separate(self):
+        self.restore()
+        c = self.case
+        c.sess.materialize(self.feats, self.req, self.pos,
+                           torch.tensor(c.frontiers, dtype=torch.int64, device="cuda"))
+        return self._round(pending=None)
+
+    def _round(self, pending):
+        c, g = self.case, self.case.geo
+        Bn, K = g.batch, g.n_masks
+        dev = "cuda"
+        anchors = torch.tensor(c.anchors, dtype=torch.int32, device=dev)
+        front = torch.tensor(c.frontiers, dtype=torch.int64, device=dev)
+        head_in, tokens, maxl, hidden = c.sess.alloc_outputs(Bn, K)
+        lo = torch.empty(g.n_layers, Bn * (K + 1), g.hidden, dtype=torch.float32, device=dev)
+        c.sess.round(anchors, front, K, head_in, hidden_out=hidden, layers_out=lo,
+                     pending=pending)
+        c.sess.head(head_in, tokens, maxl)
+        from block_drafter_gb300 import binding
+        binding.sync_status()
+        rings = [(k.clone(), v.clone()) for k, v in zip(c.sess.k, c.sess.v)]
+        return {"head_in": head_in, "tokens": tokens, "max_logit": maxl, "hidden": hidden,
+                "layers": lo, "rings": rings}
+
+    def oracle(self, requests=None):
+        c = self.case
+        reqs = list(range(c.geo.batch)) if requests is None else requests
+        rings = {"k": [Hn.np32(k0[reqs]) for k0, _ in self.rings0],
+                 "v": [Hn.np32(v0[reqs]) for _, v0 in self.rings0]}
+        # the oracle's rings are indexed by the position of the request in `reqs`
+        sel = [i for i, b in enumerate(self.req.tolist()) if b in reqs]
+        remap = {b: j for j, b in enumerate(reqs)}
+        pend = (Hn.np32(self.feats)[sel], [remap[self.req[i].item()] for i in sel],
+                self.pos.cpu().numpy()[sel])
+        wnp = Hn.weights_to_np(c.w_host)
+        ref = O.draft_round(c.geo, wnp, rings, [c.anchors[b] for b in reqs],
+                            [c.frontiers[b] for b in reqs], c.mask_id, c.geo.n_masks,
+                            pending=pend if sel else None)
+        return ref, rings, reqs
+
+    def pending_slots(self, l):
+        cap = self.case.geo.capacity(l)
+        return [(b, p % cap) for b, p in zip(self.req.tolist(), self.pos.tolist())]
+
+
+def check_against_oracle(cu, gpu, requests=None):
+    ref, rings, reqs = cu.oracle(requests)
+    rep = Hn.compare_round(cu.case, gpu, ref, requests=reqs, tol=TOL)
+    assert rep["ok"], rep
+    remap = {b: j for j, b in enumerate(reqs)}
+    worst = 0.0
+    for l in range(cu.case.geo.n_layers):
+        for b, s in cu.pending_slots(l):
+            if b not in remap:
+                continue
+            for key, i in (("k", 0), ("v", 1)):
+                got = Hn.np32(gpu["rings"][l][i][b][:, s])
+                want = rings[key][l][remap[b]][:, s]
+                worst = max(worst, Hn.rel_err(got, want))
+    assert worst <= TOL, worst
+    return rep, worst
+
+
+def check_against_separate(cu, fused, sep, h_tol=1e-3):
+    g = cu.case.geo
+    for l in range(g.n_layers):
+        for i in range(2):
+            a = Hn.np32(fused["rings"][l][i])
+            b = Hn.np32(sep["rings"][l][i])
+            scale = np.abs(b).max()
+            assert np.abs(a - b).max() <= scale * 2.0 ** -7, (l, i, np.abs(a - b).max(), scale)
+    assert Hn.rel_err(Hn.np32(fused["hidden"]), Hn.np32(sep["hidden"])) <= h_tol
+
+
+@pytest.mark.parametrize("geo,seed,n_pend", [
+    (SMALL_BF16, 0, (16, 5, 0)),
+    (SMALL_BF16, 2, (1, 16, 16)),
+    (SMALL_D64, 0, (16, 3)),
+    (bdsynth.TINY, 1, (8,)),
+    # T + n_pend > 128: the catch-up runs as its own K/V product inside the round
+    (SMALL_BF16.with_(batch=6), 5, (16, 16, 0, 16, 16, 3)),
+])
+def test_catch_up_round_matches_oracle(geo, seed, n_pend):
+    cu = CatchUp(geo, seed, n_pend)
+    fused = cu.run_fused()
+    rep, worst = check_against_oracle(cu, fused)
+    print(geo.name, seed, n_pend, rep, "ring err", worst)
+    sep = cu.run_separate()
+    check_against_separate(cu, fused, sep)
+
+
+def test_catch_up_round_with_no_pending_rows_is_the_plain_round():
+    cu = CatchUp(SMALL_BF16, 3, (2, 2, 2))
+    cu.restore()
+    a = cu._round(pending=None)
+    b = cu._round(pending=(cu.feats[:0], cu.req[:0], cu.pos[:0]))
+    assert torch.equal(a["hidden"], b["hidden"]) and torch.equal(a["tokens"], b["tokens"])
+
+
+def test_catch_up_round_is_deterministic():
+    cu = CatchUp(SMALL_BF16, 4, (16, 16, 16))
+    a = cu.run_fused()
+    b = cu.run_fused()
+    assert torch.equal(a["layers"], b["layers"]) and torch.equal(a["tokens"], b["tokens"])
+    for (ka, va), (kb, vb) in zip(a["rings"], b["rings"]):
+        assert torch.equal(ka, kb) and torch.equal(va, vb)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("geo,requests", [(bdsynth.DSPINE27B_B1, [0]),
+                                          (bdsynth.DSPINE27B_B8, [3])])
+def test_catch_up_round_full_size(geo, requests):
+    cu = CatchUp(geo, 0, (geo.W,) * geo.batch, gen_device="cuda")
+    fused = cu.run_fused()
+    sep = cu.run_separate()
+    check_against_separate(cu, fused, sep)
+    ta, tb = fused["tokens"].cpu().numpy(), sep["tokens"].cpu().numpy()
+    rep, worst = check_against_oracle(cu, fused, requests)
+    print(geo.name, rep, "ring err", worst, "token diff vs separate", int((ta != tb).sum()))

@@ -524,6 +524,62 @@ def test_round_requests_are_isolated_and_permutable():
     assert np.any(c["h"][1] != ab["h"][1])
 
 
+def _materialize_requests(g, w, feats, rows_of, frontiers):
+    """Rings for len(frontiers) requests, request b holding positions rows_of[b]."""
+    rings = {"k": [np.zeros((len(frontiers), g.n_kv_heads, g.capacity(l), g.head_dim))
+                   for l in range(g.n_layers)],
+             "v": [np.zeros((len(frontiers), g.n_kv_heads, g.capacity(l), g.head_dim))
+                   for l in range(g.n_layers)]}
+    for b, pos in enumerate(rows_of):
+        if len(pos):
+            O.materialize(g, w, feats[b][pos], pos, frontiers[b], rings=rings, request=b)
+    return rings
+
+
+def test_catch_up_round_equals_round_on_fully_materialised_context():
+    """[Frontier]: a round that first catches up its pending rows sees the same context
+    as a round whose context was materialised up to F beforehand (R-catch)."""
+    g = Geo(windows=(5, 0), full_capacity=32)
+    w = rand_weights(g, gate_bias=True)
+    F, n_pend = (9, 13), (3, 1)
+    feats = [rng.normal(0, 1, (f, g.n_target_layers * g.hidden)) for f in F]
+    full = _materialize_requests(g, w, feats, [np.arange(f) for f in F], F)
+    early = [f - n for f, n in zip(F, n_pend)]
+    part = _materialize_requests(g, w, feats, [np.arange(e) for e in early], early)
+    # pending rows in interleaved request order
+    rows = [(1, 12), (0, 6), (0, 7), (0, 8)]
+    pf = np.stack([feats[b][p] for b, p in rows])
+    pend = (pf, [b for b, _ in rows], [p for _, p in rows])
+    a = O.draft_round(g, w, full, [5, 17], list(F), 0, 5)
+    b = O.draft_round(g, w, part, [5, 17], list(F), 0, 5, pending=pend)
+    for key in ("x_layers", "h", "logits"):
+        np.testing.assert_allclose(b[key], a[key], rtol=1e-11, atol=1e-12)
+    np.testing.assert_array_equal(a["tokens"], b["tokens"])
+    # the caught-up rings hold the same live interval as the fully materialised ones
+    for l in range(g.n_layers):
+        cap = g.capacity(l)
+        for r in range(2):
+            lo, hi = O.ring_live_interval(F[r], cap)
+            sl = np.arange(lo, hi) % cap
+            for key in ("k", "v"):
+                np.testing.assert_allclose(part[key][l][r][:, sl], full[key][l][r][:, sl],
+                                           rtol=1e-12, atol=1e-13)
+
+
+def test_catch_up_touches_only_its_requests():
+    g = Geo(windows=(4, 0), full_capacity=32)
+    w = rand_weights(g)
+    F = (10, 11)
+    rings = rand_rings(g, 2, F)
+    feats = rng.normal(0, 1, (2, g.n_target_layers * g.hidden))
+    base = O.draft_round(g, w, {k: [a.copy() for a in v] for k, v in rings.items()},
+                         [5, 17], list(F), 0, 5)
+    got = O.draft_round(g, w, rings, [5, 17], list(F), 0, 5,
+                        pending=(feats, [1, 1], [9, 10]))
+    np.testing.assert_array_equal(got["h"][0], base["h"][0])
+    assert np.any(got["h"][1] != base["h"][1])
+
+
 def test_round_with_no_layer_updates_is_embedding_nearest_row():
     # W_o = 0, W_down = 0, W_write = 0: every layer is the identity, so the final state is
     # the embedding rows and each mask row's proposal is argmax_v E_v . rmsnorm(E_MASK).

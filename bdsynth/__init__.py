@@ -13,6 +13,9 @@ Draw recipe (the same for every workload):
     every activation towards zero and make the argmax comparison vacuous);
   * token-code table rows are N(0, 1) rows scaled to unit L2 norm before rounding
     (the DSpine pages build the table from normalised vectors);
+  * DFlash2 convolution: base coefficients of the current tap 1 + N(0, 0.1), of the
+    previous tap N(0, 0.1); delta projections N(0, 0.002) (the pages give no
+    initialisation; these keep every coefficient near its base at H = 5120);
   * captured target residuals ~ N(0, 1) times a per-captured-layer scale ~ U[0.5, 4];
   * anchor ids ~ U[0, V) with the MASK id excluded; frontiers as each workload states.
 """
@@ -54,6 +57,7 @@ class Workload:
     ctx_max: int = 0
     full_capacity: int = 0    # ring capacity of full-context layers (>= ctx_max)
     block_causal: bool = False
+    conv_group: int = 0       # DFlash2 grouped convolution group width (0: none)
 
     @property
     def W(self) -> int:
@@ -91,6 +95,13 @@ DSPINE27B_B1 = Workload(
 
 DSPINE27B_B8 = DSPINE27B_B1.with_(name="dspine_b16_27b_b8", batch=8, ctx_min=512, ctx_max=16384)
 
+# DFlash2 at the same 27B geometry: the dynamic grouped convolution (two taps, group
+# width 16) around both branches, no DSpine bridge.
+DFLASH2_27B_B1 = DSPINE27B_B1.with_(name="dflash2_27b_b1", code_width=0, msg_width=0,
+                                    conv_group=16)
+DFLASH2_27B_B8 = DFLASH2_27B_B1.with_(name="dflash2_27b_b8", batch=8, ctx_min=512,
+                                      ctx_max=16384)
+
 DFLASH35B_B8 = Workload(
     name="dflash_35b_a3b_b8", hidden=2048, n_layers=6, n_q_heads=32, n_kv_heads=8,
     head_dim=128, ffn=6144, vocab=151936, n_target_layers=8,
@@ -99,7 +110,8 @@ DFLASH35B_B8 = Workload(
     full_capacity=32768)
 
 WORKLOADS: Dict[str, Workload] = {w.name: w for w in
-                                  (TINY, CTX27B, DSPINE27B_B1, DSPINE27B_B8, DFLASH35B_B8)}
+                                  (TINY, CTX27B, DSPINE27B_B1, DSPINE27B_B8, DFLASH2_27B_B1,
+                                   DFLASH2_27B_B8, DFLASH35B_B8)}
 
 
 def torch_dtype(dt: str) -> torch.dtype:
@@ -142,7 +154,10 @@ IDX_ANCHORS, IDX_MASK_ID, IDX_FRONTIER, IDX_FEAT_SCALE = 9, 10, 11, 12
 IDX_FEATURES = 10_000          # + stream (one independent draw per request)
 LAYER_BASE = 100
 LAYER_SLOTS = ("in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "post_norm",
-               "w_gate", "w_up", "w_down", "r_read", "w_write")
+               "w_gate", "w_up", "w_down", "r_read", "w_write", "conv_delta_a", "conv_base_a",
+               "conv_delta_m", "conv_base_m")
+CONV_BASE_SLOTS = ("conv_base_a", "conv_base_m")
+CONV_DELTA_STD = 0.002  # delta ~ N(0, 0.14) per group at H = 5120
 NORM_SLOTS = ("in_norm", "q_norm", "k_norm", "post_norm")
 
 
@@ -157,6 +172,10 @@ def layer_shapes(w: Workload) -> Dict[str, tuple]:
     if w.code_width > 0:
         s["r_read"] = (w.code_width, H)
         s["w_write"] = (H, w.msg_width)
+    if w.conv_group > 0:
+        for br in ("a", "m"):
+            s["conv_delta_" + br] = (4 * H // w.conv_group, H)
+            s["conv_base_" + br] = (2, 2, H)
     return s
 
 
@@ -204,6 +223,13 @@ def make_weights(w: Workload, seed: int = 0, device="cpu", *, gate_bias: bool = 
                                  dtype=dt)
             elif name == "w_write" and zero_write:
                 d[name] = torch.zeros(shapes[name], device=device, dtype=dt)
+            elif name in CONV_BASE_SLOTS:
+                b = normal(shapes[name], seed, idx, std=0.1, device=device)
+                b[:, 0] += 1.0
+                d[name] = b.to(dt)
+            elif name.startswith("conv_delta"):
+                d[name] = normal(shapes[name], seed, idx, std=CONV_DELTA_STD, device=device,
+                                 dtype=dt)
             else:
                 d[name] = normal(shapes[name], seed, idx, std=0.02, device=device, dtype=dt)
         out["layers"].append(d)

@@ -345,6 +345,28 @@ def separate_catch_up(st: State, args) -> dict:
     return {"materialize_us": mat, "step_us": step}
 
 
+def dflash2_lines(args, world, hbm) -> dict:
+    """The DFlash2 variant at the same 27B geometry (dynamic grouped convolution around
+    both branches, no DSpine bridge): the same step (round with the fused catch-up + LM
+    head) at B=1 and B=8."""
+    out = {}
+    w = None
+    for geo in (bdsynth.DFLASH2_27B_B1, bdsynth.DFLASH2_27B_B8):
+        st = State(geo, args.seed, weights=w)
+        w = st.w
+        ms, per = time_graphs(st, args.steps, args.warmup, world)
+        ms = max_over_ranks(ms, world)
+        by = st.bytes_per_step()
+        gbs = by["total"] / (ms * 1e-3) / 1e9
+        out["b%d" % geo.batch] = {
+            "workload": geo.name, "us_per_step": 1000.0 * ms, "rounds_per_s": world * 1000.0 / ms,
+            "breakdown_us": {k: 1000.0 * v for k, v in per.items()},
+            "round_only": round_only(st, args), "achieved_step_gbs": gbs,
+            "frac_of_measured_hbm": gbs / hbm, "algorithmic_bytes_per_step": by}
+        del st
+    return out
+
+
 def refine_us(st: State, args) -> float:
     """Device time of the last-write refinement (tables + walk) after a round that exported
     its tail state and a top-16 head that produced the candidates."""
@@ -581,6 +603,8 @@ def main():
                       "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup),
                       "refine_tail_us": refine_us(st8, args)}
         del st8
+    if not args.no_b8 and args.workload == "b1":
+        line["dflash2"] = dflash2_lines(args, world, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         import numpy as np
         wh = host_weights(st.w)

@@ -43,11 +43,12 @@ class Config(C.Structure):
                 ("window", C.c_int * MAX_LAYERS), ("ring_capacity", C.c_int * MAX_LAYERS),
                 ("eps", C.c_float), ("rope_theta", C.c_float), ("mask_token_id", C.c_int),
                 ("code_width", C.c_int), ("msg_width", C.c_int), ("block_mask", C.c_int),
-                ("dtype", C.c_int)]
+                ("dtype", C.c_int), ("conv_group", C.c_int)]
 
 
 LAYER_FIELDS = ("in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "post_norm", "w_gate",
-                "w_up", "w_down", "r_read", "w_write")
+                "w_up", "w_down", "r_read", "w_write", "conv_delta_a", "conv_base_a",
+                "conv_delta_m", "conv_base_m")
 
 
 class LayerWeights(C.Structure):
@@ -136,7 +137,7 @@ def _stream(stream) -> Optional[int]:
 def make_config(*, hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab,
                 n_target_layers, windows: Sequence[int], ring_capacity: Sequence[int], eps,
                 rope_theta, mask_token_id, code_width=0, msg_width=0, block_causal=False,
-                dtype=BF16) -> Config:
+                dtype=BF16, conv_group=0) -> Config:
     c = Config()
     c.hidden, c.n_layers, c.n_q_heads, c.n_kv_heads = hidden, n_layers, n_q_heads, n_kv_heads
     c.head_dim, c.ffn, c.vocab, c.n_target_layers = head_dim, ffn, vocab, n_target_layers
@@ -147,6 +148,7 @@ def make_config(*, hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab
     c.code_width, c.msg_width = code_width, msg_width
     c.block_mask = CAUSAL if block_causal else BIDIRECTIONAL
     c.dtype = dtype
+    c.conv_group = conv_group
     return c
 
 

@@ -79,6 +79,8 @@ std::string check_config(const bd_config *c) {
   if ((c->code_width > 0) != (c->msg_width > 0)) return "code_width and msg_width must both be 0 or both > 0";
   if (c->code_width > 0 && (!k_ok(c->code_width) || !k_ok(c->msg_width)))
     return "code_width*elem and msg_width*elem must be multiples of 16 bytes";
+  if (c->conv_group < 0 || (c->conv_group > 0 && (c->conv_group % 4 != 0 || c->hidden % c->conv_group != 0)))
+    return "conv_group must be 0 or a multiple of 4 dividing hidden";
   for (int l = 0; l < c->n_layers; ++l) {
     if (c->window[l] < 0) return "window must be >= 0";
     if (c->ring_capacity[l] <= 0) return "ring_capacity must be > 0";
@@ -111,6 +113,9 @@ std::string check_weights(const bd_config *c, const bd_weights *w) {
       return "layer " + std::to_string(l) + ": a weight pointer is NULL or not 16-byte aligned";
     if (c->code_width > 0 && (!chk(L.r_read) || !chk(L.w_write)))
       return "layer " + std::to_string(l) + ": r_read / w_write NULL or misaligned";
+    if (c->conv_group > 0 &&
+        (!chk(L.conv_delta_a) || !chk(L.conv_base_a) || !chk(L.conv_delta_m) || !chk(L.conv_base_m)))
+      return "layer " + std::to_string(l) + ": convolution weights NULL or misaligned";
   }
   return {};
 }
@@ -180,6 +185,7 @@ struct RoundWs {
   GemmWs g;
   unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
   float *x, *z, *pre, *r, *part_o, *qkv_raw, *feat, *kv_raw;
+  float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
   float2 *rope, *part_ml;
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
@@ -197,6 +203,7 @@ size_t round_max_tiles(const bd_config *c, int T, int Tq) {
     o = std::max(o, tiles_of(c->code_width, 128));
     o = std::max(o, 3 * tiles_of(c->msg_width, 128));
   }
+  if (c->conv_group > 0) t = std::max(t, tiles_of(4 * c->hidden / c->conv_group, 128) * n_tiles_of(Tq));
   return std::max(t, o * n_tiles_of(T));
 }
 
@@ -244,6 +251,15 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_
   }
   w.part_o = cv.take<float>(po);
   w.part_ml = cv.take<float2>(pm);
+  if (c->conv_group > 0) {
+    const size_t nd = static_cast<size_t>(4) * H / c->conv_group;
+    w.cdelta_a = cv.take<float>(static_cast<size_t>(Tq) * nd);
+    w.cdelta_m = cv.take<float>(static_cast<size_t>(T) * nd);
+    w.cz = cv.take<float>(static_cast<size_t>(T) * H);
+    w.cn = cv.take<float>(static_cast<size_t>(T) * H);
+  } else {
+    w.cdelta_a = w.cdelta_m = w.cz = w.cn = nullptr;
+  }
   if (c->code_width > 0) {
     w.r = cv.take<float>(T);
     w.z = cv.take<float>(static_cast<size_t>(T) * c->code_width);
@@ -598,12 +614,43 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       if (st != BD_OK) return st;
     }
   }
+  // DFlash2 convolution: each branch's delta = W_delta X comes from its normalised input;
+  // Conv_0 prepares that input for the branch's products, and Conv_1 of the branch output
+  // is added to the residual by the next row norm (ConvFinish), which writes x back.
+  const bool conv = cfg->conv_group > 0;
+  const int gw = cfg->conv_group, ND = conv ? 4 * H / gw : 0;
+  const ConvFinish no_fin{nullptr, nullptr, nullptr, 0};
+  ConvFinish fin = no_fin;  // the previous layer's MLP finish, not yet added to x
+  int copy_layer = -1;      // layer whose layers_out copy waits for that finish
+  auto delta_gemm = [&](const void *xin, int rows, const void *wd, size_t packed_off,
+                        float *out) -> std::string {
+    GemmPlan p = make_plan(cfg, xin, rows, H);
+    p.split = split;
+    add_w(p, wd, ND, pk, packed_off);
+    p.args.epi = EPI_STORE_F32;
+    p.args.out_f32 = out;
+    p.args.ld_out = ND;
+    return launch_gemm(p, sc, s);
+  };
+  auto copy_layer_out = [&](int l) -> std::string {
+    return launch_copy_f32(rw.x, layers_out + static_cast<size_t>(l) * T * H,
+                           static_cast<size_t>(T) * H, s);
+  };
   for (int l = 0; l < cfg->n_layers; ++l) {
     const bd_layer_weights &L = w->layer[l];
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE.  The pending context rows ride
     // along in the same product: their K/V (S2) use the same W_k, W_v tiles.
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xq, nullptr,
-                          nullptr, nullptr, W, lo_q, s));
+                          conv ? rw.cn : nullptr, nullptr, W, lo_q, s, fin));
+    fin = no_fin;
+    if (copy_layer >= 0) {
+      BD_TRY(copy_layer_out(copy_layer));
+      copy_layer = -1;
+    }
+    if (conv) {  // delta_a (over every xq row, so the split layout matches), then Conv_0(n)
+      BD_TRY(delta_gemm(rw.xq, Tq, L.conv_delta_a, PL.conv_a[l], rw.cdelta_a));
+      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_a, L.conv_base_a, T, H, gw, W, rw.xq, lo_q, s));
+    }
     {
       GemmPlan p = make_plan(cfg, rw.xq, Tq, H);
       p.split = split;
@@ -675,19 +722,25 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.out_lo = lo(QD);
       BD_TRY(launch_attention(a, dt, s));
     }
-    // S6: y = x + W_o a (in place)
+    // S6: y = x + W_o a (in place; with the convolution W_o a goes to cz and the next
+    // row norm adds Conv_1 of it)
     {
       GemmPlan p = make_plan(cfg, rw.att, T, QD);
       p.split = split;
       add_w(p, L.wo, H, pk, PL.wo[l]);
-      p.args.epi = EPI_RESID_F32;
-      p.args.out_f32 = rw.x;
+      p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
+      p.args.out_f32 = conv ? rw.cz : rw.x;
       p.args.ld_out = H;
       BD_TRY(launch_gemm(p, sc, s));
     }
     // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m)
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.post_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
-                          nullptr, nullptr, W, lo(H), s));
+                          conv ? rw.cn : nullptr, nullptr, W, lo(H), s,
+                          conv ? ConvFinish{rw.cz, rw.cdelta_a, L.conv_base_a, gw} : no_fin));
+    if (conv) {  // delta_m, then Conv_0(m)
+      BD_TRY(delta_gemm(rw.xn, T, L.conv_delta_m, PL.conv_m[l], rw.cdelta_m));
+      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_m, L.conv_base_m, T, H, gw, W, rw.xn, lo(H), s));
+    }
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
       p.split = split;
@@ -704,16 +757,18 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
       p.split = split;
       add_w(p, L.w_down, H, pk, PL.w_down[l]);
-      p.args.epi = EPI_RESID_F32;
-      p.args.out_f32 = rw.x;
+      p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
+      p.args.out_f32 = conv ? rw.cz : rw.x;
       p.args.ld_out = H;
       BD_TRY(launch_gemm(p, sc, s));
     }
+    if (conv) fin = ConvFinish{rw.cz, rw.cdelta_m, L.conv_base_m, gw};
     if (cfg->code_width > 0) {
       const int Rc = cfg->code_width, Mc = cfg->msg_width;
       // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
       BD_TRY(launch_rownorm(dt, rw.x, T, H, nullptr, cfg->eps, NORM_BRIDGE, rw.xn, rw.r, nullptr,
-                            nullptr, W, lo(H), s));
+                            nullptr, W, lo(H), s, fin));
+      fin = no_fin;
       {
         GemmPlan p = make_plan(cfg, rw.xn, T, H);
         p.split = split;
@@ -755,12 +810,16 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         BD_TRY(launch_gemm(p, sc, s));
       }
     }
-    if (layers_out)
-      BD_TRY(launch_copy_f32(rw.x, layers_out + static_cast<size_t>(l) * T * H,
-                             static_cast<size_t>(T) * H, s));
+    if (layers_out) {
+      if (fin.z)
+        copy_layer = l;  // after the next row norm has added the MLP finish
+      else
+        BD_TRY(copy_layer_out(l));
+    }
   }
   BD_TRY(launch_rownorm(dt, rw.x, T, H, w->final_norm, cfg->eps, NORM_FINAL, nullptr, nullptr,
-                        hidden_out, head_in, W, 0, s));
+                        hidden_out, head_in, W, 0, s, fin));
+  if (copy_layer >= 0) BD_TRY(copy_layer_out(copy_layer));
   return BD_OK;
 }
 

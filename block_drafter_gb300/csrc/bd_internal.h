@@ -126,7 +126,7 @@ struct PackedLayout {
   size_t w_feature, head, g_recv, g_pred, a_val;
   size_t wq[BD_MAX_LAYERS], wk[BD_MAX_LAYERS], wv[BD_MAX_LAYERS], wo[BD_MAX_LAYERS];
   size_t gate_up[BD_MAX_LAYERS], w_down[BD_MAX_LAYERS], r_read[BD_MAX_LAYERS],
-      w_write[BD_MAX_LAYERS];
+      w_write[BD_MAX_LAYERS], conv_a[BD_MAX_LAYERS], conv_m[BD_MAX_LAYERS];
   size_t total;
 };
 PackedLayout packed_layout(const bd_config *c);

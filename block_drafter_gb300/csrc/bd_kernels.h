@@ -61,10 +61,26 @@ enum NormMode : int {
   NORM_FINAL = 2,   // plain, plus fp32 copy and the mask-row copy for the LM head
   NORM_CTX = 3      // plain; the lo part is written as zero (c_t enters products as bf16)
 };
-// lo_off != 0: also write the rounding residual y - hi at out + lo_off (split activation).
-std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain,
+// DFlash2 branch finish folded into the next row norm: before normalising row i, the
+// kernel adds Conv_1(z)[i] (side-1 grouped convolution of the branch output z with the
+// branch's delta) to x and writes the updated row back.  z == null: no finish.
+struct ConvFinish {
+  const float *z;      // [rows][H] branch output
+  const float *delta;  // [rows][2 sides][2 taps][H / gw] (side 1 used)
+  const void *base;    // [2 sides][2 taps][H], config dtype (side 1 used)
+  int gw;              // group width (a multiple of 4 dividing H)
+};
+// Row norm of x (one CTA per row).  lo_off != 0: also write the rounding residual y - hi
+// at out + lo_off (split activation).  f32_out: an fp32 copy of y, or null.
+std::string launch_rownorm(int dtype, float *x, int rows, int H, const void *gain,
                            float eps, int mode, void *out, float *r_out, float *f32_out,
-                           float *head_out, int W, size_t lo_off, cudaStream_t s);
+                           float *head_out, int W, size_t lo_off, cudaStream_t s,
+                           const ConvFinish &cf = ConvFinish{nullptr, nullptr, nullptr, 0});
+// DFlash2 branch input: out = Conv_0(X) (side-0 grouped convolution of the normalised
+// branch input X [rows][H] fp32 with delta [rows][2][2][H/gw]), split when lo_off != 0.
+std::string launch_conv_prepare(int dtype, const float *X, const float *delta, const void *base,
+                                int rows, int H, int gw, int W, void *out, size_t lo_off,
+                                cudaStream_t s);
 // fp32 -> bf16 hi (dst) and lo (dst + lo_off) of n elements.
 std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,
                               cudaStream_t s);

@@ -39,6 +39,10 @@ PackedLayout packed_layout(const bd_config *c) {
       L.r_read[l] = take(packed_matrix_bytes(c->code_width, H, e, false));
       L.w_write[l] = take(packed_matrix_bytes(H, c->msg_width, e, false));
     }
+    if (c->conv_group > 0) {
+      L.conv_a[l] = take(packed_matrix_bytes(4 * H / c->conv_group, H, e, false));
+      L.conv_m[l] = take(packed_matrix_bytes(4 * H / c->conv_group, H, e, false));
+    }
   }
   L.total = off;
   return L;
@@ -108,6 +112,10 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
     if (c->code_width > 0) {
       BD_PACK(W.r_read, nullptr, c->code_width, H, false, L.r_read[l]);
       BD_PACK(W.w_write, nullptr, H, c->msg_width, false, L.w_write[l]);
+    }
+    if (c->conv_group > 0) {
+      BD_PACK(W.conv_delta_a, nullptr, 4 * H / c->conv_group, H, false, L.conv_a[l]);
+      BD_PACK(W.conv_delta_m, nullptr, 4 * H / c->conv_group, H, false, L.conv_m[l]);
     }
   }
 #undef BD_PACK

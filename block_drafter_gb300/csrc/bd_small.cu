@@ -106,29 +106,66 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 
 // the sum-of-squares and the output pass (float4 loads, all issued before the reduction).
 constexpr int kNormVec = 8;
 
+// DFlash2 grouped convolution of one block row (channels 4*i4 .. 4*i4+3, one group since
+// the group width is a multiple of 4): (base[side,0] + delta[row,side,0,g]) * X[row]
+// + [i >= 1] (base[side,1] + delta[row,side,1,g]) * X[row - 1].  X rows are H wide,
+// delta rows hold [2 sides][2 taps][G groups].
 template <typename T>
-__global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, const T *gain,
-                                                      float eps, int mode, T *out, float *r_out,
+__device__ __forceinline__ float4 conv_row4(const float *X, const float *delta, const T *base,
+                                            int H, int gw, int side, int row, bool has_prev, int i4) {
+  const int G = H / gw, g = (4 * i4) / gw;
+  const float *d = delta + static_cast<size_t>(row) * 4 * G + side * 2 * G;
+  const float dc = d[g], dp = d[G + g];
+  const float4 bc = load4<T>(base + static_cast<size_t>(side) * 2 * H, i4);
+  const float4 x = reinterpret_cast<const float4 *>(X + static_cast<size_t>(row) * H)[i4];
+  float4 o = make_float4((bc.x + dc) * x.x, (bc.y + dc) * x.y, (bc.z + dc) * x.z, (bc.w + dc) * x.w);
+  if (has_prev) {
+    const float4 bp = load4<T>(base + static_cast<size_t>(side) * 2 * H + H, i4);
+    const float4 xp = reinterpret_cast<const float4 *>(X + static_cast<size_t>(row - 1) * H)[i4];
+    o.x += (bp.x + dp) * xp.x;
+    o.y += (bp.y + dp) * xp.y;
+    o.z += (bp.z + dp) * xp.z;
+    o.w += (bp.w + dp) * xp.w;
+  }
+  return o;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *gain, float eps,
+                                                      int mode, T *out, float *r_out,
                                                       float *f32_out, float *head_out, int W,
-                                                      size_t lo_off) {
+                                                      size_t lo_off, ConvFinish cf) {
   __shared__ float red[32];
   const int row = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const float *xr = x + static_cast<size_t>(row) * H;
+  float *xr = x + static_cast<size_t>(row) * H;
   const int H4 = H / 4;
+  const bool fin = cf.z != nullptr;
+  const bool has_prev = (row % W) != 0;
+  // x (+ the branch output's side-1 convolution, written back: the residual update)
+  auto load_x = [&](int i4) -> float4 {
+    float4 t = reinterpret_cast<const float4 *>(xr)[i4];
+    if (fin) {
+      const float4 c = conv_row4<T>(cf.z, cf.delta, static_cast<const T *>(cf.base), H, cf.gw, 1,
+                                    row, has_prev, i4);
+      t = make_float4(t.x + c.x, t.y + c.y, t.z + c.z, t.w + c.w);
+      reinterpret_cast<float4 *>(xr)[i4] = t;
+    }
+    return t;
+  };
   float4 xv[kNormVec];
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < kNormVec; ++k) {
     const int i4 = threadIdx.x + k * blockDim.x;
-    xv[k] = i4 < H4 ? reinterpret_cast<const float4 *>(xr)[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    xv[k] = i4 < H4 ? load_x(i4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int k = 0; k < kNormVec; ++k)
     ss += xv[k].x * xv[k].x + xv[k].y * xv[k].y + xv[k].z * xv[k].z + xv[k].w * xv[k].w;
   for (int i4 = threadIdx.x + kNormVec * blockDim.x; i4 < H4; i4 += blockDim.x) {
-    const float4 t = reinterpret_cast<const float4 *>(xr)[i4];
+    const float4 t = load_x(i4);  // written back: the output pass re-reads x
     ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
   }
   ss = block_sum(ss, red);
@@ -145,7 +182,7 @@ __global__ void __launch_bounds__(256) rownorm_kernel(const float *x, int H, con
   float *hrow = nullptr;
   if (mode == NORM_FINAL && head_out != nullptr && i > 0)
     hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
-  float *frow = (mode == NORM_FINAL && f32_out) ? f32_out + static_cast<size_t>(row) * H : nullptr;
+  float *frow = f32_out ? f32_out + static_cast<size_t>(row) * H : nullptr;
   auto emit = [&](int i4, float4 t) {
     float4 y = make_float4(t.x * scale, t.y * scale, t.z * scale, t.w * scale);
     if (mode != NORM_BRIDGE) {
@@ -182,6 +219,28 @@ __device__ __forceinline__ void store_split(T *p, size_t i, size_t lo_off, float
   const T h = from_f<T>(v);
   p[i] = h;
   if (lo_off) p[lo_off + i] = from_f<T>(v - to_f<T>(h));
+}
+
+// DFlash2 branch input: out[row] = Conv_0(X)[row] (the side-0 convolution of the
+// normalised branch input), as a split pair when lo_off != 0.  One CTA per block row.
+template <typename T>
+__global__ void __launch_bounds__(256) conv_prepare_kernel(const float *X, const float *delta,
+                                                           const T *base, int H, int gw, int W,
+                                                           T *out, size_t lo_off) {
+  const int row = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const bool has_prev = (row % W) != 0;
+  T *o = out + static_cast<size_t>(row) * H;
+  for (int i4 = threadIdx.x; i4 < H / 4; i4 += blockDim.x) {
+    const float4 y = conv_row4<T>(X, delta, base, H, gw, 0, row, has_prev, i4);
+    store4<T>(o, i4, y);
+    if (lo_off) {
+      const float4 h = make_float4(to_f<T>(from_f<T>(y.x)), to_f<T>(from_f<T>(y.y)),
+                                   to_f<T>(from_f<T>(y.z)), to_f<T>(from_f<T>(y.w)));
+      store4<T>(o + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+    }
+  }
 }
 
 // One warp per (row, head).  Lane l holds elements [l*E, l*E + E) of the head (E = D/32);
@@ -766,19 +825,33 @@ std::string launch_zero(ZeroSpan z, cudaStream_t s) {
                                 dim3(256), 0, s, z));
 }
 
-std::string launch_rownorm(int dtype, const float *x, int rows, int H, const void *gain, float eps,
+std::string launch_rownorm(int dtype, float *x, int rows, int H, const void *gain, float eps,
                            int mode, void *out, float *r_out, float *f32_out, float *head_out, int W,
-                           size_t lo_off, cudaStream_t s) {
+                           size_t lo_off, cudaStream_t s, const ConvFinish &cf) {
   cudaError_t e;
   if (dtype == 0)
     e = launch_pdl(rownorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, x, H,
                    static_cast<const __nv_bfloat16 *>(gain), eps, mode,
-                   static_cast<__nv_bfloat16 *>(out), r_out, f32_out, head_out, W, lo_off);
+                   static_cast<__nv_bfloat16 *>(out), r_out, f32_out, head_out, W, lo_off, cf);
   else
     e = launch_pdl(rownorm_kernel<float>, dim3(rows), dim3(256), 0, s, x, H,
                    static_cast<const float *>(gain), eps, mode, static_cast<float *>(out), r_out,
-                   f32_out, head_out, W, lo_off);
+                   f32_out, head_out, W, lo_off, cf);
   return err("rownorm", e);
+}
+
+std::string launch_conv_prepare(int dtype, const float *X, const float *delta, const void *base,
+                                int rows, int H, int gw, int W, void *out, size_t lo_off,
+                                cudaStream_t s) {
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_pdl(conv_prepare_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, X, delta,
+                   static_cast<const __nv_bfloat16 *>(base), H, gw, W,
+                   static_cast<__nv_bfloat16 *>(out), lo_off);
+  else
+    e = launch_pdl(conv_prepare_kernel<float>, dim3(rows), dim3(256), 0, s, X, delta,
+                   static_cast<const float *>(base), H, gw, W, static_cast<float *>(out), lo_off);
+  return err("conv prepare", e);
 }
 
 std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,

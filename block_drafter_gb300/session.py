@@ -23,7 +23,7 @@ def config_of(geo, mask_id: int) -> B.Config:
         ring_capacity=[geo.capacity(l) for l in range(geo.n_layers)], eps=geo.eps,
         rope_theta=geo.rope_theta, mask_token_id=mask_id, code_width=geo.code_width,
         msg_width=geo.msg_width, block_causal=geo.block_causal,
-        dtype=B.BF16 if geo.dtype == "bf16" else B.F32)
+        dtype=B.BF16 if geo.dtype == "bf16" else B.F32, conv_group=geo.conv_group)
 
 
 class DraftSession:

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 5
+#define BD_ABI_VERSION 6
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -74,6 +74,8 @@ typedef struct {
   int msg_width;                     /* Mc                                                 */
   int block_mask;                    /* bd_block_mask                                      */
   int dtype;                         /* bd_dtype of weights, rings and activations         */
+  int conv_group;                    /* DFlash2 dynamic grouped convolution: group width   */
+                                     /* gw (a multiple of 4 dividing H), or 0 for none     */
 } bd_config;
 
 /* Per-layer weights (dev, caller-owned, row-major [out, in], config dtype). */
@@ -91,6 +93,11 @@ typedef struct {
   const void *w_down;    /* [H, I]                                                       */
   const void *r_read;    /* [Rc, H]  DSpine per-layer code read R_l (bridge only)        */
   const void *w_write;   /* [H, Mc]  DSpine per-layer write W_l (bridge only)            */
+  /* DFlash2 convolution (conv_group = gw > 0 only): per branch (a = attention, m = MLP)
+   * the delta projection [4*H/gw, H], rows ordered (side, tap, group), and the base
+   * coefficients [2 sides][2 taps][H]. */
+  const void *conv_delta_a, *conv_base_a;
+  const void *conv_delta_m, *conv_base_m;
 } bd_layer_weights;
 
 typedef struct {
@@ -209,6 +216,12 @@ typedef struct {
  *   request's ring context and its own block -> W_o + residual -> rmsnorm -> SwiGLU +
  *   residual -> [bridge read, anchor code, gated predecessor message, RMS-scaled write;
  *   the anchor row receives no write].  Then final plain_rmsnorm.
+ *   With conv_group = gw > 0 (DFlash2, [DFlash-notes] dynamic grouped convolution) each
+ *   branch works on Conv_0 of its normalised input X and adds Conv_1 of its output, both
+ *   with delta = W_delta X as [2 sides][2 taps][H/gw] per row:
+ *     Conv_s(Y)[i, c] = (base[s,0,c] + delta[i,s,0,c/gw]) Y[i, c]
+ *                       + [i >= 1] (base[s,1,c] + delta[i,s,1,c/gw]) Y[i-1, c]
+ *   over the block rows i of each request (no history across requests or rounds).
  *
  *   anchor_ids  dev int32 [B]  anchor token a_b (< vocab)
  *   frontier    dev int64 [B]  committed context length F_b >= 1 of request b; ring row b

@@ -25,6 +25,8 @@ Sources (cited by page title and section throughout):
                   proposal row; the fallback path scores with the BF16 vocabulary head).
   [Tail]          "DSpine 完全拆解", section "前驱条件解码与 transition cache"
                   (last-write refinement, the K x K transition table, greedy walk).
+  [Conv]          "dflash.md", the DFlash2 paragraphs on the dynamic grouped convolution
+                  around the attention and MLP branches and the per-layer DFlash2 equations.
   [Frontier]      "dflash.md", the paragraph on the processed-token frontier F: committed
                   target feature rows that the drafter has not yet converted are
                   materialised before the block is proposed, so the context reaches F.
@@ -48,6 +50,13 @@ Readings taken where the pages are schematic or garbled (each also listed in DES
   R-catch  a round given pending rows first materialises them exactly as a separate
            materialisation would (each request's rows into its own rings, stored only
            inside the final live window of the frontier they complete), then drafts.
+  R-conv   DFlash2 grouped convolution (layers with conv weights): per branch,
+           delta = W_delta X reshaped [W, 2 sides, 2 taps, H/gw groups] from the branch's
+           normalised input X; Conv_s(X)[i, c] = (base[s,0,c] + delta[i,s,0,c//gw]) X[i, c]
+           + [i >= 1] (base[s,1,c] + delta[i,s,1,c//gw]) X[i-1, c] with i the block row
+           (row 0, the anchor, has no preceding tap; no history across requests or
+           rounds).  Side 0 prepares the branch input, side 1 finishes the branch output
+           with the same delta; base is stored [2 sides][2 taps][H].
   R-topk   a row's k candidates are its k largest exact logits over the whole
            vocabulary, by descending score; equal scores keep the lower token id first.
   R-tail   last-write refinement of block row i with predecessor token s: the last
@@ -276,6 +285,27 @@ def sigmoid(x):
     return 1.0 / (1.0 + np.exp(-x))
 
 
+def conv_delta(X, w_delta) -> np.ndarray:
+    """delta = W_delta X per block row, as [W, 2 sides, 2 taps, groups].  [Conv], R-conv."""
+    X = _f64(X)
+    return (X @ _f64(w_delta).T).reshape(X.shape[0], 2, 2, -1)
+
+
+def grouped_conv(X, base, delta, side: int) -> np.ndarray:
+    """Conv_side(X) over the block rows of one request ([Conv], R-conv): channel c of
+    group g = c // gw takes (base[side,0,c] + delta[i,side,0,g]) X[i,c], plus, for i >= 1,
+    (base[side,1,c] + delta[i,side,1,g]) X[i-1,c]."""
+    X = _f64(X)
+    W, H = X.shape
+    b = _f64(base).reshape(2, 2, H)
+    gw = H // delta.shape[-1]
+    cur = b[side, 0] + np.repeat(delta[:, side, 0, :], gw, axis=1)     # [W, H]
+    prev = b[side, 1] + np.repeat(delta[:, side, 1, :], gw, axis=1)
+    out = cur * X
+    out[1:] += prev[1:] * X[:-1]
+    return out
+
+
 def dflash_layer(x, lw, geo, positions, k_ctx, v_ctx, ctx_positions, frontier: int,
                  layer: int):
     """One draft layer for one request's block (no injection).  [DFlash-notes]:
@@ -284,18 +314,32 @@ def dflash_layer(x, lw, geo, positions, k_ctx, v_ctx, ctx_positions, frontier: i
         a = attention(q, [K_ctx; k], [V_ctx; v]) ; y = x + W_o a
         m = plain_rmsnorm(y, post_attention_norm)
         x_next = y + W_down(SiLU(W_gate m) * (W_up m))
+    With DFlash2 convolution weights in ``lw`` ([Conv], R-conv) each branch's normalised
+    input is prepared by Conv_0 and its output finished by Conv_1 before the residual add:
+        d_a = delta(n);  q, k, v from Conv_0(n);  y = x + Conv_1(W_o a)
+        d_m = delta(m);  z = W_down(SiLU(W_gate p) * (W_up p)), p = Conv_0(m)
+        x_next = y + Conv_1(z)
     Returns (x_next, block k, block v)."""
     D, eps, th = geo.head_dim, geo.eps, geo.rope_theta
+    conv = "conv_delta_a" in lw
     x = _f64(x)
     n = plain_rmsnorm(x, lw["in_norm"], eps)
+    if conv:
+        d_a = conv_delta(n, lw["conv_delta_a"])
+        n = grouped_conv(n, lw["conv_base_a"], d_a, 0)
     q = rope_1d(plain_head_rmsnorm(n @ _f64(lw["wq"]).T, lw["q_norm"], eps, D), positions, D, th)
     k = rope_1d(plain_head_rmsnorm(n @ _f64(lw["wk"]).T, lw["k_norm"], eps, D), positions, D, th)
     v = n @ _f64(lw["wv"]).T
     a = block_attention(q, k, v, k_ctx, v_ctx, ctx_positions, frontier, geo.windows[layer],
                         geo.block_causal, geo.n_q_heads, geo.n_kv_heads, D)
-    y = x + a @ _f64(lw["wo"]).T
+    o = a @ _f64(lw["wo"]).T
+    y = x + (grouped_conv(o, lw["conv_base_a"], d_a, 1) if conv else o)
     m = plain_rmsnorm(y, lw["post_norm"], eps)
-    x_next = y + (silu(m @ _f64(lw["w_gate"]).T) * (m @ _f64(lw["w_up"]).T)) @ _f64(lw["w_down"]).T
+    if conv:
+        d_m = conv_delta(m, lw["conv_delta_m"])
+        m = grouped_conv(m, lw["conv_base_m"], d_m, 0)
+    z = (silu(m @ _f64(lw["w_gate"]).T) * (m @ _f64(lw["w_up"]).T)) @ _f64(lw["w_down"]).T
+    x_next = y + (grouped_conv(z, lw["conv_base_m"], d_m, 1) if conv else z)
     return x_next, k, v
 
 

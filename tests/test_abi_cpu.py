@@ -71,6 +71,11 @@ def test_workspace_bytes_rejects_bad_sizes(B):
     assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0
     bad = cfg_of(bdsynth.TINY, mask_token_id=1024)
     assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0
+    for gw in (-4, 6, 3, 512):   # the convolution group must be a multiple of 4 dividing H
+        bad = cfg_of(bdsynth.TINY, conv_group=gw)
+        assert L.bd_workspace_bytes(C.byref(bad), 1, 7, 16) == 0, gw
+    ok = cfg_of(bdsynth.TINY, conv_group=16)
+    assert L.bd_workspace_bytes(C.byref(ok), 1, 7, 16) >= L.bd_workspace_bytes(C.byref(c), 1, 7, 16)
 
 
 def _fake_weights(B, c, n_layers):
@@ -180,7 +185,7 @@ def test_ring_capacity_must_hold_the_window(B):
 
 def test_packed_bytes_cover_every_matrix(B):
     """The packed image holds each projection matrix once (plus tile padding)."""
-    for name in ("dspine_b16_27b_b1", "dflash_35b_a3b_b8", "tiny_fp32"):
+    for name in ("dspine_b16_27b_b1", "dflash_35b_a3b_b8", "tiny_fp32", "dflash2_27b_b1"):
         w = bdsynth.WORKLOADS[name]
         c = cfg_of(w)
         n = B.lib().bd_packed_bytes(C.byref(c))
@@ -189,5 +194,7 @@ def test_packed_bytes_cover_every_matrix(B):
         mats = H * w.n_target_layers * H + w.vocab * H + w.n_layers * (QD * H + 2 * KD * H + H * QD + 3 * H * w.ffn)
         if w.code_width:
             mats += 3 * w.msg_width * w.code_width + w.n_layers * (w.code_width * H + H * w.msg_width)
+        if w.conv_group:
+            mats += w.n_layers * 2 * (4 * H // w.conv_group) * H
         assert n >= mats * el
         assert n < mats * el * 1.05 + (16 << 20)

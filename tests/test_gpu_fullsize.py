@@ -54,6 +54,13 @@ def test_dspine_27b_b1_full_round():
     assert rep["ok"], rep
 
 
+def test_dflash2_27b_b1_full_round():
+    rep = run_case(bdsynth.DFLASH2_27B_B1, [0])
+    record("dflash2_27b_b1", rep)
+    print(rep)
+    assert rep["ok"], rep
+
+
 def test_dspine_27b_b8_sampled_requests():
     rep = run_case(bdsynth.DSPINE27B_B8, [0, 4, 7])
     record("dspine_b16_27b_b8", rep)

@@ -91,8 +91,18 @@ def test_materialize_matches_oracle(geo):
 
 
 # ---------------------------------------------------------------- round
+# DFlash2 dynamic grouped convolution (group width 16 / 8), alone and with the bridge
+SMALL_DFLASH2 = SMALL_BF16.with_(name="small_dflash2_bf16", code_width=0, msg_width=0,
+                                 conv_group=16)
+SMALL_DFLASH2_BRIDGE = SMALL_BF16.with_(name="small_dflash2_bridge_bf16", conv_group=8)
+TINY_DFLASH2 = bdsynth.TINY.with_(name="tiny_dflash2_fp32", conv_group=16)
+
+
 @pytest.mark.parametrize("geo,seed", [(bdsynth.TINY, 0), (bdsynth.TINY, 1), (SMALL_BF16, 0),
-                                      (SMALL_BF16, 2), (SMALL_D64, 0)])
+                                      (SMALL_BF16, 2), (SMALL_D64, 0), (SMALL_DFLASH2, 0),
+                                      (SMALL_DFLASH2, 1), (SMALL_DFLASH2_BRIDGE, 2),
+                                      (TINY_DFLASH2, 0),
+                                      (SMALL_DFLASH2.with_(n_masks=6, batch=5), 3)])
 def test_round_matches_oracle(geo, seed):
     case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
     case.fill_rings()
@@ -128,6 +138,28 @@ def test_zero_write_is_bit_exact_plain_dflash():
     ga = a.run_gpu()
     geo0 = geo.with_(code_width=0, msg_width=0)
     b = Hn.Case(geo0, seed=5, weights=w, max_ctx_rows=128)
+    b.fill_rings()
+    gb = b.run_gpu()
+    assert torch.equal(ga["layers"], gb["layers"])
+    assert torch.equal(ga["tokens"], gb["tokens"])
+
+
+def test_identity_convolution_is_bit_exact_plain_dflash():
+    """DFlash2 with zero delta projections and identity base coefficients (current tap 1,
+    previous tap 0) must equal the same round without the convolution, bit for bit: the
+    branch outputs then reach the residual through the same single fp32 addition."""
+    geo = SMALL_DFLASH2
+    w = bdsynth.make_weights(geo, 9)
+    for lw in w["layers"]:
+        for br in ("a", "m"):
+            lw["conv_delta_" + br].zero_()
+            lw["conv_base_" + br].zero_()
+            lw["conv_base_" + br][:, 0] = 1.0
+    a = Hn.Case(geo, seed=9, weights=w, max_ctx_rows=128)
+    a.fill_rings()
+    ga = a.run_gpu()
+    geo0 = geo.with_(conv_group=0)
+    b = Hn.Case(geo0, seed=9, weights=w, max_ctx_rows=128)
     b.fill_rings()
     gb = b.run_gpu()
     assert torch.equal(ga["layers"], gb["layers"])

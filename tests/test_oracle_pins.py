@@ -7,6 +7,7 @@ chosen so that a plausible slip in the oracle (a dropped term, a wrong sign or
 index, a transposed operand, a mis-scaled softmax) fails at least one of them.
 """
 import cmath
+import copy
 import json
 import math
 import os
@@ -33,6 +34,24 @@ class Geo:
     def capacity(self, l):
         s = self.windows[l]
         return s if s > 0 else self.full_capacity
+
+
+def add_conv(w, g, seed=1, gw=4, identity=False):
+    """DFlash2 convolution weights for every layer of ``w`` (group width gw)."""
+    r = np.random.default_rng(seed)
+    H = g.hidden
+    for lw in w["layers"]:
+        for br in ("a", "m"):
+            if identity:
+                base = np.zeros((2, 2, H))
+                base[:, 0] = 1.0
+                lw["conv_delta_" + br] = np.zeros((4 * H // gw, H))
+            else:
+                base = r.normal(0, 0.3, (2, 2, H))
+                base[:, 0] += 1.0
+                lw["conv_delta_" + br] = r.normal(0, 0.3, (4 * H // gw, H))
+            lw["conv_base_" + br] = base
+    return w
 
 
 def rand_weights(g, seed=0, zero_write=False, gate_bias=False):
@@ -522,6 +541,93 @@ def test_round_requests_are_isolated_and_permutable():
     c = O.draft_round(g, w, rings2, [5, 17], [9, 13], 0, 5)
     np.testing.assert_array_equal(c["h"][0], ab["h"][0])
     assert np.any(c["h"][1] != ab["h"][1])
+
+
+# ----------------------------------------------------------------- DFlash2 convolution
+def test_conv_with_zero_delta_is_a_causal_two_tap_filter_per_channel():
+    """delta = 0 leaves a static depthwise filter: channel c of Conv_s(X) equals the
+    causal FIR filter [base[s,0,c], base[s,1,c]] applied down the block rows (numpy's
+    convolution, truncated to W rows).  Pins the tap order and the row direction."""
+    W, H, gw = 6, 12, 4
+    X = rng.normal(0, 1, (W, H))
+    base = rng.normal(0, 1, (2, 2, H))
+    delta = np.zeros((W, 2, 2, H // gw))
+    for side in (0, 1):
+        out = O.grouped_conv(X, base, delta, side)
+        for c in range(H):
+            ref = np.convolve(X[:, c], [base[side, 0, c], base[side, 1, c]])[:W]
+            np.testing.assert_allclose(out[:, c], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_conv_delta_is_shared_by_the_channels_of_its_group():
+    """A dynamic increment of group g changes exactly the gw channels g*gw .. g*gw+gw-1,
+    all by the same multiple of X (current tap) and of the previous row (previous tap)."""
+    W, H, gw = 5, 12, 4
+    X = rng.normal(0, 1, (W, H))
+    base = rng.normal(0, 1, (2, 2, H))
+    delta = np.zeros((W, 2, 2, H // gw))
+    ref = O.grouped_conv(X, base, delta, 1)
+    d = delta.copy()
+    d[3, 1, 0, 1] = 0.5          # row 3, side 1, current tap, group 1
+    d[3, 1, 1, 1] = -2.0         # row 3, side 1, previous tap, group 1
+    d[2, 0, 0, 2] = 7.0          # side 0 entries do not act on side 1
+    out = O.grouped_conv(X, base, d, 1)
+    diff = out - ref
+    assert np.all(diff[[0, 1, 2, 4]] == 0)
+    assert np.all(diff[3, :4] == 0) and np.all(diff[3, 8:] == 0)
+    np.testing.assert_allclose(diff[3, 4:8], 0.5 * X[3, 4:8] - 2.0 * X[2, 4:8], rtol=1e-13)
+
+
+def test_conv_row_zero_has_no_preceding_tap_and_rows_couple_only_to_the_next():
+    W, H, gw = 7, 8, 4
+    X = rng.normal(0, 1, (W, H))
+    base = rng.normal(0, 1, (2, 2, H))
+    delta = rng.normal(0, 1, (W, 2, 2, H // gw))
+    ref = O.grouped_conv(X, base, delta, 0)
+    np.testing.assert_allclose(ref[0], (base[0, 0] + np.repeat(delta[0, 0, 0], gw)) * X[0],
+                               rtol=1e-13)
+    Y = X.copy()
+    Y[3] += 1.0
+    changed = np.nonzero(np.any(O.grouped_conv(Y, base, delta, 0) != ref, axis=1))[0]
+    assert list(changed) == [3, 4]
+
+
+def test_conv_delta_projection_layout():
+    """W_delta rows are ordered (side, tap, group): row s*2G + t*G + g feeds delta[i,s,t,g]."""
+    W, H, G = 3, 8, 2
+    X = rng.normal(0, 1, (W, H))
+    Wd = np.zeros((4 * G, H))
+    Wd[1 * 2 * G + 0 * G + 1] = 1.0      # side 1, tap 0, group 1 <- sum of X
+    d = O.conv_delta(X, Wd)
+    np.testing.assert_allclose(d[:, 1, 0, 1], X.sum(axis=1), rtol=1e-13)
+    assert np.count_nonzero(d) == np.count_nonzero(X.sum(axis=1))
+
+
+def test_dflash2_layer_with_identity_conv_is_the_dflash_layer():
+    g = Geo(windows=(5, 0), code_width=0, msg_width=0)
+    w = rand_weights(g)
+    w2 = add_conv(copy.deepcopy(w), g, identity=True)
+    a, _ = _round(g, w)
+    b, _ = _round(g, w2)
+    for key in ("x_layers", "h", "logits"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_dflash2_conv_acts_on_both_branches_and_keeps_requests_isolated():
+    g = Geo(windows=(5, 0), code_width=0, msg_width=0)
+    w = add_conv(rand_weights(g), g)
+    base, rings = _round(g, w)
+    # each of the four convolutions changes the result
+    for br in ("a", "m"):
+        for side in (0, 1):
+            w2 = copy.deepcopy(w)
+            for lw in w2["layers"]:
+                lw["conv_base_" + br][side, 1] += 0.5
+            res, _ = _round(g, w2)
+            assert np.abs(res["h"] - base["h"]).max() > 1e-6, (br, side)
+    # the convolution has no history across requests: request 1's anchor leaves request 0
+    other = O.draft_round(g, w, rings, [5, 18], [9, 13], 0, 5)
+    np.testing.assert_array_equal(other["h"][0], base["h"][0])
 
 
 def _materialize_requests(g, w, feats, rows_of, frontiers):

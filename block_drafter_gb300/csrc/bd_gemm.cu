@@ -44,6 +44,7 @@ constexpr int kATileBytes = kBM * 128;  // 16 KB: 128 rows x 128 bytes
 constexpr int kXStride = 17;            // epilogue exchange row stride (floats)
 constexpr int kMaxStages = 12;
 constexpr long long kMinUnits = 8;
+constexpr double kWholeTileSlack = 1.15;
 constexpr size_t kSmemLimit = 232448 - 1024;  // 227 KB opt-in per block, less static smem
 
 // A pipeline stage holds kbox K-boxes of the weight tile (each 128 rows x 128 bytes, so
@@ -83,12 +84,14 @@ struct SegWalk {
   }
 };
 
-__device__ __forceinline__ long long unit_begin(long long U, int P, int c) {
-  return static_cast<long long>(c) * U / P;
+// CTA c's units start at unit_begin(c): the U units are cut into grains of g units (1, or
+// the k-blocks of a whole tile when every CTA takes whole tiles) dealt out evenly.
+__device__ __forceinline__ long long unit_begin(long long U, int P, int c, int g) {
+  return static_cast<long long>(c) * (U / g) / P * g;
 }
 // CTA whose unit range contains unit u.
-__device__ __forceinline__ int cta_of_unit(long long U, int P, long long u) {
-  return static_cast<int>(((u + 1) * P - 1) / U);
+__device__ __forceinline__ int cta_of_unit(long long U, int P, long long u, int g) {
+  return static_cast<int>(((u / g + 1) * P - 1) / (U / g));
 }
 
 __device__ __forceinline__ int seg_of_tile(const GemmArgs &p, int m_tile) {
@@ -529,8 +532,8 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
   const int P = p.n_ctas;
   const int LW = p.ln;
   const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
-  const int c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb);
-  const int c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1);
+  const int c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb, p.grain);
+  const int c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1, p.grain);
   const int n = c_last - c_first + 1;
   const int me = static_cast<int>(blockIdx.x) - c_first;
   unsigned *arrived = p.counters + tile;
@@ -561,7 +564,7 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
       const uint64_t pol = policy_evict_first();
       for (int i = 0; i < cn; ++i) {
         const int c = c_first + c0 + i;
-        const int cslot = (static_cast<int>(unit_begin(U, P, c) / p.kb) == tile) ? 0 : 1;
+        const int cslot = (static_cast<int>(unit_begin(U, P, c, p.grain) / p.kb) == tile) ? 0 : 1;
         const float *src = p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
                            static_cast<size_t>(k) * 16 * kBM;
         bulk_load(fs.base + static_cast<size_t>(slot0 + i) * kPiece, src, kPiece, fs.bar, pol);
@@ -731,8 +734,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long u0 = unit_begin(p.units, p.n_ctas, blockIdx.x);
-  const long long u1 = unit_begin(p.units, p.n_ctas, blockIdx.x + 1);
+  const long long u0 = unit_begin(p.units, p.n_ctas, blockIdx.x, p.grain);
+  const long long u1 = unit_begin(p.units, p.n_ctas, blockIdx.x + 1, p.grain);
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(2 * p.block_n)) ncols <<= 1;
 
@@ -991,6 +994,15 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   const long long min_units = (kMinUnits + a.kbox - 1) / a.kbox;
   const long long by_units = (a.units + min_units - 1) / min_units;
   a.n_ctas = static_cast<int>(by_units < num_sms() ? by_units : num_sms());
+  // Whole tiles per CTA when there are at least as many tiles as CTAs and the busiest CTA
+  // gets at most kWholeTileSlack times the average: no split tile, so no partial-tile
+  // stores, waits or reductions (which cost more than that imbalance).
+  a.grain = 1;
+  if (tiles >= a.n_ctas) {
+    const long long most = (tiles + a.n_ctas - 1) / a.n_ctas;
+    if (static_cast<double>(most) * a.n_ctas <= kWholeTileSlack * static_cast<double>(tiles))
+      a.grain = a.kb;
+  }
   a.stages = pick_stages(a.block_n, a.kbox);
   if (a.stages < 2) return "GEMM tile does not fit in shared memory";
   a.partials = sc.partials;

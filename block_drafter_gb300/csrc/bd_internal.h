@@ -57,6 +57,7 @@ struct __align__(16) GemmArgs {
   int split, ln, lo_row;
   int packed;                     // weights come from packed images (contiguous bulk copies)
   long long units;
+  int grain;                      // units per scheduling grain (1, or kb: whole tiles per CTA)
   int epi;
   int ld_out, ld_act, block_w, vocab;
   long long act_lo;               // SWIGLU: element offset of the lo block of out_act (0: none)

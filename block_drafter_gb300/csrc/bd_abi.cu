@@ -149,6 +149,17 @@ struct Carve {
   }
 };
 
+// When the context chunks are short (at most two 64-key blocks per split), the block's own
+// keys -- a separate hi+lo pass -- would double the last split's work and every split
+// waits for it in the merge: give them a split of their own.
+bool att_block_split(const bd_config *c, int l, int n_splits) {
+  if (n_splits < 2) return false;
+  const int cap = c->ring_capacity[l];
+  const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
+  const int blocks = (ctx + 63) / 64;
+  return (blocks + n_splits - 2) / (n_splits - 1) <= 2;
+}
+
 int att_splits(const bd_config *c, int l, int B, int W, int sms) {
   const int cap = c->ring_capacity[l];
   const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
@@ -379,8 +390,8 @@ void add_w(GemmPlan &p, const void *ptr, int rows, const uint8_t *packed_base = 
 static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
                                 const void *cmat, int n_rows, float *kv_raw, const float2 *rope,
                                 const int32_t *row_request, const int64_t *row_pos,
-                                const int64_t *ctx_frontier, int n_req, const GemmScratch &sc,
-                                cudaStream_t s) {
+                                const int64_t *ctx_frontier, int n_req, int min_back,
+                                const GemmScratch &sc, cudaStream_t s) {
   const int H = cfg->hidden, D = cfg->head_dim, KD = cfg->n_kv_heads * D;
   const uint8_t *pk = static_cast<const uint8_t *>(w->packed);
   const PackedLayout PL = packed_layout(cfg);
@@ -413,6 +424,7 @@ static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const
   h.row_req = row_request;
   h.row_pos = row_pos;
   h.frontier = ctx_frontier;
+  h.min_back = min_back;
   int n_segs = 0;
   for (int l = 0; l < cfg->n_layers; ++l) {
     HeadSeg &k = h.seg[n_segs++];
@@ -531,7 +543,7 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
   }
   // S2: every layer's raw context K and V (fp32), then head norm + RoPE + ring scatter
   return enqueue_ctx_kv(cfg, w, kv, mw.cmat, n_rows, mw.kv_raw, mw.rope, row_request, row_pos,
-                        ctx_frontier, kv->b_max, sc, s);
+                        ctx_frontier, kv->b_max, 0, sc, s);
 }
 
 bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_cache *kv,
@@ -610,7 +622,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
                             nullptr, nullptr, nullptr, 1, 0, s));
       const bd_status st = enqueue_ctx_kv(cfg, w, kv, rw.cmat, n_pend, rw.kv_raw,
                                           rw.rope + static_cast<size_t>(T) * (D / 2),
-                                          pending->request, pending->pos, frontier, B, sc, s);
+                                          pending->request, pending->pos, frontier, B,
+                                          kMaxPendPerReq, sc, s);
       if (st != BD_OK) return st;
     }
   }
@@ -690,6 +703,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         h.row_req = pending->request;
         h.row_pos = pending->pos;
         h.frontier = frontier;
+        h.min_back = kMaxPendPerReq;
       }
       BD_TRY(launch_head_post(dt, h, s));
     }
@@ -716,6 +730,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.cap = cfg->ring_capacity[l];
       a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
       a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
+      a.block_split = att_block_split(cfg, l, a.n_splits) ? 1 : 0;
+      a.n_guard = n_pend > 0 ? kMaxPendPerReq : 0;
       a.max_keys = att_max_keys(cfg, l, W);
       a.q_lo = split ? static_cast<size_t>(T) * QD : 0;
       a.blk_lo = split ? static_cast<size_t>(T) * KD : 0;

@@ -69,7 +69,8 @@ struct AttGeom {
 };
 
 // Context keys [p_lo, F) of request b (the window's oldest visible position, clipped to
-// the ring's live interval) are split into n_splits chunks of whole 64-key blocks.
+// the ring's live interval) are split into chunks of whole 64-key blocks: one per split,
+// or one per split but the last when that split only takes the block's own keys.
 __device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b, int split) {
   AttGeom g;
   g.F = a.frontier[b];
@@ -78,7 +79,8 @@ __device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b, int split) 
   if (lo < 0) lo = 0;
   g.p_lo = static_cast<int>(lo);
   g.n_ctx = g.F > lo ? static_cast<int>(g.F - lo) : 0;
-  int chunk = (g.n_ctx + a.n_splits - 1) / a.n_splits;
+  const int cs = a.block_split ? a.n_splits - 1 : a.n_splits;  // splits with context keys
+  int chunk = (g.n_ctx + cs - 1) / cs;
   chunk = (chunk + kAttKeys - 1) / kAttKeys * kAttKeys;
   g.k_begin = min(g.n_ctx, split * chunk);
   g.k_end = min(g.n_ctx, g.k_begin + chunk);
@@ -143,67 +145,110 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
   }
 }
 
-// Merge the splits of query row rr of (request b, KV head h):
+// Merge the splits of query rows r0 .. r1-1 of (request b, KV head h):
 //   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-// One warp; lanes own D/32 consecutive output dims and the split weights are computed by
-// lanes and broadcast, so the per-split loads are independent of each other.  The
-// partials were written by other CTAs of the launch: read through L2.
+// The four warps take (row, part) tasks: with fewer than three rows each row's splits are
+// shared by 4 / rows warps, whose sums meet in shared memory.  Lanes own D/32 consecutive
+// output dims; split weights are computed by lanes and broadcast, and the partial tiles are
+// loaded eight splits at a time before they are used (the loads are independent and their
+// L2 latency, not bandwidth, bounds the merge).  The partials were written by other CTAs of
+// the launch: read through L2.  Called by all threads of the CTA.
 template <typename T, int D>
-__device__ __forceinline__ void combine_row(const AttArgs &a, int b, int h, int rr, int lane) {
+__device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int r0, int r1,
+                                             int warp, int lane, float (*red)[D + 4]) {
   const int G = a.n_q_heads / a.n_kv_heads;
   const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
   constexpr int PER = D / 32;
+  constexpr int kBatch = 8;
   const float *po = a.part_o + bh * a.n_splits * kAttRows * D;
   const float2 *pml = a.part_ml + bh * a.n_splits * kAttRows;
-  float M = -INFINITY;
-  for (int s = lane; s < a.n_splits; s += 32) {
-    const float2 ml = __ldcg(pml + s * kAttRows + rr);
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
-  M = warp_max(M);
-  float acc[PER];
+  const int nrows = r1 - r0;
+  const int P = nrows >= 3 ? 1 : 4 / max(nrows, 1);  // warps per row
+  const int S = a.n_splits;
+  for (int t0 = 0; t0 < nrows * P; t0 += 4) {
+    const int t = t0 + warp;
+    const bool active = t < nrows * P;
+    const int rr = r0 + (active ? t / P : 0), part = t % P;
+    float acc[PER];
 #pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
-    const int s = s0 + lane;
-    float wgt = 0.f;
-    if (s < a.n_splits) {
-      const float2 ml = __ldcg(pml + s * kAttRows + rr);
-      if (ml.y > 0.f) {
-        wgt = exp2f(ml.x - M);
-        L += wgt * ml.y;
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float L = 0.f;
+    if (active) {
+      float M = -INFINITY;
+      for (int s = lane; s < S; s += 32) {
+        const float2 ml = __ldcg(pml + s * kAttRows + rr);
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+      }
+      M = warp_max(M);
+      const int s_begin = part * S / P, s_end = (part + 1) * S / P;
+      for (int s0 = s_begin; s0 < s_end; s0 += 32) {
+        const int s = s0 + lane;
+        float wgt = 0.f;
+        if (s < s_end) {
+          const float2 ml = __ldcg(pml + s * kAttRows + rr);
+          if (ml.y > 0.f) {
+            wgt = exp2f(ml.x - M);
+            L += wgt * ml.y;
+          }
+        }
+        const int cnt = min(32, s_end - s0);
+        for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+          float v[kBatch][PER];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const float *os = po + (static_cast<size_t>(s0 + j0 + u) * kAttRows + rr) * D + lane * PER;
+            if (j0 + u < cnt) {
+              if (PER == 4) {
+                const float4 o = __ldcg(reinterpret_cast<const float4 *>(os));
+                v[u][0] = o.x;
+                v[u][1] = o.y;
+                v[u][2] = o.z;
+                v[u][3] = o.w;
+              } else {
+                const float2 o = __ldcg(reinterpret_cast<const float2 *>(os));
+                v[u][0] = o.x;
+                v[u][1] = o.y;
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const float wj = __shfl_sync(0xffffffffu, wgt, (j0 + u) & 31);
+            if (j0 + u < cnt)
+#pragma unroll
+              for (int e = 0; e < PER; ++e) acc[e] += wj * v[u][e];
+          }
+        }
+      }
+      L = warp_sum(L);
+    }
+    if (P > 1) {  // the parts of a row meet in shared memory
+      if (active) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
+        if (lane == 0) red[warp][D] = L;
+      }
+      __syncthreads();
+      if (active && part == 0)
+        for (int q = 1; q < P; ++q) {
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] += red[warp + q][lane * PER + e];
+          L += red[warp + q][D];
+        }
+    }
+    if (active && part == 0) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int gh = rr / a.W, i = rr % a.W;
+      T *out = static_cast<T *>(a.out) +
+               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const float y = acc[e] * inv;
+        const T hi = from_f<T>(y);
+        out[e] = hi;
+        if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
       }
     }
-    const int cnt = min(32, a.n_splits - s0);
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wgt, j);
-      const float *os = po + (static_cast<size_t>(s0 + j) * kAttRows + rr) * D + lane * PER;
-      if (PER == 4) {
-        const float4 o = __ldcg(reinterpret_cast<const float4 *>(os));
-        acc[0] += wj * o.x;
-        acc[1] += wj * o.y;
-        acc[2] += wj * o.z;
-        acc[3] += wj * o.w;
-      } else {
-        const float2 o = __ldcg(reinterpret_cast<const float2 *>(os));
-        acc[0] += wj * o.x;
-        acc[1] += wj * o.y;
-      }
-    }
-  }
-  L = warp_sum(L);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int gh = rr / a.W, i = rr % a.W;
-  T *out = static_cast<T *>(a.out) +
-           (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const float y = acc[e] * inv;
-    const T hi = from_f<T>(y);
-    out[e] = hi;
-    if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
   }
 }
 
@@ -223,8 +268,10 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q_heads / a.n_kv_heads;
   const int R = G * a.W;
-  pdl_wait();
-  pdl_trigger();
+  // The frontier is an input of the round and the ring holds context written before it,
+  // except the positions >= F - n_guard that this round's catch-up may store: a first
+  // context block entirely older than that is fetched before waiting for the previous
+  // kernel (the head post-processing, which writes Q and the block's keys/values).
   const AttGeom g = att_geom(a, b, split);
   const bool do_block = split == a.n_splits - 1;
 
@@ -233,19 +280,8 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   const __nv_bfloat16 *ring_v = static_cast<const __nv_bfloat16 *>(a.ring_v);
   const __nv_bfloat16 *blk_k = static_cast<const __nv_bfloat16 *>(a.blk_k);
   const __nv_bfloat16 *blk_v = static_cast<const __nv_bfloat16 *>(a.blk_v);
-
-  // ---- Q tiles: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
   constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int c = tid; c < 2 * kAttRows * CPR; c += 128) {
-    const int part = c / (kAttRows * CPR), cc = c % (kAttRows * CPR);
-    const int rr = cc / CPR, ch = cc % CPR;
-    const bool valid = rr < R;
-    const int gh = valid ? rr / a.W : 0, i = valid ? rr % a.W : 0;
-    const __nv_bfloat16 *src = q + (part ? a.q_lo : 0) +
-                               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
-                               (h * G + gh) * D + ch * 8;
-    cp_async16(smem_u32(sQ + (part * kAttRows + rr) * RS + ch * 8), src, valid);
-  }
+
   auto load_kv = [&](int buf, int k0) {
     for (int c = tid; c < kAttKeys * CPR; c += 128) {
       const int kr = c / CPR, ch = c % CPR;
@@ -288,8 +324,26 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   const bool rvA = rowA < R, rvB = rowB < R;
 
   const int n_blocks = g.k_end > g.k_begin ? (g.k_end - g.k_begin + kAttKeys - 1) / kAttKeys : 0;
-  if (n_blocks > 0) load_kv(0, g.k_begin);
-  else if (do_block) load_block(0);
+  const bool early = n_blocks > 0 && g.p_lo + g.k_begin + kAttKeys <= g.F - a.n_guard;
+  if (early) {
+    load_kv(0, g.k_begin);
+    cp_async_commit();
+  }
+  pdl_wait();
+  pdl_trigger();
+  // Q tiles: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
+  for (int c = tid; c < 2 * kAttRows * CPR; c += 128) {
+    const int part = c / (kAttRows * CPR), cc = c % (kAttRows * CPR);
+    const int rr = cc / CPR, ch = cc % CPR;
+    const bool valid = rr < R;
+    const int gh = valid ? rr / a.W : 0, i = valid ? rr % a.W : 0;
+    const __nv_bfloat16 *src = q + (part ? a.q_lo : 0) +
+                               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
+                               (h * G + gh) * D + ch * 8;
+    cp_async16(smem_u32(sQ + (part * kAttRows + rr) * RS + ch * 8), src, valid);
+  }
+  if (n_blocks > 0 && !early) load_kv(0, g.k_begin);
+  else if (n_blocks == 0 && do_block) load_block(0);
   cp_async_commit();
   // the first context position every block row can see: keys from here on need no mask
   const long long p_all = a.window > 0 ? g.F + a.W - a.window : LLONG_MIN;
@@ -491,8 +545,9 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   __syncthreads();
   if (s_abort) return;
   const int rp = (R + a.n_splits - 1) / a.n_splits;
-  const int r1 = min(R, (split + 1) * rp);
-  for (int rr = split * rp + warp; rr < r1; rr += 4) combine_row<__nv_bfloat16, D>(a, b, h, rr, lane);
+  __shared__ float red[4][D + 4];
+  combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,
+                                 red);
   __syncthreads();
   if (tid == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
     *arrived = 0u;  // every split is past its wait: ready for the next launch

@@ -21,6 +21,9 @@ struct AttArgs {
   float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
   unsigned *counters;   // [2][B * Hkv] split arrival / done counters (start at 0)
   int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
+  int block_split;      // 1: the last split takes only the block's own keys (n_splits >= 2)
+  int n_guard;          // context positions >= F - n_guard may be written by this round's
+                        // catch-up (read only after the previous kernel has finished)
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
 };
 
@@ -120,6 +123,7 @@ struct HeadPostArgs {
   const int32_t *row_req;    // ring mode, by row - row0 of the group
   const int64_t *row_pos;
   const int64_t *frontier;
+  int min_back;              // > 0: ring rows must lie in [F - min_back, F) (else an error)
   HeadGroup grp[2];
   HeadSeg seg[kMaxHeadSegs];
 };

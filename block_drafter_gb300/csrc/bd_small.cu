@@ -305,6 +305,10 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
       return;
     }
     const long long F = a.frontier[req];
+    if (a.min_back > 0 && (pos < F - a.min_back || pos >= F)) {
+      if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      return;
+    }
     if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
     o = ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D;
   }

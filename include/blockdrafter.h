@@ -191,8 +191,10 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w,
  *
  *   feats    dev [n_rows, n_target_layers*H]  captured residual rows s_t
  *   request  dev int32 [n_rows]  request (ring row) of each row, < B of the round
- *   pos      dev int64 [n_rows]  absolute position t of each row, < frontier[request];
- *            stored in layer l only if t >= frontier[request] - ring_capacity[l]
+ *   pos      dev int64 [n_rows]  absolute position t of each row, one of the 16 newest:
+ *            frontier[request] - 16 <= t < frontier[request] (a row outside that range is
+ *            skipped and reported by bd_sync_status); stored in layer l only if
+ *            t >= frontier[request] - ring_capacity[l]
  *   n_rows   0 .. 16*B (0 = nothing pending)
  * Rows of one request must have distinct positions.
  */

@@ -57,6 +57,15 @@ Readings taken where the pages are schematic or garbled (each also listed in DES
            (row 0, the anchor, has no preceding tap; no history across requests or
            rounds).  Side 0 prepares the branch input, side 1 finishes the branch output
            with the same delta; base is stored [2 sides][2 taps][H].
+  R-fp8    FP8 retrieval ([Refine]: row-scaled FP8 scores over the whole vocabulary, 128
+           candidates, BF16 rescoring, 16 kept).  Row scale s = max|row| / 448 and codes
+           q = e4m3(row / s) (round to nearest even, largest finite 448), both computed in
+           fp32 like the kernel; the hidden row is coded the same way.  Approximate score of
+           vocabulary row v = s_v * (q_v . q_h) (the hidden row's scale is common to a row
+           and left out).  Candidates: each 128-row vocabulary tile keeps its 16 best
+           approximate scores, and the row keeps the n_cand best of those (a tile holding
+           more than 16 of the n_cand best loses its excess); ties go to the lower id.  The
+           candidates are rescored with the exact head and the k best kept (R-topk order).
   R-topk   a row's k candidates are its k largest exact logits over the whole
            vocabulary, by descending score; equal scores keep the lower token id first.
   R-tail   last-write refinement of block row i with predecessor token s: the last
@@ -404,6 +413,58 @@ def lm_head_topk(logits, k: int):
     logits = _f64(logits)
     ids = np.argsort(-logits, axis=-1, kind="stable")[:, :k]
     return ids, np.take_along_axis(logits, ids, axis=-1)
+
+
+# --------------------------------------------------------------------------- FP8 retrieval
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Round to the nearest e4m3 (OCP FP8 E4M3FN) value, ties to even, magnitudes above the
+    largest finite value 448 clamped to it.  E4M3 has 3 mantissa bits, exponent bias 7 and
+    no infinities: normal values are (1 + m/8) 2^e for e >= -6, subnormals m 2^-9."""
+    x = _f64(x)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)                      # below 2^-6 the spacing stays 2^-9
+    step = np.exp2(e - 3.0)
+    r = np.rint(a / step) * step                 # np.rint rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.sign(x) * r
+
+
+def fp8_row_code(M):
+    """Row-scaled FP8 code of each row of M (R-fp8): scale s = max|row| / 448 and codes
+    e4m3(row / s), both in fp32.  Returns (codes as float64 values, scales)."""
+    M32 = np.asarray(M, dtype=np.float32)
+    mx = np.max(np.abs(M32), axis=-1)
+    s = (mx / np.float32(E4M3_MAX)).astype(np.float32)
+    s = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((M32 / s[..., None]).astype(np.float32))
+    return q, s.astype(np.float64)
+
+
+def lm_head_topk_fp8(hidden, embed_head, n_cand: int, k: int, tile: int = 128,
+                     per_tile: int = 16):
+    """[Refine] FP8 retrieval then BF16 rescoring (R-fp8).  Returns (ids [rows, k], exact
+    scores [rows, k], candidate ids [rows, n_cand] in approximate-score order)."""
+    qE, sE = fp8_row_code(embed_head)
+    qh, _ = fp8_row_code(hidden)
+    approx = (qh @ qE.T) * sE[None, :]                       # [rows, V]
+    rows, V = approx.shape
+    pool_ids = []
+    for t0 in range(0, V, tile):
+        blk = approx[:, t0:t0 + tile]
+        ids = np.argsort(-blk, axis=-1, kind="stable")[:, :per_tile] + t0
+        pool_ids.append(ids)
+    pool = np.concatenate(pool_ids, axis=1)                  # [rows, tiles * per_tile]
+    pool_sc = np.take_along_axis(approx, pool, axis=1)
+    order = np.lexsort((pool, -pool_sc), axis=-1)[:, :n_cand]  # score desc, id asc
+    cand = np.take_along_axis(pool, order, axis=1)
+    E = _f64(embed_head)
+    exact = np.einsum("rkh,rh->rk", E[cand], _f64(hidden))
+    sel = np.lexsort((cand, -exact), axis=-1)[:, :k]
+    return (np.take_along_axis(cand, sel, axis=1), np.take_along_axis(exact, sel, axis=1), cand)
 
 
 def top2_gap(logits) -> np.ndarray:

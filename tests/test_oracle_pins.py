@@ -503,6 +503,76 @@ def test_topk_first_is_argmax_and_scores_are_dot_products():
         assert rest.max() <= sc[i, -1]
 
 
+# ----------------------------------------------------------------- FP8 retrieval
+def test_e4m3_rounding_matches_torch_float8_e4m3fn():
+    """The oracle's e4m3 rounding against PyTorch's float8_e4m3fn conversion (a library
+    routine) on a dense sweep with exact ties, subnormals and the largest finite value."""
+    torch = pytest.importorskip("torch")
+    x = rng.normal(0, 40, 100000).astype(np.float32)
+    grid = np.array([0.0] + [m * 2.0 ** -9 for m in range(1, 8)] +
+                    [(1 + m / 8) * 2.0 ** e for e in range(-6, 9) for m in range(8)])
+    grid = grid[grid <= 448]
+    mids = (grid[1:] + grid[:-1]) / 2                    # exact ties between neighbours
+    x = np.concatenate([x, grid, -grid, mids, -mids, np.float32([448.0, 460.0, -460.0])])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).float().numpy()
+    np.testing.assert_array_equal(O.e4m3_round(x), ref)
+
+
+def test_e4m3_grid_closed_forms():
+    """126 positive finite values, the largest 448 = 1.75 * 2^8, the smallest subnormal 2^-9,
+    the smallest normal 2^-6; halves go to the even neighbour; large values clamp to 448."""
+    pos = np.unique(O.e4m3_round(np.linspace(1e-4, 460, 2000000)))
+    pos = pos[pos > 0]
+    assert len(pos) == 126 and pos.max() == 448.0 and pos.min() == 2.0 ** -9
+    assert 2.0 ** -6 in pos and (2.0 ** -6 - 2.0 ** -9) in pos
+    np.testing.assert_array_equal(O.e4m3_round([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 1e6]),
+                                  [1.0, 1.25, 0.0, 2.0 ** -8, 448.0])
+
+
+def test_fp8_row_code_scales_and_codes():
+    M = rng.normal(0, 0.02, (6, 64)).astype(np.float32)
+    q, sc = O.fp8_row_code(M)
+    np.testing.assert_array_equal(np.max(np.abs(q), axis=1), 448.0)  # the row's max maps to 448
+    # scaling a row by a power of two scales its scale and leaves its codes
+    q2, s2 = O.fp8_row_code(M * np.float32(8.0))
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_allclose(s2, 8 * sc, rtol=0)
+    # codes times scale approximate the row within half an e4m3 step (relative 2^-4)
+    assert np.all(np.abs(q * sc[:, None] - M) <= np.abs(M) * 2.0 ** -4 + sc[:, None] * 2.0 ** -10)
+
+
+def test_fp8_retrieval_with_every_candidate_is_the_exact_head():
+    E = rng.normal(0, 0.02, (300, 32))
+    h = rng.normal(0, 1, (3, 32))
+    ids, sc, _ = O.lm_head_topk_fp8(h, E, n_cand=300, k=16, tile=128, per_tile=128)
+    ref_ids, ref_sc = O.lm_head_topk(O.lm_head_logits(h, E), 16)
+    np.testing.assert_array_equal(ids, ref_ids)
+    np.testing.assert_allclose(sc, ref_sc, rtol=1e-12)
+
+
+def test_fp8_retrieval_finds_the_exact_top16_on_random_heads():
+    E = rng.normal(0, 0.02, (4096, 256)).astype(np.float32)
+    h = rng.normal(0, 1, (4, 256)).astype(np.float32)
+    ids, sc, cand = O.lm_head_topk_fp8(h, E, n_cand=128, k=16)
+    ref_ids, ref_sc = O.lm_head_topk(O.lm_head_logits(h, E), 16)
+    for r in range(4):
+        assert set(ref_ids[r]) <= set(cand[r])
+    np.testing.assert_array_equal(ids, ref_ids)
+    np.testing.assert_allclose(sc, ref_sc, rtol=1e-12)
+
+
+def test_fp8_retrieval_keeps_16_per_tile():
+    """A tile holding 20 of the best rows contributes only its 16 best."""
+    H = 16
+    E = rng.normal(0, 0.01, (512, H))
+    h = np.ones((1, H))
+    E[128:148] = 0.5 + 0.01 * np.arange(20)[:, None]   # tile 1 holds the 20 best rows
+    _, _, cand = O.lm_head_topk_fp8(h, E, n_cand=32, k=4)
+    in_tile = [c for c in cand[0] if 128 <= c < 148]
+    assert sorted(in_tile) == list(range(132, 148))      # its 16 best, not all 20
+
+
 def test_lm_head_chunking_matches_product():
     h = rng.normal(0, 1, (3, 16))
     E = rng.normal(0, 1, (100, 16))

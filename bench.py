@@ -212,6 +212,10 @@ class State:
     def head_topk(self):
         self.sess.head_topk(self.head_in, TOPK, self.cand, self.cand_score)
 
+    def head_topk_fp8(self):
+        """FP8 retrieval of 128 candidates per row, BF16 rescoring, the 16 best."""
+        self.sess.head_topk_fp8(self.head_in, 128, TOPK, self.cand, self.cand_score)
+
     def round_with_tail(self):
         self.sess.round(self.anchors, self.front, self.geo.n_masks, self.head_in,
                         tail_state=self.tail, pending=(self.feats, self.row_req, self.row_pos))
@@ -584,6 +588,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_per_step": launches_per_step,
         "head_topk16_us": 1000.0 * time_call(st.head_topk, args.steps, args.warmup),
+        "head_topk16_fp8_us": 1000.0 * time_call(st.head_topk_fp8, args.steps, args.warmup),
         "refine_tail_us": refine_us(st, args),
     }
     if not args.no_b8 and args.workload == "b1":
@@ -601,6 +606,8 @@ def main():
                       "achieved_step_gbs": gbs8, "frac_of_measured_hbm": gbs8 / hbm,
                       "algorithmic_bytes_per_step": by8,
                       "head_topk16_us": 1000.0 * time_call(st8.head_topk, args.steps, args.warmup),
+                      "head_topk16_fp8_us": 1000.0 * time_call(st8.head_topk_fp8, args.steps,
+                                                               args.warmup),
                       "refine_tail_us": refine_us(st8, args)}
         del st8
     if not args.no_b8 and args.workload == "b1":

@@ -25,7 +25,7 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
            "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
            "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk",
-           "bd_refine_tail")
+           "bd_refine_tail", "bd_head_fp8_bytes", "bd_pack_head_fp8", "bd_lm_head_topk_fp8")
 
 TOPK_MAX = 16
 
@@ -114,6 +114,13 @@ def lib() -> C.CDLL:
         L.bd_lm_head_topk.restype = i
         L.bd_lm_head_topk.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, i, vp, vp, vp,
                                       sz, vp]
+        L.bd_head_fp8_bytes.restype = sz
+        L.bd_head_fp8_bytes.argtypes = [C.POINTER(Config)]
+        L.bd_pack_head_fp8.restype = i
+        L.bd_pack_head_fp8.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, sz, vp]
+        L.bd_lm_head_topk_fp8.restype = i
+        L.bd_lm_head_topk_fp8.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, vp, i, i, i,
+                                          vp, vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -196,6 +203,30 @@ def pack_weights(cfg: Config, weights: Weights, packed: torch.Tensor, stream=Non
     nbytes = packed.numel() - (aligned - base)
     _check(lib().bd_pack_weights(C.byref(cfg), C.byref(weights), aligned, nbytes, _stream(stream)))
     return aligned
+
+
+def head_fp8_bytes(cfg: Config) -> int:
+    return lib().bd_head_fp8_bytes(C.byref(cfg))
+
+
+def pack_head_fp8(cfg: Config, weights: Weights, image: torch.Tensor, stream=None) -> int:
+    """Writes the FP8 head copy into ``image`` (uint8 device tensor) at its first 1024-byte
+    aligned address and returns that address."""
+    base = image.data_ptr()
+    aligned = (base + 1023) // 1024 * 1024
+    nbytes = image.numel() - (aligned - base)
+    _check(lib().bd_pack_head_fp8(C.byref(cfg), C.byref(weights), aligned, nbytes, _stream(stream)))
+    return aligned
+
+
+def lm_head_topk_fp8(cfg: Config, weights: Weights, head_fp8: int, hidden: torch.Tensor,
+                     n_cand: int, k: int, token_out: torch.Tensor, workspace: torch.Tensor,
+                     score_out: Optional[torch.Tensor] = None, stream=None):
+    """FP8 retrieval of n_cand candidates per hidden row, BF16 rescoring, the k best."""
+    _check(lib().bd_lm_head_topk_fp8(
+        C.byref(cfg), C.byref(weights), head_fp8, _ptr(hidden), int(hidden.shape[0]), int(n_cand),
+        int(k), _ptr(token_out), _ptr(score_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def workspace_bytes(cfg: Config, b_max: int, max_masks: int, max_ctx_rows: int) -> int:

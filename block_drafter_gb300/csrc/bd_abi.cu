@@ -313,7 +313,11 @@ struct HeadWs {
   float *topk_part_val;  // [rows][slices][kTopK] per-slice lists
   int32_t *topk_part_idx;
   void *hl;  // bf16 hi/lo pair of the hidden rows [2][pad16(rows)][H]
+  void *q8;          // FP8 retrieval: e4m3 codes of the hidden rows [rows][H]
+  int32_t *ties;     // [rows][m_tiles * kTopK] candidates tied at the selection threshold
+  int32_t *cand;     // [rows][kMaxCand] selected candidates
 };
+constexpr int kMaxCand = 256;  // FP8 retrieval candidates per row
 void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   const size_t m_tiles = tiles_of(c->vocab, 128);
   const int bn = 2 * pad16(rows);
@@ -326,6 +330,9 @@ void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   const size_t slices = static_cast<size_t>(topk_slices(static_cast<int>(m_tiles)));
   w.topk_part_val = cv.take<float>(rows * slices * kTopK);
   w.topk_part_idx = cv.take<int32_t>(rows * slices * kTopK);
+  w.q8 = cv.take<char>(static_cast<size_t>(rows) * c->hidden);
+  w.ties = cv.take<int32_t>(rows * m_tiles * kTopK);
+  w.cand = cv.take<int32_t>(static_cast<size_t>(rows) * kMaxCand);
 }
 
 // Last-write refinement of B requests, K mask rows, kc candidates per row:
@@ -908,6 +915,73 @@ bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float
   return BD_OK;
 }
 
+size_t bd_head_fp8_bytes(const bd_config *cfg) {
+  if (!check_config(cfg).empty() || cfg->dtype != BD_BF16 || cfg->hidden % 16 != 0) return 0;
+  return head_fp8_image_bytes(cfg->vocab, cfg->hidden) + static_cast<size_t>(cfg->vocab) * sizeof(float);
+}
+
+bd_status bd_pack_head_fp8(const bd_config *cfg, const bd_weights *w, void *image, size_t image_bytes,
+                           void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if (cfg->dtype != BD_BF16) return fail(BD_ERR_UNSUPPORTED, "the FP8 head copy is built from a bf16 head");
+  if (cfg->hidden % 16 != 0) return fail(BD_ERR_UNSUPPORTED, "the FP8 head needs hidden % 16 == 0");
+  if (!w || !w->embed_head || !aligned16(w->embed_head))
+    return fail(BD_ERR_INVALID_ARG, "embed_head NULL or misaligned");
+  if (!image || (reinterpret_cast<uintptr_t>(image) & 1023))
+    return fail(BD_ERR_INVALID_ARG, "FP8 head image NULL or not 1024-byte aligned");
+  if (image_bytes < bd_head_fp8_bytes(cfg))
+    return fail(BD_ERR_INVALID_ARG, "FP8 head image smaller than bd_head_fp8_bytes()");
+  BD_TRY(launch_head_fp8_pack(w->embed_head, cfg->vocab, cfg->hidden, image,
+                              static_cast<cudaStream_t>(stream_)));
+  return BD_OK;
+}
+
+bd_status bd_lm_head_topk_fp8(const bd_config *cfg, const bd_weights *w, const void *head_fp8,
+                              const float *hidden, int rows, int n_cand, int k, int32_t *token_out,
+                              float *score_out, void *workspace, size_t workspace_bytes,
+                              void *stream_) {
+  std::string e = check_config(cfg);
+  if (!e.empty()) return fail(BD_ERR_INVALID_ARG, e);
+  if (cfg->dtype != BD_BF16) return fail(BD_ERR_UNSUPPORTED, "FP8 retrieval needs a bf16 head");
+  if (cfg->hidden % 16 != 0) return fail(BD_ERR_UNSUPPORTED, "FP8 retrieval needs hidden % 16 == 0");
+  const int V = cfg->vocab, H = cfg->hidden;
+  const int m_tiles = static_cast<int>(tiles_of(V, 128));
+  if (select_cand_smem(m_tiles) > 200 * 1024) return fail(BD_ERR_UNSUPPORTED, "vocab too large for FP8 retrieval");
+  if (k < 1 || k > BD_TOPK_MAX) return fail(BD_ERR_INVALID_ARG, "k must be in 1..16");
+  if (n_cand < k || n_cand > kMaxCand || n_cand > V || n_cand > m_tiles * kTopK)
+    return fail(BD_ERR_INVALID_ARG, "n_cand must be in k..256 and at most vocab");
+  if (rows < 1 || rows > kMaxB * kMaxMasks) return fail(BD_ERR_INVALID_ARG, "rows must be in 1..120");
+  if (!w || !w->embed_head || !aligned16(w->embed_head))
+    return fail(BD_ERR_INVALID_ARG, "embed_head NULL or misaligned");
+  if (!head_fp8 || (reinterpret_cast<uintptr_t>(head_fp8) & 1023))
+    return fail(BD_ERR_INVALID_ARG, "FP8 head image NULL or not 1024-byte aligned");
+  if (!hidden || !aligned16(hidden)) return fail(BD_ERR_INVALID_ARG, "hidden NULL or misaligned");
+  if (!token_out) return fail(BD_ERR_INVALID_ARG, "token_out NULL");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return fail(BD_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  Carve cv;
+  cv.base = static_cast<char *>(workspace);
+  HeadWs hw;
+  carve_head(cv, hw, cfg, rows, num_sms());
+  if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
+  // the hidden rows' codes (this first kernel also clears the GEMM tile counters)
+  BD_TRY(launch_code_rows(hidden, rows, H, hw.q8, counters_of(hw.g), s));
+  GemmPlan p = make_plan(cfg, hw.q8, rows, H);
+  p.dtype = GT_E4M3;
+  add_w(p, w->embed_head, V, static_cast<const uint8_t *>(head_fp8), 0);
+  p.args.epi = EPI_TOPK;
+  p.args.topk_val = hw.topk_val;
+  p.args.topk_idx = hw.topk_idx;
+  p.args.wscale = reinterpret_cast<const float *>(static_cast<const char *>(head_fp8) +
+                                                  head_fp8_image_bytes(V, H));
+  BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
+  BD_TRY(launch_select_cand(hw.topk_val, hw.topk_idx, m_tiles, rows, n_cand, hw.ties, hw.cand, s));
+  BD_TRY(launch_rescore(w->embed_head, V, H, hidden, hw.cand, rows, n_cand, k, token_out, score_out, s));
+  return BD_OK;
+}
+
 bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float *tail_state,
                          const int32_t *cand_ids, const float *cand_scores, int B, int n_masks, int kc,
                          int32_t *token_out, int32_t *pick_out, float *table_out, void *workspace,
@@ -975,7 +1049,7 @@ bd_status bd_sync_status(void *stream_) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
   const unsigned word = take_error_word_gemm() | take_error_word_att() | take_error_word_small() |
-                        take_error_word_pack();
+                        take_error_word_pack() | take_error_word_head8();
   if (word & DEVERR_TIMEOUT) return fail(BD_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
   if (word & DEVERR_BAD_INDEX)
     return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");

@@ -239,6 +239,22 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Two fp32 values to two e4m3 codes (round to nearest even, finite values saturate at
+// +-448): the low byte holds lo, the high byte hi.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
@@ -280,6 +296,11 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 }
 
 // ------------------------------------------------------------------ small math
+// Candidate order of the top-k heads: higher score first, equal scores to the lower id.
+__device__ __forceinline__ bool cand_better(float a, int ai, float b, int bi) {
+  return a > b || (a == b && ai < bi);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

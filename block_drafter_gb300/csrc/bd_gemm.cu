@@ -39,6 +39,11 @@ template <> struct MmaTraits<float> {
   static constexpr int UK = 8;    // kind::tf32
   static constexpr uint32_t fmt = 2;
 };
+template <> struct MmaTraits<Fp8E4M3> {
+  static constexpr int BK = 128;
+  static constexpr int UK = 32;   // kind::f8f6f4, E4M3 operands (format code 0)
+  static constexpr uint32_t fmt = 0;
+};
 
 constexpr int kATileBytes = kBM * 128;  // 16 KB: 128 rows x 128 bytes
 constexpr int kXStride = 17;            // epilogue exchange row stride (floats)
@@ -239,8 +244,10 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
           const uint32_t acc = (kbi > kb0 || j > 0 || k > 0) ? 1u : 0u;
           if constexpr (MmaTraits<T>::fmt == 1)
             umma_bf16(d, ad, bd, idesc, acc);
-          else
+          else if constexpr (MmaTraits<T>::fmt == 2)
             umma_tf32(d, ad, bd, idesc, acc);
+          else
+            umma_f8(d, ad, bd, idesc, acc);
         }
       }
       umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
@@ -312,9 +319,10 @@ __device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int 
   constexpr int kWarps = kEpiThreads / 32;
   constexpr int kRowsPerGroup = kBM * 16 / kEpiThreads;  // 8 rows per thread
   const int row_id = m_tile * kBM + ps.r;
+  const float ws = p.wscale != nullptr && row_id < p.vocab ? p.wscale[row_id] : 1.f;
 #pragma unroll
   for (int jj = 0; jj < kCW; ++jj)
-    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
+    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] * ws : -INFINITY;
   named_bar(1, kEpiThreads);
   const int col = ps.et & 15, grp = ps.et >> 4;
   float best = -INFINITY;
@@ -359,9 +367,6 @@ __device__ __forceinline__ void argmax_chunk(const GemmArgs &p, int m_tile, int 
 }
 
 // (score, id) order of the candidate lists: higher score first, equal scores lower id first.
-__device__ __forceinline__ bool cand_better(float a, int ai, float b, int bi) {
-  return a > b || (a == b && ai < bi);
-}
 
 // Per-(vocab tile, token) 16 best rows, in candidate order.  The chunk is transposed
 // through shared memory; the 16 threads of a half warp own one token column, 8 rows each,
@@ -373,9 +378,10 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs &p, int m_tile, int to
                                            EpiSmem &es) {
   static_assert(kEpiThreads == 256, "16 token columns x 16 threads per column");
   const int row_id = m_tile * kBM + ps.r;
+  const float ws = p.wscale != nullptr && row_id < p.vocab ? p.wscale[row_id] : 1.f;
 #pragma unroll
   for (int jj = 0; jj < kCW; ++jj)
-    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] : -INFINITY;
+    es.xbuf[ps.r * kXStride + ps.c0 + jj] = row_id < p.vocab ? v[jj] * ws : -INFINITY;
   uint8_t *sb = stage_claim(es, ps.et);  // also orders the transpose writes before the reads
   float *sv = reinterpret_cast<float *>(sb);                 // [16 tokens][kTopK]
   int32_t *si = reinterpret_cast<int32_t *>(sb + 16 * kTopK * 4);
@@ -439,24 +445,36 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs &p, int m_tile, int to
 // Writes the finished values v (tile row ps.r, token columns tok0+ps.c0 .. +kCW-1; j0 =
 // tok0 minus the tile's first token) of m_tile to the epilogue's destination.
 template <typename T, int EPI>
+__device__ __forceinline__ void emit_rows(const GemmMaps &maps, const GemmArgs &p, int m_tile,
+                                          int tok0, int j0, const EpiPos &ps,
+                                          const float (&v)[kCW], EpiSmem &es);
+template <typename T, int EPI>
 __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs &p, int m_tile,
                                            int tok0, int j0, const EpiPos &ps,
                                            const float (&v)[kCW], EpiSmem &es) {
-  if (EPI == EPI_ARGMAX) {
+  if constexpr (EPI == EPI_ARGMAX) {
     argmax_chunk(p, m_tile, tok0, ps, v, es);
     return;
-  }
-  if (EPI == EPI_TOPK) {
+  } else if constexpr (EPI == EPI_TOPK) {
     topk_chunk(p, m_tile, tok0, ps, v, es);
     return;
+  } else {
+    emit_rows<T, EPI>(maps, p, m_tile, tok0, j0, ps, v, es);
   }
+}
+
+// The epilogues that write rows of results (stores, residual and injection adds, SwiGLU).
+template <typename T, int EPI>
+__device__ __forceinline__ void emit_rows(const GemmMaps &maps, const GemmArgs &p, int m_tile,
+                                          int tok0, int j0, const EpiPos &ps,
+                                          const float (&v)[kCW], EpiSmem &es) {
   const int r = ps.r, c0 = ps.c0;
   if (EPI == EPI_SWIGLU && r >= 64) {  // up features go to the gate rows' threads
 #pragma unroll
     for (int jj = 0; jj < kCW; ++jj) es.xbuf[(r - 64) * kXStride + c0 + jj] = v[jj];
   }
   uint8_t *sb = stage_claim(es, ps.et);
-  if (EPI == EPI_SWIGLU) {
+  if constexpr (EPI == EPI_SWIGLU) {
     // rows 0..63: gate features f, rows 64..127: up features f (same f)
     if (r < 64) {
       T *hi = reinterpret_cast<T *>(sb);
@@ -854,7 +872,7 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return "cuTensorMapEncodeTiled is unavailable";
-  const int elem = dtype == 0 ? 2 : 4;
+  const int elem = dtype == GT_BF16 ? 2 : (dtype == GT_E4M3 ? 1 : 4);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                         static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride) * elem,
@@ -863,7 +881,10 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
                        static_cast<cuuint32_t>(planes)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
-  CUresult r = fn(&m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType ty = dtype == GT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == GT_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(&m, ty,
                   planes > 1 ? 3 : 2, const_cast<void *>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -948,7 +969,7 @@ static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStr
 
 std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stream) {
   GemmArgs &a = plan.args;
-  const int BK = plan.dtype == 0 ? 64 : 32;
+  const int BK = plan.dtype == GT_BF16 ? 64 : (plan.dtype == GT_E4M3 ? 128 : 32);  // 128 bytes
   if (plan.n_tokens <= 0 || plan.K <= 0 || plan.n_w <= 0) return "empty GEMM";
   if (plan.n_w > kMaxSegs) return "too many GEMM segments";
   a.K = plan.K;
@@ -1015,13 +1036,14 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   memset(&maps, 0, sizeof maps);
   a.packed = plan.w[0].packed != nullptr ? 1 : 0;
   if (a.packed) {
-    const int elem = plan.dtype == 0 ? 2 : 4;
+    const int elem = plan.dtype == GT_BF16 ? 2 : (plan.dtype == GT_E4M3 ? 1 : 4);
     for (int s = 0; s < a.n_segs; ++s) {
       if (!plan.w[s].packed) return "packed GEMM with an unpacked segment";
       a.seg[s].packed = static_cast<const uint8_t *>(plan.w[s].packed);
       a.seg[s].n_kb_pack = static_cast<int>(packed_kb(plan.K, elem));
     }
   } else {
+    if (plan.dtype == GT_E4M3) return "FP8 GEMMs need packed weights";
     for (int s = 0; s < plan.n_w; ++s) {
       std::string err = make_map(&maps.a[s], plan.w[s].ptr, plan.dtype, plan.K, plan.w[s].rows, BK,
                                  plan.pair_mode ? 64 : kBM);
@@ -1052,8 +1074,14 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
       break;
   }
   if (!err.empty()) return err;
-  cudaError_t e = plan.dtype == 0 ? launch_typed<__nv_bfloat16>(maps, a, stream)
-                                  : launch_typed<float>(maps, a, stream);
+  cudaError_t e;
+  if (plan.dtype == GT_E4M3) {
+    if (a.epi != EPI_TOPK || plan.split || plan.pair_mode) return "FP8 GEMMs support the top-k epilogue only";
+    e = launch_epi<Fp8E4M3, EPI_TOPK>(maps, a, stream);
+  } else {
+    e = plan.dtype == GT_BF16 ? launch_typed<__nv_bfloat16>(maps, a, stream)
+                              : launch_typed<float>(maps, a, stream);
+  }
   if (e != cudaSuccess) return std::string("GEMM launch: ") + cudaGetErrorString(e);
   return {};
 }

@@ -68,6 +68,7 @@ struct __align__(16) GemmArgs {
   int32_t *amax_idx;
   float *topk_val;                // [m_tiles][n_tokens][kTopK], descending
   int32_t *topk_idx;
+  const float *wscale;            // TOPK: per weight row score scale (FP8 row scales), or null
   float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
   unsigned *counters;             // [2][n_counter_tiles] arrival / done counters (start at 0)
   int n_counter_tiles;
@@ -88,8 +89,14 @@ struct GemmWeight {
   int rows;
   const void *packed;  // packed image of the matrix (pair mode: the interleaved pair), or null
 };
+// Operand element type of a GEMM: bf16, fp32 (tf32 products) or FP8 e4m3 (both operands
+// one byte per element; packed weights only).
+enum GemmType : int { GT_BF16 = 0, GT_F32 = 1, GT_E4M3 = 2 };
+struct Fp8E4M3 {
+  uint8_t bits;
+};
 struct GemmPlan {
-  int dtype;                 // 0 bf16, 1 fp32
+  int dtype;                 // GemmType
   int K;
   int n_tokens;
   const void *x;             // activations [n_tokens, K] (config dtype), dev
@@ -111,6 +118,7 @@ struct GemmScratch {
 unsigned take_error_word_gemm();
 unsigned take_error_word_att();
 unsigned take_error_word_small();
+unsigned take_error_word_head8();
 
 // ------------------------------------------------------------------ packed weights
 // Packed image of one [rows, K] matrix: 128-row tiles, each split into 128-byte K boxes;

@@ -44,6 +44,15 @@ struct ZeroSpan {
   unsigned *p;
   size_t n;
 };
+#ifdef __CUDACC__
+// Grid-stride zeroing of a ZeroSpan (after the kernel's pdl_wait: the previous kernel,
+// which may still use the words, has completed).
+__device__ __forceinline__ void zero_span(ZeroSpan z) {
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < z.n;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+    z.p[t] = 0u;
+}
+#endif
 
 // Round prologue: x[b*W+i] = embed[id] (fp32), id = anchor_b for i = 0 else MASK, the
 // (cos, sin) rows of positions F_b + i (rows 0 .. B*W-1), then the rows of n_pend pending
@@ -141,6 +150,19 @@ int topk_slices(int m_tiles);
 std::string launch_topk_reduce(const float *val, const int32_t *idx, int m_tiles, int rows, int k,
                                float *part_val, int32_t *part_idx, int32_t *tok_out,
                                float *score_out, cudaStream_t s);
+// FP8 retrieval head: the row-scaled e4m3 image of a bf16 head [V, H] (tiles of 128 rows x
+// 128-byte boxes, head_fp8_image_bytes(V, H) bytes, then V fp32 row scales); the e4m3 code
+// of hidden rows [rows][H]; the n_cand best of the per-tile candidate lists (radix
+// selection, scratch ties [rows][m_tiles * kTopK]); exact rescoring and the k best.
+size_t head_fp8_image_bytes(int V, int H);
+std::string launch_head_fp8_pack(const void *E, int V, int H, void *img, cudaStream_t s);
+std::string launch_code_rows(const float *h, int rows, int H, void *q, ZeroSpan z, cudaStream_t s);
+size_t select_cand_smem(int m_tiles);
+std::string launch_select_cand(const float *val, const int32_t *idx, int m_tiles, int rows,
+                               int n_cand, int32_t *ties, int32_t *cand, cudaStream_t s);
+std::string launch_rescore(const void *E, int V, int H, const float *hidden, const int32_t *cand,
+                           int rows, int n_cand, int k, int32_t *tok_out, float *score_out,
+                           cudaStream_t s);
 // Last-write refinement: state export [T][H] u | [T] r | [T][Mc] G c (from pre [T][3 Mc]),
 // the predecessor candidates' codebook rows, the refined message (hi+lo pair), the
 // refined scores [B][K-1][kc][kc] and the greedy walk.

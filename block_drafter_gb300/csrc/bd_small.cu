@@ -32,13 +32,6 @@ __device__ __forceinline__ float2 rope_cs(long long pos, double inv) {
   return make_float2(c, s);
 }
 
-// Grid-stride zeroing of a ZeroSpan (after the kernel's pdl_wait: the previous kernel,
-// which may still use the words, has completed).
-__device__ __forceinline__ void zero_span(ZeroSpan z) {
-  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < z.n;
-       t += static_cast<size_t>(gridDim.x) * blockDim.x)
-    z.p[t] = 0u;
-}
 
 template <typename T>
 __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *anchors,
@@ -409,9 +402,6 @@ __global__ void argmax_reduce_kernel(const float *val, const int32_t *idx, int m
 }
 
 // Candidate order: higher score first, equal scores to the lower id.
-__device__ __forceinline__ bool cand_better(float a, int ai, float b, int bi) {
-  return a > b || (a == b && ai < bi);
-}
 // Insert (x, xi) into the sorted list (L, I) of kTopK entries if it beats the last one.
 __device__ __forceinline__ bool cand_insert(float (&L)[kTopK], int (&I)[kTopK], float x, int xi) {
   if (!cand_better(x, xi, L[kTopK - 1], I[kTopK - 1])) return false;

@@ -87,6 +87,16 @@ class DraftSession:
         B.lm_head_topk(self.cfg, self.wstruct, hidden, k, token_out, self.workspace, score_out,
                        stream)
 
+    def head_topk_fp8(self, hidden: torch.Tensor, n_cand: int, k: int, token_out: torch.Tensor,
+                      score_out: Optional[torch.Tensor] = None, stream=None):
+        """FP8 retrieval head; the FP8 head copy is built on first use."""
+        if getattr(self, "head_fp8", None) is None:
+            self.head_fp8_buf = torch.empty(B.head_fp8_bytes(self.cfg) + 1024, dtype=torch.uint8,
+                                            device=self.device)
+            self.head_fp8 = B.pack_head_fp8(self.cfg, self.wstruct, self.head_fp8_buf, stream)
+        B.lm_head_topk_fp8(self.cfg, self.wstruct, self.head_fp8, hidden, n_cand, k, token_out,
+                           self.workspace, score_out, stream)
+
     def alloc_outputs(self, Bn: int, n_masks: int):
         W = n_masks + 1
         H = self.geo.hidden

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 6
+#define BD_ABI_VERSION 7
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -283,6 +283,41 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
 bd_status bd_lm_head_topk(const bd_config *cfg, const bd_weights *w, const float *hidden, int rows,
                           int k, int32_t *token_out, float *score_out, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * FP8 retrieval head.  "DSpine for Qwen3.8-27B: Causal Features Through Depth", section
+ * "The last write is refined using discrete candidates": the released drafter's optimized
+ * path scores the whole vocabulary approximately with a row-scaled FP8 copy of the head,
+ * takes 128 candidates, rescores them with the BF16 head and keeps 16.
+ *   image:      each head row v as e4m3(E_v / s_v), s_v = max|E_v| / 448 (round to nearest
+ *               even; fp32 division), stored in the GEMM's packed tile layout, then the V
+ *               fp32 scales s_v.  bd_pack_head_fp8 writes it from w->embed_head (a bf16
+ *               config with hidden % 16 == 0); its size is bd_head_fp8_bytes(cfg) (0 if
+ *               the config has no FP8 head), `image` 1024-byte aligned, caller-owned.
+ *   retrieval:  each hidden row is coded the same way (scale max|h| / 448); approximate
+ *               score of row v = s_v * (codes_v . codes_h) (the hidden row's common scale
+ *               is left out); each 128-row vocabulary tile keeps its 16 best, and the row
+ *               the n_cand best of those (a tile holding more than 16 of them loses its
+ *               excess; equal scores to the lower id).
+ *   rescoring:  the exact logits embed_head[c] . hidden_r of the n_cand candidates (bf16 head
+ *               rows, fp32 hidden, fp32 sums); the k best, by descending score, equal
+ *               scores to the lower id (the order of bd_lm_head_topk).
+ *
+ *   hidden     dev fp32 [rows, H];  rows 1 .. 8*15;  k 1 .. BD_TOPK_MAX;  n_cand k .. 256
+ *              (and <= vocab);  the pages' value is 128
+ *   token_out  dev int32 [rows, k]  OUT;  score_out  dev fp32 [rows, k] OUT or NULL
+ * The rescoring gives each returned id its exact logit; whether the exact top k were all
+ * among the candidates is not guaranteed (candidate generation, not an exact head).
+ * Errors: BD_ERR_UNSUPPORTED for an fp32 config or hidden % 16 != 0; BD_ERR_INVALID_ARG
+ * for out-of-range sizes or pointers.  Workspace as sized by bd_workspace_bytes.
+ */
+size_t bd_head_fp8_bytes(const bd_config *cfg);
+bd_status bd_pack_head_fp8(const bd_config *cfg, const bd_weights *w, void *image,
+                           size_t image_bytes, void *stream);
+bd_status bd_lm_head_topk_fp8(const bd_config *cfg, const bd_weights *w, const void *head_fp8,
+                              const float *hidden, int rows, int n_cand, int k,
+                              int32_t *token_out, float *score_out, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /*
  * Last-write refinement, transition tables and greedy walk (the DSpine tail).

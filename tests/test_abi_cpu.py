@@ -24,7 +24,7 @@ def B():
 def header_symbols():
     src = open(os.path.join(ROOT, "include", "blockdrafter.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(bd_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(bd_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_three_entry_points():
@@ -141,6 +141,24 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     st = L.bd_lm_head_topk(C.byref(c), C.byref(w), 0x10000, 4, 16, 0x10000, None, ws + 16, 1 << 30,
                            None)
     assert st == -5
+    # FP8 retrieval: fp32 config unsupported; k, n_cand, rows, image alignment checked
+    st = L.bd_lm_head_topk_fp8(C.byref(c), C.byref(w), 0x10000, 0x10000, 4, 128, 16, 0x10000, None,
+                               ws, 1 << 30, None)
+    assert st == -2 and b"bf16" in L.bd_last_error()
+    assert L.bd_head_fp8_bytes(C.byref(c)) == 0
+    cb = cfg_of(bdsynth.DSPINE27B_B1)
+    wb = _fake_weights(B, cb, cb.n_layers)
+    assert L.bd_head_fp8_bytes(C.byref(cb)) == 151936 * 5120 + 151936 * 4
+    for (k, nc, rows) in ((0, 128, 4), (17, 128, 4), (16, 8, 4), (16, 257, 4), (16, 128, 0),
+                          (16, 128, 121)):
+        st = L.bd_lm_head_topk_fp8(C.byref(cb), C.byref(wb), 0x10000, 0x10000, rows, nc, k,
+                                   0x10000, None, ws, 1 << 30, None)
+        assert st == -1, (k, nc, rows)
+    st = L.bd_lm_head_topk_fp8(C.byref(cb), C.byref(wb), 0x10010, 0x10000, 4, 128, 16, 0x10000,
+                               None, ws, 1 << 30, None)
+    assert st == -1 and b"1024-byte" in L.bd_last_error()
+    st = L.bd_pack_head_fp8(C.byref(cb), C.byref(wb), 0x10000, 1024, None)
+    assert st == -1 and b"smaller" in L.bd_last_error()
     # refinement: K < 2, kc out of range, missing inputs
     st = L.bd_refine_tail(C.byref(c), C.byref(w), 0x10000, 0x10000, 0x10000, 1, 1, 16, 0x10000,
                           None, None, ws, 1 << 30, None)

@@ -44,6 +44,7 @@ def _setup(dtype, H, V, rows, seed, tie_rows=None):
     wd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in wd.items()}
     ws_struct = B.make_weights(cfg, wd)
     ws = torch.empty(B.workspace_bytes(cfg, 8, 15, 16), dtype=torch.uint8, device="cuda")
+    ws_struct.keep = wd  # the struct holds raw pointers: keep the device tensors alive with it
     return B, cfg, ws_struct, ws, E, h
 
 

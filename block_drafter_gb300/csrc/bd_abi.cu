@@ -313,15 +313,18 @@ struct HeadWs {
   float *topk_part_val;  // [rows][slices][kTopK] per-slice lists
   int32_t *topk_part_idx;
   void *hl;  // bf16 hi/lo pair of the hidden rows [2][pad16(rows)][H]
-  void *q8;          // FP8 retrieval: e4m3 codes of the hidden rows [rows][H]
+  unsigned *row_done;  // FP8 retrieval: [rows] rescoring counters, right after g.counters
+  void *q8;          // e4m3 codes of the hidden rows [rows][H]
   int32_t *ties;     // [rows][m_tiles * kTopK] candidates tied at the selection threshold
   int32_t *cand;     // [rows][kMaxCand] selected candidates
+  float *cscore;     // [rows][kMaxCand] their exact scores
 };
 constexpr int kMaxCand = 256;  // FP8 retrieval candidates per row
 void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   const size_t m_tiles = tiles_of(c->vocab, 128);
   const int bn = 2 * pad16(rows);
   carve_gemm(cv, w.g, bn, m_tiles, sms);
+  w.row_done = cv.take<unsigned>(rows);
   w.hl = cv.take<char>(static_cast<size_t>(2 * pad16(rows)) * c->hidden * 2);
   w.amax_val = cv.take<float>(m_tiles * rows);
   w.amax_idx = cv.take<int32_t>(m_tiles * rows);
@@ -333,6 +336,7 @@ void carve_head(Carve &cv, HeadWs &w, const bd_config *c, int rows, int sms) {
   w.q8 = cv.take<char>(static_cast<size_t>(rows) * c->hidden);
   w.ties = cv.take<int32_t>(rows * m_tiles * kTopK);
   w.cand = cv.take<int32_t>(static_cast<size_t>(rows) * kMaxCand);
+  w.cscore = cv.take<float>(static_cast<size_t>(rows) * kMaxCand);
 }
 
 // Last-write refinement of B requests, K mask rows, kc candidates per row:
@@ -966,8 +970,10 @@ bd_status bd_lm_head_topk_fp8(const bd_config *cfg, const bd_weights *w, const v
   HeadWs hw;
   carve_head(cv, hw, cfg, rows, num_sms());
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
-  // the hidden rows' codes (this first kernel also clears the GEMM tile counters)
-  BD_TRY(launch_code_rows(hidden, rows, H, hw.q8, counters_of(hw.g), s));
+  // the hidden rows' codes (this first kernel also clears the GEMM tile counters and the
+  // rescoring counters, carved right after them)
+  const ZeroSpan zero{hw.g.counters, static_cast<size_t>(hw.row_done - hw.g.counters) + rows};
+  BD_TRY(launch_code_rows(hidden, rows, H, hw.q8, zero, s));
   GemmPlan p = make_plan(cfg, hw.q8, rows, H);
   p.dtype = GT_E4M3;
   add_w(p, w->embed_head, V, static_cast<const uint8_t *>(head_fp8), 0);
@@ -978,7 +984,8 @@ bd_status bd_lm_head_topk_fp8(const bd_config *cfg, const bd_weights *w, const v
                                                   head_fp8_image_bytes(V, H));
   BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
   BD_TRY(launch_select_cand(hw.topk_val, hw.topk_idx, m_tiles, rows, n_cand, hw.ties, hw.cand, s));
-  BD_TRY(launch_rescore(w->embed_head, V, H, hidden, hw.cand, rows, n_cand, k, token_out, score_out, s));
+  BD_TRY(launch_rescore(w->embed_head, V, H, hidden, hw.cand, rows, n_cand, k, hw.cscore,
+                        hw.row_done, token_out, score_out, s));
   return BD_OK;
 }
 

@@ -151,7 +151,7 @@ __device__ __forceinline__ uint32_t fkey(float f) {
 __global__ void __launch_bounds__(1024) select_cand_kernel(const float *val, const int32_t *idx,
                                                            int m_tiles, int rows, int n_cand,
                                                            int32_t *ties, int32_t *cand) {
-  extern __shared__ uint32_t keys[];  // [N]
+  extern __shared__ uint32_t keys[];  // [N], then the per-warp histograms [32][256]
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_need, s_n_gt, s_n_tie;
   pdl_wait();
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(1024) select_cand_kernel(const float *val, con
   const int row = blockIdx.x, tid = threadIdx.x;
   const int N = m_tiles * kTopK;
   auto src = [&](int p) { return (static_cast<size_t>(p / kTopK) * rows + row) * kTopK + p % kTopK; };
+#pragma unroll 4
   for (int p = tid; p < N; p += blockDim.x) keys[p] = fkey(val[src(p)]);
   if (tid == 0) {
     s_prefix = 0u;
@@ -166,23 +167,48 @@ __global__ void __launch_bounds__(1024) select_cand_kernel(const float *val, con
     s_n_gt = 0u;
     s_n_tie = 0u;
   }
+  // The scores of a row crowd into few digits, so each warp counts into its own histogram
+  // (same-address atomics then only collide within a warp) and the 32 are summed.
+  uint32_t *whist = keys + N + ((tid >> 5) << 8);
   uint32_t mask = 0u;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int d = tid; d < 256; d += blockDim.x) hist[d] = 0u;
+    for (int d = tid; d < 32 * 256; d += blockDim.x) keys[N + d] = 0u;
     __syncthreads();
     const uint32_t prefix = s_prefix;
     for (int p = tid; p < N; p += blockDim.x)
-      if ((keys[p] & mask) == prefix) atomicAdd(&hist[(keys[p] >> shift) & 255u], 1u);
+      if ((keys[p] & mask) == prefix) atomicAdd(&whist[(keys[p] >> shift) & 255u], 1u);
     __syncthreads();
-    if (tid == 0) {  // the digit holding the need-th largest key, counting from the top
-      uint32_t need = s_need, cum = 0u;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= need) break;
-        cum += hist[d];
+    for (int d = tid; d < 256; d += blockDim.x) {
+      uint32_t t = 0u;
+#pragma unroll 8
+      for (int w = 0; w < 32; ++w) t += keys[N + w * 256 + d];
+      hist[d] = t;
+    }
+    __syncthreads();
+    if (tid < 32) {  // the digit holding the need-th largest key, counting from the top
+      // lane l owns digits 255 - 8l .. 248 - 8l; an inclusive scan of the lanes' counts
+      // gives how many keys lie above each lane's range
+      const uint32_t need = s_need;
+      uint32_t own = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) own += hist[255 - 8 * tid - e];
+      uint32_t incl = own;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += o;
       }
-      s_need = need - cum;
-      s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+      const uint32_t above = incl - own;
+      if (above < need && incl >= need) {  // exactly one lane
+        uint32_t cum = above;
+        int d = 255 - 8 * tid;
+        for (int e = 0; e < 7; ++e, --d) {
+          if (cum + hist[d] >= need) break;
+          cum += hist[d];
+        }
+        s_need = need - cum;
+        s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+      }
     }
     mask |= 255u << shift;
     __syncthreads();
@@ -213,54 +239,67 @@ __global__ void __launch_bounds__(1024) select_cand_kernel(const float *val, con
   }
 }
 
-// One CTA (512 threads) per row: exact scores E[cand] . h of the row's candidates (bf16
-// head rows, fp32 hidden row, fp32 sums), then the k best in candidate order.
+// Exact scores E[cand] . h of the candidates (bf16 head rows, fp32 hidden row, fp32 sums):
+// CTA (g, row) of 512 threads scores candidates 16 g .. 16 g + 15 of the row, one warp
+// each, into scores [rows][n_cand].  The row's last CTA to finish (a per-row counter,
+// cleared again by that CTA) then takes the k best in candidate order.
 __global__ void __launch_bounds__(512) rescore_kernel(const __nv_bfloat16 *E, int V, int H,
                                                       const float *hidden, const int32_t *cand,
-                                                      int n_cand, int k, int32_t *tok_out,
+                                                      int n_cand, int k, float *scores,
+                                                      unsigned *row_done, int32_t *tok_out,
                                                       float *score_out) {
-  extern __shared__ float sh[];  // [H] hidden row, then [n_cand] scores
-  float *sc = sh + H;
+  __shared__ unsigned s_last;
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float *x = hidden + static_cast<size_t>(row) * H;
-  for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4)
-    *reinterpret_cast<float4 *>(sh + j) = *reinterpret_cast<const float4 *>(x + j);
-  __syncthreads();
+  const int g = blockIdx.x, row = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t *cr = cand + static_cast<size_t>(row) * n_cand;
-  for (int c = warp; c < n_cand; c += 16) {
+  float *sr = scores + static_cast<size_t>(row) * n_cand;
+  const int c = g * 16 + warp;
+  if (c < n_cand) {
     int id = cr[c];
     if (id < 0 || id >= V) {
       if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
       id = 0;
     }
     const __nv_bfloat16 *e = E + static_cast<size_t>(id) * H;
+    const float *x = hidden + static_cast<size_t>(row) * H;
     float acc = 0.f;
+#pragma unroll 5
     for (int j = lane * 8; j < H; j += 256) {
       const uint4 u = *reinterpret_cast<const uint4 *>(e + j);
+      const float4 x0 = *reinterpret_cast<const float4 *>(x + j);
+      const float4 x1 = *reinterpret_cast<const float4 *>(x + j + 4);
       const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(p2[q]);
-        acc = fmaf(f.x, sh[j + 2 * q], acc);
-        acc = fmaf(f.y, sh[j + 2 * q + 1], acc);
-      }
+      const float2 f0 = __bfloat1622float2(p2[0]), f1 = __bfloat1622float2(p2[1]);
+      const float2 f2 = __bfloat1622float2(p2[2]), f3 = __bfloat1622float2(p2[3]);
+      acc = fmaf(f0.x, x0.x, acc);
+      acc = fmaf(f0.y, x0.y, acc);
+      acc = fmaf(f1.x, x0.z, acc);
+      acc = fmaf(f1.y, x0.w, acc);
+      acc = fmaf(f2.x, x1.x, acc);
+      acc = fmaf(f2.y, x1.y, acc);
+      acc = fmaf(f3.x, x1.z, acc);
+      acc = fmaf(f3.y, x1.w, acc);
     }
     acc = warp_sum(acc);
-    if (lane == 0) sc[c] = acc;
+    if (lane == 0) sr[c] = acc;
   }
+  __threadfence();
   __syncthreads();
-  if (warp != 0) return;
+  if (threadIdx.x == 0) s_last = atomicAdd(&row_done[row], 1u) == gridDim.x - 1 ? 1u : 0u;
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();
+  if (lane == 0) row_done[row] = 0u;  // ready for the next call
   // each lane keeps its (up to 8) candidates sorted; k rounds of a warp-wide best
   constexpr int kPer = 8;
   float lv[kPer];
   int li[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    const int c = lane + 32 * i;
-    lv[i] = c < n_cand ? sc[c] : -INFINITY;
-    li[i] = c < n_cand ? cr[c] : 0x7fffffff;
+    const int cc = lane + 32 * i;
+    lv[i] = cc < n_cand ? __ldcg(sr + cc) : -INFINITY;
+    li[i] = cc < n_cand ? cr[cc] : 0x7fffffff;
   }
 #pragma unroll
   for (int i = 1; i < kPer; ++i)
@@ -322,7 +361,9 @@ std::string launch_code_rows(const float *h, int rows, int H, void *q, ZeroSpan 
                                          static_cast<uint8_t *>(q), z));
 }
 
-size_t select_cand_smem(int m_tiles) { return static_cast<size_t>(m_tiles) * kTopK * 4; }
+size_t select_cand_smem(int m_tiles) {
+  return (static_cast<size_t>(m_tiles) * kTopK + 32 * 256) * sizeof(uint32_t);
+}
 
 std::string launch_select_cand(const float *val, const int32_t *idx, int m_tiles, int rows,
                                int n_cand, int32_t *ties, int32_t *cand, cudaStream_t s) {
@@ -341,20 +382,12 @@ std::string launch_select_cand(const float *val, const int32_t *idx, int m_tiles
 }
 
 std::string launch_rescore(const void *E, int V, int H, const float *hidden, const int32_t *cand,
-                           int rows, int n_cand, int k, int32_t *tok_out, float *score_out,
-                           cudaStream_t s) {
-  const size_t smem = (static_cast<size_t>(H) + n_cand) * sizeof(float);
-  static size_t set_to = 0;
-  if (smem > 48 * 1024 && smem > set_to) {
-    cudaError_t e = cudaFuncSetAttribute(rescore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return err("fp8 rescoring", e);
-    set_to = smem;
-  }
+                           int rows, int n_cand, int k, float *scores, unsigned *row_done,
+                           int32_t *tok_out, float *score_out, cudaStream_t s) {
   return err("fp8 rescoring",
-             launch_pdl(rescore_kernel, dim3(rows), dim3(512), smem, s,
+             launch_pdl(rescore_kernel, dim3((n_cand + 15) / 16, rows), dim3(512), 0, s,
                         static_cast<const __nv_bfloat16 *>(E), V, H, hidden, cand, n_cand, k,
-                        tok_out, score_out));
+                        scores, row_done, tok_out, score_out));
 }
 
 }  // namespace bd

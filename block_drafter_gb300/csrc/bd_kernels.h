@@ -160,9 +160,10 @@ std::string launch_code_rows(const float *h, int rows, int H, void *q, ZeroSpan 
 size_t select_cand_smem(int m_tiles);
 std::string launch_select_cand(const float *val, const int32_t *idx, int m_tiles, int rows,
                                int n_cand, int32_t *ties, int32_t *cand, cudaStream_t s);
+// scores [rows][n_cand] scratch; row_done [rows] counters, zero on entry and left zero.
 std::string launch_rescore(const void *E, int V, int H, const float *hidden, const int32_t *cand,
-                           int rows, int n_cand, int k, int32_t *tok_out, float *score_out,
-                           cudaStream_t s);
+                           int rows, int n_cand, int k, float *scores, unsigned *row_done,
+                           int32_t *tok_out, float *score_out, cudaStream_t s);
 // Last-write refinement: state export [T][H] u | [T] r | [T][Mc] G c (from pre [T][3 Mc]),
 // the predecessor candidates' codebook rows, the refined message (hi+lo pair), the
 // refined scores [B][K-1][kc][kc] and the greedy walk.

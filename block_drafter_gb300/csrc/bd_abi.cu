@@ -643,6 +643,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   // is added to the residual by the next row norm (ConvFinish), which writes x back.
   const bool conv = cfg->conv_group > 0;
   const int gw = cfg->conv_group, ND = conv ? 4 * H / gw : 0;
+  const bool mlp16 = pk != nullptr && packed_f16(cfg);  // fp16 MLP products (packed image)
   const ConvFinish no_fin{nullptr, nullptr, nullptr, 0};
   ConvFinish fin = no_fin;  // the previous layer's MLP finish, not yet added to x
   int copy_layer = -1;      // layer whose layers_out copy waits for that finish
@@ -760,29 +761,43 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.ld_out = H;
       BD_TRY(launch_gemm(p, sc, s));
     }
-    // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m)
+    // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m).  With the packed image
+    // (fp16 MLP matrices) m and the SwiGLU product are fp16 operands, else bf16 pairs.
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.post_norm, cfg->eps, NORM_PLAIN, rw.xn, nullptr,
-                          conv ? rw.cn : nullptr, nullptr, W, lo(H), s,
-                          conv ? ConvFinish{rw.cz, rw.cdelta_a, L.conv_base_a, gw} : no_fin));
+                          conv ? rw.cn : nullptr, nullptr, W, mlp16 ? 0 : lo(H), s,
+                          conv ? ConvFinish{rw.cz, rw.cdelta_a, L.conv_base_a, gw} : no_fin, mlp16));
     if (conv) {  // delta_m, then Conv_0(m)
-      BD_TRY(delta_gemm(rw.xn, T, L.conv_delta_m, PL.conv_m[l], rw.cdelta_m));
-      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_m, L.conv_base_m, T, H, gw, W, rw.xn, lo(H), s));
+      if (mlp16) {
+        GemmPlan p = make_plan(cfg, rw.xn, T, H);
+        p.dtype = GT_F16;
+        add_w(p, L.conv_delta_m, ND, pk, PL.conv_m[l]);
+        p.args.epi = EPI_STORE_F32;
+        p.args.out_f32 = rw.cdelta_m;
+        p.args.ld_out = ND;
+        BD_TRY(launch_gemm(p, sc, s));
+      } else {
+        BD_TRY(delta_gemm(rw.xn, T, L.conv_delta_m, PL.conv_m[l], rw.cdelta_m));
+      }
+      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_m, L.conv_base_m, T, H, gw, W, rw.xn,
+                                 mlp16 ? 0 : lo(H), s, mlp16));
     }
     {
       GemmPlan p = make_plan(cfg, rw.xn, T, H);
-      p.split = split;
+      p.split = split && !mlp16;
+      if (mlp16) p.dtype = GT_F16;
       add_w(p, L.w_gate, cfg->ffn, pk, PL.gate_up[l]);
       add_w(p, L.w_up, cfg->ffn, pk, PL.gate_up[l]);
       p.pair_mode = true;
       p.args.epi = EPI_SWIGLU;
       p.args.out_act = rw.hmid;
       p.args.ld_act = cfg->ffn;
-      p.args.act_lo = static_cast<long long>(lo(cfg->ffn));
+      p.args.act_lo = mlp16 ? 0 : static_cast<long long>(lo(cfg->ffn));
       BD_TRY(launch_gemm(p, sc, s));
     }
     {
       GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
-      p.split = split;
+      p.split = split && !mlp16;
+      if (mlp16) p.dtype = GT_F16;
       add_w(p, L.w_down, H, pk, PL.w_down[l]);
       p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
       p.args.out_f32 = conv ? rw.cz : rw.x;
@@ -868,14 +883,20 @@ static bd_status head_prepare(const bd_config *cfg, const bd_weights *w, const f
   cv.base = static_cast<char *>(workspace);
   carve_head(cv, hw, cfg, rows, num_sms());
   if (cv.off > workspace_bytes) return fail(BD_ERR_WORKSPACE, "workspace too small for the head");
-  const bool split = cfg->dtype == BD_BF16;
-  if (split)  // bf16 hi/lo pair of the fp32 hidden rows: the head sees ~16 mantissa bits
+  // With the packed image the head is fp16 and the hidden rows become fp16 operands;
+  // otherwise (bf16 head) a bf16 hi/lo pair of the fp32 rows, ~16 mantissa bits.
+  const bool head16 = w->packed != nullptr && packed_f16(cfg);
+  const bool split = cfg->dtype == BD_BF16 && !head16;
+  if (head16)
+    BD_TRY(launch_rows_f16(hidden, static_cast<size_t>(rows) * cfg->hidden, hw.hl, counters_of(hw.g), s));
+  else if (split)
     BD_TRY(launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hw.hl,
                              static_cast<size_t>(pad16(rows)) * cfg->hidden, counters_of(hw.g), s));
   else
     BD_TRY(launch_zero(counters_of(hw.g), s));
-  p = make_plan(cfg, split ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
+  p = make_plan(cfg, (split || head16) ? static_cast<const void *>(hw.hl) : hidden, rows, cfg->hidden);
   p.split = split;
+  if (head16) p.dtype = GT_F16;
   add_w(p, w->embed_head, cfg->vocab, static_cast<const uint8_t *>(w->packed),
         w->packed ? packed_layout(cfg).head : 0);
   return BD_OK;
@@ -1060,6 +1081,8 @@ bd_status bd_sync_status(void *stream_) {
   if (word & DEVERR_TIMEOUT) return fail(BD_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
   if (word & DEVERR_BAD_INDEX)
     return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");
+  if (word & DEVERR_RANGE)
+    return fail(BD_ERR_INVALID_ARG, "a weight packed as fp16 is beyond the fp16 range (|w| > 65504)");
   return BD_OK;
 }
 

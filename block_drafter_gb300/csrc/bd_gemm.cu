@@ -29,20 +29,30 @@ namespace bd {
 BD_DEFINE_ERROR_TAKER(take_error_word_gemm)
 
 template <typename T> struct MmaTraits;
+// kind: 0 = kind::f16 (fmt 0 fp16, 1 bf16), 1 = kind::tf32, 2 = kind::f8f6f4 (fmt 0 E4M3)
 template <> struct MmaTraits<__nv_bfloat16> {
   static constexpr int BK = 64;   // k elements per 128-byte smem row
-  static constexpr int UK = 16;   // k per tcgen05.mma (kind::f16)
+  static constexpr int UK = 16;   // k per tcgen05.mma
   static constexpr uint32_t fmt = 1;
+  static constexpr int kind = 0;
+};
+template <> struct MmaTraits<__half> {
+  static constexpr int BK = 64;
+  static constexpr int UK = 16;
+  static constexpr uint32_t fmt = 0;
+  static constexpr int kind = 0;
 };
 template <> struct MmaTraits<float> {
   static constexpr int BK = 32;
-  static constexpr int UK = 8;    // kind::tf32
+  static constexpr int UK = 8;
   static constexpr uint32_t fmt = 2;
+  static constexpr int kind = 1;
 };
 template <> struct MmaTraits<Fp8E4M3> {
   static constexpr int BK = 128;
-  static constexpr int UK = 32;   // kind::f8f6f4, E4M3 operands (format code 0)
+  static constexpr int UK = 32;
   static constexpr uint32_t fmt = 0;
+  static constexpr int kind = 2;
 };
 
 constexpr int kATileBytes = kBM * 128;  // 16 KB: 128 rows x 128 bytes
@@ -242,9 +252,9 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
           const uint64_t ad = umma_desc_sw128(abase + j * kATileBytes + k * 32);
           const uint64_t bd = umma_desc_sw128(bbase + j * box_b + k * 32);
           const uint32_t acc = (kbi > kb0 || j > 0 || k > 0) ? 1u : 0u;
-          if constexpr (MmaTraits<T>::fmt == 1)
-            umma_bf16(d, ad, bd, idesc, acc);
-          else if constexpr (MmaTraits<T>::fmt == 2)
+          if constexpr (MmaTraits<T>::kind == 0)
+            umma_bf16(d, ad, bd, idesc, acc);  // kind::f16 (the idesc selects bf16 / fp16)
+          else if constexpr (MmaTraits<T>::kind == 1)
             umma_tf32(d, ad, bd, idesc, acc);
           else
             umma_f8(d, ad, bd, idesc, acc);
@@ -872,7 +882,7 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return "cuTensorMapEncodeTiled is unavailable";
-  const int elem = dtype == GT_BF16 ? 2 : (dtype == GT_E4M3 ? 1 : 4);
+  const int elem = (dtype == GT_BF16 || dtype == GT_F16) ? 2 : (dtype == GT_E4M3 ? 1 : 4);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                         static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride) * elem,
@@ -881,7 +891,8 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
                        static_cast<cuuint32_t>(planes)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
-  const CUtensorMapDataType ty = dtype == GT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+  const CUtensorMapDataType ty = dtype == GT_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == GT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                  : dtype == GT_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUresult r = fn(&m, ty,
@@ -969,7 +980,8 @@ static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStr
 
 std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stream) {
   GemmArgs &a = plan.args;
-  const int BK = plan.dtype == GT_BF16 ? 64 : (plan.dtype == GT_E4M3 ? 128 : 32);  // 128 bytes
+  const int BK = (plan.dtype == GT_BF16 || plan.dtype == GT_F16) ? 64
+                 : (plan.dtype == GT_E4M3 ? 128 : 32);  // 128 bytes
   if (plan.n_tokens <= 0 || plan.K <= 0 || plan.n_w <= 0) return "empty GEMM";
   if (plan.n_w > kMaxSegs) return "too many GEMM segments";
   a.K = plan.K;
@@ -1036,14 +1048,14 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   memset(&maps, 0, sizeof maps);
   a.packed = plan.w[0].packed != nullptr ? 1 : 0;
   if (a.packed) {
-    const int elem = plan.dtype == GT_BF16 ? 2 : (plan.dtype == GT_E4M3 ? 1 : 4);
+    const int elem = (plan.dtype == GT_BF16 || plan.dtype == GT_F16) ? 2 : (plan.dtype == GT_E4M3 ? 1 : 4);
     for (int s = 0; s < a.n_segs; ++s) {
       if (!plan.w[s].packed) return "packed GEMM with an unpacked segment";
       a.seg[s].packed = static_cast<const uint8_t *>(plan.w[s].packed);
       a.seg[s].n_kb_pack = static_cast<int>(packed_kb(plan.K, elem));
     }
   } else {
-    if (plan.dtype == GT_E4M3) return "FP8 GEMMs need packed weights";
+    if (plan.dtype == GT_E4M3 || plan.dtype == GT_F16) return "FP8 / fp16 GEMMs need packed weights";
     for (int s = 0; s < plan.n_w; ++s) {
       std::string err = make_map(&maps.a[s], plan.w[s].ptr, plan.dtype, plan.K, plan.w[s].rows, BK,
                                  plan.pair_mode ? 64 : kBM);
@@ -1078,6 +1090,8 @@ std::string launch_gemm(GemmPlan &plan, const GemmScratch &sc, cudaStream_t stre
   if (plan.dtype == GT_E4M3) {
     if (a.epi != EPI_TOPK || plan.split || plan.pair_mode) return "FP8 GEMMs support the top-k epilogue only";
     e = launch_epi<Fp8E4M3, EPI_TOPK>(maps, a, stream);
+  } else if (plan.dtype == GT_F16) {
+    e = launch_typed<__half>(maps, a, stream);
   } else {
     e = plan.dtype == GT_BF16 ? launch_typed<__nv_bfloat16>(maps, a, stream)
                               : launch_typed<float>(maps, a, stream);

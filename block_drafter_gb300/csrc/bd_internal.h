@@ -13,7 +13,7 @@
 namespace bd {
 
 // Device error word flags (set by kernels, read and cleared by bd_sync_status()).
-enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u };
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u, DEVERR_RANGE = 4u };
 
 // ------------------------------------------------------------------ GEMM
 // D[tok, out] = X[tok, :] . W[out, :]  computed swap-AB on tcgen05: weight rows fill the
@@ -89,9 +89,9 @@ struct GemmWeight {
   int rows;
   const void *packed;  // packed image of the matrix (pair mode: the interleaved pair), or null
 };
-// Operand element type of a GEMM: bf16, fp32 (tf32 products) or FP8 e4m3 (both operands
-// one byte per element; packed weights only).
-enum GemmType : int { GT_BF16 = 0, GT_F32 = 1, GT_E4M3 = 2 };
+// Operand element type of a GEMM: bf16, fp32 (tf32 products), FP8 e4m3 (both operands one
+// byte per element; packed weights only) or fp16 (packed weights converted from bf16).
+enum GemmType : int { GT_BF16 = 0, GT_F32 = 1, GT_E4M3 = 2, GT_F16 = 3 };
 struct Fp8E4M3 {
   uint8_t bits;
 };
@@ -139,6 +139,11 @@ struct PackedLayout {
   size_t total;
 };
 PackedLayout packed_layout(const bd_config *c);
+// In a bf16 config the packed image stores the MLP matrices (gate/up, down, and the MLP
+// branch's convolution delta) and the head as fp16: those products take fp16 activations
+// (one operand of 11 significant bits instead of a bf16 hi+lo pair), which halves their
+// tensor work and activation traffic.  Other matrices stay bf16.
+inline bool packed_f16(const bd_config *c) { return c->dtype == BD_BF16; }
 std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cudaStream_t s);
 unsigned take_error_word_pack();
 

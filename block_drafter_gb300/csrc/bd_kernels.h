@@ -84,18 +84,22 @@ struct ConvFinish {
 };
 // Row norm of x (one CTA per row).  lo_off != 0: also write the rounding residual y - hi
 // at out + lo_off (split activation).  f32_out: an fp32 copy of y, or null.
+// out_f16 (bf16 config): the output is fp16 (lo_off must then be 0).
 std::string launch_rownorm(int dtype, float *x, int rows, int H, const void *gain,
                            float eps, int mode, void *out, float *r_out, float *f32_out,
                            float *head_out, int W, size_t lo_off, cudaStream_t s,
-                           const ConvFinish &cf = ConvFinish{nullptr, nullptr, nullptr, 0});
+                           const ConvFinish &cf = ConvFinish{nullptr, nullptr, nullptr, 0},
+                           bool out_f16 = false);
 // DFlash2 branch input: out = Conv_0(X) (side-0 grouped convolution of the normalised
 // branch input X [rows][H] fp32 with delta [rows][2][2][H/gw]), split when lo_off != 0.
 std::string launch_conv_prepare(int dtype, const float *X, const float *delta, const void *base,
                                 int rows, int H, int gw, int W, void *out, size_t lo_off,
-                                cudaStream_t s);
+                                cudaStream_t s, bool out_f16 = false);
 // fp32 -> bf16 hi (dst) and lo (dst + lo_off) of n elements.
 std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,
                               cudaStream_t s);
+// fp32 -> fp16 of n elements.
+std::string launch_rows_f16(const float *src, size_t n, void *dst, ZeroSpan z, cudaStream_t s);
 
 // c = sqrt(Rc) z / (||z|| + eps) for non-anchor rows; sqrt(Rc) * codebook[anchor] for anchors.
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,

@@ -122,16 +122,20 @@ extern "C" bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_we
   cudaStream_t s = static_cast<cudaStream_t>(stream_);
   // the first kernel clears the tile counters before the GEMM uses them
   const ZeroSpan zero{counters, 2 * m_tiles};
-  const bool split = cfg->dtype == BD_BF16;
+  // the packed head is fp16 in a bf16 config (fp16 hidden rows); the raw head takes the
+  // rows as a bf16 hi/lo pair
+  const bool head16 = w->packed != nullptr && packed_f16(cfg);
+  const bool split = cfg->dtype == BD_BF16 && !head16;
   const size_t pad = (static_cast<size_t>(rows) + 15) / 16 * 16;
-  err = split ? launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hl,
-                                  pad * cfg->hidden, zero, s)
-              : launch_zero(zero, s);
+  err = head16  ? launch_rows_f16(hidden, static_cast<size_t>(rows) * cfg->hidden, hl, zero, s)
+        : split ? launch_split_rows(hidden, static_cast<size_t>(rows) * cfg->hidden, hl,
+                                    pad * cfg->hidden, zero, s)
+                : launch_zero(zero, s);
   if (!err.empty()) return fail(BD_ERR_CUDA, err);
   GemmPlan p;
   memset(&p, 0, sizeof p);
-  p.dtype = split ? 0 : 1;
-  p.x = split ? static_cast<const void *>(hl) : hidden;
+  p.dtype = head16 ? GT_F16 : (split ? GT_BF16 : GT_F32);
+  p.x = (split || head16) ? static_cast<const void *>(hl) : hidden;
   p.n_tokens = rows;
   p.K = cfg->hidden;
   p.split = split;

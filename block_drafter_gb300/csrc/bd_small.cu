@@ -84,6 +84,13 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bf
   return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
 template <typename T> __device__ __forceinline__ void store4(T *p, int i4, float4 v);
+template <> __device__ __forceinline__ void store4<__half>(__half *p, int i4, float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&b);
+  reinterpret_cast<uint2 *>(p)[i4] = u;
+}
 template <> __device__ __forceinline__ void store4<float>(float *p, int i4, float4 v) {
   reinterpret_cast<float4 *>(p)[i4] = v;
 }
@@ -123,9 +130,10 @@ __device__ __forceinline__ float4 conv_row4(const float *X, const float *delta, 
   return o;
 }
 
-template <typename T>
+// T: weight (gain, convolution base) type; O: the normalised output's type.
+template <typename T, typename O>
 __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *gain, float eps,
-                                                      int mode, T *out, float *r_out,
+                                                      int mode, O *out, float *r_out,
                                                       float *f32_out, float *head_out, int W,
                                                       size_t lo_off, ConvFinish cf) {
   __shared__ float red[32];
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
     scale = rsqrtf(ss / H + eps);
   }
   const int i = row % W;
-  T *orow = (mode == NORM_FINAL) ? nullptr : out + static_cast<size_t>(row) * H;
+  O *orow = (mode == NORM_FINAL) ? nullptr : out + static_cast<size_t>(row) * H;
   float *hrow = nullptr;
   if (mode == NORM_FINAL && head_out != nullptr && i > 0)
     hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
@@ -186,13 +194,13 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
       y.w *= g.w;
     }
     if (orow) {
-      store4<T>(orow, i4, y);
+      store4<O>(orow, i4, y);
       if (lo_off && mode == NORM_CTX) {
-        store4<T>(orow + lo_off, i4, make_float4(0.f, 0.f, 0.f, 0.f));
+        store4<O>(orow + lo_off, i4, make_float4(0.f, 0.f, 0.f, 0.f));
       } else if (lo_off) {  // residual of the rounding: hi + lo carries ~16 mantissa bits
-        const float4 h = make_float4(to_f<T>(from_f<T>(y.x)), to_f<T>(from_f<T>(y.y)),
-                                     to_f<T>(from_f<T>(y.z)), to_f<T>(from_f<T>(y.w)));
-        store4<T>(orow + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+        const float4 h = make_float4(to_f<O>(from_f<O>(y.x)), to_f<O>(from_f<O>(y.y)),
+                                     to_f<O>(from_f<O>(y.z)), to_f<O>(from_f<O>(y.w)));
+        store4<O>(orow + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
       }
     }
     if (hrow) reinterpret_cast<float4 *>(hrow)[i4] = y;
@@ -216,22 +224,22 @@ __device__ __forceinline__ void store_split(T *p, size_t i, size_t lo_off, float
 
 // DFlash2 branch input: out[row] = Conv_0(X)[row] (the side-0 convolution of the
 // normalised branch input), as a split pair when lo_off != 0.  One CTA per block row.
-template <typename T>
+template <typename T, typename O>
 __global__ void __launch_bounds__(256) conv_prepare_kernel(const float *X, const float *delta,
                                                            const T *base, int H, int gw, int W,
-                                                           T *out, size_t lo_off) {
+                                                           O *out, size_t lo_off) {
   const int row = blockIdx.x;
   pdl_wait();
   pdl_trigger();
   const bool has_prev = (row % W) != 0;
-  T *o = out + static_cast<size_t>(row) * H;
+  O *o = out + static_cast<size_t>(row) * H;
   for (int i4 = threadIdx.x; i4 < H / 4; i4 += blockDim.x) {
     const float4 y = conv_row4<T>(X, delta, base, H, gw, 0, row, has_prev, i4);
-    store4<T>(o, i4, y);
+    store4<O>(o, i4, y);
     if (lo_off) {
-      const float4 h = make_float4(to_f<T>(from_f<T>(y.x)), to_f<T>(from_f<T>(y.y)),
-                                   to_f<T>(from_f<T>(y.z)), to_f<T>(from_f<T>(y.w)));
-      store4<T>(o + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
+      const float4 h = make_float4(to_f<O>(from_f<O>(y.x)), to_f<O>(from_f<O>(y.y)),
+                                   to_f<O>(from_f<O>(y.z)), to_f<O>(from_f<O>(y.w)));
+      store4<O>(o + lo_off, i4, make_float4(y.x - h.x, y.y - h.y, y.z - h.z, y.w - h.w));
     }
   }
 }
@@ -553,6 +561,16 @@ __global__ void __launch_bounds__(32) topk_final_kernel(const float *part_val,
 }
 
 // fp32 rows -> bf16 hi rows [0, rows) and lo rows [lo_row, lo_row + rows).
+// fp32 -> fp16 (the operand type of the head's products when its packed copy is fp16).
+__global__ void rows_f16_kernel(const float *src, size_t n, __half *dst, ZeroSpan z) {
+  pdl_wait();
+  pdl_trigger();
+  zero_span(z);
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[t] = __float2half_rn(src[t]);
+}
+
 __global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off,
                                   ZeroSpan z) {
   pdl_wait();
@@ -821,14 +839,18 @@ std::string launch_zero(ZeroSpan z, cudaStream_t s) {
 
 std::string launch_rownorm(int dtype, float *x, int rows, int H, const void *gain, float eps,
                            int mode, void *out, float *r_out, float *f32_out, float *head_out, int W,
-                           size_t lo_off, cudaStream_t s, const ConvFinish &cf) {
+                           size_t lo_off, cudaStream_t s, const ConvFinish &cf, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(rownorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, x, H,
-                   static_cast<const __nv_bfloat16 *>(gain), eps, mode,
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(rownorm_kernel<__nv_bfloat16, __half>, dim3(rows), dim3(256), 0, s, x, H,
+                   static_cast<const __nv_bfloat16 *>(gain), eps, mode, static_cast<__half *>(out),
+                   r_out, f32_out, head_out, W, lo_off, cf);
+  else if (dtype == 0)
+    e = launch_pdl(rownorm_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s, x,
+                   H, static_cast<const __nv_bfloat16 *>(gain), eps, mode,
                    static_cast<__nv_bfloat16 *>(out), r_out, f32_out, head_out, W, lo_off, cf);
   else
-    e = launch_pdl(rownorm_kernel<float>, dim3(rows), dim3(256), 0, s, x, H,
+    e = launch_pdl(rownorm_kernel<float, float>, dim3(rows), dim3(256), 0, s, x, H,
                    static_cast<const float *>(gain), eps, mode, static_cast<float *>(out), r_out,
                    f32_out, head_out, W, lo_off, cf);
   return err("rownorm", e);
@@ -836,16 +858,26 @@ std::string launch_rownorm(int dtype, float *x, int rows, int H, const void *gai
 
 std::string launch_conv_prepare(int dtype, const float *X, const float *delta, const void *base,
                                 int rows, int H, int gw, int W, void *out, size_t lo_off,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(conv_prepare_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, X, delta,
-                   static_cast<const __nv_bfloat16 *>(base), H, gw, W,
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(conv_prepare_kernel<__nv_bfloat16, __half>, dim3(rows), dim3(256), 0, s, X,
+                   delta, static_cast<const __nv_bfloat16 *>(base), H, gw, W,
+                   static_cast<__half *>(out), lo_off);
+  else if (dtype == 0)
+    e = launch_pdl(conv_prepare_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s,
+                   X, delta, static_cast<const __nv_bfloat16 *>(base), H, gw, W,
                    static_cast<__nv_bfloat16 *>(out), lo_off);
   else
-    e = launch_pdl(conv_prepare_kernel<float>, dim3(rows), dim3(256), 0, s, X, delta,
+    e = launch_pdl(conv_prepare_kernel<float, float>, dim3(rows), dim3(256), 0, s, X, delta,
                    static_cast<const float *>(base), H, gw, W, static_cast<float *>(out), lo_off);
   return err("conv prepare", e);
+}
+
+std::string launch_rows_f16(const float *src, size_t n, void *dst, ZeroSpan z, cudaStream_t s) {
+  const size_t blocks = (n + 255) / 256;
+  return err("fp16 rows", launch_pdl(rows_f16_kernel, dim3(blocks < 2048 ? blocks : 2048),
+                                     dim3(256), 0, s, src, n, static_cast<__half *>(dst), z));
 }
 
 std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_off, ZeroSpan z,

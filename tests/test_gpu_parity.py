@@ -187,8 +187,11 @@ def test_round_is_deterministic_and_requests_independent():
 
 @pytest.mark.parametrize("geo", [SMALL_BF16, bdsynth.TINY])
 def test_packed_and_raw_weights_give_identical_results(geo):
-    """The packed image is a permutation of the weights: materialisation, round and head
-    must be bit-identical with and without it."""
+    """The packed image is a permutation of the weights, except that in a bf16 config it
+    stores the MLP and head matrices as fp16 (their products then take fp16 activations
+    instead of bf16 hi+lo pairs).  Materialisation is bit-identical with and without it;
+    in the fp32 config so are the round and the head.  In bf16 both paths meet the oracle
+    and agree with each other to 2e-3, tokens equal where the oracle's gap exceeds 1e-2."""
     a = Hn.Case(geo, seed=8, max_ctx_rows=128, packed=True)
     b = Hn.Case(geo, seed=8, max_ctx_rows=128, packed=False, weights=a.w_host)
     a.fill_rings()
@@ -196,5 +199,12 @@ def test_packed_and_raw_weights_give_identical_results(geo):
     for l in range(geo.n_layers):
         assert torch.equal(a.sess.k[l], b.sess.k[l]) and torch.equal(a.sess.v[l], b.sess.v[l])
     ga, gb = a.run_gpu(), b.run_gpu()
-    for key in ("layers", "hidden", "tokens", "max_logit"):
-        assert torch.equal(ga[key], gb[key]), key
+    if geo.dtype == "f32":
+        for key in ("layers", "hidden", "tokens", "max_logit"):
+            assert torch.equal(ga[key], gb[key]), key
+        return
+    ref = a.run_oracle()
+    for case, g in ((a, ga), (b, gb)):
+        rep = Hn.compare_round(case, g, ref, tol=TOL)
+        assert rep["ok"], rep
+    assert Hn.rel_err(Hn.np32(ga["hidden"]), Hn.np32(gb["hidden"])) <= 2e-3

@@ -643,7 +643,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   // is added to the residual by the next row norm (ConvFinish), which writes x back.
   const bool conv = cfg->conv_group > 0;
   const int gw = cfg->conv_group, ND = conv ? 4 * H / gw : 0;
-  const bool mlp16 = pk != nullptr && packed_f16(cfg);  // fp16 MLP products (packed image)
+  // packed image of a bf16 config: the MLP and head products and the attention take fp16
+  // operands (one 16-bit operand instead of a bf16 hi+lo pair)
+  const bool mlp16 = pk != nullptr && packed_f16(cfg);
   const ConvFinish no_fin{nullptr, nullptr, nullptr, 0};
   ConvFinish fin = no_fin;  // the previous layer's MLP finish, not yet added to x
   int copy_layer = -1;      // layer whose layers_out copy waits for that finish
@@ -698,17 +700,18 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       h.W = W;
       h.eps = cfg->eps;
       h.rope = rw.rope;
-      const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
-      const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
-      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo};
-      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo};
-      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo};
+      const size_t qlo = split && !mlp16 ? static_cast<size_t>(T) * QD : 0;
+      const size_t klo = split && !mlp16 ? static_cast<size_t>(T) * KD : 0;
+      const int a16 = mlp16 ? 1 : 0;
+      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo, a16};
+      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo, a16};
+      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo, a16};
       h.n_groups = 1;
       h.grp[0] = HeadGroup{0, T, 0, 3, cfg->n_q_heads + 2 * cfg->n_kv_heads};
       if (fuse) {  // the pending rows' context K/V go to the rings (before attention)
         const int cap = cfg->ring_capacity[l];
-        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0};
-        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0};
+        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0, 0};
+        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0, 0};
         h.n_groups = 2;
         h.grp[1] = HeadGroup{T, n_pend, 3, 2, 2 * cfg->n_kv_heads};
         h.n_req = B;
@@ -745,8 +748,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.block_split = att_block_split(cfg, l, a.n_splits) ? 1 : 0;
       a.n_guard = n_pend > 0 ? kMaxPendPerReq : 0;
       a.max_keys = att_max_keys(cfg, l, W);
-      a.q_lo = split ? static_cast<size_t>(T) * QD : 0;
-      a.blk_lo = split ? static_cast<size_t>(T) * KD : 0;
+      a.f16 = mlp16 ? 1 : 0;
+      a.q_lo = split && !mlp16 ? static_cast<size_t>(T) * QD : 0;
+      a.blk_lo = split && !mlp16 ? static_cast<size_t>(T) * KD : 0;
       a.out_lo = lo(QD);
       BD_TRY(launch_attention(a, dt, s));
     }

@@ -47,6 +47,33 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 8 bf16 values (16 bytes of shared memory) rewritten in place as fp16, saturating at
+// +-65504 (exact for every bf16 value of magnitude 2^-14 .. 65504).
+__device__ __forceinline__ void bf16x8_to_f16_inplace(__nv_bfloat16 *p) {
+  uint4 v = *reinterpret_cast<const uint4 *>(p);
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+    f.x = fminf(fmaxf(f.x, -65504.f), 65504.f);
+    f.y = fminf(fmaxf(f.y, -65504.f), 65504.f);
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    w[i] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint32_t pack_f16(float x0, float x1) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
@@ -256,7 +283,10 @@ __device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int
 // pairs (fp32 accumulate), so their rounding does not reach the output; the ring's K/V
 // are exact bf16 data.  The block's own keys/values (produced this round, hi+lo) are
 // processed by the last split in a separate 16-key pass.
-template <int D>
+// F16: Q, P and the block's keys/values are single fp16 operands (11 significant bits) and
+// each ring tile is rewritten as fp16 in shared memory once it lands (exact within fp16's
+// range): half the MMAs of the hi+lo form.
+template <int D, bool F16>
 __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_constant__ AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int RS = D + kAttPad;  // smem row stride (elements)
@@ -299,16 +329,27 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   // Block keys/values [Kh; Kl; Vh; Vl] (16 rows each, rows >= W zero) go into the K
   // buffer the context loop leaves free after its last block (buffer n_blocks & 1); they
   // are loaded while that last block is processed.
-  auto load_block = [&](int buf) {
+  auto load_block = [&](int buf) {  // F16: [K; V], 16 rows each
     __nv_bfloat16 *dstb = sK + buf * kAttKeys * RS;
-    for (int c = tid; c < 4 * 16 * CPR; c += 128) {
+    for (int c = tid; c < (F16 ? 2 : 4) * 16 * CPR; c += 128) {
       const int part = c / (16 * CPR), cc = c % (16 * CPR);
       const int j = cc / CPR, ch = cc % CPR;
       const bool valid = j < a.W;
-      const __nv_bfloat16 *base = (part < 2 ? blk_k : blk_v) + ((part & 1) ? a.blk_lo : 0);
+      const __nv_bfloat16 *base = F16 ? (part == 0 ? blk_k : blk_v)
+                                      : (part < 2 ? blk_k : blk_v) + ((part & 1) ? a.blk_lo : 0);
       const __nv_bfloat16 *src =
           base + ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.W + (valid ? j : 0)) * D + ch * 8;
       cp_async16(smem_u32(dstb + (part * 16 + j) * RS + ch * 8), src, valid);
+    }
+  };
+
+  // F16: the ring chunks this thread loaded into buffer `buf`, rewritten as fp16 (called
+  // after its copies have landed and before the barrier that publishes the tile)
+  auto convert_kv = [&](int buf) {
+    for (int c = tid; c < kAttKeys * CPR; c += 128) {
+      const int kr = c / CPR, ch = c % CPR;
+      bf16x8_to_f16_inplace(sK + (buf * kAttKeys + kr) * RS + ch * 8);
+      bf16x8_to_f16_inplace(sV + (buf * kAttKeys + kr) * RS + ch * 8);
     }
   };
 
@@ -332,7 +373,7 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   pdl_wait();
   pdl_trigger();
   // Q tiles: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
-  for (int c = tid; c < 2 * kAttRows * CPR; c += 128) {
+  for (int c = tid; c < (F16 ? 1 : 2) * kAttRows * CPR; c += 128) {
     const int part = c / (kAttRows * CPR), cc = c % (kAttRows * CPR);
     const int rr = cc / CPR, ch = cc % CPR;
     const bool valid = rr < R;
@@ -348,6 +389,7 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   // the first context position every block row can see: keys from here on need no mask
   const long long p_all = a.window > 0 ? g.F + a.W - a.window : LLONG_MIN;
   cp_async_wait<0>();
+  if (F16 && n_blocks > 0) convert_kv(0);
   __syncthreads();
 
   // A fragments of Q (hi or lo) for k-step ks
@@ -373,7 +415,7 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t qh[4], ql[4];
       q_frag(0, ks, qh);
-      q_frag(1, ks, ql);
+      if (!F16) q_frag(1, ks, ql);
 #pragma unroll
       for (int nt = 0; nt < kAttKeys / 8; nt += 2) {
         const int mi = lane >> 3;
@@ -381,10 +423,15 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
         const int col = ks * 16 + (mi & 1) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(smem_u32(sK + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        mma16816(s[nt], qh, b0, b1);
-        mma16816(s[nt + 1], qh, b2, b3);
-        mma16816(s[nt], ql, b0, b1);
-        mma16816(s[nt + 1], ql, b2, b3);
+        if constexpr (F16) {
+          mma16816_f16(s[nt], qh, b0, b1);
+          mma16816_f16(s[nt + 1], qh, b2, b3);
+        } else {
+          mma16816(s[nt], qh, b0, b1);
+          mma16816(s[nt + 1], qh, b2, b3);
+          mma16816(s[nt], ql, b0, b1);
+          mma16816(s[nt + 1], ql, b2, b3);
+        }
       }
     }
     if (k0 + kAttKeys <= g.k_end && g.p_lo + k0 >= p_all) {  // every key visible to every row
@@ -416,10 +463,17 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
 #pragma unroll
     for (int kk = 0; kk < kAttKeys / 16; ++kk) {
       uint32_t ph[4], pl[4];
-      split_pack(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-      split_pack(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-      split_pack(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-      split_pack(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+      if constexpr (F16) {
+        ph[0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
+        ph[1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
+        ph[2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        ph[3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      } else {
+        split_pack(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+        split_pack(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+        split_pack(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+        split_pack(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+      }
 #pragma unroll
       for (int nd = 0; nd < D / 8; nd += 2) {
         const int mi = lane >> 3;
@@ -427,13 +481,19 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
         const int col = (nd + (mi >> 1)) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(smem_u32(sV + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        mma16816(o[nd], ph, b0, b1);
-        mma16816(o[nd + 1], ph, b2, b3);
-        mma16816(o[nd], pl, b0, b1);
-        mma16816(o[nd + 1], pl, b2, b3);
+        if constexpr (F16) {
+          mma16816_f16(o[nd], ph, b0, b1);
+          mma16816_f16(o[nd + 1], ph, b2, b3);
+        } else {
+          mma16816(o[nd], ph, b0, b1);
+          mma16816(o[nd + 1], ph, b2, b3);
+          mma16816(o[nd], pl, b0, b1);
+          mma16816(o[nd + 1], pl, b2, b3);
+        }
       }
     }
     cp_async_wait<0>();
+    if (F16 && blk + 1 < n_blocks) convert_kv(buf ^ 1);
     __syncthreads();
   }
 
@@ -442,8 +502,10 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
       cp_async_wait<0>();
       __syncthreads();
     }
-    const __nv_bfloat16 *sB = sK + (n_blocks & 1) * kAttKeys * RS;  // [Kh; Kl; Vh; Vl]
-    // S = Qh Kh + Ql Kh + Qh Kl over the (up to) 16 block keys
+    // [Kh; Kl; Vh; Vl] (F16: [K; V]), 16 rows each
+    const __nv_bfloat16 *sB = sK + (n_blocks & 1) * kAttKeys * RS;
+    constexpr int kV = F16 ? 1 : 2;  // first V part
+    // S = Qh Kh + Ql Kh + Qh Kl over the (up to) 16 block keys (F16: Q K)
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -451,19 +513,24 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t qh[4], ql[4];
       q_frag(0, ks, qh);
-      q_frag(1, ks, ql);
       const int mi = lane >> 3;
       const int key = (mi >> 1) * 8 + (lane & 7);
       const int col = ks * 16 + (mi & 1) * 8;
       uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
       ldsm_x4(smem_u32(sB + (0 * 16 + key) * RS + col), h0, h1, h2, h3);
-      ldsm_x4(smem_u32(sB + (1 * 16 + key) * RS + col), l0, l1, l2, l3);
-      mma16816(s[0], qh, h0, h1);
-      mma16816(s[1], qh, h2, h3);
-      mma16816(s[0], ql, h0, h1);
-      mma16816(s[1], ql, h2, h3);
-      mma16816(s[0], qh, l0, l1);
-      mma16816(s[1], qh, l2, l3);
+      if constexpr (F16) {
+        mma16816_f16(s[0], qh, h0, h1);
+        mma16816_f16(s[1], qh, h2, h3);
+      } else {
+        q_frag(1, ks, ql);
+        ldsm_x4(smem_u32(sB + (1 * 16 + key) * RS + col), l0, l1, l2, l3);
+        mma16816(s[0], qh, h0, h1);
+        mma16816(s[1], qh, h2, h3);
+        mma16816(s[0], ql, h0, h1);
+        mma16816(s[1], ql, h2, h3);
+        mma16816(s[0], qh, l0, l1);
+        mma16816(s[1], qh, l2, l3);
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -484,24 +551,36 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
       o[n][3] *= alpha[1];
     }
     uint32_t ph[4], pl[4];
-    split_pack(s[0][0], s[0][1], ph[0], pl[0]);
-    split_pack(s[0][2], s[0][3], ph[1], pl[1]);
-    split_pack(s[1][0], s[1][1], ph[2], pl[2]);
-    split_pack(s[1][2], s[1][3], ph[3], pl[3]);
+    if constexpr (F16) {
+      ph[0] = pack_f16(s[0][0], s[0][1]);
+      ph[1] = pack_f16(s[0][2], s[0][3]);
+      ph[2] = pack_f16(s[1][0], s[1][1]);
+      ph[3] = pack_f16(s[1][2], s[1][3]);
+    } else {
+      split_pack(s[0][0], s[0][1], ph[0], pl[0]);
+      split_pack(s[0][2], s[0][3], ph[1], pl[1]);
+      split_pack(s[1][0], s[1][1], ph[2], pl[2]);
+      split_pack(s[1][2], s[1][3], ph[3], pl[3]);
+    }
 #pragma unroll
     for (int nd = 0; nd < D / 8; nd += 2) {
       const int mi = lane >> 3;
       const int key = (mi & 1) * 8 + (lane & 7);
       const int col = (nd + (mi >> 1)) * 8;
       uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-      ldsm_x4_t(smem_u32(sB + (2 * 16 + key) * RS + col), h0, h1, h2, h3);
-      ldsm_x4_t(smem_u32(sB + (3 * 16 + key) * RS + col), l0, l1, l2, l3);
-      mma16816(o[nd], ph, h0, h1);
-      mma16816(o[nd + 1], ph, h2, h3);
-      mma16816(o[nd], pl, h0, h1);
-      mma16816(o[nd + 1], pl, h2, h3);
-      mma16816(o[nd], ph, l0, l1);
-      mma16816(o[nd + 1], ph, l2, l3);
+      ldsm_x4_t(smem_u32(sB + (kV * 16 + key) * RS + col), h0, h1, h2, h3);
+      if constexpr (F16) {
+        mma16816_f16(o[nd], ph, h0, h1);
+        mma16816_f16(o[nd + 1], ph, h2, h3);
+      } else {
+        ldsm_x4_t(smem_u32(sB + (3 * 16 + key) * RS + col), l0, l1, l2, l3);
+        mma16816(o[nd], ph, h0, h1);
+        mma16816(o[nd + 1], ph, h2, h3);
+        mma16816(o[nd], pl, h0, h1);
+        mma16816(o[nd + 1], pl, h2, h3);
+        mma16816(o[nd], ph, l0, l1);
+        mma16816(o[nd + 1], ph, l2, l3);
+      }
     }
   }
 
@@ -651,25 +730,14 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
     return {};
   }
   const size_t smem = attention_smem_bytes(a.head_dim);
-  if (a.head_dim == 128) {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(attention_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-      set = true;
-    }
-    e = launch_pdl(attention_bf16_kernel<128>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128),
-                   smem, stream, a);
-  } else {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(attention_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-      set = true;
-    }
-    e = launch_pdl(attention_bf16_kernel<64>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128), smem,
-                   stream, a);
-  }
+  auto go = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    return launch_pdl(kernel, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128), smem, stream, a);
+  };
+  if (a.head_dim == 128)
+    e = a.f16 ? go(attention_bf16_kernel<128, true>) : go(attention_bf16_kernel<128, false>);
+  else
+    e = a.f16 ? go(attention_bf16_kernel<64, true>) : go(attention_bf16_kernel<64, false>);
   if (e != cudaSuccess) return std::string("attention launch: ") + cudaGetErrorString(e);
   return {};
 }

@@ -24,6 +24,8 @@ struct AttArgs {
   int block_split;      // 1: the last split takes only the block's own keys (n_splits >= 2)
   int n_guard;          // context positions >= F - n_guard may be written by this round's
                         // catch-up (read only after the previous kernel has finished)
+  int f16;              // bf16 path: q and the block K/V are single fp16 operands (no lo
+                        // halves); the ring's bf16 tiles are converted in shared memory
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
 };
 
@@ -123,6 +125,7 @@ struct HeadSeg {
   const void *norm;  // [D] gain (query/key segments)
   void *dst;
   size_t lo_off;     // != 0: also store the rounding residual at dst + lo_off
+  int f16;           // store fp16 (the attention's fp16 operands) instead of the config type
 };
 // Rows row0 .. row0+rows-1 take segments seg0 .. seg0+n_segs-1 (total_heads heads in all).
 struct HeadGroup {

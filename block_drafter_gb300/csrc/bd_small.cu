@@ -313,6 +313,12 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
     if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
     o = ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D;
   }
+  if (sg.f16) {
+    __half *dh = static_cast<__half *>(sg.dst) + o + d0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dh[e] = __float2half_rn(v[e]);
+    return;
+  }
   T *dst = static_cast<T *>(sg.dst) + o + d0;
 #pragma unroll
   for (int e = 0; e < E; ++e) store_split(dst, e, sg.lo_off, v[e]);

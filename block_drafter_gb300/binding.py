@@ -25,7 +25,8 @@ STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "B
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
            "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
            "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk",
-           "bd_refine_tail", "bd_head_fp8_bytes", "bd_pack_head_fp8", "bd_lm_head_topk_fp8")
+           "bd_refine_tail", "bd_head_fp8_bytes", "bd_pack_head_fp8", "bd_lm_head_topk_fp8",
+           "bd_selftest_wait")
 
 TOPK_MAX = 16
 
@@ -114,6 +115,8 @@ def lib() -> C.CDLL:
         L.bd_lm_head_topk.restype = i
         L.bd_lm_head_topk.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, i, i, vp, vp, vp,
                                       sz, vp]
+        L.bd_selftest_wait.restype = i
+        L.bd_selftest_wait.argtypes = [vp, i, vp]
         L.bd_head_fp8_bytes.restype = sz
         L.bd_head_fp8_bytes.argtypes = [C.POINTER(Config)]
         L.bd_pack_head_fp8.restype = i
@@ -311,6 +314,11 @@ def lm_head_argmax_noalloc(cfg: Config, weights: Weights, hidden: torch.Tensor,
 
 def kernel_launches() -> int:
     return int(lib().bd_kernel_launches())
+
+
+def selftest_wait(flag: torch.Tensor, limit_us: int, stream=None):
+    """One bounded wait for flag[0] >= 1 (int32 device tensor); see bd_selftest_wait."""
+    _check(lib().bd_selftest_wait(_ptr(flag), int(limit_us), _stream(stream)))
 
 
 def sync_status(stream=None):

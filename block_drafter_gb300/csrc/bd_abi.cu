@@ -1077,6 +1077,14 @@ bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float 
   return BD_OK;
 }
 
+bd_status bd_selftest_wait(const unsigned *flag, int limit_us, void *stream_) {
+  if (!flag || (reinterpret_cast<uintptr_t>(flag) & 3)) return fail(BD_ERR_INVALID_ARG, "flag NULL or misaligned");
+  if (limit_us < 1 || limit_us > 2000000) return fail(BD_ERR_INVALID_ARG, "limit_us must be in 1..2000000");
+  BD_TRY(launch_wait_selftest(flag, static_cast<unsigned long long>(limit_us) * 1000ull,
+                              static_cast<cudaStream_t>(stream_)));
+  return BD_OK;
+}
+
 bd_status bd_sync_status(void *stream_) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));

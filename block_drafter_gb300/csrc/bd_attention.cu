@@ -609,17 +609,8 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    s_abort = 0;
     atomicAdd(arrived, 1u);
-    const unsigned long long t0 = globaltimer();
-    while (ld_acquire(arrived) < static_cast<unsigned>(a.n_splits)) {
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        atomicOr(&g_error_word, DEVERR_TIMEOUT);
-        s_abort = 1;
-        break;
-      }
-      __nanosleep(32);
-    }
+    s_abort = wait_count(arrived, static_cast<unsigned>(a.n_splits)) ? 0 : 1;
   }
   __syncthreads();
   if (s_abort) return;

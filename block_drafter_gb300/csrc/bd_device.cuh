@@ -175,6 +175,21 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Bounded wait (one thread) until the counter *c reaches n, written by other CTAs of the
+// same launch.  Returns false, with the device error word flagged, if limit_ns of
+// %globaltimer pass first -- the caller then unwinds instead of waiting on.
+__device__ __forceinline__ bool wait_count(const unsigned *c, unsigned n,
+                                           unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = globaltimer();
+  while (ld_acquire(c) < n) {
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(&g_error_word, DEVERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

@@ -571,15 +571,7 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
   const int et = ps.et;
   if (my_chunks > 0) {
     if (et == 0) {
-      const unsigned long long t0 = globaltimer();
-      while (ld_acquire(arrived) < static_cast<unsigned>(n)) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          atomicOr(&g_error_word, DEVERR_TIMEOUT);
-          *sabort = 1;
-          break;
-        }
-        __nanosleep(64);
-      }
+      if (!wait_count(arrived, static_cast<unsigned>(n))) *sabort = 1;
       fence_proxy_async_global();
     }
     named_bar(1, kEpiThreads);

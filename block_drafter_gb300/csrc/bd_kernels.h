@@ -145,6 +145,8 @@ struct HeadPostArgs {
 };
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);
 
+// One bounded wait (the inter-CTA wait of the GEMM and attention kernels) for *flag >= 1.
+std::string launch_wait_selftest(const unsigned *flag, unsigned long long limit_ns, cudaStream_t s);
 // Per-row argmax over per-tile (max, lowest argmax) pairs; lowest id on ties.
 std::string launch_argmax_reduce(const float *val, const int32_t *idx, int m_tiles, int rows,
                                  int32_t *tok_out, float *max_out, cudaStream_t s);

@@ -807,6 +807,14 @@ __global__ void __launch_bounds__(32) tail_walk_kernel(const float *table, const
   }
 }
 
+// Self-test of the failure path: one thread waits, bounded, for a counter that only the
+// caller sets, with the same wait the split-tile reductions and attention splits use.
+__global__ void wait_selftest_kernel(const unsigned *flag, unsigned long long limit_ns) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) wait_count(flag, 1u, limit_ns);
+}
+
 // ------------------------------------------------------------------ launchers
 static std::string err(const char *what, cudaError_t e) {
   return e == cudaSuccess ? std::string() : std::string(what) + ": " + cudaGetErrorString(e);
@@ -1026,6 +1034,10 @@ std::string launch_tail_walk(const float *table, const float *cand_score, const 
   const size_t smem = static_cast<size_t>(K - 1) * kc * kc * sizeof(float);
   return err("tail walk", launch_pdl(tail_walk_kernel, dim3(B), dim3(32), smem, s, table, cand_score,
                                      cand, K, kc, token_out, pick_out));
+}
+
+std::string launch_wait_selftest(const unsigned *flag, unsigned long long limit_ns, cudaStream_t s) {
+  return err("wait self-test", launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, s, flag, limit_ns));
 }
 
 }  // namespace bd

@@ -375,6 +375,14 @@ bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_weights *w,
  * Graph replays do not pass through the library and are not counted. */
 uint64_t bd_kernel_launches(void);
 
+/* Failure-path self-test: enqueues one thread that waits, with the bounded inter-CTA wait
+ * the split-tile reductions and attention splits use, for the dev uint32 *flag (4-byte
+ * aligned, caller-owned) to become >= 1, giving up after limit_us microseconds
+ * (1 .. 2,000,000; those kernels use 2 s).  A wait that gives up flags the device error
+ * word, so the next bd_sync_status returns BD_ERR_DEVICE_TIMEOUT, and ends: nothing hangs
+ * and the context stays usable. */
+bd_status bd_selftest_wait(const unsigned *flag, int limit_us, void *stream);
+
 /* Thread-local description of the last non-OK status returned on this thread. */
 const char *bd_last_error(void);
 

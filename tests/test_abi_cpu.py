@@ -159,6 +159,10 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     assert st == -1 and b"1024-byte" in L.bd_last_error()
     st = L.bd_pack_head_fp8(C.byref(cb), C.byref(wb), 0x10000, 1024, None)
     assert st == -1 and b"smaller" in L.bd_last_error()
+    # failure-path self-test: flag and limit checked on the host
+    assert L.bd_selftest_wait(None, 1000, None) == -1
+    assert L.bd_selftest_wait(0x10000, 0, None) == -1
+    assert L.bd_selftest_wait(0x10002, 1000, None) == -1
     # refinement: K < 2, kc out of range, missing inputs
     st = L.bd_refine_tail(C.byref(c), C.byref(w), 0x10000, 0x10000, 0x10000, 1, 1, 16, 0x10000,
                           None, None, ws, 1 << 30, None)

@@ -20,7 +20,7 @@ OBJDIR = os.path.join(ROOT, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["bd_abi.cu", "bd_gemm.cu", "bd_attention.cu", "bd_small.cu", "bd_noalloc.cu", "bd_pack.cu",
-           "bd_head8.cu"]
+           "bd_head8.cu", "bd_bridge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v", f"-I{INCLUDE}"]

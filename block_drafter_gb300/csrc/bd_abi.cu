@@ -197,6 +197,8 @@ struct RoundWs {
   unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
   float *x, *z, *pre, *r, *part_o, *qkv_raw, *feat, *kv_raw;
   float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
+  unsigned *br_bar;    // [L][5] fused-bridge barrier counters, right after att_cnt
+  float *zpart, *sspart, *zsq;  // fused-bridge partial sums
   float2 *rope, *part_ml;
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
@@ -239,6 +241,17 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_
   if (n_pend > 0 && !fuse) tiles = std::max(tiles, mat_max_tiles(c, n_pend));
   carve_gemm(cv, w.g, 2 * std::max(std::min(TQ, 128), pad16(std::min(n_pend, 128))), tiles, sms);
   w.att_cnt = cv.take<unsigned>(2 * static_cast<size_t>(B) * c->n_kv_heads);
+  const BridgePlan bp = c->code_width > 0 && c->conv_group == 0
+                            ? bridge_plan(c->dtype, T, H, c->code_width, c->msg_width, sms)
+                            : BridgePlan{};
+  w.br_bar = bp.ok ? cv.take<unsigned>(5 * static_cast<size_t>(c->n_layers)) : nullptr;
+  if (bp.ok) {
+    w.zpart = cv.take<float>(static_cast<size_t>(bp.n_kz) * c->code_width * T);
+    w.sspart = cv.take<float>(static_cast<size_t>(bp.n_kz) * T);
+    w.zsq = cv.take<float>(static_cast<size_t>(T) * ((c->code_width + 127) / 128));
+  } else {
+    w.zpart = w.sspart = w.zsq = nullptr;
+  }
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
   w.qkv_raw = cv.take<float>(static_cast<size_t>(Tq) * (QD + 2 * KD));
   w.feat = n_pend > 0 ? cv.take<float>(static_cast<size_t>(n_pend) * H) : nullptr;
@@ -611,8 +624,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   // S3: block input rows and the RoPE table of positions F_b + i
   // the first kernel clears the GEMM tile counters and the attention split counters
   // (carved back to back)
-  const ZeroSpan zero{rw.g.counters, static_cast<size_t>(rw.att_cnt - rw.g.counters) +
-                                         2 * static_cast<size_t>(B) * cfg->n_kv_heads};
+  // (and the fused bridge's barrier counters, carved right after them)
+  const ZeroSpan zero{rw.g.counters,
+                      rw.br_bar ? static_cast<size_t>(rw.br_bar - rw.g.counters) + 5 * cfg->n_layers
+                                : static_cast<size_t>(rw.att_cnt - rw.g.counters) +
+                                      2 * static_cast<size_t>(B) * cfg->n_kv_heads};
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
                            cfg->mask_token_id, rw.x, rw.rope, D / 2, freq,
                            n_pend > 0 ? pending->pos : nullptr, n_pend, zero, s));
@@ -809,7 +825,44 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       BD_TRY(launch_gemm(p, sc, s));
     }
     if (conv) fin = ConvFinish{rw.cz, rw.cdelta_m, L.conv_base_m, gw};
-    if (cfg->code_width > 0) {
+    if (cfg->code_width > 0 && rw.br_bar && pk) {  // S8 + S9 in one launch (small blocks)
+      const BridgePlan bp = bridge_plan(dt, T, H, cfg->code_width, cfg->msg_width, sms);
+      BridgeArgs ba;
+      memset(&ba, 0, sizeof ba);
+      ba.x = rw.x;
+      ba.pk_r = pk + PL.r_read[l];
+      ba.pk_w = pk + PL.w_write[l];
+      ba.pk_g = pk + PL.g_recv;
+      ba.pk_gp = pk + PL.g_pred;
+      ba.pk_a = pk + PL.a_val;
+      ba.gate_bias = static_cast<const __nv_bfloat16 *>(w->gate_bias);
+      ba.codebook = static_cast<const __nv_bfloat16 *>(w->codebook);
+      ba.anchors = anchor_ids;
+      ba.r = rw.r;
+      ba.zpart = rw.zpart;
+      ba.sspart = rw.sspart;
+      ba.z = rw.z;
+      ba.zsq = rw.zsq;
+      ba.m = static_cast<__nv_bfloat16 *>(rw.m);
+      ba.tail = tail_state && l == cfg->n_layers - 1 ? tail_state : nullptr;
+      ba.bar = rw.br_bar + 5 * l;
+      ba.T = T;
+      ba.W = W;
+      ba.H = H;
+      ba.Rc = cfg->code_width;
+      ba.Mc = cfg->msg_width;
+      ba.V = cfg->vocab;
+      ba.TP = TP;
+      ba.n_kz = bp.n_kz;
+      ba.kz = bp.kz;
+      ba.n1 = bp.n1;
+      ba.n3 = bp.n3;
+      ba.kc3 = bp.kc3;
+      ba.s1_bytes = bp.s1_bytes;
+      ba.s5_bytes = bp.s5_bytes;
+      ba.eps = cfg->eps;
+      BD_TRY(launch_bridge(ba, bp, sms, s));
+    } else if (cfg->code_width > 0) {
       const int Rc = cfg->code_width, Mc = cfg->msg_width;
       // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
       BD_TRY(launch_rownorm(dt, rw.x, T, H, nullptr, cfg->eps, NORM_BRIDGE, rw.xn, rw.r, nullptr,
@@ -1089,7 +1142,7 @@ bd_status bd_sync_status(void *stream_) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
   const unsigned word = take_error_word_gemm() | take_error_word_att() | take_error_word_small() |
-                        take_error_word_pack() | take_error_word_head8();
+                        take_error_word_pack() | take_error_word_head8() | take_error_word_bridge();
   if (word & DEVERR_TIMEOUT) return fail(BD_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
   if (word & DEVERR_BAD_INDEX)
     return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");

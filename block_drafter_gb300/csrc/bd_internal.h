@@ -119,6 +119,7 @@ unsigned take_error_word_gemm();
 unsigned take_error_word_att();
 unsigned take_error_word_small();
 unsigned take_error_word_head8();
+unsigned take_error_word_bridge();
 
 // ------------------------------------------------------------------ packed weights
 // Packed image of one [rows, K] matrix: 128-row tiles, each split into 128-byte K boxes;

@@ -1,5 +1,6 @@
 // Launchers of the non-GEMM kernels (attention, norms, embedding, bridge helpers).
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -144,6 +145,38 @@ struct HeadPostArgs {
   HeadSeg seg[kMaxHeadSegs];
 };
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);
+
+// Fused DSpine bridge for blocks of T <= 32 rows (bf16 config, packed weight image): one
+// launch, one CTA per SM, phases separated by grid barriers (bar: 3 counters, zero on
+// entry).  See bd_bridge.cu.
+struct BridgeArgs {
+  float *x;                                       // [T][H] residual, updated in place
+  const uint8_t *pk_r, *pk_w;                     // packed R_l [Rc][H], W_l [H][Mc]
+  const uint8_t *pk_g, *pk_gp, *pk_a;             // packed G, G_p, A [Mc][Rc]
+  const __nv_bfloat16 *gate_bias;                 // [Mc] or null
+  const __nv_bfloat16 *codebook;                  // [V][Rc]
+  const int32_t *anchors;                         // [B]
+  float *r;                                       // [T] OUT RMS of the pre-injection rows
+  float *zpart, *sspart;                          // [n_kz][T][Rc], [n_kz][T]
+  float *z, *zsq;                                 // [T][Rc], [T][ceil(Rc / 128)]
+  __nv_bfloat16 *m;                               // message hi/lo pair [2][TP][Mc]
+  float *tail;                                    // tail state export, or null
+  unsigned *bar;                                  // [3]
+  int T, W, H, Rc, Mc, V, TP;
+  int n_kz, kz, n1, n3, kc3;                      // from the plan
+  size_t s1_bytes, s5_bytes;
+  float eps;
+};
+// Work split and shared-memory areas of one launch; ok = false when the shape does not fit.
+struct BridgePlan {
+  bool ok;
+  int n_kz, kz;   // K chunks of the code read (P1 CTAs: ceil(Rc / 128) * n_kz)
+  int n1, n3;     // CTAs of P1 and of P3 (Mc / 16)
+  int kc3;        // K chunk of the P3 staging
+  size_t s1_bytes, s5_bytes, sa_bytes, smem;
+};
+BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms);
+std::string launch_bridge(const BridgeArgs &args, const BridgePlan &plan, int sms, cudaStream_t s);
 
 // One bounded wait (the inter-CTA wait of the GEMM and attention kernels) for *flag >= 1.
 std::string launch_wait_selftest(const unsigned *flag, unsigned long long limit_ns, cudaStream_t s);

@@ -102,7 +102,10 @@ TINY_DFLASH2 = bdsynth.TINY.with_(name="tiny_dflash2_fp32", conv_group=16)
                                       (SMALL_BF16, 2), (SMALL_D64, 0), (SMALL_DFLASH2, 0),
                                       (SMALL_DFLASH2, 1), (SMALL_DFLASH2_BRIDGE, 2),
                                       (TINY_DFLASH2, 0),
-                                      (SMALL_DFLASH2.with_(n_masks=6, batch=5), 3)])
+                                      (SMALL_DFLASH2.with_(n_masks=6, batch=5), 3),
+                                      # blocks of at most 32 rows: the one-launch bridge
+                                      (SMALL_BF16.with_(batch=2), 4), (SMALL_BF16.with_(batch=1), 5),
+                                      (SMALL_BF16.with_(batch=4, n_masks=7), 6)])
 def test_round_matches_oracle(geo, seed):
     case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
     case.fill_rings()
@@ -121,8 +124,9 @@ def test_round_block_causal_matches_oracle():
     assert rep["ok"], rep
 
 
-def test_round_gate_bias_matches_oracle():
-    case = Hn.Case(SMALL_BF16, seed=4, gate_bias=True, max_ctx_rows=128)
+@pytest.mark.parametrize("batch", [3, 2])  # 2: the one-launch bridge
+def test_round_gate_bias_matches_oracle(batch):
+    case = Hn.Case(SMALL_BF16.with_(batch=batch), seed=4, gate_bias=True, max_ctx_rows=128)
     case.fill_rings()
     rep = Hn.compare_round(case, case.run_gpu(), case.run_oracle(), tol=TOL)
     assert rep["ok"], rep

@@ -81,7 +81,8 @@ def _compare(case, gpu):
     return rep
 
 
-@pytest.mark.parametrize("geo,seed", [(SMALL_BF16, 0), (SMALL_BF16, 3), (bdsynth.TINY, 1)])
+@pytest.mark.parametrize("geo,seed", [(SMALL_BF16, 0), (SMALL_BF16, 3), (bdsynth.TINY, 1),
+                                      (SMALL_BF16.with_(batch=2), 4)])  # one-launch bridge
 def test_refine_tail_matches_oracle(geo, seed):
     case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
     case.fill_rings()

@@ -841,7 +841,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.r = rw.r;
       ba.zpart = rw.zpart;
       ba.sspart = rw.sspart;
-      ba.z = rw.z;
+      ba.zc = static_cast<__nv_bfloat16 *>(rw.c);
       ba.zsq = rw.zsq;
       ba.m = static_cast<__nv_bfloat16 *>(rw.m);
       ba.tail = tail_state && l == cfg->n_layers - 1 ? tail_state : nullptr;
@@ -857,9 +857,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.kz = bp.kz;
       ba.n1 = bp.n1;
       ba.n3 = bp.n3;
-      ba.kc3 = bp.kc3;
-      ba.s1_bytes = bp.s1_bytes;
-      ba.s5_bytes = bp.s5_bytes;
+      ba.p3_boxes = bp.p3_boxes;
+      ba.sw_bytes = bp.sw_bytes;
       ba.eps = cfg->eps;
       BD_TRY(launch_bridge(ba, bp, sms, s));
     } else if (cfg->code_width > 0) {

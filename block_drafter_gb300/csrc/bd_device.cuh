@@ -177,16 +177,18 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 }
 // Bounded wait (one thread) until the counter *c reaches n, written by other CTAs of the
 // same launch.  Returns false, with the device error word flagged, if limit_ns of
-// %globaltimer pass first -- the caller then unwinds instead of waiting on.
+// %globaltimer pass first -- the caller then unwinds instead of waiting on.  sleep_ns
+// between polls (0: poll without pausing, for a barrier whose CTAs are all resident).
 __device__ __forceinline__ bool wait_count(const unsigned *c, unsigned n,
-                                           unsigned long long limit_ns = kWaitLimitNs) {
+                                           unsigned long long limit_ns = kWaitLimitNs,
+                                           unsigned sleep_ns = 64) {
   const unsigned long long t0 = globaltimer();
   while (ld_acquire(c) < n) {
     if (globaltimer() - t0 > limit_ns) {
       atomicOr(&g_error_word, DEVERR_TIMEOUT);
       return false;
     }
-    __nanosleep(64);
+    if (sleep_ns) __nanosleep(sleep_ns);
   }
   return true;
 }

@@ -158,13 +158,14 @@ struct BridgeArgs {
   const int32_t *anchors;                         // [B]
   float *r;                                       // [T] OUT RMS of the pre-injection rows
   float *zpart, *sspart;                          // [n_kz][T][Rc], [n_kz][T]
-  float *z, *zsq;                                 // [T][Rc], [T][ceil(Rc / 128)]
-  __nv_bfloat16 *m;                               // message hi/lo pair [2][TP][Mc]
+  __nv_bfloat16 *zc;                              // z' hi/lo boxes (2 TP rows x Rc)
+  float *zsq;                                     // [T][ceil(Rc / 128)]
+  __nv_bfloat16 *m;                               // message hi/lo boxes (2 TP rows x Mc)
   float *tail;                                    // tail state export, or null
   unsigned *bar;                                  // [3]
   int T, W, H, Rc, Mc, V, TP;
-  int n_kz, kz, n1, n3, kc3;                      // from the plan
-  size_t s1_bytes, s5_bytes;
+  int n_kz, kz, n1, n3, p3_boxes;                 // from the plan
+  size_t sw_bytes;
   float eps;
 };
 // Work split and shared-memory areas of one launch; ok = false when the shape does not fit.
@@ -172,8 +173,8 @@ struct BridgePlan {
   bool ok;
   int n_kz, kz;   // K chunks of the code read (P1 CTAs: ceil(Rc / 128) * n_kz)
   int n1, n3;     // CTAs of P1 and of P3 (Mc / 16)
-  int kc3;        // K chunk of the P3 staging
-  size_t s1_bytes, s5_bytes, sa_bytes, smem;
+  int p3_boxes;   // K boxes of the codes staged at once in P3
+  size_t sw_bytes, sa_bytes, smem;  // weight area, activation area, their sum
 };
 BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms);
 std::string launch_bridge(const BridgeArgs &args, const BridgePlan &plan, int sms, cudaStream_t s);

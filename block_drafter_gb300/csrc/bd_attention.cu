@@ -180,6 +180,76 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
 // loaded eight splits at a time before they are used (the loads are independent and their
 // L2 latency, not bandwidth, bounds the merge).  The partials were written by other CTAs of
 // the launch: read through L2.  Called by all threads of the CTA.
+// Few splits (S <= kFewSplits): each warp merges rows r0 + warp, r0 + warp + 4, ... two at
+// a time, with every load of the pair (the splits' (m, l) and partial rows) issued before
+// any arithmetic, so a pair costs one round trip to L2.  Splits are added in index order.
+constexpr int kFewSplits = 8;
+template <typename T, int D>
+__device__ __forceinline__ void combine_rows_few(const AttArgs &a, int b, int h, int r0, int r1,
+                                                 int warp, int lane) {
+  constexpr int PER = D / 32, RB = 2;
+  const int G = a.n_q_heads / a.n_kv_heads, S = a.n_splits;
+  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
+  const float *po = a.part_o + bh * S * kAttRows * D;
+  const float2 *pml = a.part_ml + bh * S * kAttRows;
+  for (int base = r0 + warp; base < r1; base += 4 * RB) {
+    float2 ml[RB][kFewSplits];
+    float v[RB][kFewSplits][PER];
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int rr = base + 4 * i;
+#pragma unroll
+      for (int sp = 0; sp < kFewSplits; ++sp) {
+        const bool ok = rr < r1 && sp < S;
+        ml[i][sp] = ok ? __ldcg(pml + sp * kAttRows + rr) : make_float2(-INFINITY, 0.f);
+        const float *os = po + (static_cast<size_t>(ok ? sp : 0) * kAttRows + (ok ? rr : 0)) * D + lane * PER;
+        if (PER == 4) {
+          const float4 o = ok ? __ldcg(reinterpret_cast<const float4 *>(os)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i][sp][0] = o.x;
+          v[i][sp][1 % PER] = o.y;
+          v[i][sp][2 % PER] = o.z;
+          v[i][sp][3 % PER] = o.w;
+        } else {
+          const float2 o = ok ? __ldcg(reinterpret_cast<const float2 *>(os)) : make_float2(0.f, 0.f);
+          v[i][sp][0] = o.x;
+          v[i][sp][1 % PER] = o.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int rr = base + 4 * i;
+      if (rr >= r1) break;
+      float M = -INFINITY;
+#pragma unroll
+      for (int sp = 0; sp < kFewSplits; ++sp)
+        if (ml[i][sp].y > 0.f) M = fmaxf(M, ml[i][sp].x);
+      float L = 0.f, acc[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < kFewSplits; ++sp)
+        if (ml[i][sp].y > 0.f) {
+          const float wgt = exp2f(ml[i][sp].x - M);
+          L += wgt * ml[i][sp].y;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] += wgt * v[i][sp][e];
+        }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int gh = rr / a.W, qi = rr % a.W;
+      T *out = static_cast<T *>(a.out) +
+               (static_cast<size_t>(b) * a.W + qi) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const float y = acc[e] * inv;
+        const T hi = from_f<T>(y);
+        out[e] = hi;
+        if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
+      }
+    }
+  }
+}
+
 template <typename T, int D>
 __device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int r0, int r1,
                                              int warp, int lane, float (*red)[D + 4]) {
@@ -312,18 +382,20 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   const __nv_bfloat16 *blk_v = static_cast<const __nv_bfloat16 *>(a.blk_v);
   constexpr int CPR = D / 8;  // 16-byte chunks per row
 
+  // Each thread copies chunk ch of the rows r0, r0 + rstep, ...; the ring slot of a row
+  // advances with it (one modulo per tile, then wrap-around by subtraction).
+  const size_t ring_head = (static_cast<size_t>(b) * a.n_kv_heads + h) * static_cast<size_t>(a.cap);
   auto load_kv = [&](int buf, int k0) {
-    for (int c = tid; c < kAttKeys * CPR; c += 128) {
-      const int kr = c / CPR, ch = c % CPR;
-      const int k = k0 + kr;
-      const bool valid = k < g.k_end;
-      size_t off = 0;
-      if (valid) {
-        const long long p = g.p_lo + k;
-        off = ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.cap + p % a.cap) * D;
-      }
+    constexpr int rstep = 128 / CPR;
+    const int ch = tid % CPR, r0 = tid / CPR;
+    int slot = static_cast<int>((static_cast<long long>(g.p_lo) + k0 + r0) % a.cap);
+    for (int kr = r0; kr < kAttKeys; kr += rstep) {
+      const bool valid = k0 + kr < g.k_end;
+      const size_t off = valid ? (ring_head + slot) * D : 0;
       cp_async16(smem_u32(sK + (buf * kAttKeys + kr) * RS + ch * 8), ring_k + off + ch * 8, valid);
       cp_async16(smem_u32(sV + (buf * kAttKeys + kr) * RS + ch * 8), ring_v + off + ch * 8, valid);
+      slot += rstep;
+      while (slot >= a.cap) slot -= a.cap;
     }
   };
   // Block keys/values [Kh; Kl; Vh; Vl] (16 rows each, rows >= W zero) go into the K
@@ -610,14 +682,17 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   __syncthreads();
   if (tid == 0) {
     atomicAdd(arrived, 1u);
-    s_abort = wait_count(arrived, static_cast<unsigned>(a.n_splits)) ? 0 : 1;
+    s_abort = wait_count(arrived, static_cast<unsigned>(a.n_splits), kWaitLimitNs, 0) ? 0 : 1;
   }
   __syncthreads();
   if (s_abort) return;
   const int rp = (R + a.n_splits - 1) / a.n_splits;
   __shared__ float red[4][D + 4];
-  combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,
-                                 red);
+  if (a.n_splits <= kFewSplits)
+    combine_rows_few<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane);
+  else
+    combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,
+                                   red);
   __syncthreads();
   if (tid == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
     *arrived = 0u;  // every split is past its wait: ready for the next launch

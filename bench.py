@@ -522,9 +522,11 @@ def main():
     binding.lib()
     if args.profile_case:
         # One warm step, then the profiled step inside the NVTX range "profiled_step"
-        # (ncu --nvtx --nvtx-include "profiled_step/").  GEMM launch order of the step:
+        # (ncu --nvtx --nvtx-include "profiled_step/").  GEMM launch order of the B=1 step:
         # [0] W_feature (catch-up), [1] QKV (+ the pending rows' K/V), [2] W_o, [3] gate/up,
-        # [4] down, [5] code read, [6] gate/value maps, [7] write, [8] LM head.
+        # [4] down, [5] LM head (the bridge runs as one bridge_kernel launch).  At B=8 the
+        # pending rows' K/V is its own product after QKV, and the bridge's code read,
+        # gate/value maps and write are GEMMs after the down projection.
         base = bdsynth.DSPINE27B_B1 if args.workload == "b1" else bdsynth.DSPINE27B_B8
         geo = base if args.profile_full else base.with_(n_layers=1, windows=(2048,))
         st = State(geo, args.seed)

@@ -22,11 +22,14 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 }
 
 // (cos, sin) of pos * inv_freq[j]: the product and its reduction modulo 2 pi are done in
-// double precision so that large positions keep full single-precision angles.
+// double precision so that large positions keep full single-precision angles.  The
+// multiple of 2 pi comes from a product with 1 / (2 pi) (a rounding there can leave the
+// reduced angle just outside [0, 2 pi), which sincosf takes as it is).
 __device__ __forceinline__ float2 rope_cs(long long pos, double inv) {
   const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
   double ang = static_cast<double>(pos) * inv;
-  ang -= floor(ang / two_pi) * two_pi;
+  ang -= floor(ang * inv_two_pi) * two_pi;
   float s, c;
   sincosf(static_cast<float>(ang), &s, &c);
   return make_float2(c, s);

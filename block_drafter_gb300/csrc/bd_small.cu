@@ -36,6 +36,17 @@ __device__ __forceinline__ float2 rope_cs(long long pos, double inv) {
 }
 
 
+template <typename T> __device__ __forceinline__ float4 load4(const T *p, int i4);
+template <> __device__ __forceinline__ float4 load4<float>(const float *p, int i4) {
+  return reinterpret_cast<const float4 *>(p)[i4];
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p, int i4) {
+  const uint2 u = reinterpret_cast<const uint2 *>(p)[i4];
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
 template <typename T>
 __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *anchors,
                                   const int64_t *frontier, int W, int n_tok, int mask_id, float *x,
@@ -57,7 +68,21 @@ __global__ void round_prep_kernel(const T *embed, int H, int V, const int32_t *a
     id = 0;
   }
   const T *e = embed + static_cast<size_t>(id) * H;
-  for (int h = threadIdx.x; h < H; h += blockDim.x) x[static_cast<size_t>(tok) * H + h] = to_f<T>(e[h]);
+  float *xr = x + static_cast<size_t>(tok) * H;
+  constexpr int U = 8;  // float4 loads in flight per thread (H % 4 == 0)
+  for (int base = threadIdx.x; base < H / 4; base += U * blockDim.x) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base + u * blockDim.x;
+      v[u] = i4 < H / 4 ? load4<T>(e, i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base + u * blockDim.x;
+      if (i4 < H / 4) reinterpret_cast<float4 *>(xr)[i4] = v[u];
+    }
+  }
   const long long pos = frontier[b] + i;
   for (int j = threadIdx.x; j < half; j += blockDim.x)
     rope[static_cast<size_t>(tok) * half + j] = rope_cs(pos, freq.inv[j]);
@@ -75,17 +100,6 @@ __global__ void rope_table_kernel(const int64_t *pos, int n, float2 *rope, int h
   }
 }
 
-template <typename T> __device__ __forceinline__ float4 load4(const T *p, int i4);
-template <> __device__ __forceinline__ float4 load4<float>(const float *p, int i4) {
-  return reinterpret_cast<const float4 *>(p)[i4];
-}
-template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p, int i4) {
-  const uint2 u = reinterpret_cast<const uint2 *>(p)[i4];
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-  return make_float4(fa.x, fa.y, fb.x, fb.y);
-}
 template <typename T> __device__ __forceinline__ void store4(T *p, int i4, float4 v);
 template <> __device__ __forceinline__ void store4<__half>(__half *p, int i4, float4 v) {
   __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);

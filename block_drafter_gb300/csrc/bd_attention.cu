@@ -180,26 +180,26 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
 // loaded eight splits at a time before they are used (the loads are independent and their
 // L2 latency, not bandwidth, bounds the merge).  The partials were written by other CTAs of
 // the launch: read through L2.  Called by all threads of the CTA.
-// Few splits (S <= kFewSplits): each warp merges rows r0 + warp, r0 + warp + 4, ... two at
-// a time, with every load of the pair (the splits' (m, l) and partial rows) issued before
-// any arithmetic, so a pair costs one round trip to L2.  Splits are added in index order.
-constexpr int kFewSplits = 8;
-template <typename T, int D>
+// Few splits (S <= SMAX): each warp merges rows r0 + warp, r0 + warp + 4, ... RB at a time,
+// with every load of those rows (the splits' (m, l) and partial rows) issued before any
+// arithmetic, so they cost one round trip to L2.  Splits are added in index order.
+constexpr int kFewSplits = 16;
+template <typename T, int D, int SMAX, int RB>
 __device__ __forceinline__ void combine_rows_few(const AttArgs &a, int b, int h, int r0, int r1,
                                                  int warp, int lane) {
-  constexpr int PER = D / 32, RB = 2;
+  constexpr int PER = D / 32;
   const int G = a.n_q_heads / a.n_kv_heads, S = a.n_splits;
   const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
   const float *po = a.part_o + bh * S * kAttRows * D;
   const float2 *pml = a.part_ml + bh * S * kAttRows;
   for (int base = r0 + warp; base < r1; base += 4 * RB) {
-    float2 ml[RB][kFewSplits];
-    float v[RB][kFewSplits][PER];
+    float2 ml[RB][SMAX];
+    float v[RB][SMAX][PER];
 #pragma unroll
     for (int i = 0; i < RB; ++i) {
       const int rr = base + 4 * i;
 #pragma unroll
-      for (int sp = 0; sp < kFewSplits; ++sp) {
+      for (int sp = 0; sp < SMAX; ++sp) {
         const bool ok = rr < r1 && sp < S;
         ml[i][sp] = ok ? __ldcg(pml + sp * kAttRows + rr) : make_float2(-INFINITY, 0.f);
         const float *os = po + (static_cast<size_t>(ok ? sp : 0) * kAttRows + (ok ? rr : 0)) * D + lane * PER;
@@ -222,13 +222,13 @@ __device__ __forceinline__ void combine_rows_few(const AttArgs &a, int b, int h,
       if (rr >= r1) break;
       float M = -INFINITY;
 #pragma unroll
-      for (int sp = 0; sp < kFewSplits; ++sp)
+      for (int sp = 0; sp < SMAX; ++sp)
         if (ml[i][sp].y > 0.f) M = fmaxf(M, ml[i][sp].x);
       float L = 0.f, acc[PER];
 #pragma unroll
       for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll
-      for (int sp = 0; sp < kFewSplits; ++sp)
+      for (int sp = 0; sp < SMAX; ++sp)
         if (ml[i][sp].y > 0.f) {
           const float wgt = exp2f(ml[i][sp].x - M);
           L += wgt * ml[i][sp].y;
@@ -688,8 +688,12 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   if (s_abort) return;
   const int rp = (R + a.n_splits - 1) / a.n_splits;
   __shared__ float red[4][D + 4];
-  if (a.n_splits <= kFewSplits)
-    combine_rows_few<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane);
+  if (a.n_splits <= 8)
+    combine_rows_few<__nv_bfloat16, D, 8, 2>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp),
+                                             warp, lane);
+  else if (a.n_splits <= kFewSplits)
+    combine_rows_few<__nv_bfloat16, D, kFewSplits, 1>(a, b, h, min(R, split * rp),
+                                                      min(R, (split + 1) * rp), warp, lane);
   else
     combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,
                                    red);

@@ -155,10 +155,18 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
                                                       size_t lo_off, ConvFinish cf) {
   __shared__ float red[32];
   const int row = blockIdx.x;
+  const int H4 = H / 4;
+  // the gain (a weight: no earlier kernel writes it) is loaded before the dependency wait
+  const bool has_gain = mode != NORM_BRIDGE && gain != nullptr;
+  float4 gv[kNormVec];
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i4 = threadIdx.x + k * blockDim.x;
+    gv[k] = has_gain && i4 < H4 ? load4<T>(gain, i4) : make_float4(1.f, 1.f, 1.f, 1.f);
+  }
   pdl_wait();
   pdl_trigger();
   float *xr = x + static_cast<size_t>(row) * H;
-  const int H4 = H / 4;
   const bool fin = cf.z != nullptr;
   const bool has_prev = (row % W) != 0;
   // x (+ the branch output's side-1 convolution, written back: the residual update)
@@ -201,10 +209,9 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
   if (mode == NORM_FINAL && head_out != nullptr && i > 0)
     hrow = head_out + (static_cast<size_t>(row / W) * (W - 1) + (i - 1)) * H;
   float *frow = f32_out ? f32_out + static_cast<size_t>(row) * H : nullptr;
-  auto emit = [&](int i4, float4 t) {
+  auto emit = [&](int i4, float4 t, float4 g) {
     float4 y = make_float4(t.x * scale, t.y * scale, t.z * scale, t.w * scale);
     if (mode != NORM_BRIDGE) {
-      const float4 g = load4<T>(gain, i4);
       y.x *= g.x;
       y.y *= g.y;
       y.z *= g.z;
@@ -226,10 +233,11 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
 #pragma unroll
   for (int k = 0; k < kNormVec; ++k) {
     const int i4 = threadIdx.x + k * blockDim.x;
-    if (i4 < H4) emit(i4, xv[k]);
+    if (i4 < H4) emit(i4, xv[k], gv[k]);
   }
   for (int i4 = threadIdx.x + kNormVec * blockDim.x; i4 < H4; i4 += blockDim.x)
-    emit(i4, reinterpret_cast<const float4 *>(xr)[i4]);
+    emit(i4, reinterpret_cast<const float4 *>(xr)[i4],
+         has_gain ? load4<T>(gain, i4) : make_float4(1.f, 1.f, 1.f, 1.f));
 }
 
 template <typename T>

@@ -105,7 +105,11 @@ TINY_DFLASH2 = bdsynth.TINY.with_(name="tiny_dflash2_fp32", conv_group=16)
                                       (SMALL_DFLASH2.with_(n_masks=6, batch=5), 3),
                                       # blocks of at most 32 rows: the one-launch bridge
                                       (SMALL_BF16.with_(batch=2), 4), (SMALL_BF16.with_(batch=1), 5),
-                                      (SMALL_BF16.with_(batch=4, n_masks=7), 6)])
+                                      (SMALL_BF16.with_(batch=4, n_masks=7), 6),
+                                      # 8 rows in a 16-row tile; a code of 192 (a partial
+                                      # 128-row tile) with a 128-wide message
+                                      (SMALL_BF16.with_(batch=1, n_masks=7), 7),
+                                      (SMALL_BF16.with_(batch=2, code_width=192, msg_width=128), 8)])
 def test_round_matches_oracle(geo, seed):
     case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
     case.fill_rings()
@@ -132,10 +136,11 @@ def test_round_gate_bias_matches_oracle(batch):
     assert rep["ok"], rep
 
 
-def test_zero_write_is_bit_exact_plain_dflash():
+@pytest.mark.parametrize("batch", [3, 2])  # 2: the one-launch bridge
+def test_zero_write_is_bit_exact_plain_dflash(batch):
     """With every W_l = 0 the DSpine round must equal the same round with the bridge
     disabled (code_width = 0), bit for bit."""
-    geo = SMALL_BF16
+    geo = SMALL_BF16.with_(batch=batch)
     w = bdsynth.make_weights(geo, 5, zero_write=True)
     a = Hn.Case(geo, seed=5, weights=w, max_ctx_rows=128)
     a.fill_rings()
@@ -170,26 +175,29 @@ def test_identity_convolution_is_bit_exact_plain_dflash():
     assert torch.equal(ga["tokens"], gb["tokens"])
 
 
-def test_round_is_deterministic_and_requests_independent():
-    geo = SMALL_BF16
+@pytest.mark.parametrize("batch", [3, 2])  # 2: the one-launch bridge
+def test_round_is_deterministic_and_requests_independent(batch):
+    geo = SMALL_BF16.with_(batch=batch)
     case = Hn.Case(geo, seed=6, max_ctx_rows=128)
     case.fill_rings()
     g1 = case.run_gpu()
     g2 = case.run_gpu()
     assert torch.equal(g1["layers"], g2["layers"])
     assert torch.equal(g1["tokens"], g2["tokens"])
-    # changing request 2's anchor must leave requests 0 and 1 unchanged
+    # changing the last request's anchor must leave the others unchanged
+    last = batch - 1
     case.anchors = list(case.anchors)
-    case.anchors[2] = (case.anchors[2] + 17) % geo.vocab
-    if case.anchors[2] == case.mask_id:
-        case.anchors[2] = (case.anchors[2] + 1) % geo.vocab
+    case.anchors[last] = (case.anchors[last] + 17) % geo.vocab
+    if case.anchors[last] == case.mask_id:
+        case.anchors[last] = (case.anchors[last] + 1) % geo.vocab
     g3 = case.run_gpu()
     W = geo.W
-    assert torch.equal(g3["hidden"][:2 * W], g1["hidden"][:2 * W])
-    assert not torch.equal(g3["hidden"][2 * W:], g1["hidden"][2 * W:])
+    assert torch.equal(g3["hidden"][:last * W], g1["hidden"][:last * W])
+    assert not torch.equal(g3["hidden"][last * W:], g1["hidden"][last * W:])
 
 
-@pytest.mark.parametrize("geo", [SMALL_BF16, bdsynth.TINY])
+# batch 2: the packed round takes the one-launch bridge, the raw one the five launches
+@pytest.mark.parametrize("geo", [SMALL_BF16, SMALL_BF16.with_(batch=2), bdsynth.TINY])
 def test_packed_and_raw_weights_give_identical_results(geo):
     """The packed image is a permutation of the weights, except that in a bf16 config it
     stores the MLP and head matrices as fp16 (their products then take fp16 activations

@@ -11,13 +11,13 @@
 //       c_t = sqrt(Rc) z'_t / (|z'_t| + eps (r_t + eps)) (the code of x_t / (r_t + eps);
 //       anchors sqrt(Rc) C[a]); g = sigmoid(G c_t + G_p c_{t-1} + b), m_t = g * (A c_{t-1}),
 //       m_0 = 0; the tail export of the last layer
-//   P5  x_t += r_t W_l m_t for every row but the anchor
+//   P4  x_t += r_t W_l m_t for every row but the anchor
 // The products run on mma.sync across the CTA's 8 warps, on bf16 hi + lo activation pairs
 // (~16 mantissa bits): at these shapes (N = 32 token columns, K-steps only) a single thread
 // issuing tcgen05.mma spends ~40 ns per instruction, more than the whole product takes on
 // the warps' tensor instructions.  Weights come from the packed image, whose boxes are in
 // the 128-byte-swizzled order (conflict-free ldmatrix): the first phase's as bulk copies
-// issued before the dependency wait, P5's as soon as the CTA's first product has released
+// issued before the dependency wait, P4's as soon as the CTA's first product has released
 // its weight area.  The activations (x, the codes, the message) are written in the same
 // swizzled box order, so the codes and the message reach shared memory as single bulk
 // copies.  Partial sums are added in a fixed order, so results are deterministic.  Every
@@ -35,11 +35,11 @@ BD_DEFINE_ERROR_TAKER(take_error_word_bridge)
 
 constexpr int kBrThreads = 256;  // 8 warps
 constexpr int kBrMaxKz = 32;     // K chunks of the code read (P1), at most
-constexpr int kW5Rows = 32;      // rows of W_l per P5 item
+constexpr int kW4Rows = 32;      // rows of W_l per P4 item
 constexpr int kBrMaxJ = 4;       // float4 columns per lane of a P1 chunk: kz <= 512
 constexpr int kBrMaxGz = 16;     // 128-row groups of the code: Rc <= 2048
 constexpr int kP3Stride = 6144;  // bytes per K box of the P3 weights: G, G_p, A slices of 16 rows
-constexpr int kP5Stride = 8192;  // bytes per K box of the P5 weights: two 32-row items
+constexpr int kP4Stride = 8192;  // bytes per K box of the P4 weights: two 32-row items
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1) {
@@ -133,9 +133,9 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
   constexpr int NTOK = NT * 8, R = 2 * NTOK;   // B operand rows: hi tokens, then lo tokens
   constexpr uint32_t kBoxB = R * 128;          // bytes of one 64-column activation box
   extern __shared__ __align__(1024) uint8_t br_smem[];
-  uint8_t *sw = br_smem;                // weights: the P1 chunk or the P3 slices, then P5's rows
+  uint8_t *sw = br_smem;                // weights: the P1 chunk or the P3 slices, then P4's rows
   uint8_t *sa = br_smem + a.sw_bytes;   // activation boxes, then fp32 partial-sum tables
-  // 0: first weights, 1: P5 weights, 2: P3 codes, 3: P5 message
+  // 0: first weights, 1: P4 weights, 2: P3 codes, 3: P4 message
   __shared__ __align__(8) uint64_t mb[4];
   __shared__ float red[kBrThreads / 32];
   __shared__ float s_scale[32];
@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
   const int T = a.T, H = a.H, Rc = a.Rc, Mc = a.Mc, W = a.W, cta = blockIdx.x;
   const int nbh = H / 64, nbc = Rc / 64, nbm = Mc / 64, gz = (Rc + 127) / 128;
   const bool in_p1 = cta < a.n1, in_p3 = cta >= a.n1 && cta < a.n1 + a.n3;
-  const int n5 = H / kW5Rows;
-  const int my5 = cta < n5 ? (n5 - 1 - cta) / static_cast<int>(gridDim.x) + 1 : 0;
+  const int n4 = H / kW4Rows;
+  const int my4 = cta < n4 ? (n4 - 1 - cta) / static_cast<int>(gridDim.x) + 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&mb[i], 1);
@@ -153,16 +153,16 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
   }
   __syncthreads();
 
-  // P5's rows of W_l (item it, box b at b * kP5Stride + it * 4096), thread 0
-  auto load_w5 = [&]() {
-    if (my5 == 0) return;
+  // P4's rows of W_l (item it, box b at b * kP4Stride + it * 4096), thread 0
+  auto load_w4 = [&]() {
+    if (my4 == 0) return;
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(&mb[1], static_cast<uint32_t>(my5 * nbm * 4096));
-    for (int it = 0; it < my5; ++it) {
+    mbar_arrive_expect_tx(&mb[1], static_cast<uint32_t>(my4 * nbm * 4096));
+    for (int it = 0; it < my4; ++it) {
       const int p = cta + it * static_cast<int>(gridDim.x);
-      const int tw = p * kW5Rows / 128, ro = p * kW5Rows % 128;
+      const int tw = p * kW4Rows / 128, ro = p * kW4Rows % 128;
       for (int b = 0; b < nbm; ++b)
-        bulk_load(sw + b * kP5Stride + it * 4096,
+        bulk_load(sw + b * kP4Stride + it * 4096,
                   a.pk_w + (static_cast<size_t>(tw) * nbm + b) * kPackBox + ro * 128, 4096, &mb[1],
                   pol);
     }
@@ -187,10 +187,10 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
                     img[mat] + (static_cast<size_t>(tj) * nbc + b) * kPackBox + ro * 128, 2048,
                     &mb[0], pol);
     } else {
-      load_w5();
+      load_w4();
     }
   }
-  bool w1_pending = in_p1 || in_p3, w5_pending = !in_p1 && !in_p3 && my5 > 0;
+  bool w1_pending = in_p1 || in_p3, w4_pending = !in_p1 && !in_p3 && my4 > 0;
 
   auto body = [&]() -> void {
     pdl_wait();
@@ -256,9 +256,9 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       __syncthreads();  // every warp is done with the weight area
       if (threadIdx.x == 0) {
         fence_proxy_async_shared();
-        load_w5();
+        load_w4();
       }
-      w5_pending = my5 > 0;
+      w4_pending = my4 > 0;
       if (gi * 128 + r0 < Rc) {
         float *zp = a.zpart + static_cast<size_t>(q) * T * Rc;
 #pragma unroll
@@ -375,9 +375,9 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       }
       if (threadIdx.x == 0) {
         fence_proxy_async_shared();
-        load_w5();
+        load_w4();
       }
-      w5_pending = my5 > 0;
+      w4_pending = my4 > 0;
       // per-warp K partials [warp][mat][16 rows][NTOK], added in warp order and scaled
       float *red3 = reinterpret_cast<float *>(sa);
 #pragma unroll
@@ -412,9 +412,9 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
     }
     if (!grid_sync(a.bar + 2, &s_ok)) return;
 
-    // ---- P5: x_t += r_t W_l m_t, 32 rows of W_l per item (item it, K box b at
-    // b * kP5Stride + it * 4096); warps: two 16-row tiles x four K quarters
-    if (my5 > 0) {
+    // ---- P4: x_t += r_t W_l m_t, 32 rows of W_l per item (item it, K box b at
+    // b * kP4Stride + it * 4096); warps: two 16-row tiles x four K quarters
+    if (my4 > 0) {
       if (threadIdx.x == 0) {
         fence_proxy_async_global();
         fence_proxy_async_shared();
@@ -422,30 +422,30 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         bulk_load(sa, a.m, static_cast<uint32_t>(nbm) * kBoxB, &mb[3], policy_evict_first());
       }
       // the residual entries this thread updates, loaded while the copies land
-      constexpr int kMaxUpd = 2 * kW5Rows * NTOK / kBrThreads;
-      const int n_upd = my5 * kW5Rows * T;
+      constexpr int kMaxUpd = 2 * kW4Rows * NTOK / kBrThreads;
+      const int n_upd = my4 * kW4Rows * T;
       float xv[kMaxUpd];
 #pragma unroll
       for (int u = 0; u < kMaxUpd; ++u) {
         const int idx = threadIdx.x + u * kBrThreads;
-        const int it = idx / (kW5Rows * T), rem = idx % (kW5Rows * T);
-        const int row = rem % kW5Rows, t = rem / kW5Rows;
+        const int it = idx / (kW4Rows * T), rem = idx % (kW4Rows * T);
+        const int row = rem % kW4Rows, t = rem / kW4Rows;
         xv[u] = idx < n_upd ? __ldcg(a.x + static_cast<size_t>(t) * H +
-                                     (cta + it * static_cast<int>(gridDim.x)) * kW5Rows + row)
+                                     (cta + it * static_cast<int>(gridDim.x)) * kW4Rows + row)
                             : 0.f;
       }
-      w5_pending = false;
+      w4_pending = false;
       const bool ok_w = cta_wait(&mb[1], 0), ok_m = cta_wait(&mb[3], 0);
       if (!ok_w || !ok_m) return;
       const __nv_bfloat16 *sm = reinterpret_cast<const __nv_bfloat16 *>(sa);
-      float *red5 = reinterpret_cast<float *>(sa + static_cast<size_t>(nbm) * kBoxB);
+      float *red4 = reinterpret_cast<float *>(sa + static_cast<size_t>(nbm) * kBoxB);
       const int mt = warp & 1, kq = warp >> 1, kw = Mc / 4;
-      for (int it = 0; it < my5; ++it) {
+      for (int it = 0; it < my4; ++it) {
         float acc[NT][4] = {};
-        for (int s5 = 0; s5 < kw / 16; ++s5) {
-          const int k = kq * kw + s5 * 16, b = k / 64, kc = (k % 64) / 16;
+        for (int s4 = 0; s4 < kw / 16; ++s4) {
+          const int k = kq * kw + s4 * 16, b = k / 64, kc = (k % 64) / 16;
           uint32_t A[4];
-          ld_a(sw + b * kP5Stride + it * 4096, mt * 16, kc, A);
+          ld_a(sw + b * kP4Stride + it * 4096, mt * 16, kc, A);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             uint32_t Bf[4];
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int row = mt * 16 + g4 + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
-            red5[((it * 4 + kq) * kW5Rows + row) * NTOK + t] = acc[nt][e];
+            red4[((it * 4 + kq) * kW4Rows + row) * NTOK + t] = acc[nt][e];
           }
       }
       __syncthreads();
@@ -467,13 +467,13 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       for (int u = 0; u < kMaxUpd; ++u) {
         const int idx = threadIdx.x + u * kBrThreads;
         if (idx >= n_upd) break;
-        const int it = idx / (kW5Rows * T), rem = idx % (kW5Rows * T);
-        const int row = rem % kW5Rows, t = rem / kW5Rows;
+        const int it = idx / (kW4Rows * T), rem = idx % (kW4Rows * T);
+        const int row = rem % kW4Rows, t = rem / kW4Rows;
         if (t % W == 0) continue;
         float v = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v += red5[((it * 4 + q) * kW5Rows + row) * NTOK + t];
-        a.x[static_cast<size_t>(t) * H + (cta + it * static_cast<int>(gridDim.x)) * kW5Rows + row] =
+        for (int q = 0; q < 4; ++q) v += red4[((it * 4 + q) * kW4Rows + row) * NTOK + t];
+        a.x[static_cast<size_t>(t) * H + (cta + it * static_cast<int>(gridDim.x)) * kW4Rows + row] =
             xv[u] + __ldcg(a.r + t) * v;
       }
     }
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
   body();
   // copies still in flight after an early exit are waited for (bounded) before the CTA ends
   if (w1_pending) mbar_wait(&mb[0], 0);
-  if (w5_pending) mbar_wait(&mb[1], 0);
+  if (w4_pending) mbar_wait(&mb[1], 0);
 }
 
 // ------------------------------------------------------------------ host
@@ -512,18 +512,18 @@ BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms) {
   if (p.kz > 128 * kBrMaxJ) return p;
   p.n_kz = (H + p.kz - 1) / p.kz;
   p.n1 = gz * p.n_kz;
-  const int n5 = H / kW5Rows, it5 = (n5 + sms - 1) / sms;
-  if (it5 > 2) return p;  // P5 holds two items per K box
+  const int n4 = H / kW4Rows, it4 = (n4 + sms - 1) / sms;
+  if (it4 > 2) return p;  // P4 holds two items per K box
   const int nbc = Rc / 64, nbm = Mc / 64;
-  // weight area: the P1 chunk, the P3 slices or the P5 items
+  // weight area: the P1 chunk, the P3 slices or the P4 items
   p.sw_bytes = std::max(static_cast<size_t>(p.kz / 64) * kPackBox,
-                        std::max(static_cast<size_t>(nbc) * kP3Stride, static_cast<size_t>(nbm) * kP5Stride));
+                        std::max(static_cast<size_t>(nbc) * kP3Stride, static_cast<size_t>(nbm) * kP4Stride));
   p.sw_bytes = (p.sw_bytes + 1023) / 1024 * 1024;
   p.p3_boxes = static_cast<int>(std::min(static_cast<size_t>(nbc), std::max<size_t>(1, 65536 / box)));
   const size_t red3 = static_cast<size_t>(8) * 3 * 16 * ntok * 4;
-  const size_t p5 = static_cast<size_t>(nbm) * box + static_cast<size_t>(it5) * 4 * kW5Rows * ntok * 4;
+  const size_t p4 = static_cast<size_t>(nbm) * box + static_cast<size_t>(it4) * 4 * kW4Rows * ntok * 4;
   p.sa_bytes = std::max(std::max(static_cast<size_t>(p.kz / 64) * box, static_cast<size_t>(p.p3_boxes) * box),
-                        std::max(red3, p5));
+                        std::max(red3, p4));
   p.smem = p.sw_bytes + p.sa_bytes;
   const int lim = max_dyn_smem();
   p.ok = lim > 0 && p.smem + 1024 <= static_cast<size_t>(lim);

@@ -51,3 +51,36 @@ def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
     top2 = np.sort(logits, axis=1)[:, -2:]
     sel = top2[:, 1] - top2[:, 0] > 1e-3
     assert (tok.cpu().numpy()[sel] == logits.argmax(axis=1)[sel]).all()
+
+
+# the block geometry of the small parity cases: batch 3 (48 rows) takes the five-launch
+# bridge, batch 2 (32 rows) the one-launch bridge
+_SMALL = bdsynth.Workload(
+    name="small_bf16", hidden=512, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
+    ffn=1024, vocab=4000, n_target_layers=3, windows=(64, 0), code_width=128, msg_width=64,
+    batch=3, n_masks=15, dtype="bf16", ctx_min=40, ctx_max=300, full_capacity=320)
+
+
+@pytest.mark.parametrize("batch", [3, 2])
+def test_out_of_range_anchor_is_reported_without_a_fault(batch):
+    """An anchor id outside the vocabulary is a device-side index error: the kernels that
+    read it clamp the index (no out-of-bounds access), flag the error word, and
+    bd_sync_status reports BD_ERR_INVALID_ARG once; a valid round afterwards is clean and
+    repeats the result of a round that never saw the bad id."""
+    import harness as Hn
+    from block_drafter_gb300 import binding as B
+    geo = _SMALL.with_(batch=batch)
+    case = Hn.Case(geo, seed=11, max_ctx_rows=128)
+    case.fill_rings()
+    good = case.run_gpu()
+    anchors = list(case.anchors)
+    case.anchors = list(anchors)
+    case.anchors[batch - 1] = geo.vocab          # one past the last id
+    with pytest.raises(B.BdError) as err:
+        case.run_gpu()
+    assert err.value.status == -1                # BD_ERR_INVALID_ARG
+    B.sync_status()                              # reported once, then clear
+    case.anchors = anchors
+    again = case.run_gpu()
+    assert torch.equal(again["layers"], good["layers"])
+    assert torch.equal(again["tokens"], good["tokens"])

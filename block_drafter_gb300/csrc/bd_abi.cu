@@ -199,7 +199,7 @@ struct RoundWs {
   unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
   float *x, *z, *pre, *r, *part_o, *qkv_raw, *feat, *kv_raw;
   float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
-  unsigned *br_bar;    // [L][5] fused-bridge barrier counters, right after att_cnt
+  unsigned *br_bar;    // [L][5] fused-bridge barrier counters (3 used), right after att_cnt
   float *zpart, *sspart, *zsq;  // fused-bridge partial sums
   float2 *rope, *part_ml;
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;

@@ -373,11 +373,6 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         }
         __syncthreads();  // the chunk's boxes (and, at the end, the weights) are free
       }
-      if (threadIdx.x == 0) {
-        fence_proxy_async_shared();
-        load_w4();
-      }
-      w4_pending = my4 > 0;
       // per-warp K partials [warp][mat][16 rows][NTOK], added in warp order and scaled
       float *red3 = reinterpret_cast<float *>(sa);
 #pragma unroll
@@ -409,6 +404,13 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         }
         put_split(m + act_off(R, t, jj), m + act_off(R, NTOK + t, jj), mv);
       }
+      // the weight area is free since the chunk loop's last barrier: phase 4's rows, issued
+      // now so that their copies overlap the grid barrier
+      if (threadIdx.x == 0) {
+        fence_proxy_async_shared();
+        load_w4();
+      }
+      w4_pending = my4 > 0;
     }
     if (!grid_sync(a.bar + 2, &s_ok)) return;
 

@@ -275,8 +275,6 @@ template <typename T, int E>
 __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ HeadPostArgs a) {
   const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
   int wg = warp, g = 0;
   if (a.n_groups > 1 && wg >= a.grp[0].rows * a.grp[0].total_heads) {
     wg -= a.grp[0].rows * a.grp[0].total_heads;
@@ -285,8 +283,7 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   const HeadGroup gr = a.grp[g];
   const int rr = wg / gr.total_heads;  // row within the group
   int hg = wg % gr.total_heads;
-  if (rr >= gr.rows) return;
-  const int row = gr.row0 + rr;
+  const bool live = rr < gr.rows;
   int si = gr.seg0;
   while (si + 1 < gr.seg0 + gr.n_segs && hg >= a.seg[si].n_heads) {
     hg -= a.seg[si].n_heads;
@@ -295,6 +292,15 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   const HeadSeg sg = a.seg[si];
   const int D = E * 32, half = D / 2;
   const int d0 = lane * E;
+  // the head-norm gain (a weight: no earlier kernel writes it) before the dependency wait
+  float gn[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    gn[e] = live && sg.kind != HK_V ? to_f<T>(static_cast<const T *>(sg.norm)[d0 + e]) : 1.f;
+  pdl_wait();
+  pdl_trigger();
+  if (!live) return;
+  const int row = gr.row0 + rr;
   const float *src = a.raw + static_cast<size_t>(row) * a.ld_raw + sg.col0 + hg * D + d0;
   float v[E];
 #pragma unroll
@@ -305,9 +311,8 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
     for (int e = 0; e < E; ++e) ss += v[e] * v[e];
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
-    const T *gain = static_cast<const T *>(sg.norm);
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] *= inv * to_f<T>(gain[d0 + e]);
+    for (int e = 0; e < E; ++e) v[e] *= inv * gn[e];
     const float2 *cs = a.rope + static_cast<size_t>(row) * half;
 #pragma unroll
     for (int e = 0; e < E; ++e) {

@@ -183,7 +183,7 @@ __device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)
 // Few splits (S <= SMAX): each warp merges rows r0 + warp, r0 + warp + 4, ... RB at a time,
 // with every load of those rows (the splits' (m, l) and partial rows) issued before any
 // arithmetic, so they cost one round trip to L2.  Splits are added in index order.
-constexpr int kFewSplits = 16;
+constexpr int kFewSplits = 8;
 template <typename T, int D, int SMAX, int RB>
 __device__ __forceinline__ void combine_rows_few(const AttArgs &a, int b, int h, int r0, int r1,
                                                  int warp, int lane) {
@@ -688,11 +688,8 @@ __global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_con
   if (s_abort) return;
   const int rp = (R + a.n_splits - 1) / a.n_splits;
   __shared__ float red[4][D + 4];
-  if (a.n_splits <= 8)
-    combine_rows_few<__nv_bfloat16, D, 8, 2>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp),
-                                             warp, lane);
-  else if (a.n_splits <= kFewSplits)
-    combine_rows_few<__nv_bfloat16, D, kFewSplits, 1>(a, b, h, min(R, split * rp),
+  if (a.n_splits <= kFewSplits)
+    combine_rows_few<__nv_bfloat16, D, kFewSplits, 2>(a, b, h, min(R, split * rp),
                                                       min(R, (split + 1) * rp), warp, lane);
   else
     combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,

@@ -17,10 +17,10 @@
 // issuing tcgen05.mma spends ~40 ns per instruction, more than the whole product takes on
 // the warps' tensor instructions.  Weights come from the packed image, whose boxes are in
 // the 128-byte-swizzled order (conflict-free ldmatrix): the first phase's as bulk copies
-// issued before the dependency wait, P4's as soon as the CTA's first product has released
-// its weight area.  The activations (x, the codes, the message) are written in the same
-// swizzled box order, so the codes and the message reach shared memory as single bulk
-// copies.  Partial sums are added in a fixed order, so results are deterministic.  Every
+// issued before the dependency wait, P4's once the CTA's earlier product is done with the
+// weight area (after the code-read product, or after the gate/value CTAs' message).  The
+// activations (x, the codes, the message) are written in the same swizzled box order, so
+// the codes and the message reach shared memory as single bulk copies.  Partial sums are added in a fixed order, so results are deterministic.  Every
 // CTA is resident at once (grid = SM count, one CTA per SM), each wait is bounded
 // (wait_count, mbar_wait), and a wait that gives up ends the launch with the error word set.
 #include "bd_device.cuh"

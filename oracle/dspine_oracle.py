@@ -31,7 +31,7 @@ Sources (cited by page title and section throughout):
                   target feature rows that the drafter has not yet converted are
                   materialised before the block is proposed, so the context reaches F.
 
-Readings taken where the pages are schematic or garbled (each also listed in the design doc):
+Readings taken where the pages are schematic or garbled:
   R-gate   g = sigmoid(G c_t + G_p c_{t-1} + b), m = g * (A c_{t-1}); b absent means 0.
   R-eps    the bridge floor epsilon is the config's RMSNorm eps; r itself has no eps.
   R-scale  the code scale is sqrt(Rc); anchor code = sqrt(Rc) * codebook[anchor].

@@ -756,6 +756,80 @@ def test_catch_up_touches_only_its_requests():
     assert np.any(got["h"][1] != base["h"][1])
 
 
+def test_round_block_rows_sit_at_frontier_plus_i_with_head_norm_before_rope():
+    """[DFlash-notes] draft input table (anchor at position F, mask i at F + i) and per-layer
+    equations (q = rope(head_rmsnorm(W_q n))), worked out by hand on a D = 2 geometry.
+
+    One layer, one head, W_q = W_k = I, W_v = 0, W_o = I, no MLP, unit norms except a
+    non-uniform query head-norm gain g = (2, 1/2), eps = 0.  Both embedding rows are
+    e = (1, 0), so n = head_rmsnorm(e) = (sqrt 2, 0) and, head norm first, then RoPE
+    (D = 2: angle = position), a row at position P has
+        q = 2 sqrt2 (cos P, sin P),   k = sqrt2 (cos P, sin P).
+    Every context key is (0, 1) (the rings hold rotated keys), so a query at P scores
+    q.(0,1)/sqrt2 = 2 sin P on each of them; against a block row at P' it scores
+    4 cos(P - P')/sqrt2.  Block-causal: row i sees the context and rows 0..i.  The block
+    values are 0, so x_i' = e + sum_p w_p v_p over the context values v_p.
+    RoPE after the head norm gives 0.5 sin P on the context instead; block positions
+    0..W-1 or F-1+i shift P: each such reading changes the values below."""
+    g = Geo(hidden=2, n_layers=1, n_q_heads=1, n_kv_heads=1, head_dim=2, ffn=2, vocab=4,
+            windows=(0,), code_width=0, msg_width=0, eps=0.0, rope_theta=1e4,
+            block_causal=True, full_capacity=8)
+    I2, Z2 = np.eye(2), np.zeros((2, 2))
+    w = {"w_feature": np.zeros((2, 4)), "context_norm": np.ones(2), "final_norm": np.ones(2),
+         "embed_head": np.array([[1.0, 0.0], [1.0, 0.0], [0.0, 1.0], [0.0, -1.0]]),
+         "layers": [{"in_norm": np.ones(2), "wq": I2, "wk": I2, "wv": Z2,
+                     "q_norm": np.array([2.0, 0.5]), "k_norm": np.ones(2), "wo": I2,
+                     "post_norm": np.ones(2), "w_gate": Z2, "w_up": Z2, "w_down": Z2}]}
+    F, K = 3, 2
+    vals = [(1.0, -2.0), (0.5, 3.0), (-4.0, 1.0)]                 # context values, positions 0..2
+    rings = {"k": [np.zeros((1, 1, 8, 2))], "v": [np.zeros((1, 1, 8, 2))]}
+    for p in range(F):
+        rings["k"][0][0, 0, p] = (0.0, 1.0)
+        rings["v"][0][0, 0, p] = vals[p]
+    res = O.draft_round(g, w, rings, [1], [F], 0, K, with_head=False)
+    r2 = math.sqrt(2.0)
+    for i in range(K + 1):
+        P = F + i
+        ctx = [math.exp(2.0 * math.sin(P))] * F
+        blk = [math.exp(4.0 * math.cos(P - (F + j)) / r2) for j in range(i + 1)]
+        tot = sum(ctx) + sum(blk)
+        want = [1.0 + sum(c * v[0] for c, v in zip(ctx, vals)) / tot,
+                sum(c * v[1] for c, v in zip(ctx, vals)) / tot]
+        np.testing.assert_allclose(res["x_layers"][0][0, i], want, rtol=1e-13, atol=1e-14)
+
+
+def test_context_kv_head_norm_before_rope_hand_value():
+    """[DFlash-notes] context K/V: k = rope(head_rmsnorm(W_k c), t).  With W_k = I,
+    c = (1, 0), key gain (2, 1/2), eps = 0 and D = 2 (angle = t):
+    head_rmsnorm(c) = (sqrt 2, 0), times the gain (2 sqrt2, 0), rotated by t:
+    k = 2 sqrt2 (cos t, sin t).  Rotating first would give (2 sqrt2 cos t, sin t / sqrt2)."""
+    for t in (0, 3, 7):
+        k, v = O.context_kv(np.array([[1.0, 0.0]]), [t], np.eye(2), np.eye(2),
+                            np.array([2.0, 0.5]), 0.0, 2, 1e4)
+        np.testing.assert_allclose(k[0], 2 * math.sqrt(2.0) * np.array([math.cos(t), math.sin(t)]),
+                                   rtol=1e-14, atol=1e-15)
+        np.testing.assert_array_equal(v[0], [1.0, 0.0])
+
+
+def test_round_is_invariant_to_shifting_every_position():
+    """RoPE scores depend only on position differences and the window rule only on
+    distances ([DFlash-notes] local-window attention rule), so materialising the same
+    features at positions D..F+D-1 and drafting at frontier F+D must reproduce the
+    round at frontier F: the block must move with the frontier.  (Local layers only: a
+    full-context layer attends from position 0, so it has no shift symmetry.)"""
+    g = Geo(windows=(5, 4), full_capacity=40)
+    w = rand_weights(g, gate_bias=True)
+    F, shift = 9, 13
+    feats = rng.normal(0, 1, (F, g.n_target_layers * g.hidden))
+    a_r = O.materialize(g, w, feats, np.arange(F), F)
+    b_r = O.materialize(g, w, feats, np.arange(F) + shift, F + shift)
+    a = O.draft_round(g, w, a_r, [5], [F], 0, 6)
+    b = O.draft_round(g, w, b_r, [5], [F + shift], 0, 6)
+    for key in ("x_layers", "h", "logits"):
+        np.testing.assert_allclose(b[key], a[key], rtol=1e-9, atol=1e-11)
+    np.testing.assert_array_equal(a["tokens"], b["tokens"])
+
+
 def test_round_with_no_layer_updates_is_embedding_nearest_row():
     # W_o = 0, W_down = 0, W_write = 0: every layer is the identity, so the final state is
     # the embedding rows and each mask row's proposal is argmax_v E_v . rmsnorm(E_MASK).

@@ -39,6 +39,7 @@ import torch  # noqa: E402
 import bdsynth  # noqa: E402
 
 TOPK = 16  # candidates per proposal row of the top-k head (timed beside the step)
+CPU_SAMPLES = 4  # oracle steps timed for the cpu_baseline (about 3 s each on 16 cores)
 METRIC = "draft rounds/s (B=1, W=16, 27B DSpine-b16 geometry)"
 UNIT = "rounds/s"
 
@@ -371,6 +372,30 @@ def dflash2_lines(args, world, hbm) -> dict:
     return out
 
 
+def dflash35b_line(args, world, hbm, peak_kind) -> dict:
+    """Plain DFlash at the 35B-A3B draft geometry, B=8 (5 local layers with window 4096 and
+    one full-context layer, contexts uniform in [4096, 32768], no injection): the same step
+    (round with the fused catch-up + LM head) and the round alone."""
+    geo = bdsynth.DFLASH35B_B8
+    st = State(geo, args.seed)
+    ms, per = time_graphs(st, args.steps, args.warmup, world)
+    ms = max_over_ranks(ms, world)
+    by = st.bytes_per_step()
+    gbs = by["total"] / (ms * 1e-3) / 1e9
+    ro = round_only(st, args)
+    kt = kernel_times(st, min(args.steps, 10), args.warmup, hbm)
+    dom = dominant(kt)
+    out = {"workload": geo.name, "contexts": st.F, "us_per_step": 1000.0 * ms,
+           "rounds_per_s": world * 1000.0 / ms,
+           "breakdown_us": {k: 1000.0 * v for k, v in per.items()}, "round_only": ro,
+           "achieved_step_gbs": gbs, "frac_of_measured_hbm": gbs / hbm,
+           "algorithmic_bytes_per_step": by,
+           "roofline": roofline_entry(dom, kt, hbm, peak_kind, KIND_NAMES[dom]), "kernels": kt}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def refine_us(st: State, args) -> float:
     """Device time of the last-write refinement (tables + walk) after a round that exported
     its tail state and a top-16 head that produced the candidates."""
@@ -378,6 +403,126 @@ def refine_us(st: State, args) -> float:
     st.head_topk()
     torch.cuda.synchronize()
     return 1000.0 * time_call(st.refine, args.steps, args.warmup)
+
+
+KERNEL_KINDS = ("qkv", "attention", "wo", "gate_up", "down", "bridge", "head")
+
+
+def kernel_bytes(st: State) -> dict:
+    """Algorithmic bytes of each kernel kind's launches in one step (weights as stored,
+    2 bytes per element; the attention's windowed context K/V of every request; the head
+    adds its fp32 input rows)."""
+    geo = st.geo
+    H, D = geo.hidden, geo.head_dim
+    QD, KD = geo.n_q_heads * D, geo.n_kv_heads * D
+    el = 2 if geo.dtype == "bf16" else 4
+    att = []
+    for l in range(geo.n_layers):
+        S = geo.windows[l]
+        ctx = sum((min(F, S - 1) if S > 0 else F) for F in st.F)
+        att.append(ctx * KD * el * 2)
+    out = {"qkv": [(QD + 2 * KD) * H * el] * geo.n_layers, "attention": att,
+           "wo": [H * QD * el] * geo.n_layers, "gate_up": [2 * geo.ffn * H * el] * geo.n_layers,
+           "down": [H * geo.ffn * el] * geo.n_layers,
+           "head": [geo.vocab * H * el + st.head_in.numel() * 4]}
+    if geo.code_width and geo.batch * geo.W <= 32:  # the one-launch bridge (small blocks)
+        Rc, Mc = geo.code_width, geo.msg_width
+        out["bridge"] = [(Rc * H + H * Mc + 3 * Mc * Rc) * el] * geo.n_layers
+    return out
+
+
+def kernel_times(st: State, steps: int, warmup: int, hbm: float) -> dict:
+    """Per-launch device time of each kernel kind of the step, from CUDA events the library
+    records around those launches (bd_set_timing_events) in a captured step, averaged over
+    the layers and ``steps`` replays.  An event between two launches removes their
+    programmatic overlap, so this runs apart from the timed step; the bracketed launch
+    itself is measured from the moment its predecessor has finished."""
+    from block_drafter_gb300 import binding
+    nbytes = kernel_bytes(st)
+    out = {}
+    for kind in KERNEL_KINDS:
+        if kind not in nbytes:
+            continue
+        n = len(nbytes[kind])
+        b = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        binding.set_timing_events(kind, b, e)
+        try:
+            g = capture(st.step)
+        finally:
+            binding.set_timing_events(None)
+        for _ in range(warmup):
+            g.replay()
+        tot = [0.0] * n
+        try:
+            for _ in range(steps):
+                g.replay()
+                torch.cuda.synchronize()
+                for i in range(n):
+                    tot[i] += b[i].elapsed_time(e[i])
+        except RuntimeError as ex:  # an event was never recorded
+            torch.cuda.synchronize()
+            out[kind] = {"error": str(ex)[:200]}
+            continue
+        us = [1000.0 * t / steps for t in tot]
+        by = sum(nbytes[kind])
+        gbs = by / (sum(us) * 1e-6) / 1e9
+        out[kind] = {"launches": n, "us_per_launch": sum(us) / n, "us_per_step": sum(us),
+                     "bytes_per_launch": by / n, "achieved_gbs": gbs, "frac_of_measured_hbm": gbs / hbm}
+        del g
+    return out
+
+
+def dominant(kt: dict) -> str:
+    """The kernel kind with the largest device time per step."""
+    ok = {k: v for k, v in kt.items() if "us_per_step" in v}
+    if not ok:
+        raise RuntimeError(f"no kernel kind was timed: {kt}")
+    return max(ok, key=lambda k: ok[k]["us_per_step"])
+
+
+def roofline_entry(kind: str, kt: dict, hbm: float, peak_kind: str, what: str) -> dict:
+    k = kt[kind]
+    return {"bound": "hbm", "kernel": what, "achieved": k["achieved_gbs"], "peak": hbm, "unit": "GB/s",
+            "frac": k["achieved_gbs"] / hbm, "traffic": recorded_traffic(kind),
+            "algorithmic_bytes": k["bytes_per_launch"], "us_per_launch": k["us_per_launch"],
+            "peak_kind": peak_kind}
+
+
+KIND_NAMES = {"qkv": "Q/K/V product (tcgen05 GEMM)", "attention": "block attention",
+              "wo": "output projection (tcgen05 GEMM, residual epilogue)",
+              "gate_up": "SwiGLU gate/up product (tcgen05 GEMM, SwiGLU epilogue)",
+              "down": "down projection (tcgen05 GEMM, residual epilogue)",
+              "bridge": "fused DSpine bridge (code read + gate/message + write)",
+              "head": "LM head product (tcgen05 GEMM, per-tile argmax epilogue)"}
+
+
+def materialize_line(st: State, steps: int, warmup: int, tf_sust: float, tf_burst: float,
+                     hbm: float) -> dict:
+    """Context K/V materialisation of a 2048-row prefill chunk at positions 0..2047 (27B
+    geometry: W_feature 25600 -> 5120 with the context norm, then every layer's W_k|W_v,
+    head norm, RoPE and ring store).  Uses the B=1 state's weights and request-0 rings."""
+    geo = st.geo
+    n = 2048
+    dev = "cuda"
+    feats = bdsynth.target_features(bdsynth.CTX27B, n, 0, stream=77, device=dev)
+    req = torch.zeros(n, dtype=torch.int32, device=dev)
+    pos = torch.arange(n, dtype=torch.int64, device=dev)
+    front = torch.tensor([n], dtype=torch.int64, device=dev)
+
+    def call():
+        st.sess.materialize(feats, req, pos, front)
+    ms = time_call(call, steps, warmup)
+    H = geo.hidden
+    KD = geo.n_kv_heads * geo.head_dim
+    flops = 2.0 * n * geo.n_target_layers * H * H + 2.0 * n * geo.n_layers * 2 * KD * H
+    by = (H * geo.n_target_layers * H + geo.n_layers * 2 * KD * H) * 2 + n * geo.n_target_layers * H * 2 \
+        + geo.n_layers * n * 2 * KD * 2
+    tfs = flops / (ms * 1e-3) / 1e12
+    return {"workload": bdsynth.CTX27B.name, "rows": n, "us": 1000.0 * ms, "tflops": tfs,
+            "flops": flops, "frac_of_sustained_bf16": tfs / tf_sust, "frac_of_burst_bf16": tfs / tf_burst,
+            "bound": "tensor", "algorithmic_bytes": by,
+            "frac_of_measured_hbm": by / (ms * 1e-3) / 1e9 / hbm}
 
 
 def time_e2e(st: State, steps: int, warmup: int):
@@ -409,14 +554,16 @@ def time_e2e(st: State, steps: int, warmup: int):
     return e0.elapsed_time(e1) / steps, bi, bo
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the roofline kernel from the committed ncu record, if the
+def recorded_traffic(kind: str):
+    """DRAM bytes per launch of one kernel kind from the committed ncu record, if the
     kernel's sources are unchanged since the counters were taken (else None)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p))
+    rec = json.load(open(p)).get("kernels", {}).get(kind)
+    if rec is None:
+        return None
     h = hashlib.sha256()
     for f in rec["source_files"]:
         fp = os.path.join(ROOT, f)
@@ -430,8 +577,9 @@ def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return d["hbm_gbs"], d.get("bf16_tflops_sustained", 1715.0), "measured"
-    return 6800.0, 1700.0, "fallback"
+        return (d["hbm_gbs"], d.get("bf16_tflops_sustained", 1715.0), d.get("bf16_tflops", 1875.0),
+                "measured")
+    return 6800.0, 1700.0, 1900.0, "fallback"
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -553,7 +701,7 @@ def main():
     ms, per = time_graphs(st, args.steps, args.warmup, world)
     ck = clocks.stop()
     ms = max_over_ranks(ms, world)
-    hbm, tf, peak_kind = peaks()
+    hbm, tf, tf_burst, peak_kind = peaks()
     by = st.bytes_per_step()
     head_bytes = by["head"] + st.head_in.numel() * st.head_in.element_size()  # weights + fp32 rows
     head_gbs = head_bytes / (per["head"] * 1e-3) / 1e9
@@ -583,10 +731,11 @@ def main():
         "achieved_step_gbs": step_gbs,
         "step_roofline_frac": {"of_measured_hbm": step_gbs / hbm, "of_8tbs": step_gbs / 8000.0},
         "algorithmic_bytes_per_step": by,
-        "roofline": {"bound": "hbm", "kernel": "LM head call (tcgen05 GEMM + split-vocab argmax reduce)",
-                     "achieved": head_gbs, "peak": hbm, "unit": "GB/s", "frac": head_gbs / hbm,
-                     "traffic": recorded_traffic(), "algorithmic_bytes": head_bytes,
-                     "peak_kind": peak_kind},
+        "roofline_lm_head_call": {"bound": "hbm",
+                                  "kernel": "LM head call (tcgen05 GEMM + split-vocab argmax reduce)",
+                                  "achieved": head_gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": head_gbs / hbm, "algorithmic_bytes": head_bytes,
+                                  "peak_kind": peak_kind},
         "clocks": ck,
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
@@ -596,6 +745,12 @@ def main():
         "head_topk16_fp8_us": 1000.0 * time_call(st.head_topk_fp8, args.steps, args.warmup),
         "refine_tail_us": refine_us(st, args),
     }
+    # per-kernel device times inside the step; the roofline entry is the kernel kind with
+    # the largest share of the step
+    kt = kernel_times(st, min(args.steps, 10), args.warmup, hbm)
+    dom = dominant(kt)
+    line["roofline"] = roofline_entry(dom, kt, hbm, peak_kind, KIND_NAMES[dom])
+    line["kernels"] = kt
     if not args.no_b8 and args.workload == "b1":
         geo8 = bdsynth.DSPINE27B_B8
         st8 = State(geo8, args.seed, weights=st.w)
@@ -614,19 +769,30 @@ def main():
                       "head_topk16_fp8_us": 1000.0 * time_call(st8.head_topk_fp8, args.steps,
                                                                args.warmup),
                       "refine_tail_us": refine_us(st8, args)}
+        kt8 = kernel_times(st8, min(args.steps, 10), args.warmup, hbm)
+        dom8 = dominant(kt8)
+        line["b8"]["roofline"] = roofline_entry(dom8, kt8, hbm, peak_kind, KIND_NAMES[dom8])
+        line["b8"]["kernels"] = kt8
         del st8
     if not args.no_b8 and args.workload == "b1":
         line["dflash2"] = dflash2_lines(args, world, hbm)
+        line["dflash_35b_b8"] = dflash35b_line(args, world, hbm, peak_kind)
     if rank == 0 and not args.no_cpu_baseline:
-        import numpy as np
         wh = host_weights(st.w)
         feats = st.feats[:geo.W].float().cpu().numpy()
         pos = st.row_pos[:geo.W].cpu().numpy()
-        t = oracle_step_sample(geo, wh, st.F, st.anchors_l, st.mask, feats, pos)
+        ts = [oracle_step_sample(geo, wh, st.F, st.anchors_l, st.mask, feats, pos)
+              for _ in range(CPU_SAMPLES)]
+        t = statistics.mean(ts)
         line["cpu_baseline"] = {"value": 1.0 / t, "unit": UNIT, "cores": cpu_threads(),
                                 "kind": "oracle",
-                                "sample": "one full step of request 0 (catch-up of 16 rows, "
-                                          "5-layer round, full LM head) at B=1, timed once"}
+                                "sample": f"one full step of request 0 (catch-up of 16 rows, "
+                                          f"5-layer round, full LM head) at B=1, mean of "
+                                          f"{CPU_SAMPLES} runs",
+                                "seconds_per_sample": ts}
+    if args.workload == "b1":
+        # last: it overwrites request 0's rings of the B=1 state
+        line["ctx_materialize_2048"] = materialize_line(st, args.steps, args.warmup, tf, tf_burst, hbm)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

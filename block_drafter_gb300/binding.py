@@ -20,13 +20,13 @@ BF16, F32 = 0, 1
 BIDIRECTIONAL, CAUSAL = 0, 1
 
 STATUS = {0: "BD_OK", -1: "BD_ERR_INVALID_ARG", -2: "BD_ERR_UNSUPPORTED", -3: "BD_ERR_CUDA",
-          -4: "BD_ERR_DEVICE_TIMEOUT", -5: "BD_ERR_WORKSPACE"}
+          -4: "BD_ERR_DEVICE_TIMEOUT", -5: "BD_ERR_WORKSPACE", -6: "BD_ERR_RANGE"}
 
 EXPORTS = ("bd_abi_version", "bd_workspace_bytes", "bd_ctx_kv_materialize", "bd_draft_round",
            "bd_lm_head_argmax", "bd_last_error", "bd_sync_status", "bd_kernel_launches",
            "bd_packed_bytes", "bd_pack_weights", "bd_lm_head_argmax_noalloc", "bd_lm_head_topk",
            "bd_refine_tail", "bd_head_fp8_bytes", "bd_pack_head_fp8", "bd_lm_head_topk_fp8",
-           "bd_selftest_wait")
+           "bd_selftest_wait", "bd_set_timing_events")
 
 TOPK_MAX = 16
 
@@ -124,6 +124,8 @@ def lib() -> C.CDLL:
         L.bd_lm_head_topk_fp8.restype = i
         L.bd_lm_head_topk_fp8.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, vp, i, i, i,
                                           vp, vp, vp, sz, vp]
+        L.bd_set_timing_events.restype = i
+        L.bd_set_timing_events.argtypes = [i, C.POINTER(vp), C.POINTER(vp), i]
         _lib = L
     return _lib
 
@@ -310,6 +312,25 @@ def lm_head_argmax_noalloc(cfg: Config, weights: Weights, hidden: torch.Tensor,
     _check(lib().bd_lm_head_argmax_noalloc(
         C.byref(cfg), C.byref(weights), _ptr(hidden), int(hidden.shape[0]), _ptr(token_out),
         _ptr(max_logit_out), _stream(stream)))
+
+
+TIME_KINDS = {"qkv": 1, "attention": 2, "wo": 3, "gate_up": 4, "down": 5, "bridge": 6, "head": 7}
+
+
+def set_timing_events(kind: Optional[str], begin=(), end=()):
+    """Bracket the launches of one kernel kind with CUDA events (bd_set_timing_events);
+    ``begin``/``end`` are torch.cuda.Event objects with timing enabled.  kind None clears."""
+    if kind is None:
+        _check(lib().bd_set_timing_events(0, None, None, 0))
+        return
+    n = len(begin)
+    assert n == len(end) and n > 0
+    for ev in list(begin) + list(end):  # torch creates the CUDA event on first record
+        if ev.cuda_event == 0:
+            ev.record()
+    arr_b = (C.c_void_p * n)(*[ev.cuda_event for ev in begin])
+    arr_e = (C.c_void_p * n)(*[ev.cuda_event for ev in end])
+    _check(lib().bd_set_timing_events(TIME_KINDS[kind], arr_b, arr_e, n))
 
 
 def kernel_launches() -> int:

@@ -15,6 +15,16 @@
 
 namespace {
 thread_local std::string t_last_error;
+
+// Launch bracketing for measurement (bd_set_timing_events): while a kind is set, the
+// i-th launch of that kind in a call is bracketed by begin[i] / end[i].
+struct Timing {
+  int kind = BD_TIME_NONE;
+  int n = 0;
+  int next = 0;
+  cudaEvent_t begin[BD_TIMING_MAX], end[BD_TIMING_MAX];
+};
+thread_local Timing t_timing;
 }  // namespace
 
 namespace bd {
@@ -36,6 +46,28 @@ bd_status fail(bd_status s, const std::string &msg) {
   do {                                                     \
     std::string _e = (expr);                               \
     if (!_e.empty()) return fail(BD_ERR_CUDA, _e);         \
+  } while (0)
+
+// Records the next begin event of `kind` (if that kind is being timed) on stream s.
+std::string timing_begin(int kind, cudaStream_t s) {
+  Timing &t = t_timing;
+  if (t.kind != kind || t.next >= t.n) return {};
+  // external: inside stream capture the record becomes an event node of the graph
+  const cudaError_t e = cudaEventRecordWithFlags(t.begin[t.next], s, cudaEventRecordExternal);
+  return e == cudaSuccess ? std::string() : std::string("cudaEventRecord: ") + cudaGetErrorString(e);
+}
+std::string timing_end(int kind, cudaStream_t s) {
+  Timing &t = t_timing;
+  if (t.kind != kind || t.next >= t.n) return {};
+  const cudaError_t e = cudaEventRecordWithFlags(t.end[t.next++], s, cudaEventRecordExternal);
+  return e == cudaSuccess ? std::string() : std::string("cudaEventRecord: ") + cudaGetErrorString(e);
+}
+// launch_expr bracketed by the timing events of `kind`
+#define BD_TIMED(kind, expr)              \
+  do {                                    \
+    BD_TRY(timing_begin((kind), s));      \
+    BD_TRY(expr);                         \
+    BD_TRY(timing_end((kind), s));        \
   } while (0)
 
 constexpr int kMaxB = 8;
@@ -409,6 +441,11 @@ void add_w(GemmPlan &p, const void *ptr, int rows, const uint8_t *packed_base = 
 
 }  // namespace
 
+namespace bd {
+// The configuration checks every entry point applies, for entry points in other files.
+std::string validate_config(const bd_config *c) { return check_config(c); }
+}  // namespace bd
+
 // S2 for n context rows c (config dtype, [n][H]): every layer's raw K|V in one product
 // (up to kMaxSegs/2 layers per launch) into kv_raw [n][L*2*Hkv*D], then head norm + RoPE +
 // ring scatter of every layer in one launch (row r at position pos[r] of ring row
@@ -604,6 +641,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     if (cfg->dtype == BD_F32 && att_max_keys(cfg, l, W) > 48 * 1024)
       return fail(BD_ERR_UNSUPPORTED, "fp32 attention supports at most 49152 keys per layer");
   cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  t_timing.next = 0;
   const int sms = num_sms();
   Carve cv;
   cv.base = static_cast<char *>(workspace);
@@ -708,7 +746,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.seg[0].out_col = 0;
       p.args.seg[1].out_col = QD;
       p.args.seg[2].out_col = QD + KD;
-      BD_TRY(launch_gemm(p, sc, s));
+      BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
       HeadPostArgs h;
       memset(&h, 0, sizeof h);
       h.raw = rw.qkv_raw;
@@ -770,7 +808,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.q_lo = split && !mlp16 ? static_cast<size_t>(T) * QD : 0;
       a.blk_lo = split && !mlp16 ? static_cast<size_t>(T) * KD : 0;
       a.out_lo = lo(QD);
-      BD_TRY(launch_attention(a, dt, s));
+      BD_TIMED(BD_TIME_ATTENTION, launch_attention(a, dt, s));
     }
     // S6: y = x + W_o a (in place; with the convolution W_o a goes to cz and the next
     // row norm adds Conv_1 of it)
@@ -781,7 +819,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
       p.args.out_f32 = conv ? rw.cz : rw.x;
       p.args.ld_out = H;
-      BD_TRY(launch_gemm(p, sc, s));
+      BD_TIMED(BD_TIME_WO, launch_gemm(p, sc, s));
     }
     // S7: m = rmsnorm(y); x = y + W_down(SiLU(W_gate m) * W_up m).  With the packed image
     // (fp16 MLP matrices) m and the SwiGLU product are fp16 operands, else bf16 pairs.
@@ -814,7 +852,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.out_act = rw.hmid;
       p.args.ld_act = cfg->ffn;
       p.args.act_lo = mlp16 ? 0 : static_cast<long long>(lo(cfg->ffn));
-      BD_TRY(launch_gemm(p, sc, s));
+      BD_TIMED(BD_TIME_GATE_UP, launch_gemm(p, sc, s));
     }
     {
       GemmPlan p = make_plan(cfg, rw.hmid, T, cfg->ffn);
@@ -824,7 +862,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
       p.args.out_f32 = conv ? rw.cz : rw.x;
       p.args.ld_out = H;
-      BD_TRY(launch_gemm(p, sc, s));
+      BD_TIMED(BD_TIME_DOWN, launch_gemm(p, sc, s));
     }
     if (conv) fin = ConvFinish{rw.cz, rw.cdelta_m, L.conv_base_m, gw};
     if (cfg->code_width > 0 && rw.br_bar && pk) {  // S8 + S9 in one launch (small blocks)
@@ -862,7 +900,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.p3_boxes = bp.p3_boxes;
       ba.sw_bytes = bp.sw_bytes;
       ba.eps = cfg->eps;
-      BD_TRY(launch_bridge(ba, bp, sms, s));
+      BD_TIMED(BD_TIME_BRIDGE, launch_bridge(ba, bp, sms, s));
     } else if (cfg->code_width > 0) {
       const int Rc = cfg->code_width, Mc = cfg->msg_width;
       // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
@@ -972,7 +1010,8 @@ bd_status bd_lm_head_argmax(const bd_config *cfg, const bd_weights *w, const flo
   p.args.epi = EPI_ARGMAX;
   p.args.amax_val = hw.amax_val;
   p.args.amax_idx = hw.amax_idx;
-  BD_TRY(launch_gemm(p, scratch_of(hw.g), s));
+  t_timing.next = 0;
+  BD_TIMED(BD_TIME_HEAD, launch_gemm(p, scratch_of(hw.g), s));
   BD_TRY(launch_argmax_reduce(hw.amax_val, hw.amax_idx, static_cast<int>(tiles_of(cfg->vocab, 128)),
                               rows, token_out, max_logit_out, s));
   return BD_OK;
@@ -1139,6 +1178,27 @@ bd_status bd_selftest_wait(const unsigned *flag, int limit_us, void *stream_) {
   return BD_OK;
 }
 
+bd_status bd_set_timing_events(int kind, void *const *begin, void *const *end, int n) {
+  if (kind == BD_TIME_NONE) {
+    t_timing = Timing();
+    return BD_OK;
+  }
+  if (kind < BD_TIME_QKV || kind > BD_TIME_HEAD) return fail(BD_ERR_INVALID_ARG, "unknown timing kind");
+  if (n < 1 || n > BD_TIMING_MAX || !begin || !end)
+    return fail(BD_ERR_INVALID_ARG, "timing events: n must be in 1..BD_TIMING_MAX with both arrays given");
+  for (int i = 0; i < n; ++i)
+    if (!begin[i] || !end[i]) return fail(BD_ERR_INVALID_ARG, "timing events: NULL event");
+  Timing t;
+  t.kind = kind;
+  t.n = n;
+  for (int i = 0; i < n; ++i) {
+    t.begin[i] = static_cast<cudaEvent_t>(begin[i]);
+    t.end[i] = static_cast<cudaEvent_t>(end[i]);
+  }
+  t_timing = t;
+  return BD_OK;
+}
+
 bd_status bd_sync_status(void *stream_) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return fail(BD_ERR_CUDA, std::string("stream: ") + cudaGetErrorString(e));
@@ -1148,7 +1208,10 @@ bd_status bd_sync_status(void *stream_) {
   if (word & DEVERR_BAD_INDEX)
     return fail(BD_ERR_INVALID_ARG, "a device-side index (token id, request or position) was out of range");
   if (word & DEVERR_RANGE)
-    return fail(BD_ERR_INVALID_ARG, "a weight packed as fp16 is beyond the fp16 range (|w| > 65504)");
+    return fail(BD_ERR_RANGE, "a weight packed as fp16 is beyond the fp16 range (|w| > 65504)");
+  if (word & DEVERR_F16)
+    return fail(BD_ERR_RANGE, "an activation stored as an fp16 operand was beyond the fp16 range "
+                              "(|x| > 65504) or not finite");
   return BD_OK;
 }
 

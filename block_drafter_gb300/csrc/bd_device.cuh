@@ -23,6 +23,13 @@ static __device__ unsigned g_error_word = 0;
     return v;                                                                \
   }
 
+// fp32 -> fp16 for an activation operand; a value beyond +-65504 (or not finite) would
+// become +-inf, so it sets DEVERR_F16 instead of passing silently (the store still happens).
+__device__ __forceinline__ bool f16_out_of_range(float x) { return !(fabsf(x) <= 65504.f); }
+__device__ __forceinline__ void flag_f16_range(bool bad) {
+  if (bad) atomicOr(&g_error_word, DEVERR_F16);
+}
+
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 

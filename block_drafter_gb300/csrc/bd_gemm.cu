@@ -17,6 +17,8 @@
 // Warp roles: warp 0 = TMA producer (one lane), warp 1 = TMEM owner and MMA issuer (one
 // lane), warps 2-5 = epilogue (128 threads, one accumulator row each).
 #include "bd_device.cuh"
+
+#include <type_traits>
 #include "bd_internal.h"
 
 #include <cstdio>
@@ -489,16 +491,19 @@ __device__ __forceinline__ void emit_rows(const GemmMaps &maps, const GemmArgs &
     if (r < 64) {
       T *hi = reinterpret_cast<T *>(sb);
       T *lo = hi + 16 * 64;
+      bool bad = false;
 #pragma unroll
       for (int jj = 0; jj < kCW; ++jj) {
         const int c = c0 + jj;
         const float g = v[jj];
         const float u = es.xbuf[r * kXStride + c];
         const float h = g / (1.0f + __expf(-g)) * u;
+        if constexpr (std::is_same<T, __half>::value) bad |= f16_out_of_range(h);
         const T hv = from_f<T>(h);
         hi[c * 64 + r] = hv;
         if (p.act_lo) lo[c * 64 + r] = from_f<T>(h - to_f<T>(hv));
       }
+      flag_f16_range(bad);
     }
   } else {
     float *f = reinterpret_cast<float *>(sb);

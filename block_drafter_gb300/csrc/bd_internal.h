@@ -13,7 +13,9 @@
 namespace bd {
 
 // Device error word flags (set by kernels, read and cleared by bd_sync_status()).
-enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u, DEVERR_RANGE = 4u };
+// DEVERR_RANGE: a weight beyond the fp16 range met the packed image's fp16 conversion;
+// DEVERR_F16: an activation beyond the fp16 range (or not finite) met an fp16 operand store.
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BAD_INDEX = 2u, DEVERR_RANGE = 4u, DEVERR_F16 = 8u };
 
 // ------------------------------------------------------------------ GEMM
 // D[tok, out] = X[tok, :] . W[out, :]  computed swap-AB on tcgen05: weight rows fill the
@@ -140,6 +142,8 @@ struct PackedLayout {
   size_t total;
 };
 PackedLayout packed_layout(const bd_config *c);
+// Empty when the configuration passes the checks every entry point applies.
+std::string validate_config(const bd_config *c);
 // In a bf16 config the packed image stores the MLP matrices (gate/up, down, and the MLP
 // branch's convolution delta) and the head as fp16: those products take fp16 activations
 // (one operand of 11 significant bits instead of a bf16 hi+lo pair), which halves their

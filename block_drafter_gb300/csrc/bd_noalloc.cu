@@ -12,7 +12,9 @@
 // counters that must start at zero are cleared by each call before its kernels run.
 // The host needs the array's device address, which cudaGetSymbolAddress provides; the
 // first call on a device looks it up (with that device current) and caches it, so that
-// first call should come before any stream capture.
+// first call should come before any stream capture.  The cached address belongs to the
+// device's context of that moment: after cudaDeviceReset on that device this entry point
+// must not be called again in the same process.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -80,13 +82,10 @@ extern "C" bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_we
                                                const float *hidden, int rows, int32_t *token_out,
                                                float *max_logit_out, void *stream_) {
   using namespace bd;
-  if (!cfg) return fail(BD_ERR_INVALID_ARG, "config is NULL");
-  if (cfg->dtype != BD_BF16 && cfg->dtype != BD_F32)
-    return fail(BD_ERR_INVALID_ARG, "dtype must be BD_BF16 or BD_F32");
-  const int elem = cfg->dtype == BD_BF16 ? 2 : 4;
-  if (cfg->hidden <= 0 || (static_cast<long long>(cfg->hidden) * elem) % 16 != 0)
-    return fail(BD_ERR_INVALID_ARG, "hidden must be > 0 and hidden*elem a multiple of 16 bytes");
-  if (cfg->vocab <= 0) return fail(BD_ERR_INVALID_ARG, "vocab must be > 0");
+  // the whole configuration is checked as every entry point checks it: the packed image's
+  // head offset depends on every layer's sizes
+  const std::string bad_cfg = validate_config(cfg);
+  if (!bad_cfg.empty()) return fail(BD_ERR_INVALID_ARG, bad_cfg);
   if (rows < 1 || static_cast<size_t>(rows) > kMaxRows || static_cast<size_t>(cfg->hidden) > kMaxHidden ||
       static_cast<size_t>(cfg->vocab) > BD_NOALLOC_MAX_VOCAB) {
     char b[200];

@@ -102,6 +102,8 @@ __global__ void rope_table_kernel(const int64_t *pos, int n, float2 *rope, int h
 
 template <typename T> __device__ __forceinline__ void store4(T *p, int i4, float4 v);
 template <> __device__ __forceinline__ void store4<__half>(__half *p, int i4, float4 v) {
+  flag_f16_range(f16_out_of_range(v.x) || f16_out_of_range(v.y) || f16_out_of_range(v.z) ||
+                 f16_out_of_range(v.w));
   __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t *>(&a);
@@ -345,8 +347,13 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   }
   if (sg.f16) {
     __half *dh = static_cast<__half *>(sg.dst) + o + d0;
+    bool bad = false;
 #pragma unroll
-    for (int e = 0; e < E; ++e) dh[e] = __float2half_rn(v[e]);
+    for (int e = 0; e < E; ++e) {
+      bad |= f16_out_of_range(v[e]);
+      dh[e] = __float2half_rn(v[e]);
+    }
+    flag_f16_range(bad);
     return;
   }
   T *dst = static_cast<T *>(sg.dst) + o + d0;
@@ -603,8 +610,10 @@ __global__ void rows_f16_kernel(const float *src, size_t n, __half *dst, ZeroSpa
   pdl_trigger();
   zero_span(z);
   for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < n;
-       t += static_cast<size_t>(gridDim.x) * blockDim.x)
+       t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    flag_f16_range(f16_out_of_range(src[t]));
     dst[t] = __float2half_rn(src[t]);
+  }
 }
 
 __global__ void split_rows_kernel(const float *src, size_t n, __nv_bfloat16 *dst, size_t lo_off,

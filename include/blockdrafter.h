@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define BD_ABI_VERSION 7
+#define BD_ABI_VERSION 8
 #define BD_MAX_LAYERS 16
 
 typedef enum {
@@ -45,7 +45,10 @@ typedef enum {
   BD_ERR_UNSUPPORTED = -2,     /* geometry the kernels do not implement (never a fallback) */
   BD_ERR_CUDA = -3,            /* a CUDA runtime/driver call failed                        */
   BD_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait gave up                       */
-  BD_ERR_WORKSPACE = -5        /* workspace too small or misaligned                        */
+  BD_ERR_WORKSPACE = -5,       /* workspace too small or misaligned                        */
+  BD_ERR_RANGE = -6            /* a value met an fp16 conversion beyond +-65504 (or not
+                                  finite): a weight while packing, or an activation on its
+                                  way into an fp16 tensor-core operand (bd_sync_status)     */
 } bd_status;
 
 typedef enum { BD_BF16 = 0, BD_F32 = 1 } bd_dtype;
@@ -146,9 +149,19 @@ size_t bd_packed_bytes(const bd_config *cfg);
  * caller-owned, >= bd_packed_bytes(cfg) bytes, 1024-byte aligned).  The image holds each
  * matrix as 128-row x 128-byte tiles, each tile contiguous and already in the 128-byte
  * swizzled order the tensor cores read from shared memory (the SwiGLU gate and up
- * matrices interleaved 64 rows each per tile); out-of-range rows/columns are zero.  It is
- * a pure permutation of the weights: results are identical with or without it.  Run it
+ * matrices interleaved 64 rows each per tile); out-of-range rows/columns are zero.  Run it
  * once after loading the weights, then set w->packed = packed.
+ *
+ * The image is not only a permutation.  In a bf16 config it stores the MLP matrices
+ * (W_gate, W_up, W_down, and with conv_group > 0 the MLP branch's W_delta) and the LM
+ * head as fp16, and the products that read them then take fp16 activations (see
+ * bd_draft_round and bd_lm_head_argmax); all other matrices stay bf16, bit for bit.  The
+ * conversion is exact for every bf16 value of magnitude 2^-14 .. 65504; smaller values
+ * become fp16 subnormals with an absolute error of at most 2^-25; a value beyond
+ * +-65504 makes the next bd_sync_status return BD_ERR_RANGE.  Results with and without
+ * the image therefore differ by these roundings and the activations' fp16 rounding
+ * (about 1e-3 of max|h| at the 27B geometry), not bit for bit.  In an fp32 config the
+ * image is a pure permutation.
  */
 bd_status bd_pack_weights(const bd_config *cfg, const bd_weights *w, void *packed,
                           size_t packed_bytes, void *stream);
@@ -207,10 +220,20 @@ typedef struct {
 
 /*
  * One masked-block draft forward (S3 .. S9 and the final norm) for B requests.
- * Numerics (bf16 config): weights and context K/V are used as stored; the residual
- * stream is fp32; every activation that feeds a tensor-core product (normed rows,
- * attention output, SwiGLU product, codes, messages, queries, softmax weights and the
- * block's own keys/values) enters as a bf16 hi+lo pair with fp32 accumulation.
+ * Numerics (bf16 config): the residual stream, norms, softmax statistics and every
+ * accumulator are fp32; context K/V are used as stored (bf16).
+ *   Without the packed image (w->packed NULL) the weights are used as stored and every
+ *   activation that feeds a tensor-core product (normed rows, attention output, SwiGLU
+ *   product, codes, messages, queries, softmax weights, the block's own keys/values)
+ *   enters as a bf16 hi+lo pair (about 16 significant bits).
+ *   With the packed image the MLP products read fp16 weights (see bd_pack_weights) and
+ *   take fp16 activations (the normed rows and the SwiGLU product, 11 significant bits);
+ *   the attention takes fp16 queries, softmax weights and block keys/values, and converts
+ *   its bf16 ring tiles to fp16 in shared memory (ring values beyond +-65504 saturate);
+ *   the other products (Q/K/V, W_o, the bridge's code read, gate/value maps and write)
+ *   keep bf16 weights and bf16 hi+lo activation pairs.  An activation beyond the fp16
+ *   range on its way into an fp16 operand is still stored (as +-inf) and makes the next
+ *   bd_sync_status return BD_ERR_RANGE.
  * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for
  * the injection after every layer when code_width > 0:
  *   row (b, 0) = embed(anchor_ids[b]) at position F_b; rows (b, i>=1) = embed(MASK) at
@@ -250,9 +273,12 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
 /*
  * Tied LM head with per-row argmax (S10).  [DFlash-notes], proposal head:
  *   logits = embed_head . hidden_r ;  token_out[r] = argmax_v logits[v]
- * Ties resolve to the lowest token id.  fp32 accumulation; in a bf16 config each hidden
- * row enters the tensor cores as a bf16 hi+lo pair (about 16 mantissa bits), the head
- * weights as stored.
+ * Ties resolve to the lowest token id.  fp32 accumulation.  In a bf16 config without
+ * the packed image each hidden row enters the tensor cores as a bf16 hi+lo pair (about
+ * 16 significant bits) against the bf16 head as stored; with the packed image the head
+ * is its fp16 copy (see bd_pack_weights) and each hidden row enters as fp16 (11
+ * significant bits; a value beyond +-65504 makes bd_sync_status return BD_ERR_RANGE).
+ * An fp32 config uses tf32 tensor-core products on the fp32 rows and head.
  *
  *   hidden         dev fp32 [rows, H] (e.g. bd_draft_round's head_in)
  *   rows           1 .. 8*15
@@ -361,7 +387,10 @@ bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float 
  * that must start at zero are cleared by every call), so calls that overlap on the GPU
  * -- on two streams or from two threads -- race and must be ordered by the caller.
  * The first call on a device looks up the array's device address (with that device
- * current) and caches it; make that first call before any stream capture.
+ * current) and caches it; make that first call before any stream capture.  The cached
+ * address belongs to the device's context of that moment: after cudaDeviceReset on that
+ * device, do not call this entry point again in the same process.
+ * The configuration is checked as bd_lm_head_argmax checks it (BD_ERR_INVALID_ARG).
  */
 #define BD_NOALLOC_MAX_ROWS 32
 #define BD_NOALLOC_MAX_HIDDEN 8192
@@ -370,6 +399,34 @@ bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float 
 bd_status bd_lm_head_argmax_noalloc(const bd_config *cfg, const bd_weights *w,
                                     const float *hidden, int rows, int32_t *token_out,
                                     float *max_logit_out, void *stream);
+
+/*
+ * Measurement hook (no counterpart in the papers): brackets single kernel launches with
+ * caller-created CUDA events (cudaEvent_t passed as void*, timing enabled), so that a
+ * benchmark can time one kernel of a round, also inside a captured graph.  While a kind
+ * is set on the calling thread, the i-th launch of that kind within each later
+ * bd_draft_round call (or bd_lm_head_argmax call, for BD_TIME_HEAD) is preceded by
+ * cudaEventRecord(begin[i]) and followed by cudaEventRecord(end[i]) on the call's
+ * stream, for i < n; further launches of the kind are not bracketed.  The events stay
+ * owned by the caller and must outlive every call (or graph replay) that records them.
+ * An event between two launches removes their programmatic overlap, so a bracketed
+ * round runs slightly slower than an unbracketed one.  kind BD_TIME_NONE clears the
+ * setting (begin, end and n are then ignored).
+ * Errors: BD_ERR_INVALID_ARG for an unknown kind, n outside 1..BD_TIMING_MAX or a NULL
+ * event.
+ */
+#define BD_TIMING_MAX 32
+typedef enum {
+  BD_TIME_NONE = 0,
+  BD_TIME_QKV = 1,        /* the Q/K/V product of each layer                    */
+  BD_TIME_ATTENTION = 2,  /* the block attention of each layer                  */
+  BD_TIME_WO = 3,         /* the output projection of each layer                */
+  BD_TIME_GATE_UP = 4,    /* the SwiGLU gate/up product of each layer           */
+  BD_TIME_DOWN = 5,       /* the down projection of each layer                  */
+  BD_TIME_BRIDGE = 6,     /* the one-launch DSpine bridge of each layer         */
+  BD_TIME_HEAD = 7        /* the LM-head product of bd_lm_head_argmax           */
+} bd_time_kind;
+bd_status bd_set_timing_events(int kind, void *const *begin, void *const *end, int n);
 
 /* Number of kernels this library has enqueued (all threads) since it was loaded.
  * Graph replays do not pass through the library and are not counted. */
@@ -388,7 +445,9 @@ const char *bd_last_error(void);
 
 /* Synchronises `stream`, then reads and clears the device error word.  Returns
  * BD_ERR_DEVICE_TIMEOUT if a bounded device wait gave up since the last check,
- * BD_ERR_CUDA if the stream reports an error, BD_OK otherwise. */
+ * BD_ERR_INVALID_ARG if a kernel met an out-of-range id or position, BD_ERR_RANGE if a
+ * value met an fp16 conversion beyond +-65504 (or was not finite), BD_ERR_CUDA if the
+ * stream reports an error, BD_OK otherwise. */
 bd_status bd_sync_status(void *stream);
 
 #ifdef __cplusplus

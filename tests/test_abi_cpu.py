@@ -185,6 +185,35 @@ def test_entry_points_reject_invalid_arguments_on_host(B):
     assert st == -1 and b"bridge" in L.bd_last_error()
 
 
+def test_noalloc_head_checks_the_whole_config_on_host(B):
+    """The no-allocation head applies the same configuration checks as the other entry
+    points (the packed image's head offset depends on every layer's sizes), then its own
+    size limits."""
+    L = B.lib()
+    c = cfg_of(bdsynth.TINY)
+    w = _fake_weights(B, c, c.n_layers)
+    for field, val, msg in (("n_layers", 99, b"n_layers"), ("head_dim", 96, b"head_dim"),
+                            ("ffn", 3, b"ffn"), ("n_target_layers", 0, b"n_target_layers"),
+                            ("mask_token_id", 5000, b"mask_token_id")):
+        bad = cfg_of(bdsynth.TINY, **{field: val})
+        st = L.bd_lm_head_argmax_noalloc(C.byref(bad), C.byref(w), 0x10000, 4, 0x10000, None, None)
+        assert st == -1 and msg in L.bd_last_error(), field
+    st = L.bd_lm_head_argmax_noalloc(C.byref(c), C.byref(w), 0x10000, 33, 0x10000, None, None)
+    assert st == -1 and b"rows <= 32" in L.bd_last_error()
+
+
+def test_timing_hook_checks_its_arguments_on_host(B):
+    L = B.lib()
+    ev = (C.c_void_p * 2)(0x1000, 0x2000)
+    null = (C.c_void_p * 2)(0x1000, None)
+    assert L.bd_set_timing_events(99, ev, ev, 2) == -1
+    assert L.bd_set_timing_events(4, ev, ev, 0) == -1
+    assert L.bd_set_timing_events(4, ev, ev, 33) == -1
+    assert L.bd_set_timing_events(4, ev, null, 2) == -1
+    assert L.bd_set_timing_events(4, None, ev, 2) == -1
+    assert L.bd_set_timing_events(0, None, None, 0) == 0
+
+
 def test_unsupported_geometry_is_an_error_not_a_fallback(B):
     L = B.lib()
     # bf16 with 8 query heads per KV head and W = 16 -> 128 query rows per KV head

@@ -84,3 +84,53 @@ def test_out_of_range_anchor_is_reported_without_a_fault(batch):
     again = case.run_gpu()
     assert torch.equal(again["layers"], good["layers"])
     assert torch.equal(again["tokens"], good["tokens"])
+
+
+def test_packed_weight_beyond_fp16_range_is_reported():
+    """The packed image stores the MLP matrices as fp16 in a bf16 config: a weight beyond
+    +-65504 cannot be represented, so packing flags it and bd_sync_status returns
+    BD_ERR_RANGE once (no fault); an in-range image afterwards reports nothing."""
+    from block_drafter_gb300 import binding as B
+    from block_drafter_gb300.session import DraftSession
+    geo = _SMALL.with_(batch=1, n_layers=1, windows=(64,))
+    w = bdsynth.make_weights(geo, seed=4, device="cuda")
+    B.sync_status()
+    w["layers"][0]["w_down"][7, 3] = 1.0e5        # bf16 holds it, fp16 does not
+    DraftSession(geo, w, mask_id=0, b_max=1, max_ctx_rows=16)
+    with pytest.raises(B.BdError) as err:
+        B.sync_status()
+    assert err.value.status == -6 and "65504" in str(err.value)
+    B.sync_status()
+    w["layers"][0]["w_down"][7, 3] = 0.5
+    DraftSession(geo, w, mask_id=0, b_max=1, max_ctx_rows=16)
+    B.sync_status()
+
+
+def test_fp16_activation_overflow_is_reported():
+    """With the packed image the SwiGLU product is stored as an fp16 operand of the down
+    projection.  Scaling one layer's gate and up matrices by 1000 (still in fp16 range)
+    pushes SiLU(g) * u far beyond 65504: the store would be +-inf, so the epilogue flags it
+    and bd_sync_status returns BD_ERR_RANGE; the same session with its weights restored
+    drafts cleanly again."""
+    import harness as Hn
+    from block_drafter_gb300 import binding as B
+    geo = _SMALL.with_(batch=1)
+    case = Hn.Case(geo, seed=12, max_ctx_rows=128)
+    case.fill_rings()
+    good = case.run_gpu()
+    lw = case.w_dev["layers"][0]
+    saved = (lw["w_gate"].clone(), lw["w_up"].clone())
+    lw["w_gate"].mul_(1000.0)
+    lw["w_up"].mul_(1000.0)
+    B.pack_weights(case.sess.cfg, case.sess.wstruct, case.sess.packed)
+    B.sync_status()                                # the scaled weights are in range
+    with pytest.raises(B.BdError) as err:
+        case.run_gpu()
+    assert err.value.status == -6 and "activation" in str(err.value)
+    B.sync_status()
+    lw["w_gate"].copy_(saved[0])
+    lw["w_up"].copy_(saved[1])
+    B.pack_weights(case.sess.cfg, case.sess.wstruct, case.sess.packed)
+    again = case.run_gpu()
+    assert torch.equal(again["layers"], good["layers"])
+    assert torch.equal(again["tokens"], good["tokens"])

@@ -45,6 +45,35 @@ def test_noalloc_head_matches_workspace_head_twice(B, dtype, H, V, rows):
         torch.testing.assert_close(mx, max_ref, rtol=2e-3, atol=2e-3)
 
 
+@pytest.mark.parametrize("big", [False, True])
+def test_noalloc_head_with_packed_image_matches_workspace_head_twice(B, big):
+    """A caller holding the packed weight image takes the fp16 head path (fp16 head rows,
+    fp16 hidden rows); both entry points must still agree on the same packed weights."""
+    import bdsynth
+    from block_drafter_gb300.session import DraftSession
+    if big:
+        geo = bdsynth.DSPINE27B_B1.with_(n_layers=1, windows=(2048,))
+        rows = 15
+    else:
+        geo = bdsynth.TINY.with_(dtype="bf16", hidden=512, vocab=4000, n_layers=1, windows=(0,))
+        rows = 9
+    wd = bdsynth.make_weights(geo, seed=3, device="cuda")
+    sess = DraftSession(geo, wd, mask_id=0, b_max=1, max_ctx_rows=16)
+    assert sess.wstruct.packed
+    g = torch.Generator().manual_seed(11 + rows)
+    tok_ref = torch.empty(rows, dtype=torch.int32, device="cuda")
+    max_ref = torch.empty(rows, dtype=torch.float32, device="cuda")
+    for call in range(2):
+        h = torch.randn(rows, geo.hidden, generator=g).cuda()
+        B.lm_head_argmax(sess.cfg, sess.wstruct, h, tok_ref, sess.workspace, max_ref)
+        tok = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
+        mx = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+        B.lm_head_argmax_noalloc(sess.cfg, sess.wstruct, h, tok, mx)
+        B.sync_status()
+        assert torch.equal(tok, tok_ref), (call, tok, tok_ref)
+        torch.testing.assert_close(mx, max_ref, rtol=2e-3, atol=2e-3)
+
+
 def test_noalloc_head_rejects_sizes_beyond_its_scratch(B):
     import bdsynth
     from block_drafter_gb300.session import config_of
@@ -56,3 +85,8 @@ def test_noalloc_head_rejects_sizes_beyond_its_scratch(B):
     tok = torch.empty(33, dtype=torch.int32, device="cuda")
     with pytest.raises(B.BdError, match="rows <= 32"):
         B.lm_head_argmax_noalloc(cfg, ws_struct, h, tok)
+    # a configuration the other entry points reject is rejected here too
+    bad = config_of(bdsynth.TINY.with_(hidden=256, vocab=1024, dtype="bf16"), 0)
+    bad.n_layers = 99
+    with pytest.raises(B.BdError, match="n_layers"):
+        B.lm_head_argmax_noalloc(bad, ws_struct, h[:4], tok[:4])

@@ -48,19 +48,26 @@ bd_status fail(bd_status s, const std::string &msg) {
     if (!_e.empty()) return fail(BD_ERR_CUDA, _e);         \
   } while (0)
 
-// Records the next begin event of `kind` (if that kind is being timed) on stream s.
+// Records event ev on stream s; inside stream capture as an external event node of the
+// graph (a plain record there would only mark a capture dependency).
+std::string record_timing_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e == cudaSuccess)
+    e = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                            : cudaEventRecord(ev, s);
+  return e == cudaSuccess ? std::string() : std::string("timing event: ") + cudaGetErrorString(e);
+}
+// Records the next begin / end event of `kind` (if that kind is being timed) on stream s.
 std::string timing_begin(int kind, cudaStream_t s) {
   Timing &t = t_timing;
   if (t.kind != kind || t.next >= t.n) return {};
-  // external: inside stream capture the record becomes an event node of the graph
-  const cudaError_t e = cudaEventRecordWithFlags(t.begin[t.next], s, cudaEventRecordExternal);
-  return e == cudaSuccess ? std::string() : std::string("cudaEventRecord: ") + cudaGetErrorString(e);
+  return record_timing_event(t.begin[t.next], s);
 }
 std::string timing_end(int kind, cudaStream_t s) {
   Timing &t = t_timing;
   if (t.kind != kind || t.next >= t.n) return {};
-  const cudaError_t e = cudaEventRecordWithFlags(t.end[t.next++], s, cudaEventRecordExternal);
-  return e == cudaSuccess ? std::string() : std::string("cudaEventRecord: ") + cudaGetErrorString(e);
+  return record_timing_event(t.end[t.next++], s);
 }
 // launch_expr bracketed by the timing events of `kind`
 #define BD_TIMED(kind, expr)              \

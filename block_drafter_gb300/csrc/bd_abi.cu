@@ -191,25 +191,16 @@ struct Carve {
 // When the context chunks are short (at most two 64-key blocks per split), the block's own
 // keys -- a separate hi+lo pass -- would double the last split's work and every split
 // waits for it in the merge: give them a split of their own.
-bool att_block_split(const bd_config *c, int l, int n_splits) {
-  if (n_splits < 2) return false;
-  const int cap = c->ring_capacity[l];
-  const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
-  const int blocks = (ctx + 63) / 64;
-  return (blocks + n_splits - 2) / (n_splits - 1) <= 2;
-}
-
+// Key splits of a layer's bf16 attention: one CTA per (split, KV head, request) and one
+// CTA per SM (the splits of a head merge inside the launch, so all of them must be
+// resident together), at most one split per 128-slot tile of the ring.
 int att_splits(const bd_config *c, int l, int B, int W, int sms) {
+  (void)W;
   const int cap = c->ring_capacity[l];
-  const int ctx = c->window[l] > 0 ? std::min(c->window[l] - 1, cap) : cap;
-  const int max_keys = ctx + W;
-  const int max_splits = (max_keys + 63) / 64;  // at least one 64-key block per split
-  // two attention CTAs fit per SM: fill 2 * SMs slots in a single wave (at B=1, 16 splits
-  // of two key blocks each ran 2 us slower than 33 of one: a block costs ~2.3 us of
-  // latency per CTA, more than the wider merge)
-  int s = (2 * sms) / (B * c->n_kv_heads);
+  const int tiles = (cap + attention_tile_keys() - 1) / attention_tile_keys();
+  int s = sms / (B * c->n_kv_heads);
   if (s < 1) s = 1;
-  return s < max_splits ? s : max_splits;
+  return s < tiles ? s : tiles;
 }
 int att_max_keys(const bd_config *c, int l, int W) {
   const int cap = c->ring_capacity[l];
@@ -644,6 +635,8 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const int G = cfg->n_q_heads / cfg->n_kv_heads;
   if (cfg->dtype == BD_BF16 && G * W > attention_rows_max())
     return fail(BD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*(n_masks+1) must be <= 64");
+  if (cfg->dtype == BD_BF16 && static_cast<long long>(B) * cfg->n_kv_heads > num_sms())
+    return fail(BD_ERR_UNSUPPORTED, "B * n_kv_heads must not exceed the number of SMs");
   for (int l = 0; l < cfg->n_layers; ++l)
     if (cfg->dtype == BD_F32 && att_max_keys(cfg, l, W) > 48 * 1024)
       return fail(BD_ERR_UNSUPPORTED, "fp32 attention supports at most 49152 keys per layer");
@@ -763,9 +756,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       h.W = W;
       h.eps = cfg->eps;
       h.rope = rw.rope;
-      const size_t qlo = split && !mlp16 ? static_cast<size_t>(T) * QD : 0;
-      const size_t klo = split && !mlp16 ? static_cast<size_t>(T) * KD : 0;
-      const int a16 = mlp16 ? 1 : 0;
+      // the attention takes the queries and the block's keys/values as bf16 hi+lo planes
+      const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
+      const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
+      const int a16 = 0;
       h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo, a16};
       h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo, a16};
       h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo, a16};
@@ -808,12 +802,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.cap = cfg->ring_capacity[l];
       a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
       a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
-      a.block_split = att_block_split(cfg, l, a.n_splits) ? 1 : 0;
       a.n_guard = n_pend > 0 ? kMaxPendPerReq : 0;
       a.max_keys = att_max_keys(cfg, l, W);
-      a.f16 = mlp16 ? 1 : 0;
-      a.q_lo = split && !mlp16 ? static_cast<size_t>(T) * QD : 0;
-      a.blk_lo = split && !mlp16 ? static_cast<size_t>(T) * KD : 0;
+      a.q_lo = split ? static_cast<size_t>(T) * QD : 0;
+      a.blk_lo = split ? static_cast<size_t>(T) * KD : 0;
       a.out_lo = lo(QD);
       BD_TIMED(BD_TIME_ATTENTION, launch_attention(a, dt, s));
     }

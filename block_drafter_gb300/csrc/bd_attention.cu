@@ -8,11 +8,26 @@
 // (F+i) - p < S for a local layer; every populated position for a full layer.  Block
 // key j is visible iff |j - i| < S (local) and, block-causal, j <= i.
 //
-// bf16 path: one CTA per (key split, KV head, request).  All G = Hq/Hkv query heads of
-// the KV head and all W rows (G*W <= 64 query rows) share each K/V tile, so the
-// windowed context is streamed once per KV head.  QK^T and PV run on mma.sync bf16
-// tensor-core instructions with an online (max-subtracted, base-2) softmax; each split
-// writes an unnormalised partial (O, m, l) and a combine kernel merges the splits.
+// bf16 path, on the 5th-generation tensor cores.  One CTA per (key split, KV head,
+// request); all G = Hq/Hkv query heads of the KV head and all W block rows (G*W <= 64
+// query rows) share every K/V tile, so the windowed context is streamed once per KV head.
+// Warp roles: warp 0 issues the TMA loads of 128-key K/V tiles (two-stage pipeline),
+// warp 1 issues the tcgen05 MMAs, warps 2-5 (one TMEM lane quarter each) run the softmax.
+//   S^T = K Q^T:  keys are the MMA's M side (128 TMEM lanes, one key per softmax thread);
+//                 the N side holds the query rows twice, as the bf16 hi and lo halves of
+//                 the fp32 queries, so one MMA gives both products and each thread adds
+//                 its two columns.
+//   O^T += V^T P^T: d is the M side, the N side holds the probabilities' bf16 hi and lo
+//                 halves (written by the softmax threads into shared memory, each key its
+//                 own row); the two halves are added once, at the end.
+// Keys are taken in ring-slot order (the ring holds rotated keys, so the order of keys
+// does not matter to the softmax): a tile is 128 consecutive slots, loaded by one 2-D TMA
+// box per 64-column half, and never wraps.  The softmax keeps a reference maximum per
+// query and rescales only when a tile exceeds it by more than 2^8 (the probabilities stay
+// below 256, well inside bf16); the exact maxima and the row sums are reduced across the
+// 128 threads through shared memory.  The block's own 16 keys (hi and lo rows)
+// form the last tile of the last split.  Splits write unnormalised partials (O, m, l) and
+// merge inside the launch.
 #include "bd_device.cuh"
 #include "bd_internal.h"
 #include "bd_kernels.h"
@@ -23,153 +38,52 @@ namespace bd {
 
 BD_DEFINE_ERROR_TAKER(take_error_word_att)
 
-constexpr int kAttRows = 64;     // query rows per CTA (4 warps x 16)
-constexpr int kAttKeys = 64;     // keys per pipeline block
-constexpr int kAttPad = 8;       // bf16 padding per smem row (bank-conflict-free ldmatrix)
+constexpr int kAttRows = 64;         // query rows per (request, KV head): G*W <= 64
+constexpr int kTileKeys = 128;       // context keys per tile (the S MMA's M side)
+constexpr int kAttThreads = 192;     // producer warp, MMA warp, four softmax warps
+constexpr int kSoftThreads = 128;
+constexpr int kBarSoft = 1;          // named barrier of the softmax warps
+constexpr int kBarVote = 2;          // their votes (barrier with an OR reduction)
+constexpr uint32_t kAtom = 16384;    // 128 rows x 128 bytes (64 bf16 of each row)
+// shared memory (offsets from the 1024-aligned base); every tile is [2 atoms][128 rows][128 B]
+constexpr uint32_t kOffQ = 0;                       // rows 0..63 hi, 64..127 lo queries
+constexpr uint32_t kOffK = 2 * kAtom;               // [2 stages] key tiles
+constexpr uint32_t kOffV = kOffK + 2 * 2 * kAtom;   // [2 stages] value tiles
+constexpr uint32_t kOffP = kOffV + 2 * 2 * kAtom;   // atom 0: hi probabilities, atom 1: lo
+constexpr uint32_t kOffRed = kOffP + 2 * kAtom;     // float m_ref[64], alpha[64], l[64]
+constexpr uint32_t kOffBar = kOffRed + 3 * 64 * 4;
+constexpr int kNumBars = 11;  // full[2], empty[2], sfull[2], sfree[2], pfull, pvdone, qready
+constexpr size_t kAttSmem = kOffBar + kNumBars * 8 + 16 + 1024;
+// TMEM columns: S^T double buffer at 0 and 128, O^T at 256
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
-                                          uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                             uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
-      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// 8 bf16 values (16 bytes of shared memory) rewritten in place as fp16, saturating at
-// +-65504 (exact for every bf16 value of magnitude 2^-14 .. 65504).
-__device__ __forceinline__ void bf16x8_to_f16_inplace(__nv_bfloat16 *p) {
-  uint4 v = *reinterpret_cast<const uint4 *>(p);
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-    f.x = fminf(fmaxf(f.x, -65504.f), 65504.f);
-    f.y = fminf(fmaxf(f.y, -65504.f), 65504.f);
-    const __half2 h = __floats2half2_rn(f.x, f.y);
-    w[i] = *reinterpret_cast<const uint32_t *>(&h);
-  }
-  *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-__device__ __forceinline__ uint32_t pack_f16(float x0, float x1) {
-  const __half2 h = __floats2half2_rn(x0, x1);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+struct AttMaps {
+  CUtensorMap ring_k, ring_v;  // [B*Hkv*cap rows, D], box 128 rows x 64
+  CUtensorMap blk_k, blk_v;    // [2*B*Hkv*W rows (hi plane, lo plane), D], box 16 rows x 64
+};
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-struct AttGeom {
-  long long F;
-  int p_lo, n_ctx, k_begin, k_end;
-};
-
-// Context keys [p_lo, F) of request b (the window's oldest visible position, clipped to
-// the ring's live interval) are split into chunks of whole 64-key blocks: one per split,
-// or one per split but the last when that split only takes the block's own keys.
-__device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b, int split) {
-  AttGeom g;
-  g.F = a.frontier[b];
-  long long lo = a.window > 0 ? g.F - a.window + 1 : 0;
-  if (g.F - a.cap > lo) lo = g.F - a.cap;  // the ring holds [F - cap, F)
-  if (lo < 0) lo = 0;
-  g.p_lo = static_cast<int>(lo);
-  g.n_ctx = g.F > lo ? static_cast<int>(g.F - lo) : 0;
-  const int cs = a.block_split ? a.n_splits - 1 : a.n_splits;  // splits with context keys
-  int chunk = (g.n_ctx + cs - 1) / cs;
-  chunk = (chunk + kAttKeys - 1) / kAttKeys * kAttKeys;
-  g.k_begin = min(g.n_ctx, split * chunk);
-  g.k_end = min(g.n_ctx, g.k_begin + chunk);
-  return g;
-}
-
-// Is context key k (0-based from p_lo) visible from block row i?
-__device__ __forceinline__ bool ctx_visible(const AttArgs &a, const AttGeom &g, int i, int k) {
-  if (k >= g.k_end) return false;
-  const long long p = g.p_lo + k;
-  return a.window <= 0 || (g.F + i) - p < a.window;
-}
-// Is block key j visible from block row i?
-__device__ __forceinline__ bool blk_visible(const AttArgs &a, int i, int j) {
-  if (j >= a.W) return false;
-  if (a.window > 0 && abs(j - i) >= a.window) return false;
-  return !a.causal || j <= i;
-}
-
-// hi/lo split of a probability pair for the bf16 A operand of P.V
-__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t *>(&h);
-  lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-
-// Online-softmax update of one warp's 16 rows for a tile of NT*8 keys (scores already
-// scaled to log2 units and masked with -inf); returns the probabilities in s.
-template <int NT>
-__device__ __forceinline__ void softmax_update(float (&s)[NT][4], float (&m_run)[2],
-                                               float (&l_run)[2], float (&alpha)[2]) {
-  float mx[2] = {-INFINITY, -INFINITY};
+// Column reduction of a [128 threads][64] value table through shared memory (the free
+// probability tile): element (row r, column q) sits at r*64 + (q ^ (r & 31)), so both the
+// row writes of a warp and the column reads of 32 threads touch 32 distinct banks.
+__device__ __forceinline__ void table_store(float *scr, int r, const float (&v)[64]) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-    mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-    const float m_new = fmaxf(m_run[hr], mx[hr]);
-    alpha[hr] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[hr] - m_new);
-    m_run[hr] = m_new;
+  for (int q = 0; q < 64; ++q) scr[r * 64 + (q ^ (r & 31))] = v[q];
+}
+template <bool MAX>
+__device__ __forceinline__ float table_column(const float *scr, int q) {
+  float acc = MAX ? -INFINITY : 0.f;
+#pragma unroll 8
+  for (int r = 0; r < 128; ++r) {
+    const float x = scr[r * 64 + (q ^ (r & 31))];
+    acc = MAX ? fmaxf(acc, x) : acc + x;
   }
-  float ls[2] = {0.f, 0.f};
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int hr = e >> 1;
-      const float pv = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m_run[hr]);
-      s[nt][e] = pv;
-      ls[hr] += pv;
-    }
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 1);
-    ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 2);
-    l_run[hr] = l_run[hr] * alpha[hr] + ls[hr];
-  }
+  return acc;
 }
 
 // Merge the splits of query rows r0 .. r1-1 of (request b, KV head h):
@@ -325,7 +239,7 @@ __device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int
         for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
         if (lane == 0) red[warp][D] = L;
       }
-      __syncthreads();
+      named_bar(kBarSoft, kSoftThreads);
       if (active && part == 0)
         for (int q = 1; q < P; ++q) {
 #pragma unroll
@@ -349,356 +263,489 @@ __device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int
   }
 }
 
-// bf16 tensor-core path.  Q and the softmax probabilities P enter the MMAs as hi+lo bf16
-// pairs (fp32 accumulate), so their rounding does not reach the output; the ring's K/V
-// are exact bf16 data.  The block's own keys/values (produced this round, hi+lo) are
-// processed by the last split in a separate 16-key pass.
-// F16: Q, P and the block's keys/values are single fp16 operands (11 significant bits) and
-// each ring tile is rewritten as fp16 in shared memory once it lands (exact within fp16's
-// range): half the MMAs of the hi+lo form.
-template <int D, bool F16>
-__global__ void __launch_bounds__(128, 2) attention_bf16_kernel(const __grid_constant__ AttArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  constexpr int RS = D + kAttPad;  // smem row stride (elements)
-  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [2][64][RS] hi, lo
-  __nv_bfloat16 *sK = sQ + 2 * kAttRows * RS;                          // [2][64][RS]
-  __nv_bfloat16 *sV = sK + 2 * kAttKeys * RS;                          // [2][64][RS]
+// Position of ring slot s of a request at frontier F (the ring holds [F - cap, F) when
+// F >= cap, else positions 0..F-1 at their own slots).
+__device__ __forceinline__ long long slot_position(long long F, int cap, int s) {
+  if (F < cap) return s;
+  const long long base = F - cap;
+  long long d = (static_cast<long long>(s) - base) % cap;
+  if (d < 0) d += cap;
+  return base + d;
+}
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const int R = G * a.W;
-  // The frontier is an input of the round and the ring holds context written before it,
-  // except the positions >= F - n_guard that this round's catch-up may store: a first
-  // context block entirely older than that is fetched before waiting for the previous
-  // kernel (the head post-processing, which writes Q and the block's keys/values).
-  const AttGeom g = att_geom(a, b, split);
-  const bool do_block = split == a.n_splits - 1;
-
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *ring_k = static_cast<const __nv_bfloat16 *>(a.ring_k);
-  const __nv_bfloat16 *ring_v = static_cast<const __nv_bfloat16 *>(a.ring_v);
-  const __nv_bfloat16 *blk_k = static_cast<const __nv_bfloat16 *>(a.blk_k);
-  const __nv_bfloat16 *blk_v = static_cast<const __nv_bfloat16 *>(a.blk_v);
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-
-  // Each thread copies chunk ch of the rows r0, r0 + rstep, ...; the ring slot of a row
-  // advances with it (one modulo per tile, then wrap-around by subtraction).
-  const size_t ring_head = (static_cast<size_t>(b) * a.n_kv_heads + h) * static_cast<size_t>(a.cap);
-  auto load_kv = [&](int buf, int k0) {
-    constexpr int rstep = 128 / CPR;
-    const int ch = tid % CPR, r0 = tid / CPR;
-    int slot = static_cast<int>((static_cast<long long>(g.p_lo) + k0 + r0) % a.cap);
-    for (int kr = r0; kr < kAttKeys; kr += rstep) {
-      const bool valid = k0 + kr < g.k_end;
-      const size_t off = valid ? (ring_head + slot) * D : 0;
-      cp_async16(smem_u32(sK + (buf * kAttKeys + kr) * RS + ch * 8), ring_k + off + ch * 8, valid);
-      cp_async16(smem_u32(sV + (buf * kAttKeys + kr) * RS + ch * 8), ring_v + off + ch * 8, valid);
-      slot += rstep;
-      while (slot >= a.cap) slot -= a.cap;
-    }
-  };
-  // Block keys/values [Kh; Kl; Vh; Vl] (16 rows each, rows >= W zero) go into the K
-  // buffer the context loop leaves free after its last block (buffer n_blocks & 1); they
-  // are loaded while that last block is processed.
-  auto load_block = [&](int buf) {  // F16: [K; V], 16 rows each
-    __nv_bfloat16 *dstb = sK + buf * kAttKeys * RS;
-    for (int c = tid; c < (F16 ? 2 : 4) * 16 * CPR; c += 128) {
-      const int part = c / (16 * CPR), cc = c % (16 * CPR);
-      const int j = cc / CPR, ch = cc % CPR;
-      const bool valid = j < a.W;
-      const __nv_bfloat16 *base = F16 ? (part == 0 ? blk_k : blk_v)
-                                      : (part < 2 ? blk_k : blk_v) + ((part & 1) ? a.blk_lo : 0);
-      const __nv_bfloat16 *src =
-          base + ((static_cast<size_t>(b) * a.n_kv_heads + h) * a.W + (valid ? j : 0)) * D + ch * 8;
-      cp_async16(smem_u32(dstb + (part * 16 + j) * RS + ch * 8), src, valid);
-    }
-  };
-
-  // F16: the ring chunks this thread loaded into buffer `buf`, rewritten as fp16 (called
-  // after its copies have landed and before the barrier that publishes the tile)
-  auto convert_kv = [&](int buf) {
-    for (int c = tid; c < kAttKeys * CPR; c += 128) {
-      const int kr = c / CPR, ch = c % CPR;
-      bf16x8_to_f16_inplace(sK + (buf * kAttKeys + kr) * RS + ch * 8);
-      bf16x8_to_f16_inplace(sV + (buf * kAttKeys + kr) * RS + ch * 8);
-    }
-  };
-
-  float o[D / 8][4];
+// ------------------------------------------------------------------ producer (one thread)
+template <int D>
+__device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm, uint64_t *full,
+                             uint64_t *empty, int b, int g, long long F, int t_begin, int n_ctx,
+                             int nt, volatile int *sabort, int &issued) {
+  constexpr int NB = D / 64;  // 64-column boxes per row
+  const uint64_t pol_ring = policy_evict_first();
+  const int cap = a.cap;
+  const int row0 = (b * a.n_kv_heads + g) * cap;
+  auto issue = [&](int t) {
+    const int st = t & 1;
+    uint64_t *bar = &full[st];
+    uint8_t *dk = sm + kOffK + st * 2 * kAtom;
+    uint8_t *dv = sm + kOffV + st * 2 * kAtom;
+    if (t < n_ctx) {
+      const int s0 = (t_begin + t) * kTileKeys;
+      mbar_arrive_expect_tx(bar, 2u * NB * kAtom);
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  const float sl2 = 1.4426950408889634f * rsqrtf(static_cast<float>(D));  // log2(e)/sqrt(D)
-
-  const int g4 = lane >> 2, t4 = lane & 3;
-  const int rowA = warp * 16 + g4, rowB = rowA + 8;
-  const int iA = rowA % a.W, iB = rowB % a.W;
-  const bool rvA = rowA < R, rvB = rowB < R;
-
-  const int n_blocks = g.k_end > g.k_begin ? (g.k_end - g.k_begin + kAttKeys - 1) / kAttKeys : 0;
-  const bool early = n_blocks > 0 && g.p_lo + g.k_begin + kAttKeys <= g.F - a.n_guard;
-  if (early) {
-    load_kv(0, g.k_begin);
-    cp_async_commit();
-  }
+      for (int kb = 0; kb < NB; ++kb) {
+        tma_load_2d(dk + kb * kAtom, &maps.ring_k, bar, kb * 64, row0 + s0, pol_ring);
+        tma_load_2d(dv + kb * kAtom, &maps.ring_v, bar, kb * 64, row0 + s0, pol_ring);
+      }
+    } else {  // the block's keys/values: hi rows to tile rows 0..15, lo rows to 16..31
+      const int brow = (b * a.n_kv_heads + g) * a.W;
+      const int lo_row = a.B * a.n_kv_heads * a.W;
+      const uint64_t pol = policy_evict_last();
+      mbar_arrive_expect_tx(bar, 4u * NB * 16 * 128);
+#pragma unroll
+      for (int kb = 0; kb < NB; ++kb) {
+        tma_load_2d(dk + kb * kAtom, &maps.blk_k, bar, kb * 64, brow, pol);
+        tma_load_2d(dk + kb * kAtom + 16 * 128, &maps.blk_k, bar, kb * 64, lo_row + brow, pol);
+        tma_load_2d(dv + kb * kAtom, &maps.blk_v, bar, kb * 64, brow, pol);
+        tma_load_2d(dv + kb * kAtom + 16 * 128, &maps.blk_v, bar, kb * 64, lo_row + brow, pol);
+      }
+    }
+    issued = t + 1;
+  };
+  // The ring holds context written before this round, except the positions >= F - n_guard
+  // that this round's catch-up may store (the previous kernel): a first tile without them
+  // is fetched before waiting for the previous kernel.
+  auto safe = [&](int t) {
+    if (t >= n_ctx) return false;
+    const int s0 = (t_begin + t) * kTileKeys;
+    for (int j = 0; j < a.n_guard; ++j) {
+      const long long p = F - 1 - j;
+      if (p < 0) break;
+      const int slot = static_cast<int>(p % cap);
+      if (slot >= s0 && slot < s0 + kTileKeys) return false;
+    }
+    return true;
+  };
+  int t = 0;
+  if (nt > 0 && safe(0)) issue(t++);
   pdl_wait();
-  pdl_trigger();
-  // Q tiles: row rr = g_head * W + i  <-  q[(b*W + i), (h*G + g_head)*D + d]
-  for (int c = tid; c < (F16 ? 1 : 2) * kAttRows * CPR; c += 128) {
-    const int part = c / (kAttRows * CPR), cc = c % (kAttRows * CPR);
-    const int rr = cc / CPR, ch = cc % CPR;
-    const bool valid = rr < R;
-    const int gh = valid ? rr / a.W : 0, i = valid ? rr % a.W : 0;
-    const __nv_bfloat16 *src = q + (part ? a.q_lo : 0) +
-                               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
-                               (h * G + gh) * D + ch * 8;
-    cp_async16(smem_u32(sQ + (part * kAttRows + rr) * RS + ch * 8), src, valid);
+  for (; t < nt; ++t) {
+    if (t >= 2 && (*sabort || !mbar_wait(&empty[t & 1], ((t >> 1) - 1) & 1))) {
+      *sabort = 1;
+      return;
+    }
+    issue(t);
   }
-  if (n_blocks > 0 && !early) load_kv(0, g.k_begin);
-  else if (n_blocks == 0 && do_block) load_block(0);
-  cp_async_commit();
-  // the first context position every block row can see: keys from here on need no mask
-  const long long p_all = a.window > 0 ? g.F + a.W - a.window : LLONG_MIN;
-  cp_async_wait<0>();
-  if (F16 && n_blocks > 0) convert_kv(0);
-  __syncthreads();
+}
 
-  // A fragments of Q (hi or lo) for k-step ks
-  auto q_frag = [&](int part, int ks, uint32_t (&f)[4]) {
-    const int mi = lane >> 3;
-    const int row = warp * 16 + (mi & 1) * 8 + (lane & 7);
-    const int col = ks * 16 + (mi >> 1) * 8;
-    ldsm_x4(smem_u32(sQ + (part * kAttRows + row) * RS + col), f[0], f[1], f[2], f[3]);
+// ------------------------------------------------------------------ MMA issuer (one thread)
+template <int D>
+__device__ void att_mma(uint8_t *sm, uint64_t *full, uint64_t *empty, uint64_t *sfull,
+                        uint64_t *sfree, uint64_t *pfull, uint64_t *pvdone, uint64_t *qready,
+                        uint32_t tmem, int n_ctx, int nt, volatile int *sabort) {
+  const uint32_t idesc_s = umma_idesc(1, 128, 128);                           // both K-major
+  const uint32_t idesc_o = umma_idesc(1, 128, 128) | (1u << 15) | (1u << 16);  // both MN-major
+  if (!mbar_wait(qready, 0)) {
+    *sabort = 1;
+    return;
+  }
+  tc_fence_after();
+  const uint32_t q_base = smem_u32(sm + kOffQ);
+  const uint32_t p_base = smem_u32(sm + kOffP);
+  auto pv = [&](int u) -> bool {
+    if (*sabort || !mbar_wait(pfull, u & 1)) return false;
+    tc_fence_after();
+    const uint32_t v_base = smem_u32(sm + kOffV + (u & 1) * 2 * kAtom);
+    const int nk = u < n_ctx ? kTileKeys / 16 : 2;  // the block tile has 32 key rows
+    for (int kk = 0; kk < nk; ++kk)
+      umma_bf16(tmem + kTmemO, umma_desc_sw128_mn(v_base + kk * 2048, kAtom, 1024),
+                umma_desc_sw128_mn(p_base + kk * 2048, kAtom, 1024), idesc_o,
+                (u > 0 || kk > 0) ? 1u : 0u);
+    umma_commit(&empty[u & 1]);  // the K/V stage is free
+    umma_commit(pvdone);         // the probabilities are consumed, O^T is up to date
+    return true;
   };
-
-  for (int blk = 0; blk < n_blocks; ++blk) {
-    const int buf = blk & 1;
-    const int k0 = g.k_begin + blk * kAttKeys;
-    if (blk + 1 < n_blocks) load_kv(buf ^ 1, k0 + kAttKeys);
-    else if (do_block) load_block(buf ^ 1);
-    cp_async_commit();
-
-    // S = (Qh + Ql) K^T for 16 rows x 64 keys
-    float s[kAttKeys / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < kAttKeys / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t qh[4], ql[4];
-      q_frag(0, ks, qh);
-      if (!F16) q_frag(1, ks, ql);
-#pragma unroll
-      for (int nt = 0; nt < kAttKeys / 8; nt += 2) {
-        const int mi = lane >> 3;
-        const int key = (nt + (mi >> 1)) * 8 + (lane & 7);
-        const int col = ks * 16 + (mi & 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(sK + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        if constexpr (F16) {
-          mma16816_f16(s[nt], qh, b0, b1);
-          mma16816_f16(s[nt + 1], qh, b2, b3);
-        } else {
-          mma16816(s[nt], qh, b0, b1);
-          mma16816(s[nt + 1], qh, b2, b3);
-          mma16816(s[nt], ql, b0, b1);
-          mma16816(s[nt + 1], ql, b2, b3);
-        }
-      }
+  for (int t = 0; t < nt; ++t) {
+    const int st = t & 1;
+    if (*sabort || !mbar_wait(&full[st], (t >> 1) & 1) ||
+        (t >= 2 && !mbar_wait(&sfree[st], ((t >> 1) - 1) & 1))) {
+      *sabort = 1;
+      return;
     }
-    if (k0 + kAttKeys <= g.k_end && g.p_lo + k0 >= p_all) {  // every key visible to every row
+    tc_fence_after();
+    const uint32_t k_base = smem_u32(sm + kOffK + st * 2 * kAtom);
 #pragma unroll
-      for (int nt = 0; nt < kAttKeys / 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[nt][e] *= sl2;
-    } else {
-#pragma unroll
-      for (int nt = 0; nt < kAttKeys / 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = k0 + nt * 8 + 2 * t4 + (e & 1);
-          const bool top = e < 2;
-          const bool vis = (top ? rvA : rvB) && ctx_visible(a, g, top ? iA : iB, k);
-          s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
-        }
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+      umma_bf16(tmem + st * 128, umma_desc_sw128(k_base + off), umma_desc_sw128(q_base + off),
+                idesc_s, kk > 0 ? 1u : 0u);
     }
-    float alpha[2];
-    softmax_update<kAttKeys / 8>(s, m_run, l_run, alpha);
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
-    }
-    // O += (Ph + Pl) V
-#pragma unroll
-    for (int kk = 0; kk < kAttKeys / 16; ++kk) {
-      uint32_t ph[4], pl[4];
-      if constexpr (F16) {
-        ph[0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
-        ph[1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-        ph[2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        ph[3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-      } else {
-        split_pack(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-        split_pack(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-        split_pack(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-        split_pack(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-      }
-#pragma unroll
-      for (int nd = 0; nd < D / 8; nd += 2) {
-        const int mi = lane >> 3;
-        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
-        const int col = (nd + (mi >> 1)) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(sV + (buf * kAttKeys + key) * RS + col), b0, b1, b2, b3);
-        if constexpr (F16) {
-          mma16816_f16(o[nd], ph, b0, b1);
-          mma16816_f16(o[nd + 1], ph, b2, b3);
-        } else {
-          mma16816(o[nd], ph, b0, b1);
-          mma16816(o[nd + 1], ph, b2, b3);
-          mma16816(o[nd], pl, b0, b1);
-          mma16816(o[nd + 1], pl, b2, b3);
-        }
-      }
-    }
-    cp_async_wait<0>();
-    if (F16 && blk + 1 < n_blocks) convert_kv(buf ^ 1);
-    __syncthreads();
-  }
-
-  if (do_block) {
-    if (n_blocks == 0) {  // the block tile was loaded with Q; nothing else is in flight
-      cp_async_wait<0>();
-      __syncthreads();
-    }
-    // [Kh; Kl; Vh; Vl] (F16: [K; V]), 16 rows each
-    const __nv_bfloat16 *sB = sK + (n_blocks & 1) * kAttKeys * RS;
-    constexpr int kV = F16 ? 1 : 2;  // first V part
-    // S = Qh Kh + Ql Kh + Qh Kl over the (up to) 16 block keys (F16: Q K)
-    float s[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t qh[4], ql[4];
-      q_frag(0, ks, qh);
-      const int mi = lane >> 3;
-      const int key = (mi >> 1) * 8 + (lane & 7);
-      const int col = ks * 16 + (mi & 1) * 8;
-      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-      ldsm_x4(smem_u32(sB + (0 * 16 + key) * RS + col), h0, h1, h2, h3);
-      if constexpr (F16) {
-        mma16816_f16(s[0], qh, h0, h1);
-        mma16816_f16(s[1], qh, h2, h3);
-      } else {
-        q_frag(1, ks, ql);
-        ldsm_x4(smem_u32(sB + (1 * 16 + key) * RS + col), l0, l1, l2, l3);
-        mma16816(s[0], qh, h0, h1);
-        mma16816(s[1], qh, h2, h3);
-        mma16816(s[0], ql, h0, h1);
-        mma16816(s[1], ql, h2, h3);
-        mma16816(s[0], qh, l0, l1);
-        mma16816(s[1], qh, l2, l3);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = nt * 8 + 2 * t4 + (e & 1);
-        const bool top = e < 2;
-        const bool vis = (top ? rvA : rvB) && blk_visible(a, top ? iA : iB, j);
-        s[nt][e] = vis ? s[nt][e] * sl2 : -INFINITY;
-      }
-    float alpha[2];
-    softmax_update<2>(s, m_run, l_run, alpha);
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
-    }
-    uint32_t ph[4], pl[4];
-    if constexpr (F16) {
-      ph[0] = pack_f16(s[0][0], s[0][1]);
-      ph[1] = pack_f16(s[0][2], s[0][3]);
-      ph[2] = pack_f16(s[1][0], s[1][1]);
-      ph[3] = pack_f16(s[1][2], s[1][3]);
-    } else {
-      split_pack(s[0][0], s[0][1], ph[0], pl[0]);
-      split_pack(s[0][2], s[0][3], ph[1], pl[1]);
-      split_pack(s[1][0], s[1][1], ph[2], pl[2]);
-      split_pack(s[1][2], s[1][3], ph[3], pl[3]);
-    }
-#pragma unroll
-    for (int nd = 0; nd < D / 8; nd += 2) {
-      const int mi = lane >> 3;
-      const int key = (mi & 1) * 8 + (lane & 7);
-      const int col = (nd + (mi >> 1)) * 8;
-      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-      ldsm_x4_t(smem_u32(sB + (kV * 16 + key) * RS + col), h0, h1, h2, h3);
-      if constexpr (F16) {
-        mma16816_f16(o[nd], ph, h0, h1);
-        mma16816_f16(o[nd + 1], ph, h2, h3);
-      } else {
-        ldsm_x4_t(smem_u32(sB + (3 * 16 + key) * RS + col), l0, l1, l2, l3);
-        mma16816(o[nd], ph, h0, h1);
-        mma16816(o[nd + 1], ph, h2, h3);
-        mma16816(o[nd], pl, h0, h1);
-        mma16816(o[nd + 1], pl, h2, h3);
-        mma16816(o[nd], ph, l0, l1);
-        mma16816(o[nd + 1], ph, l2, l3);
-      }
+    umma_commit(&sfull[st]);
+    if (t >= 1 && !pv(t - 1)) {  // the previous tile's P.V, behind this tile's scores
+      *sabort = 1;
+      return;
     }
   }
+  if (nt > 0 && !pv(nt - 1)) *sabort = 1;
+}
 
-  // ---- partial outputs
-  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
-  float *po = a.part_o + (bh * a.n_splits + split) * kAttRows * D;
-  float2 *pml = a.part_ml + (bh * a.n_splits + split) * kAttRows;
+// Loads columns [c0, c0+32) and [c0+64, c0+96) of this thread's TMEM lane and returns
+// their sums (the hi and lo halves of one product) in v[j0 .. j0+31].
+template <int J0>
+__device__ __forceinline__ void tmem_pair_sum(uint32_t taddr, float (&v)[64]) {
+  uint32_t h[32], l[32];
+  tmem_ld32_nowait(taddr + J0, h);
+  tmem_ld32_nowait(taddr + 64 + J0, l);
+  tmem_ld_wait();
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    const int col = n * 8 + 2 * t4;
-    *reinterpret_cast<float2 *>(po + rowA * D + col) = make_float2(o[n][0], o[n][1]);
-    *reinterpret_cast<float2 *>(po + rowB * D + col) = make_float2(o[n][2], o[n][3]);
-  }
-  if (t4 == 0) {
-    pml[rowA] = make_float2(m_run[0], l_run[0]);
-    pml[rowB] = make_float2(m_run[1], l_run[1]);
-  }
+  for (int j = 0; j < 32; ++j) v[J0 + j] = __uint_as_float(h[j]) + __uint_as_float(l[j]);
+}
 
-  // ---- merge the splits in this launch: every split of (b, h) counts itself once its
-  // partial is stored, waits (bounded) for the others, then merges its share of the rows.
-  // A launch has at most two CTAs per SM and never more than two per SM of the GPU, so all
-  // splits are resident together; each stores its partial before it waits.
-  __shared__ int s_abort;
-  unsigned *arrived = a.counters + bh;
-  unsigned *done = a.counters + static_cast<size_t>(a.B) * a.n_kv_heads + bh;
-  __threadfence();
-  __syncthreads();
+// ------------------------------------------------------------------ kernel
+template <int D>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    attention_tc_kernel(const __grid_constant__ AttMaps maps, const __grid_constant__ AttArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *m_ref = reinterpret_cast<float *>(sm + kOffRed);  // per query: reference max (log2 units)
+  float *alpha = m_ref + 64, *l_fin = alpha + 64;          // rescale factors, row sums
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint64_t *full = bars, *empty = bars + 2, *sfull = bars + 4, *sfree = bars + 6;
+  uint64_t *pfull = bars + 8, *pvdone = bars + 9, *qready = bars + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+  volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.n_q_heads / a.n_kv_heads, W = a.W, R = G * W;
+  // the frontier is an input of the round, readable before the dependency wait
+  const long long F = a.frontier[b];
+  const int cap = a.cap;
+  const int n_slots = F < cap ? static_cast<int>(F > 0 ? F : 0) : cap;
+  const int n_tiles = (n_slots + kTileKeys - 1) / kTileKeys;
+  const int per = (n_tiles + a.n_splits - 1) / a.n_splits;
+  const int t_begin = min(n_tiles, split * per);
+  const int n_ctx = min(n_tiles, t_begin + per) - t_begin;
+  const bool do_block = split == a.n_splits - 1;
+  const int nt = n_ctx + (do_block ? 1 : 0);
+
   if (tid == 0) {
-    atomicAdd(arrived, 1u);
-    s_abort = wait_count(arrived, static_cast<unsigned>(a.n_splits), kWaitLimitNs, 0) ? 0 : 1;
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], 1);
+    mbar_init(&empty[1], 1);
+    mbar_init(&sfull[0], 1);
+    mbar_init(&sfull[1], 1);
+    mbar_init(&sfree[0], kSoftThreads);
+    mbar_init(&sfree[1], kSoftThreads);
+    mbar_init(pfull, kSoftThreads);
+    mbar_init(pvdone, 1);
+    mbar_init(qready, kSoftThreads);
+    *sabort = 0;
+    fence_barrier_init();
   }
-  __syncthreads();
-  if (s_abort) return;
-  const int rp = (R + a.n_splits - 1) / a.n_splits;
-  __shared__ float red[4][D + 4];
-  if (a.n_splits <= kFewSplits)
-    combine_rows_few<__nv_bfloat16, D, kFewSplits, 2>(a, b, h, min(R, split * rp),
-                                                      min(R, (split + 1) * rp), warp, lane);
-  else
-    combine_rows<__nv_bfloat16, D>(a, b, h, min(R, split * rp), min(R, (split + 1) * rp), warp, lane,
-                                   red);
-  __syncthreads();
-  if (tid == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
-    *arrived = 0u;  // every split is past its wait: ready for the next launch
-    *done = 0u;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.ring_k);
+    tma_prefetch_desc(&maps.ring_v);
+    tma_prefetch_desc(&maps.blk_k);
+    tma_prefetch_desc(&maps.blk_v);
   }
+  if (warp == 1) {  // TMEM before the trigger: a dependent kernel cannot take it first
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) att_producer<D>(maps, a, sm, full, empty, b, g, F, t_begin, n_ctx, nt, sabort, issued);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) att_mma<D>(sm, full, empty, sfull, sfree, pfull, pvdone, qready, tmem, n_ctx, nt, sabort);
+    __syncwarp();
+  } else {
+    const int qd = warp & 3;           // TMEM lane quarter of this warp
+    const int kr = qd * 32 + lane;     // S^T lane = key row of a tile; O^T lane = output dim
+    const int st_id = tid - 64;        // 0..127 among the softmax threads
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    pdl_wait();
+    // Query tile: row n = plane*64 + r, r = head_in_group * W + i, plane 0 = hi, 1 = lo
+    {
+      const int n = st_id, plane = n >> 6, r = n & 63;
+      const bool ok = r < R;
+      const int hh = ok ? r / W : 0, i = ok ? r % W : 0;
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          static_cast<const __nv_bfloat16 *>(a.q) + (plane ? a.q_lo : 0) +
+          (static_cast<size_t>(b) * W + i) * a.n_q_heads * D + static_cast<size_t>(g * G + hh) * D);
+      uint4 v[D / 8];
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) v[ch] = ok ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch)
+        *reinterpret_cast<uint4 *>(sm + kOffQ + (ch >> 3) * kAtom + n * 128 +
+                                   (((ch & 7) ^ (n & 7)) << 4)) = v[ch];
+    }
+    if (st_id < 64) m_ref[st_id] = -INFINITY;
+    fence_proxy_async_shared();
+    mbar_arrive(qready);
+    named_bar(kBarSoft, kSoftThreads);
+
+    const float sl2 = 1.4426950408889634f * rsqrtf(static_cast<float>(D));  // log2(e)/sqrt(D)
+    float lsum[64];
+#pragma unroll
+    for (int q = 0; q < 64; ++q) lsum[q] = 0.f;
+    bool abort = false;
+    for (int t = 0; t < nt && !abort; ++t) {
+      const int sb = t & 1;
+      bool ok = !*sabort && mbar_wait(&sfull[sb], (t >> 1) & 1);
+      if (named_bar_or(kBarVote, kSoftThreads, !ok)) {
+        abort = true;
+        break;
+      }
+      tc_fence_after();
+      float s[64];
+      tmem_pair_sum<0>(tmem + lane_off + sb * 128, s);
+      tmem_pair_sum<32>(tmem + lane_off + sb * 128, s);
+      tc_fence_before();
+      mbar_arrive(&sfree[sb]);  // the S buffer may take the tile after next
+      const bool blk = t >= n_ctx;
+      if (blk && qd == 0) {  // add the lo key rows (lanes 16..31) to their hi rows
+#pragma unroll
+        for (int q = 0; q < 64; ++q) s[q] += __shfl_down_sync(0xffffffffu, s[q], 16);
+      }
+      // visibility: context key at position p is seen by rows i <= i_max; block key kr by
+      // rows i with the block rule
+      int i_max = -1;
+      if (!blk) {
+        const int slot = (t_begin + t) * kTileKeys + kr;
+        if (slot < n_slots) {
+          const long long p = slot_position(F, cap, slot);
+          if (a.window > 0) {
+            const long long m = p - (F - a.window + 1);
+            i_max = m < 0 ? -1 : (m > W ? W : static_cast<int>(m));
+          } else {
+            i_max = W;
+          }
+        }
+      }
+      bool need = false;
+      {
+        int i = 0;
+#pragma unroll
+        for (int q = 0; q < 64; ++q) {
+          bool vis;
+          if (!blk)
+            vis = q < R && i <= i_max;
+          else
+            vis = q < R && kr < W && qd == 0 && (!a.causal || kr <= i) &&
+                  (a.window <= 0 || abs(kr - i) < a.window);
+          const float x = vis ? s[q] * sl2 : -INFINITY;
+          s[q] = x;
+          need |= x > m_ref[q] + 8.f;
+          i = (i + 1 == W) ? 0 : i + 1;
+        }
+      }
+      need = named_bar_or(kBarVote, kSoftThreads, need);
+      // the previous tile's P.V has finished: the probability tile is free, O^T is stable
+      ok = t == 0 || mbar_wait(pvdone, (t - 1) & 1);
+      if (named_bar_or(kBarVote, kSoftThreads, !ok)) {
+        abort = true;
+        break;
+      }
+      if (need) {  // new reference maxima (exact over this tile), rescale l and O^T
+        float *scr = reinterpret_cast<float *>(sm + kOffP);  // free: the last P.V is done
+        table_store(scr, kr, s);
+        named_bar(kBarSoft, kSoftThreads);
+        if (st_id < 64) {
+          const float tm = table_column<true>(scr, st_id);
+          const float m_old = m_ref[st_id], m_new = fmaxf(m_old, tm);
+          alpha[st_id] = m_new == -INFINITY ? 1.f : exp2f(m_old - m_new);
+          m_ref[st_id] = m_new;
+        }
+        named_bar(kBarSoft, kSoftThreads);
+#pragma unroll
+        for (int q = 0; q < 64; ++q) lsum[q] *= alpha[q];
+        if (t > 0) {  // O^T row kr: columns c and c + 64 belong to query c
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32_nowait(tmem + lane_off + kTmemO + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[(c0 + j) & 63]);
+            tmem_st32(tmem + lane_off + kTmemO + c0, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // probabilities: bf16 hi and lo halves, key row kr of the P^T tile
+      const bool dup = blk && qd == 0 && kr >= 16;  // block lo-key rows repeat rows 0..15
+      if (!dup) {
+        uint8_t *rowp = sm + kOffP + kr * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q0 = c * 8 + 2 * e;
+            const float p0 = s[q0] == -INFINITY ? 0.f : exp2f(s[q0] - m_ref[q0]);
+            const float p1 = s[q0 + 1] == -INFINITY ? 0.f : exp2f(s[q0 + 1] - m_ref[q0 + 1]);
+            lsum[q0] += p0;
+            lsum[q0 + 1] += p1;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(h);
+            hw[e] = *reinterpret_cast<const uint32_t *>(&h);
+            lw[e] = pack_bf16(p0 - hf.x, p1 - hf.y);
+          }
+          const uint32_t sw = static_cast<uint32_t>((c ^ (kr & 7)) << 4);
+          *reinterpret_cast<uint4 *>(rowp + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4 *>(rowp + kAtom + sw) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+      if (blk && qd == 0) {
+        __syncwarp();
+        if (dup) {  // same swizzle phase: kr & 7 == (kr - 16) & 7
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t o = static_cast<uint32_t>(c << 4);
+            *reinterpret_cast<uint4 *>(sm + kOffP + kr * 128 + o) =
+                *reinterpret_cast<const uint4 *>(sm + kOffP + (kr - 16) * 128 + o);
+            *reinterpret_cast<uint4 *>(sm + kOffP + kAtom + kr * 128 + o) =
+                *reinterpret_cast<const uint4 *>(sm + kOffP + kAtom + (kr - 16) * 128 + o);
+          }
+        }
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      mbar_arrive(pfull);
+    }
+    if (!abort && nt > 0) {
+      const bool ok = mbar_wait(pvdone, (nt - 1) & 1);
+      abort = named_bar_or(kBarVote, kSoftThreads, !ok);
+    }
+    if (!abort) {
+      // row sums of the 128 threads' partial sums
+      float *scr = reinterpret_cast<float *>(sm + kOffP);  // free: the last P.V is done
+      table_store(scr, kr, lsum);
+      named_bar(kBarSoft, kSoftThreads);
+      if (st_id < 64) l_fin[st_id] = table_column<false>(scr, st_id);
+      named_bar(kBarSoft, kSoftThreads);
+      // O^T row kr (output dim d = kr): query q is columns q and q + 64
+      float o[64];
+      if (nt > 0) {
+        tc_fence_after();
+        tmem_pair_sum<0>(tmem + lane_off + kTmemO, o);
+        tmem_pair_sum<32>(tmem + lane_off + kTmemO, o);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) o[q] = 0.f;
+      }
+      const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + g;
+      if (a.n_splits == 1) {
+        if (kr < D) {
+          __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+          int hh = 0, i = 0;
+#pragma unroll
+          for (int q = 0; q < 64; ++q) {
+            if (q < R) {
+              const float L = l_fin[q];
+              const float y = L > 0.f ? o[q] / L : 0.f;
+              const size_t idx = (static_cast<size_t>(b) * W + i) * a.n_q_heads * D +
+                                 static_cast<size_t>(g * G + hh) * D + kr;
+              const __nv_bfloat16 h = __float2bfloat16_rn(y);
+              out[idx] = h;
+              if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(h));
+            }
+            if (++i == W) {
+              i = 0;
+              ++hh;
+            }
+          }
+        }
+      } else {
+        float *po = a.part_o + (bh * a.n_splits + split) * kAttRows * D;
+        if (kr < D) {
+#pragma unroll
+          for (int q = 0; q < 64; ++q) po[static_cast<size_t>(q) * D + kr] = o[q];
+        }
+        if (st_id < 64)
+          a.part_ml[(bh * a.n_splits + split) * kAttRows + st_id] = make_float2(m_ref[st_id], l_fin[st_id]);
+        // merge the splits in this launch: every split of (b, g) counts itself once its
+        // partial is stored, waits (bounded) for the others, then merges its share of the
+        // rows.  The launch has at most one CTA per SM, so all splits are resident together,
+        // and each stores its partial before it waits.
+        unsigned *arrived = a.counters + bh;
+        unsigned *done = a.counters + static_cast<size_t>(a.B) * a.n_kv_heads + bh;
+        __threadfence();
+        named_bar(kBarSoft, kSoftThreads);
+        bool wok = true;
+        if (st_id == 0) {
+          atomicAdd(arrived, 1u);
+          wok = wait_count(arrived, static_cast<unsigned>(a.n_splits), kWaitLimitNs, 0);
+        }
+        if (!named_bar_or(kBarVote, kSoftThreads, !wok)) {
+          const int rp = (R + a.n_splits - 1) / a.n_splits;
+          const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
+          if (a.n_splits <= kFewSplits)
+            combine_rows_few<__nv_bfloat16, D, kFewSplits, 2>(a, b, g, r0, r1, warp - 2, lane);
+          else
+            combine_rows<__nv_bfloat16, D>(a, b, g, r0, r1, warp - 2, lane,
+                                           reinterpret_cast<float (*)[D + 4]>(sm + kOffP));
+          named_bar(kBarSoft, kSoftThreads);
+          if (st_id == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
+            *arrived = 0u;  // every split is past its wait: ready for the next launch
+            *done = 0u;
+          }
+        }
+      }
+    }
+    if (abort) *sabort = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*sabort && warp == 0 && lane == 0) {
+    // a wait gave up: let the loads still in flight land before the CTA exits (bounded)
+    for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&full[t & 1], (t >> 1) & 1);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ fp32 path
+// Context keys [p_lo, F) of request b: the window's oldest visible position, clipped to
+// the ring's live interval [F - cap, F).
+struct AttGeom {
+  long long F;
+  int p_lo, n_ctx;
+};
+__device__ __forceinline__ AttGeom att_geom(const AttArgs &a, int b) {
+  AttGeom g;
+  g.F = a.frontier[b];
+  long long lo = a.window > 0 ? g.F - a.window + 1 : 0;
+  if (g.F - a.cap > lo) lo = g.F - a.cap;
+  if (lo < 0) lo = 0;
+  g.p_lo = static_cast<int>(lo);
+  g.n_ctx = g.F > lo ? static_cast<int>(g.F - lo) : 0;
+  return g;
+}
+// Is context key k (0-based from p_lo) visible from block row i?
+__device__ __forceinline__ bool ctx_visible(const AttArgs &a, const AttGeom &g, int i, int k) {
+  if (k >= g.n_ctx) return false;
+  const long long p = g.p_lo + k;
+  return a.window <= 0 || (g.F + i) - p < a.window;
+}
+// Is block key j visible from block row i?
+__device__ __forceinline__ bool blk_visible(const AttArgs &a, int i, int j) {
+  if (j >= a.W) return false;
+  if (a.window > 0 && abs(j - i) >= a.window) return false;
+  return !a.causal || j <= i;
 }
 
 // fp32 path (small geometries): one CTA per (query head, request), exact fp32 softmax.
@@ -710,9 +757,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(const __grid_constan
   const int D = a.head_dim;
   pdl_wait();
   pdl_trigger();
-  AttGeom g = att_geom(a, b, 0);
-  g.k_begin = 0;
-  g.k_end = g.n_ctx;
+  const AttGeom g = att_geom(a, b);
   const int n_keys = g.n_ctx + a.W;
   const float *q = static_cast<const float *>(a.q);
   const float *rk = static_cast<const float *>(a.ring_k);
@@ -771,9 +816,6 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(const __grid_constan
   }
 }
 
-size_t attention_smem_bytes(int head_dim) {
-  return static_cast<size_t>(2 * kAttRows + 4 * kAttKeys) * (head_dim + kAttPad) * 2;
-}
 size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim) {
   return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows * head_dim;
 }
@@ -781,6 +823,21 @@ size_t attention_ml_count(int B, int n_kv_heads, int n_splits) {
   return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows;
 }
 int attention_rows_max() { return kAttRows; }
+int attention_tile_keys() { return kTileKeys; }
+
+template <int D>
+static cudaError_t launch_tc(const AttMaps &m, const AttArgs &a, cudaStream_t stream) {
+  static bool set = false;  // one flag per head dimension
+  if (!set) {
+    const cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kAttSmem));
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  return launch_pdl(attention_tc_kernel<D>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(kAttThreads),
+                    kAttSmem, stream, m, a);
+}
 
 std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
   cudaError_t e;
@@ -796,15 +853,22 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
     if (e != cudaSuccess) return std::string("attention launch: ") + cudaGetErrorString(e);
     return {};
   }
-  const size_t smem = attention_smem_bytes(a.head_dim);
-  auto go = [&](auto kernel) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    return launch_pdl(kernel, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(128), smem, stream, a);
-  };
-  if (a.head_dim == 128)
-    e = a.f16 ? go(attention_bf16_kernel<128, true>) : go(attention_bf16_kernel<128, false>);
-  else
-    e = a.f16 ? go(attention_bf16_kernel<64, true>) : go(attention_bf16_kernel<64, false>);
+  // bf16: the query and block planes must be contiguous (lo plane right after hi)
+  const int D = a.head_dim;
+  const long long T = static_cast<long long>(a.B) * a.W;
+  if (a.q_lo != static_cast<size_t>(T * a.n_q_heads * D) ||
+      a.blk_lo != static_cast<size_t>(T * a.n_kv_heads * D))
+    return "attention: hi/lo planes of the queries and block keys must be contiguous";
+  AttMaps m;
+  const int ring_rows = a.B * a.n_kv_heads * a.cap;
+  const int blk_rows = 2 * a.B * a.n_kv_heads * a.W;
+  std::string err;
+  if (!(err = make_tensor_map_2d(&m.ring_k, a.ring_k, GT_BF16, D, ring_rows, 64, kTileKeys, true)).empty() ||
+      !(err = make_tensor_map_2d(&m.ring_v, a.ring_v, GT_BF16, D, ring_rows, 64, kTileKeys, true)).empty() ||
+      !(err = make_tensor_map_2d(&m.blk_k, a.blk_k, GT_BF16, D, blk_rows, 64, 16, true)).empty() ||
+      !(err = make_tensor_map_2d(&m.blk_v, a.blk_v, GT_BF16, D, blk_rows, 64, 16, true)).empty())
+    return err;
+  e = D == 128 ? launch_tc<128>(m, a, stream) : launch_tc<64>(m, a, stream);
   if (e != cudaSuccess) return std::string("attention launch: ") + cudaGetErrorString(e);
   return {};
 }

@@ -911,6 +911,11 @@ static std::string make_map(CUtensorMap *out, const void *ptr, int dtype, int in
   return {};
 }
 
+std::string make_tensor_map_2d(CUtensorMap *out, const void *ptr, int dtype, int inner, int outer,
+                               int box_inner, int box_outer, bool swizzle, long long stride) {
+  return make_map(out, ptr, dtype, inner, outer, box_inner, box_outer, swizzle, stride);
+}
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {

@@ -153,6 +153,11 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
 unsigned take_error_word_pack();
 
 size_t gemm_partial_floats(int n_ctas, int block_n);
+// 2-D tiled tensor map of a row-major [outer, inner] matrix (rows `stride` elements apart,
+// 0 = inner) with boxes of box_outer x box_inner elements, 128-byte swizzled when
+// `swizzle`; out-of-bounds elements read as zero.  Encoded once per distinct argument set.
+std::string make_tensor_map_2d(CUtensorMap *out, const void *ptr, int dtype, int inner, int outer,
+                               int box_inner, int box_outer, bool swizzle, long long stride = 0);
 int num_sms();
 int gemm_block_n(int n_tokens);
 

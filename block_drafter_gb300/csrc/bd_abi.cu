@@ -193,14 +193,23 @@ struct Carve {
 // waits for it in the merge: give them a split of their own.
 // Key splits of a layer's bf16 attention: one CTA per (split, KV head, request) and one
 // CTA per SM (the splits of a head merge inside the launch, so all of them must be
-// resident together), at most one split per 128-slot tile of the ring.
-int att_splits(const bd_config *c, int l, int B, int W, int sms) {
-  (void)W;
+// resident together), at most one split per 128-slot tile of the ring, plus one split for
+// the block's own keys alone when that still fits (att_block_split).
+int att_ctx_splits(const bd_config *c, int l, int B, int sms) {
   const int cap = c->ring_capacity[l];
   const int tiles = (cap + attention_tile_keys() - 1) / attention_tile_keys();
   int s = sms / (B * c->n_kv_heads);
   if (s < 1) s = 1;
+  if (s > attention_max_splits()) s = attention_max_splits();
   return s < tiles ? s : tiles;
+}
+bool att_block_split(const bd_config *c, int l, int B, int sms) {
+  const int s = att_ctx_splits(c, l, B, sms);
+  return s + 1 <= attention_max_splits() && (s + 1) * B * c->n_kv_heads <= sms;
+}
+int att_splits(const bd_config *c, int l, int B, int W, int sms) {
+  (void)W;
+  return att_ctx_splits(c, l, B, sms) + (att_block_split(c, l, B, sms) ? 1 : 0);
 }
 int att_max_keys(const bd_config *c, int l, int W) {
   const int cap = c->ring_capacity[l];
@@ -756,19 +765,20 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       h.W = W;
       h.eps = cfg->eps;
       h.rope = rw.rope;
-      // the attention takes the queries and the block's keys/values as bf16 hi+lo planes
+      // the attention takes the queries and the block's keys/values as bf16 hi+lo planes,
+      // the queries scaled by log2(e)/sqrt(D) (its scores come out in log2 units)
       const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
       const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
-      const int a16 = 0;
-      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo, a16};
-      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo, a16};
-      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo, a16};
+      const float qs = split ? static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D))) : 0.f;
+      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo, qs};
+      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo, 0.f};
+      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo, 0.f};
       h.n_groups = 1;
       h.grp[0] = HeadGroup{0, T, 0, 3, cfg->n_q_heads + 2 * cfg->n_kv_heads};
       if (fuse) {  // the pending rows' context K/V go to the rings (before attention)
         const int cap = cfg->ring_capacity[l];
-        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0, 0};
-        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0, 0};
+        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0, 0.f};
+        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0, 0.f};
         h.n_groups = 2;
         h.grp[1] = HeadGroup{T, n_pend, 3, 2, 2 * cfg->n_kv_heads};
         h.n_req = B;
@@ -802,6 +812,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.cap = cfg->ring_capacity[l];
       a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
       a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
+      a.block_split = dt == BD_BF16 && att_block_split(cfg, l, B, sms) ? 1 : 0;
       a.n_guard = n_pend > 0 ? kMaxPendPerReq : 0;
       a.max_keys = att_max_keys(cfg, l, W);
       a.q_lo = split ? static_cast<size_t>(T) * QD : 0;

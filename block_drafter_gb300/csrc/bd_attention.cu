@@ -12,7 +12,8 @@
 // request); all G = Hq/Hkv query heads of the KV head and all W block rows (G*W <= 64
 // query rows) share every K/V tile, so the windowed context is streamed once per KV head.
 // Warp roles: warp 0 issues the TMA loads of 128-key K/V tiles (two-stage pipeline),
-// warp 1 issues the tcgen05 MMAs, warps 2-5 (one TMEM lane quarter each) run the softmax.
+// warp 1 issues the tcgen05 MMAs, warps 2-9 run the softmax (two warps per TMEM lane
+// quarter, each taking half of the query columns).
 //   S^T = K Q^T:  keys are the MMA's M side (128 TMEM lanes, one key per softmax thread);
 //                 the N side holds the query rows twice, as the bf16 hi and lo halves of
 //                 the fp32 queries, so one MMA gives both products and each thread adds
@@ -40,8 +41,8 @@ BD_DEFINE_ERROR_TAKER(take_error_word_att)
 
 constexpr int kAttRows = 64;         // query rows per (request, KV head): G*W <= 64
 constexpr int kTileKeys = 128;       // context keys per tile (the S MMA's M side)
-constexpr int kAttThreads = 192;     // producer warp, MMA warp, four softmax warps
-constexpr int kSoftThreads = 128;
+constexpr int kAttThreads = 320;     // producer warp, MMA warp, eight softmax warps
+constexpr int kSoftThreads = 256;
 constexpr int kBarSoft = 1;          // named barrier of the softmax warps
 constexpr int kBarVote = 2;          // their votes (barrier with an OR reduction)
 constexpr uint32_t kAtom = 16384;    // 128 rows x 128 bytes (64 bf16 of each row)
@@ -50,9 +51,9 @@ constexpr uint32_t kOffQ = 0;                       // rows 0..63 hi, 64..127 lo
 constexpr uint32_t kOffK = 2 * kAtom;               // [2 stages] key tiles
 constexpr uint32_t kOffV = kOffK + 2 * 2 * kAtom;   // [2 stages] value tiles
 constexpr uint32_t kOffP = kOffV + 2 * 2 * kAtom;   // atom 0: hi probabilities, atom 1: lo
-constexpr uint32_t kOffRed = kOffP + 2 * kAtom;     // float m_ref[64], alpha[64], l[64]
-constexpr uint32_t kOffBar = kOffRed + 3 * 64 * 4;
-constexpr int kNumBars = 11;  // full[2], empty[2], sfull[2], sfree[2], pfull, pvdone, qready
+constexpr uint32_t kOffRed = kOffP + 2 * kAtom;     // m_ref[64], alpha[64], l[64], q_row[64], red[4][64]
+constexpr uint32_t kOffBar = kOffRed + 8 * 64 * 4;
+constexpr int kNumBars = 15;  // full_k/v[2], empty_k/v[2], sfull[2], sfree[2], pfull, pvdone, qready
 constexpr size_t kAttSmem = kOffBar + kNumBars * 8 + 16 + 1024;
 // TMEM columns: S^T double buffer at 0 and 128, O^T at 256
 constexpr uint32_t kTmemCols = 512;
@@ -68,197 +69,114 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Column reduction of a [128 threads][64] value table through shared memory (the free
-// probability tile): element (row r, column q) sits at r*64 + (q ^ (r & 31)), so both the
-// row writes of a warp and the column reads of 32 threads touch 32 distinct banks.
-__device__ __forceinline__ void table_store(float *scr, int r, const float (&v)[64]) {
-#pragma unroll
-  for (int q = 0; q < 64; ++q) scr[r * 64 + (q ^ (r & 31))] = v[q];
+// 2^x (ex2.approx.ftz: relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
-template <bool MAX>
-__device__ __forceinline__ float table_column(const float *scr, int q) {
-  float acc = MAX ? -INFINITY : 0.f;
-#pragma unroll 8
-  for (int r = 0; r < 128; ++r) {
-    const float x = scr[r * 64 + (q ^ (r & 31))];
-    acc = MAX ? fmaxf(acc, x) : acc + x;
-  }
-  return acc;
+// (x0, x1) -> packed bf16 hi pair and the packed bf16 pair of the residuals x - hi
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  uint32_t hv, lv;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hv) : "f"(x1), "f"(x0));
+  const float h0 = __uint_as_float(hv << 16), h1 = __uint_as_float(hv & 0xffff0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lv) : "f"(x1 - h1), "f"(x0 - h0));
+  hi = hv;
+  lo = lv;
 }
-
-// Merge the splits of query rows r0 .. r1-1 of (request b, KV head h):
-//   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-// The four warps take (row, part) tasks: with fewer than three rows each row's splits are
-// shared by 4 / rows warps, whose sums meet in shared memory.  Lanes own D/32 consecutive
-// output dims; split weights are computed by lanes and broadcast, and the partial tiles are
-// loaded eight splits at a time before they are used (the loads are independent and their
-// L2 latency, not bandwidth, bounds the merge).  The partials were written by other CTAs of
-// the launch: read through L2.  Called by all threads of the CTA.
-// Few splits (S <= SMAX): each warp merges rows r0 + warp, r0 + warp + 4, ... RB at a time,
-// with every load of those rows (the splits' (m, l) and partial rows) issued before any
-// arithmetic, so they cost one round trip to L2.  Splits are added in index order.
-constexpr int kFewSplits = 8;
-template <typename T, int D, int SMAX, int RB>
-__device__ __forceinline__ void combine_rows_few(const AttArgs &a, int b, int h, int r0, int r1,
-                                                 int warp, int lane) {
-  constexpr int PER = D / 32;
-  const int G = a.n_q_heads / a.n_kv_heads, S = a.n_splits;
-  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
+// Merge of the splits' partials (O, m, l) of query rows r0 .. r1-1 of (request b, KV head
+// g) by the 256 softmax threads:
+//   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max over splits with l_s > 0.
+// The (m, l) of every (split, row) are loaded first, then each thread takes float4 chunks of
+// the rows and issues up to 16 partial loads before any arithmetic (one round trip to L2 per
+// pass; one pass when chunks x splits fit).  The partials were written by other CTAs of the launch: read through
+// L2.  Splits are added in index order.  scr: shared scratch of 3 * kMaxMergeSplits * 64 + 64
+// floats.
+constexpr int kMaxMergeSplits = 32;
+template <int D>
+__device__ void merge_splits(const AttArgs &a, int b, int g, int r0, int r1, int tid, float *scr) {
+  const int S = a.n_splits, nr = r1 - r0;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + g;
   const float *po = a.part_o + bh * S * kAttRows * D;
   const float2 *pml = a.part_ml + bh * S * kAttRows;
-  for (int base = r0 + warp; base < r1; base += 4 * RB) {
-    float2 ml[RB][SMAX];
-    float v[RB][SMAX][PER];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      const int rr = base + 4 * i;
-#pragma unroll
-      for (int sp = 0; sp < SMAX; ++sp) {
-        const bool ok = rr < r1 && sp < S;
-        ml[i][sp] = ok ? __ldcg(pml + sp * kAttRows + rr) : make_float2(-INFINITY, 0.f);
-        const float *os = po + (static_cast<size_t>(ok ? sp : 0) * kAttRows + (ok ? rr : 0)) * D + lane * PER;
-        if (PER == 4) {
-          const float4 o = ok ? __ldcg(reinterpret_cast<const float4 *>(os)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[i][sp][0] = o.x;
-          v[i][sp][1 % PER] = o.y;
-          v[i][sp][2 % PER] = o.z;
-          v[i][sp][3 % PER] = o.w;
-        } else {
-          const float2 o = ok ? __ldcg(reinterpret_cast<const float2 *>(os)) : make_float2(0.f, 0.f);
-          v[i][sp][0] = o.x;
-          v[i][sp][1 % PER] = o.y;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      const int rr = base + 4 * i;
-      if (rr >= r1) break;
-      float M = -INFINITY;
-#pragma unroll
-      for (int sp = 0; sp < SMAX; ++sp)
-        if (ml[i][sp].y > 0.f) M = fmaxf(M, ml[i][sp].x);
-      float L = 0.f, acc[PER];
-#pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int sp = 0; sp < SMAX; ++sp)
-        if (ml[i][sp].y > 0.f) {
-          const float wgt = exp2f(ml[i][sp].x - M);
-          L += wgt * ml[i][sp].y;
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] += wgt * v[i][sp][e];
-        }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const int gh = rr / a.W, qi = rr % a.W;
-      T *out = static_cast<T *>(a.out) +
-               (static_cast<size_t>(b) * a.W + qi) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const float y = acc[e] * inv;
-        const T hi = from_f<T>(y);
-        out[e] = hi;
-        if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
-      }
-    }
+  float *sm_m = scr, *sm_l = scr + kMaxMergeSplits * 64, *sm_w = sm_l + kMaxMergeSplits * 64;
+  float *inv_l = sm_w + kMaxMergeSplits * 64;
+  for (int i = tid; i < S * nr; i += kSoftThreads) {
+    const int sp = i / nr, r = i - sp * nr;
+    const float2 ml = __ldcg(pml + sp * kAttRows + r0 + r);
+    sm_m[sp * 64 + r] = ml.x;
+    sm_l[sp * 64 + r] = ml.y;
   }
-}
-
-template <typename T, int D>
-__device__ __forceinline__ void combine_rows(const AttArgs &a, int b, int h, int r0, int r1,
-                                             int warp, int lane, float (*red)[D + 4]) {
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + h;
-  constexpr int PER = D / 32;
-  constexpr int kBatch = 8;
-  const float *po = a.part_o + bh * a.n_splits * kAttRows * D;
-  const float2 *pml = a.part_ml + bh * a.n_splits * kAttRows;
-  const int nrows = r1 - r0;
-  const int P = nrows >= 3 ? 1 : 4 / max(nrows, 1);  // warps per row
-  const int S = a.n_splits;
-  for (int t0 = 0; t0 < nrows * P; t0 += 4) {
-    const int t = t0 + warp;
-    const bool active = t < nrows * P;
-    const int rr = r0 + (active ? t / P : 0), part = t % P;
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  named_bar(kBarSoft, kSoftThreads);
+  if (tid < nr) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp)
+      if (sm_l[sp * 64 + tid] > 0.f) M = fmaxf(M, sm_m[sp * 64 + tid]);
     float L = 0.f;
-    if (active) {
-      float M = -INFINITY;
-      for (int s = lane; s < S; s += 32) {
-        const float2 ml = __ldcg(pml + s * kAttRows + rr);
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);
-      }
-      M = warp_max(M);
-      const int s_begin = part * S / P, s_end = (part + 1) * S / P;
-      for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-        const int s = s0 + lane;
-        float wgt = 0.f;
-        if (s < s_end) {
-          const float2 ml = __ldcg(pml + s * kAttRows + rr);
-          if (ml.y > 0.f) {
-            wgt = exp2f(ml.x - M);
-            L += wgt * ml.y;
-          }
-        }
-        const int cnt = min(32, s_end - s0);
-        for (int j0 = 0; j0 < cnt; j0 += kBatch) {
-          float v[kBatch][PER];
+    for (int sp = 0; sp < S; ++sp) {
+      const float l = sm_l[sp * 64 + tid];
+      const float w = l > 0.f ? exp2f(sm_m[sp * 64 + tid] - M) : 0.f;
+      sm_w[sp * 64 + tid] = w;
+      L += w * l;
+    }
+    inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
+  }
+  named_bar(kBarSoft, kSoftThreads);
+  constexpr int C4 = D / 4;  // float4 chunks per row
+  constexpr int kLoads = 16;  // partial loads in flight per thread
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+  const int total = nr * C4;
+  const int SB = min(S, kLoads);                  // splits per batch of loads
+  const int per = max(1, min(4, kLoads / SB));    // chunks per thread and pass
+  for (int c0 = tid; c0 < total; c0 += kSoftThreads * per) {
+    float4 acc[4];
 #pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const float *os = po + (static_cast<size_t>(s0 + j0 + u) * kAttRows + rr) * D + lane * PER;
-            if (j0 + u < cnt) {
-              if (PER == 4) {
-                const float4 o = __ldcg(reinterpret_cast<const float4 *>(os));
-                v[u][0] = o.x;
-                v[u][1] = o.y;
-                v[u][2] = o.z;
-                v[u][3] = o.w;
-              } else {
-                const float2 o = __ldcg(reinterpret_cast<const float2 *>(os));
-                v[u][0] = o.x;
-                v[u][1] = o.y;
-              }
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < S; sp0 += SB) {
+      // every load of the batch first: chunk c0 + k*256 of split sp0 + j in v[k*SB + j]
+      float4 v[kLoads];
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i) {
+        const int k = i / SB, sp = sp0 + i - k * SB;
+        const int c = c0 + k * kSoftThreads;
+        if (k < per && c < total && sp < S) {
+          const int r = c / C4, d4 = c - r * C4;
+          v[i] = __ldcg(reinterpret_cast<const float4 *>(po + (static_cast<size_t>(sp) * kAttRows + r0 + r) * D) + d4);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i) {
+        const int k = i / SB, sp = sp0 + i - k * SB;
+        const int c = c0 + k * kSoftThreads;
+        if (k < per && c < total && sp < S) {
+          const float w = sm_w[sp * 64 + c / C4];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            if (kk == k) {
+              acc[kk].x += w * v[i].x;
+              acc[kk].y += w * v[i].y;
+              acc[kk].z += w * v[i].z;
+              acc[kk].w += w * v[i].w;
             }
-          }
-#pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const float wj = __shfl_sync(0xffffffffu, wgt, (j0 + u) & 31);
-            if (j0 + u < cnt)
-#pragma unroll
-              for (int e = 0; e < PER; ++e) acc[e] += wj * v[u][e];
-          }
         }
       }
-      L = warp_sum(L);
     }
-    if (P > 1) {  // the parts of a row meet in shared memory
-      if (active) {
 #pragma unroll
-        for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
-        if (lane == 0) red[warp][D] = L;
-      }
-      named_bar(kBarSoft, kSoftThreads);
-      if (active && part == 0)
-        for (int q = 1; q < P; ++q) {
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] += red[warp + q][lane * PER + e];
-          L += red[warp + q][D];
-        }
-    }
-    if (active && part == 0) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const int gh = rr / a.W, i = rr % a.W;
-      T *out = static_cast<T *>(a.out) +
-               (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D + (h * G + gh) * D + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const float y = acc[e] * inv;
-        const T hi = from_f<T>(y);
-        out[e] = hi;
-        if (a.out_lo) out[a.out_lo + e] = from_f<T>(y - to_f<T>(hi));
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int c = c0 + k * kSoftThreads;
+      if (k >= per || c >= total) break;
+      const int r = c / C4, d4 = c - r * C4;
+      const float4 acck = acc[k];
+      const float il = inv_l[r];
+      const int q = r0 + r, hh = q / a.W, i = q - hh * a.W;
+      const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
+                         static_cast<size_t>(g * G + hh) * D + 4 * d4;
+      uint32_t hw[2], lw[2];
+      split_bf16x2(acck.x * il, acck.y * il, hw[0], lw[0]);
+      split_bf16x2(acck.z * il, acck.w * il, hw[1], lw[1]);
+      *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
+      if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
     }
   }
 }
@@ -274,41 +192,40 @@ __device__ __forceinline__ long long slot_position(long long F, int cap, int s) 
 }
 
 // ------------------------------------------------------------------ producer (one thread)
+// K and V tiles have stages of their own: a K stage is free once the S MMA that read it has
+// completed, a V stage once its P.V has; both streams are polled without blocking.
 template <int D>
-__device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm, uint64_t *full,
-                             uint64_t *empty, int b, int g, long long F, int t_begin, int n_ctx,
-                             int nt, volatile int *sabort, int &issued) {
+__device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm, uint64_t *full_k,
+                             uint64_t *full_v, uint64_t *empty_k, uint64_t *empty_v, int b, int g,
+                             long long F, int t_begin, int n_ctx, int nt, volatile int *sabort,
+                             int &issued_k, int &issued_v) {
   constexpr int NB = D / 64;  // 64-column boxes per row
   const uint64_t pol_ring = policy_evict_first();
+  const uint64_t pol_blk = policy_evict_last();
   const int cap = a.cap;
   const int row0 = (b * a.n_kv_heads + g) * cap;
-  auto issue = [&](int t) {
-    const int st = t & 1;
-    uint64_t *bar = &full[st];
-    uint8_t *dk = sm + kOffK + st * 2 * kAtom;
-    uint8_t *dv = sm + kOffV + st * 2 * kAtom;
+  const int brow = (b * a.n_kv_heads + g) * a.W;
+  const int lo_row = a.B * a.n_kv_heads * a.W;
+  // one operand (K: v = 0, V: v = 1) of tile t into its stage t & 1
+  auto issue = [&](int t, int v) {
+    uint64_t *bar = v ? &full_v[t & 1] : &full_k[t & 1];
+    uint8_t *dst = sm + (v ? kOffV : kOffK) + (t & 1) * 2 * kAtom;
+    const CUtensorMap *ring = v ? &maps.ring_v : &maps.ring_k;
+    const CUtensorMap *blk = v ? &maps.blk_v : &maps.blk_k;
     if (t < n_ctx) {
       const int s0 = (t_begin + t) * kTileKeys;
-      mbar_arrive_expect_tx(bar, 2u * NB * kAtom);
+      mbar_arrive_expect_tx(bar, NB * kAtom);
 #pragma unroll
-      for (int kb = 0; kb < NB; ++kb) {
-        tma_load_2d(dk + kb * kAtom, &maps.ring_k, bar, kb * 64, row0 + s0, pol_ring);
-        tma_load_2d(dv + kb * kAtom, &maps.ring_v, bar, kb * 64, row0 + s0, pol_ring);
-      }
+      for (int kb = 0; kb < NB; ++kb) tma_load_2d(dst + kb * kAtom, ring, bar, kb * 64, row0 + s0, pol_ring);
     } else {  // the block's keys/values: hi rows to tile rows 0..15, lo rows to 16..31
-      const int brow = (b * a.n_kv_heads + g) * a.W;
-      const int lo_row = a.B * a.n_kv_heads * a.W;
-      const uint64_t pol = policy_evict_last();
-      mbar_arrive_expect_tx(bar, 4u * NB * 16 * 128);
+      mbar_arrive_expect_tx(bar, 2u * NB * 16 * 128);
 #pragma unroll
       for (int kb = 0; kb < NB; ++kb) {
-        tma_load_2d(dk + kb * kAtom, &maps.blk_k, bar, kb * 64, brow, pol);
-        tma_load_2d(dk + kb * kAtom + 16 * 128, &maps.blk_k, bar, kb * 64, lo_row + brow, pol);
-        tma_load_2d(dv + kb * kAtom, &maps.blk_v, bar, kb * 64, brow, pol);
-        tma_load_2d(dv + kb * kAtom + 16 * 128, &maps.blk_v, bar, kb * 64, lo_row + brow, pol);
+        tma_load_2d(dst + kb * kAtom, blk, bar, kb * 64, brow, pol_blk);
+        tma_load_2d(dst + kb * kAtom + 16 * 128, blk, bar, kb * 64, lo_row + brow, pol_blk);
       }
     }
-    issued = t + 1;
+    if (v) issued_v = t + 1; else issued_k = t + 1;
   };
   // The ring holds context written before this round, except the positions >= F - n_guard
   // that this round's catch-up may store (the previous kernel): a first tile without them
@@ -324,23 +241,41 @@ __device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm,
     }
     return true;
   };
-  int t = 0;
-  if (nt > 0 && safe(0)) issue(t++);
+  int tk = 0, tv = 0;
+  if (nt > 0 && safe(0)) {
+    issue(0, 0);
+    issue(0, 1);
+    tk = tv = 1;
+  }
   pdl_wait();
-  for (; t < nt; ++t) {
-    if (t >= 2 && (*sabort || !mbar_wait(&empty[t & 1], ((t >> 1) - 1) & 1))) {
+  unsigned long long last = globaltimer();
+  while (tk < nt || tv < nt) {
+    if (*sabort) return;
+    bool prog = false;
+    if (tk < nt && (tk < 2 || mbar_test_wait(&empty_k[tk & 1], ((tk >> 1) - 1) & 1))) {
+      issue(tk++, 0);
+      prog = true;
+    }
+    if (tv < nt && tv < tk && (tv < 2 || mbar_test_wait(&empty_v[tv & 1], ((tv >> 1) - 1) & 1))) {
+      issue(tv++, 1);
+      prog = true;
+    }
+    if (prog) {
+      last = globaltimer();
+    } else if (globaltimer() - last > kWaitLimitNs) {
+      atomicOr(&g_error_word, DEVERR_TIMEOUT);
       *sabort = 1;
       return;
     }
-    issue(t);
   }
 }
 
 // ------------------------------------------------------------------ MMA issuer (one thread)
 template <int D>
-__device__ void att_mma(uint8_t *sm, uint64_t *full, uint64_t *empty, uint64_t *sfull,
-                        uint64_t *sfree, uint64_t *pfull, uint64_t *pvdone, uint64_t *qready,
-                        uint32_t tmem, int n_ctx, int nt, volatile int *sabort) {
+__device__ void att_mma(uint8_t *sm, uint64_t *full_k, uint64_t *full_v, uint64_t *empty_k,
+                        uint64_t *empty_v, uint64_t *sfull, uint64_t *sfree, uint64_t *pfull,
+                        uint64_t *pvdone, uint64_t *qready, uint32_t tmem, int n_ctx, int nt,
+                        volatile int *sabort) {
   const uint32_t idesc_s = umma_idesc(1, 128, 128);                           // both K-major
   const uint32_t idesc_o = umma_idesc(1, 128, 128) | (1u << 15) | (1u << 16);  // both MN-major
   if (!mbar_wait(qready, 0)) {
@@ -350,53 +285,82 @@ __device__ void att_mma(uint8_t *sm, uint64_t *full, uint64_t *empty, uint64_t *
   tc_fence_after();
   const uint32_t q_base = smem_u32(sm + kOffQ);
   const uint32_t p_base = smem_u32(sm + kOffP);
-  auto pv = [&](int u) -> bool {
-    if (*sabort || !mbar_wait(pfull, u & 1)) return false;
-    tc_fence_after();
-    const uint32_t v_base = smem_u32(sm + kOffV + (u & 1) * 2 * kAtom);
-    const int nk = u < n_ctx ? kTileKeys / 16 : 2;  // the block tile has 32 key rows
-    for (int kk = 0; kk < nk; ++kk)
-      umma_bf16(tmem + kTmemO, umma_desc_sw128_mn(v_base + kk * 2048, kAtom, 1024),
-                umma_desc_sw128_mn(p_base + kk * 2048, kAtom, 1024), idesc_o,
-                (u > 0 || kk > 0) ? 1u : 0u);
-    umma_commit(&empty[u & 1]);  // the K/V stage is free
-    umma_commit(pvdone);         // the probabilities are consumed, O^T is up to date
-    return true;
-  };
-  for (int t = 0; t < nt; ++t) {
-    const int st = t & 1;
-    if (*sabort || !mbar_wait(&full[st], (t >> 1) & 1) ||
-        (t >= 2 && !mbar_wait(&sfree[st], ((t >> 1) - 1) & 1))) {
-      *sabort = 1;
-      return;
-    }
-    tc_fence_after();
-    const uint32_t k_base = smem_u32(sm + kOffK + st * 2 * kAtom);
+  // S of tile ns needs its K tile and a free S buffer; P.V of tile np needs its
+  // probabilities.  Both are polled without blocking, so a P.V is issued as soon as its
+  // probabilities are ready (the stage it frees is what the producer refills next).
+  int ns = 0, np = 0;
+  unsigned long long last = globaltimer();
+  while (np < nt) {
+    if (*sabort) return;
+    bool prog = false;
+    if (ns < nt && mbar_test_wait(&full_k[ns & 1], (ns >> 1) & 1) &&
+        (ns < 2 || mbar_test_wait(&sfree[ns & 1], ((ns >> 1) - 1) & 1))) {
+      tc_fence_after();
+      const uint32_t k_base = smem_u32(sm + kOffK + (ns & 1) * 2 * kAtom);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-      umma_bf16(tmem + st * 128, umma_desc_sw128(k_base + off), umma_desc_sw128(q_base + off),
-                idesc_s, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+        umma_bf16(tmem + (ns & 1) * 128, umma_desc_sw128(k_base + off), umma_desc_sw128(q_base + off),
+                  idesc_s, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&sfull[ns & 1]);
+      umma_commit(&empty_k[ns & 1]);  // the K stage is free
+      ++ns;
+      prog = true;
     }
-    umma_commit(&sfull[st]);
-    if (t >= 1 && !pv(t - 1)) {  // the previous tile's P.V, behind this tile's scores
+    if (np < ns && mbar_test_wait(pfull, np & 1) && mbar_test_wait(&full_v[np & 1], (np >> 1) & 1)) {
+      tc_fence_after();
+      const uint32_t v_base = smem_u32(sm + kOffV + (np & 1) * 2 * kAtom);
+      const int nk = np < n_ctx ? kTileKeys / 16 : 2;  // the block tile has 32 key rows
+      for (int kk = 0; kk < nk; ++kk)
+        umma_bf16(tmem + kTmemO, umma_desc_sw128_mn(v_base + kk * 2048, kAtom, 1024),
+                  umma_desc_sw128_mn(p_base + kk * 2048, kAtom, 1024), idesc_o,
+                  (np > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&empty_v[np & 1]);  // the V stage is free
+      umma_commit(pvdone);            // the probabilities are consumed, O^T is up to date
+      ++np;
+      prog = true;
+    }
+    if (prog) {
+      last = globaltimer();
+    } else if (globaltimer() - last > kWaitLimitNs) {
+      atomicOr(&g_error_word, DEVERR_TIMEOUT);
       *sabort = 1;
       return;
     }
   }
-  if (nt > 0 && !pv(nt - 1)) *sabort = 1;
 }
 
-// Loads columns [c0, c0+32) and [c0+64, c0+96) of this thread's TMEM lane and returns
-// their sums (the hi and lo halves of one product) in v[j0 .. j0+31].
-template <int J0>
-__device__ __forceinline__ void tmem_pair_sum(uint32_t taddr, float (&v)[64]) {
-  uint32_t h[32], l[32];
-  tmem_ld32_nowait(taddr + J0, h);
-  tmem_ld32_nowait(taddr + 64 + J0, l);
+// Columns [c, c+32) and [c+64, c+96) of this thread's TMEM lane (taddr = lane base + c),
+// added: the hi and lo halves of one product.
+__device__ __forceinline__ void tmem_pair32(uint32_t taddr, float (&v)[32]) {
+  uint32_t hv[32], lv[32];
+  tmem_ld32_nowait(taddr, hv);
+  tmem_ld32_nowait(taddr + 64, lv);
   tmem_ld_wait();
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[J0 + j] = __uint_as_float(h[j]) + __uint_as_float(l[j]);
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(hv[j]) + __uint_as_float(lv[j]);
+}
+
+// Butterfly reduce-scatter of 32 values over the warp: afterwards v[0] of lane j holds the
+// warp-wide sum of entry j.  At each step a lane keeps one half of its entries and adds its
+// partner's copy of that half.
+template <int N, int O>
+__device__ __forceinline__ void bfly_sum_step(float (&v)[32], int lane) {
+  const bool up = (lane & O) != 0;
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const float send = up ? v[j] : v[j + N / 2];
+    const float keep = up ? v[j + N / 2] : v[j];
+    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+  }
+}
+__device__ __forceinline__ void bfly_sum32(float (&v)[32], int lane) {
+  bfly_sum_step<32, 16>(v, lane);
+  bfly_sum_step<16, 8>(v, lane);
+  bfly_sum_step<8, 4>(v, lane);
+  bfly_sum_step<4, 2>(v, lane);
+  bfly_sum_step<2, 1>(v, lane);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -406,11 +370,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float *m_ref = reinterpret_cast<float *>(sm + kOffRed);  // per query: reference max (log2 units)
-  float *alpha = m_ref + 64, *l_fin = alpha + 64;          // rescale factors, row sums
+  float *m_ref_s = reinterpret_cast<float *>(sm + kOffRed);  // per query: reference max (log2 units)
+  float *alpha = m_ref_s + 64, *l_fin = alpha + 64;          // rescale factors, row sums
+  int *q_row = reinterpret_cast<int *>(l_fin + 64);           // block row of each query
+  float *red_max = reinterpret_cast<float *>(q_row + 64);     // [4 warps][64 queries] scratch
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-  uint64_t *full = bars, *empty = bars + 2, *sfull = bars + 4, *sfree = bars + 6;
-  uint64_t *pfull = bars + 8, *pvdone = bars + 9, *qready = bars + 10;
+  uint64_t *full_k = bars, *full_v = bars + 2, *empty_k = bars + 4, *empty_v = bars + 6;
+  uint64_t *sfull = bars + 8, *sfree = bars + 10;
+  uint64_t *pfull = bars + 12, *pvdone = bars + 13, *qready = bars + 14;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -422,17 +389,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int cap = a.cap;
   const int n_slots = F < cap ? static_cast<int>(F > 0 ? F : 0) : cap;
   const int n_tiles = (n_slots + kTileKeys - 1) / kTileKeys;
-  const int per = (n_tiles + a.n_splits - 1) / a.n_splits;
-  const int t_begin = min(n_tiles, split * per);
+  // with block_split the last split takes only the block's own keys
+  const int ctx_splits = a.n_splits - (a.block_split ? 1 : 0);
+  const int per = (n_tiles + ctx_splits - 1) / ctx_splits;
+  const int t_begin = split < ctx_splits ? min(n_tiles, split * per) : n_tiles;
   const int n_ctx = min(n_tiles, t_begin + per) - t_begin;
   const bool do_block = split == a.n_splits - 1;
   const int nt = n_ctx + (do_block ? 1 : 0);
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(&empty[0], 1);
-    mbar_init(&empty[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full_k[i], 1);
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty_k[i], 1);
+      mbar_init(&empty_v[i], 1);
+    }
     mbar_init(&sfull[0], 1);
     mbar_init(&sfull[1], 1);
     mbar_init(&sfree[0], kSoftThreads);
@@ -459,164 +430,200 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
 
-  int issued = 0;
+  int issued_k = 0, issued_v = 0;
   if (warp == 0) {
-    if (lane == 0) att_producer<D>(maps, a, sm, full, empty, b, g, F, t_begin, n_ctx, nt, sabort, issued);
+    if (lane == 0)
+      att_producer<D>(maps, a, sm, full_k, full_v, empty_k, empty_v, b, g, F, t_begin, n_ctx, nt, sabort,
+                      issued_k, issued_v);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) att_mma<D>(sm, full, empty, sfull, sfree, pfull, pvdone, qready, tmem, n_ctx, nt, sabort);
+    if (lane == 0)
+      att_mma<D>(sm, full_k, full_v, empty_k, empty_v, sfull, sfree, pfull, pvdone, qready, tmem, n_ctx, nt,
+                 sabort);
     __syncwarp();
   } else {
-    const int qd = warp & 3;           // TMEM lane quarter of this warp
-    const int kr = qd * 32 + lane;     // S^T lane = key row of a tile; O^T lane = output dim
-    const int st_id = tid - 64;        // 0..127 among the softmax threads
+    // softmax warps 2..9: lane quarter qd of the tiles (key row / output dim kr), query
+    // half h (queries h*32 .. h*32+31)
+    const int qd = warp & 3;
+    const int kr = qd * 32 + lane;
+    const int h = (warp - 2) >> 2;
+    const int st_id = tid - 64;  // 0..255 among the softmax threads
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    // every wait is made warp-uniform (the TMEM loads after it are warp-collective); after a
+    // wait gives up the others return at once, so all threads still pass the same barriers
+    auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
+      bool ok = !*sabort && mbar_wait(bar, parity);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) *sabort = 1;
+      return ok;
+    };
     pdl_wait();
-    // Query tile: row n = plane*64 + r, r = head_in_group * W + i, plane 0 = hi, 1 = lo
+    // query tile (queried rows already scaled by log2(e)/sqrt(D), so the scores come out in
+    // log2 units): tile row r (hi plane) and row 64 + r (lo plane) hold query r =
+    // head_in_group*W + i.  Each thread copies one 64-column half of one plane row.
     {
-      const int n = st_id, plane = n >> 6, r = n & 63;
-      const bool ok = r < R;
-      const int hh = ok ? r / W : 0, i = ok ? r % W : 0;
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          static_cast<const __nv_bfloat16 *>(a.q) + (plane ? a.q_lo : 0) +
-          (static_cast<size_t>(b) * W + i) * a.n_q_heads * D + static_cast<size_t>(g * G + hh) * D);
-      uint4 v[D / 8];
+      const int n = st_id & 127, half = st_id >> 7, plane = n >> 6, r = n & 63;
+      if (half * 64 < D) {
+        const bool ok = r < R;
+        const int hh = ok ? r / W : 0, i = ok ? r % W : 0;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const __nv_bfloat16 *>(a.q) + (plane ? a.q_lo : 0) +
+            (static_cast<size_t>(b) * W + i) * a.n_q_heads * D + static_cast<size_t>(g * G + hh) * D +
+            half * 64);
+        uint4 v[8];
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) v[ch] = ok ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c) v[c] = ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch)
-        *reinterpret_cast<uint4 *>(sm + kOffQ + (ch >> 3) * kAtom + n * 128 +
-                                   (((ch & 7) ^ (n & 7)) << 4)) = v[ch];
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(sm + kOffQ + half * kAtom + n * 128 + ((c ^ (n & 7)) << 4)) = v[c];
+      }
     }
-    if (st_id < 64) m_ref[st_id] = -INFINITY;
+    if (st_id < 64) {
+      const int q = st_id;
+      q_row[q] = q < R ? q % W : (1 << 20);  // block row of query q (never visible past R)
+      m_ref_s[q] = -1e30f;
+    }
     fence_proxy_async_shared();
     mbar_arrive(qready);
     named_bar(kBarSoft, kSoftThreads);
 
-    const float sl2 = 1.4426950408889634f * rsqrtf(static_cast<float>(D));  // log2(e)/sqrt(D)
-    float lsum[64];
+    // reference maxima (log2 units) of this thread's 32 queries; a finite start value, so
+    // that a hidden key (-inf) gives a zero probability before the first reference is set
+    constexpr float kNoRef = -1e30f;
+    float mr[32], lsum[32];
 #pragma unroll
-    for (int q = 0; q < 64; ++q) lsum[q] = 0.f;
-    bool abort = false;
-    for (int t = 0; t < nt && !abort; ++t) {
+    for (int j = 0; j < 32; ++j) {
+      mr[j] = kNoRef;
+      lsum[j] = 0.f;
+    }
+    uint8_t *prow = sm + kOffP + kr * 128;
+    const uint32_t swz = static_cast<uint32_t>(kr & 7);
+    // ring slot of position F - cap (the oldest) once the ring is full
+    const int base_slot = F >= cap ? static_cast<int>(F % cap) : 0;
+    for (int t = 0; t < nt; ++t) {
       const int sb = t & 1;
-      bool ok = !*sabort && mbar_wait(&sfull[sb], (t >> 1) & 1);
-      if (named_bar_or(kBarVote, kSoftThreads, !ok)) {
-        abort = true;
-        break;
+      float s[32];
+      if (wait_ok(&sfull[sb], (t >> 1) & 1)) {
+        tc_fence_after();
+        tmem_pair32(tmem + lane_off + sb * 128 + h * 32, s);
       }
-      tc_fence_after();
-      float s[64];
-      tmem_pair_sum<0>(tmem + lane_off + sb * 128, s);
-      tmem_pair_sum<32>(tmem + lane_off + sb * 128, s);
       tc_fence_before();
       mbar_arrive(&sfree[sb]);  // the S buffer may take the tile after next
-      const bool blk = t >= n_ctx;
-      if (blk && qd == 0) {  // add the lo key rows (lanes 16..31) to their hi rows
-#pragma unroll
-        for (int q = 0; q < 64; ++q) s[q] += __shfl_down_sync(0xffffffffu, s[q], 16);
-      }
-      // visibility: context key at position p is seen by rows i <= i_max; block key kr by
-      // rows i with the block rule
-      int i_max = -1;
-      if (!blk) {
+      // hide the keys a query's block row may not see (-inf)
+      if (t < n_ctx) {
         const int slot = (t_begin + t) * kTileKeys + kr;
-        if (slot < n_slots) {
-          const long long p = slot_position(F, cap, slot);
-          if (a.window > 0) {
-            const long long m = p - (F - a.window + 1);
-            i_max = m < 0 ? -1 : (m > W ? W : static_cast<int>(m));
-          } else {
-            i_max = W;
-          }
+        int vis_rows;  // this key is seen by block rows 0 .. vis_rows-1
+        if (slot >= n_slots) {
+          vis_rows = 0;
+        } else if (a.window <= 0) {
+          vis_rows = W;
+        } else {  // position p sits in the window of row i iff p >= F + i - window + 1
+          int d = slot - base_slot;
+          if (d < 0) d += cap;
+          const int m = F >= cap ? d + a.window - 1 - cap : slot - static_cast<int>(F) + a.window - 1;
+          vis_rows = m < 0 ? 0 : (m >= W ? W : m + 1);
         }
-      }
-      bool need = false;
-      {
-        int i = 0;
+        if (vis_rows == 0) {
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          bool vis;
-          if (!blk)
-            vis = q < R && i <= i_max;
-          else
-            vis = q < R && kr < W && qd == 0 && (!a.causal || kr <= i) &&
-                  (a.window <= 0 || abs(kr - i) < a.window);
-          const float x = vis ? s[q] * sl2 : -INFINITY;
-          s[q] = x;
-          need |= x > m_ref[q] + 8.f;
-          i = (i + 1 == W) ? 0 : i + 1;
+          for (int j = 0; j < 32; ++j) s[j] = -INFINITY;
+        } else if (vis_rows < W) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = q_row[h * 32 + j] < vis_rows ? s[j] : -INFINITY;
+        }
+      } else {  // the block tile: lanes 16..31 of quarter 0 hold the lo key rows
+        if (qd == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] += __shfl_down_sync(0xffffffffu, s[j], 16);
+        }
+        const bool key_ok = qd == 0 && kr < W;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int i = q_row[h * 32 + j];
+          const bool vis = key_ok && i < W && (!a.causal || kr <= i) &&
+                           (a.window <= 0 || abs(kr - i) < a.window);
+          s[j] = vis ? s[j] : -INFINITY;
         }
       }
-      need = named_bar_or(kBarVote, kSoftThreads, need);
-      // the previous tile's P.V has finished: the probability tile is free, O^T is stable
-      ok = t == 0 || mbar_wait(pvdone, (t - 1) & 1);
-      if (named_bar_or(kBarVote, kSoftThreads, !ok)) {
-        abort = true;
-        break;
-      }
-      if (need) {  // new reference maxima (exact over this tile), rescale l and O^T
-        float *scr = reinterpret_cast<float *>(sm + kOffP);  // free: the last P.V is done
-        table_store(scr, kr, s);
+      // the reference moves when a tile exceeds it by more than 2^8 (s stays the raw score:
+      // before the first reference s - m_ref would lose s against the start value)
+      float dmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dmax = fmaxf(dmax, s[j] - mr[j]);
+      const bool need = named_bar_or(kBarVote, kSoftThreads, dmax > 8.f);
+      if (need) {  // new reference maxima (exact over this tile): rescale l and O^T
+        // column maxima: warp reduction on order-preserving integer images, then the
+        // four warps of this query half through shared memory
+        int mine = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          int bits = __float_as_int(s[j]);
+          bits = bits >= 0 ? bits : bits ^ 0x7FFFFFFF;
+          const int wmax = __reduce_max_sync(0xffffffffu, bits);
+          mine = lane == j ? wmax : mine;
+        }
+        mine = mine >= 0 ? mine : mine ^ 0x7FFFFFFF;
+        red_max[qd * 64 + h * 32 + lane] = __int_as_float(mine);
+        if (t > 0) wait_ok(pvdone, (t - 1) & 1);  // O^T stable before it is rescaled
         named_bar(kBarSoft, kSoftThreads);
         if (st_id < 64) {
-          const float tm = table_column<true>(scr, st_id);
-          const float m_old = m_ref[st_id], m_new = fmaxf(m_old, tm);
-          alpha[st_id] = m_new == -INFINITY ? 1.f : exp2f(m_old - m_new);
-          m_ref[st_id] = m_new;
+          const float tm = fmaxf(fmaxf(red_max[st_id], red_max[64 + st_id]),
+                                 fmaxf(red_max[128 + st_id], red_max[192 + st_id]));
+          const float m_old = m_ref_s[st_id], m_new = fmaxf(m_old, tm);
+          alpha[st_id] = exp2f(m_old - m_new);
+          m_ref_s[st_id] = m_new;
         }
         named_bar(kBarSoft, kSoftThreads);
+        const float *arow = alpha + h * 32;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) lsum[q] *= alpha[q];
-        if (t > 0) {  // O^T row kr: columns c and c + 64 belong to query c
+        for (int j = 0; j < 32; ++j) {
+          mr[j] = m_ref_s[h * 32 + j];
+          lsum[j] *= arow[j];
+        }
+        if (t > 0 && __all_sync(0xffffffffu, *sabort == 0)) {  // O^T row kr, this half's columns
           tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+#pragma unroll 1
+          for (int part = 0; part < 2; ++part) {  // hi columns, then lo columns
+            const uint32_t ta = tmem + lane_off + kTmemO + part * 64 + h * 32;
             uint32_t o[32];
-            tmem_ld32_nowait(tmem + lane_off + kTmemO + c0, o);
+            tmem_ld32_nowait(ta, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[(c0 + j) & 63]);
-            tmem_st32(tmem + lane_off + kTmemO + c0, o);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * arow[j]);
+            tmem_st32(ta, o);
           }
           tmem_st_wait();
         }
+      } else if (t > 0) {
+        wait_ok(pvdone, (t - 1) & 1);  // the previous tile's P.V has read the P tile
       }
-      // probabilities: bf16 hi and lo halves, key row kr of the P^T tile
-      const bool dup = blk && qd == 0 && kr >= 16;  // block lo-key rows repeat rows 0..15
-      if (!dup) {
-        uint8_t *rowp = sm + kOffP + kr * 128;
+      // probabilities, bf16 hi and lo halves, key row kr of the P^T tile
+      const bool dup = t >= n_ctx && qd == 0 && kr >= 16;  // block lo-key rows repeat 0..15
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t hw[4], lw[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ph[4], pl[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q0 = c * 8 + 2 * e;
-            const float p0 = s[q0] == -INFINITY ? 0.f : exp2f(s[q0] - m_ref[q0]);
-            const float p1 = s[q0 + 1] == -INFINITY ? 0.f : exp2f(s[q0 + 1] - m_ref[q0 + 1]);
-            lsum[q0] += p0;
-            lsum[q0 + 1] += p1;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            const float2 hf = __bfloat1622float2(h);
-            hw[e] = *reinterpret_cast<const uint32_t *>(&h);
-            lw[e] = pack_bf16(p0 - hf.x, p1 - hf.y);
-          }
-          const uint32_t sw = static_cast<uint32_t>((c ^ (kr & 7)) << 4);
-          *reinterpret_cast<uint4 *>(rowp + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4 *>(rowp + kAtom + sw) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int j = c * 8 + 2 * e;
+          const float p0 = ex2_approx(s[j] - mr[j]), p1 = ex2_approx(s[j + 1] - mr[j + 1]);
+          lsum[j] += p0;
+          lsum[j + 1] += p1;
+          split_bf16x2(p0, p1, ph[e], pl[e]);
+        }
+        if (!dup) {
+          const uint32_t off = static_cast<uint32_t>(((h * 4 + c) ^ swz) << 4);
+          *reinterpret_cast<uint4 *>(prow + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4 *>(prow + kAtom + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
         }
       }
-      if (blk && qd == 0) {
+      if (t >= n_ctx && qd == 0) {
         __syncwarp();
-        if (dup) {  // same swizzle phase: kr & 7 == (kr - 16) & 7
+        if (dup) {  // kr & 7 == (kr - 16) & 7: the same swizzle positions
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t o = static_cast<uint32_t>(c << 4);
-            *reinterpret_cast<uint4 *>(sm + kOffP + kr * 128 + o) =
-                *reinterpret_cast<const uint4 *>(sm + kOffP + (kr - 16) * 128 + o);
-            *reinterpret_cast<uint4 *>(sm + kOffP + kAtom + kr * 128 + o) =
-                *reinterpret_cast<const uint4 *>(sm + kOffP + kAtom + (kr - 16) * 128 + o);
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t off = static_cast<uint32_t>(((h * 4 + c) ^ swz) << 4);
+            *reinterpret_cast<uint4 *>(prow + off) = *reinterpret_cast<const uint4 *>(prow - 16 * 128 + off);
+            *reinterpret_cast<uint4 *>(prow + kAtom + off) =
+                *reinterpret_cast<const uint4 *>(prow - 16 * 128 + kAtom + off);
           }
         }
       }
@@ -624,46 +631,42 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       tc_fence_before();
       mbar_arrive(pfull);
     }
-    if (!abort && nt > 0) {
-      const bool ok = mbar_wait(pvdone, (nt - 1) & 1);
-      abort = named_bar_or(kBarVote, kSoftThreads, !ok);
-    }
+    if (nt > 0) wait_ok(pvdone, (nt - 1) & 1);
+    const bool abort = named_bar_or(kBarVote, kSoftThreads, *sabort != 0);
     if (!abort) {
-      // row sums of the 128 threads' partial sums
-      float *scr = reinterpret_cast<float *>(sm + kOffP);  // free: the last P.V is done
-      table_store(scr, kr, lsum);
+      // row sums: butterfly over the warp (lane j ends with query h*32 + j), then the four
+      // warps of this query half
+      bfly_sum32(lsum, lane);
+      red_max[qd * 64 + h * 32 + lane] = lsum[0];
       named_bar(kBarSoft, kSoftThreads);
-      if (st_id < 64) l_fin[st_id] = table_column<false>(scr, st_id);
+      if (st_id < 64)
+        l_fin[st_id] = (red_max[st_id] + red_max[64 + st_id]) + (red_max[128 + st_id] + red_max[192 + st_id]);
       named_bar(kBarSoft, kSoftThreads);
-      // O^T row kr (output dim d = kr): query q is columns q and q + 64
-      float o[64];
+      // O^T row kr (output dim d = kr): query q sits in columns q and q + 64
+      float o[32];
       if (nt > 0) {
         tc_fence_after();
-        tmem_pair_sum<0>(tmem + lane_off + kTmemO, o);
-        tmem_pair_sum<32>(tmem + lane_off + kTmemO, o);
+        tmem_pair32(tmem + lane_off + kTmemO + h * 32, o);
       } else {
 #pragma unroll
-        for (int q = 0; q < 64; ++q) o[q] = 0.f;
+        for (int j = 0; j < 32; ++j) o[j] = 0.f;
       }
       const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + g;
       if (a.n_splits == 1) {
         if (kr < D) {
           __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-          int hh = 0, i = 0;
 #pragma unroll
-          for (int q = 0; q < 64; ++q) {
+          for (int j = 0; j < 32; ++j) {
+            const int q = h * 32 + j;
             if (q < R) {
+              const int hh = q / W, i = q - hh * W;
               const float L = l_fin[q];
-              const float y = L > 0.f ? o[q] / L : 0.f;
+              const float y = L > 0.f ? o[j] / L : 0.f;
               const size_t idx = (static_cast<size_t>(b) * W + i) * a.n_q_heads * D +
                                  static_cast<size_t>(g * G + hh) * D + kr;
-              const __nv_bfloat16 h = __float2bfloat16_rn(y);
-              out[idx] = h;
-              if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(h));
-            }
-            if (++i == W) {
-              i = 0;
-              ++hh;
+              const __nv_bfloat16 hv = __float2bfloat16_rn(y);
+              out[idx] = hv;
+              if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(hv));
             }
           }
         }
@@ -671,14 +674,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         float *po = a.part_o + (bh * a.n_splits + split) * kAttRows * D;
         if (kr < D) {
 #pragma unroll
-          for (int q = 0; q < 64; ++q) po[static_cast<size_t>(q) * D + kr] = o[q];
+          for (int j = 0; j < 32; ++j) po[static_cast<size_t>(h * 32 + j) * D + kr] = o[j];
         }
         if (st_id < 64)
-          a.part_ml[(bh * a.n_splits + split) * kAttRows + st_id] = make_float2(m_ref[st_id], l_fin[st_id]);
+          a.part_ml[(bh * a.n_splits + split) * kAttRows + st_id] = make_float2(m_ref_s[st_id], l_fin[st_id]);
         // merge the splits in this launch: every split of (b, g) counts itself once its
         // partial is stored, waits (bounded) for the others, then merges its share of the
-        // rows.  The launch has at most one CTA per SM, so all splits are resident together,
-        // and each stores its partial before it waits.
+        // rows.  The launch has at most one CTA per SM, so all splits
+        // are resident together, and each stores its partial before it waits.
         unsigned *arrived = a.counters + bh;
         unsigned *done = a.counters + static_cast<size_t>(a.B) * a.n_kv_heads + bh;
         __threadfence();
@@ -691,26 +694,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (!named_bar_or(kBarVote, kSoftThreads, !wok)) {
           const int rp = (R + a.n_splits - 1) / a.n_splits;
           const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
-          if (a.n_splits <= kFewSplits)
-            combine_rows_few<__nv_bfloat16, D, kFewSplits, 2>(a, b, g, r0, r1, warp - 2, lane);
-          else
-            combine_rows<__nv_bfloat16, D>(a, b, g, r0, r1, warp - 2, lane,
-                                           reinterpret_cast<float (*)[D + 4]>(sm + kOffP));
+          merge_splits<D>(a, b, g, r0, r1, st_id, reinterpret_cast<float *>(sm + kOffP));
           named_bar(kBarSoft, kSoftThreads);
           if (st_id == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
             *arrived = 0u;  // every split is past its wait: ready for the next launch
             *done = 0u;
           }
+        } else {
+          *sabort = 1;
         }
       }
     }
-    if (abort) *sabort = 1;
   }
   tc_fence_before();
   __syncthreads();
   if (*sabort && warp == 0 && lane == 0) {
     // a wait gave up: let the loads still in flight land before the CTA exits (bounded)
-    for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&full[t & 1], (t >> 1) & 1);
+    for (int t = max(0, issued_k - 2); t < issued_k; ++t) mbar_wait(&full_k[t & 1], (t >> 1) & 1);
+    for (int t = max(0, issued_v - 2); t < issued_v; ++t) mbar_wait(&full_v[t & 1], (t >> 1) & 1);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -824,6 +825,7 @@ size_t attention_ml_count(int B, int n_kv_heads, int n_splits) {
 }
 int attention_rows_max() { return kAttRows; }
 int attention_tile_keys() { return kTileKeys; }
+int attention_max_splits() { return kMaxMergeSplits; }
 
 template <int D>
 static cudaError_t launch_tc(const AttMaps &m, const AttArgs &a, cudaStream_t stream) {

@@ -22,6 +22,7 @@ struct AttArgs {
   float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
   unsigned *counters;   // [2][B * Hkv] split arrival / done counters (start at 0)
   int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
+  int block_split;      // 1: the last split takes only the block's own keys
   int n_guard;          // context positions >= F - n_guard may be written by this round's
                         // catch-up (read only after the previous kernel has finished)
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
@@ -31,7 +32,8 @@ struct AttArgs {
 size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim);
 size_t attention_ml_count(int B, int n_kv_heads, int n_splits);
 int attention_rows_max();
-int attention_tile_keys();  // context keys per tile of the bf16 kernel
+int attention_tile_keys();    // context keys per tile of the bf16 kernel
+int attention_max_splits();   // key splits the bf16 kernel merges at most
 std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream);
 
 // theta^(-2j/D) for j < D/2, computed on the host in double precision.
@@ -124,7 +126,7 @@ struct HeadSeg {
   const void *norm;  // [D] gain (query/key segments)
   void *dst;
   size_t lo_off;     // != 0: also store the rounding residual at dst + lo_off
-  int f16;           // store fp16 (the attention's fp16 operands) instead of the config type
+  float scale;       // multiplies the stored values (0 stands for 1)
 };
 // Rows row0 .. row0+rows-1 take segments seg0 .. seg0+n_segs-1 (total_heads heads in all).
 struct HeadGroup {

@@ -345,16 +345,9 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
     if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
     o = ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D;
   }
-  if (sg.f16) {
-    __half *dh = static_cast<__half *>(sg.dst) + o + d0;
-    bool bad = false;
+  if (sg.scale != 0.f) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      bad |= f16_out_of_range(v[e]);
-      dh[e] = __float2half_rn(v[e]);
-    }
-    flag_f16_range(bad);
-    return;
+    for (int e = 0; e < E; ++e) v[e] *= sg.scale;
   }
   T *dst = static_cast<T *>(sg.dst) + o + d0;
 #pragma unroll

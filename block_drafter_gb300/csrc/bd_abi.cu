@@ -191,25 +191,19 @@ struct Carve {
 // When the context chunks are short (at most two 64-key blocks per split), the block's own
 // keys -- a separate hi+lo pass -- would double the last split's work and every split
 // waits for it in the merge: give them a split of their own.
-// Key splits of a layer's bf16 attention: one CTA per (split, KV head, request) and one
-// CTA per SM (the splits of a head merge inside the launch, so all of them must be
-// resident together), at most one split per 128-slot tile of the ring, plus one split for
-// the block's own keys alone when that still fits (att_block_split).
-int att_ctx_splits(const bd_config *c, int l, int B, int sms) {
+// Key splits of a layer's bf16 attention (one CTA per split, KV head and request; the
+// splits of a head form one cluster and merge through distributed shared memory, so the
+// grid may exceed one wave): enough splits to fill the SMs once (one CTA per SM), more
+// when a head's ring holds over 16 tiles of 128 slots, at most one split per tile and at
+// most the portable cluster size.
+int att_splits(const bd_config *c, int l, int B, int W, int sms) {
+  (void)W;
   const int cap = c->ring_capacity[l];
   const int tiles = (cap + attention_tile_keys() - 1) / attention_tile_keys();
-  int s = sms / (B * c->n_kv_heads);
+  int s = std::max(sms / (B * c->n_kv_heads), (tiles + 15) / 16);
   if (s < 1) s = 1;
   if (s > attention_max_splits()) s = attention_max_splits();
   return s < tiles ? s : tiles;
-}
-bool att_block_split(const bd_config *c, int l, int B, int sms) {
-  const int s = att_ctx_splits(c, l, B, sms);
-  return s + 1 <= attention_max_splits() && (s + 1) * B * c->n_kv_heads <= sms;
-}
-int att_splits(const bd_config *c, int l, int B, int W, int sms) {
-  (void)W;
-  return att_ctx_splits(c, l, B, sms) + (att_block_split(c, l, B, sms) ? 1 : 0);
 }
 int att_max_keys(const bd_config *c, int l, int W) {
   const int cap = c->ring_capacity[l];
@@ -235,12 +229,11 @@ size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + ti
 
 struct RoundWs {
   GemmWs g;
-  unsigned *att_cnt;  // [2][B * Hkv] attention split counters, right after g.counters
-  float *x, *z, *pre, *r, *part_o, *qkv_raw, *feat, *kv_raw;
+  float *x, *z, *pre, *r, *qkv_raw, *feat, *kv_raw;
   float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
-  unsigned *br_bar;    // [L][5] fused-bridge barrier counters (3 used), right after att_cnt
+  unsigned *br_bar;    // [L][5] fused-bridge barrier counters (3 used), right after g.counters
   float *zpart, *sspart, *zsq;  // fused-bridge partial sums
-  float2 *rope, *part_ml;
+  float2 *rope;
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
 int pad16(int n) { return (n + 15) / 16 * 16; }
@@ -281,7 +274,6 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_
   size_t tiles = round_max_tiles(c, T, Tq);
   if (n_pend > 0 && !fuse) tiles = std::max(tiles, mat_max_tiles(c, n_pend));
   carve_gemm(cv, w.g, 2 * std::max(std::min(TQ, 128), pad16(std::min(n_pend, 128))), tiles, sms);
-  w.att_cnt = cv.take<unsigned>(2 * static_cast<size_t>(B) * c->n_kv_heads);
   const BridgePlan bp = c->code_width > 0 && c->conv_group == 0
                             ? bridge_plan(c->dtype, T, H, c->code_width, c->msg_width, sms)
                             : BridgePlan{};
@@ -308,14 +300,6 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_
   w.att = cv.take<char>(static_cast<size_t>(2 * TP) * QD * e);
   w.hmid = cv.take<char>(static_cast<size_t>(2 * TP) * c->ffn * e);
   w.rope = cv.take<float2>(static_cast<size_t>(T + n_pend) * (c->head_dim / 2));
-  size_t po = 0, pm = 0;
-  for (int l = 0; l < c->n_layers; ++l) {
-    const int s = att_splits(c, l, B, W, sms);
-    po = std::max(po, attention_partial_floats(B, c->n_kv_heads, s, c->head_dim));
-    pm = std::max(pm, attention_ml_count(B, c->n_kv_heads, s));
-  }
-  w.part_o = cv.take<float>(po);
-  w.part_ml = cv.take<float2>(pm);
   if (c->conv_group > 0) {
     const size_t nd = static_cast<size_t>(4) * H / c->conv_group;
     w.cdelta_a = cv.take<float>(static_cast<size_t>(Tq) * nd);
@@ -644,8 +628,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   const int G = cfg->n_q_heads / cfg->n_kv_heads;
   if (cfg->dtype == BD_BF16 && G * W > attention_rows_max())
     return fail(BD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*(n_masks+1) must be <= 64");
-  if (cfg->dtype == BD_BF16 && static_cast<long long>(B) * cfg->n_kv_heads > num_sms())
-    return fail(BD_ERR_UNSUPPORTED, "B * n_kv_heads must not exceed the number of SMs");
   for (int l = 0; l < cfg->n_layers; ++l)
     if (cfg->dtype == BD_F32 && att_max_keys(cfg, l, W) > 48 * 1024)
       return fail(BD_ERR_UNSUPPORTED, "fp32 attention supports at most 49152 keys per layer");
@@ -671,13 +653,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   auto lo = [&](int K) -> size_t { return split ? static_cast<size_t>(TP) * K : 0; };
 
   // S3: block input rows and the RoPE table of positions F_b + i
-  // the first kernel clears the GEMM tile counters and the attention split counters
-  // (carved back to back)
-  // (and the fused bridge's barrier counters, carved right after them)
-  const ZeroSpan zero{rw.g.counters,
-                      rw.br_bar ? static_cast<size_t>(rw.br_bar - rw.g.counters) + 5 * cfg->n_layers
-                                : static_cast<size_t>(rw.att_cnt - rw.g.counters) +
-                                      2 * static_cast<size_t>(B) * cfg->n_kv_heads};
+  // the first kernel clears the GEMM tile counters (and the fused bridge's barrier
+  // counters, carved right after them)
+  const ZeroSpan zero{rw.g.counters, rw.br_bar ? static_cast<size_t>(rw.br_bar - rw.g.counters) +
+                                                     5 * cfg->n_layers
+                                               : 2 * rw.g.n_counters};
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
                            cfg->mask_token_id, rw.x, rw.rope, D / 2, freq,
                            n_pend > 0 ? pending->pos : nullptr, n_pend, zero, s));
@@ -800,9 +780,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.blk_v = rw.vblk;
       a.out = rw.att;
       a.frontier = frontier;
-      a.part_o = rw.part_o;
-      a.part_ml = rw.part_ml;
-      a.counters = rw.att_cnt;
       a.B = B;
       a.W = W;
       a.n_q_heads = cfg->n_q_heads;
@@ -812,7 +789,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.cap = cfg->ring_capacity[l];
       a.causal = cfg->block_mask == BD_BLOCK_CAUSAL ? 1 : 0;
       a.n_splits = dt == BD_BF16 ? att_splits(cfg, l, B, W, sms) : 1;
-      a.block_split = dt == BD_BF16 && att_block_split(cfg, l, B, sms) ? 1 : 0;
       a.n_guard = n_pend > 0 ? kMaxPendPerReq : 0;
       a.max_keys = att_max_keys(cfg, l, W);
       a.q_lo = split ? static_cast<size_t>(T) * QD : 0;

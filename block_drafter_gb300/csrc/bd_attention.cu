@@ -45,6 +45,7 @@ constexpr int kAttThreads = 320;     // producer warp, MMA warp, eight softmax w
 constexpr int kSoftThreads = 256;
 constexpr int kBarSoft = 1;          // named barrier of the softmax warps
 constexpr int kBarVote = 2;          // their votes (barrier with an OR reduction)
+constexpr int kMaxSplits = 8;        // key splits of one (request, KV head): one portable cluster
 constexpr uint32_t kAtom = 16384;    // 128 rows x 128 bytes (64 bf16 of each row)
 // shared memory (offsets from the 1024-aligned base); every tile is [2 atoms][128 rows][128 B]
 constexpr uint32_t kOffQ = 0;                       // rows 0..63 hi, 64..127 lo queries
@@ -84,103 +85,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
   hi = hv;
   lo = lv;
 }
-// Merge of the splits' partials (O, m, l) of query rows r0 .. r1-1 of (request b, KV head
-// g) by the 256 softmax threads:
-//   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max over splits with l_s > 0.
-// The (m, l) of every (split, row) are loaded first, then each thread takes float4 chunks of
-// the rows and issues up to 16 partial loads before any arithmetic (one round trip to L2 per
-// pass; one pass when chunks x splits fit).  The partials were written by other CTAs of the launch: read through
-// L2.  Splits are added in index order.  scr: shared scratch of 3 * kMaxMergeSplits * 64 + 64
-// floats.
-constexpr int kMaxMergeSplits = 32;
-template <int D>
-__device__ void merge_splits(const AttArgs &a, int b, int g, int r0, int r1, int tid, float *scr) {
-  const int S = a.n_splits, nr = r1 - r0;
-  const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + g;
-  const float *po = a.part_o + bh * S * kAttRows * D;
-  const float2 *pml = a.part_ml + bh * S * kAttRows;
-  float *sm_m = scr, *sm_l = scr + kMaxMergeSplits * 64, *sm_w = sm_l + kMaxMergeSplits * 64;
-  float *inv_l = sm_w + kMaxMergeSplits * 64;
-  for (int i = tid; i < S * nr; i += kSoftThreads) {
-    const int sp = i / nr, r = i - sp * nr;
-    const float2 ml = __ldcg(pml + sp * kAttRows + r0 + r);
-    sm_m[sp * 64 + r] = ml.x;
-    sm_l[sp * 64 + r] = ml.y;
-  }
-  named_bar(kBarSoft, kSoftThreads);
-  if (tid < nr) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < S; ++sp)
-      if (sm_l[sp * 64 + tid] > 0.f) M = fmaxf(M, sm_m[sp * 64 + tid]);
-    float L = 0.f;
-    for (int sp = 0; sp < S; ++sp) {
-      const float l = sm_l[sp * 64 + tid];
-      const float w = l > 0.f ? exp2f(sm_m[sp * 64 + tid] - M) : 0.f;
-      sm_w[sp * 64 + tid] = w;
-      L += w * l;
-    }
-    inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
-  }
-  named_bar(kBarSoft, kSoftThreads);
-  constexpr int C4 = D / 4;  // float4 chunks per row
-  constexpr int kLoads = 16;  // partial loads in flight per thread
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-  const int total = nr * C4;
-  const int SB = min(S, kLoads);                  // splits per batch of loads
-  const int per = max(1, min(4, kLoads / SB));    // chunks per thread and pass
-  for (int c0 = tid; c0 < total; c0 += kSoftThreads * per) {
-    float4 acc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < S; sp0 += SB) {
-      // every load of the batch first: chunk c0 + k*256 of split sp0 + j in v[k*SB + j]
-      float4 v[kLoads];
-#pragma unroll
-      for (int i = 0; i < kLoads; ++i) {
-        const int k = i / SB, sp = sp0 + i - k * SB;
-        const int c = c0 + k * kSoftThreads;
-        if (k < per && c < total && sp < S) {
-          const int r = c / C4, d4 = c - r * C4;
-          v[i] = __ldcg(reinterpret_cast<const float4 *>(po + (static_cast<size_t>(sp) * kAttRows + r0 + r) * D) + d4);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kLoads; ++i) {
-        const int k = i / SB, sp = sp0 + i - k * SB;
-        const int c = c0 + k * kSoftThreads;
-        if (k < per && c < total && sp < S) {
-          const float w = sm_w[sp * 64 + c / C4];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            if (kk == k) {
-              acc[kk].x += w * v[i].x;
-              acc[kk].y += w * v[i].y;
-              acc[kk].z += w * v[i].z;
-              acc[kk].w += w * v[i].w;
-            }
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int c = c0 + k * kSoftThreads;
-      if (k >= per || c >= total) break;
-      const int r = c / C4, d4 = c - r * C4;
-      const float4 acck = acc[k];
-      const float il = inv_l[r];
-      const int q = r0 + r, hh = q / a.W, i = q - hh * a.W;
-      const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
-                         static_cast<size_t>(g * G + hh) * D + 4 * d4;
-      uint32_t hw[2], lw[2];
-      split_bf16x2(acck.x * il, acck.y * il, hw[0], lw[0]);
-      split_bf16x2(acck.z * il, acck.w * il, hw[1], lw[1]);
-      *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
-      if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
-    }
-  }
-}
-
 // Position of ring slot s of a request at frontier F (the ring holds [F - cap, F) when
 // F >= cap, else positions 0..F-1 at their own slots).
 __device__ __forceinline__ long long slot_position(long long F, int cap, int s) {
@@ -232,14 +136,15 @@ __device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm,
   // is fetched before waiting for the previous kernel.
   auto safe = [&](int t) {
     if (t >= n_ctx) return false;
-    const int s0 = (t_begin + t) * kTileKeys;
-    for (int j = 0; j < a.n_guard; ++j) {
-      const long long p = F - 1 - j;
-      if (p < 0) break;
-      const int slot = static_cast<int>(p % cap);
-      if (slot >= s0 && slot < s0 + kTileKeys) return false;
-    }
-    return true;
+    if (a.n_guard == 0) return true;
+    // guard positions [max(0, F - n_guard), F) occupy n consecutive slots from g0 (mod cap)
+    const long long p0 = F - a.n_guard > 0 ? F - a.n_guard : 0;
+    const int n = static_cast<int>(F - p0);
+    if (n >= cap) return false;
+    const int g0 = static_cast<int>(p0 % cap);
+    const int s0 = (t_begin + t) * kTileKeys, s1 = s0 + kTileKeys;  // the tile's slots [s0, s1)
+    const int e0 = g0 + n;                                          // guard slots [g0, e0) and,
+    return (e0 <= s0 || g0 >= s1) && (e0 - cap <= s0);             // wrapped, [0, e0 - cap)
   };
   int tk = 0, tv = 0;
   if (nt > 0 && safe(0)) {
@@ -363,6 +268,107 @@ __device__ __forceinline__ void bfly_sum32(float (&v)[32], int lane) {
   bfly_sum_step<2, 1>(v, lane);
 }
 
+// Final outputs of one thread (output dim kr, queries h*32 .. h*32+31) from unnormalised
+// sums o and row sums l: bf16 hi (and lo) planes, token-major [B*W][Hq*D].
+__device__ __forceinline__ void write_out(const AttArgs &a, int b, int g, int kr, int h,
+                                          const float *l, const float (&o)[32]) {
+  const int D = a.head_dim, W = a.W, G = a.n_q_heads / a.n_kv_heads, R = G * W;
+  if (kr >= D) return;
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int q = h * 32 + j;
+    if (q < R) {
+      const int hh = q / W, i = q - hh * W;
+      const float L = l[q];
+      const float y = L > 0.f ? o[j] / L : 0.f;
+      const size_t idx = (static_cast<size_t>(b) * W + i) * a.n_q_heads * D +
+                         static_cast<size_t>(g * G + hh) * D + kr;
+      const __nv_bfloat16 hv = __float2bfloat16_rn(y);
+      out[idx] = hv;
+      if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(hv));
+    }
+  }
+}
+
+// Merge of the cluster's partials (O, m, l) for query rows r0 .. r1-1 of (request b, KV
+// head g), by the 256 softmax threads of one CTA:
+//   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max over splits with l_s > 0,
+// reading split s's partial from CTA s of the cluster (distributed shared memory): its
+// [query][D] fp32 tile at kOffP and its per-query m, l.  Splits are added in rank order.
+// scr: local scratch of 3 * 8 * 64 + 64 floats.
+template <int D>
+__device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, int tid, uint8_t *sm,
+                              float *scr) {
+  constexpr int kMax = kMaxSplits;
+  const int S = a.n_splits, nr = r1 - r0;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  float *sm_m = scr, *sm_l = scr + kMax * 64, *sm_w = sm_l + kMax * 64, *inv_l = sm_w + kMax * 64;
+  const uint32_t ml_base = smem_u32(sm + kOffRed);       // m_ref[64], then alpha[64], l[64]
+  const uint32_t p_base = smem_u32(sm + kOffP);
+  for (int i = tid; i < S * nr; i += kSoftThreads) {
+    const int sp = i / nr, r = i - sp * nr;
+    const uint32_t rm = cluster_map(ml_base, static_cast<uint32_t>(sp));
+    sm_m[sp * 64 + r] = ld_cluster_f32(rm + (r0 + r) * 4);
+    sm_l[sp * 64 + r] = ld_cluster_f32(rm + (128 + r0 + r) * 4);
+  }
+  named_bar(kBarSoft, kSoftThreads);
+  if (tid < nr) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp)
+      if (sm_l[sp * 64 + tid] > 0.f) M = fmaxf(M, sm_m[sp * 64 + tid]);
+    float L = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+      const float l = sm_l[sp * 64 + tid];
+      const float w = l > 0.f ? exp2f(sm_m[sp * 64 + tid] - M) : 0.f;
+      sm_w[sp * 64 + tid] = w;
+      L += w * l;
+    }
+    inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
+  }
+  named_bar(kBarSoft, kSoftThreads);
+  constexpr int C4 = D / 4;  // float4 chunks per row
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+  // two chunks per pass, every remote load of the pass issued before any arithmetic
+  for (int c0 = tid; c0 < nr * C4; c0 += 2 * kSoftThreads) {
+    float4 v[2][kMax];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = c0 + k * kSoftThreads;
+      const int r = c / C4, d4 = c - r * C4;
+      const uint32_t off = static_cast<uint32_t>(((r0 + r) * D + 4 * d4) * 4);
+#pragma unroll
+      for (int sp = 0; sp < kMax; ++sp)
+        if (sp < S && c < nr * C4) v[k][sp] = ld_cluster_f4(cluster_map(p_base + off, static_cast<uint32_t>(sp)));
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+    const int c = c0 + k * kSoftThreads;
+    if (c >= nr * C4) break;
+    const int r = c / C4, d4 = c - r * C4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < kMax; ++sp)
+      if (sp < S) {
+        const float w = sm_w[sp * 64 + r];
+        acc.x += w * v[k][sp].x;
+        acc.y += w * v[k][sp].y;
+        acc.z += w * v[k][sp].z;
+        acc.w += w * v[k][sp].w;
+      }
+    const float il = inv_l[r];
+    const int q = r0 + r, hh = q / a.W, i = q - hh * a.W;
+    const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
+                       static_cast<size_t>(g * G + hh) * D + 4 * d4;
+    uint32_t hw[2], lw[2];
+    split_bf16x2(acc.x * il, acc.y * il, hw[0], lw[0]);
+    split_bf16x2(acc.z * il, acc.w * il, hw[1], lw[1]);
+    *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
+    if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
@@ -389,10 +395,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int cap = a.cap;
   const int n_slots = F < cap ? static_cast<int>(F > 0 ? F : 0) : cap;
   const int n_tiles = (n_slots + kTileKeys - 1) / kTileKeys;
-  // with block_split the last split takes only the block's own keys
-  const int ctx_splits = a.n_splits - (a.block_split ? 1 : 0);
-  const int per = (n_tiles + ctx_splits - 1) / ctx_splits;
-  const int t_begin = split < ctx_splits ? min(n_tiles, split * per) : n_tiles;
+  const int per = (n_tiles + a.n_splits - 1) / a.n_splits;
+  const int t_begin = min(n_tiles, split * per);
   const int n_ctx = min(n_tiles, t_begin + per) - t_begin;
   const bool do_block = split == a.n_splits - 1;
   const int nt = n_ctx + (do_block ? 1 : 0);
@@ -651,60 +655,25 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0.f;
       }
-      const size_t bh = static_cast<size_t>(b) * a.n_kv_heads + g;
       if (a.n_splits == 1) {
-        if (kr < D) {
-          __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+        write_out(a, b, g, kr, h, l_fin, o);
+      } else if (kr < D) {  // this split's partial, for the cluster's merge: [query][D] fp32
+        float *po = reinterpret_cast<float *>(sm + kOffP);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int q = h * 32 + j;
-            if (q < R) {
-              const int hh = q / W, i = q - hh * W;
-              const float L = l_fin[q];
-              const float y = L > 0.f ? o[j] / L : 0.f;
-              const size_t idx = (static_cast<size_t>(b) * W + i) * a.n_q_heads * D +
-                                 static_cast<size_t>(g * G + hh) * D + kr;
-              const __nv_bfloat16 hv = __float2bfloat16_rn(y);
-              out[idx] = hv;
-              if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(hv));
-            }
-          }
-        }
-      } else {
-        float *po = a.part_o + (bh * a.n_splits + split) * kAttRows * D;
-        if (kr < D) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) po[static_cast<size_t>(h * 32 + j) * D + kr] = o[j];
-        }
-        if (st_id < 64)
-          a.part_ml[(bh * a.n_splits + split) * kAttRows + st_id] = make_float2(m_ref_s[st_id], l_fin[st_id]);
-        // merge the splits in this launch: every split of (b, g) counts itself once its
-        // partial is stored, waits (bounded) for the others, then merges its share of the
-        // rows.  The launch has at most one CTA per SM, so all splits
-        // are resident together, and each stores its partial before it waits.
-        unsigned *arrived = a.counters + bh;
-        unsigned *done = a.counters + static_cast<size_t>(a.B) * a.n_kv_heads + bh;
-        __threadfence();
-        named_bar(kBarSoft, kSoftThreads);
-        bool wok = true;
-        if (st_id == 0) {
-          atomicAdd(arrived, 1u);
-          wok = wait_count(arrived, static_cast<unsigned>(a.n_splits), kWaitLimitNs, 0);
-        }
-        if (!named_bar_or(kBarVote, kSoftThreads, !wok)) {
-          const int rp = (R + a.n_splits - 1) / a.n_splits;
-          const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
-          merge_splits<D>(a, b, g, r0, r1, st_id, reinterpret_cast<float *>(sm + kOffP));
-          named_bar(kBarSoft, kSoftThreads);
-          if (st_id == 0 && atomicAdd(done, 1u) == static_cast<unsigned>(a.n_splits - 1)) {
-            *arrived = 0u;  // every split is past its wait: ready for the next launch
-            *done = 0u;
-          }
-        } else {
-          *sabort = 1;
-        }
+        for (int j = 0; j < 32; ++j) po[(h * 32 + j) * D + kr] = o[j];
       }
     }
+  }
+  if (a.n_splits > 1) {
+    // the splits of (b, g) form one cluster: merge their partials through distributed
+    // shared memory (every thread of every CTA passes both cluster barriers)
+    cluster_sync();
+    if (warp >= 2) {
+      const int rp = (R + a.n_splits - 1) / a.n_splits;
+      const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
+      merge_cluster<D>(a, b, g, r0, r1, tid - 64, sm, reinterpret_cast<float *>(sm + kOffK));
+    }
+    cluster_sync();  // no CTA leaves while the others still read its partial
   }
   tc_fence_before();
   __syncthreads();
@@ -817,15 +786,9 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(const __grid_constan
   }
 }
 
-size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim) {
-  return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows * head_dim;
-}
-size_t attention_ml_count(int B, int n_kv_heads, int n_splits) {
-  return static_cast<size_t>(B) * n_kv_heads * n_splits * kAttRows;
-}
 int attention_rows_max() { return kAttRows; }
 int attention_tile_keys() { return kTileKeys; }
-int attention_max_splits() { return kMaxMergeSplits; }
+int attention_max_splits() { return kMaxSplits; }
 
 template <int D>
 static cudaError_t launch_tc(const AttMaps &m, const AttArgs &a, cudaStream_t stream) {
@@ -837,8 +800,8 @@ static cudaError_t launch_tc(const AttMaps &m, const AttArgs &a, cudaStream_t st
     if (e != cudaSuccess) return e;
     set = true;
   }
-  return launch_pdl(attention_tc_kernel<D>, dim3(a.n_splits, a.n_kv_heads, a.B), dim3(kAttThreads),
-                    kAttSmem, stream, m, a);
+  return launch_pdl_cluster(attention_tc_kernel<D>, dim3(a.n_splits, a.n_kv_heads, a.B),
+                            dim3(kAttThreads), kAttSmem, stream, a.n_splits, m, a);
 }
 
 std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {

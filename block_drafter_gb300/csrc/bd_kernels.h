@@ -18,22 +18,16 @@ struct AttArgs {
   const void *blk_v;
   void *out;            // [B*W, Hq*D] attention output (config dtype)
   const int64_t *frontier;  // [B]
-  float *part_o;        // [B, Hkv, n_splits, 64, D] fp32 unnormalised partial outputs
-  float2 *part_ml;      // [B, Hkv, n_splits, 64] (running max in log2 units, sum)
-  unsigned *counters;   // [2][B * Hkv] split arrival / done counters (start at 0)
   int B, W, n_q_heads, n_kv_heads, head_dim, window, cap, causal, n_splits, max_keys;
-  int block_split;      // 1: the last split takes only the block's own keys
   int n_guard;          // context positions >= F - n_guard may be written by this round's
                         // catch-up (read only after the previous kernel has finished)
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
                                 // (q and blk lo planes directly follow their hi planes)
 };
 
-size_t attention_partial_floats(int B, int n_kv_heads, int n_splits, int head_dim);
-size_t attention_ml_count(int B, int n_kv_heads, int n_splits);
 int attention_rows_max();
 int attention_tile_keys();    // context keys per tile of the bf16 kernel
-int attention_max_splits();   // key splits the bf16 kernel merges at most
+int attention_max_splits();   // key splits (one cluster) of a head at most
 std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream);
 
 // theta^(-2j/D) for j < D/2, computed on the host in double precision.

@@ -544,23 +544,20 @@ __device__ __forceinline__ void load_row_scales(const GemmArgs &p, int tile_tok0
 }
 
 // Split tiles.  Every CTA that computed part of a tile stores its fp32 partial (layout
-// [LW columns][128 rows]) in its own slot and counts itself on the tile's counter.  After
-// its mainloop each contributor waits until all n have arrived and then sums its share
-// of the tile's 16-column chunks (chunk k belongs to the contributor k mod n) over all n
-// partials, in CTA order, so results do not depend on which CTA got there first.  Every
-// contributor of a tile waits only for partials that the others write before their own
-// waits, and all CTAs of a launch are resident at once (one per SM), so the waits end.
-struct FixupStage {
-  uint8_t *base;     // stage area (the pipeline's A and B buffers, idle after the mainloop)
-  int pieces;        // 8 KB pieces it holds
-  uint64_t *bar;     // completion barrier of the piece loads
-  uint32_t phase;
-};
+// [LW columns][128 rows], straight from registers: a warp writes 128 contiguous bytes per
+// column) in its own slot and counts itself on the tile's counter.  After its mainloop each
+// contributor waits until all n have arrived and then sums its share of the tile's
+// 16-column chunks (chunk k belongs to the contributor k mod n) over all n partials, in CTA
+// order, so results do not depend on which CTA got there first.  The partial values a
+// thread adds (its row, its columns of the chunk) are loaded straight from L2, up to
+// kFixLoads at a time before any of them is used.  Every contributor of a tile waits only
+// for partials that the others write before their own waits, and all CTAs of a launch are
+// resident at once (one per SM), so the waits end.
+constexpr int kFixLoads = 32;
 
 template <typename T, int EPI>
 __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, const EpiPos &ps,
-                           FixupStage &fs, EpiSmem &es, volatile int *sabort) {
-  constexpr uint32_t kPiece = 16 * kBM * 4;
+                           EpiSmem &es, volatile int *sabort) {
   const long long U = p.units;
   const int P = p.n_ctas;
   const int LW = p.ln;
@@ -577,71 +574,42 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
   if (my_chunks > 0) {
     if (et == 0) {
       if (!wait_count(arrived, static_cast<unsigned>(n))) *sabort = 1;
-      fence_proxy_async_global();
     }
     named_bar(1, kEpiThreads);
     if (*sabort) return false;
     if (EPI == EPI_INJECT) load_row_scales(p, n_tile * LW, LW, et, es);
-    // Issue the loads of as many whole chunks (n partial pieces each) as the stage area
-    // holds, wait once, then sum and emit them; a tile with more partials than pieces
-    // takes several rounds per chunk.
-    auto load = [&](int k, int c0, int cn, int slot0) {
-      const uint64_t pol = policy_evict_first();
-      for (int i = 0; i < cn; ++i) {
-        const int c = c_first + c0 + i;
-        const int cslot = (static_cast<int>(unit_begin(U, P, c, p.grain) / p.kb) == tile) ? 0 : 1;
-        const float *src = p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
-                           static_cast<size_t>(k) * 16 * kBM;
-        bulk_load(fs.base + static_cast<size_t>(slot0 + i) * kPiece, src, kPiece, fs.bar, pol);
-      }
+    // this thread's first value of chunk k in contributor i's partial
+    auto src = [&](int i, int k) -> const float * {
+      const int c = c_first + i;
+      const int cslot = (static_cast<int>(unit_begin(U, P, c, p.grain) / p.kb) == tile) ? 0 : 1;
+      return p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
+             static_cast<size_t>(k * 16 + ps.c0) * kBM + ps.r;
     };
-    auto add = [&](float (&acc)[kCW], int slot0, int cn) {
-      for (int i = 0; i < cn; ++i) {
-        const float *src =
-            reinterpret_cast<const float *>(fs.base + static_cast<size_t>(slot0 + i) * kPiece);
+    // one chunk at a time (one call site of the emit code: it is cold, once-per-tile code);
+    // the contributors' values of a chunk are loaded G at a time before they are added
+    constexpr int G = kFixLoads / kCW;
+    for (int j = 0; j < my_chunks; ++j) {
+      const int k = me + j * n;
+      float acc[kCW];
 #pragma unroll
-        for (int jj = 0; jj < kCW; ++jj) acc[jj] += src[(ps.c0 + jj) * kBM + ps.r];
-      }
-    };
-    if (n <= fs.pieces) {
-      const int per_batch = fs.pieces / n;
-      for (int b0 = 0; b0 < my_chunks; b0 += per_batch) {
-        const int bn = min(per_batch, my_chunks - b0);
-        if (et == 0) {
-          mbar_arrive_expect_tx(fs.bar, static_cast<uint32_t>(bn * n) * kPiece);
-          for (int j = 0; j < bn; ++j) load(me + (b0 + j) * n, 0, n, j * n);
-        }
-        if (!mbar_wait(fs.bar, fs.phase)) return false;
-        fs.phase ^= 1u;
-        for (int j = 0; j < bn; ++j) {
-          const int k = me + (b0 + j) * n;
-          float acc[kCW];
+      for (int jj = 0; jj < kCW; ++jj) acc[jj] = 0.f;
+      for (int i0 = 0; i0 < n; i0 += G) {
+        float v[G][kCW];
 #pragma unroll
-          for (int jj = 0; jj < kCW; ++jj) acc[jj] = 0.f;
-          add(acc, j * n, n);
-          emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, ps, acc, es);
-        }
-        named_bar(1, kEpiThreads);  // every thread is done with the pieces before they are refilled
-      }
-    } else {
-      for (int j = 0; j < my_chunks; ++j) {
-        const int k = me + j * n;
-        float acc[kCW];
+        for (int g = 0; g < G; ++g)
+          if (i0 + g < n) {
+            const float *sp = src(i0 + g, k);
 #pragma unroll
-        for (int jj = 0; jj < kCW; ++jj) acc[jj] = 0.f;
-        for (int c0 = 0; c0 < n; c0 += fs.pieces) {
-          const int cn = min(fs.pieces, n - c0);
-          if (et == 0) {
-            mbar_arrive_expect_tx(fs.bar, static_cast<uint32_t>(cn) * kPiece);
-            load(k, c0, cn, 0);
+            for (int jj = 0; jj < kCW; ++jj) v[g][jj] = __ldcg(sp + static_cast<size_t>(jj) * kBM);
           }
-          if (!mbar_wait(fs.bar, fs.phase)) return false;
-          fs.phase ^= 1u;
-          add(acc, 0, cn);
-          named_bar(1, kEpiThreads);
-        }
-        emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, ps, acc, es);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (i0 + g < n) {
+#pragma unroll
+            for (int jj = 0; jj < kCW; ++jj) acc[jj] += v[g][jj];
+          }
       }
+      emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + k * 16, k * 16, ps, acc, es);
     }
   }
   if (et == 0) {
@@ -656,7 +624,7 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
 template <typename T, int EPI>
 __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t *accf,
                               uint64_t *acce, uint32_t tmem_base, long long u0, long long u1,
-                              EpiSmem &es, FixupStage &fs, volatile int *sabort) {
+                              EpiSmem &es, volatile int *sabort) {
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   EpiPos ps;
@@ -687,28 +655,18 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
                            static_cast<uint32_t>(a * p.block_n);
     if (!whole) {
       const int slot = (tile == first_tile) ? 0 : 1;
-      float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM;
+      float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM + r;
       for (int j0 = 0; j0 < LW; j0 += 16) {
         float v[kCW];
         tmem_ld_logical(tbase, j0 + ps.c0, LW, p.split, v);
-        uint8_t *sb = stage_claim(es, et);
-        float *f = reinterpret_cast<float *>(sb);
 #pragma unroll
-        for (int jj = 0; jj < kCW; ++jj) f[(ps.c0 + jj) * kBM + r] = v[jj];
-        stage_publish();
-        if (et == 0) {
-          bulk_store(mine + static_cast<size_t>(j0) * kBM, sb, 16 * kBM * 4);
-          bulk_commit();
-        }
+        for (int jj = 0; jj < kCW; ++jj) mine[static_cast<size_t>(j0 + ps.c0 + jj) * kBM] = v[jj];
       }
       tc_fence_before();
       mbar_arrive(&acce[a]);  // the accumulator is free for the MMA warp
-      if (et == 0) {
-        bulk_wait<0>();  // the partial has reached global memory
-        fence_proxy_async_global();
-        __threadfence();
-        atomicAdd(&p.counters[tile], 1u);
-      }
+      __threadfence();        // this thread's part of the partial is visible before the count
+      named_bar(1, kEpiThreads);
+      if (et == 0) atomicAdd(&p.counters[tile], 1u);
       if (split0 < 0) split0 = tile; else split1 = tile;
       continue;
     }
@@ -720,11 +678,10 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
     tc_fence_before();
     mbar_arrive(&acce[a]);
   }
-  // Every accumulator of this CTA has been waited for, so all of its MMAs (and the loads
-  // they consumed) are complete: the stage area is free for the fixups.
-  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, ps, fs, es, sabort)) {
+  // The split tiles this CTA contributed to, reduced after its own mainloop.
+  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, ps, es, sabort)) {
     *sabort = 1;
-  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, ps, fs, es, sabort)) {
+  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, ps, es, sabort)) {
     *sabort = 1;
   }
   if (et == 0) bulk_wait<0>();  // every store of this CTA is complete before it exits
@@ -754,8 +711,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *empty = full + p.stages;
   uint64_t *accf = empty + p.stages;
   uint64_t *acce = accf + 2;
-  uint64_t *fixb = acce + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fixb + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
   volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -773,7 +729,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(&accf[1], 1);
     mbar_init(&acce[0], kEpiThreads);
     mbar_init(&acce[1], kEpiThreads);
-    mbar_init(&fixb[0], 1);
     *sabort = 0;
     fence_barrier_init();
   }
@@ -803,8 +758,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) gemm_mma<T>(p, sA, sB, full, empty, accf, acce, tmem_base, u0, u1, sabort);
     __syncwarp();
   } else {
-    FixupStage fs{smem, static_cast<int>(L.off_x / kOutStage), fixb, 0u};
-    gemm_epilogue<T, EPI>(maps, p, accf, acce, tmem_base, u0, u1, es, fs, sabort);
+    gemm_epilogue<T, EPI>(maps, p, accf, acce, tmem_base, u0, u1, es, sabort);
   }
   tc_fence_before();
   __syncthreads();

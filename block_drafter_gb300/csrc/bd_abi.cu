@@ -453,6 +453,7 @@ static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const
   for (int l0 = 0; l0 < cfg->n_layers; l0 += kMaxSegs / 2) {
     const int l1 = std::min(cfg->n_layers, l0 + kMaxSegs / 2);
     GemmPlan p = make_plan(cfg, cmat, n_rows, H);
+    if (pk && packed_f16(cfg)) p.dtype = GT_F16;  // the packed W_k|W_v are fp16, c_t too
     p.args.epi = EPI_STORE_F32;
     p.args.out_f32 = kv_raw;
     p.args.ld_out = ldkv;
@@ -593,7 +594,8 @@ bd_status bd_ctx_kv_materialize(const bd_config *cfg, const bd_weights *w, const
     p.args.ld_out = H;
     BD_TRY(launch_gemm(p, sc, s));
     BD_TRY(launch_rownorm(cfg->dtype, mw.feat, n_rows, H, w->context_norm, cfg->eps, NORM_PLAIN,
-                          mw.cmat, nullptr, nullptr, nullptr, 1, 0, s));
+                          mw.cmat, nullptr, nullptr, nullptr, 1, 0, s, ConvFinish{nullptr, nullptr, nullptr, 0},
+                          pk != nullptr && packed_f16(cfg)));
   }
   // S2: every layer's raw context K and V (fp32), then head norm + RoPE + ring scatter
   return enqueue_ctx_kv(cfg, w, kv, mw.cmat, n_rows, mw.kv_raw, mw.rope, row_request, row_pos,
@@ -661,7 +663,11 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   BD_TRY(launch_round_prep(dt, w->embed_head, H, cfg->vocab, anchor_ids, frontier, B, W,
                            cfg->mask_token_id, rw.x, rw.rope, D / 2, freq,
                            n_pend > 0 ? pending->pos : nullptr, n_pend, zero, s));
-  const size_t lo_q = split ? static_cast<size_t>(TQ) * H : 0;  // lo block of xq
+  // packed image of a bf16 config: the Q/K/V, W_o, MLP and head products (and the context
+  // rows' K/V products) take fp16 operands: one 16-bit operand instead of a bf16 hi+lo pair
+  const bool f16 = pk != nullptr && packed_f16(cfg);
+  const ConvFinish no_fin{nullptr, nullptr, nullptr, 0};
+  const size_t lo_q = split && !f16 ? static_cast<size_t>(TQ) * H : 0;  // lo block of xq
   if (n_pend > 0) {  // S1 of the catch-up: c_t = plain_rmsnorm(W_feature s_t)
     GemmPlan p = make_plan(cfg, pending->feats, n_pend, cfg->n_target_layers * H);
     add_w(p, w->w_feature, H, pk, PL.w_feature);
@@ -672,10 +678,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     if (fuse) {  // into rows T.. of xq, with a zero lo part
       char *ctx_rows = static_cast<char *>(rw.xq) + static_cast<size_t>(T) * H * elem_bytes(cfg);
       BD_TRY(launch_rownorm(dt, rw.feat, n_pend, H, w->context_norm, cfg->eps, NORM_CTX, ctx_rows,
-                            nullptr, nullptr, nullptr, 1, lo_q, s));
+                            nullptr, nullptr, nullptr, 1, lo_q, s, no_fin, f16));
     } else {  // S2 of the catch-up as its own product over every layer
       BD_TRY(launch_rownorm(dt, rw.feat, n_pend, H, w->context_norm, cfg->eps, NORM_PLAIN, rw.cmat,
-                            nullptr, nullptr, nullptr, 1, 0, s));
+                            nullptr, nullptr, nullptr, 1, 0, s, no_fin, f16));
       const bd_status st = enqueue_ctx_kv(cfg, w, kv, rw.cmat, n_pend, rw.kv_raw,
                                           rw.rope + static_cast<size_t>(T) * (D / 2),
                                           pending->request, pending->pos, frontier, B,
@@ -688,16 +694,14 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
   // is added to the residual by the next row norm (ConvFinish), which writes x back.
   const bool conv = cfg->conv_group > 0;
   const int gw = cfg->conv_group, ND = conv ? 4 * H / gw : 0;
-  // packed image of a bf16 config: the MLP and head products and the attention take fp16
-  // operands (one 16-bit operand instead of a bf16 hi+lo pair)
-  const bool mlp16 = pk != nullptr && packed_f16(cfg);
-  const ConvFinish no_fin{nullptr, nullptr, nullptr, 0};
+  const bool mlp16 = f16;
   ConvFinish fin = no_fin;  // the previous layer's MLP finish, not yet added to x
   int copy_layer = -1;      // layer whose layers_out copy waits for that finish
   auto delta_gemm = [&](const void *xin, int rows, const void *wd, size_t packed_off,
                         float *out) -> std::string {
     GemmPlan p = make_plan(cfg, xin, rows, H);
-    p.split = split;
+    p.split = split && !f16;
+    if (f16) p.dtype = GT_F16;
     add_w(p, wd, ND, pk, packed_off);
     p.args.epi = EPI_STORE_F32;
     p.args.out_f32 = out;
@@ -713,7 +717,7 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE.  The pending context rows ride
     // along in the same product: their K/V (S2) use the same W_k, W_v tiles.
     BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xq, nullptr,
-                          conv ? rw.cn : nullptr, nullptr, W, lo_q, s, fin));
+                          conv ? rw.cn : nullptr, nullptr, W, lo_q, s, fin, f16));
     fin = no_fin;
     if (copy_layer >= 0) {
       BD_TRY(copy_layer_out(copy_layer));
@@ -721,11 +725,12 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     }
     if (conv) {  // delta_a (over every xq row, so the split layout matches), then Conv_0(n)
       BD_TRY(delta_gemm(rw.xq, Tq, L.conv_delta_a, PL.conv_a[l], rw.cdelta_a));
-      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_a, L.conv_base_a, T, H, gw, W, rw.xq, lo_q, s));
+      BD_TRY(launch_conv_prepare(dt, rw.cn, rw.cdelta_a, L.conv_base_a, T, H, gw, W, rw.xq, lo_q, s, f16));
     }
     {
       GemmPlan p = make_plan(cfg, rw.xq, Tq, H);
-      p.split = split;
+      p.split = split && !f16;
+      if (f16) p.dtype = GT_F16;
       add_w(p, L.wq, QD, pk, PL.wq[l]);
       add_w(p, L.wk, KD, pk, PL.wk[l]);
       add_w(p, L.wv, KD, pk, PL.wv[l]);
@@ -793,14 +798,16 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       a.max_keys = att_max_keys(cfg, l, W);
       a.q_lo = split ? static_cast<size_t>(T) * QD : 0;
       a.blk_lo = split ? static_cast<size_t>(T) * KD : 0;
-      a.out_lo = lo(QD);
+      a.out_lo = f16 ? 0 : lo(QD);
+      a.out_f16 = f16 ? 1 : 0;  // W_o takes fp16 operands with the packed image
       BD_TIMED(BD_TIME_ATTENTION, launch_attention(a, dt, s));
     }
     // S6: y = x + W_o a (in place; with the convolution W_o a goes to cz and the next
     // row norm adds Conv_1 of it)
     {
       GemmPlan p = make_plan(cfg, rw.att, T, QD);
-      p.split = split;
+      p.split = split && !f16;
+      if (f16) p.dtype = GT_F16;
       add_w(p, L.wo, H, pk, PL.wo[l]);
       p.args.epi = conv ? EPI_STORE_F32 : EPI_RESID_F32;
       p.args.out_f32 = conv ? rw.cz : rw.x;

@@ -269,12 +269,13 @@ __device__ __forceinline__ void bfly_sum32(float (&v)[32], int lane) {
 }
 
 // Final outputs of one thread (output dim kr, queries h*32 .. h*32+31) from unnormalised
-// sums o and row sums l: bf16 hi (and lo) planes, token-major [B*W][Hq*D].
+// sums o and row sums l, token-major [B*W][Hq*D]: one fp16 plane (out_f16, the operand of
+// an fp16 output projection) or bf16 hi (and lo) planes.
 __device__ __forceinline__ void write_out(const AttArgs &a, int b, int g, int kr, int h,
                                           const float *l, const float (&o)[32]) {
   const int D = a.head_dim, W = a.W, G = a.n_q_heads / a.n_kv_heads, R = G * W;
   if (kr >= D) return;
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int q = h * 32 + j;
@@ -284,11 +285,18 @@ __device__ __forceinline__ void write_out(const AttArgs &a, int b, int g, int kr
       const float y = L > 0.f ? o[j] / L : 0.f;
       const size_t idx = (static_cast<size_t>(b) * W + i) * a.n_q_heads * D +
                          static_cast<size_t>(g * G + hh) * D + kr;
-      const __nv_bfloat16 hv = __float2bfloat16_rn(y);
-      out[idx] = hv;
-      if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(hv));
+      if (a.out_f16) {
+        bad |= f16_out_of_range(y);
+        static_cast<__half *>(a.out)[idx] = __float2half_rn(y);
+      } else {
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+        const __nv_bfloat16 hv = __float2bfloat16_rn(y);
+        out[idx] = hv;
+        if (a.out_lo) out[a.out_lo + idx] = __float2bfloat16_rn(y - __bfloat162float(hv));
+      }
     }
   }
+  flag_f16_range(bad);
 }
 
 // Merge of the cluster's partials (O, m, l) for query rows r0 .. r1-1 of (request b, KV
@@ -360,11 +368,20 @@ __device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, in
     const int q = r0 + r, hh = q / a.W, i = q - hh * a.W;
     const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
                        static_cast<size_t>(g * G + hh) * D + 4 * d4;
-    uint32_t hw[2], lw[2];
-    split_bf16x2(acc.x * il, acc.y * il, hw[0], lw[0]);
-    split_bf16x2(acc.z * il, acc.w * il, hw[1], lw[1]);
-    *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
-    if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
+    const float y0 = acc.x * il, y1 = acc.y * il, y2 = acc.z * il, y3 = acc.w * il;
+    if (a.out_f16) {
+      flag_f16_range(f16_out_of_range(y0) || f16_out_of_range(y1) || f16_out_of_range(y2) ||
+                     f16_out_of_range(y3));
+      const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
+      *reinterpret_cast<uint2 *>(static_cast<__half *>(a.out) + idx) =
+          make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+    } else {
+      uint32_t hw[2], lw[2];
+      split_bf16x2(y0, y1, hw[0], lw[0]);
+      split_bf16x2(y2, y3, hw[1], lw[1]);
+      *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
+      if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
+    }
     }
   }
 }

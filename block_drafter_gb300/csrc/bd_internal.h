@@ -144,10 +144,12 @@ struct PackedLayout {
 PackedLayout packed_layout(const bd_config *c);
 // Empty when the configuration passes the checks every entry point applies.
 std::string validate_config(const bd_config *c);
-// In a bf16 config the packed image stores the MLP matrices (gate/up, down, and the MLP
-// branch's convolution delta) and the head as fp16: those products take fp16 activations
-// (one operand of 11 significant bits instead of a bf16 hi+lo pair), which halves their
-// tensor work and activation traffic.  Other matrices stay bf16.
+// In a bf16 config the packed image stores the attention-branch matrices (W_q, W_k, W_v,
+// W_o and the attention branch's convolution delta), the MLP matrices (gate/up, down, and
+// the MLP branch's convolution delta) and the head as fp16: those products take fp16
+// activations (one operand of 11 significant bits instead of a bf16 hi+lo pair), which
+// halves their tensor work, activation traffic and shared memory per stage.  W_feature and
+// the bridge matrices stay bf16.
 inline bool packed_f16(const bd_config *c) { return c->dtype == BD_BF16; }
 std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cudaStream_t s);
 unsigned take_error_word_pack();

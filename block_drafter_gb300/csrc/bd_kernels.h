@@ -23,6 +23,7 @@ struct AttArgs {
                         // catch-up (read only after the previous kernel has finished)
   size_t q_lo, blk_lo, out_lo;  // bf16: element offsets of the lo halves of q, blk_k/v, out
                                 // (q and blk lo planes directly follow their hi planes)
+  int out_f16;                  // bf16 config: the output is one fp16 plane (out_lo unused)
 };
 
 int attention_rows_max();

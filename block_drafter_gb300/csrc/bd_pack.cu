@@ -1,7 +1,9 @@
 // Packed weight image: every projection matrix stored as contiguous 16 KB boxes (128 rows
 // x 128 bytes of K) in the 128-byte-swizzled order the tensor cores read from shared
-// memory, so a GEMM pipeline stage is one contiguous bulk copy of kbox boxes.  A pure
-// permutation of the weights (plus zero padding of partial tiles).
+// memory, so a GEMM pipeline stage is one contiguous bulk copy of kbox boxes.  In a bf16
+// config the attention-branch and MLP matrices and the head are converted to fp16 on the
+// way (exact within fp16's range); the others are a pure permutation (plus zero padding of
+// partial tiles).
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -127,10 +129,10 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
   }
   for (int l = 0; l < c->n_layers; ++l) {
     const bd_layer_weights &W = w->layer[l];
-    BD_PACK(W.wq, nullptr, QD, H, false, L.wq[l]);
-    BD_PACK(W.wk, nullptr, KD, H, false, L.wk[l]);
-    BD_PACK(W.wv, nullptr, KD, H, false, L.wv[l]);
-    BD_PACK(W.wo, nullptr, H, QD, false, L.wo[l]);
+    BD_PACK16(W.wq, nullptr, QD, H, false, L.wq[l]);
+    BD_PACK16(W.wk, nullptr, KD, H, false, L.wk[l]);
+    BD_PACK16(W.wv, nullptr, KD, H, false, L.wv[l]);
+    BD_PACK16(W.wo, nullptr, H, QD, false, L.wo[l]);
     BD_PACK16(W.w_gate, W.w_up, c->ffn, H, true, L.gate_up[l]);
     BD_PACK16(W.w_down, nullptr, H, c->ffn, false, L.w_down[l]);
     if (c->code_width > 0) {
@@ -138,7 +140,7 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
       BD_PACK(W.w_write, nullptr, H, c->msg_width, false, L.w_write[l]);
     }
     if (c->conv_group > 0) {
-      BD_PACK(W.conv_delta_a, nullptr, 4 * H / c->conv_group, H, false, L.conv_a[l]);
+      BD_PACK16(W.conv_delta_a, nullptr, 4 * H / c->conv_group, H, false, L.conv_a[l]);
       BD_PACK16(W.conv_delta_m, nullptr, 4 * H / c->conv_group, H, false, L.conv_m[l]);
     }
   }

@@ -152,15 +152,18 @@ size_t bd_packed_bytes(const bd_config *cfg);
  * matrices interleaved 64 rows each per tile); out-of-range rows/columns are zero.  Run it
  * once after loading the weights, then set w->packed = packed.
  *
- * The image is not only a permutation.  In a bf16 config it stores the MLP matrices
- * (W_gate, W_up, W_down, and with conv_group > 0 the MLP branch's W_delta) and the LM
- * head as fp16, and the products that read them then take fp16 activations (see
- * bd_draft_round and bd_lm_head_argmax); all other matrices stay bf16, bit for bit.  The
+ * The image is not only a permutation.  In a bf16 config it stores the attention-branch
+ * matrices (W_q, W_k, W_v, W_o, and with conv_group > 0 the attention branch's W_delta),
+ * the MLP matrices (W_gate, W_up, W_down, and the MLP branch's W_delta) and the LM head as
+ * fp16, and the products that read them then take fp16 activations (see
+ * bd_ctx_kv_materialize, bd_draft_round and bd_lm_head_argmax); W_feature and the bridge
+ * matrices (R_l, W_l, G, G_p, A) stay bf16, bit for bit.  The
  * conversion is exact for every bf16 value of magnitude 2^-14 .. 65504; smaller values
  * become fp16 subnormals with an absolute error of at most 2^-25; a value beyond
  * +-65504 makes the next bd_sync_status return BD_ERR_RANGE.  Results with and without
  * the image therefore differ by these roundings and the activations' fp16 rounding
- * (about 1e-3 of max|h| at the 27B geometry), not bit for bit.  In an fp32 config the
+ * (about 1e-3 of max|h| at the 27B geometry; context K/V by up to one bf16 unit), not bit
+ * for bit.  In an fp32 config the
  * image is a pure permutation.
  */
 bd_status bd_pack_weights(const bd_config *cfg, const bd_weights *w, void *packed,
@@ -172,7 +175,8 @@ bd_status bd_pack_weights(const bd_config *cfg, const bd_weights *w, void *packe
  *   for each layer l:  k = rope_1d(plain_head_rmsnorm(W_k^l c_t, k_norm^l), t)
  *                      v = W_v^l c_t
  * stored (bf16 round-to-nearest in a bf16 config) into ring row `row_request[r]` at
- * slot row_pos[r] mod ring_capacity[l].
+ * slot row_pos[r] mod ring_capacity[l].  In a bf16 config c_t enters the K/V products as
+ * bf16, or as fp16 with the packed image (whose W_k, W_v are fp16; see bd_pack_weights).
  *
  *   target_feats  dev [n_rows, n_target_layers*H]  captured residual rows s_t (the
  *                 target layers' residual outputs concatenated in recorded order)
@@ -226,14 +230,14 @@ typedef struct {
  *   activation that feeds a tensor-core product (normed rows, attention output, SwiGLU
  *   product, codes, messages, queries, softmax weights, the block's own keys/values)
  *   enters as a bf16 hi+lo pair (about 16 significant bits).
- *   With the packed image the MLP products read fp16 weights (see bd_pack_weights) and
- *   take fp16 activations (the normed rows and the SwiGLU product, 11 significant bits);
- *   the attention takes fp16 queries, softmax weights and block keys/values, and converts
- *   its bf16 ring tiles to fp16 in shared memory (ring values beyond +-65504 saturate);
- *   the other products (Q/K/V, W_o, the bridge's code read, gate/value maps and write)
- *   keep bf16 weights and bf16 hi+lo activation pairs.  An activation beyond the fp16
- *   range on its way into an fp16 operand is still stored (as +-inf) and makes the next
- *   bd_sync_status return BD_ERR_RANGE.
+ *   With the packed image the Q/K/V, W_o and MLP products read fp16 weights (see
+ *   bd_pack_weights) and take fp16 activations (the normed rows, the attention output,
+ *   the SwiGLU product: 11 significant bits); the bridge's code read, gate/value maps and
+ *   write keep bf16 weights and bf16 hi+lo activation pairs.  An activation beyond the
+ *   fp16 range on its way into an fp16 operand is still stored (as +-inf) and makes the
+ *   next bd_sync_status return BD_ERR_RANGE.
+ *   The attention always takes the queries, softmax weights and the block's own keys/values
+ *   as bf16 hi+lo pairs against the ring's bf16 keys/values as stored.
  * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for
  * the injection after every layer when code_width > 0:
  *   row (b, 0) = embed(anchor_ids[b]) at position F_b; rows (b, i>=1) = embed(MASK) at

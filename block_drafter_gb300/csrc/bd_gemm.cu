@@ -279,18 +279,46 @@ struct EpiPos {
   int c0;  // first column of this thread's slice of a chunk
 };
 
-// Columns col..col+kCW-1 of the accumulator: the hi half, plus the lo half that sits LW
-// columns further when the activation operand is split.
-__device__ __forceinline__ void tmem_ld_logical(uint32_t tbase, int col, int LW, int split,
-                                                float (&v)[kCW]) {
-  static_assert(kCW == 8, "tmem_ld_logical loads 8 columns per thread");
-  tmem_ld8(tbase + col, v);
-  if (split) {
-    float w[kCW];
-    tmem_ld8(tbase + LW + col, w);
+// Up to four 16-column chunks of the accumulator at once: the kCW columns col + 16 i ..
+// + kCW - 1 (i < nc) of this thread's row go to v[kCW i ..], each the hi half plus, when the
+// activation operand is split, the lo half that sits LW columns further.  One wait covers
+// all the loads of a group of four.
+__device__ __forceinline__ void tmem_ld_chunks(uint32_t tbase, int col, int LW, int split, int nc,
+                                               float (&v)[4 * kCW]) {
+  static_assert(kCW == 8, "tmem_ld_chunks loads 8 columns per chunk and thread");
+  const uint32_t t = tbase + static_cast<uint32_t>(col);
+  if (nc == 4) {
+    tmem_ld8x4(t, t + 16, t + 32, t + 48, v);
+    if (split) {
+      float w[4 * kCW];
+      tmem_ld8x4(t + LW, t + LW + 16, t + LW + 32, t + LW + 48, w);
 #pragma unroll
-    for (int jj = 0; jj < kCW; ++jj) v[jj] += w[jj];
+      for (int i = 0; i < 4 * kCW; ++i) v[i] += w[i];
+    }
+    return;
   }
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    if (c >= nc) break;
+    float h[kCW];
+    tmem_ld8(t + 16 * c, h);
+    if (split) {
+      float w[kCW];
+      tmem_ld8(t + LW + 16 * c, w);
+#pragma unroll
+      for (int jj = 0; jj < kCW; ++jj) h[jj] += w[jj];
+    }
+#pragma unroll
+    for (int jj = 0; jj < kCW; ++jj) v[c * kCW + jj] = h[jj];
+  }
+}
+
+// Chunk c (0..3, at run time) of a group loaded by tmem_ld_chunks, without indexing the
+// register array by a run-time value.
+__device__ __forceinline__ void chunk_of(const float (&v4)[4 * kCW], int c, float (&v)[kCW]) {
+#pragma unroll
+  for (int jj = 0; jj < kCW; ++jj)
+    v[jj] = c == 0 ? v4[jj] : c == 1 ? v4[kCW + jj] : c == 2 ? v4[2 * kCW + jj] : v4[3 * kCW + jj];
 }
 
 // Results leave the SM through shared memory: the epilogue threads write a chunk of 16
@@ -545,7 +573,8 @@ __device__ __forceinline__ void load_row_scales(const GemmArgs &p, int tile_tok0
 
 // Split tiles.  Every CTA that computed part of a tile stores its fp32 partial (layout
 // [LW columns][128 rows], straight from registers: a warp writes 128 contiguous bytes per
-// column) in its own slot and counts itself on the tile's counter.  After its mainloop each
+// column) in its own slot (0 for the CTA's first tile, 1 for its last) and counts itself on
+// the tile's counter.  After its mainloop each
 // contributor waits until all n have arrived and then sums its share of the tile's
 // 16-column chunks (chunk k belongs to the contributor k mod n) over all n partials, in CTA
 // order, so results do not depend on which CTA got there first.  The partial values a
@@ -555,16 +584,33 @@ __device__ __forceinline__ void load_row_scales(const GemmArgs &p, int tile_tok0
 // resident at once (one per SM), so the waits end.
 constexpr int kFixLoads = 32;
 
-template <typename T, int EPI>
-__device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, const EpiPos &ps,
-                           EpiSmem &es, volatile int *sabort) {
+// The contributors of a split tile: CTAs c_first .. c_first + n - 1.  Each of them except
+// c_first starts its unit range inside the tile, so the tile is its first (slot 0);
+// c_first holds it in slot 1 when its range began in an earlier tile.  Worked out before
+// the CTA's mainloop ends (the 64-bit divisions stay off the epilogue's critical path).
+struct SplitInfo {
+  int tile, c_first, n, slot0;
+};
+__device__ __forceinline__ SplitInfo split_info(const GemmArgs &p, int tile) {
   const long long U = p.units;
   const int P = p.n_ctas;
+  const long long first_unit = static_cast<long long>(tile) * p.kb;
+  SplitInfo si;
+  si.tile = tile;
+  si.c_first = cta_of_unit(U, P, first_unit, p.grain);
+  si.n = cta_of_unit(U, P, first_unit + p.kb - 1, p.grain) - si.c_first + 1;
+  si.slot0 = unit_begin(U, P, si.c_first, p.grain) < first_unit ? 1 : 0;
+  return si;
+}
+
+template <typename T, int EPI>
+__device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, const SplitInfo &si,
+                           const EpiPos &ps, EpiSmem &es, volatile int *sabort) {
+  const int tile = si.tile;
   const int LW = p.ln;
   const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
-  const int c_first = cta_of_unit(U, P, static_cast<long long>(tile) * p.kb, p.grain);
-  const int c_last = cta_of_unit(U, P, static_cast<long long>(tile + 1) * p.kb - 1, p.grain);
-  const int n = c_last - c_first + 1;
+  const int c_first = si.c_first;
+  const int n = si.n;
   const int me = static_cast<int>(blockIdx.x) - c_first;
   unsigned *arrived = p.counters + tile;
   unsigned *done = p.counters + p.n_counter_tiles + tile;
@@ -580,9 +626,8 @@ __device__ bool fixup_tile(const GemmMaps &maps, const GemmArgs &p, int tile, co
     if (EPI == EPI_INJECT) load_row_scales(p, n_tile * LW, LW, et, es);
     // this thread's first value of chunk k in contributor i's partial
     auto src = [&](int i, int k) -> const float * {
-      const int c = c_first + i;
-      const int cslot = (static_cast<int>(unit_begin(U, P, c, p.grain) / p.kb) == tile) ? 0 : 1;
-      return p.partials + (static_cast<size_t>(c) * 2 + cslot) * LW * kBM +
+      const int cslot = i == 0 ? si.slot0 : 0;
+      return p.partials + (static_cast<size_t>(c_first + i) * 2 + cslot) * LW * kBM +
              static_cast<size_t>(k * 16 + ps.c0) * kBM + ps.r;
     };
     // one chunk at a time (one call site of the emit code: it is cold, once-per-tile code);
@@ -634,10 +679,22 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
   const int r = ps.r, et = ps.et;
   const int cta = blockIdx.x;
   const int first_tile = static_cast<int>(u0 / p.kb);
+  // Only the first and the last tile of a CTA's unit range can be split.
+  SplitInfo sp0{-1, 0, 0, 0}, sp1{-1, 0, 0, 0};
+  {
+    SegWalk sw{u0, u1, p.kb};
+    int t, a0, a1;
+    while (sw.next(t, a0, a1))
+      if (a0 != 0 || a1 != p.kb) {
+        if (sp0.tile < 0)
+          sp0 = split_info(p, t);
+        else
+          sp1 = split_info(p, t);
+      }
+  }
   pdl_wait();
   SegWalk w{u0, u1, p.kb};
   int tile, kb0, kb1, e = 0;
-  int split0 = -1, split1 = -1;  // split tiles this CTA contributed to
   while (w.next(tile, kb0, kb1)) {
     const int a = e & 1;
     const uint32_t ra = static_cast<uint32_t>(e >> 1);
@@ -656,33 +713,51 @@ __device__ void gemm_epilogue(const GemmMaps &maps, const GemmArgs &p, uint64_t 
     if (!whole) {
       const int slot = (tile == first_tile) ? 0 : 1;
       float *mine = p.partials + (static_cast<size_t>(cta) * 2 + slot) * LW * kBM + r;
-      for (int j0 = 0; j0 < LW; j0 += 16) {
-        float v[kCW];
-        tmem_ld_logical(tbase, j0 + ps.c0, LW, p.split, v);
+      for (int j0 = 0; j0 < LW; j0 += 64) {
+        const int nc = min(4, (LW - j0) >> 4);
+        float v4[4 * kCW];
+        tmem_ld_chunks(tbase, j0 + ps.c0, LW, p.split, nc, v4);
 #pragma unroll
-        for (int jj = 0; jj < kCW; ++jj) mine[static_cast<size_t>(j0 + ps.c0 + jj) * kBM] = v[jj];
+        for (int c = 0; c < 4; ++c)
+          if (c < nc)
+#pragma unroll
+            for (int jj = 0; jj < kCW; ++jj)
+              mine[static_cast<size_t>(j0 + 16 * c + ps.c0 + jj) * kBM] = v4[c * kCW + jj];
       }
       tc_fence_before();
       mbar_arrive(&acce[a]);  // the accumulator is free for the MMA warp
-      __threadfence();        // this thread's part of the partial is visible before the count
+      // The barrier orders every thread's partial stores before thread 0's fence, which
+      // makes them visible at device scope before the count.
       named_bar(1, kEpiThreads);
-      if (et == 0) atomicAdd(&p.counters[tile], 1u);
-      if (split0 < 0) split0 = tile; else split1 = tile;
+      if (et == 0) {
+        __threadfence();
+        atomicAdd(&p.counters[tile], 1u);
+      }
       continue;
     }
-    for (int j0 = 0; j0 < LW; j0 += 16) {
-      float v[kCW];
-      tmem_ld_logical(tbase, j0 + ps.c0, LW, p.split, v);
-      emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + j0, j0, ps, v, es);
+    for (int j0 = 0; j0 < LW; j0 += 64) {
+      const int nc = min(4, (LW - j0) >> 4);
+      float v4[4 * kCW];
+      tmem_ld_chunks(tbase, j0 + ps.c0, LW, p.split, nc, v4);
+      if (j0 + 64 >= LW) {  // every column of the tile is in registers
+        tc_fence_before();
+        mbar_arrive(&acce[a]);
+      }
+      for (int c = 0; c < nc; ++c) {
+        float v[kCW];
+        chunk_of(v4, c, v);
+        emit_chunk<T, EPI>(maps, p, m_tile, n_tile * LW + j0 + 16 * c, j0 + 16 * c, ps, v, es);
+      }
     }
-    tc_fence_before();
-    mbar_arrive(&acce[a]);
   }
   // The split tiles this CTA contributed to, reduced after its own mainloop.
-  if (split0 >= 0 && !fixup_tile<T, EPI>(maps, p, split0, ps, es, sabort)) {
-    *sabort = 1;
-  } else if (split1 >= 0 && !fixup_tile<T, EPI>(maps, p, split1, ps, es, sabort)) {
-    *sabort = 1;
+  for (int i = 0; i < 2; ++i) {
+    const SplitInfo si = i == 0 ? sp0 : sp1;
+    if (si.tile < 0) break;
+    if (!fixup_tile<T, EPI>(maps, p, si, ps, es, sabort)) {
+      *sabort = 1;
+      break;
+    }
   }
   if (et == 0) bulk_wait<0>();  // every store of this CTA is complete before it exits
 }

@@ -188,9 +188,6 @@ struct Carve {
   }
 };
 
-// When the context chunks are short (at most two 64-key blocks per split), the block's own
-// keys -- a separate hi+lo pass -- would double the last split's work and every split
-// waits for it in the merge: give them a split of their own.
 // Key splits of a layer's bf16 attention (one CTA per split, KV head and request; the
 // splits of a head form one cluster and merge through distributed shared memory, so the
 // grid may exceed one wave): enough splits to fill the SMs once (one CTA per SM), more
@@ -203,6 +200,9 @@ int att_splits(const bd_config *c, int l, int B, int W, int sms) {
   int s = std::max(sms / (B * c->n_kv_heads), (tiles + 15) / 16);
   if (s < 1) s = 1;
   if (s > attention_max_splits()) s = attention_max_splits();
+  // a grid of several waves (a long full-context window at B > 1) keeps clusters of at most
+  // four: larger clusters find fewer places to run and merge more partials (measured)
+  if (s > 4 && B * c->n_kv_heads * s > sms) s = 4;
   return s < tiles ? s : tiles;
 }
 int att_max_keys(const bd_config *c, int l, int W) {

@@ -303,69 +303,64 @@ __device__ __forceinline__ void write_out(const AttArgs &a, int b, int g, int kr
 // head g), by the 256 softmax threads of one CTA:
 //   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max over splits with l_s > 0,
 // reading split s's partial from CTA s of the cluster (distributed shared memory): its
-// [query][D] fp32 tile at kOffP and its per-query m, l.  Splits are added in rank order.
-// scr: local scratch of 3 * 8 * 64 + 64 floats.
+// [query][D] fp32 tile at kOffP and its per-query m, l.  Each thread takes 4 output columns
+// of a row and issues every remote load it needs (the row's m and l of every split and
+// their 4 columns) before any arithmetic, so a chunk costs one remote round trip and needs
+// no barrier; splits are added in rank order.
 template <int D>
-__device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, int tid, uint8_t *sm,
-                              float *scr) {
+__device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, int tid, uint8_t *sm) {
   constexpr int kMax = kMaxSplits;
+  constexpr int C4 = D / 4;  // float4 chunks per row
   const int S = a.n_splits, nr = r1 - r0;
   const int G = a.n_q_heads / a.n_kv_heads;
-  float *sm_m = scr, *sm_l = scr + kMax * 64, *sm_w = sm_l + kMax * 64, *inv_l = sm_w + kMax * 64;
-  const uint32_t ml_base = smem_u32(sm + kOffRed);       // m_ref[64], then alpha[64], l[64]
+  const uint32_t ml_base = smem_u32(sm + kOffRed);  // m_ref[64], then alpha[64], l[64]
   const uint32_t p_base = smem_u32(sm + kOffP);
-  for (int i = tid; i < S * nr; i += kSoftThreads) {
-    const int sp = i / nr, r = i - sp * nr;
-    const uint32_t rm = cluster_map(ml_base, static_cast<uint32_t>(sp));
-    sm_m[sp * 64 + r] = ld_cluster_f32(rm + (r0 + r) * 4);
-    sm_l[sp * 64 + r] = ld_cluster_f32(rm + (128 + r0 + r) * 4);
-  }
-  named_bar(kBarSoft, kSoftThreads);
-  if (tid < nr) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < S; ++sp)
-      if (sm_l[sp * 64 + tid] > 0.f) M = fmaxf(M, sm_m[sp * 64 + tid]);
-    float L = 0.f;
-    for (int sp = 0; sp < S; ++sp) {
-      const float l = sm_l[sp * 64 + tid];
-      const float w = l > 0.f ? exp2f(sm_m[sp * 64 + tid] - M) : 0.f;
-      sm_w[sp * 64 + tid] = w;
-      L += w * l;
-    }
-    inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
-  }
-  named_bar(kBarSoft, kSoftThreads);
-  constexpr int C4 = D / 4;  // float4 chunks per row
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-  // two chunks per pass, every remote load of the pass issued before any arithmetic
-  for (int c0 = tid; c0 < nr * C4; c0 += 2 * kSoftThreads) {
-    float4 v[2][kMax];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int c = c0 + k * kSoftThreads;
-      const int r = c / C4, d4 = c - r * C4;
-      const uint32_t off = static_cast<uint32_t>(((r0 + r) * D + 4 * d4) * 4);
-#pragma unroll
-      for (int sp = 0; sp < kMax; ++sp)
-        if (sp < S && c < nr * C4) v[k][sp] = ld_cluster_f4(cluster_map(p_base + off, static_cast<uint32_t>(sp)));
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-    const int c = c0 + k * kSoftThreads;
-    if (c >= nr * C4) break;
-    const int r = c / C4, d4 = c - r * C4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = tid; c < nr * C4; c += kSoftThreads) {
+    const int r = c / C4, d4 = c - r * C4, q = r0 + r;
+    const uint32_t o_off = p_base + static_cast<uint32_t>((q * D + 4 * d4) * 4);
+    float m[kMax], l[kMax];
+    float4 v[4];
 #pragma unroll
     for (int sp = 0; sp < kMax; ++sp)
       if (sp < S) {
-        const float w = sm_w[sp * 64 + r];
-        acc.x += w * v[k][sp].x;
-        acc.y += w * v[k][sp].y;
-        acc.z += w * v[k][sp].z;
-        acc.w += w * v[k][sp].w;
+        const uint32_t rm = cluster_map(ml_base, static_cast<uint32_t>(sp));
+        m[sp] = ld_cluster_f32(rm + q * 4);
+        l[sp] = ld_cluster_f32(rm + (128 + q) * 4);
+        if (sp < 4) v[sp] = ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(sp)));
       }
-    const float il = inv_l[r];
-    const int q = r0 + r, hh = q / a.W, i = q - hh * a.W;
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kMax; ++sp)
+      if (sp < S && l[sp] > 0.f) M = fmaxf(M, m[sp]);
+    float L = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kMax; ++sp)
+      if (sp < S) {
+        m[sp] = l[sp] > 0.f ? exp2f(m[sp] - M) : 0.f;  // the split's weight
+        L += m[sp] * l[sp];
+      }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s0 = 0; s0 < kMax; s0 += 4) {
+      if (s0 >= S) break;
+      if (s0 > 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (s0 + k < S) v[k] = ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(s0 + k)));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (s0 + k < S) {
+          const float w = m[s0 + k];
+          acc.x += w * v[k].x;
+          acc.y += w * v[k].y;
+          acc.z += w * v[k].z;
+          acc.w += w * v[k].w;
+        }
+    }
+    const float il = L > 0.f ? 1.f / L : 0.f;
+    const int hh = q / a.W, i = q - hh * a.W;
     const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
                        static_cast<size_t>(g * G + hh) * D + 4 * d4;
     const float y0 = acc.x * il, y1 = acc.y * il, y2 = acc.z * il, y3 = acc.w * il;
@@ -381,7 +376,6 @@ __device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, in
       split_bf16x2(y2, y3, hw[1], lw[1]);
       *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
       if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
-    }
     }
   }
 }
@@ -688,7 +682,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     if (warp >= 2) {
       const int rp = (R + a.n_splits - 1) / a.n_splits;
       const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
-      merge_cluster<D>(a, b, g, r0, r1, tid - 64, sm, reinterpret_cast<float *>(sm + kOffK));
+      merge_cluster<D>(a, b, g, r0, r1, tid - 64, sm);
     }
     cluster_sync();  // no CTA leaves while the others still read its partial
   }

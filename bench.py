@@ -720,9 +720,11 @@ def main():
                    "step": "draft round with the catch-up of 16 pending rows per request fused in "
                            "+ LM head argmax",
                    "l2": "inputs larger than L2 (weights streamed per step >> 129 MB)",
-                   "operands": "bf16 weights (packed image: MLP and head converted exactly to fp16); "
-                               "fp16 activations in the MLP, head and attention products, bf16 "
-                               "hi+lo pairs in the others; fp32 accumulation and residual stream",
+                   "operands": "bf16 weights (packed image: Q/K/V, W_o, MLP and head converted "
+                               "to fp16); fp16 activations in those products, bf16 hi+lo pairs "
+                               "in the feature projection, the bridge products and the "
+                               "attention's scores and probabilities; fp32 accumulation and "
+                               "residual stream",
                    "parallelism": f"replicas x{world}"},
         "us_per_step": 1000.0 * ms,
         "breakdown_us": {k: 1000.0 * v for k, v in per.items()},

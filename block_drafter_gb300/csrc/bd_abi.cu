@@ -874,9 +874,9 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.r = rw.r;
       ba.zpart = rw.zpart;
       ba.sspart = rw.sspart;
-      ba.zc = static_cast<__nv_bfloat16 *>(rw.c);
+      ba.zc = static_cast<__half *>(rw.c);
       ba.zsq = rw.zsq;
-      ba.m = static_cast<__nv_bfloat16 *>(rw.m);
+      ba.m = static_cast<__half *>(rw.m);
       ba.tail = tail_state && l == cfg->n_layers - 1 ? tail_state : nullptr;
       ba.bar = rw.br_bar + 5 * l;
       ba.T = T;
@@ -897,12 +897,14 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     } else if (cfg->code_width > 0) {
       const int Rc = cfg->code_width, Mc = cfg->msg_width;
       // S8: r = RMS(x); z = R_l (x / (r + eps)); c = sqrt(Rc) z / (|z| + eps); anchor code
+      // (with the packed image the bridge's products take single fp16 operands)
       BD_TRY(launch_rownorm(dt, rw.x, T, H, nullptr, cfg->eps, NORM_BRIDGE, rw.xn, rw.r, nullptr,
-                            nullptr, W, lo(H), s, fin));
+                            nullptr, W, f16 ? 0 : lo(H), s, fin, f16));
       fin = no_fin;
       {
         GemmPlan p = make_plan(cfg, rw.xn, T, H);
-        p.split = split;
+        p.split = split && !f16;
+        if (f16) p.dtype = GT_F16;
         add_w(p, L.r_read, Rc, pk, PL.r_read[l]);
         p.args.epi = EPI_STORE_F32;
         p.args.out_f32 = rw.z;
@@ -910,11 +912,12 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         BD_TRY(launch_gemm(p, sc, s));
       }
       BD_TRY(launch_code(dt, rw.z, T, Rc, w->codebook, anchor_ids, cfg->vocab, W, cfg->eps, rw.c,
-                         lo(Rc), s));
+                         f16 ? 0 : lo(Rc), s, f16));
       // S9: [G c; G_p c; A c] in one launch, gate/message, then the RMS-scaled write
       {
         GemmPlan p = make_plan(cfg, rw.c, T, Rc);
-        p.split = split;
+        p.split = split && !f16;
+        if (f16) p.dtype = GT_F16;
         add_w(p, w->g_recv, Mc, pk, PL.g_recv);
         add_w(p, w->g_pred, Mc, pk, PL.g_pred);
         add_w(p, w->a_val, Mc, pk, PL.a_val);
@@ -926,12 +929,13 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         p.args.seg[2].out_col = 2 * Mc;
         BD_TRY(launch_gemm(p, sc, s));
       }
-      BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, lo(Mc), s));
+      BD_TRY(launch_message(dt, rw.pre, T, Mc, w->gate_bias, W, rw.m, f16 ? 0 : lo(Mc), s, f16));
       if (tail_state && l == cfg->n_layers - 1)  // the state the last-write refinement redoes
         BD_TRY(launch_tail_export(rw.x, rw.r, rw.pre, T, H, Mc, tail_state, s));
       {
         GemmPlan p = make_plan(cfg, rw.m, T, Mc);
-        p.split = split;
+        p.split = split && !f16;
+        if (f16) p.dtype = GT_F16;
         add_w(p, L.w_write, H, pk, PL.w_write[l]);
         p.args.epi = EPI_INJECT;
         p.args.out_f32 = rw.x;
@@ -1131,10 +1135,13 @@ bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float 
   const PackedLayout PL = packed_layout(cfg);
   float *table = table_out ? table_out : tw.table;
 
+  // the packed image holds the bridge matrices as fp16: fp16 operands on both sides
+  const bool f16 = pk != nullptr && packed_f16(cfg);
   BD_TRY(launch_zero(counters_of(tw.g), s));
-  BD_TRY(launch_tail_gather(dt, w->codebook, cfg->vocab, Rc, cand_ids, K, kc, n, tw.cg, s));
+  BD_TRY(launch_tail_gather(dt, w->codebook, cfg->vocab, Rc, cand_ids, K, kc, n, tw.cg, s, f16));
   {  // G_p C_s and A C_s for every predecessor candidate (codebook rows are exact inputs)
     GemmPlan p = make_plan(cfg, tw.cg, n, Rc);
+    if (f16) p.dtype = GT_F16;
     add_w(p, w->g_pred, Mc, pk, PL.g_pred);
     add_w(p, w->a_val, Mc, pk, PL.a_val);
     p.args.epi = EPI_STORE_F32;
@@ -1144,13 +1151,14 @@ bd_status bd_refine_tail(const bd_config *cfg, const bd_weights *w, const float 
     p.args.seg[1].out_col = Mc;
     BD_TRY(launch_gemm(p, scratch_of(tw.g), s));
   }
-  const bool split = dt == BD_BF16;
+  const bool split = dt == BD_BF16 && !f16;
   const size_t lo_m = split ? static_cast<size_t>(pad16(n)) * Mc : 0;
   BD_TRY(launch_tail_message(dt, tw.pre2, gc, w->gate_bias, K, W, kc, Mc,
-                             std::sqrt(static_cast<float>(Rc)), n, tw.m, lo_m, s));
+                             std::sqrt(static_cast<float>(Rc)), n, tw.m, lo_m, s, f16));
   {  // delta = W_L m, the refined write before its RMS scale
     GemmPlan p = make_plan(cfg, tw.m, n, Mc);
     p.split = split;
+    if (f16) p.dtype = GT_F16;
     add_w(p, w->layer[cfg->n_layers - 1].w_write, H, pk, PL.w_write[cfg->n_layers - 1]);
     p.args.epi = EPI_STORE_F32;
     p.args.out_f32 = tw.delta;

@@ -12,8 +12,8 @@
 //       anchors sqrt(Rc) C[a]); g = sigmoid(G c_t + G_p c_{t-1} + b), m_t = g * (A c_{t-1}),
 //       m_0 = 0; the tail export of the last layer
 //   P4  x_t += r_t W_l m_t for every row but the anchor
-// The products run on mma.sync across the CTA's 8 warps, on bf16 hi + lo activation pairs
-// (~16 mantissa bits): at these shapes (N = 32 token columns, K-steps only) a single thread
+// The products run on mma.sync across the CTA's 8 warps with the packed image's fp16
+// weights and fp16 hi + lo activation pairs (~22 mantissa bits): at these shapes (N = 32 token columns, K-steps only) a single thread
 // issuing tcgen05.mma spends ~40 ns per instruction, more than the whole product takes on
 // the warps' tensor instructions.  Weights come from the packed image, whose boxes are in
 // the 128-byte-swizzled order (conflict-free ldmatrix): the first phase's as bulk copies
@@ -41,10 +41,10 @@ constexpr int kBrMaxGz = 16;     // 128-row groups of the code: Rc <= 2048
 constexpr int kP3Stride = 6144;  // bytes per K box of the P3 weights: G, G_p, A slices of 16 rows
 constexpr int kP4Stride = 8192;  // bytes per K box of the P4 weights: two 32-row items
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
       "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -56,7 +56,7 @@ __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                : "r"(addr));
 }
 // A fragment (16 rows x 16 k) of a weight slice in the packed image's order: rows of 128
-// bytes (64 bf16 of one K box), 16-byte chunk c of row r stored at chunk c ^ (r % 8); the
+// bytes (64 fp16 of one K box), 16-byte chunk c of row r stored at chunk c ^ (r % 8); the
 // slice starts at a row that is a multiple of 8.  kc: which 16 columns of the box.
 __device__ __forceinline__ void ld_a(const uint8_t *box, int row0, int kc, uint32_t (&A)[4]) {
   const int lane = threadIdx.x & 31, mi = lane >> 3, ri = lane & 7;
@@ -72,18 +72,21 @@ __device__ __forceinline__ int act_off(int R, int r, int k) {
 }
 // B fragments of 8 tokens x 16 k (k a multiple of 16): hi b0, hi b1, lo b0, lo b1.
 template <int R>
-__device__ __forceinline__ void ld_b(const __nv_bfloat16 *sx, int n0, int k, uint32_t (&Bf)[4]) {
+__device__ __forceinline__ void ld_b(const __half *sx, int n0, int k, uint32_t (&Bf)[4]) {
   const int lane = threadIdx.x & 31, mi = lane >> 3, ri = lane & 7;
   const int row = (mi >> 1) * (R / 2) + n0 + ri;
   ldsm4(smem_u32(sx + act_off(R, row, k + 8 * (mi & 1))), Bf[0], Bf[1], Bf[2], Bf[3]);
 }
 
-// bf16 hi + lo pair of four values (8-byte stores)
-__device__ __forceinline__ void split4(float4 v, __nv_bfloat16 *hi, __nv_bfloat16 *lo) {
-  const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
-  const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-  const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
-  const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+// fp16 hi + lo pair of four values (8-byte stores); a value beyond fp16's range sets the
+// range error instead of passing as inf.
+__device__ __forceinline__ void split4(float4 v, __half *hi, __half *lo) {
+  flag_f16_range(f16_out_of_range(v.x) || f16_out_of_range(v.y) || f16_out_of_range(v.z) ||
+                 f16_out_of_range(v.w));
+  const __half2 h0 = __floats2half2_rn(v.x, v.y), h1 = __floats2half2_rn(v.z, v.w);
+  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  const __half2 l0 = __floats2half2_rn(v.x - f0.x, v.y - f0.y);
+  const __half2 l1 = __floats2half2_rn(v.z - f1.x, v.w - f1.y);
   uint2 uh, ul;
   uh.x = *reinterpret_cast<const uint32_t *>(&h0);
   uh.y = *reinterpret_cast<const uint32_t *>(&h1);
@@ -92,10 +95,11 @@ __device__ __forceinline__ void split4(float4 v, __nv_bfloat16 *hi, __nv_bfloat1
   *reinterpret_cast<uint2 *>(hi) = uh;
   *reinterpret_cast<uint2 *>(lo) = ul;
 }
-__device__ __forceinline__ void put_split(__nv_bfloat16 *hi, __nv_bfloat16 *lo, float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+__device__ __forceinline__ void put_split(__half *hi, __half *lo, float v) {
+  flag_f16_range(f16_out_of_range(v));
+  const __half h = __float2half_rn(v);
   *hi = h;
-  *lo = __float2bfloat16_rn(v - __bfloat162float(h));
+  *lo = __float2half_rn(v - __half2float(h));
 }
 
 // Grid-wide barrier on a counter that starts at zero: every CTA's writes before it are
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
     if (in_p1) {
       const int gi = cta / a.n_kz, q = cta % a.n_kz;
       const int k0 = q * a.kz, klen = min(a.kz, H - k0);
-      __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(sa);
+      __half *sx = reinterpret_cast<__half *>(sa);
       float4 v[NT][kBrMaxJ];
 #pragma unroll
       for (int u = 0; u < NT; ++u)
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
               uint32_t Bf[4], Bf2[4];
               ld_b<R>(sx, nt * 8, b * 64 + kc * 16, Bf);
               ld_b<R>(sx, nt * 8, b * 64 + kc * 16 + 16, Bf2);
-              mma_bf16_16816(acc[nt], A, Bf[0], Bf[1]);
-              mma_bf16_16816(acc2[nt], A2, Bf2[0], Bf2[1]);
-              mma_bf16_16816(acc[nt], A, Bf[2], Bf[3]);
-              mma_bf16_16816(acc2[nt], A2, Bf2[2], Bf2[3]);
+              mma_f16_16816(acc[nt], A, Bf[0], Bf[1]);
+              mma_f16_16816(acc2[nt], A2, Bf2[0], Bf2[1]);
+              mma_f16_16816(acc[nt], A, Bf[2], Bf[3]);
+              mma_f16_16816(acc2[nt], A2, Bf2[2], Bf2[3]);
             }
           }
       }
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
     }
     if (!grid_sync(a.bar + 0, &s_ok)) return;
 
-    // ---- P2: z' = the chunk sums in order, as bf16 hi/lo activation boxes (the anchor
+    // ---- P2: z' = the chunk sums in order, as fp16 hi/lo activation boxes (the anchor
     // rows: their codebook rows); r; |z'|^2 per row group
     for (int it = cta; it < T * gz; it += gridDim.x) {
       const int t = it / gz, gi = it % gz;
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         }
       }
       const int row = gi * 128 + threadIdx.x;
-      __nv_bfloat16 *zh = a.zc + act_off(R, t, row), *zl = a.zc + act_off(R, NTOK + t, row);
+      __half *zh = a.zc + act_off(R, t, row), *zl = a.zc + act_off(R, NTOK + t, row);
       if (t % W == 0) {  // anchor: the code is sqrt(Rc) C[a], its scale applied after the product
         if (threadIdx.x < 128 && row < Rc) {
           int an = a.anchors[t / W];
@@ -295,8 +299,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
             atomicOr(&g_error_word, DEVERR_BAD_INDEX);
             an = 0;
           }
-          *zh = a.codebook[static_cast<size_t>(an) * Rc + row];
-          *zl = __float2bfloat16_rn(0.f);
+          put_split(zh, zl, __bfloat162float(a.codebook[static_cast<size_t>(an) * Rc + row]));
         }
         continue;
       }
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       }
       w1_pending = false;
       const bool ok_w = cta_wait(&mb[0], 0);  // (a failure returns once the codes have landed)
-      const __nv_bfloat16 *sx = reinterpret_cast<const __nv_bfloat16 *>(sa);
+      const __half *sx = reinterpret_cast<const __half *>(sa);
       float acc[3][NT][4] = {};
       for (int b0 = 0, ch = 0; b0 < nbc; b0 += a.p3_boxes, ++ch) {
         const int nb = min(a.p3_boxes, nbc - b0);
@@ -366,8 +369,8 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
             ld_b<R>(sx, nt * 8, ks * 16, Bf);
 #pragma unroll
             for (int mat = 0; mat < 3; ++mat) {
-              mma_bf16_16816(acc[mat][nt], A[mat], Bf[0], Bf[1]);
-              mma_bf16_16816(acc[mat][nt], A[mat], Bf[2], Bf[3]);
+              mma_f16_16816(acc[mat][nt], A[mat], Bf[0], Bf[1]);
+              mma_f16_16816(acc[mat][nt], A[mat], Bf[2], Bf[3]);
             }
           }
         }
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         for (int w = 0; w < kBrThreads / 32; ++w) v += red3[((w * 3 + mat) * 16 + j) * NTOK + t];
         return v * s_scale[t];
       };
-      __nv_bfloat16 *m = a.m;
+      __half *m = a.m;
       for (int idx = threadIdx.x; idx < 16 * T; idx += kBrThreads) {
         const int j = idx % 16, t = idx / 16, jj = j0 + j;
         const float gc = pre(0, j, t);
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       w4_pending = false;
       const bool ok_w = cta_wait(&mb[1], 0), ok_m = cta_wait(&mb[3], 0);
       if (!ok_w || !ok_m) return;
-      const __nv_bfloat16 *sm = reinterpret_cast<const __nv_bfloat16 *>(sa);
+      const __half *sm = reinterpret_cast<const __half *>(sa);
       float *red4 = reinterpret_cast<float *>(sa + static_cast<size_t>(nbm) * kBoxB);
       const int mt = warp & 1, kq = warp >> 1, kw = Mc / 4;
       for (int it = 0; it < my4; ++it) {
@@ -452,8 +455,8 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
           for (int nt = 0; nt < NT; ++nt) {
             uint32_t Bf[4];
             ld_b<R>(sm, nt * 8, k, Bf);
-            mma_bf16_16816(acc[nt], A, Bf[0], Bf[1]);
-            mma_bf16_16816(acc[nt], A, Bf[2], Bf[3]);
+            mma_f16_16816(acc[nt], A, Bf[0], Bf[1]);
+            mma_f16_16816(acc[nt], A, Bf[2], Bf[3]);
           }
         }
 #pragma unroll

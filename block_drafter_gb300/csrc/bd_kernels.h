@@ -1,6 +1,7 @@
 // Launchers of the non-GEMM kernels (attention, norms, embedding, bridge helpers).
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -102,10 +103,10 @@ std::string launch_rows_f16(const float *src, size_t n, void *dst, ZeroSpan z, c
 // c = sqrt(Rc) z / (||z|| + eps) for non-anchor rows; sqrt(Rc) * codebook[anchor] for anchors.
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
                         const int32_t *anchors, int V, int W, float eps, void *c_out,
-                        size_t lo_off, cudaStream_t s);
+                        size_t lo_off, cudaStream_t s, bool out_f16 = false);
 // m_i = sigmoid(G c_i + G_p c_{i-1} + b) * (A c_{i-1}) for i >= 1, m_0 = 0.
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias,
-                           int W, void *m_out, size_t lo_off, cudaStream_t s);
+                           int W, void *m_out, size_t lo_off, cudaStream_t s, bool out_f16 = false);
 // Head post-processing of raw fp32 projections [rows, ld_raw]: for each head of each
 // segment, plain_head_rmsnorm + split-half RoPE (query/key segments) or a copy (value
 // segments), rounded to the config dtype and scattered to its destination.
@@ -153,9 +154,9 @@ struct BridgeArgs {
   const int32_t *anchors;                         // [B]
   float *r;                                       // [T] OUT RMS of the pre-injection rows
   float *zpart, *sspart;                          // [n_kz][T][Rc], [n_kz][T]
-  __nv_bfloat16 *zc;                              // z' hi/lo boxes (2 TP rows x Rc)
+  __half *zc;                                     // z' fp16 hi/lo boxes (2 TP rows x Rc)
   float *zsq;                                     // [T][ceil(Rc / 128)]
-  __nv_bfloat16 *m;                               // message hi/lo boxes (2 TP rows x Mc)
+  __half *m;                                      // message fp16 hi/lo boxes (2 TP rows x Mc)
   float *tail;                                    // tail state export, or null
   unsigned *bar;                                  // [3]
   int T, W, H, Rc, Mc, V, TP;
@@ -208,10 +209,10 @@ std::string launch_rescore(const void *E, int V, int H, const float *hidden, con
 std::string launch_tail_export(const float *x, const float *r, const float *pre, int T, int H,
                                int Mc, float *out, cudaStream_t s);
 std::string launch_tail_gather(int dtype, const void *codebook, int V, int Rc, const int32_t *cand,
-                               int K, int kc, int n_pairs, void *out, cudaStream_t s);
+                               int K, int kc, int n_pairs, void *out, cudaStream_t s, bool out_f16 = false);
 std::string launch_tail_message(int dtype, const float *pre2, const float *gc, const void *bias, int K,
                                 int W, int kc, int Mc, float scale, int n_pairs, void *m_out,
-                                size_t lo_off, cudaStream_t s);
+                                size_t lo_off, cudaStream_t s, bool out_f16 = false);
 std::string launch_tail_scores(int dtype, const float *u, const float *r, const float *delta,
                                const void *embed, const void *gain, const int32_t *cand, int B, int K,
                                int W, int kc, int H, int V, float eps, float *table, cudaStream_t s);

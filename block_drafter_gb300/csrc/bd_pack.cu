@@ -1,9 +1,9 @@
 // Packed weight image: every projection matrix stored as contiguous 16 KB boxes (128 rows
 // x 128 bytes of K) in the 128-byte-swizzled order the tensor cores read from shared
 // memory, so a GEMM pipeline stage is one contiguous bulk copy of kbox boxes.  In a bf16
-// config the attention-branch and MLP matrices and the head are converted to fp16 on the
-// way (exact within fp16's range); the others are a pure permutation (plus zero padding of
-// partial tiles).
+// config every matrix but the feature projection W_feature is converted to fp16 on the way
+// (exact within fp16's range down to 2^-14); W_feature is a pure permutation (plus zero
+// padding of partial tiles).
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -123,9 +123,9 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
   BD_PACK(w->w_feature, nullptr, H, c->n_target_layers * H, false, L.w_feature);
   BD_PACK16(w->embed_head, nullptr, c->vocab, H, false, L.head);
   if (c->code_width > 0) {
-    BD_PACK(w->g_recv, nullptr, c->msg_width, c->code_width, false, L.g_recv);
-    BD_PACK(w->g_pred, nullptr, c->msg_width, c->code_width, false, L.g_pred);
-    BD_PACK(w->a_val, nullptr, c->msg_width, c->code_width, false, L.a_val);
+    BD_PACK16(w->g_recv, nullptr, c->msg_width, c->code_width, false, L.g_recv);
+    BD_PACK16(w->g_pred, nullptr, c->msg_width, c->code_width, false, L.g_pred);
+    BD_PACK16(w->a_val, nullptr, c->msg_width, c->code_width, false, L.a_val);
   }
   for (int l = 0; l < c->n_layers; ++l) {
     const bd_layer_weights &W = w->layer[l];
@@ -136,8 +136,8 @@ std::string pack_all(const bd_config *c, const bd_weights *w, uint8_t *base, cud
     BD_PACK16(W.w_gate, W.w_up, c->ffn, H, true, L.gate_up[l]);
     BD_PACK16(W.w_down, nullptr, H, c->ffn, false, L.w_down[l]);
     if (c->code_width > 0) {
-      BD_PACK(W.r_read, nullptr, c->code_width, H, false, L.r_read[l]);
-      BD_PACK(W.w_write, nullptr, H, c->msg_width, false, L.w_write[l]);
+      BD_PACK16(W.r_read, nullptr, c->code_width, H, false, L.r_read[l]);
+      BD_PACK16(W.w_write, nullptr, H, c->msg_width, false, L.w_write[l]);
     }
     if (c->conv_group > 0) {
       BD_PACK16(W.conv_delta_a, nullptr, 4 * H / c->conv_group, H, false, L.conv_a[l]);

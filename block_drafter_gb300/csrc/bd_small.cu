@@ -3,6 +3,8 @@
 // reduction.  Each launches with programmatic dependent launch and waits for the
 // previous kernel before touching data it produced or consumes.
 #include "bd_device.cuh"
+
+#include <type_traits>
 #include "bd_internal.h"
 #include "bd_kernels.h"
 
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(256) rownorm_kernel(float *x, int H, const T *
 
 template <typename T>
 __device__ __forceinline__ void store_split(T *p, size_t i, size_t lo_off, float v) {
+  if (std::is_same<T, __half>::value) flag_f16_range(f16_out_of_range(v));
   const T h = from_f<T>(v);
   p[i] = h;
   if (lo_off) p[lo_off + i] = from_f<T>(v - to_f<T>(h));
@@ -354,15 +357,15 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   for (int e = 0; e < E; ++e) store_split(dst, e, sg.lo_off, v[e]);
 }
 
-template <typename T>
+template <typename T, typename O>
 __global__ void code_kernel(const float *z, int Rc, const T *codebook, const int32_t *anchors,
-                            int V, int W, float eps, T *c_out, size_t lo_off) {
+                            int V, int W, float eps, O *c_out, size_t lo_off) {
   __shared__ float red[32];
   const int row = blockIdx.x, b = row / W, i = row % W;
   pdl_wait();
   pdl_trigger();
   const float scale = sqrtf(static_cast<float>(Rc));
-  T *c = c_out + static_cast<size_t>(row) * Rc;
+  O *c = c_out + static_cast<size_t>(row) * Rc;
   if (i == 0) {
     int a = anchors[b];
     if (a < 0 || a >= V) {
@@ -381,13 +384,13 @@ __global__ void code_kernel(const float *z, int Rc, const T *codebook, const int
   for (int k = threadIdx.x; k < Rc; k += blockDim.x) store_split(c, k, lo_off, zr[k] * s);
 }
 
-template <typename T>
-__global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, T *m_out,
+template <typename T, typename O>
+__global__ void message_kernel(const float *pre, int Mc, const T *bias, int W, O *m_out,
                                size_t lo_off) {
   const int row = blockIdx.x, i = row % W;
   pdl_wait();
   pdl_trigger();
-  T *m = m_out + static_cast<size_t>(row) * Mc;
+  O *m = m_out + static_cast<size_t>(row) * Mc;
   if (i == 0) {
     for (int k = threadIdx.x; k < Mc; k += blockDim.x) store_split(m, k, lo_off, 0.f);
     return;
@@ -659,9 +662,9 @@ __global__ void tail_export_kernel(const float *x, const float *r, const float *
 
 // Pair n = ((b * (K - 1) + (i - 2)) * kc + p) takes predecessor candidate p of block row
 // i - 1: its codebook row, for the predecessor-gate and value maps.
-template <typename T>
+template <typename T, typename O>
 __global__ void tail_gather_kernel(const T *codebook, int V, int Rc, const int32_t *cand, int K,
-                                   int kc, int n_pairs, T *out) {
+                                   int kc, int n_pairs, O *out) {
   pdl_wait();
   pdl_trigger();
   const int n = blockIdx.x;
@@ -673,14 +676,16 @@ __global__ void tail_gather_kernel(const T *codebook, int V, int Rc, const int32
     s = 0;
   }
   const T *src = codebook + static_cast<size_t>(s) * Rc;
-  for (int k = threadIdx.x; k < Rc; k += blockDim.x) out[static_cast<size_t>(n) * Rc + k] = src[k];
+  for (int k = threadIdx.x; k < Rc; k += blockDim.x)
+    out[static_cast<size_t>(n) * Rc + k] = from_f<O>(to_f<T>(src[k]));
 }
 
 // m = sigmoid(G c_i + sqrt(Rc) G_p C_s + b) * (sqrt(Rc) A C_s) for pair n (row i of request
-// b); pre2 [n][2 Mc] = [G_p C_s, A C_s]; written as the bf16 hi+lo pair of the write GEMM.
-template <typename T>
+// b); pre2 [n][2 Mc] = [G_p C_s, A C_s]; written as the write GEMM's operand (an fp16 row,
+// or a bf16 hi+lo pair).
+template <typename T, typename O>
 __global__ void tail_message_kernel(const float *pre2, const float *gc, const T *bias, int K, int W,
-                                    int kc, int Mc, float scale, T *m_out, size_t lo_off) {
+                                    int kc, int Mc, float scale, O *m_out, size_t lo_off) {
   pdl_wait();
   pdl_trigger();
   const int n = blockIdx.x;
@@ -950,28 +955,36 @@ std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
 
 std::string launch_code(int dtype, const float *z, int rows, int Rc, const void *codebook,
                         const int32_t *anchors, int V, int W, float eps, void *c_out,
-                        size_t lo_off, cudaStream_t s) {
+                        size_t lo_off, cudaStream_t s, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(code_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, z, Rc,
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(code_kernel<__nv_bfloat16, __half>, dim3(rows), dim3(256), 0, s, z, Rc,
+                   static_cast<const __nv_bfloat16 *>(codebook), anchors, V, W, eps,
+                   static_cast<__half *>(c_out), static_cast<size_t>(0));
+  else if (dtype == 0)
+    e = launch_pdl(code_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s, z, Rc,
                    static_cast<const __nv_bfloat16 *>(codebook), anchors, V, W, eps,
                    static_cast<__nv_bfloat16 *>(c_out), lo_off);
   else
-    e = launch_pdl(code_kernel<float>, dim3(rows), dim3(256), 0, s, z, Rc,
+    e = launch_pdl(code_kernel<float, float>, dim3(rows), dim3(256), 0, s, z, Rc,
                    static_cast<const float *>(codebook), anchors, V, W, eps,
                    static_cast<float *>(c_out), lo_off);
   return err("code", e);
 }
 
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias, int W,
-                           void *m_out, size_t lo_off, cudaStream_t s) {
+                           void *m_out, size_t lo_off, cudaStream_t s, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(message_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, pre, Mc,
-                   static_cast<const __nv_bfloat16 *>(bias), W, static_cast<__nv_bfloat16 *>(m_out),
-                   lo_off);
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(message_kernel<__nv_bfloat16, __half>, dim3(rows), dim3(256), 0, s, pre, Mc,
+                   static_cast<const __nv_bfloat16 *>(bias), W, static_cast<__half *>(m_out),
+                   static_cast<size_t>(0));
+  else if (dtype == 0)
+    e = launch_pdl(message_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s, pre,
+                   Mc, static_cast<const __nv_bfloat16 *>(bias), W,
+                   static_cast<__nv_bfloat16 *>(m_out), lo_off);
   else
-    e = launch_pdl(message_kernel<float>, dim3(rows), dim3(256), 0, s, pre, Mc,
+    e = launch_pdl(message_kernel<float, float>, dim3(rows), dim3(256), 0, s, pre, Mc,
                    static_cast<const float *>(bias), W, static_cast<float *>(m_out), lo_off);
   return err("message", e);
 }
@@ -1016,14 +1029,18 @@ std::string launch_tail_export(const float *x, const float *r, const float *pre,
 }
 
 std::string launch_tail_gather(int dtype, const void *codebook, int V, int Rc, const int32_t *cand,
-                               int K, int kc, int n_pairs, void *out, cudaStream_t s) {
+                               int K, int kc, int n_pairs, void *out, cudaStream_t s, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(tail_gather_kernel<__nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s,
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(tail_gather_kernel<__nv_bfloat16, __half>, dim3(n_pairs), dim3(128), 0, s,
+                   static_cast<const __nv_bfloat16 *>(codebook), V, Rc, cand, K, kc, n_pairs,
+                   static_cast<__half *>(out));
+  else if (dtype == 0)
+    e = launch_pdl(tail_gather_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s,
                    static_cast<const __nv_bfloat16 *>(codebook), V, Rc, cand, K, kc, n_pairs,
                    static_cast<__nv_bfloat16 *>(out));
   else
-    e = launch_pdl(tail_gather_kernel<float>, dim3(n_pairs), dim3(128), 0, s,
+    e = launch_pdl(tail_gather_kernel<float, float>, dim3(n_pairs), dim3(128), 0, s,
                    static_cast<const float *>(codebook), V, Rc, cand, K, kc, n_pairs,
                    static_cast<float *>(out));
   return err("tail gather", e);
@@ -1031,14 +1048,18 @@ std::string launch_tail_gather(int dtype, const void *codebook, int V, int Rc, c
 
 std::string launch_tail_message(int dtype, const float *pre2, const float *gc, const void *bias, int K,
                                 int W, int kc, int Mc, float scale, int n_pairs, void *m_out,
-                                size_t lo_off, cudaStream_t s) {
+                                size_t lo_off, cudaStream_t s, bool out_f16) {
   cudaError_t e;
-  if (dtype == 0)
-    e = launch_pdl(tail_message_kernel<__nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s, pre2, gc,
-                   static_cast<const __nv_bfloat16 *>(bias), K, W, kc, Mc, scale,
+  if (dtype == 0 && out_f16)
+    e = launch_pdl(tail_message_kernel<__nv_bfloat16, __half>, dim3(n_pairs), dim3(128), 0, s, pre2,
+                   gc, static_cast<const __nv_bfloat16 *>(bias), K, W, kc, Mc, scale,
+                   static_cast<__half *>(m_out), static_cast<size_t>(0));
+  else if (dtype == 0)
+    e = launch_pdl(tail_message_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(n_pairs), dim3(128), 0, s,
+                   pre2, gc, static_cast<const __nv_bfloat16 *>(bias), K, W, kc, Mc, scale,
                    static_cast<__nv_bfloat16 *>(m_out), lo_off);
   else
-    e = launch_pdl(tail_message_kernel<float>, dim3(n_pairs), dim3(128), 0, s, pre2, gc,
+    e = launch_pdl(tail_message_kernel<float, float>, dim3(n_pairs), dim3(128), 0, s, pre2, gc,
                    static_cast<const float *>(bias), K, W, kc, Mc, scale,
                    static_cast<float *>(m_out), lo_off);
   return err("tail message", e);

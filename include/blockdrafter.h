@@ -154,10 +154,10 @@ size_t bd_packed_bytes(const bd_config *cfg);
  *
  * The image is not only a permutation.  In a bf16 config it stores the attention-branch
  * matrices (W_q, W_k, W_v, W_o, and with conv_group > 0 the attention branch's W_delta),
- * the MLP matrices (W_gate, W_up, W_down, and the MLP branch's W_delta) and the LM head as
- * fp16, and the products that read them then take fp16 activations (see
- * bd_ctx_kv_materialize, bd_draft_round and bd_lm_head_argmax); W_feature and the bridge
- * matrices (R_l, W_l, G, G_p, A) stay bf16, bit for bit.  The
+ * the MLP matrices (W_gate, W_up, W_down, and the MLP branch's W_delta), the bridge
+ * matrices (R_l, W_l, G, G_p, A) and the LM head as fp16, and the products that read them
+ * then take fp16 activations (see bd_ctx_kv_materialize, bd_draft_round, bd_lm_head_argmax
+ * and bd_refine_tail); W_feature stays bf16, bit for bit.  The
  * conversion is exact for every bf16 value of magnitude 2^-14 .. 65504; smaller values
  * become fp16 subnormals with an absolute error of at most 2^-25; a value beyond
  * +-65504 makes the next bd_sync_status return BD_ERR_RANGE.  Results with and without
@@ -230,12 +230,12 @@ typedef struct {
  *   activation that feeds a tensor-core product (normed rows, attention output, SwiGLU
  *   product, codes, messages, queries, softmax weights, the block's own keys/values)
  *   enters as a bf16 hi+lo pair (about 16 significant bits).
- *   With the packed image the Q/K/V, W_o and MLP products read fp16 weights (see
+ *   With the packed image the Q/K/V, W_o, MLP and bridge products read fp16 weights (see
  *   bd_pack_weights) and take fp16 activations (the normed rows, the attention output,
- *   the SwiGLU product: 11 significant bits); the bridge's code read, gate/value maps and
- *   write keep bf16 weights and bf16 hi+lo activation pairs.  An activation beyond the
- *   fp16 range on its way into an fp16 operand is still stored (as +-inf) and makes the
- *   next bd_sync_status return BD_ERR_RANGE.
+ *   the SwiGLU product, the codes and messages: 11 significant bits; for B * W <= 32
+ *   the one-launch bridge takes the codes, messages and the raw residual rows as fp16
+ *   hi+lo pairs).  An activation beyond the fp16 range on its way into an fp16 operand is
+ *   still stored (as +-inf) and makes the next bd_sync_status return BD_ERR_RANGE.
  *   The attention always takes the queries, softmax weights and the block's own keys/values
  *   as bf16 hi+lo pairs against the ring's bf16 keys/values as stored.
  * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for
@@ -361,6 +361,9 @@ bd_status bd_lm_head_topk_fp8(const bd_config *cfg, const bd_weights *w, const v
  * over row i's candidates j.  Row 1 keeps its own scores (its predecessor is the anchor,
  * which the round already used).  The greedy walk takes row 1's lowest-rank best
  * candidate, then for i = 2..K the lowest-rank best of the table row of row i-1's choice.
+ * With the packed image the products read its fp16 G_p, A and W_L and take the codebook
+ * rows and messages as fp16; without it, bf16 weights with exact bf16 codebook rows and
+ * bf16 hi+lo messages.
  *
  *   tail_state   dev fp32, from bd_draft_round of the same B and n_masks
  *   cand_ids     dev int32 [B*K, kc]  candidates of the mask rows (e.g. bd_lm_head_topk)

@@ -891,7 +891,10 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.n1 = bp.n1;
       ba.n3 = bp.n3;
       ba.p3_boxes = bp.p3_boxes;
-      ba.sw_bytes = bp.sw_bytes;
+      ba.off_x = bp.off_x;
+      ba.off_c = bp.off_c;
+      ba.off_w4 = bp.off_w4;
+      ba.off_red = bp.off_red;
       ba.eps = cfg->eps;
       BD_TIMED(BD_TIME_BRIDGE, launch_bridge(ba, bp, sms, s));
     } else if (cfg->code_width > 0) {

@@ -1,9 +1,9 @@
-// Fused DSpine bridge for small blocks ("DSpine for Qwen3.8-27B: Causal Features Through
-// Depth", section "The bridge: read 1,024 features, write through rank 512"; "DSpine 完全
-// 拆解", sections on adjacent causal injection, gating and write-back).  With T = B*W <= 32
-// rows the bridge's three products stream only 19 MB of weights at the 27B size, and as
-// five separate launches (row norm, code read, code, gate maps + message, write) its time
-// was dominated by launch boundaries, dependency waits and split-tile reductions.  Here one
+// Fused DSpine bridge ("DSpine for Qwen3.8-27B: Causal Features Through Depth", section
+// "The bridge: read 1,024 features, write through rank 512"; "DSpine 完全拆解", sections on
+// adjacent causal injection, gating and write-back).  For T = B*W <= 32 rows the
+// bridge's three products stream only 19 MB of weights at the 27B size, and as five
+// separate launches (row norm, code read, code, gate maps + message, write) its time was
+// dominated by launch boundaries, dependency waits and split-tile reductions.  Here one
 // launch of one CTA per SM runs it in four phases separated by grid-wide barriers:
 //   P1  z'_q = R_l[:, K_q] x[:, K_q] per K chunk q, and the chunk's sums of squares of x
 //   P2  z' = sum_q z'_q (fixed order), r_t = RMS(x_t), |z'|^2 partial sums per row group
@@ -13,16 +13,17 @@
 //       m_0 = 0; the tail export of the last layer
 //   P4  x_t += r_t W_l m_t for every row but the anchor
 // The products run on mma.sync across the CTA's 8 warps with the packed image's fp16
-// weights and fp16 hi + lo activation pairs (~22 mantissa bits): at these shapes (N = 32 token columns, K-steps only) a single thread
-// issuing tcgen05.mma spends ~40 ns per instruction, more than the whole product takes on
-// the warps' tensor instructions.  Weights come from the packed image, whose boxes are in
-// the 128-byte-swizzled order (conflict-free ldmatrix): the first phase's as bulk copies
-// issued before the dependency wait, P4's once the CTA's earlier product is done with the
-// weight area (after the code-read product, or after the gate/value CTAs' message).  The
-// activations (x, the codes, the message) are written in the same swizzled box order, so
-// the codes and the message reach shared memory as single bulk copies.  Partial sums are added in a fixed order, so results are deterministic.  Every
-// CTA is resident at once (grid = SM count, one CTA per SM), each wait is bounded
-// (wait_count, mbar_wait), and a wait that gives up ends the launch with the error word set.
+// weights and fp16 activations (the row chunks, codes and messages): at these shapes
+// (N <= 32 token columns, short K per CTA) the warps' tensor instructions finish each
+// product in a few microseconds without a TMEM round trip.  Weights come from the packed
+// image, whose boxes are in the 128-byte-swizzled order (conflict-free ldmatrix): the
+// first phase's as bulk copies issued before the dependency wait, P4's once the CTA's
+// earlier product is done with that area.  The activations (x, the codes, the message)
+// are written in the same swizzled box order, so the codes and the message reach shared
+// memory as single bulk copies.  Partial sums are added in a fixed order, so results are
+// deterministic.  Every CTA is resident at once (grid = SM count, one CTA per SM), each
+// wait is bounded (wait_count, mbar_wait), and a wait that gives up ends the launch with
+// the error word set.
 #include "bd_device.cuh"
 #include "bd_internal.h"
 #include "bd_kernels.h"
@@ -36,7 +37,12 @@ BD_DEFINE_ERROR_TAKER(take_error_word_bridge)
 constexpr int kBrThreads = 256;  // 8 warps
 constexpr int kBrMaxKz = 32;     // K chunks of the code read (P1), at most
 constexpr int kW4Rows = 32;      // rows of W_l per P4 item
-constexpr int kBrMaxJ = 4;       // float4 columns per lane of a P1 chunk: kz <= 512
+// Block rows of one launch (B * W).  The phases are written for any multiple of 16 rows up
+// to 128, but at B * W = 128 (27B geometry) one launch measured slower than the separate
+// products (a 1588 against a 1560 us step): its code read stages 128 rows of fp32 residual
+// per CTA and its gate phase runs on only Mc / 16 CTAs.
+constexpr int kBrMaxT = 32;
+constexpr int kBrMaxJ = 4;       // float4 columns per lane of a P1 chunk row: kz <= 512
 constexpr int kBrMaxGz = 16;     // 128-row groups of the code: Rc <= 2048
 constexpr int kP3Stride = 6144;  // bytes per K box of the P3 weights: G, G_p, A slices of 16 rows
 constexpr int kP4Stride = 8192;  // bytes per K box of the P4 weights: two 32-row items
@@ -64,42 +70,35 @@ __device__ __forceinline__ void ld_a(const uint8_t *box, int row0, int kc, uint3
   ldsm4(smem_u32(box) + row * 128 + ((chunk ^ (row & 7)) << 4), A[0], A[1], A[2], A[3]);
 }
 
-// Activations as the MMA's B operand: [R rows = hi tokens, then lo tokens] x K, stored as
-// K boxes of 64 columns, each box R rows of 128 bytes with the 16-byte chunk c of row r at
-// chunk c ^ (r % 8) (the packed weights' swizzle).  Element offset:
+// Activations as the MMA's B operand: R token rows x K, stored as K boxes of 64 columns,
+// each box R rows of 128 bytes with the 16-byte chunk c of row r at chunk c ^ (r % 8) (the
+// packed weights' swizzle).  Element offset:
 __device__ __forceinline__ int act_off(int R, int r, int k) {
   return (k >> 6) * (R * 64) + r * 64 + ((((k & 63) >> 3) ^ (r & 7)) << 3) + (k & 7);
 }
-// B fragments of 8 tokens x 16 k (k a multiple of 16): hi b0, hi b1, lo b0, lo b1.
+// B fragments of two 8-token n-tiles (tokens n0 .. n0+7 and n0+8 .. n0+15) x 16 k (k a
+// multiple of 16): b0, b1 of the first, then of the second.
 template <int R>
-__device__ __forceinline__ void ld_b(const __half *sx, int n0, int k, uint32_t (&Bf)[4]) {
+__device__ __forceinline__ void ld_b2(const __half *sx, int n0, int k, uint32_t (&Bf)[4]) {
   const int lane = threadIdx.x & 31, mi = lane >> 3, ri = lane & 7;
-  const int row = (mi >> 1) * (R / 2) + n0 + ri;
+  const int row = n0 + (mi >> 1) * 8 + ri;
   ldsm4(smem_u32(sx + act_off(R, row, k + 8 * (mi & 1))), Bf[0], Bf[1], Bf[2], Bf[3]);
 }
 
-// fp16 hi + lo pair of four values (8-byte stores); a value beyond fp16's range sets the
-// range error instead of passing as inf.
-__device__ __forceinline__ void split4(float4 v, __half *hi, __half *lo) {
+// fp16 activation stores (four values: one 8-byte store); a value beyond fp16's range
+// sets the range error instead of passing as inf.
+__device__ __forceinline__ void put4(__half *dst, float4 v) {
   flag_f16_range(f16_out_of_range(v.x) || f16_out_of_range(v.y) || f16_out_of_range(v.z) ||
                  f16_out_of_range(v.w));
   const __half2 h0 = __floats2half2_rn(v.x, v.y), h1 = __floats2half2_rn(v.z, v.w);
-  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-  const __half2 l0 = __floats2half2_rn(v.x - f0.x, v.y - f0.y);
-  const __half2 l1 = __floats2half2_rn(v.z - f1.x, v.w - f1.y);
-  uint2 uh, ul;
-  uh.x = *reinterpret_cast<const uint32_t *>(&h0);
-  uh.y = *reinterpret_cast<const uint32_t *>(&h1);
-  ul.x = *reinterpret_cast<const uint32_t *>(&l0);
-  ul.y = *reinterpret_cast<const uint32_t *>(&l1);
-  *reinterpret_cast<uint2 *>(hi) = uh;
-  *reinterpret_cast<uint2 *>(lo) = ul;
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t *>(&h0);
+  u.y = *reinterpret_cast<const uint32_t *>(&h1);
+  *reinterpret_cast<uint2 *>(dst) = u;
 }
-__device__ __forceinline__ void put_split(__half *hi, __half *lo, float v) {
+__device__ __forceinline__ void put1(__half *dst, float v) {
   flag_f16_range(f16_out_of_range(v));
-  const __half h = __float2half_rn(v);
-  *hi = h;
-  *lo = __float2half_rn(v - __half2float(h));
+  *dst = __float2half_rn(v);
 }
 
 // Grid-wide barrier on a counter that starts at zero: every CTA's writes before it are
@@ -134,15 +133,24 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity) {
 
 template <int NT>
 __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_constant__ BridgeArgs a) {
-  constexpr int NTOK = NT * 8, R = 2 * NTOK;   // B operand rows: hi tokens, then lo tokens
-  constexpr uint32_t kBoxB = R * 128;          // bytes of one 64-column activation box
+  constexpr int NTOK = NT * 8;             // token rows of the activation boxes
+  constexpr int NP = NT / 2;               // pairs of 8-token n-tiles
+  constexpr int NKS3 = 8 / NP;             // P3: warps per token pair, each a K share
+  constexpr int P4P = NP >= 4 ? NP / 4 : 1;       // P4: token pairs per warp
+  constexpr int NKS4 = NP >= 4 ? 1 : 4 / NP;      // P4: K shares of a token pair
+  constexpr uint32_t kBoxB = NTOK * 128;   // bytes of one 64-column activation box
   extern __shared__ __align__(1024) uint8_t br_smem[];
-  uint8_t *sw = br_smem;                // weights: the P1 chunk or the P3 slices, then P4's rows
-  uint8_t *sa = br_smem + a.sw_bytes;   // activation boxes, then fp32 partial-sum tables
+  // shared-memory areas: P1 uses [R chunk | x chunk], P3 [weight slices | code chunk | ...
+  // sums], P4 [message | W_l rows | sums]; an area is refilled only after its phase is done
+  uint8_t *sw = br_smem;                              // P1 / P3 weights, P4 message boxes
+  __half *sx1 = reinterpret_cast<__half *>(br_smem + a.off_x);
+  uint8_t *sc3 = br_smem + a.off_c;
+  uint8_t *sw4 = br_smem + a.off_w4;
+  float *sred = reinterpret_cast<float *>(br_smem + a.off_red);
   // 0: first weights, 1: P4 weights, 2: P3 codes, 3: P4 message
   __shared__ __align__(8) uint64_t mb[4];
   __shared__ float red[kBrThreads / 32];
-  __shared__ float s_scale[32];
+  __shared__ float s_scale[kBrMaxT];
   __shared__ int s_ok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g4 = lane >> 2, t4 = lane & 3;
   const int T = a.T, H = a.H, Rc = a.Rc, Mc = a.Mc, W = a.W, cta = blockIdx.x;
@@ -166,7 +174,7 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       const int p = cta + it * static_cast<int>(gridDim.x);
       const int tw = p * kW4Rows / 128, ro = p * kW4Rows % 128;
       for (int b = 0; b < nbm; ++b)
-        bulk_load(sw + b * kP4Stride + it * 4096,
+        bulk_load(sw4 + b * kP4Stride + it * 4096,
                   a.pk_w + (static_cast<size_t>(tw) * nbm + b) * kPackBox + ro * 128, 4096, &mb[1],
                   pol);
     }
@@ -204,60 +212,61 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
     if (in_p1) {
       const int gi = cta / a.n_kz, q = cta % a.n_kz;
       const int k0 = q * a.kz, klen = min(a.kz, H - k0);
-      __half *sx = reinterpret_cast<__half *>(sa);
-      float4 v[NT][kBrMaxJ];
+      // the chunk of every token row as fp16 (rows past T as zeros); row group 0 also
+      // takes the rows' sums of squares and the tail export
+      // (kRB rows of a warp at a time, every load of the batch issued before any is used)
+      constexpr int kRB = NTOK / (kBrThreads / 32) < 4 ? NTOK / (kBrThreads / 32) : 4;
+      for (int t0 = warp; t0 < NTOK; t0 += kRB * (kBrThreads / 32)) {
+        float4 xv[kRB][kBrMaxJ];
 #pragma unroll
-      for (int u = 0; u < NT; ++u)
+        for (int u = 0; u < kRB; ++u)
 #pragma unroll
-        for (int jj = 0; jj < kBrMaxJ; ++jj) {
-          const int t = warp + 8 * u, j = lane * 4 + jj * 128;
-          v[u][jj] = t < T && j < klen
-                         ? __ldcg(reinterpret_cast<const float4 *>(a.x + static_cast<size_t>(t) * H + k0 + j))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+          for (int jj = 0; jj < kBrMaxJ; ++jj) {
+            const int t = t0 + u * (kBrThreads / 32), j = lane * 4 + jj * 128;
+            xv[u][jj] = t < T && j < klen
+                            ? __ldcg(reinterpret_cast<const float4 *>(a.x + static_cast<size_t>(t) * H + k0 + j))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
 #pragma unroll
-      for (int u = 0; u < NT; ++u) {
-        const int t = warp + 8 * u;
-        float ss = 0.f;
+        for (int u = 0; u < kRB; ++u) {
+          const int t = t0 + u * (kBrThreads / 32);
+          float ss = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < kBrMaxJ; ++jj) {
-          const int j = lane * 4 + jj * 128;
-          if (j >= klen) break;
-          const float4 x4 = v[u][jj];
-          if (gi == 0 && a.tail && t < T)  // u: the pre-injection residual
-            *reinterpret_cast<float4 *>(a.tail + static_cast<size_t>(t) * H + k0 + j) = x4;
-          ss += x4.x * x4.x + x4.y * x4.y + x4.z * x4.z + x4.w * x4.w;
-          split4(x4, sx + act_off(R, t, j), sx + act_off(R, NTOK + t, j));
-        }
-        if (gi == 0 && t < T) {
-          ss = warp_sum(ss);
-          if (lane == 0) a.sspart[q * T + t] = ss;
+          for (int jj = 0; jj < kBrMaxJ; ++jj) {
+            const int j = lane * 4 + jj * 128;
+            if (j >= klen) break;
+            const float4 x4 = xv[u][jj];
+            if (gi == 0 && a.tail && t < T)  // u: the pre-injection residual
+              *reinterpret_cast<float4 *>(a.tail + static_cast<size_t>(t) * H + k0 + j) = x4;
+            ss += x4.x * x4.x + x4.y * x4.y + x4.z * x4.z + x4.w * x4.w;
+            put4(sx1 + act_off(NTOK, t, j), x4);
+          }
+          if (gi == 0 && t < T) {
+            ss = warp_sum(ss);
+            if (lane == 0) a.sspart[q * T + t] = ss;
+          }
         }
       }
       w1_pending = false;
-      if (!cta_wait(&mb[0], 0)) return;
+      if (!cta_wait(&mb[0], 0)) return;  // (its barrier also publishes the activation rows)
       const int r0 = warp * 16;
-      float acc[NT][4] = {}, acc2[NT][4] = {};  // even and odd 16-column steps
+      float acc[NT][4] = {};
       if (gi * 128 + r0 < Rc) {
         for (int b = 0; b < klen / 64; ++b)
 #pragma unroll
-          for (int kc = 0; kc < 4; kc += 2) {
-            uint32_t A[4], A2[4];
+          for (int kc = 0; kc < 4; ++kc) {
+            uint32_t A[4];
             ld_a(sw + b * kPackBox, r0, kc, A);
-            ld_a(sw + b * kPackBox, r0, kc + 1, A2);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              uint32_t Bf[4], Bf2[4];
-              ld_b<R>(sx, nt * 8, b * 64 + kc * 16, Bf);
-              ld_b<R>(sx, nt * 8, b * 64 + kc * 16 + 16, Bf2);
-              mma_f16_16816(acc[nt], A, Bf[0], Bf[1]);
-              mma_f16_16816(acc2[nt], A2, Bf2[0], Bf2[1]);
-              mma_f16_16816(acc[nt], A, Bf[2], Bf[3]);
-              mma_f16_16816(acc2[nt], A2, Bf2[2], Bf2[3]);
+            for (int np = 0; np < NP; ++np) {
+              uint32_t Bf[4];
+              ld_b2<NTOK>(sx1, np * 16, b * 64 + kc * 16, Bf);
+              mma_f16_16816(acc[2 * np], A, Bf[0], Bf[1]);
+              mma_f16_16816(acc[2 * np + 1], A, Bf[2], Bf[3]);
             }
           }
       }
-      __syncthreads();  // every warp is done with the weight area
+      __syncthreads();  // every warp is done with the weight and activation areas
       if (threadIdx.x == 0) {
         fence_proxy_async_shared();
         load_w4();
@@ -270,17 +279,21 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int row = gi * 128 + r0 + g4 + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
-            if (row < Rc && t < T) zp[static_cast<size_t>(t) * Rc + row] = acc[nt][e] + acc2[nt][e];
+            if (row < Rc && t < T) zp[static_cast<size_t>(t) * Rc + row] = acc[nt][e];
           }
       }
     }
     if (!grid_sync(a.bar + 0, &s_ok)) return;
 
-    // ---- P2: z' = the chunk sums in order, as fp16 hi/lo activation boxes (the anchor
-    // rows: their codebook rows); r; |z'|^2 per row group
-    for (int it = cta; it < T * gz; it += gridDim.x) {
-      const int t = it / gz, gi = it % gz;
-      if (gi == 0 && warp == 4) {
+    // ---- P2: z' = the chunk sums in order, as fp16 activation boxes (the anchor rows:
+    // their codebook rows); r; |z'|^2 per row group.  Each half of the CTA (128 threads,
+    // one row each) takes one (token, row group) item per pass.
+    for (int base = cta; base < T * gz; base += 2 * static_cast<int>(gridDim.x)) {
+      const int h = threadIdx.x >> 7, lt = threadIdx.x & 127;
+      const int it = base + h * static_cast<int>(gridDim.x);
+      const bool valid = it < T * gz;
+      const int t = valid ? it / gz : 0, gi = valid ? it % gz : 0;
+      if (valid && gi == 0 && (lt >> 5) == 0) {  // the half's first warp: r_t
         float ss = 0.f;
         for (int q = lane; q < a.n_kz; q += 32) ss += __ldcg(a.sspart + q * T + t);
         ss = warp_sum(ss);
@@ -290,47 +303,51 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
           if (a.tail) a.tail[static_cast<size_t>(T) * H + t] = r;
         }
       }
-      const int row = gi * 128 + threadIdx.x;
-      __half *zh = a.zc + act_off(R, t, row), *zl = a.zc + act_off(R, NTOK + t, row);
-      if (t % W == 0) {  // anchor: the code is sqrt(Rc) C[a], its scale applied after the product
-        if (threadIdx.x < 128 && row < Rc) {
+      const int row = gi * 128 + lt;
+      float z = 0.f;
+      if (valid && row < Rc) {
+        __half *zh = a.zc + act_off(NTOK, t, row);
+        if (t % W == 0) {  // anchor: the code is sqrt(Rc) C[a], its scale applied after the product
           int an = a.anchors[t / W];
           if (an < 0 || an >= a.V) {
             atomicOr(&g_error_word, DEVERR_BAD_INDEX);
             an = 0;
           }
-          put_split(zh, zl, __bfloat162float(a.codebook[static_cast<size_t>(an) * Rc + row]));
+          put1(zh, __bfloat162float(a.codebook[static_cast<size_t>(an) * Rc + row]));
+        } else {
+          float pv[kBrMaxKz];
+#pragma unroll
+          for (int q = 0; q < kBrMaxKz; ++q)
+            pv[q] = q < a.n_kz ? __ldcg(a.zpart + (static_cast<size_t>(q) * T + t) * Rc + row) : 0.f;
+#pragma unroll
+          for (int q = 0; q < kBrMaxKz; ++q) z += pv[q];
+          put1(zh, z);
         }
-        continue;
       }
-      float z = 0.f;
-      if (threadIdx.x < 128 && row < Rc) {
-        float pv[kBrMaxKz];
-#pragma unroll
-        for (int q = 0; q < kBrMaxKz; ++q)
-          pv[q] = q < a.n_kz ? __ldcg(a.zpart + (static_cast<size_t>(q) * T + t) * Rc + row) : 0.f;
-#pragma unroll
-        for (int q = 0; q < kBrMaxKz; ++q) z += pv[q];
-        put_split(zh, zl, z);
-      }
-      const float zz = block_sum(z * z, red);
-      if (threadIdx.x == 0) a.zsq[t * gz + gi] = zz;
+      // |z'|^2 of the half's item: its four warps' sums in order
+      const float v = warp_sum(z * z);
+      if (lane == 0) red[warp] = v;
+      __syncthreads();
+      if (lt == 0 && valid && t % W != 0)
+        a.zsq[t * gz + gi] = ((red[4 * h] + red[4 * h + 1]) + red[4 * h + 2]) + red[4 * h + 3];
+      __syncthreads();
     }
     if (!grid_sync(a.bar + 1, &s_ok)) return;
 
     // ---- P3: [G; G_p; A] z' for rows j0 .. j0+15, scaled per token into the products of
-    // the codes c_t = s_t z'_t; gate maps and message
+    // the codes c_t = s_t z'_t; gate maps and message.  Warp w takes token pair w % NP
+    // (16 columns) and the K steps w / NP, w / NP + NKS3, ...
     if (in_p3) {
       const int j0 = (cta - a.n1) * 16;
-      // the code boxes in chunks of p3_boxes (the rows T .. NTOK-1 hold stale values;
-      // they only reach accumulator columns that are never read)
+      // the code boxes in chunks of p3_boxes (rows T .. NTOK-1 hold stale values; they
+      // only reach accumulator columns that are never read)
       const uint8_t *zc = reinterpret_cast<const uint8_t *>(a.zc);
       auto load_codes = [&](int b0) {  // thread 0
         const int nb = min(a.p3_boxes, nbc - b0);
         fence_proxy_async_global();
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&mb[2], static_cast<uint32_t>(nb) * kBoxB);
-        bulk_load(sa, zc + static_cast<size_t>(b0) * kBoxB, static_cast<uint32_t>(nb) * kBoxB, &mb[2],
+        bulk_load(sc3, zc + static_cast<size_t>(b0) * kBoxB, static_cast<uint32_t>(nb) * kBoxB, &mb[2],
                   policy_evict_first());
       };
       if (threadIdx.x == 0) load_codes(0);
@@ -351,52 +368,49 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       }
       w1_pending = false;
       const bool ok_w = cta_wait(&mb[0], 0);  // (a failure returns once the codes have landed)
-      const __half *sx = reinterpret_cast<const __half *>(sa);
-      float acc[3][NT][4] = {};
+      const __half *sx = reinterpret_cast<const __half *>(sc3);
+      const int tp = warp % NP, ks0 = warp / NP;
+      float acc[3][2][4] = {};
       for (int b0 = 0, ch = 0; b0 < nbc; b0 += a.p3_boxes, ++ch) {
         const int nb = min(a.p3_boxes, nbc - b0);
         if (ch > 0 && threadIdx.x == 0) load_codes(b0);
         const bool ok_c = cta_wait(&mb[2], static_cast<uint32_t>(ch) & 1u);
         if (!ok_w || !ok_c) return;
-        for (int ks = warp; ks < nb * 4; ks += kBrThreads / 32) {
+        for (int ks = ks0; ks < nb * 4; ks += NKS3) {
           const int b = b0 + ks / 4, kc = ks % 4;
           uint32_t A[3][4];
 #pragma unroll
           for (int mat = 0; mat < 3; ++mat) ld_a(sw + b * kP3Stride + mat * 2048, 0, kc, A[mat]);
+          uint32_t Bf[4];
+          ld_b2<NTOK>(sx, tp * 16, ks * 16, Bf);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            uint32_t Bf[4];
-            ld_b<R>(sx, nt * 8, ks * 16, Bf);
-#pragma unroll
-            for (int mat = 0; mat < 3; ++mat) {
-              mma_f16_16816(acc[mat][nt], A[mat], Bf[0], Bf[1]);
-              mma_f16_16816(acc[mat][nt], A[mat], Bf[2], Bf[3]);
-            }
+          for (int mat = 0; mat < 3; ++mat) {
+            mma_f16_16816(acc[mat][0], A[mat], Bf[0], Bf[1]);
+            mma_f16_16816(acc[mat][1], A[mat], Bf[2], Bf[3]);
           }
         }
         __syncthreads();  // the chunk's boxes (and, at the end, the weights) are free
       }
-      // per-warp K partials [warp][mat][16 rows][NTOK], added in warp order and scaled
-      float *red3 = reinterpret_cast<float *>(sa);
+      // K-share partials [share][mat][16 rows][NTOK], added in share order and scaled
 #pragma unroll
       for (int mat = 0; mat < 3; ++mat)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = g4 + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
-            red3[((warp * 3 + mat) * 16 + row) * NTOK + t] = acc[mat][nt][e];
+            const int row = g4 + (e >> 1) * 8, t = tp * 16 + nt * 8 + 2 * t4 + (e & 1);
+            sred[((ks0 * 3 + mat) * 16 + row) * NTOK + t] = acc[mat][nt][e];
           }
       __syncthreads();
       auto pre = [&](int mat, int j, int t) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kBrThreads / 32; ++w) v += red3[((w * 3 + mat) * 16 + j) * NTOK + t];
+        for (int k = 0; k < NKS3; ++k) v += sred[((k * 3 + mat) * 16 + j) * NTOK + t];
         return v * s_scale[t];
       };
       __half *m = a.m;
       for (int idx = threadIdx.x; idx < 16 * T; idx += kBrThreads) {
-        const int j = idx % 16, t = idx / 16, jj = j0 + j;
+        const int t = idx % T, j = idx / T, jj = j0 + j;  // consecutive threads: consecutive t
         const float gc = pre(0, j, t);
         if (a.tail) a.tail[static_cast<size_t>(T) * H + T + static_cast<size_t>(t) * Mc + jj] = gc;  // G c_t
         float mv = 0.f;
@@ -405,10 +419,10 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
           const float g = 1.f / (1.f + expf(-zg));
           mv = g * pre(2, j, t - 1);
         }
-        put_split(m + act_off(R, t, jj), m + act_off(R, NTOK + t, jj), mv);
+        put1(m + act_off(NTOK, t, jj), mv);
       }
-      // the weight area is free since the chunk loop's last barrier: phase 4's rows, issued
-      // now so that their copies overlap the grid barrier
+      // the weight and code areas are free since the chunk loop's last barrier: phase 4's
+      // rows, issued now so that their copies overlap the grid barrier
       if (threadIdx.x == 0) {
         fence_proxy_async_shared();
         load_w4();
@@ -418,14 +432,16 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
     if (!grid_sync(a.bar + 2, &s_ok)) return;
 
     // ---- P4: x_t += r_t W_l m_t, 32 rows of W_l per item (item it, K box b at
-    // b * kP4Stride + it * 4096); warps: two 16-row tiles x four K quarters
+    // b * kP4Stride + it * 4096); warp w: 16-row half w & 1 of the item, and of the four
+    // warp pairs each takes P4P token pairs (NT >= 8) or a K share of one token pair
     if (my4 > 0) {
       if (threadIdx.x == 0) {
         fence_proxy_async_global();
         fence_proxy_async_shared();
         mbar_arrive_expect_tx(&mb[3], static_cast<uint32_t>(nbm) * kBoxB);
-        bulk_load(sa, a.m, static_cast<uint32_t>(nbm) * kBoxB, &mb[3], policy_evict_first());
+        bulk_load(sw, a.m, static_cast<uint32_t>(nbm) * kBoxB, &mb[3], policy_evict_first());
       }
+      if (threadIdx.x < T) s_scale[threadIdx.x] = __ldcg(a.r + threadIdx.x);  // r_t (P3 is done)
       // the residual entries this thread updates, loaded while the copies land
       constexpr int kMaxUpd = 2 * kW4Rows * NTOK / kBrThreads;
       const int n_upd = my4 * kW4Rows * T;
@@ -442,29 +458,30 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
       w4_pending = false;
       const bool ok_w = cta_wait(&mb[1], 0), ok_m = cta_wait(&mb[3], 0);
       if (!ok_w || !ok_m) return;
-      const __half *sm = reinterpret_cast<const __half *>(sa);
-      float *red4 = reinterpret_cast<float *>(sa + static_cast<size_t>(nbm) * kBoxB);
-      const int mt = warp & 1, kq = warp >> 1, kw = Mc / 4;
+      const __half *sm = reinterpret_cast<const __half *>(sw);
+      const int mt = warp & 1, grp = warp >> 1;
+      const int tp0 = NP >= 4 ? grp * P4P : grp % NP, ks = NP >= 4 ? 0 : grp / NP;
+      const int kw = Mc / NKS4;
       for (int it = 0; it < my4; ++it) {
-        float acc[NT][4] = {};
+        float acc[2 * P4P][4] = {};
         for (int s4 = 0; s4 < kw / 16; ++s4) {
-          const int k = kq * kw + s4 * 16, b = k / 64, kc = (k % 64) / 16;
+          const int k = ks * kw + s4 * 16, b = k / 64, kc = (k % 64) / 16;
           uint32_t A[4];
-          ld_a(sw + b * kP4Stride + it * 4096, mt * 16, kc, A);
+          ld_a(sw4 + b * kP4Stride + it * 4096, mt * 16, kc, A);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
+          for (int p = 0; p < P4P; ++p) {
             uint32_t Bf[4];
-            ld_b<R>(sm, nt * 8, k, Bf);
-            mma_f16_16816(acc[nt], A, Bf[0], Bf[1]);
-            mma_f16_16816(acc[nt], A, Bf[2], Bf[3]);
+            ld_b2<NTOK>(sm, (tp0 + p) * 16, k, Bf);
+            mma_f16_16816(acc[2 * p], A, Bf[0], Bf[1]);
+            mma_f16_16816(acc[2 * p + 1], A, Bf[2], Bf[3]);
           }
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < 2 * P4P; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = mt * 16 + g4 + (e >> 1) * 8, t = nt * 8 + 2 * t4 + (e & 1);
-            red4[((it * 4 + kq) * kW4Rows + row) * NTOK + t] = acc[nt][e];
+            const int row = mt * 16 + g4 + (e >> 1) * 8, t = tp0 * 16 + nt * 8 + 2 * t4 + (e & 1);
+            sred[((it * NKS4 + ks) * kW4Rows + row) * NTOK + t] = acc[nt][e];
           }
       }
       __syncthreads();
@@ -477,9 +494,9 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         if (t % W == 0) continue;
         float v = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v += red4[((it * 4 + q) * kW4Rows + row) * NTOK + t];
+        for (int q = 0; q < NKS4; ++q) v += sred[((it * NKS4 + q) * kW4Rows + row) * NTOK + t];
         a.x[static_cast<size_t>(t) * H + (cta + it * static_cast<int>(gridDim.x)) * kW4Rows + row] =
-            xv[u] + __ldcg(a.r + t) * v;
+            xv[u] + s_scale[t] * v;
       }
     }
   };
@@ -502,12 +519,15 @@ static int max_dyn_smem() {
   return v;
 }
 
+// Token rows of the activation boxes for T block rows (the kernel's NT * 8).
+static int bridge_ntok(int T) { return T <= 16 ? 16 : 32; }
+
 BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms) {
   BridgePlan p = {};
-  if (dtype != 0 || T < 1 || T > 32 || H % 64 || Rc % 64 || Mc % 64 || Rc < 64 || Mc < 64 ||
+  if (dtype != 0 || T < 1 || T > kBrMaxT || H % 64 || Rc % 64 || Mc % 64 || Rc < 64 || Mc < 64 ||
       Rc > 128 * kBrMaxGz)
     return p;
-  const size_t ntok = T <= 16 ? 16 : 32, box = 2 * ntok * 128;  // bytes of an activation box
+  const size_t ntok = bridge_ntok(T), box = ntok * 128;  // bytes of an activation box
   const int gz = (Rc + 127) / 128;
   p.n3 = Mc / 16;
   const int avail = sms - p.n3;
@@ -520,18 +540,26 @@ BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms) {
   const int n4 = H / kW4Rows, it4 = (n4 + sms - 1) / sms;
   if (it4 > 2) return p;  // P4 holds two items per K box
   const int nbc = Rc / 64, nbm = Mc / 64;
-  // weight area: the P1 chunk, the P3 slices or the P4 items
-  p.sw_bytes = std::max(static_cast<size_t>(p.kz / 64) * kPackBox,
-                        std::max(static_cast<size_t>(nbc) * kP3Stride, static_cast<size_t>(nbm) * kP4Stride));
-  p.sw_bytes = (p.sw_bytes + 1023) / 1024 * 1024;
-  p.p3_boxes = static_cast<int>(std::min(static_cast<size_t>(nbc), std::max<size_t>(1, 65536 / box)));
-  const size_t red3 = static_cast<size_t>(8) * 3 * 16 * ntok * 4;
-  const size_t p4 = static_cast<size_t>(nbm) * box + static_cast<size_t>(it4) * 4 * kW4Rows * ntok * 4;
-  p.sa_bytes = std::max(std::max(static_cast<size_t>(p.kz / 64) * box, static_cast<size_t>(p.p3_boxes) * box),
-                        std::max(red3, p4));
-  p.smem = p.sw_bytes + p.sa_bytes;
-  const int lim = max_dyn_smem();
-  p.ok = lim > 0 && p.smem + 1024 <= static_cast<size_t>(lim);
+  const int np = static_cast<int>(ntok / 16), nks3 = 8 / np, nks4 = np >= 4 ? 1 : 4 / np;
+  auto up = [](size_t v) { return (v + 1023) / 1024 * 1024; };
+  // P1: [R chunk | x chunk]; P3: [weight slices | code chunk]; P4: [message | W_l rows |
+  // sums] (the P3 sums share P4's area)
+  p.off_x = up(static_cast<size_t>(p.kz / 64) * kPackBox);
+  p.off_c = up(static_cast<size_t>(nbc) * kP3Stride);
+  p.off_w4 = up(static_cast<size_t>(nbm) * box);
+  p.off_red = up(p.off_w4 + static_cast<size_t>(nbm) * kP4Stride);
+  const size_t red3 = static_cast<size_t>(nks3) * 3 * 16 * ntok * 4;
+  const size_t red4 = static_cast<size_t>(it4) * nks4 * kW4Rows * ntok * 4;
+  const size_t p1 = p.off_x + static_cast<size_t>(p.kz / 64) * box;
+  const size_t p4 = p.off_red + std::max(red3, red4);
+  const int lim = max_dyn_smem() - 2048;  // the kernel's static shared memory and alignment
+  // the code chunk: as many boxes as fit beside the weight slices
+  const size_t room = static_cast<size_t>(lim) > p.off_c ? static_cast<size_t>(lim) - p.off_c : 0;
+  p.p3_boxes = static_cast<int>(std::min(static_cast<size_t>(nbc), room / box));
+  if (p.p3_boxes < 1) return p;
+  const size_t p3 = p.off_c + static_cast<size_t>(p.p3_boxes) * box;
+  p.smem = std::max(std::max(p1, p3), p4);
+  p.ok = lim > 0 && p.smem <= static_cast<size_t>(lim);
   return p;
 }
 
@@ -543,7 +571,7 @@ std::string launch_bridge(const BridgeArgs &args, const BridgePlan &plan, int sm
     if (r != cudaSuccess) return r;
     return launch_pdl(kernel, dim3(sms), dim3(kBrThreads), plan.smem, s, args);
   };
-  if (args.T <= 16)
+  if (bridge_ntok(args.T) == 16)
     e = go(bridge_kernel<2>);
   else
     e = go(bridge_kernel<4>);

@@ -161,7 +161,7 @@ struct BridgeArgs {
   unsigned *bar;                                  // [3]
   int T, W, H, Rc, Mc, V, TP;
   int n_kz, kz, n1, n3, p3_boxes;                 // from the plan
-  size_t sw_bytes;
+  size_t off_x, off_c, off_w4, off_red;           // shared-memory areas (from the plan)
   float eps;
 };
 // Work split and shared-memory areas of one launch; ok = false when the shape does not fit.
@@ -170,7 +170,8 @@ struct BridgePlan {
   int n_kz, kz;   // K chunks of the code read (P1 CTAs: ceil(Rc / 128) * n_kz)
   int n1, n3;     // CTAs of P1 and of P3 (Mc / 16)
   int p3_boxes;   // K boxes of the codes staged at once in P3
-  size_t sw_bytes, sa_bytes, smem;  // weight area, activation area, their sum
+  size_t off_x, off_c, off_w4, off_red;  // P1 activations, P3 codes, P4 W_l rows, sums
+  size_t smem;                           // dynamic shared memory of the launch
 };
 BridgePlan bridge_plan(int dtype, int T, int H, int Rc, int Mc, int sms);
 std::string launch_bridge(const BridgeArgs &args, const BridgePlan &plan, int sms, cudaStream_t s);

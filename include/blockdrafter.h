@@ -233,9 +233,9 @@ typedef struct {
  *   With the packed image the Q/K/V, W_o, MLP and bridge products read fp16 weights (see
  *   bd_pack_weights) and take fp16 activations (the normed rows, the attention output,
  *   the SwiGLU product, the codes and messages: 11 significant bits; for B * W <= 32
- *   the one-launch bridge takes the codes, messages and the raw residual rows as fp16
- *   hi+lo pairs).  An activation beyond the fp16 range on its way into an fp16 operand is
- *   still stored (as +-inf) and makes the next bd_sync_status return BD_ERR_RANGE.
+ *   the one-launch bridge also takes the raw residual rows, unnormalised, as fp16).  An
+ *   activation beyond the fp16 range on its way into an fp16 operand is still stored (as
+ *   +-inf) and makes the next bd_sync_status return BD_ERR_RANGE.
  *   The attention always takes the queries, softmax weights and the block's own keys/values
  *   as bf16 hi+lo pairs against the ring's bf16 keys/values as stored.
  * [DFlash-notes] draft input table and per-layer equations; [Bridge] and [Gate] for

@@ -213,7 +213,10 @@ def test_catch_up_round_full_size(geo, requests):
     cu = CatchUp(geo, 0, (geo.W,) * geo.batch, gen_device="cuda")
     fused = cu.run_fused()
     sep = cu.run_separate()
-    check_against_separate(cu, fused, sep)
+    # the one-launch bridge rounds the raw residual rows to fp16 (11 bits): where the two
+    # paths' rings differ by a bf16 unit, those roundings can land on either side, and five
+    # layers carry that to ~1e-3 of the hidden rows (each path is also held to the oracle)
+    check_against_separate(cu, fused, sep, h_tol=2e-3)
     ta, tb = fused["tokens"].cpu().numpy(), sep["tokens"].cpu().numpy()
     rep, worst = check_against_oracle(cu, fused, requests)
     print(geo.name, rep, "ring err", worst, "token diff vs separate", int((ta != tb).sum()))

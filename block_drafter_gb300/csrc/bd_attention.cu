@@ -54,7 +54,7 @@ constexpr uint32_t kOffV = kOffK + 2 * 2 * kAtom;   // [2 stages] value tiles
 constexpr uint32_t kOffP = kOffV + 2 * 2 * kAtom;   // atom 0: hi probabilities, atom 1: lo
 constexpr uint32_t kOffRed = kOffP + 2 * kAtom;     // m_ref[64], alpha[64], l[64], q_row[64], red[4][64]
 constexpr uint32_t kOffBar = kOffRed + 8 * 64 * 4;
-constexpr int kNumBars = 15;  // full_k/v[2], empty_k/v[2], sfull[2], sfree[2], pfull, pvdone, qready
+constexpr int kNumBars = 16;  // full_k/v[2], empty_k/v[2], sfull[2], sfree[2], pfull, pvdone, qready, qtma
 constexpr size_t kAttSmem = kOffBar + kNumBars * 8 + 16 + 1024;
 // TMEM columns: S^T double buffer at 0 and 128, O^T at 256
 constexpr uint32_t kTmemCols = 512;
@@ -63,6 +63,7 @@ constexpr uint32_t kTmemO = 256;
 struct AttMaps {
   CUtensorMap ring_k, ring_v;  // [B*Hkv*cap rows, D], box 128 rows x 64
   CUtensorMap blk_k, blk_v;    // [2*B*Hkv*W rows (hi plane, lo plane), D], box 16 rows x 64
+  CUtensorMap q;               // [2*B*W rows (hi plane, lo plane), Hq*D], box W rows x 64
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -100,9 +101,9 @@ __device__ __forceinline__ long long slot_position(long long F, int cap, int s) 
 // completed, a V stage once its P.V has; both streams are polled without blocking.
 template <int D>
 __device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm, uint64_t *full_k,
-                             uint64_t *full_v, uint64_t *empty_k, uint64_t *empty_v, int b, int g,
-                             long long F, int t_begin, int n_ctx, int nt, volatile int *sabort,
-                             int &issued_k, int &issued_v) {
+                             uint64_t *full_v, uint64_t *empty_k, uint64_t *empty_v, uint64_t *qtma,
+                             int b, int g, long long F, int t_begin, int n_ctx, int nt,
+                             volatile int *sabort, int &issued_k, int &issued_v) {
   constexpr int NB = D / 64;  // 64-column boxes per row
   const uint64_t pol_ring = policy_evict_first();
   const uint64_t pol_blk = policy_evict_last();
@@ -153,6 +154,16 @@ __device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm,
     tk = tv = 1;
   }
   pdl_wait();
+  if (qtma != nullptr) {  // the query tile: hi rows 0..63, lo rows 64..127, W rows per head
+    const int G = a.n_q_heads / a.n_kv_heads, W = a.W, T = a.B * a.W;
+    mbar_arrive_expect_tx(qtma, static_cast<uint32_t>(2 * G * NB * W * 128));
+    for (int p = 0; p < 2; ++p)
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int kb = 0; kb < NB; ++kb)
+          tma_load_2d(sm + kOffQ + kb * kAtom + (p * 64 + hh * W) * 128, &maps.q, qtma,
+                      (g * G + hh) * D + kb * 64, p * T + b * W, pol_blk);
+  }
   unsigned long long last = globaltimer();
   while (tk < nt || tv < nt) {
     if (*sabort) return;
@@ -179,11 +190,11 @@ __device__ void att_producer(const AttMaps &maps, const AttArgs &a, uint8_t *sm,
 template <int D>
 __device__ void att_mma(uint8_t *sm, uint64_t *full_k, uint64_t *full_v, uint64_t *empty_k,
                         uint64_t *empty_v, uint64_t *sfull, uint64_t *sfree, uint64_t *pfull,
-                        uint64_t *pvdone, uint64_t *qready, uint32_t tmem, int n_ctx, int nt,
-                        volatile int *sabort) {
+                        uint64_t *pvdone, uint64_t *qready, uint64_t *qtma, uint32_t tmem, int n_ctx,
+                        int nt, volatile int *sabort) {
   const uint32_t idesc_s = umma_idesc(1, 128, 128);                           // both K-major
   const uint32_t idesc_o = umma_idesc(1, 128, 128) | (1u << 15) | (1u << 16);  // both MN-major
-  if (!mbar_wait(qready, 0)) {
+  if (!mbar_wait(qready, 0) || (qtma != nullptr && !mbar_wait(qtma, 0))) {
     *sabort = 1;
     return;
   }
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint64_t *full_k = bars, *full_v = bars + 2, *empty_k = bars + 4, *empty_v = bars + 6;
   uint64_t *sfull = bars + 8, *sfree = bars + 10;
-  uint64_t *pfull = bars + 12, *pvdone = bars + 13, *qready = bars + 14;
+  uint64_t *pfull = bars + 12, *pvdone = bars + 13, *qready = bars + 14, *qtma = bars + 15;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *sabort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -410,6 +421,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int t_begin = min(n_tiles, split * per);
   const int n_ctx = min(n_tiles, t_begin + per) - t_begin;
   const bool do_block = split == a.n_splits - 1;
+  const bool q_tma = W % 8 == 0;  // the query tile by TMA (see the softmax warps' Q load)
   const int nt = n_ctx + (do_block ? 1 : 0);
 
   if (tid == 0) {
@@ -426,6 +438,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_init(pfull, kSoftThreads);
     mbar_init(pvdone, 1);
     mbar_init(qready, kSoftThreads);
+    mbar_init(qtma, 1);
     *sabort = 0;
     fence_barrier_init();
   }
@@ -434,6 +447,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     tma_prefetch_desc(&maps.ring_v);
     tma_prefetch_desc(&maps.blk_k);
     tma_prefetch_desc(&maps.blk_v);
+    tma_prefetch_desc(&maps.q);
   }
   if (warp == 1) {  // TMEM before the trigger: a dependent kernel cannot take it first
     tmem_alloc(tmem_slot, kTmemCols);
@@ -448,13 +462,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   int issued_k = 0, issued_v = 0;
   if (warp == 0) {
     if (lane == 0)
-      att_producer<D>(maps, a, sm, full_k, full_v, empty_k, empty_v, b, g, F, t_begin, n_ctx, nt, sabort,
-                      issued_k, issued_v);
+      att_producer<D>(maps, a, sm, full_k, full_v, empty_k, empty_v, q_tma ? qtma : nullptr, b, g, F,
+                      t_begin, n_ctx, nt, sabort, issued_k, issued_v);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0)
-      att_mma<D>(sm, full_k, full_v, empty_k, empty_v, sfull, sfree, pfull, pvdone, qready, tmem, n_ctx, nt,
-                 sabort);
+      att_mma<D>(sm, full_k, full_v, empty_k, empty_v, sfull, sfree, pfull, pvdone, qready,
+                 q_tma ? qtma : nullptr, tmem, n_ctx, nt, sabort);
     __syncwarp();
   } else {
     // softmax warps 2..9: lane quarter qd of the tiles (key row / output dim kr), query
@@ -475,10 +489,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     pdl_wait();
     // query tile (queried rows already scaled by log2(e)/sqrt(D), so the scores come out in
     // log2 units): tile row r (hi plane) and row 64 + r (lo plane) hold query r =
-    // head_in_group*W + i.  Each thread copies one 64-column half of one plane row.
+    // head_in_group*W + i.  With W a multiple of 8 the producer loads it by TMA (each
+    // head's W rows land 1024-byte aligned) and these threads only clear the rows past R;
+    // else each thread copies one 64-column half of one plane row.
     {
       const int n = st_id & 127, half = st_id >> 7, plane = n >> 6, r = n & 63;
-      if (half * 64 < D) {
+      if (q_tma) {
+        if (half * 64 < D && r >= R)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(sm + kOffQ + half * kAtom + n * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
+      } else if (half * 64 < D) {
         const bool ok = r < R;
         const int hh = ok ? r / W : 0, i = ok ? r % W : 0;
         const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -692,6 +713,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // a wait gave up: let the loads still in flight land before the CTA exits (bounded)
     for (int t = max(0, issued_k - 2); t < issued_k; ++t) mbar_wait(&full_k[t & 1], (t >> 1) & 1);
     for (int t = max(0, issued_v - 2); t < issued_v; ++t) mbar_wait(&full_v[t & 1], (t >> 1) & 1);
+    if (q_tma) mbar_wait(qtma, 0);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -842,7 +864,9 @@ std::string launch_attention(const AttArgs &a, int dtype, cudaStream_t stream) {
   if (!(err = make_tensor_map_2d(&m.ring_k, a.ring_k, GT_BF16, D, ring_rows, 64, kTileKeys, true)).empty() ||
       !(err = make_tensor_map_2d(&m.ring_v, a.ring_v, GT_BF16, D, ring_rows, 64, kTileKeys, true)).empty() ||
       !(err = make_tensor_map_2d(&m.blk_k, a.blk_k, GT_BF16, D, blk_rows, 64, 16, true)).empty() ||
-      !(err = make_tensor_map_2d(&m.blk_v, a.blk_v, GT_BF16, D, blk_rows, 64, 16, true)).empty())
+      !(err = make_tensor_map_2d(&m.blk_v, a.blk_v, GT_BF16, D, blk_rows, 64, 16, true)).empty() ||
+      !(err = make_tensor_map_2d(&m.q, a.q, GT_BF16, a.n_q_heads * D, static_cast<int>(2 * T), 64,
+                                 a.W <= 256 ? a.W : 256, true)).empty())
     return err;
   e = D == 128 ? launch_tc<128>(m, a, stream) : launch_tc<64>(m, a, stream);
   if (e != cudaSuccess) return std::string("attention launch: ") + cudaGetErrorString(e);

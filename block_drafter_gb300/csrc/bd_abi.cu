@@ -885,7 +885,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.Rc = cfg->code_width;
       ba.Mc = cfg->msg_width;
       ba.V = cfg->vocab;
-      ba.TP = TP;
       ba.n_kz = bp.n_kz;
       ba.kz = bp.kz;
       ba.n1 = bp.n1;

@@ -154,12 +154,12 @@ struct BridgeArgs {
   const int32_t *anchors;                         // [B]
   float *r;                                       // [T] OUT RMS of the pre-injection rows
   float *zpart, *sspart;                          // [n_kz][T][Rc], [n_kz][T]
-  __half *zc;                                     // z' fp16 hi/lo boxes (2 TP rows x Rc)
+  __half *zc;                                     // z' fp16 activation boxes (16 or 32 rows x Rc)
   float *zsq;                                     // [T][ceil(Rc / 128)]
-  __half *m;                                      // message fp16 hi/lo boxes (2 TP rows x Mc)
+  __half *m;                                      // message fp16 boxes (16 or 32 rows x Mc)
   float *tail;                                    // tail state export, or null
-  unsigned *bar;                                  // [3]
-  int T, W, H, Rc, Mc, V, TP;
+  unsigned *bar;                                  // [3] grid-barrier counters
+  int T, W, H, Rc, Mc, V;
   int n_kz, kz, n1, n3, p3_boxes;                 // from the plan
   size_t off_x, off_c, off_w4, off_red;           // shared-memory areas (from the plan)
   float eps;

@@ -525,7 +525,7 @@ __device__ __forceinline__ void emit_rows(const GemmMaps &maps, const GemmArgs &
         const int c = c0 + jj;
         const float g = v[jj];
         const float u = es.xbuf[r * kXStride + c];
-        const float h = g / (1.0f + __expf(-g)) * u;
+        const float h = __fdividef(g, 1.0f + __expf(-g)) * u;  // SiLU(g) u (-> 0 as g -> -inf)
         if constexpr (std::is_same<T, __half>::value) bad |= f16_out_of_range(h);
         const T hv = from_f<T>(h);
         hi[c * 64 + r] = hv;

@@ -509,30 +509,30 @@ __device__ __forceinline__ void emit_rows(const GemmMaps &maps, const GemmArgs &
                                           int tok0, int j0, const EpiPos &ps,
                                           const float (&v)[kCW], EpiSmem &es) {
   const int r = ps.r, c0 = ps.c0;
-  if (EPI == EPI_SWIGLU && r >= 64) {  // up features go to the gate rows' threads
+  if (EPI == EPI_SWIGLU) {  // the chunk goes through the exchange buffer (see below)
 #pragma unroll
-    for (int jj = 0; jj < kCW; ++jj) es.xbuf[(r - 64) * kXStride + c0 + jj] = v[jj];
+    for (int jj = 0; jj < kCW; ++jj) es.xbuf[r * kXStride + c0 + jj] = v[jj];
   }
   uint8_t *sb = stage_claim(es, ps.et);
   if constexpr (EPI == EPI_SWIGLU) {
-    // rows 0..63: gate features f, rows 64..127: up features f (same f)
-    if (r < 64) {
-      T *hi = reinterpret_cast<T *>(sb);
-      T *lo = hi + 16 * 64;
-      bool bad = false;
+    // rows 0..63: gate features f, rows 64..127: up features f (same f); thread et takes
+    // feature et % 64 of tokens 4 (et / 64) .. + 3
+    static_assert(kEpiThreads == 256, "64 features x 4 token groups");
+    T *hi = reinterpret_cast<T *>(sb);
+    T *lo = hi + 16 * 64;
+    const int f = ps.et & 63, cb = (ps.et >> 6) * 4;
+    bool bad = false;
 #pragma unroll
-      for (int jj = 0; jj < kCW; ++jj) {
-        const int c = c0 + jj;
-        const float g = v[jj];
-        const float u = es.xbuf[r * kXStride + c];
-        const float h = __fdividef(g, 1.0f + __expf(-g)) * u;  // SiLU(g) u (-> 0 as g -> -inf)
-        if constexpr (std::is_same<T, __half>::value) bad |= f16_out_of_range(h);
-        const T hv = from_f<T>(h);
-        hi[c * 64 + r] = hv;
-        if (p.act_lo) lo[c * 64 + r] = from_f<T>(h - to_f<T>(hv));
-      }
-      flag_f16_range(bad);
+    for (int k = 0; k < 4; ++k) {
+      const int c = cb + k;
+      const float g = es.xbuf[f * kXStride + c], u = es.xbuf[(64 + f) * kXStride + c];
+      const float h = __fdividef(g, 1.0f + __expf(-g)) * u;  // SiLU(g) u (-> 0 as g -> -inf)
+      if constexpr (std::is_same<T, __half>::value) bad |= f16_out_of_range(h);
+      const T hv = from_f<T>(h);
+      hi[c * 64 + f] = hv;
+      if (p.act_lo) lo[c * 64 + f] = from_f<T>(h - to_f<T>(hv));
     }
+    flag_f16_range(bad);
   } else {
     float *f = reinterpret_cast<float *>(sb);
 #pragma unroll

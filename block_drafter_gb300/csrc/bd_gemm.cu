@@ -139,8 +139,8 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
     return static_cast<uint32_t>(boxes(kbi)) * (kATileBytes + box_b);
   };
 
-  auto load_a = [&](int m_tile, int kbi, uint8_t *dst, uint64_t *bar) {
-    const int s = p.pair_mode ? 0 : seg_of_tile(p, m_tile);
+  // s: the tile's weight segment (looked up once per tile)
+  auto load_a = [&](int m_tile, int s, int kbi, uint8_t *dst, uint64_t *bar) {
     const int nb = boxes(kbi);
     if (p.packed) {  // the unit's boxes are one contiguous piece of the packed image
       const GemmSeg &sg = p.seg[s];
@@ -185,30 +185,38 @@ __device__ void gemm_producer(const GemmMaps &maps, const GemmArgs &p, uint8_t *
     int tile, kb0, kb1, q = 0;
     while (q < pre && w.next(tile, kb0, kb1)) {
       const int m_tile = tile / p.n_tiles_n;
+      const int sg = p.pair_mode ? 0 : seg_of_tile(p, m_tile);
       for (int kbi = kb0; kbi < kb1 && q < pre; ++kbi, ++q) {
         mbar_arrive_expect_tx(&full[q], unit_bytes(kbi));
-        load_a(m_tile, kbi, sA + static_cast<size_t>(q) * a_bytes, &full[q]);
+        load_a(m_tile, sg, kbi, sA + static_cast<size_t>(q) * a_bytes, &full[q]);
       }
     }
   }
   pdl_wait();
   SegWalk w{u0, u1, p.kb};
   int tile, kb0, kb1;
-  long long q = 0;
+  // stage s of pass `round` over the ring (counted incrementally: no division per stage)
+  int q = 0, s = 0;
+  uint32_t round = 0;
   while (w.next(tile, kb0, kb1)) {
     const int m_tile = tile / p.n_tiles_n, n_tile = tile % p.n_tiles_n;
-    for (int kbi = kb0; kbi < kb1; ++kbi, ++q) {
-      const int s = static_cast<int>(q % S);
-      const uint32_t round = static_cast<uint32_t>(q / S);
+    const int sg = p.pair_mode ? 0 : seg_of_tile(p, m_tile);
+    for (int kbi = kb0; kbi < kb1; ++kbi) {
       if (q >= pre) {
         if (*sabort || !mbar_wait(&empty[s], (round & 1u) ^ 1u)) {
           *sabort = 1;
           return;
         }
         mbar_arrive_expect_tx(&full[s], unit_bytes(kbi));
-        load_a(m_tile, kbi, sA + static_cast<size_t>(s) * a_bytes, &full[s]);
+        load_a(m_tile, sg, kbi, sA + static_cast<size_t>(s) * a_bytes, &full[s]);
+      } else {
+        ++q;
       }
       load_b(n_tile, kbi, sB + static_cast<size_t>(s) * b_bytes, &full[s]);
+      if (++s == S) {
+        s = 0;
+        ++round;
+      }
     }
   }
 }
@@ -228,7 +236,8 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
   const int n_boxes = (p.K + BK - 1) / BK;
   SegWalk w{u0, u1, p.kb};
   int tile, kb0, kb1, e = 0;
-  long long q = 0;
+  int s = 0;           // stage of the next unit
+  uint32_t phase = 0;  // parity of its pass over the ring
   while (w.next(tile, kb0, kb1)) {
     const int a = e & 1;
     const uint32_t ra = static_cast<uint32_t>(e >> 1);
@@ -238,9 +247,8 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
     }
     tc_fence_after();
     const uint32_t d = tmem_base + static_cast<uint32_t>(a * p.block_n);
-    for (int kbi = kb0; kbi < kb1; ++kbi, ++q) {
-      const int s = static_cast<int>(q % S);
-      if (*sabort || !mbar_wait(&full[s], static_cast<uint32_t>(q / S) & 1u)) {
+    for (int kbi = kb0; kbi < kb1; ++kbi) {
+      if (*sabort || !mbar_wait(&full[s], phase)) {
         *sabort = 1;
         return;
       }
@@ -263,6 +271,10 @@ __device__ void gemm_mma(const GemmArgs &p, uint8_t *sA, uint8_t *sB, uint64_t *
         }
       }
       umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+      }
     }
     umma_commit(&accf[a]);     // accumulator ready for the epilogue
     ++e;

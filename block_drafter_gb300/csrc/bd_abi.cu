@@ -237,9 +237,8 @@ struct RoundWs {
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
 };
 int pad16(int n) { return (n + 15) / 16 * 16; }
-// Upper bound on the n-tiles of a GEMM over n tokens (split activations: 128 tokens per
-// tile; otherwise gemm_block_n's tile, never smaller).
-int n_tiles_of(int n) { return (pad16(n) + 127) / 128; }
+// Upper bound on the n-tiles of a GEMM over n tokens.
+int n_tiles_of(int n) { return gemm_max_n_tiles(n); }
 // Tiles of the round's largest GEMM: the Q/K/V product also carries the T_q - T pending
 // context rows, the others the T block rows; the catch-up's feature projection has H rows.
 size_t round_max_tiles(const bd_config *c, int T, int Tq) {
@@ -328,8 +327,7 @@ struct MatWs {
   float2 *rope;
 };
 size_t mat_max_tiles(const bd_config *c, int n) {
-  const int bn = gemm_block_n(n);
-  const size_t ntn = static_cast<size_t>((n + bn - 1) / bn);
+  const size_t ntn = static_cast<size_t>(gemm_max_n_tiles(n));
   const size_t kv_tiles = static_cast<size_t>(std::min(c->n_layers, kMaxSegs / 2)) * 2 *
                           tiles_of(c->n_kv_heads * c->head_dim, 128);
   return std::max(tiles_of(c->hidden, 128), kv_tiles) * ntn;

@@ -162,6 +162,8 @@ std::string make_tensor_map_2d(CUtensorMap *out, const void *ptr, int dtype, int
                                int box_inner, int box_outer, bool swizzle, long long stride = 0);
 int num_sms();
 int gemm_block_n(int n_tokens);
+// Upper bound on the token tiles of a GEMM over n_tokens, whatever tile width it takes.
+int gemm_max_n_tiles(int n_tokens);
 
 // Launch; returns an error message or empty string.
 std::string launch_gemm(GemmPlan &plan, const GemmScratch &scratch, cudaStream_t stream);

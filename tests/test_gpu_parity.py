@@ -109,7 +109,10 @@ TINY_DFLASH2 = bdsynth.TINY.with_(name="tiny_dflash2_fp32", conv_group=16)
                                       # 8 rows in a 16-row tile; a code of 192 (a partial
                                       # 128-row tile) with a 128-wide message
                                       (SMALL_BF16.with_(batch=1, n_masks=7), 7),
-                                      (SMALL_BF16.with_(batch=2, code_width=192, msg_width=128), 8)])
+                                      (SMALL_BF16.with_(batch=2, code_width=192, msg_width=128), 8),
+                                      # 96 rows: small-weight products take 64-token tiles (a
+                                      # full one and a ragged one of 32)
+                                      (SMALL_BF16.with_(batch=6), 9)])
 def test_round_matches_oracle(geo, seed):
     case = Hn.Case(geo, seed=seed, max_ctx_rows=128)
     case.fill_rings()

@@ -315,78 +315,92 @@ __device__ __forceinline__ void write_out(const AttArgs &a, int b, int g, int kr
 //   out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max over splits with l_s > 0,
 // reading split s's partial from CTA s of the cluster (distributed shared memory): its
 // [query][D] fp32 tile at kOffP and its per-query m, l.  Each thread takes 4 output columns
-// of a row and issues every remote load it needs (the row's m and l of every split and
-// their 4 columns) before any arithmetic, so a chunk costs one remote round trip and needs
-// no barrier; splits are added in rank order.
-template <int D>
+// of a row per chunk and NCH chunks at a time, and issues every remote load they need (the
+// rows' m and l of the SM <= kMaxSplits splits and up to four splits' columns) before any
+// arithmetic, so NCH chunks cost one remote round trip (plus one per further group of four
+// splits) and need no barrier; splits are added in rank order.
+template <int D, int NCH, int SM>
 __device__ void merge_cluster(const AttArgs &a, int b, int g, int r0, int r1, int tid, uint8_t *sm) {
-  constexpr int kMax = kMaxSplits;
-  constexpr int C4 = D / 4;  // float4 chunks per row
-  const int S = a.n_splits, nr = r1 - r0;
+  constexpr int C4 = D / 4;             // float4 chunks per row
+  constexpr int SB = SM < 4 ? SM : 4;   // splits whose columns are loaded up front
+  const int S = a.n_splits, total = (r1 - r0) * C4;
   const int G = a.n_q_heads / a.n_kv_heads;
   const uint32_t ml_base = smem_u32(sm + kOffRed);  // m_ref[64], then alpha[64], l[64]
   const uint32_t p_base = smem_u32(sm + kOffP);
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-  for (int c = tid; c < nr * C4; c += kSoftThreads) {
-    const int r = c / C4, d4 = c - r * C4, q = r0 + r;
-    const uint32_t o_off = p_base + static_cast<uint32_t>((q * D + 4 * d4) * 4);
-    float m[kMax], l[kMax];
-    float4 v[4];
+  for (int c0 = tid; c0 < total; c0 += NCH * kSoftThreads) {
+    float m[NCH][SM], l[NCH][SM];
+    float4 v[NCH][SB];
 #pragma unroll
-    for (int sp = 0; sp < kMax; ++sp)
-      if (sp < S) {
-        const uint32_t rm = cluster_map(ml_base, static_cast<uint32_t>(sp));
-        m[sp] = ld_cluster_f32(rm + q * 4);
-        l[sp] = ld_cluster_f32(rm + (128 + q) * 4);
-        if (sp < 4) v[sp] = ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(sp)));
-      }
-    float M = -INFINITY;
+    for (int k = 0; k < NCH; ++k) {
+      const int c = c0 + k * kSoftThreads;
+      if (c >= total) break;
+      const int r = c / C4, q = r0 + r;
+      const uint32_t o_off = p_base + static_cast<uint32_t>((q * D + 4 * (c - r * C4)) * 4);
 #pragma unroll
-    for (int sp = 0; sp < kMax; ++sp)
-      if (sp < S && l[sp] > 0.f) M = fmaxf(M, m[sp]);
-    float L = 0.f;
-#pragma unroll
-    for (int sp = 0; sp < kMax; ++sp)
-      if (sp < S) {
-        m[sp] = l[sp] > 0.f ? exp2f(m[sp] - M) : 0.f;  // the split's weight
-        L += m[sp] * l[sp];
-      }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s0 = 0; s0 < kMax; s0 += 4) {
-      if (s0 >= S) break;
-      if (s0 > 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (s0 + k < S) v[k] = ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(s0 + k)));
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (s0 + k < S) {
-          const float w = m[s0 + k];
-          acc.x += w * v[k].x;
-          acc.y += w * v[k].y;
-          acc.z += w * v[k].z;
-          acc.w += w * v[k].w;
+      for (int sp = 0; sp < SM; ++sp)
+        if (sp < S) {
+          const uint32_t rm = cluster_map(ml_base, static_cast<uint32_t>(sp));
+          m[k][sp] = ld_cluster_f32(rm + q * 4);
+          l[k][sp] = ld_cluster_f32(rm + (128 + q) * 4);
+          if (sp < SB) v[k][sp] = ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(sp)));
         }
     }
-    const float il = L > 0.f ? 1.f / L : 0.f;
-    const int hh = q / a.W, i = q - hh * a.W;
-    const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
-                       static_cast<size_t>(g * G + hh) * D + 4 * d4;
-    const float y0 = acc.x * il, y1 = acc.y * il, y2 = acc.z * il, y3 = acc.w * il;
-    if (a.out_f16) {
-      flag_f16_range(f16_out_of_range(y0) || f16_out_of_range(y1) || f16_out_of_range(y2) ||
-                     f16_out_of_range(y3));
-      const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
-      *reinterpret_cast<uint2 *>(static_cast<__half *>(a.out) + idx) =
-          make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
-    } else {
-      uint32_t hw[2], lw[2];
-      split_bf16x2(y0, y1, hw[0], lw[0]);
-      split_bf16x2(y2, y3, hw[1], lw[1]);
-      *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
-      if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      const int c = c0 + k * kSoftThreads;
+      if (c >= total) break;
+      const int r = c / C4, d4 = c - r * C4, q = r0 + r;
+      const uint32_t o_off = p_base + static_cast<uint32_t>((q * D + 4 * d4) * 4);
+      float M = -INFINITY;
+#pragma unroll
+      for (int sp = 0; sp < SM; ++sp)
+        if (sp < S && l[k][sp] > 0.f) M = fmaxf(M, m[k][sp]);
+      float L = 0.f;
+      float w[SM];
+#pragma unroll
+      for (int sp = 0; sp < SM; ++sp)
+        if (sp < S) {
+          w[sp] = l[k][sp] > 0.f ? exp2f(m[k][sp] - M) : 0.f;  // the split's weight
+          L += w[sp] * l[k][sp];
+        }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s0 = 0; s0 < SM; s0 += 4) {
+        if (s0 >= S) break;
+        float4 u[SB];
+#pragma unroll
+        for (int j = 0; j < SB; ++j)
+          if (s0 + j < S)
+            u[j] = s0 == 0 ? v[k][j] : ld_cluster_f4(cluster_map(o_off, static_cast<uint32_t>(s0 + j)));
+#pragma unroll
+        for (int j = 0; j < SB; ++j)
+          if (s0 + j < S) {
+            const float ws = w[s0 + j];
+            acc.x += ws * u[j].x;
+            acc.y += ws * u[j].y;
+            acc.z += ws * u[j].z;
+            acc.w += ws * u[j].w;
+          }
+      }
+      const float il = L > 0.f ? 1.f / L : 0.f;
+      const int hh = q / a.W, i = q - hh * a.W;
+      const size_t idx = (static_cast<size_t>(b) * a.W + i) * a.n_q_heads * D +
+                         static_cast<size_t>(g * G + hh) * D + 4 * d4;
+      const float y0 = acc.x * il, y1 = acc.y * il, y2 = acc.z * il, y3 = acc.w * il;
+      if (a.out_f16) {
+        flag_f16_range(f16_out_of_range(y0) || f16_out_of_range(y1) || f16_out_of_range(y2) ||
+                       f16_out_of_range(y3));
+        const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(a.out) + idx) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+      } else {
+        uint32_t hw[2], lw[2];
+        split_bf16x2(y0, y1, hw[0], lw[0]);
+        split_bf16x2(y2, y3, hw[1], lw[1]);
+        *reinterpret_cast<uint2 *>(out + idx) = make_uint2(hw[0], hw[1]);
+        if (a.out_lo) *reinterpret_cast<uint2 *>(out + a.out_lo + idx) = make_uint2(lw[0], lw[1]);
+      }
     }
   }
 }
@@ -703,7 +717,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     if (warp >= 2) {
       const int rp = (R + a.n_splits - 1) / a.n_splits;
       const int r0 = min(R, split * rp), r1 = min(R, (split + 1) * rp);
-      merge_cluster<D>(a, b, g, r0, r1, tid - 64, sm);
+      // more chunks in flight when fewer splits' values are loaded per chunk
+      if (a.n_splits <= 2)
+        merge_cluster<D, 4, 2>(a, b, g, r0, r1, tid - 64, sm);
+      else if (a.n_splits <= 4)
+        merge_cluster<D, 2, 4>(a, b, g, r0, r1, tid - 64, sm);
+      else
+        merge_cluster<D, 1, kMaxSplits>(a, b, g, r0, r1, tid - 64, sm);
     }
     cluster_sync();  // no CTA leaves while the others still read its partial
   }

@@ -741,7 +741,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       p.args.seg[0].out_col = 0;
       p.args.seg[1].out_col = QD;
       p.args.seg[2].out_col = QD + KD;
-      BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
       HeadPostArgs h;
       memset(&h, 0, sizeof h);
       h.raw = rw.qkv_raw;
@@ -773,7 +772,41 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
         h.frontier = frontier;
         h.min_back = kMaxPendPerReq;
       }
-      BD_TRY(launch_head_post(dt, h, s));
+      if (D == 64 || D == 128) {  // the head post-processing in the product's epilogue
+        QkvPost &e = p.args.qkv;
+        e.D = D;
+        e.W = W;
+        e.n_q_heads = cfg->n_q_heads;
+        e.n_kv_heads = cfg->n_kv_heads;
+        e.T = T;
+        e.n_pend = fuse ? n_pend : 0;
+        e.out_f32 = dt == BD_BF16 ? 0 : 1;
+        e.eps = cfg->eps;
+        e.q_scale = qs;
+        e.rope = rw.rope;
+        e.q_norm = L.q_norm;
+        e.k_norm = L.k_norm;
+        e.q = rw.q;
+        e.kblk = rw.kblk;
+        e.vblk = rw.vblk;
+        e.q_lo = qlo;
+        e.kv_lo = klo;
+        if (fuse) {
+          e.n_req = B;
+          e.min_back = kMaxPendPerReq;
+          e.cap = cfg->ring_capacity[l];
+          e.kring = kv->k[l];
+          e.vring = kv->v[l];
+          e.row_req = pending->request;
+          e.row_pos = pending->pos;
+          e.frontier = frontier;
+        }
+        p.args.epi = EPI_QKV;
+        BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
+      } else {
+        BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
+        BD_TRY(launch_head_post(dt, h, s));
+      }
     }
     // S5: block attention over the ring context and the block
     {

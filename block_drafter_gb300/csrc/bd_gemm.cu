@@ -500,6 +500,110 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs &p, int m_tile, int to
   }
 }
 
+// EPI_QKV, one 16-column chunk of a 128-row tile (one head of D = 128, two of D = 64).  The
+// chunk is exchanged through shared memory; thread et then takes token column et / 16 and
+// the eight rows (head dims) 8 (et % 16) .. + 7, so the D / 8 threads of a head are adjacent
+// lanes of one half-warp: the head's sum of squares is a shuffle tree over them and the RoPE
+// partner of dim d (d +- D/2) sits D / 16 lanes away.
+__device__ __forceinline__ float qkv_gain(const QkvPost &h, const void *g, int d) {
+  return h.out_f32 ? static_cast<const float *>(g)[d]
+                   : __bfloat162float(static_cast<const __nv_bfloat16 *>(g)[d]);
+}
+__device__ __forceinline__ void qkv_chunk(const GemmArgs &p, int m_tile, int tok0,
+                                          const EpiPos &ps, const float (&v)[kCW], EpiSmem &es) {
+  const QkvPost &h = p.qkv;
+#pragma unroll
+  for (int jj = 0; jj < kCW; ++jj) es.xbuf[ps.r * kXStride + ps.c0 + jj] = v[jj];
+  named_bar(1, kEpiThreads);
+  const int c = ps.et >> 4, row0 = (ps.et & 15) * 8;
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = es.xbuf[(row0 + i) * kXStride + c];
+  named_bar(1, kEpiThreads);  // the exchange buffer is free for the next chunk
+  const int s = seg_of_tile(p, m_tile);  // 0: queries, 1: keys, 2: values
+  const int D = h.D, half = D / 2;
+  const int head = (m_tile - p.seg[s].tile_begin) * (kBM / D) + row0 / D;
+  const int d0 = row0 % D;
+  const int tok = tok0 + c;
+  const bool live = tok < p.n_tokens;
+  if (s != 2) {  // every lane takes part in the shuffles, live or not
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+    for (int o = 1; o < D / 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss / static_cast<float>(D) + h.eps);
+    const void *gn = s == 0 ? h.q_norm : h.k_norm;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] *= inv * qkv_gain(h, gn, d0 + i);
+    const float2 *cs = h.rope + static_cast<size_t>(live ? tok : 0) * half;
+    float pv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, x[i], D / 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d = d0 + i;
+      const float2 cr = cs[d % half];
+      x[i] = d < half ? x[i] * cr.x - pv[i] * cr.y : x[i] * cr.x + pv[i] * cr.y;
+    }
+  }
+  // a padding head of a partial last tile (D = 64 with an odd head count) is not stored
+  if (!live || head >= (s == 0 ? h.n_q_heads : h.n_kv_heads)) return;
+  size_t o, lo;
+  void *dst;
+  if (tok < h.T) {  // block row b * W + i
+    if (s == 0) {
+      o = static_cast<size_t>(tok) * h.n_q_heads * D + static_cast<size_t>(head) * D;
+      dst = h.q;
+      lo = h.q_lo;
+      if (h.q_scale != 0.f)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= h.q_scale;
+    } else {
+      const int b = tok / h.W, i = tok % h.W;
+      o = ((static_cast<size_t>(b) * h.n_kv_heads + head) * h.W + i) * D;
+      dst = s == 1 ? h.kblk : h.vblk;
+      lo = h.kv_lo;
+    }
+  } else {  // pending context row: its key and value to the ring, if its position is live
+    if (s == 0) return;
+    const int rr = tok - h.T;
+    const int req = h.row_req[rr];
+    const long long pos = h.row_pos[rr];
+    if (req < 0 || req >= h.n_req || pos < 0) {
+      atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      return;
+    }
+    const long long F = h.frontier[req];
+    if (h.min_back > 0 && (pos < F - h.min_back || pos >= F)) {
+      atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+      return;
+    }
+    if (pos < F - h.cap || pos >= F) return;  // outside the final live window
+    o = ((static_cast<size_t>(req) * h.n_kv_heads + head) * h.cap + pos % h.cap) * D;
+    dst = s == 1 ? h.kring : h.vring;
+    lo = 0;
+  }
+  o += d0;
+  if (h.out_f32) {
+    float4 *f = reinterpret_cast<float4 *>(static_cast<float *>(dst) + o);
+    f[0] = make_float4(x[0], x[1], x[2], x[3]);
+    f[1] = make_float4(x[4], x[5], x[6], x[7]);
+  } else {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      const float2 hf = __bfloat1622float2(hv);
+      const __nv_bfloat162 lv = __floats2bfloat162_rn(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+      hw[i] = *reinterpret_cast<const uint32_t *>(&hv);
+      lw[i] = *reinterpret_cast<const uint32_t *>(&lv);
+    }
+    __nv_bfloat16 *bd = static_cast<__nv_bfloat16 *>(dst) + o;
+    *reinterpret_cast<uint4 *>(bd) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    if (lo) *reinterpret_cast<uint4 *>(bd + lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
 // Writes the finished values v (tile row ps.r, token columns tok0+ps.c0 .. +kCW-1; j0 =
 // tok0 minus the tile's first token) of m_tile to the epilogue's destination.
 template <typename T, int EPI>
@@ -512,6 +616,9 @@ __device__ __forceinline__ void emit_chunk(const GemmMaps &maps, const GemmArgs 
                                            const float (&v)[kCW], EpiSmem &es) {
   if constexpr (EPI == EPI_ARGMAX) {
     argmax_chunk(p, m_tile, tok0, ps, v, es);
+    return;
+  } else if constexpr (EPI == EPI_QKV) {
+    qkv_chunk(p, m_tile, tok0, ps, v, es);
     return;
   } else if constexpr (EPI == EPI_TOPK) {
     topk_chunk(p, m_tile, tok0, ps, v, es);
@@ -831,7 +938,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < (p.pair_mode ? 2 : p.n_segs); ++s) tma_prefetch_desc(&maps.a[s]);
   }
   if (threadIdx.x == 64) {  // result maps, used by the epilogue's stores
-    const int n_out = EPI == EPI_STORE_F32 ? p.n_segs : (EPI == EPI_ARGMAX || EPI == EPI_TOPK ? 0 : 1);
+    const int n_out = EPI == EPI_STORE_F32 ? p.n_segs
+                      : (EPI == EPI_ARGMAX || EPI == EPI_TOPK || EPI == EPI_QKV ? 0 : 1);
     for (int s = 0; s < n_out; ++s) tma_prefetch_desc(&maps.out[s]);
   }
   if (warp == 1) {
@@ -1024,6 +1132,7 @@ static cudaError_t launch_typed(const GemmMaps &maps, const GemmArgs &a, cudaStr
     case EPI_SWIGLU: return launch_epi<T, EPI_SWIGLU>(maps, a, stream);
     case EPI_ARGMAX: return launch_epi<T, EPI_ARGMAX>(maps, a, stream);
     case EPI_TOPK: return launch_epi<T, EPI_TOPK>(maps, a, stream);
+    case EPI_QKV: return launch_epi<T, EPI_QKV>(maps, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

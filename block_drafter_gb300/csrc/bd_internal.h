@@ -36,7 +36,8 @@ enum EpiMode : int {
   EPI_INJECT = 2,     // x[tok*ld + row] += scale[tok] * acc for non-anchor rows
   EPI_SWIGLU = 3,     // pair tiles: out[tok*ld_act + f] = SiLU(gate_f) * up_f
   EPI_ARGMAX = 4,     // per-tile (max, lowest argmax) over 128 vocabulary rows
-  EPI_TOPK = 5        // per-tile 16 best (score, id) over 128 vocabulary rows
+  EPI_TOPK = 5,       // per-tile 16 best (score, id) over 128 vocabulary rows
+  EPI_QKV = 6         // Q/K/V product: head RMSNorm + RoPE, scattered to the attention inputs
 };
 constexpr int kTopK = 16;  // candidates per tile and per row of the top-k head
 
@@ -46,6 +47,26 @@ struct GemmSeg {
   int out_col;            // EPI_STORE_F32: column offset of this segment in the output row
   int n_kb_pack;          // packed: 128-byte K boxes per 128-row tile
   const uint8_t *packed;  // packed image of this matrix (see PackedLayout), or null
+};
+
+// EPI_QKV: the Q/K/V product's epilogue post-processes the heads (plain head RMSNorm and
+// split-half RoPE of query and key heads, a copy of value heads; results in the config
+// dtype) and scatters them to the attention's inputs.  Token columns < T are block rows:
+// queries token-major [T][Hq*D] (times q_scale unless 0), keys and values [B][Hkv][W][D]
+// (each with a bf16 lo plane when the offset is set).  Columns T .. T+n_pend-1 are pending
+// context rows (request, position per row) whose keys and values go to the rings when the
+// position is live.  Tiles of 128 rows hold 128 / D heads (D = 64 or 128).
+struct QkvPost {
+  int D, W, n_q_heads, n_kv_heads, T, n_pend, out_f32;
+  int n_req, min_back, cap;
+  float eps, q_scale;
+  const float2 *rope;           // [token][D/2] (cos, sin) by token column
+  const void *q_norm, *k_norm;  // [D] head-norm gains
+  void *q, *kblk, *vblk;
+  size_t q_lo, kv_lo;           // element offsets of the lo planes (0: none)
+  void *kring, *vring;          // [B][Hkv][cap][D]
+  const int32_t *row_req;       // [n_pend]
+  const int64_t *row_pos, *frontier;
 };
 
 struct __align__(16) GemmArgs {
@@ -74,6 +95,7 @@ struct __align__(16) GemmArgs {
   float *partials;                // [n_ctas][2][block_n * 128] fp32 stream-K partial tiles
   unsigned *counters;             // [2][n_counter_tiles] arrival / done counters (start at 0)
   int n_counter_tiles;
+  QkvPost qkv;                    // EPI_QKV
   GemmSeg seg[kMaxSegs];
 };
 

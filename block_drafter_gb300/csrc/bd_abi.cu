@@ -229,7 +229,7 @@ size_t tiles_of(int rows, int tile_rows) { return static_cast<size_t>((rows + ti
 
 struct RoundWs {
   GemmWs g;
-  float *x, *z, *pre, *r, *qkv_raw, *feat, *kv_raw;
+  float *x, *z, *pre, *r, *feat, *kv_raw;
   float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
   unsigned *br_bar;    // [L][5] fused-bridge barrier counters (4 used), right after g.counters
   float *zpart, *sspart, *zsq;  // fused-bridge partial sums
@@ -285,7 +285,6 @@ void carve_round(Carve &cv, RoundWs &w, const bd_config *c, int B, int W, int n_
     w.zpart = w.sspart = w.zsq = nullptr;
   }
   w.x = cv.take<float>(static_cast<size_t>(T) * H);
-  w.qkv_raw = cv.take<float>(static_cast<size_t>(Tq) * (QD + 2 * KD));
   w.feat = n_pend > 0 ? cv.take<float>(static_cast<size_t>(n_pend) * H) : nullptr;
   w.cmat = n_pend > 0 && !fuse ? cv.take<char>(static_cast<size_t>(n_pend) * H * e) : nullptr;
   w.kv_raw = n_pend > 0 && !fuse
@@ -735,78 +734,40 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       add_w(p, L.wq, QD, pk, PL.wq[l]);
       add_w(p, L.wk, KD, pk, PL.wk[l]);
       add_w(p, L.wv, KD, pk, PL.wv[l]);
-      p.args.epi = EPI_STORE_F32;
-      p.args.out_f32 = rw.qkv_raw;
-      p.args.ld_out = QD + 2 * KD;
-      p.args.seg[0].out_col = 0;
-      p.args.seg[1].out_col = QD;
-      p.args.seg[2].out_col = QD + KD;
-      HeadPostArgs h;
-      memset(&h, 0, sizeof h);
-      h.raw = rw.qkv_raw;
-      h.ld_raw = QD + 2 * KD;
-      h.D = D;
-      h.n_kv_heads = cfg->n_kv_heads;
-      h.W = W;
-      h.eps = cfg->eps;
-      h.rope = rw.rope;
+      // S4's head post-processing (head RMSNorm + RoPE, queries scaled by log2(e)/sqrt(D)
+      // so that the attention's scores come out in log2 units) in the product's epilogue:
       // the attention takes the queries and the block's keys/values as bf16 hi+lo planes,
-      // the queries scaled by log2(e)/sqrt(D) (its scores come out in log2 units)
-      const size_t qlo = split ? static_cast<size_t>(T) * QD : 0;
-      const size_t klo = split ? static_cast<size_t>(T) * KD : 0;
-      const float qs = split ? static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D))) : 0.f;
-      h.seg[0] = HeadSeg{HK_Q, HD_TOKEN_MAJOR, 0, cfg->n_q_heads, QD, 0, L.q_norm, rw.q, qlo, qs};
-      h.seg[1] = HeadSeg{HK_K, HD_BLOCK, QD, cfg->n_kv_heads, 0, 0, L.k_norm, rw.kblk, klo, 0.f};
-      h.seg[2] = HeadSeg{HK_V, HD_BLOCK, QD + KD, cfg->n_kv_heads, 0, 0, nullptr, rw.vblk, klo, 0.f};
-      h.n_groups = 1;
-      h.grp[0] = HeadGroup{0, T, 0, 3, cfg->n_q_heads + 2 * cfg->n_kv_heads};
-      if (fuse) {  // the pending rows' context K/V go to the rings (before attention)
-        const int cap = cfg->ring_capacity[l];
-        h.seg[3] = HeadSeg{HK_K, HD_RING, QD, cfg->n_kv_heads, 0, cap, L.k_norm, kv->k[l], 0, 0.f};
-        h.seg[4] = HeadSeg{HK_V, HD_RING, QD + KD, cfg->n_kv_heads, 0, cap, nullptr, kv->v[l], 0, 0.f};
-        h.n_groups = 2;
-        h.grp[1] = HeadGroup{T, n_pend, 3, 2, 2 * cfg->n_kv_heads};
-        h.n_req = B;
-        h.row_req = pending->request;
-        h.row_pos = pending->pos;
-        h.frontier = frontier;
-        h.min_back = kMaxPendPerReq;
+      // and the pending rows' keys/values go to the rings before the attention reads them
+      QkvPost &e = p.args.qkv;
+      e.D = D;
+      e.W = W;
+      e.n_q_heads = cfg->n_q_heads;
+      e.n_kv_heads = cfg->n_kv_heads;
+      e.T = T;
+      e.n_pend = fuse ? n_pend : 0;
+      e.out_f32 = dt == BD_BF16 ? 0 : 1;
+      e.eps = cfg->eps;
+      e.q_scale = split ? static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D))) : 0.f;
+      e.rope = rw.rope;
+      e.q_norm = L.q_norm;
+      e.k_norm = L.k_norm;
+      e.q = rw.q;
+      e.kblk = rw.kblk;
+      e.vblk = rw.vblk;
+      e.q_lo = split ? static_cast<size_t>(T) * QD : 0;
+      e.kv_lo = split ? static_cast<size_t>(T) * KD : 0;
+      if (fuse) {
+        e.n_req = B;
+        e.min_back = kMaxPendPerReq;
+        e.cap = cfg->ring_capacity[l];
+        e.kring = kv->k[l];
+        e.vring = kv->v[l];
+        e.row_req = pending->request;
+        e.row_pos = pending->pos;
+        e.frontier = frontier;
       }
-      if (D == 64 || D == 128) {  // the head post-processing in the product's epilogue
-        QkvPost &e = p.args.qkv;
-        e.D = D;
-        e.W = W;
-        e.n_q_heads = cfg->n_q_heads;
-        e.n_kv_heads = cfg->n_kv_heads;
-        e.T = T;
-        e.n_pend = fuse ? n_pend : 0;
-        e.out_f32 = dt == BD_BF16 ? 0 : 1;
-        e.eps = cfg->eps;
-        e.q_scale = qs;
-        e.rope = rw.rope;
-        e.q_norm = L.q_norm;
-        e.k_norm = L.k_norm;
-        e.q = rw.q;
-        e.kblk = rw.kblk;
-        e.vblk = rw.vblk;
-        e.q_lo = qlo;
-        e.kv_lo = klo;
-        if (fuse) {
-          e.n_req = B;
-          e.min_back = kMaxPendPerReq;
-          e.cap = cfg->ring_capacity[l];
-          e.kring = kv->k[l];
-          e.vring = kv->v[l];
-          e.row_req = pending->request;
-          e.row_pos = pending->pos;
-          e.frontier = frontier;
-        }
-        p.args.epi = EPI_QKV;
-        BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
-      } else {
-        BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
-        BD_TRY(launch_head_post(dt, h, s));
-      }
+      p.args.epi = EPI_QKV;
+      BD_TIMED(BD_TIME_QKV, launch_gemm(p, sc, s));
     }
     // S5: block attention over the ring context and the block
     {

@@ -231,7 +231,7 @@ struct RoundWs {
   GemmWs g;
   float *x, *z, *pre, *r, *feat, *kv_raw;
   float *cdelta_a, *cdelta_m, *cz, *cn;  // DFlash2 convolution: deltas, branch output, fp32 X
-  unsigned *br_bar;    // [L][5] fused-bridge barrier counters (4 used), right after g.counters
+  unsigned *br_bar;    // [L][5] fused-bridge barrier counters (3 used), right after g.counters
   float *zpart, *sspart, *zsq;  // fused-bridge partial sums
   float2 *rope;
   void *xn, *xq, *cmat, *q, *kblk, *vblk, *att, *hmid, *c, *m;
@@ -709,15 +709,12 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
     return launch_copy_f32(rw.x, layers_out + static_cast<size_t>(l) * T * H,
                            static_cast<size_t>(T) * H, s);
   };
-  bool xq_ready = false;  // the previous layer's one-launch bridge wrote this layer's norm
   for (int l = 0; l < cfg->n_layers; ++l) {
     const bd_layer_weights &L = w->layer[l];
     // S4: n = rmsnorm(x); q, k, v with head norm + RoPE.  The pending context rows ride
     // along in the same product: their K/V (S2) use the same W_k, W_v tiles.
-    if (!xq_ready)
-      BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xq, nullptr,
-                            conv ? rw.cn : nullptr, nullptr, W, lo_q, s, fin, f16));
-    xq_ready = false;
+    BD_TRY(launch_rownorm(dt, rw.x, T, H, L.in_norm, cfg->eps, NORM_PLAIN, rw.xq, nullptr,
+                          conv ? rw.cn : nullptr, nullptr, W, lo_q, s, fin, f16));
     fin = no_fin;
     if (copy_layer >= 0) {
       BD_TRY(copy_layer_out(copy_layer));
@@ -873,13 +870,6 @@ bd_status bd_draft_round(const bd_config *cfg, const bd_weights *w, const bd_kv_
       ba.zsq = rw.zsq;
       ba.m = static_cast<__half *>(rw.m);
       ba.tail = tail_state && l == cfg->n_layers - 1 ? tail_state : nullptr;
-      // the next layer's input norm in the same launch (the one-launch bridge runs without
-      // the convolution, so there is no branch finish to add to x first)
-      if (l + 1 < cfg->n_layers) {
-        ba.next_norm = static_cast<const __nv_bfloat16 *>(w->layer[l + 1].in_norm);
-        ba.xq = static_cast<__half *>(rw.xq);
-        xq_ready = true;
-      }
       ba.bar = rw.br_bar + 5 * l;
       ba.T = T;
       ba.W = W;

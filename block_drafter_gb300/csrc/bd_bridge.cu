@@ -4,7 +4,7 @@
 // bridge's three products stream only 19 MB of weights at the 27B size, and as five
 // separate launches (row norm, code read, code, gate maps + message, write) its time was
 // dominated by launch boundaries, dependency waits and split-tile reductions.  Here one
-// launch of one CTA per SM runs it in four (five) phases separated by grid-wide barriers:
+// launch of one CTA per SM runs it in four phases separated by grid-wide barriers:
 //   P1  z'_q = R_l[:, K_q] x[:, K_q] per K chunk q, and the chunk's sums of squares of x
 //   P2  z' = sum_q z'_q (fixed order), r_t = RMS(x_t), |z'|^2 partial sums per row group
 //   P3  [G; G_p; A] z', scaled per token into the products of the codes
@@ -12,8 +12,6 @@
 //       anchors sqrt(Rc) C[a]); g = sigmoid(G c_t + G_p c_{t-1} + b), m_t = g * (A c_{t-1}),
 //       m_0 = 0; the tail export of the last layer
 //   P4  x_t += r_t W_l m_t for every row but the anchor
-//   P5  (all layers but the last) the next layer's input RMSNorm of the updated rows, as
-//       the fp16 operand of its Q/K/V product: the residual write and the next norm fused
 // The products run on mma.sync across the CTA's 8 warps with the packed image's fp16
 // weights and fp16 activations (the row chunks, codes and messages): at these shapes
 // (N <= 32 token columns, short K per CTA) the warps' tensor instructions finish each
@@ -499,40 +497,6 @@ __global__ void __launch_bounds__(kBrThreads, 1) bridge_kernel(const __grid_cons
         for (int q = 0; q < NKS4; ++q) v += sred[((it * NKS4 + q) * kW4Rows + row) * NTOK + t];
         a.x[static_cast<size_t>(t) * H + (cta + it * static_cast<int>(gridDim.x)) * kW4Rows + row] =
             xv[u] + s_scale[t] * v;
-      }
-    }
-
-    // ---- P5 (next_norm set): the next layer's input RMSNorm of the updated rows, stored as
-    // the fp16 operand of its Q/K/V product (the residual write and the next norm in one
-    // launch), with the row-norm kernel's arithmetic and summation order.  CTAs 0..T-1 take
-    // one row each; the others leave after the barrier, so the next product's CTAs can start
-    // on their SMs and stream weights meanwhile (holding every SM to spread the norm over
-    // all CTAs measured slower).
-    if (a.next_norm != nullptr) {
-      if (!grid_sync(a.bar + 3, &s_ok)) return;
-      const int H4 = H / 4;
-      for (int t = cta; t < T; t += static_cast<int>(gridDim.x)) {
-        const float4 *xr = reinterpret_cast<const float4 *>(a.x + static_cast<size_t>(t) * H);
-        float ss = 0.f;
-        for (int i4 = threadIdx.x; i4 < H4; i4 += kBrThreads) {
-          const float4 v = __ldcg(xr + i4);
-          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-        ss = block_sum(ss, red);
-        const float scale = rsqrtf(ss / H + a.eps);
-        __half *o = a.xq + static_cast<size_t>(t) * H;
-        for (int i4 = threadIdx.x; i4 < H4; i4 += kBrThreads) {
-          const float4 v = __ldcg(xr + i4);
-          const uint2 gu = reinterpret_cast<const uint2 *>(a.next_norm)[i4];
-          const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
-          const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
-          float4 y = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
-          y.x *= g01.x;
-          y.y *= g01.y;
-          y.z *= g23.x;
-          y.w *= g23.y;
-          put4(o + 4 * i4, y);
-        }
       }
     }
   };

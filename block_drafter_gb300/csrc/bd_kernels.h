@@ -143,7 +143,7 @@ struct HeadPostArgs {
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);
 
 // Fused DSpine bridge for blocks of T <= 32 rows (bf16 config, packed weight image): one
-// launch, one CTA per SM, phases separated by grid barriers (bar: 4 counters, zero on
+// launch, one CTA per SM, phases separated by grid barriers (bar: 3 counters, zero on
 // entry).  See bd_bridge.cu.
 struct BridgeArgs {
   float *x;                                       // [T][H] residual, updated in place
@@ -158,9 +158,7 @@ struct BridgeArgs {
   float *zsq;                                     // [T][ceil(Rc / 128)]
   __half *m;                                      // message fp16 boxes (16 or 32 rows x Mc)
   float *tail;                                    // tail state export, or null
-  const __nv_bfloat16 *next_norm;                 // [H] next layer's input-norm gain, or null
-  __half *xq;                                     // [T][H] OUT its fp16 normalised rows (next_norm)
-  unsigned *bar;                                  // [4] grid-barrier counters
+  unsigned *bar;                                  // [3] grid-barrier counters
   int T, W, H, Rc, Mc, V;
   int n_kz, kz, n1, n3, p3_boxes;                 // from the plan
   size_t off_x, off_c, off_w4, off_red;           // shared-memory areas (from the plan)

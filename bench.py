@@ -489,7 +489,7 @@ def roofline_entry(kind: str, kt: dict, hbm: float, peak_kind: str, what: str) -
             "peak_kind": peak_kind}
 
 
-KIND_NAMES = {"qkv": "Q/K/V product (tcgen05 GEMM)", "attention": "block attention",
+KIND_NAMES = {"qkv": "Q/K/V product (tcgen05 GEMM, head RMSNorm + RoPE epilogue)", "attention": "block attention",
               "wo": "output projection (tcgen05 GEMM, residual epilogue)",
               "gate_up": "SwiGLU gate/up product (tcgen05 GEMM, SwiGLU epilogue)",
               "down": "down projection (tcgen05 GEMM, residual epilogue)",

@@ -619,15 +619,12 @@ def cpu_threads():
 
 
 # ----------------------------------------------------------------------------- main
-def run_reference(args, rank, world):
-    """The reference arm: the fp64 CPU oracle as it stands, on the host cores.  Each step
-    is one full oracle step of request 0 of the B=1 workload (catch-up materialisation of
-    its 16 pending rows, the 5-layer round over the 2047-position window, the LM head),
+def reference_line(geo, args) -> dict:
+    """The reference arm's JSON line for workload ``geo``: the fp64 CPU oracle as it stands,
+    on the host cores.  Each step is one full oracle step of request 0 (catch-up
+    materialisation of its W pending rows, the round over its context window, the LM head),
     i.e. exactly the per-request work of one GPU step at B=1."""
-    if rank != 0:
-        return
     import numpy as np
-    geo = bdsynth.DSPINE27B_B1
     w = bdsynth.make_weights(geo, args.seed, device="cpu")
     wh = {k: (None if v is None else v.float().numpy()) for k, v in w.items() if k != "layers"}
     wh["layers"] = [{kk: vv.float().numpy() for kk, vv in lw.items()} for lw in w["layers"]]
@@ -644,17 +641,23 @@ def run_reference(args, rank, world):
             ts.append(t)
     t_step = statistics.mean(ts)
     val = 1.0 / t_step
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * t_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": geo.name, "B": 1, "W": geo.W, "context": F[0],
+            "config": {"workload": geo.name, "B": 1, "W": geo.W, "context": int(F[0]),
                        "window": geo.windows[0]},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                             "sample": "one full oracle step of request 0 per step: catch-up of "
-                                       "16 rows, 5-layer round, full LM head"},
+                             "sample": f"one full oracle step of request 0 per step: catch-up of "
+                                       f"{geo.W} rows, {geo.n_layers}-layer round, full LM head"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The reference arm on the metric's workload (the 27B B=1 round); rank 0 only."""
+    if rank != 0:
+        return
+    print(json.dumps(reference_line(bdsynth.DSPINE27B_B1, args)), flush=True)
 
 
 def main():

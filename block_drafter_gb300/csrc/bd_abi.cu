@@ -469,7 +469,6 @@ static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const
   h.ld_raw = ldkv;
   h.D = D;
   h.n_kv_heads = cfg->n_kv_heads;
-  h.W = 1;
   h.n_req = n_req;
   h.eps = cfg->eps;
   h.rope = rope;
@@ -481,7 +480,6 @@ static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const
   for (int l = 0; l < cfg->n_layers; ++l) {
     HeadSeg &k = h.seg[n_segs++];
     k.kind = HK_K;
-    k.dst_mode = HD_RING;
     k.col0 = l * 2 * KD;
     k.n_heads = cfg->n_kv_heads;
     k.cap = cfg->ring_capacity[l];
@@ -494,8 +492,9 @@ static bd_status enqueue_ctx_kv(const bd_config *cfg, const bd_weights *w, const
     v.norm = nullptr;
     v.dst = kv->v[l];
   }
-  h.n_groups = 1;
-  h.grp[0] = HeadGroup{0, n_rows, 0, n_segs, 2 * cfg->n_layers * cfg->n_kv_heads};
+  h.rows = n_rows;
+  h.n_segs = n_segs;
+  h.total_heads = 2 * cfg->n_layers * cfg->n_kv_heads;
   BD_TRY(launch_head_post(cfg->dtype, h, s));
   return BD_OK;
 }

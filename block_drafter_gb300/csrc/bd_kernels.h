@@ -107,37 +107,28 @@ std::string launch_code(int dtype, const float *z, int rows, int Rc, const void 
 // m_i = sigmoid(G c_i + G_p c_{i-1} + b) * (A c_{i-1}) for i >= 1, m_0 = 0.
 std::string launch_message(int dtype, const float *pre, int rows, int Mc, const void *bias,
                            int W, void *m_out, size_t lo_off, cudaStream_t s, bool out_f16 = false);
-// Head post-processing of raw fp32 projections [rows, ld_raw]: for each head of each
-// segment, plain_head_rmsnorm + split-half RoPE (query/key segments) or a copy (value
-// segments), rounded to the config dtype and scattered to its destination.
-enum HeadKind : int { HK_Q = 0, HK_K = 1, HK_V = 2 };
-enum HeadDst : int {
-  HD_TOKEN_MAJOR = 0,  // dst[row * ld + head * D + d]
-  HD_BLOCK = 1,        // dst[((b * Hkv + head) * W + i) * D + d], row = b * W + i
-  HD_RING = 2          // dst[((req * Hkv + head) * cap + pos % cap) * D + d] if pos is live
-};
+// Head post-processing of the context rows' raw fp32 key/value projections [rows, ld_raw]
+// (every layer's keys and values in one row): plain_head_rmsnorm + split-half RoPE of key
+// heads, a copy of value heads, rounded to the config dtype and stored in the ring slot of
+// the row's position (request row_req[r], position row_pos[r]) when it lies in the final
+// live window [F - cap, F).  A row whose request or position is invalid sets the
+// bad-index error.
+enum HeadKind : int { HK_K = 1, HK_V = 2 };
 constexpr int kMaxHeadSegs = 32;
 struct HeadSeg {
-  int kind, dst_mode, col0, n_heads, ld, cap;
-  const void *norm;  // [D] gain (query/key segments)
-  void *dst;
-  size_t lo_off;     // != 0: also store the rounding residual at dst + lo_off
-  float scale;       // multiplies the stored values (0 stands for 1)
-};
-// Rows row0 .. row0+rows-1 take segments seg0 .. seg0+n_segs-1 (total_heads heads in all).
-struct HeadGroup {
-  int row0, rows, seg0, n_segs, total_heads;
+  int kind, col0, n_heads, cap;  // column of the segment's first head in a raw row; ring size
+  const void *norm;              // [D] key-norm gain (key segments)
+  void *dst;                     // ring [B][Hkv][cap][D]
 };
 struct HeadPostArgs {
   const float *raw;
-  int ld_raw, D, n_kv_heads, W, n_req, n_groups;
+  int ld_raw, D, n_kv_heads, n_req, rows, n_segs, total_heads;
   float eps;
-  const float2 *rope;        // [rows][D/2], by absolute row
-  const int32_t *row_req;    // ring mode, by row - row0 of the group
+  const float2 *rope;        // [rows][D/2]
+  const int32_t *row_req;    // [rows]
   const int64_t *row_pos;
   const int64_t *frontier;
-  int min_back;              // > 0: ring rows must lie in [F - min_back, F) (else an error)
-  HeadGroup grp[2];
+  int min_back;              // > 0: rows must lie in [F - min_back, F) (else an error)
   HeadSeg seg[kMaxHeadSegs];
 };
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s);

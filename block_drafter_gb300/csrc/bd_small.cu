@@ -280,17 +280,11 @@ template <typename T, int E>
 __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ HeadPostArgs a) {
   const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  int wg = warp, g = 0;
-  if (a.n_groups > 1 && wg >= a.grp[0].rows * a.grp[0].total_heads) {
-    wg -= a.grp[0].rows * a.grp[0].total_heads;
-    g = 1;
-  }
-  const HeadGroup gr = a.grp[g];
-  const int rr = wg / gr.total_heads;  // row within the group
-  int hg = wg % gr.total_heads;
-  const bool live = rr < gr.rows;
-  int si = gr.seg0;
-  while (si + 1 < gr.seg0 + gr.n_segs && hg >= a.seg[si].n_heads) {
+  const int rr = warp / a.total_heads;  // context row
+  int hg = warp % a.total_heads;
+  const bool live = rr < a.rows;
+  int si = 0;
+  while (si + 1 < a.n_segs && hg >= a.seg[si].n_heads) {
     hg -= a.seg[si].n_heads;
     ++si;
   }
@@ -301,16 +295,15 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
   float gn[E];
 #pragma unroll
   for (int e = 0; e < E; ++e)
-    gn[e] = live && sg.kind != HK_V ? to_f<T>(static_cast<const T *>(sg.norm)[d0 + e]) : 1.f;
+    gn[e] = live && sg.kind == HK_K ? to_f<T>(static_cast<const T *>(sg.norm)[d0 + e]) : 1.f;
   pdl_wait();
   pdl_trigger();
   if (!live) return;
-  const int row = gr.row0 + rr;
-  const float *src = a.raw + static_cast<size_t>(row) * a.ld_raw + sg.col0 + hg * D + d0;
+  const float *src = a.raw + static_cast<size_t>(rr) * a.ld_raw + sg.col0 + hg * D + d0;
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) v[e] = src[e];
-  if (sg.kind != HK_V) {
+  if (sg.kind == HK_K) {
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) ss += v[e] * v[e];
@@ -318,7 +311,7 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
     const float inv = rsqrtf(ss / static_cast<float>(D) + a.eps);
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] *= inv * gn[e];
-    const float2 *cs = a.rope + static_cast<size_t>(row) * half;
+    const float2 *cs = a.rope + static_cast<size_t>(rr) * half;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float pv = __shfl_xor_sync(0xffffffffu, v[e], 16);
@@ -327,34 +320,22 @@ __global__ void __launch_bounds__(256) head_post_kernel(const __grid_constant__ 
       v[e] = d < half ? v[e] * c.x - pv * c.y : v[e] * c.x + pv * c.y;
     }
   }
-  size_t o;
-  if (sg.dst_mode == HD_TOKEN_MAJOR) {
-    o = static_cast<size_t>(row) * sg.ld + hg * D;
-  } else if (sg.dst_mode == HD_BLOCK) {
-    const int b = row / a.W, i = row % a.W;
-    o = ((static_cast<size_t>(b) * a.n_kv_heads + hg) * a.W + i) * D;
-  } else {
-    const int req = a.row_req[rr];
-    const long long pos = a.row_pos[rr];
-    if (req < 0 || req >= a.n_req || pos < 0) {
-      if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
-      return;
-    }
-    const long long F = a.frontier[req];
-    if (a.min_back > 0 && (pos < F - a.min_back || pos >= F)) {
-      if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
-      return;
-    }
-    if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
-    o = ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D;
+  const int req = a.row_req[rr];
+  const long long pos = a.row_pos[rr];
+  if (req < 0 || req >= a.n_req || pos < 0) {
+    if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+    return;
   }
-  if (sg.scale != 0.f) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] *= sg.scale;
+  const long long F = a.frontier[req];
+  if (a.min_back > 0 && (pos < F - a.min_back || pos >= F)) {
+    if (lane == 0) atomicOr(&g_error_word, DEVERR_BAD_INDEX);
+    return;
   }
-  T *dst = static_cast<T *>(sg.dst) + o + d0;
+  if (pos < F - sg.cap || pos >= F) return;  // outside the final live window
+  T *dst = static_cast<T *>(sg.dst) +
+           ((static_cast<size_t>(req) * a.n_kv_heads + hg) * sg.cap + pos % sg.cap) * D + d0;
 #pragma unroll
-  for (int e = 0; e < E; ++e) store_split(dst, e, sg.lo_off, v[e]);
+  for (int e = 0; e < E; ++e) store_split(dst, e, 0, v[e]);
 }
 
 template <typename T, typename O>
@@ -940,8 +921,7 @@ std::string launch_split_rows(const float *src, size_t n, void *dst, size_t lo_o
 }
 
 std::string launch_head_post(int dtype, const HeadPostArgs &a, cudaStream_t s) {
-  long long warps = 0;
-  for (int g = 0; g < a.n_groups; ++g) warps += static_cast<long long>(a.grp[g].rows) * a.grp[g].total_heads;
+  const long long warps = static_cast<long long>(a.rows) * a.total_heads;
   const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
   cudaError_t e;
   if (a.D == 128)
